@@ -1,0 +1,172 @@
+"""Reference tile orders of the distributed swizzle, written from their definitions.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Sources:
+* DITRON page, section 3.2 (论文 §3.2, Fig. 3): a stateless ``swizzle_func`` maps
+  the original tile id to a new one with a rank-aware offset; rank r starts at
+  ``r mod world_size``.  Gather mode (AllGather-GEMM): local HBM acts as a cache
+  of remote memory, own data first while remote chunks are fetched.  Scatter
+  mode (GEMM-ReduceScatter): first compute the tiles whose results go to the
+  farthest rank.
+* Triton-distributed talk, "不完全なブロックスケジューリング": with non-perfect
+  tiling an AllGather tile that straddles ranks waits for the latest data it
+  needs and runs last; in ReduceScatter the tiles that remote ranks depend on
+  run first.
+* AutoOverlap page, section 5.4 / Fig. 6: the tile scheduler follows chunk
+  arrival order across chunks and keeps a locality-preserving traversal
+  inside a chunk; chunks stay where they are.
+
+The appendix that gives DITRON's exact transform is not available, so these
+readings are fixed here (and implemented independently by the CUDA side):
+
+Notation: W ranks, own rank r, M rows in total, Ms = M/W rows per rank, chunk
+rows Cr, nC = ceil(Ms/Cr) chunks per rank, tiles BM x BN, Tm = ceil(M/BM),
+Tn = ceil(N/BN); group width G (default 8).
+
+* chunk (s, j) covers global rows [s*Ms + j*Cr, s*Ms + min((j+1)*Cr, Ms)).
+* AllGather, swizzle on: pos(s, j) = ((s - r) mod W) * nC + j.  key(i) = max pos
+  over the chunks that m-tile i reads.  Tiles (i, n) are sorted by
+  (key(i), band(i), n, i), band(i) = (rank of i among the m-tiles that share its
+  key, in ascending i) // G.  Chunks are transferred in ascending pos.
+* AllGather, swizzle off: tile order i-major (i * Tn + n); transfer order
+  ascending (s, j); pos(s, j) = s * nC + j.
+* ReduceScatter, swizzle on: source rank q sends to s in the order
+  dpos_q(s) = (s - q - 1) mod W (next rank first, its own block last).
+  key(q, i) = min over the chunks (s, j) that m-tile i writes of
+  dpos_q(s) * nC + j.  Tiles (q, i, n) sorted by (key, q, band, n, i), band taken
+  among the m-tiles of the same (q, key).
+* ReduceScatter, swizzle off: lexicographic (q, i, n).
+* ReduceScatter arrivals: unit (s, j, n) = rows of chunk (s, j) x column tile n.
+  It is complete after W * (number of m-tiles that overlap chunk (s, j))
+  partial tiles have arrived.
+"""
+from __future__ import annotations
+
+from collections import defaultdict
+
+
+def cdiv(a, b):
+    return -(-a // b)
+
+
+def geometry(world_size, m, n, chunk_rows, bm, bn):
+    """Return (Ms, nC, Tm, Tn) for the given problem and tiling."""
+    if world_size < 1 or m % world_size:
+        raise ValueError("M must be a positive multiple of W")
+    ms = m // world_size
+    nc = cdiv(ms, chunk_rows) if ms > 0 else 0
+    return ms, nc, cdiv(m, bm), cdiv(n, bn)
+
+
+def chunk_of_row(g, ms, chunk_rows):
+    """(rank, chunk) that holds global row g."""
+    s = g // ms
+    return s, (g - s * ms) // chunk_rows
+
+
+def chunk_rows_range(s, j, ms, chunk_rows):
+    """Global row range [lo, hi) of chunk (s, j)."""
+    lo = s * ms + j * chunk_rows
+    return lo, s * ms + min((j + 1) * chunk_rows, ms)
+
+
+def tile_chunks(i, m, ms, chunk_rows, bm):
+    """Set of chunks that m-tile i touches, by visiting every one of its rows."""
+    return {chunk_of_row(g, ms, chunk_rows) for g in range(i * bm, min((i + 1) * bm, m))}
+
+
+def ag_pos(s, j, world_size, rank, nc, swizzle=True):
+    """Position of chunk (s, j) in rank `rank`'s gather (transfer and key) order."""
+    if swizzle:
+        return ((s - rank) % world_size) * nc + j
+    return s * nc + j
+
+
+def ag_transfer_order(world_size, rank, m, chunk_rows, swizzle=True):
+    """Chunks (s, j) in the order the gather moves them."""
+    ms = m // world_size
+    nc = cdiv(ms, chunk_rows) if ms else 0
+    chunks = [(s, j) for s in range(world_size) for j in range(nc)]
+    return sorted(chunks, key=lambda c: ag_pos(c[0], c[1], world_size, rank, nc, swizzle))
+
+
+def _bands(keys_by_tile, group):
+    """band index of every m-tile: rank among same-key m-tiles (ascending i) // G."""
+    members = defaultdict(list)
+    for i in sorted(keys_by_tile):
+        members[keys_by_tile[i]].append(i)
+    band = {}
+    for lst in members.values():
+        for idx, i in enumerate(lst):
+            band[i] = idx // group
+    return band
+
+
+def ag_keys(world_size, rank, m, chunk_rows, bm, swizzle=True):
+    """key(i) = latest gather position among the chunks m-tile i reads."""
+    ms = m // world_size
+    nc = cdiv(ms, chunk_rows) if ms else 0
+    tm = cdiv(m, bm)
+    return {i: max(ag_pos(s, j, world_size, rank, nc, swizzle)
+                   for (s, j) in tile_chunks(i, m, ms, chunk_rows, bm))
+            for i in range(tm)}
+
+
+def ag_order(world_size, rank, m, n, chunk_rows, bm, bn, swizzle=True, group=8):
+    """Tile ids (i * Tn + n) of the AllGather-GEMM in execution order."""
+    _, _, tm, tn = geometry(world_size, m, n, chunk_rows, bm, bn)
+    if tm == 0 or tn == 0:
+        return []
+    if not swizzle:
+        return [i * tn + c for i in range(tm) for c in range(tn)]
+    keys = ag_keys(world_size, rank, m, chunk_rows, bm, True)
+    band = _bands(keys, group)
+    entries = sorted((keys[i], band[i], c, i) for i in range(tm) for c in range(tn))
+    return [i * tn + c for (_, _, c, i) in entries]
+
+
+def rs_dpos(q, s, world_size):
+    """Send order of destination s for source rank q: q+1 first, q itself last."""
+    return (s - q - 1) % world_size
+
+
+def rs_keys(world_size, q, m, chunk_rows, bm):
+    """key(q, i) = most urgent (smallest) send position among the chunks m-tile i writes."""
+    ms = m // world_size
+    nc = cdiv(ms, chunk_rows) if ms else 0
+    tm = cdiv(m, bm)
+    return {i: min(rs_dpos(q, s, world_size) * nc + j
+                   for (s, j) in tile_chunks(i, m, ms, chunk_rows, bm))
+            for i in range(tm)}
+
+
+def rs_order(world_size, m, n, chunk_rows, bm, bn, swizzle=True, group=8):
+    """Tile ids ((q * Tm + i) * Tn + n) of the GEMM-ReduceScatter in execution order."""
+    _, _, tm, tn = geometry(world_size, m, n, chunk_rows, bm, bn)
+    if tm == 0 or tn == 0:
+        return []
+    if not swizzle:
+        return list(range(world_size * tm * tn))
+    entries = []
+    for q in range(world_size):
+        keys = rs_keys(world_size, q, m, chunk_rows, bm)
+        band = _bands(keys, group)
+        for i in range(tm):
+            for c in range(tn):
+                entries.append((keys[i], q, band[i], c, i))
+    entries.sort()
+    return [(q * tm + i) * tn + c for (_, q, _, c, i) in entries]
+
+
+def rs_expected_arrivals(world_size, m, n, chunk_rows, bm, bn):
+    """{(s, j, n): partial tiles that must arrive before unit (s, j, n) is reduced}."""
+    ms, nc, tm, tn = geometry(world_size, m, n, chunk_rows, bm, bn)
+    out = {}
+    for s in range(world_size):
+        for j in range(nc):
+            lo, hi = chunk_rows_range(s, j, ms, chunk_rows)
+            mtiles = {g // bm for g in range(lo, hi)}
+            for c in range(tn):
+                out[(s, j, c)] = world_size * len(mtiles)
+    return out

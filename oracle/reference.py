@@ -1,0 +1,79 @@
+"""Float64 reference results of the fused AllGather-GEMM and GEMM-ReduceScatter.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Definitions followed (DITRON page, sections "4. 支持的并行策略" and "3.2 中端":
+tensor parallelism uses AllGather+GEMM and GEMM+ReduceScatter; Triton-distributed
+talk, "GEMM ReduceScatter" paragraph: every rank computes a partial product and
+the reduced rows are scattered to their owner ranks):
+
+* AllGather-GEMM over W ranks: A = concat_rows(A_0, ..., A_{W-1}); C = A @ B.
+* GEMM-ReduceScatter over W ranks: P_q = A_q @ B_q (rank q holds a K slice);
+  S = sum_q P_q; rank s receives rows s*M/W .. (s+1)*M/W - 1 of S.
+
+Inputs are float64 arrays holding exact bf16 values; outputs are float64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def ag_gemm(shards, b):
+    """C = concat_rows(shards) @ b, in float64 (one library matmul)."""
+    a = np.concatenate([np.asarray(x, dtype=np.float64) for x in shards], axis=0)
+    return a @ np.asarray(b, dtype=np.float64)
+
+
+def gemm_rs(a_list, b_list):
+    """Per-rank partial products, summed over ranks, rows scattered.
+
+    Returns a list of W float64 arrays; entry s is rows [s*M/W, (s+1)*M/W) of
+    sum_q a_list[q] @ b_list[q].
+    """
+    w = len(a_list)
+    if w != len(b_list) or w < 1:
+        raise ValueError("need one A and one B per rank")
+    s_full = None
+    for q in range(w):
+        p_q = np.asarray(a_list[q], dtype=np.float64) @ np.asarray(b_list[q], dtype=np.float64)
+        s_full = p_q if s_full is None else s_full + p_q
+    m = s_full.shape[0]
+    if m % w:
+        raise ValueError("M must be a multiple of W")
+    ms = m // w
+    return [s_full[s * ms:(s + 1) * ms] for s in range(w)]
+
+
+def ag_gemm_entries(shards, b, rows, cols):
+    """Selected entries C[rows[t], cols[t]] of the AllGather-GEMM, one dot each.
+
+    Row g of the gathered A is row g - s*Ms of shard s = g // Ms.
+    """
+    ms = shards[0].shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    out = np.empty(rows.shape[0], dtype=np.float64)
+    bt = np.asarray(b)
+    for t in range(rows.shape[0]):
+        s = int(rows[t]) // ms
+        a_row = np.asarray(shards[s][int(rows[t]) - s * ms], dtype=np.float64)
+        out[t] = float(np.dot(a_row, np.asarray(bt[:, int(cols[t])], dtype=np.float64)))
+    return out
+
+
+def gemm_rs_entries(a_list, b_list, dest, rows, cols):
+    """Selected entries out_dest[t][rows[t], cols[t]] of the GEMM-ReduceScatter.
+
+    out_s[m, n] = sum over q of A_q[s*Ms + m, :] . B_q[:, n], summed in q order.
+    """
+    w = len(a_list)
+    ms = a_list[0].shape[0] // w
+    out = np.empty(len(rows), dtype=np.float64)
+    for t in range(len(rows)):
+        g = int(dest[t]) * ms + int(rows[t])
+        acc = 0.0
+        for q in range(w):
+            acc += float(np.dot(np.asarray(a_list[q][g], dtype=np.float64),
+                                np.asarray(b_list[q][:, int(cols[t])], dtype=np.float64)))
+        out[t] = acc
+    return out

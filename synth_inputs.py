@@ -1,0 +1,160 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the CPU oracle.
+
+This module only draws numbers and rounds them to bfloat16; it holds none of
+the arithmetic of the fused AllGather-GEMM / GEMM-ReduceScatter.  Both the CUDA
+path and the oracle read the same bf16 bit patterns produced here.
+
+Recipe (one generator per workload):
+  * numpy ``Generator(PCG64(seed))``, float64 draws;
+  * "uniform": U[-1, 1]; "normal(s)": N(0, s^2);
+  * each float64 draw is rounded to the nearest bfloat16, ties to even;
+  * AllGather-GEMM draw order: the gathered A (M x K, row-major; shard s is
+    rows s*M/W .. (s+1)*M/W - 1), then B (K x N);
+  * GEMM-ReduceScatter draw order: A_0 .. A_{W-1} (each M x K_rank), then
+    B_0 .. B_{W-1} (each K_rank x N).
+
+The workloads below stand in for the "real-model shapes" that the DITRON and
+AutoOverlap/Syncopate evaluations draw from Llama/Qwen/Mixtral/GPT/DeepSeek
+(their shape appendix is not available), with the sizes, seeds and value
+distributions of the five benchmark configurations.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+
+def bf16_bits_from_f64(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to bfloat16 (round to nearest, ties to even).
+
+    Returns the uint16 bit patterns.  Rounding is done exactly in float64: the
+    significand m in [0.5, 1) is scaled by 2^8, rounded half-to-even by rint,
+    and scaled back; the result then has 8 significant bits and converts to
+    float32 exactly, whose top 16 bits are the bfloat16 pattern.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    r = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+    tiny = (r != 0) & (np.abs(r) < np.ldexp(1.0, -126))
+    if np.any(tiny):
+        raise ValueError("draw below the bf16 normal range; pick another seed")
+    if np.any(np.abs(r) >= np.ldexp(1.0, 128)):
+        raise ValueError("draw above the bf16 range")
+    r32 = r.astype(np.float32)
+    return (r32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def f64_from_bf16_bits(bits: np.ndarray) -> np.ndarray:
+    """Exact float64 values of bfloat16 bit patterns."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def _draw(rng: np.random.Generator, dist: str, shape) -> np.ndarray:
+    if dist == "uniform":
+        return rng.uniform(-1.0, 1.0, size=shape)
+    if dist.startswith("normal(") and dist.endswith(")"):
+        std = float(dist[len("normal("):-1])
+        return rng.normal(0.0, std, size=shape)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def _draw_bf16(rng, dist, shape, row_block=4096):
+    """Draw a row-major matrix in row blocks (same stream as one big draw)."""
+    rows, cols = shape
+    out = np.empty(shape, dtype=np.uint16)
+    for r0 in range(0, rows, row_block):
+        r1 = min(rows, r0 + row_block)
+        out[r0:r1] = bf16_bits_from_f64(_draw(rng, dist, (r1 - r0, cols)))
+    return out
+
+
+@dataclass
+class AGInputs:
+    world_size: int
+    shards: list            # W arrays uint16 [M/W, K]
+    b: np.ndarray           # uint16 [K, N]
+
+
+@dataclass
+class RSInputs:
+    world_size: int
+    a: list                 # W arrays uint16 [M, K_rank]
+    b: list                 # W arrays uint16 [K_rank, N]
+
+
+def make_ag_inputs(world_size: int, m: int, n: int, k: int, seed: int,
+                   dist_a: str = "uniform", dist_b: str = "uniform") -> AGInputs:
+    """Inputs of one AllGather-GEMM: W row shards of A (M x K) and B (K x N)."""
+    if m % world_size:
+        raise ValueError("M must be a multiple of the world size")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = _draw_bf16(rng, dist_a, (m, k))
+    b = _draw_bf16(rng, dist_b, (k, n))
+    ms = m // world_size
+    shards = [np.ascontiguousarray(a[s * ms:(s + 1) * ms]) for s in range(world_size)]
+    return AGInputs(world_size, shards, b)
+
+
+def make_rs_inputs(world_size: int, m: int, n: int, k_rank: int, seed: int,
+                   dist_a: str = "uniform", dist_b: str = "uniform") -> RSInputs:
+    """Inputs of one GEMM-ReduceScatter: per rank A_q (M x K_rank), B_q (K_rank x N)."""
+    if m % world_size:
+        raise ValueError("M must be a multiple of the world size")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = [_draw_bf16(rng, dist_a, (m, k_rank)) for _ in range(world_size)]
+    b = [_draw_bf16(rng, dist_b, (k_rank, n)) for _ in range(world_size)]
+    return RSInputs(world_size, a, b)
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One benchmark / parity workload: shapes, seed, distributions, chunking."""
+    name: str
+    op: str                 # "ag" or "rs"
+    world_size: int
+    m: int                  # total rows (gathered M for AG; M for RS)
+    n: int
+    k: int                  # AG: full K; RS: K per rank
+    seed: int
+    dist_a: str
+    dist_b: str
+    chunk_rows: int
+    note: str = ""
+
+    @property
+    def flops(self) -> float:
+        if self.op == "ag":
+            return 2.0 * self.m * self.n * self.k
+        return 2.0 * self.m * self.n * self.k * self.world_size
+
+    def make(self):
+        if self.op == "ag":
+            return make_ag_inputs(self.world_size, self.m, self.n, self.k, self.seed,
+                                  self.dist_a, self.dist_b)
+        return make_rs_inputs(self.world_size, self.m, self.n, self.k, self.seed,
+                              self.dist_a, self.dist_b)
+
+
+WORKLOADS = {
+    # small AllGather-GEMM, W=2: A shards 256x512, B 512x512, U[-1,1], seed 0, chunk 128
+    "ag_w2_m512_n512_k512": Workload("ag_w2_m512_n512_k512", "ag", 2, 512, 512, 512, 0,
+                                     "uniform", "uniform", 128),
+    # GEMM-ReduceScatter, W=4: A_q 2048x2048, B_q 2048x4096, N(0,0.02), seed 1, chunk 256
+    "rs_w4_m2048_n4096_k2048": Workload("rs_w4_m2048_n4096_k2048", "rs", 4, 2048, 4096, 2048, 1,
+                                        "normal(0.02)", "normal(0.02)", 256),
+    # Llama-70B-like TP=8 FFN pair, seed 2: activations N(0,1), weights N(0,0.02)
+    "ag_w8_m8192_n3584_k8192": Workload("ag_w8_m8192_n3584_k8192", "ag", 8, 8192, 3584, 8192, 2,
+                                        "normal(1.0)", "normal(0.02)", 256),
+    "rs_w8_m8192_n8192_k3584": Workload("rs_w8_m8192_n8192_k3584", "rs", 8, 8192, 8192, 3584, 2,
+                                        "normal(1.0)", "normal(0.02)", 256),
+    # non-perfect tiling, W=6, U[-1,1], seed 3, chunk 192: every edge ragged
+    "ag_w6_m6000_n3000_k5120": Workload("ag_w6_m6000_n3000_k5120", "ag", 6, 6000, 3000, 5120, 3,
+                                        "uniform", "uniform", 192),
+    "rs_w6_m6000_n5120_k3000": Workload("rs_w6_m6000_n5120_k3000", "rs", 6, 6000, 5120, 3000, 3,
+                                        "uniform", "uniform", 192),
+    # largest AllGather-GEMM (chunk/backend sweep), W=8, U[-1,1], seed 4
+    "ag_w8_m16384_n8192_k8192": Workload("ag_w8_m16384_n8192_k8192", "ag", 8, 16384, 8192, 8192, 4,
+                                         "uniform", "uniform", 256),
+}

@@ -1,0 +1,242 @@
+"""Pins of the tile-order oracle (distributed swizzle, gather and scatter modes).
+
+Checked against: the hand-written worked orders in tests/golden (from the
+DITRON Fig. 3 rule and the Triton-distributed non-perfect tiling rule),
+bijection on tile ids including ragged edges, identity when the swizzle is
+off, dependency safety of the gather order (simulated chunk arrival), the
+own-rank-first / own-rank-last properties, the group raster inside a chunk,
+and brute-force arrival counts.
+"""
+import itertools
+import os
+
+import pytest
+
+from oracle import plan
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, order = line.split(":")
+            rows.append((head.split(), [int(x) for x in order.split()]))
+    return rows
+
+
+def test_golden_rank_offset_orders():
+    w, ms, bm, bn = 4, 128, 128, 256
+    for head, order in _read_golden("ditron_fig3_rank_offset.txt"):
+        kind, sw = head[0], bool(int(head[1]))
+        if kind == "ag":
+            r = int(head[2])
+            assert plan.ag_order(w, r, w * ms, bn, ms, bm, bn, swizzle=sw) == order
+        else:
+            assert plan.rs_order(w, w * ms, bn, ms, bm, bn, swizzle=sw) == order
+
+
+def test_golden_nonperfect_tiling():
+    for head, order in _read_golden("nonperfect_tiling_w2.txt"):
+        if head[0] == "ag":
+            assert plan.ag_order(2, int(head[1]), 6, 1, 3, 2, 1) == order
+        else:
+            assert plan.rs_order(2, 6, 1, 3, 2, 1) == order
+
+
+GRID = [
+    # (W, M, N, Cr, BM, BN)
+    (1, 100, 300, 64, 128, 256),
+    (2, 512, 512, 128, 128, 256),
+    (3, 390, 520, 50, 128, 256),
+    (4, 2048, 4096, 256, 128, 256),
+    (6, 6000, 3000, 192, 128, 256),
+    (8, 80, 64, 4, 128, 256),
+    (8, 1024, 1000, 7, 64, 96),
+    (5, 35, 17, 3, 4, 8),
+    (7, 700, 33, 1000, 96, 16),
+]
+
+
+@pytest.mark.parametrize("case", GRID)
+@pytest.mark.parametrize("swizzle", [True, False])
+def test_orders_are_bijections(case, swizzle):
+    w, m, n, cr, bm, bn = case
+    _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    for r in range(w):
+        o = plan.ag_order(w, r, m, n, cr, bm, bn, swizzle)
+        assert sorted(o) == list(range(tm * tn))
+    o = plan.rs_order(w, m, n, cr, bm, bn, swizzle)
+    assert sorted(o) == list(range(w * tm * tn))
+
+
+@pytest.mark.parametrize("case", GRID)
+def test_swizzle_off_is_identity(case):
+    w, m, n, cr, bm, bn = case
+    _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    for r in range(w):
+        assert plan.ag_order(w, r, m, n, cr, bm, bn, False) == list(range(tm * tn))
+    assert plan.rs_order(w, m, n, cr, bm, bn, False) == list(range(w * tm * tn))
+
+
+def _rows_of_mtile(i, m, bm):
+    return range(i * bm, min((i + 1) * bm, m))
+
+
+@pytest.mark.parametrize("case", GRID)
+@pytest.mark.parametrize("swizzle", [True, False])
+def test_gather_order_is_dependency_monotone(case, swizzle):
+    """Simulated arrival: chunks land one by one in transfer order; the index of the
+    last chunk each tile needs never decreases along the tile order, so no tile is
+    held up by a chunk later than the one the next tile needs."""
+    w, m, n, cr, bm, bn = case
+    ms, nc, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    for r in range(w):
+        arrival = {c: t for t, c in enumerate(plan.ag_transfer_order(w, r, m, cr, swizzle))}
+        assert sorted(arrival) == [(s, j) for s in range(w) for j in range(nc)]
+        needed = []
+        for tile in plan.ag_order(w, r, m, n, cr, bm, bn, swizzle):
+            i = tile // tn
+            needed.append(max(arrival[plan.chunk_of_row(g, ms, cr)] for g in _rows_of_mtile(i, m, bm)))
+        if swizzle:
+            assert needed == sorted(needed)
+
+
+@pytest.mark.parametrize("case", GRID)
+def test_gather_own_rank_first(case):
+    w, m, n, cr, bm, bn = case
+    ms, nc, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    for r in range(w):
+        order = plan.ag_order(w, r, m, n, cr, bm, bn, True)
+        own = [t for t in order
+               if all(g // ms == r for g in _rows_of_mtile(t // tn, m, bm))]
+        if own:
+            # every tile that reads only its own rank's rows precedes all others
+            assert order[:len(own)] == own
+        # the first chunk transferred is the own rank's first chunk
+        assert plan.ag_transfer_order(w, r, m, cr, True)[0] == (r, 0)
+
+
+@pytest.mark.parametrize("case", GRID)
+def test_gather_straddling_tile_last(case):
+    w, m, n, cr, bm, bn = case
+    ms, nc, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    for r in range(1, w):
+        i = (r * ms - 1) // bm  # m-tile holding the last row of rank r-1
+        if (r * ms) // bm == i and i * bm < r * ms < min((i + 1) * bm, m):
+            # it waits for the last chunk of rank r-1, the latest chunk of the gather,
+            # so it runs after every tile that needs only earlier chunks
+            keys = plan.ag_keys(w, r, m, cr, bm, True)
+            assert keys[i] == w * nc - 1 == max(keys.values())
+            order = plan.ag_order(w, r, m, n, cr, bm, bn, True)
+            first = min(p for p, t in enumerate(order) if t // tn == i)
+            assert all(keys[t // tn] == keys[i] for t in order[first:])
+
+
+@pytest.mark.parametrize("case", GRID)
+def test_scatter_next_rank_first_own_last(case):
+    w, m, n, cr, bm, bn = case
+    ms, nc, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    order = plan.rs_order(w, m, n, cr, bm, bn, True)
+    for q in range(w):
+        mine = [(t // tn) % tm for t in order if t // (tm * tn) == q]
+        dests = [{g // ms for g in _rows_of_mtile(i, m, bm)} for i in mine]
+        nxt = (q + 1) % w
+        assert nxt in dests[0]
+        if w > 1:
+            own_only = [k for k, d in enumerate(dests) if d == {q}]
+            # tiles that feed only the own block come after every tile that feeds another rank
+            assert own_only == list(range(len(dests) - len(own_only), len(dests)))
+
+
+@pytest.mark.parametrize("case", GRID)
+def test_scatter_steps_interleave_ranks(case):
+    """Within one send step all ranks' tiles are interleaved: the key sequence is
+    non-decreasing along the order and, at equal key, the source ranks ascend."""
+    w, m, n, cr, bm, bn = case
+    ms, nc, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    keys = {q: plan.rs_keys(w, q, m, cr, bm) for q in range(w)}
+    seq = []
+    for t in plan.rs_order(w, m, n, cr, bm, bn, True):
+        q, i = t // (tm * tn), (t // tn) % tm
+        seq.append((keys[q][i], q))
+    assert seq == sorted(seq)
+
+
+@pytest.mark.parametrize("case", GRID)
+def test_group_raster_inside_chunk(case):
+    """Inside one key group, bands of up to G m-tiles are swept column by column."""
+    w, m, n, cr, bm, bn = case
+    _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    g = 8
+    order = plan.ag_order(w, 0, m, n, cr, bm, bn, True, group=g)
+    keys = plan.ag_keys(w, 0, m, cr, bm, True)
+    pos = 0
+    while pos < len(order):
+        k = keys[order[pos] // tn]
+        grp = list(itertools.takewhile(lambda t: keys[t // tn] == k, order[pos:]))
+        mt = sorted({t // tn for t in grp})
+        assert len(grp) == len(mt) * tn
+        for b0 in range(0, len(mt), g):
+            band = mt[b0:b0 + g]
+            seg = grp[b0 * tn:(b0 + len(band)) * tn]
+            assert seg == [i * tn + c for c in range(tn) for i in band]
+        pos += len(grp)
+
+
+@pytest.mark.parametrize("case", GRID)
+def test_arrival_counts_brute_force(case):
+    w, m, n, cr, bm, bn = case
+    ms, nc, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    counts = {}
+    for t in plan.rs_order(w, m, n, cr, bm, bn, True):
+        q, i, c = t // (tm * tn), (t // tn) % tm, t % tn
+        for u in {plan.chunk_of_row(g, ms, cr) for g in _rows_of_mtile(i, m, bm)}:
+            counts[(u[0], u[1], c)] = counts.get((u[0], u[1], c), 0) + 1
+    assert counts == plan.rs_expected_arrivals(w, m, n, cr, bm, bn)
+
+
+def test_chunk_map_covers_rows_once():
+    for (w, m, n, cr, bm, bn) in GRID:
+        ms, nc, _, _ = plan.geometry(w, m, n, cr, bm, bn)
+        seen = []
+        for s in range(w):
+            for j in range(nc):
+                lo, hi = plan.chunk_rows_range(s, j, ms, cr)
+                assert lo < hi
+                seen.extend(range(lo, hi))
+                assert all(plan.chunk_of_row(g, ms, cr) == (s, j) for g in range(lo, hi))
+        assert seen == list(range(m))
+
+
+_ORIG_AG_ORDER = plan.ag_order
+
+
+def _mut_ag_order_negative_offset(w, r, m, n, cr, bm, bn, swizzle=True, group=8):
+    return _ORIG_AG_ORDER(w, (-r) % w, m, n, cr, bm, bn, swizzle, group)
+
+
+def _mut_ag_order_min_key(w, r, m, n, cr, bm, bn, swizzle=True, group=8):
+    _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    ms = m // w
+    nc = plan.cdiv(ms, cr)
+    keys = {i: min(plan.ag_pos(s, j, w, r, nc) for (s, j) in plan.tile_chunks(i, m, ms, cr, bm))
+            for i in range(tm)}
+    ent = sorted((keys[i], c, i) for i in range(tm) for c in range(tn))
+    return [i * tn + c for (_, c, i) in ent]
+
+
+@pytest.mark.parametrize("mutant", [_mut_ag_order_negative_offset, _mut_ag_order_min_key])
+def test_plan_pins_catch_planted_mistakes(mutant, monkeypatch):
+    monkeypatch.setattr(plan, "ag_order", mutant)
+    caught = False
+    for fn in (test_golden_rank_offset_orders, test_golden_nonperfect_tiling):
+        try:
+            fn()
+        except AssertionError:
+            caught = True
+    assert caught
