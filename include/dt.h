@@ -1,0 +1,194 @@
+/*
+ * dt.h - C ABI of the chunk-centric fused AllGather-GEMM and GEMM-ReduceScatter
+ *        for one GB300 (sm_103a).
+ *
+ * What is computed (DITRON page, section 4 "支持的并行策略": tensor parallelism overlaps
+ * AllGather with GEMM and GEMM with ReduceScatter; Triton-distributed talk, "GEMM
+ * ReduceScatter" paragraph):
+ *   AllGather-GEMM     C   = concat_rows(A_0 .. A_{W-1}) * B
+ *   GEMM-ReduceScatter out_s = rows [s*M/W, (s+1)*M/W) of  sum_q A_q * B_q
+ * W tensor-parallel ranks are emulated as W "virtual ranks" whose buffers live in the
+ * one GPU's HBM.  The user-facing signature is the local GEMM's plus rank and world size
+ * (AutoOverlap page, section 3: the fused operator keeps the local kernel's signature and
+ * adds rank / world size / mesh).
+ *
+ * How (AutoOverlap page, sections 4-5; DITRON page, section 3.2):
+ *   - communication moves in chunks of `chunk_rows` rows; a per-chunk ready flag flips
+ *     when a chunk has landed (chunk abstraction, P2P pull for AllGather, push for
+ *     ReduceScatter);
+ *   - one persistent tcgen05 GEMM consumes tiles in the rank-aware swizzle order
+ *     (gather mode: own rank first, remote chunks in arrival order, tiles that straddle
+ *     ranks after the chunks they need; scatter mode: the next rank's rows first, the
+ *     own block last) and waits per tile only for the chunks that tile reads;
+ *   - the chunk transfer runs on the copy engine, on in-kernel TMA bulk copies, or on
+ *     vectorised loads/stores (AutoOverlap page, Table 2 / Fig. 7);
+ *   - GEMM-ReduceScatter scatters fp32 partial tiles into the destination's slots and the
+ *     last arriving tile of a (chunk x column-tile) unit reduces the W partials in fixed
+ *     rank order q = 0..W-1, so results do not depend on tile order, chunk size or backend.
+ *
+ * Conventions
+ *   - Matrices are row-major with explicit leading dimensions in ELEMENTS.
+ *   - Inputs are bf16.  Outputs are bf16 (round to nearest even) or fp32.
+ *   - All pointers named "device" are CUDA device pointers on the current device, 16-byte
+ *     aligned; leading dimensions are multiples of 8 elements (16-byte TMA strides).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous
+ *     and stream-ordered; inputs must stay unchanged, and outputs and the workspace
+ *     untouched, until the stream has passed the call.
+ *   - The caller owns every buffer, including the workspace.  The library never allocates
+ *     device memory.  It keeps a small host-side record per workspace pointer (call epoch,
+ *     which plan is resident) and, once per device, a side stream and two events for the
+ *     copy-engine backend.
+ *   - Errors in the arguments are returned synchronously and nothing is launched.  Errors
+ *     found on the device (a bounded wait that ran out) are written to the workspace's
+ *     error word and returned by dt_check(); every device wait is bounded by
+ *     `timeout_us`, after which the kernel records the error and exits cleanly.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef DT_H_
+#define DT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DT_MAX_WORLD 16
+
+typedef enum {
+  DT_OK = 0,
+  DT_ERR_INVALID = 1,      /* bad argument (message: dt_last_error())                    */
+  DT_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement                 */
+  DT_ERR_TIMEOUT = 3,      /* a bounded device wait ran out (from dt_check)               */
+  DT_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed                         */
+  DT_ERR_WORKSPACE = 5     /* workspace missing, misaligned or smaller than required      */
+} dt_status;
+
+typedef enum {
+  DT_XFER_AUTO = 0,        /* pick per chunk size                                          */
+  DT_XFER_COPY_ENGINE = 1, /* host-issued cudaMemcpy2DAsync + stream flag write per chunk  */
+  DT_XFER_TMA = 2,         /* in-kernel cp.async.bulk, global -> shared -> global          */
+  DT_XFER_LDST = 3         /* in-kernel 16-byte vector loads/stores                        */
+} dt_xfer;
+
+typedef enum { DT_BF16 = 0, DT_F32 = 1 } dt_dtype;
+
+typedef enum { DT_OP_AG_GEMM = 0, DT_OP_GEMM_RS = 1 } dt_op;
+
+/* Problem description shared by every call.  Fill with dt_args_default() first. */
+typedef struct dt_args {
+  int32_t world_size;  /* W, 1..DT_MAX_WORLD                                               */
+  int32_t rank;        /* AllGather-GEMM: the rank whose view is computed (0..W-1);
+                          its own shard is "local", the other W-1 are "remote".  RS: unused */
+  int64_t m;           /* rows: gathered M for AG, M for RS; M % W == 0                    */
+  int64_t n;           /* columns of B and C; multiple of 8                                */
+  int64_t k;           /* AG: full K (multiple of 8); RS: K per rank                       */
+  int64_t chunk_rows;  /* rows per communication chunk, >= 1                               */
+  int32_t swizzle;     /* 1: rank-aware swizzle order; 0: naive order (all ranks tile 0)   */
+  int32_t backend;     /* dt_xfer, AllGather chunk transfer                                */
+  int32_t out_dtype;   /* dt_dtype of C / out_s                                            */
+  int32_t tile_m;      /* 0 or 128                                                         */
+  int32_t tile_n;      /* 0 or 256                                                         */
+  int32_t group;       /* m-tiles per band of the in-chunk raster; 0 = 8                   */
+  int64_t lda;         /* AG: of every shard; RS: of every A_q   (0 = K)                   */
+  int64_t ldb;         /* of B / every B_q                       (0 = N)                   */
+  int64_t ldc;         /* of C / every out_s                     (0 = N)                   */
+  int64_t timeout_us;  /* bound of every device wait; 0 = 2 s (env DT_WAIT_TIMEOUT_US)     */
+  int32_t num_sms;     /* persistent grid size; 0 = all SMs                                */
+  int32_t reserved;
+} dt_args;
+
+/* Fill `a` with defaults: W=1, rank 0, swizzle on, AUTO backend, bf16 output, 128x256
+ * tiles, group 8.  Sizes are zero and must be set by the caller. */
+void dt_args_default(dt_args* a);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int dt_version(void);
+
+/* sizeof(dt_args) as compiled into the library, for binding layout checks. */
+size_t dt_sizeof_args(void);
+
+/* Human-readable name of a status. Never NULL. */
+const char* dt_status_string(dt_status s);
+
+/* Message describing the last DT_ERR_INVALID / DT_ERR_UNSUPPORTED / DT_ERR_CUDA of the
+ * calling thread ("" if none).  Valid until the thread's next call. */
+const char* dt_last_error(void);
+
+/* Bytes of device workspace that `op` (dt_op) needs for `a`; 0 if `a` is invalid.
+ * AG: control block + per-chunk flags/counters + tile order + the gather buffer
+ *     (M x K bf16).  RS: control block + per-unit counters + tile order + the fp32
+ *     partial slots (W x W x M/W x N fp32). */
+size_t dt_workspace_size(const dt_args* a, int op);
+
+/* Zero the control block of a workspace laid out for (a, op) on `stream` and forget the
+ * library's record of it.  Optional: the first call that sees a workspace (or a changed
+ * layout) does the same. */
+dt_status dt_workspace_init(const dt_args* a, int op, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/* Fused AllGather-GEMM, rank a->rank's view.
+ *   a_shards : host array of W device pointers; shard s is A_s [M/W x K] bf16, ld = lda
+ *   b        : device pointer, B [K x N] bf16, ld = ldb
+ *   c        : device pointer, C [M x N] (out_dtype), ld = ldc
+ *   workspace: device pointer of >= dt_workspace_size(a, DT_OP_AG_GEMM) bytes, 256-byte
+ *              aligned, used by one call at a time.
+ * Rows of shard s are gathered into the workspace chunk by chunk (own rank first, then
+ * r+1, r+2, ...), each chunk's ready flag is released, and the persistent GEMM waits per
+ * tile for the chunks of its rows (DITRON page section 3.2 "Gather模式").  K == 0 writes
+ * zeros; M == 0 or N == 0 does nothing. */
+dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c,
+                     void* workspace, size_t ws_bytes, const dt_args* a, void* stream);
+
+/* Fused GEMM-ReduceScatter over all W virtual ranks.
+ *   a   : host array of W device pointers, A_q [M x K] bf16 (K = per-rank K), ld = lda
+ *   b   : host array of W device pointers, B_q [K x N] bf16, ld = ldb
+ *   out : host array of W device pointers, out_s [M/W x N] (out_dtype), ld = ldc
+ * Every tile (q, i, n) is one partial product; its fp32 rows are pushed into destination
+ * s's slot q and the last of the W * (m-tiles per chunk) arrivals of a unit reduces the
+ * slots in order q = 0..W-1 (DITRON page section 3.2 "Scatter模式"; Triton-distributed
+ * talk, notify/wait of the GEMM-ReduceScatter example). */
+dt_status dt_gemm_rs(const void* const* a, const void* const* b, void* const* out,
+                     void* workspace, size_t ws_bytes, const dt_args* a_args, void* stream);
+
+/* Kernel-level-overlap baselines with the same arguments and results (AutoOverlap page,
+ * section 2.1 / Fig. 2(b)): AG = per-chunk copies on a second stream and one launch of the
+ * same GEMM per chunk, gated by events; RS = one GEMM launch per destination block writing
+ * fp32 partials, then a separate reduction kernel on a second stream. */
+dt_status dt_ag_gemm_kernel_overlap(const void* const* a_shards, const void* b, void* c,
+                                    void* workspace, size_t ws_bytes, const dt_args* a,
+                                    void* stream);
+dt_status dt_gemm_rs_kernel_overlap(const void* const* a, const void* const* b,
+                                    void* const* out, void* workspace, size_t ws_bytes,
+                                    const dt_args* a_args, void* stream);
+
+/* Tile execution order of `op` for `a` computed on the host: order[p] is the tile run at
+ * position p.  AG tile id = i*Tn + n; RS tile id = (q*Tm + i)*Tn + n, with
+ * Tm = ceil(M/tile_m), Tn = ceil(N/tile_n).  `len` must equal the tile count.
+ * (DITRON page section 3.2: swizzle_func maps the original tile id to the new one.) */
+dt_status dt_swizzle_plan(const dt_args* a, int op, int32_t* order_host, int64_t len);
+
+/* The same order evaluated by the device kernel that the fused calls use, written to
+ * `order_dev` (device pointer, len int32) on `stream`. */
+dt_status dt_swizzle_plan_device(const dt_args* a, int op, int32_t* order_dev, int64_t len,
+                                 void* stream);
+
+/* Synchronise `stream`, read and clear the workspace's device error word.
+ * Returns DT_OK or DT_ERR_TIMEOUT; `info` (may be NULL) receives 4 words:
+ * {device code, site, detail0, detail1}. */
+dt_status dt_check(void* workspace, void* stream, uint32_t* info);
+
+/* Failure-detection testing, host side only: the next copy-engine AllGather-GEMM call on
+ * this process leaves out the copy and the ready-flag write of transfer step `step` (the
+ * position in the gather order; -1 clears).  The tiles that need that chunk wait until
+ * `timeout_us`, record DT_ERR_TIMEOUT in the workspace and exit; the CUDA context stays
+ * usable.  (Syncopate summary page, "局限与后续工作": fault injection for lost signals and
+ * timeouts.) */
+dt_status dt_debug_drop_transfer(int32_t step);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DT_H_ */

@@ -20,6 +20,8 @@ distributions of the five benchmark configurations.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 
 import numpy as np
@@ -60,13 +62,23 @@ def _draw(rng: np.random.Generator, dist: str, shape) -> np.ndarray:
     raise ValueError(f"unknown distribution {dist!r}")
 
 
-def _draw_bf16(rng, dist, shape, row_block=4096):
-    """Draw a row-major matrix in row blocks (same stream as one big draw)."""
+def _draw_bf16(rng, dist, shape, row_block=1024):
+    """Draw a row-major matrix in row blocks (the same stream as one big draw).
+
+    Draws are sequential; the rounding of each block runs on a thread pool."""
     rows, cols = shape
     out = np.empty(shape, dtype=np.uint16)
-    for r0 in range(0, rows, row_block):
-        r1 = min(rows, r0 + row_block)
-        out[r0:r1] = bf16_bits_from_f64(_draw(rng, dist, (r1 - r0, cols)))
+
+    def _round(r0, x):
+        out[r0:r0 + x.shape[0]] = bf16_bits_from_f64(x)
+
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        futs = []
+        for r0 in range(0, rows, row_block):
+            r1 = min(rows, r0 + row_block)
+            futs.append(ex.submit(_round, r0, _draw(rng, dist, (r1 - r0, cols))))
+        for f in futs:
+            f.result()
     return out
 
 

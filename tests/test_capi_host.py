@@ -1,0 +1,144 @@
+"""CPU checks of the C ABI library: it loads, exports every function include/dt.h declares,
+its argument struct matches the binding, argument errors come back synchronously, and
+its host evaluation of the tile order equals the oracle's bit for bit.
+
+No call here launches GPU work.
+"""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import plan as oplan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def dt():
+    from tile_level_communication_gb300 import build
+    build.build()
+    import tile_level_communication_gb300 as t
+    t.capi.lib()
+    return t
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "dt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dt_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(dt):
+    names = _declared_functions()
+    assert len(names) >= 14
+    h = ctypes.CDLL(dt.capi.LIB_PATH)
+    missing = [n for n in names if not hasattr(h, n)]
+    assert not missing, missing
+    # and the binding knows the same set
+    assert set(names) == set(dt.capi._SIGS)
+
+
+def test_args_layout_matches(dt):
+    assert dt.capi.lib().dt_sizeof_args() == ctypes.sizeof(dt.capi.DtArgs)
+    assert dt.capi.lib().dt_version() >= 100
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(world_size=0, m=8, n=8, k=8), "DT_ERR_INVALID"),
+    (dict(world_size=17, m=17, n=8, k=8), "DT_ERR_INVALID"),
+    (dict(world_size=3, m=8, n=8, k=8), "DT_ERR_INVALID"),          # M % W
+    (dict(world_size=2, m=8, n=12, k=8), "DT_ERR_UNSUPPORTED"),     # N % 8
+    (dict(world_size=2, m=8, n=8, k=12), "DT_ERR_UNSUPPORTED"),     # AG K % 8
+    (dict(world_size=2, m=8, n=8, k=8, rank=2), "DT_ERR_INVALID"),
+    (dict(world_size=2, m=8, n=8, k=8, chunk_rows=0), "DT_ERR_INVALID"),
+    (dict(world_size=2, m=8, n=8, k=8, lda=4), "DT_ERR_INVALID"),
+    (dict(world_size=2, m=8, n=8, k=8, lda=12), "DT_ERR_INVALID"),  # 16-byte rows
+])
+def test_argument_errors_are_synchronous(dt, kw, status):
+    w = kw.pop("world_size")
+    m, n, k = kw.pop("m"), kw.pop("n"), kw.pop("k")
+    a = dt.make_args(w, m, n, k, **kw)
+    with pytest.raises(dt.DtError):
+        dt.workspace_size(a, dt.OP_AG)  # returns 0: invalid
+    # the fused call rejects the same arguments, with the status, before touching a pointer
+    with pytest.raises(dt.DtError) as ei:
+        dt.ag_gemm([1] * max(1, min(w, 16)), 1, 1, 256, a, stream=0, ws_bytes=1 << 30)
+    assert ei.value.status == getattr(dt.capi, status)
+
+
+def test_workspace_errors(dt):
+    a = dt.make_args(2, 512, 512, 512, chunk_rows=128)
+    need = dt.workspace_size(a, dt.OP_AG)
+    assert need >= 512 * 512 * 2
+    with pytest.raises(dt.DtError) as ei:
+        dt.ag_gemm([256, 512], 1024, 2048, 4096, a, stream=0, ws_bytes=need - 1)
+    assert "DT_ERR_WORKSPACE" in str(ei.value)
+    with pytest.raises(dt.DtError) as ei:
+        dt.ag_gemm([256, 512], 1024, 2048, 4096 + 16, a, stream=0, ws_bytes=need)
+    assert "DT_ERR_WORKSPACE" in str(ei.value)  # not 256-byte aligned
+    with pytest.raises(dt.DtError) as ei:
+        dt.ag_gemm([256, 8], 1024, 2048, 4096, a, stream=0, ws_bytes=need)
+    assert "DT_ERR_INVALID" in str(ei.value)    # shard not 16-byte aligned
+    r = dt.make_args(4, 2048, 4096, 2048, chunk_rows=256)
+    assert dt.workspace_size(r, dt.OP_RS) >= 4 * 4 * 512 * 4096 * 4
+
+
+# ----------------------------------------------------------------------------- plan parity
+
+PLAN_GRID = [
+    # (W, M, N, Cr) with the library's 128 x 256 tiles
+    (1, 128, 256, 128), (1, 100, 264, 64), (2, 512, 512, 128), (2, 6, 8, 3),
+    (3, 390, 520, 50), (4, 2048, 4096, 256), (6, 6000, 3000, 192), (6, 6000, 5120, 192),
+    (8, 80, 64, 4), (8, 1024, 1000, 7), (5, 35, 16, 3), (7, 700, 40, 1000),
+    (8, 8192, 3584, 256), (8, 8192, 8192, 256), (8, 16384, 8192, 64), (16, 4096, 512, 100),
+    (3, 3 * 129, 8, 1), (4, 4 * 127, 8, 127), (2, 2 * 300, 264, 1000),
+]
+
+
+@pytest.mark.parametrize("case", PLAN_GRID)
+@pytest.mark.parametrize("swizzle", [True, False])
+def test_host_plan_matches_oracle_ag(dt, case, swizzle):
+    w, m, n, cr = case
+    for r in range(w):
+        a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr, swizzle=swizzle)
+        got = dt.swizzle_plan(a, dt.OP_AG)
+        want = oplan.ag_order(w, r, m, n, cr, 128, 256, swizzle)
+        assert got.tolist() == want, (case, r)
+
+
+@pytest.mark.parametrize("case", PLAN_GRID)
+@pytest.mark.parametrize("swizzle", [True, False])
+def test_host_plan_matches_oracle_rs(dt, case, swizzle):
+    w, m, n, cr = case
+    a = dt.make_args(w, m, n, 8, chunk_rows=cr, swizzle=swizzle)
+    got = dt.swizzle_plan(a, dt.OP_RS)
+    want = oplan.rs_order(w, m, n, cr, 128, 256, swizzle)
+    assert got.tolist() == want, case
+
+
+@pytest.mark.parametrize("group", [1, 3, 8, 64])
+def test_host_plan_group_width(dt, group):
+    for (w, m, n, cr) in [(4, 2048, 4096, 256), (6, 6000, 3000, 192)]:
+        a = dt.make_args(w, m, n, 8, rank=w - 1, chunk_rows=cr, group=group)
+        assert dt.swizzle_plan(a, dt.OP_AG).tolist() == oplan.ag_order(
+            w, w - 1, m, n, cr, 128, 256, True, group)
+        assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(
+            w, m, n, cr, 128, 256, True, group)
+
+
+def test_host_plan_random_sweep(dt):
+    rng = np.random.Generator(np.random.PCG64(5))
+    for _ in range(60):
+        w = int(rng.integers(1, 9))
+        ms = int(rng.integers(1, 700))
+        m = w * ms
+        n = 8 * int(rng.integers(1, 80))
+        cr = int(rng.integers(1, 2 * ms + 2))
+        r = int(rng.integers(0, w))
+        a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr)
+        assert dt.swizzle_plan(a, dt.OP_AG).tolist() == oplan.ag_order(w, r, m, n, cr, 128, 256)
+        assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(w, m, n, cr, 128, 256)

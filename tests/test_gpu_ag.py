@@ -1,0 +1,206 @@
+"""GPU parity of the fused AllGather-GEMM (through the C ABI) against the float64 oracle.
+
+Covers the small W=2 workload for every transfer backend, swizzle on/off, both ranks and
+both output types; the ragged W=6 workload (every tile edge ragged); bit-identity across
+tile order, chunk size, backend and the kernel-level-overlap baseline; edge cases (W=1,
+one-row shards, chunk of one row, chunks larger than a shard, K not a multiple of the
+k-block, K=0, M=0, padded leading dimensions with canaries); the bounded-wait failure
+path; and sampled entries at the full sizes in the benchmark's launch configuration.
+"""
+import numpy as np
+import pytest
+
+from gpu_helpers import (assert_close, bits_equal, dev_bf16, load_dt, need_gpu, out_tensor,
+                         to_f64, torch, workspace)
+from oracle import reference
+from synth_inputs import WORKLOADS, f64_from_bf16_bits, make_ag_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dt():
+    need_gpu()
+    return load_dt()
+
+
+def _oracle(inp):
+    return reference.ag_gemm([f64_from_bf16_bits(s) for s in inp.shards], f64_from_bf16_bits(inp.b))
+
+
+def _run(dt, inp, m, n, k, out_dtype="bf16", lda=0, ldb=0, ldc=0, fn=None, ws=None, **kw):
+    w = inp.world_size
+    args = dt.make_args(w, m, n, k, out_dtype=out_dtype, lda=lda, ldb=ldb, ldc=ldc, **kw)
+    shards = [dev_bf16(s, lda) for s in inp.shards]
+    b = dev_bf16(inp.b, ldb)
+    c = out_tensor(m, n, out_dtype, ldc)
+    if ws is None:
+        ws = workspace(dt.workspace_size(args, dt.OP_AG))
+    (fn or dt.ag_gemm)(shards, b, c, ws, args)
+    st, info = dt.check(ws)
+    assert st == 0, (dt.capi.status_string(st), info)
+    return c
+
+
+@pytest.fixture(scope="module")
+def small():
+    wl = WORKLOADS["ag_w2_m512_n512_k512"]
+    inp = wl.make()
+    return wl, inp, _oracle(inp)
+
+
+@pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
+@pytest.mark.parametrize("swizzle", [True, False])
+@pytest.mark.parametrize("rank", [0, 1])
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_small_parity(dt, small, backend, swizzle, rank, out_dtype):
+    wl, inp, ref = small
+    c = _run(dt, inp, wl.m, wl.n, wl.k, out_dtype, chunk_rows=wl.chunk_rows, backend=backend,
+             swizzle=swizzle, rank=rank)
+    assert_close(to_f64(c), ref, out_dtype, f"{backend} swz={swizzle} r={rank}")
+
+
+def test_small_bit_identical_across_variants(dt, small):
+    wl, inp, ref = small
+    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=128, backend="tma")
+    for backend in ["copy_engine", "tma", "ldst"]:
+        for swizzle in [True, False]:
+            for cr in [1, 64, 100, 128, 256, 1000]:
+                c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, backend=backend, swizzle=swizzle,
+                         rank=1)
+                assert bits_equal(c, base), (backend, swizzle, cr)
+    c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=128, fn=dt.ag_gemm_kernel_overlap)
+    assert bits_equal(c, base)
+
+
+@pytest.fixture(scope="module")
+def ragged():
+    wl = WORKLOADS["ag_w6_m6000_n3000_k5120"]
+    inp = wl.make()
+    return wl, inp, _oracle(inp)
+
+
+@pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
+def test_ragged_parity_and_identity(dt, ragged, backend):
+    wl, inp, ref = ragged
+    outs = []
+    for rank, swizzle, cr in [(0, True, wl.chunk_rows), (5, True, wl.chunk_rows), (3, False, 77),
+                              (2, True, 1000)]:
+        c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, backend=backend, swizzle=swizzle,
+                 rank=rank)
+        assert_close(to_f64(c), ref, "bf16", f"{backend} r={rank}")
+        outs.append(c)
+    assert all(bits_equal(outs[0], o) for o in outs[1:])
+    c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, rank=4,
+             fn=dt.ag_gemm_kernel_overlap)
+    assert bits_equal(outs[0], c)
+
+
+@pytest.mark.parametrize("case", [
+    # (W, M, N, K, chunk_rows)
+    (1, 128, 256, 64, 128),
+    (1, 300, 264, 72, 64),
+    (3, 3, 8, 8, 1),          # one row per shard, one 8-column tile
+    (4, 4 * 33, 40, 136, 1),  # chunk of one row, K not a multiple of 64
+    (2, 2 * 70, 24, 8, 500),  # chunk larger than a shard
+    (8, 8 * 16, 520, 200, 5),
+    (16, 16 * 9, 16, 16, 4),
+])
+@pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
+def test_edge_shapes(dt, case, backend):
+    w, m, n, k, cr = case
+    inp = make_ag_inputs(w, m, n, k, seed=31 + m)
+    ref = _oracle(inp)
+    for rank in sorted({0, w - 1}):
+        c = _run(dt, inp, m, n, k, chunk_rows=cr, backend=backend, rank=rank)
+        assert_close(to_f64(c), ref, "bf16", f"{case} {backend} r={rank}")
+
+
+@pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
+def test_padded_leading_dims_and_canaries(dt, backend):
+    w, m, n, k = 3, 3 * 50, 72, 96
+    inp = make_ag_inputs(w, m, n, k, seed=77)
+    ref = _oracle(inp)
+    lda, ldb, ldc = 104, 80, 88
+    for out_dtype in ["bf16", "f32"]:
+        c = _run(dt, inp, m, n, k, out_dtype, lda=lda, ldb=ldb, ldc=ldc, chunk_rows=16,
+                 backend=backend, rank=1)
+        assert_close(to_f64(c, n), ref, out_dtype)
+        # the padding columns of C were filled with NaN and must be untouched
+        assert torch.isnan(c[:, n:].float()).all()
+
+
+def test_k_zero_and_m_zero(dt):
+    inp = make_ag_inputs(2, 8, 16, 8, seed=1)
+    args = dt.make_args(2, 8, 16, 0, chunk_rows=4)
+    c = out_tensor(8, 16, "bf16")
+    ws = workspace(dt.workspace_size(args, dt.OP_AG))
+    dt.ag_gemm([dev_bf16(s) for s in inp.shards], dev_bf16(inp.b), c, ws, args)
+    torch.cuda.synchronize()
+    assert (c.float() == 0).all()
+    args0 = dt.make_args(2, 0, 16, 8, chunk_rows=4)
+    dt.ag_gemm([dev_bf16(s) for s in inp.shards], dev_bf16(inp.b), c, ws, args0)
+    torch.cuda.synchronize()
+
+
+def test_workspace_reuse_across_problems(dt):
+    """One workspace, alternating problems and backends: epochs and layouts stay coherent."""
+    big = make_ag_inputs(4, 4 * 96, 264, 128, seed=5)
+    small_ = make_ag_inputs(2, 2 * 40, 8, 64, seed=6)
+    ref_big, ref_small = _oracle(big), _oracle(small_)
+    a_big = dt.make_args(4, 4 * 96, 264, 128, chunk_rows=32)
+    ws = workspace(dt.workspace_size(a_big, dt.OP_AG))
+    for it in range(3):
+        for backend in ["tma", "copy_engine", "ldst"]:
+            c = _run(dt, big, 4 * 96, 264, 128, chunk_rows=32, backend=backend, rank=it % 4, ws=ws)
+            assert_close(to_f64(c), ref_big, "bf16")
+            c = _run(dt, small_, 2 * 40, 8, 64, chunk_rows=7, backend=backend, rank=1, ws=ws)
+            assert_close(to_f64(c), ref_small, "bf16")
+
+
+def test_lost_chunk_times_out_and_context_survives(dt, small):
+    """Host-made fault: one chunk's copy and flag are never issued; the consumer tiles'
+    bounded waits run out, the error comes back through dt_check, and the next call works."""
+    wl, inp, ref = small
+    args = dt.make_args(2, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, backend="copy_engine",
+                        rank=0, timeout_us=200_000)
+    shards = [dev_bf16(s) for s in inp.shards]
+    b = dev_bf16(inp.b)
+    c = out_tensor(wl.m, wl.n, "bf16")
+    ws = workspace(dt.workspace_size(args, dt.OP_AG))
+    dt.debug_drop_transfer(3)  # the second chunk of rank 1
+    dt.ag_gemm(shards, b, c, ws, args)
+    st, info = dt.check(ws)
+    assert st == dt.capi.DT_ERR_TIMEOUT, (st, info)
+    assert info[0] == 1  # a chunk's ready flag did not flip
+    c2 = out_tensor(wl.m, wl.n, "bf16")
+    dt.ag_gemm(shards, b, c2, ws, args)
+    st, info = dt.check(ws)
+    assert st == 0, info
+    assert_close(to_f64(c2), ref, "bf16")
+
+
+def _sampled_indices(m, n, rng, count=1500):
+    rows = np.concatenate([rng.integers(0, m, count), [0, m - 1, m // 2, 127, 128]])
+    cols = np.concatenate([rng.integers(0, n, count), [0, n - 1, n // 2, 255, 256 % n]])
+    return rows, cols
+
+
+@pytest.mark.parametrize("name,backend,chunk", [
+    ("ag_w8_m8192_n3584_k8192", "auto", 256),
+    ("ag_w8_m16384_n8192_k8192", "auto", 256),
+    ("ag_w8_m16384_n8192_k8192", "copy_engine", 2048),
+    ("ag_w8_m16384_n8192_k8192", "ldst", 64),
+])
+def test_full_size_sampled(dt, name, backend, chunk):
+    wl = WORKLOADS[name]
+    inp = wl.make()
+    c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=chunk, backend=backend, rank=3)
+    rng = np.random.Generator(np.random.PCG64(9))
+    rows, cols = _sampled_indices(wl.m, wl.n, rng)
+    ref = reference.ag_gemm_entries([f64_from_bf16_bits(s) for s in inp.shards],
+                                    f64_from_bf16_bits(inp.b), rows, cols)
+    got = c.float()[torch.as_tensor(rows, device="cuda"), torch.as_tensor(cols, device="cuda")]
+    # the tolerance scale is the largest |C| over the sample
+    assert_close(got.cpu().numpy(), ref, "bf16", name)
+    assert torch.isfinite(c.float()).all()

@@ -1,0 +1,170 @@
+"""GPU parity of the fused GEMM-ReduceScatter (through the C ABI) against the float64 oracle.
+
+Covers the W=4 workload, the ragged W=6 workload, swizzle on/off, chunk sizes, bf16 and
+fp32 outputs, bit-identity across orders / chunks / the kernel-level-overlap baseline,
+edge cases (W=1, one-row blocks, chunk of one row, K not a multiple of the k-block, K=0,
+padded leading dimensions with canaries) and sampled entries at the full W=8 size.
+"""
+import numpy as np
+import pytest
+
+from gpu_helpers import (assert_close, bits_equal, dev_bf16, load_dt, need_gpu, out_tensor,
+                         to_f64, torch, workspace)
+from oracle import reference
+from synth_inputs import WORKLOADS, f64_from_bf16_bits, make_rs_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dt():
+    need_gpu()
+    return load_dt()
+
+
+def _oracle(inp):
+    return reference.gemm_rs([f64_from_bf16_bits(a) for a in inp.a],
+                             [f64_from_bf16_bits(b) for b in inp.b])
+
+
+def _run(dt, inp, m, n, k, out_dtype="bf16", lda=0, ldb=0, ldc=0, fn=None, ws=None, **kw):
+    w = inp.world_size
+    args = dt.make_args(w, m, n, k, out_dtype=out_dtype, lda=lda, ldb=ldb, ldc=ldc, **kw)
+    a = [dev_bf16(x, lda) for x in inp.a]
+    b = [dev_bf16(x, ldb) for x in inp.b]
+    outs = [out_tensor(m // w, n, out_dtype, ldc) for _ in range(w)]
+    if ws is None:
+        ws = workspace(dt.workspace_size(args, dt.OP_RS))
+    (fn or dt.gemm_rs)(a, b, outs, ws, args)
+    st, info = dt.check(ws)
+    assert st == 0, (dt.capi.status_string(st), info)
+    return outs
+
+
+def _check_all(outs, ref, out_dtype, n=None, what=""):
+    for s, (o, r) in enumerate(zip(outs, ref)):
+        assert_close(to_f64(o, n), r, out_dtype, f"{what} rank {s}")
+
+
+@pytest.fixture(scope="module")
+def w4():
+    wl = WORKLOADS["rs_w4_m2048_n4096_k2048"]
+    inp = wl.make()
+    return wl, inp, _oracle(inp)
+
+
+@pytest.mark.parametrize("swizzle", [True, False])
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_w4_parity(dt, w4, swizzle, out_dtype):
+    wl, inp, ref = w4
+    outs = _run(dt, inp, wl.m, wl.n, wl.k, out_dtype, chunk_rows=wl.chunk_rows, swizzle=swizzle)
+    _check_all(outs, ref, out_dtype, what=f"swz={swizzle}")
+
+
+def test_w4_bit_identical_across_variants(dt, w4):
+    wl, inp, ref = w4
+    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256)
+    for swizzle in [True, False]:
+        for cr in [1, 64, 100, 512, 4096]:
+            outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=swizzle)
+            assert all(bits_equal(o, b) for o, b in zip(outs, base)), (swizzle, cr)
+    for group in [1, 3]:
+        outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, group=group)
+        assert all(bits_equal(o, b) for o, b in zip(outs, base))
+    outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, fn=dt.gemm_rs_kernel_overlap)
+    assert all(bits_equal(o, b) for o, b in zip(outs, base))
+
+
+def test_ragged_parity_and_identity(dt):
+    wl = WORKLOADS["rs_w6_m6000_n5120_k3000"]
+    inp = wl.make()
+    ref = _oracle(inp)
+    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows)
+    _check_all(base, ref, "bf16", what="ragged")
+    for swizzle, cr in [(False, wl.chunk_rows), (True, 77), (True, 1000)]:
+        outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=swizzle)
+        assert all(bits_equal(o, b) for o, b in zip(outs, base)), (swizzle, cr)
+    outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, fn=dt.gemm_rs_kernel_overlap)
+    assert all(bits_equal(o, b) for o, b in zip(outs, base))
+
+
+@pytest.mark.parametrize("case", [
+    # (W, M, N, K_rank, chunk_rows)
+    (1, 128, 256, 64, 128),
+    (1, 300, 264, 72, 64),
+    (3, 3, 8, 8, 1),
+    (4, 4 * 33, 40, 136, 1),
+    (2, 2 * 70, 24, 8, 500),
+    (8, 8 * 16, 520, 200, 5),
+    (16, 16 * 9, 16, 16, 4),
+    (5, 5 * 130, 256, 20, 130),
+])
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_edge_shapes(dt, case, out_dtype):
+    w, m, n, k, cr = case
+    inp = make_rs_inputs(w, m, n, k, seed=41 + m)
+    ref = _oracle(inp)
+    for swizzle in [True, False]:
+        outs = _run(dt, inp, m, n, k, out_dtype, chunk_rows=cr, swizzle=swizzle)
+        _check_all(outs, ref, out_dtype, what=f"{case}")
+
+
+def test_padded_leading_dims_and_canaries(dt):
+    w, m, n, k = 3, 3 * 50, 72, 96
+    inp = make_rs_inputs(w, m, n, k, seed=78)
+    ref = _oracle(inp)
+    lda, ldb, ldc = 104, 80, 88
+    for out_dtype in ["bf16", "f32"]:
+        outs = _run(dt, inp, m, n, k, out_dtype, lda=lda, ldb=ldb, ldc=ldc, chunk_rows=16)
+        _check_all(outs, ref, out_dtype, n)
+        for o in outs:
+            assert torch.isnan(o[:, n:].float()).all()
+
+
+def test_k_zero(dt):
+    args = dt.make_args(2, 8, 16, 0, chunk_rows=4)
+    outs = [out_tensor(4, 16, "f32") for _ in range(2)]
+    a = [torch.zeros((8, 8), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    b = [torch.zeros((8, 16), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    ws = workspace(dt.workspace_size(args, dt.OP_RS))
+    dt.gemm_rs(a, b, outs, ws, dt.make_args(2, 8, 16, 0, chunk_rows=4, out_dtype="f32"))
+    torch.cuda.synchronize()
+    assert all((o == 0).all() for o in outs)
+
+
+def test_repeated_calls_reuse_counters(dt, w4):
+    """Arrival counters return to zero inside each call, so back-to-back calls on one
+    workspace keep reducing correctly."""
+    wl, inp, ref = w4
+    args = dt.make_args(4, wl.m, wl.n, wl.k, chunk_rows=128)
+    ws = workspace(dt.workspace_size(args, dt.OP_RS))
+    a = [dev_bf16(x) for x in inp.a]
+    b = [dev_bf16(x) for x in inp.b]
+    first = None
+    for it in range(4):
+        outs = [out_tensor(wl.m // 4, wl.n, "bf16") for _ in range(4)]
+        dt.gemm_rs(a, b, outs, ws, args)
+        st, info = dt.check(ws)
+        assert st == 0, info
+        if first is None:
+            first = outs
+            _check_all(outs, ref, "bf16")
+        else:
+            assert all(bits_equal(o, f) for o, f in zip(outs, first))
+
+
+def test_full_size_sampled(dt):
+    wl = WORKLOADS["rs_w8_m8192_n8192_k3584"]
+    inp = wl.make()
+    outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows)
+    rng = np.random.Generator(np.random.PCG64(10))
+    ms = wl.m // wl.world_size
+    cnt = 400
+    dest = np.concatenate([rng.integers(0, wl.world_size, cnt), [0, wl.world_size - 1]])
+    rows = np.concatenate([rng.integers(0, ms, cnt), [0, ms - 1]])
+    cols = np.concatenate([rng.integers(0, wl.n, cnt), [wl.n - 1, 0]])
+    ref = reference.gemm_rs_entries([f64_from_bf16_bits(a) for a in inp.a],
+                                    [f64_from_bf16_bits(b) for b in inp.b], dest, rows, cols)
+    got = np.array([float(outs[int(d)][int(r), int(c)].float()) for d, r, c in zip(dest, rows, cols)])
+    assert_close(got, ref, "bf16", "rs full")
+    assert all(torch.isfinite(o.float()).all() for o in outs)

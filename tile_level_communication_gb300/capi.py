@@ -1,0 +1,213 @@
+"""ctypes binding of libdt.so (include/dt.h): argument marshalling only.
+
+Every step of the fused AllGather-GEMM / GEMM-ReduceScatter runs in the library's CUDA
+kernels; this module converts Python arguments into the C structs and pointers, calls the
+C entry point with the same name, and raises ``DtError`` on a non-OK status.  Tensors may be
+anything with ``data_ptr()`` (torch tensors) or plain integer addresses.  When the library
+is not built, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdt.so")
+
+DT_OK, DT_ERR_INVALID, DT_ERR_UNSUPPORTED, DT_ERR_TIMEOUT, DT_ERR_CUDA, DT_ERR_WORKSPACE = range(6)
+BACKENDS = {"auto": 0, "copy_engine": 1, "tma": 2, "ldst": 3}
+DTYPES = {"bf16": 0, "f32": 1}
+OP_AG, OP_RS = 0, 1
+MAX_WORLD = 16
+
+# every function include/dt.h declares: name -> (restype, argtypes)
+_P = ctypes.c_void_p
+_SIGS = {
+    "dt_args_default": (None, [_P]),
+    "dt_version": (ctypes.c_int, []),
+    "dt_sizeof_args": (ctypes.c_size_t, []),
+    "dt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "dt_last_error": (ctypes.c_char_p, []),
+    "dt_workspace_size": (ctypes.c_size_t, [_P, ctypes.c_int]),
+    "dt_workspace_init": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "dt_ag_gemm": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_gemm_rs": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_ag_gemm_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_gemm_rs_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_swizzle_plan": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64]),
+    "dt_swizzle_plan_device": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64, _P]),
+    "dt_check": (ctypes.c_int, [_P, _P, _P]),
+    "dt_debug_drop_transfer": (ctypes.c_int, [ctypes.c_int32]),
+}
+
+
+class DtArgs(ctypes.Structure):
+    """Mirror of ``dt_args``."""
+    _fields_ = [
+        ("world_size", ctypes.c_int32), ("rank", ctypes.c_int32),
+        ("m", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+        ("chunk_rows", ctypes.c_int64),
+        ("swizzle", ctypes.c_int32), ("backend", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+        ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("group", ctypes.c_int32),
+        ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
+        ("timeout_us", ctypes.c_int64),
+        ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    ]
+
+
+class DtError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_string(status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; run `python -m tile_level_communication_gb300.build`")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, argt) in _SIGS.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = argt
+        if h.dt_sizeof_args() != ctypes.sizeof(DtArgs):
+            raise RuntimeError("dt_args layout mismatch between libdt.so and the binding")
+        _lib = h
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().dt_status_string(status).decode()
+    except Exception:  # library missing: still format the error
+        return f"status {status}"
+
+
+def _raise(status: int):
+    if status != DT_OK:
+        raise DtError(status, lib().dt_last_error().decode())
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _ptr_array(xs):
+    arr = (ctypes.c_void_p * len(xs))()
+    for i, x in enumerate(xs):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def make_args(world_size: int, m: int, n: int, k: int, *, rank: int = 0, chunk_rows: int = 128,
+              swizzle: bool = True, backend: str = "auto", out_dtype: str = "bf16",
+              lda: int = 0, ldb: int = 0, ldc: int = 0, timeout_us: int = 0, num_sms: int = 0,
+              group: int = 8) -> DtArgs:
+    a = DtArgs()
+    lib().dt_args_default(ctypes.byref(a))
+    a.world_size, a.rank, a.m, a.n, a.k = world_size, rank, m, n, k
+    a.chunk_rows = chunk_rows
+    a.swizzle = 1 if swizzle else 0
+    a.backend = BACKENDS[backend]
+    a.out_dtype = DTYPES[out_dtype]
+    a.lda, a.ldb, a.ldc = lda, ldb, ldc
+    a.timeout_us = timeout_us
+    a.num_sms = num_sms
+    a.group = group
+    return a
+
+
+def workspace_size(args: DtArgs, op: int) -> int:
+    n = lib().dt_workspace_size(ctypes.byref(args), op)
+    if n == 0:
+        raise DtError(DT_ERR_INVALID, lib().dt_last_error().decode())
+    return int(n)
+
+
+def workspace_init(args: DtArgs, op: int, workspace, nbytes: int, stream=None):
+    _raise(lib().dt_workspace_init(ctypes.byref(args), op, _ptr(workspace), nbytes, _stream(stream)))
+
+
+def _nbytes(workspace, nbytes):
+    if nbytes is not None:
+        return nbytes
+    return int(workspace.numel() * workspace.element_size())
+
+
+def ag_gemm(shards, b, c, workspace, args: DtArgs, stream=None, ws_bytes=None):
+    _raise(lib().dt_ag_gemm(_ptr_array(shards), _ptr(b), _ptr(c), _ptr(workspace),
+                            _nbytes(workspace, ws_bytes), ctypes.byref(args), _stream(stream)))
+
+
+def gemm_rs(a_list, b_list, out_list, workspace, args: DtArgs, stream=None, ws_bytes=None):
+    _raise(lib().dt_gemm_rs(_ptr_array(a_list), _ptr_array(b_list), _ptr_array(out_list),
+                            _ptr(workspace), _nbytes(workspace, ws_bytes), ctypes.byref(args),
+                            _stream(stream)))
+
+
+def ag_gemm_kernel_overlap(shards, b, c, workspace, args: DtArgs, stream=None, ws_bytes=None):
+    _raise(lib().dt_ag_gemm_kernel_overlap(_ptr_array(shards), _ptr(b), _ptr(c), _ptr(workspace),
+                                           _nbytes(workspace, ws_bytes), ctypes.byref(args),
+                                           _stream(stream)))
+
+
+def gemm_rs_kernel_overlap(a_list, b_list, out_list, workspace, args: DtArgs, stream=None,
+                           ws_bytes=None):
+    _raise(lib().dt_gemm_rs_kernel_overlap(_ptr_array(a_list), _ptr_array(b_list),
+                                           _ptr_array(out_list), _ptr(workspace),
+                                           _nbytes(workspace, ws_bytes), ctypes.byref(args),
+                                           _stream(stream)))
+
+
+def tile_count(args: DtArgs, op: int) -> int:
+    tm = -(-args.m // 128)
+    tn = -(-args.n // 256)
+    return (1 if op == OP_AG else args.world_size) * tm * tn
+
+
+def swizzle_plan(args: DtArgs, op: int) -> np.ndarray:
+    """Host evaluation of the tile order (order[p] = tile run at position p)."""
+    t = tile_count(args, op)
+    out = np.zeros(t, dtype=np.int32)
+    _raise(lib().dt_swizzle_plan(ctypes.byref(args), op, out.ctypes.data, t))
+    return out
+
+
+def swizzle_plan_device(args: DtArgs, op: int, order_dev, stream=None):
+    """Device evaluation into ``order_dev`` (int32 device buffer of tile_count entries)."""
+    _raise(lib().dt_swizzle_plan_device(ctypes.byref(args), op, _ptr(order_dev),
+                                        tile_count(args, op), _stream(stream)))
+
+
+def debug_drop_transfer(step: int):
+    """Host-side fault injection: the next copy-engine AllGather call skips transfer `step`."""
+    _raise(lib().dt_debug_drop_transfer(step))
+
+
+def check(workspace, stream=None):
+    """Synchronise, read and clear the device error word; returns (status, info[4])."""
+    info = (ctypes.c_uint32 * 4)()
+    st = lib().dt_check(_ptr(workspace), _stream(stream), info)
+    return st, list(info)

@@ -1,0 +1,775 @@
+// C ABI of the fused AllGather-GEMM / GEMM-ReduceScatter (declared in include/dt.h).
+//
+// Host responsibilities: argument validation, workspace layout, the per-workspace call
+// epoch (so ready flags never need resetting), tensor-map encoding, the plan kernel, the
+// copy-engine chunk transfer, kernel launches, and the kernel-level-overlap baselines.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/dt.h"
+#include "dt_internal.h"
+
+using namespace dt;
+
+namespace {
+
+// ------------------------------------------------------------------------------ errors
+thread_local std::string g_last_error;
+
+dt_status fail(dt_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+dt_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define DT_CUDA(call)                                    \
+  do {                                                   \
+    cudaError_t e_ = (call);                             \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);  \
+  } while (0)
+
+// ------------------------------------------------------------------------------ driver entry points
+typedef CUresult (*PfnEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*PfnWriteValue32)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+void* driver_fn(const char* name) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return fn;
+}
+
+PfnEncodeTiled encode_tiled() {
+  static PfnEncodeTiled fn = reinterpret_cast<PfnEncodeTiled>(driver_fn("cuTensorMapEncodeTiled"));
+  return fn;
+}
+PfnWriteValue32 write_value32() {
+  static PfnWriteValue32 fn = reinterpret_cast<PfnWriteValue32>(driver_fn("cuStreamWriteValue32"));
+  return fn;
+}
+
+// 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per row, `outer`
+// rows `row_stride_bytes` apart; boxes of box_inner x box_outer elements.
+dt_status make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  PfnEncodeTiled enc = encode_tiled();
+  if (!enc) return fail(DT_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(DT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %llu x %llu, stride %llu",
+                static_cast<int>(r), (unsigned long long)inner, (unsigned long long)outer,
+                (unsigned long long)row_stride_bytes);
+  return DT_OK;
+}
+
+// ------------------------------------------------------------------------------ derived problem
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Derived {
+  int op;
+  int32_t W, rank, G, Tm, Tn, KB, T, nC;
+  int64_t M, N, K, Ms, Cr, lda, ldb, ldc, ld_gather;
+  bool swizzle, f32;
+  int backend;  // resolved for AG
+  uint64_t timeout_ns;
+  Geom geom;
+  size_t off_ready, off_pieces, off_cnt, off_order, ctl_bytes, off_data, total;
+};
+
+bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+uint64_t default_timeout_ns() {
+  static uint64_t v = [] {
+    const char* e = getenv("DT_WAIT_TIMEOUT_US");
+    long long us = e ? atoll(e) : 0;
+    if (us <= 0) us = 2000000;
+    return static_cast<uint64_t>(us) * 1000ull;
+  }();
+  return v;
+}
+
+dt_status derive(const dt_args* a, int op, Derived* d) {
+  if (!a) return fail(DT_ERR_INVALID, "args is NULL");
+  if (op != DT_OP_AG_GEMM && op != DT_OP_GEMM_RS) return fail(DT_ERR_INVALID, "unknown op %d", op);
+  d->op = op;
+  d->W = a->world_size;
+  if (d->W < 1 || d->W > DT_MAX_WORLD)
+    return fail(DT_ERR_INVALID, "world_size %d outside 1..%d", d->W, DT_MAX_WORLD);
+  d->rank = a->rank;
+  if (op == DT_OP_AG_GEMM && (d->rank < 0 || d->rank >= d->W))
+    return fail(DT_ERR_INVALID, "rank %d outside 0..%d", d->rank, d->W - 1);
+  if (op == DT_OP_GEMM_RS) d->rank = 0;
+  d->M = a->m;
+  d->N = a->n;
+  d->K = a->k;
+  if (d->M < 0 || d->N < 0 || d->K < 0) return fail(DT_ERR_INVALID, "negative size");
+  if (d->M >= (1ll << 31) || d->N >= (1ll << 31) || d->K >= (1ll << 31))
+    return fail(DT_ERR_UNSUPPORTED, "sizes must be below 2^31");
+  if (d->M % d->W) return fail(DT_ERR_INVALID, "M=%lld is not a multiple of W=%d", (long long)d->M, d->W);
+  if (d->N % 8) return fail(DT_ERR_UNSUPPORTED, "N=%lld must be a multiple of 8", (long long)d->N);
+  if (op == DT_OP_AG_GEMM && d->K % 8)
+    return fail(DT_ERR_UNSUPPORTED, "AllGather K=%lld must be a multiple of 8", (long long)d->K);
+  d->Cr = a->chunk_rows;
+  if (d->Cr < 1) return fail(DT_ERR_INVALID, "chunk_rows must be >= 1");
+  d->lda = a->lda ? a->lda : d->K;
+  d->ldb = a->ldb ? a->ldb : d->N;
+  d->ldc = a->ldc ? a->ldc : d->N;
+  if (d->lda < d->K || d->ldb < d->N || d->ldc < d->N)
+    return fail(DT_ERR_INVALID, "leading dimension smaller than the row length");
+  if ((d->lda % 8) || (d->ldb % 8) || (d->ldc % 8))
+    return fail(DT_ERR_INVALID, "leading dimensions must be multiples of 8 elements (16-byte rows)");
+  if ((a->tile_m != 0 && a->tile_m != kBM) || (a->tile_n != 0 && a->tile_n != kBN))
+    return fail(DT_ERR_UNSUPPORTED, "tiles other than %dx%d are not built", kBM, kBN);
+  if (a->out_dtype != DT_BF16 && a->out_dtype != DT_F32)
+    return fail(DT_ERR_INVALID, "unknown out_dtype %d", a->out_dtype);
+  d->f32 = a->out_dtype == DT_F32;
+  d->swizzle = a->swizzle != 0;
+  d->G = a->group > 0 ? a->group : 8;
+  d->timeout_ns = a->timeout_us > 0 ? static_cast<uint64_t>(a->timeout_us) * 1000ull
+                                    : default_timeout_ns();
+  d->Ms = d->M / d->W;
+  d->geom = make_geom(d->W, d->rank, d->M, d->N, d->Cr, kBM, kBN, d->G, d->swizzle ? 1 : 0);
+  d->nC = d->geom.nC;
+  d->Tm = d->geom.Tm;
+  d->Tn = d->geom.Tn;
+  d->KB = static_cast<int32_t>(cdiv64(d->K, kBK));
+  const int64_t T64 = (op == DT_OP_AG_GEMM ? 1 : d->W) * static_cast<int64_t>(d->Tm) * d->Tn;
+  if (T64 >= (1ll << 31)) return fail(DT_ERR_UNSUPPORTED, "too many tiles");
+  d->T = static_cast<int32_t>(T64);
+  if (static_cast<int64_t>(d->W) * d->nC >= (1ll << 24))
+    return fail(DT_ERR_UNSUPPORTED, "too many chunks; raise chunk_rows");
+  d->ld_gather = d->K;  // K % 8 == 0: 16-byte rows, back to back
+  int be = a->backend;
+  if (be < DT_XFER_AUTO || be > DT_XFER_LDST) return fail(DT_ERR_INVALID, "unknown backend %d", be);
+  if (op == DT_OP_AG_GEMM && be == DT_XFER_AUTO) {
+    // large chunks amortise the copy engine's per-transfer launch cost; smaller ones move
+    // on in-kernel TMA bulk copies
+    const int64_t chunk_bytes = std::min<int64_t>(d->Cr, d->Ms) * d->K * 2;
+    be = chunk_bytes >= (8ll << 20) ? DT_XFER_COPY_ENGINE : DT_XFER_TMA;
+  }
+  d->backend = be;
+  // workspace layout: error word | control arrays | tile order || data
+  const size_t nchunks = static_cast<size_t>(d->W) * d->nC;
+  size_t off = 256;
+  d->off_ready = d->off_pieces = d->off_cnt = 0;
+  if (op == DT_OP_AG_GEMM) {
+    d->off_ready = off;
+    off = align_up(off + 4 * nchunks, 256);
+    d->off_pieces = off;
+    off = align_up(off + 4 * nchunks, 256);
+  } else {
+    d->off_cnt = off;
+    off = align_up(off + 4 * nchunks * d->Tn, 256);
+  }
+  d->off_order = off;
+  off = align_up(off + 4 * static_cast<size_t>(d->T), 1024);
+  d->ctl_bytes = off;
+  d->off_data = off;
+  if (op == DT_OP_AG_GEMM)
+    d->total = off + static_cast<size_t>(d->M) * d->ld_gather * 2;
+  else
+    d->total = off + static_cast<size_t>(d->W) * d->W * d->Ms * d->N * 4;
+  return DT_OK;
+}
+
+// ------------------------------------------------------------------------------ per-workspace state
+struct LayoutKey {
+  int op, W, rank, G, swz;
+  long long M, N, K, Cr;
+  bool operator==(const LayoutKey& o) const {
+    return op == o.op && W == o.W && rank == o.rank && G == o.G && swz == o.swz && M == o.M &&
+           N == o.N && K == o.K && Cr == o.Cr;
+  }
+};
+
+struct WsState {
+  LayoutKey key;
+  uint32_t epoch;
+  bool plan_ready;
+};
+
+std::mutex g_mu;
+std::map<const void*, WsState> g_ws;
+
+// host-side fault injection for failure-detection tests: transfer step whose copy and flag
+// write the next copy-engine AllGather call leaves out (-1: none)
+int32_t g_drop_transfer = -1;
+
+LayoutKey key_of(const Derived& d) {
+  return LayoutKey{d.op, d.W, d.rank, d.G, d.swizzle ? 1 : 0, d.M, d.N, d.K, d.Cr};
+}
+
+// Bring the workspace to this call: clear its control block if it is new or was laid out
+// for another problem, bump the epoch, and write the tile order if it is not resident.
+dt_status prepare_workspace(const Derived& d, void* ws, cudaStream_t stream, uint32_t* epoch);
+
+// ------------------------------------------------------------------------------ device info
+struct DevCtx {
+  int sms = 0;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+  std::vector<cudaEvent_t> chunk_events;
+};
+std::mutex g_dev_mu;
+std::map<int, DevCtx> g_dev;
+
+dt_status dev_ctx(DevCtx** out) {
+  int dev = 0;
+  DT_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevCtx& c = g_dev[dev];
+  if (c.sms == 0) {
+    DT_CUDA(cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev));
+    DT_CUDA(cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking));
+    DT_CUDA(cudaEventCreateWithFlags(&c.ev_start, cudaEventDisableTiming));
+    DT_CUDA(cudaEventCreateWithFlags(&c.ev_done, cudaEventDisableTiming));
+  }
+  *out = &c;
+  return DT_OK;
+}
+
+// ------------------------------------------------------------------------------ small kernels
+__global__ void plan_kernel(Geom g, int op, int32_t* order, int32_t T) {
+  const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  int64_t pos;
+  if (op == DT_OP_AG_GEMM) {
+    pos = ag_position(g, t / g.Tn, t % g.Tn);
+  } else {
+    const int32_t per_q = g.Tm * g.Tn;
+    const int32_t q = t / per_q;
+    const int32_t rem = t - q * per_q;
+    pos = rs_position(g, q, rem / g.Tn, rem % g.Tn);
+  }
+  if (pos >= 0 && pos < T) order[pos] = t;
+}
+
+__global__ void zero_rows_kernel(uint8_t* dst, int64_t rows, int64_t row_bytes, int64_t ld_bytes) {
+  const int64_t nv = row_bytes / 16;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < rows * nv;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = e / nv, v = e - r * nv;
+    reinterpret_cast<uint4*>(dst + r * ld_bytes)[v] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// out_s = sum over q (in order) of the fp32 partial slots recv[s][q]
+__global__ void reduce_slots_kernel(const float* recv, int32_t W, int64_t Ms, int64_t N, int32_t s,
+                                    void* out, int64_t ldc, int f32) {
+  const int64_t nv = N / 4;
+  const size_t slot = static_cast<size_t>(Ms) * N;
+  const float* base = recv + static_cast<size_t>(s) * W * slot;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < Ms * nv;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = e / nv, v = e - r * nv;
+    const float* src = base + r * N + v * 4;
+    float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
+    for (int32_t q = 1; q < W; ++q) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(src + q * slot));
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
+    }
+    if (f32) {
+      reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + r * ldc)[v] = acc;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 w;
+      w.x = *reinterpret_cast<uint32_t*>(&lo);
+      w.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + r * ldc)[v] = w;
+    }
+  }
+}
+
+dt_status launch_zero(void* dst, int64_t rows, int64_t row_bytes, int64_t ld_bytes,
+                      cudaStream_t stream) {
+  if (rows <= 0 || row_bytes <= 0) return DT_OK;
+  const int64_t work = rows * (row_bytes / 16);
+  const int grid = static_cast<int>(std::min<int64_t>(cdiv64(work, 256), 4096));
+  zero_rows_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<uint8_t*>(dst), rows, row_bytes,
+                                             ld_bytes);
+  DT_CUDA(cudaGetLastError());
+  return DT_OK;
+}
+
+dt_status prepare_workspace(const Derived& d, void* ws, cudaStream_t stream, uint32_t* epoch) {
+  bool need_plan = false;
+  bool need_clear = false;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_ws.find(ws);
+    const LayoutKey key = key_of(d);
+    if (it == g_ws.end() || !(it->second.key == key)) {
+      g_ws[ws] = WsState{key, 0u, false};
+      it = g_ws.find(ws);
+      need_clear = true;
+    }
+    WsState& st = it->second;
+    if (++st.epoch == 0u) st.epoch = 1u;
+    *epoch = st.epoch;
+    need_plan = !st.plan_ready;
+    st.plan_ready = true;
+  }
+  if (need_clear) DT_CUDA(cudaMemsetAsync(ws, 0, d.ctl_bytes, stream));
+  if (need_plan && d.T > 0) {
+    int32_t* order = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + d.off_order);
+    plan_kernel<<<static_cast<unsigned>(cdiv64(d.T, 256)), 256, 0, stream>>>(d.geom, d.op, order,
+                                                                              d.T);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      g_ws[ws].plan_ready = false;
+      return cuda_fail(e, "plan kernel launch");
+    }
+  }
+  return DT_OK;
+}
+
+dt_status check_ws(const Derived& d, void* ws, size_t bytes) {
+  if (!ws) return fail(DT_ERR_WORKSPACE, "workspace is NULL");
+  if (!is_aligned(ws, 256)) return fail(DT_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (bytes < d.total)
+    return fail(DT_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", bytes, d.total);
+  return DT_OK;
+}
+
+void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
+  memset(&p, 0, sizeof(p));
+  uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+  p.err = reinterpret_cast<uint32_t*>(w);
+  p.order = reinterpret_cast<const int32_t*>(w + d.off_order);
+  p.g = d.geom;
+  p.ldc = d.ldc;
+  p.row_lo = 0;
+  p.row_hi = d.M;
+  p.Tm = d.Tm;
+  p.KB = d.KB;
+  p.T = d.T;
+  p.epoch = epoch;
+  p.timeout_ns = d.timeout_ns;
+}
+
+// ------------------------------------------------------------------------------ AllGather
+dt_status ag_common(const void* const* a_shards, const void* b, void* c, void* ws,
+                    size_t ws_bytes, const dt_args* a, Derived* d) {
+  dt_status s = derive(a, DT_OP_AG_GEMM, d);
+  if (s != DT_OK) return s;
+  if (!a_shards) return fail(DT_ERR_INVALID, "a_shards is NULL");
+  if (d->M == 0 || d->N == 0) return DT_OK;
+  for (int i = 0; i < d->W; ++i)
+    if (!a_shards[i] || !is_aligned(a_shards[i], 16))
+      return fail(DT_ERR_INVALID, "shard %d is NULL or not 16-byte aligned", i);
+  if (!b || !is_aligned(b, 16) || !c || !is_aligned(c, 16))
+    return fail(DT_ERR_INVALID, "B and C must be non-NULL and 16-byte aligned");
+  return check_ws(*d, ws, ws_bytes);
+}
+
+// copy chunk (s, j) of shard s into the gather buffer on `st`
+dt_status ce_copy_chunk(const Derived& d, const void* const* a_shards, uint8_t* gather, int32_t s,
+                        int32_t j, cudaStream_t st) {
+  const int64_t r0 = static_cast<int64_t>(j) * d.Cr;
+  const int64_t rows = std::min<int64_t>(d.Cr, d.Ms - r0);
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(a_shards[s]) + r0 * d.lda * 2;
+  uint8_t* dst = gather + (static_cast<int64_t>(s) * d.Ms + r0) * d.ld_gather * 2;
+  if (d.lda == d.K)
+    DT_CUDA(cudaMemcpyAsync(dst, src, static_cast<size_t>(rows * d.K * 2), cudaMemcpyDeviceToDevice, st));
+  else
+    DT_CUDA(cudaMemcpy2DAsync(dst, d.ld_gather * 2, src, d.lda * 2, d.K * 2, rows,
+                              cudaMemcpyDeviceToDevice, st));
+  return DT_OK;
+}
+
+}  // namespace
+
+// ================================================================================ C ABI
+extern "C" {
+
+void dt_args_default(dt_args* a) {
+  if (!a) return;
+  memset(a, 0, sizeof(*a));
+  a->world_size = 1;
+  a->swizzle = 1;
+  a->backend = DT_XFER_AUTO;
+  a->out_dtype = DT_BF16;
+  a->tile_m = kBM;
+  a->tile_n = kBN;
+  a->group = 8;
+  a->chunk_rows = 128;
+}
+
+int dt_version(void) { return 100; }
+
+size_t dt_sizeof_args(void) { return sizeof(dt_args); }
+
+const char* dt_status_string(dt_status s) {
+  switch (s) {
+    case DT_OK: return "DT_OK";
+    case DT_ERR_INVALID: return "DT_ERR_INVALID";
+    case DT_ERR_UNSUPPORTED: return "DT_ERR_UNSUPPORTED";
+    case DT_ERR_TIMEOUT: return "DT_ERR_TIMEOUT";
+    case DT_ERR_CUDA: return "DT_ERR_CUDA";
+    case DT_ERR_WORKSPACE: return "DT_ERR_WORKSPACE";
+  }
+  return "DT_ERR_UNKNOWN";
+}
+
+const char* dt_last_error(void) { return g_last_error.c_str(); }
+
+size_t dt_workspace_size(const dt_args* a, int op) {
+  Derived d;
+  if (derive(a, op, &d) != DT_OK) return 0;
+  return d.total;
+}
+
+dt_status dt_workspace_init(const dt_args* a, int op, void* ws, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = derive(a, op, &d);
+  if (s != DT_OK) return s;
+  s = check_ws(d, ws, ws_bytes);
+  if (s != DT_OK) return s;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_ws.erase(ws);
+  }
+  DT_CUDA(cudaMemsetAsync(ws, 0, d.ctl_bytes, reinterpret_cast<cudaStream_t>(stream)));
+  return DT_OK;
+}
+
+dt_status dt_swizzle_plan(const dt_args* a, int op, int32_t* order, int64_t len) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = derive(a, op, &d);
+  if (s != DT_OK) return s;
+  if (len != d.T) return fail(DT_ERR_INVALID, "len %lld != tile count %d", (long long)len, d.T);
+  if (d.T == 0) return DT_OK;
+  if (!order) return fail(DT_ERR_INVALID, "order is NULL");
+  std::vector<uint8_t> seen(d.T, 0);
+  for (int32_t t = 0; t < d.T; ++t) {
+    int64_t pos;
+    if (op == DT_OP_AG_GEMM) {
+      pos = ag_position(d.geom, t / d.Tn, t % d.Tn);
+    } else {
+      const int32_t per_q = d.Tm * d.Tn;
+      const int32_t q = t / per_q, rem = t - q * per_q;
+      pos = rs_position(d.geom, q, rem / d.Tn, rem % d.Tn);
+    }
+    if (pos < 0 || pos >= d.T || seen[pos]) return fail(DT_ERR_INVALID, "plan is not a bijection");
+    seen[pos] = 1;
+    order[pos] = t;
+  }
+  return DT_OK;
+}
+
+dt_status dt_swizzle_plan_device(const dt_args* a, int op, int32_t* order_dev, int64_t len,
+                                 void* stream) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = derive(a, op, &d);
+  if (s != DT_OK) return s;
+  if (len != d.T) return fail(DT_ERR_INVALID, "len %lld != tile count %d", (long long)len, d.T);
+  if (d.T == 0) return DT_OK;
+  if (!order_dev) return fail(DT_ERR_INVALID, "order is NULL");
+  plan_kernel<<<static_cast<unsigned>(cdiv64(d.T, 256)), 256, 0,
+                reinterpret_cast<cudaStream_t>(stream)>>>(d.geom, op, order_dev, d.T);
+  DT_CUDA(cudaGetLastError());
+  return DT_OK;
+}
+
+dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* ws,
+                     size_t ws_bytes, const dt_args* a, void* stream_) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = ag_common(a_shards, b, c, ws, ws_bytes, a, &d);
+  if (s != DT_OK || d.M == 0 || d.N == 0) return s;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (d.K == 0) return launch_zero(c, d.M, d.N * (d.f32 ? 4 : 2), d.ldc * (d.f32 ? 4 : 2), stream);
+  DevCtx* dev = nullptr;
+  if ((s = dev_ctx(&dev)) != DT_OK) return s;
+  uint32_t epoch = 0;
+  if ((s = prepare_workspace(d, ws, stream, &epoch)) != DT_OK) return s;
+
+  uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+  uint8_t* gather = w + d.off_data;
+  KParams p;
+  fill_common(p, d, ws, epoch);
+  for (int i = 0; i < d.W; ++i) p.shard[i] = reinterpret_cast<const uint8_t*>(a_shards[i]);
+  p.out[0] = c;
+  p.gather = gather;
+  p.ready = reinterpret_cast<uint32_t*>(w + d.off_ready);
+  p.pieces_done = reinterpret_cast<uint32_t*>(w + d.off_pieces);
+  p.lda_src = d.lda;
+  p.ld_gather = d.ld_gather;
+  p.wait_flags = 1;
+  p.row_bytes = d.K * 2;
+  if (p.row_bytes <= kCopyBuf) {
+    p.rows_per_piece = static_cast<int32_t>(kCopyBuf / p.row_bytes);
+    p.segs_per_row = 1;
+  } else {
+    p.rows_per_piece = 0;
+    p.segs_per_row = static_cast<int32_t>(cdiv64(p.row_bytes, kCopyBuf));
+  }
+  auto pieces = [&](int64_t rows) -> int32_t {
+    return p.rows_per_piece > 0 ? static_cast<int32_t>(cdiv64(rows, p.rows_per_piece))
+                                : static_cast<int32_t>(rows * p.segs_per_row);
+  };
+  p.pieces_full = pieces(std::min<int64_t>(d.Cr, d.Ms));
+  p.pieces_last = pieces(d.Ms - static_cast<int64_t>(d.nC - 1) * d.Cr);
+  p.src_rows_contig = d.lda == d.K ? 1 : 0;
+  if ((s = make_tmap(&p.tmA[0], gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
+  if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
+
+  const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
+  const int grid = static_cast<int>(std::min<int64_t>(d.T, sms));
+  if (d.backend == DT_XFER_COPY_ENGINE) {
+    PfnWriteValue32 wv = write_value32();
+    if (!wv) return fail(DT_ERR_CUDA, "cuStreamWriteValue32 entry point unavailable");
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DT_CUDA(cudaEventRecord(dev->ev_start, stream));
+    DT_CUDA(cudaStreamWaitEvent(dev->side, dev->ev_start, 0));
+    const int32_t nchunks = d.W * d.nC;
+    const int32_t drop = g_drop_transfer;
+    g_drop_transfer = -1;
+    bool launched = false;
+    for (int32_t tc = 0; tc < nchunks; ++tc) {
+      if (tc == d.nC && !launched) {  // own chunks are queued; start the GEMM
+        cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
+        launched = true;
+      }
+      int32_t cs, cj;
+      ag_transfer_chunk(d.geom, tc, cs, cj);
+      if (tc == drop) continue;  // the message never arrives: its consumers time out
+      if ((s = ce_copy_chunk(d, a_shards, gather, cs, cj, dev->side)) != DT_OK) return s;
+      const CUdeviceptr flag =
+          reinterpret_cast<CUdeviceptr>(p.ready + (static_cast<int64_t>(cs) * d.nC + cj));
+      const CUresult r = wv(reinterpret_cast<CUstream>(dev->side), flag, epoch, 0);
+      if (r != CUDA_SUCCESS) return fail(DT_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)r);
+    }
+    if (!launched) {
+      cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
+    }
+    DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
+    DT_CUDA(cudaStreamWaitEvent(stream, dev->ev_done, 0));
+    return DT_OK;
+  }
+  const int copy = d.backend == DT_XFER_TMA ? kCopyTma : kCopyLdst;
+  cudaError_t e = launch_ag_kernel(p, copy, d.f32, grid, true, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
+  return DT_OK;
+}
+
+dt_status dt_ag_gemm_kernel_overlap(const void* const* a_shards, const void* b, void* c,
+                                    void* ws, size_t ws_bytes, const dt_args* a, void* stream_) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = ag_common(a_shards, b, c, ws, ws_bytes, a, &d);
+  if (s != DT_OK || d.M == 0 || d.N == 0) return s;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (d.K == 0) return launch_zero(c, d.M, d.N * (d.f32 ? 4 : 2), d.ldc * (d.f32 ? 4 : 2), stream);
+  DevCtx* dev = nullptr;
+  if ((s = dev_ctx(&dev)) != DT_OK) return s;
+  uint8_t* gather = reinterpret_cast<uint8_t*>(ws) + d.off_data;
+  KParams p;
+  fill_common(p, d, ws, 0);
+  p.out[0] = c;
+  p.plain = 1;
+  p.wait_flags = 0;
+  if ((s = make_tmap(&p.tmA[0], gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
+  if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
+  const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
+  const int32_t nchunks = d.W * d.nC;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  while (static_cast<int32_t>(dev->chunk_events.size()) < nchunks) {
+    cudaEvent_t ev;
+    DT_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    dev->chunk_events.push_back(ev);
+  }
+  DT_CUDA(cudaEventRecord(dev->ev_start, stream));
+  DT_CUDA(cudaStreamWaitEvent(dev->side, dev->ev_start, 0));
+  for (int32_t tc = 0; tc < nchunks; ++tc) {
+    int32_t cs, cj;
+    ag_transfer_chunk(d.geom, tc, cs, cj);
+    if ((s = ce_copy_chunk(d, a_shards, gather, cs, cj, dev->side)) != DT_OK) return s;
+    DT_CUDA(cudaEventRecord(dev->chunk_events[tc], dev->side));
+    DT_CUDA(cudaStreamWaitEvent(stream, dev->chunk_events[tc], 0));
+    // one launch of the same GEMM over this chunk's rows
+    const int64_t lo = static_cast<int64_t>(cs) * d.Ms + static_cast<int64_t>(cj) * d.Cr;
+    const int64_t hi = static_cast<int64_t>(cs) * d.Ms + std::min<int64_t>((cj + 1) * d.Cr, d.Ms);
+    p.row_lo = lo;
+    p.row_hi = hi;
+    p.Tm = static_cast<int32_t>(cdiv64(hi - lo, kBM));
+    p.T = p.Tm * d.Tn;
+    const int grid = std::min(p.T, sms);
+    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "per-chunk GEMM launch");
+  }
+  DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
+  DT_CUDA(cudaStreamWaitEvent(stream, dev->ev_done, 0));
+  return DT_OK;
+}
+
+// ------------------------------------------------------------------------------ ReduceScatter
+static dt_status rs_common(const void* const* a_, const void* const* b_, void* const* out, void* ws,
+                           size_t ws_bytes, const dt_args* a, Derived* d) {
+  dt_status s = derive(a, DT_OP_GEMM_RS, d);
+  if (s != DT_OK) return s;
+  if (!a_ || !b_ || !out) return fail(DT_ERR_INVALID, "a, b and out arrays must be non-NULL");
+  if (d->M == 0 || d->N == 0) return DT_OK;
+  for (int i = 0; i < d->W; ++i) {
+    if (!a_[i] || !is_aligned(a_[i], 16) || !b_[i] || !is_aligned(b_[i], 16))
+      return fail(DT_ERR_INVALID, "A_%d / B_%d NULL or not 16-byte aligned", i, i);
+    if (!out[i] || !is_aligned(out[i], 16))
+      return fail(DT_ERR_INVALID, "out_%d NULL or not 16-byte aligned", i);
+  }
+  return check_ws(*d, ws, ws_bytes);
+}
+
+static dt_status rs_params(KParams& p, const Derived& d, const void* const* a_,
+                           const void* const* b_, void* const* out, void* ws, uint32_t epoch) {
+  fill_common(p, d, ws, epoch);
+  uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+  p.recv = reinterpret_cast<float*>(w + d.off_data);
+  p.unit_cnt = reinterpret_cast<uint32_t*>(w + d.off_cnt);
+  for (int q = 0; q < d.W; ++q) {
+    p.out[q] = out[q];
+    dt_status s = make_tmap(&p.tmA[q], a_[q], d.K, d.M, d.lda * 2, 64, kBM);
+    if (s != DT_OK) return s;
+    s = make_tmap(&p.tmB[q], b_[q], d.N, d.K, d.ldb * 2, 64, kBK);
+    if (s != DT_OK) return s;
+  }
+  return DT_OK;
+}
+
+dt_status dt_gemm_rs(const void* const* a_, const void* const* b_, void* const* out, void* ws,
+                     size_t ws_bytes, const dt_args* a, void* stream_) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = rs_common(a_, b_, out, ws, ws_bytes, a, &d);
+  if (s != DT_OK || d.M == 0 || d.N == 0) return s;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const int64_t eb = d.f32 ? 4 : 2;
+  if (d.K == 0) {
+    for (int q = 0; q < d.W; ++q)
+      if ((s = launch_zero(out[q], d.Ms, d.N * eb, d.ldc * eb, stream)) != DT_OK) return s;
+    return DT_OK;
+  }
+  DevCtx* dev = nullptr;
+  if ((s = dev_ctx(&dev)) != DT_OK) return s;
+  uint32_t epoch = 0;
+  if ((s = prepare_workspace(d, ws, stream, &epoch)) != DT_OK) return s;
+  KParams p;
+  if ((s = rs_params(p, d, a_, b_, out, ws, epoch)) != DT_OK) return s;
+  const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
+  const int grid = static_cast<int>(std::min<int64_t>(d.T, sms));
+  cudaError_t e = launch_rs_kernel(p, d.f32, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fused GEMM-ReduceScatter launch");
+  return DT_OK;
+}
+
+dt_status dt_gemm_rs_kernel_overlap(const void* const* a_, const void* const* b_, void* const* out,
+                                    void* ws, size_t ws_bytes, const dt_args* a, void* stream_) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = rs_common(a_, b_, out, ws, ws_bytes, a, &d);
+  if (s != DT_OK || d.M == 0 || d.N == 0) return s;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const int64_t eb = d.f32 ? 4 : 2;
+  if (d.K == 0) {
+    for (int q = 0; q < d.W; ++q)
+      if ((s = launch_zero(out[q], d.Ms, d.N * eb, d.ldc * eb, stream)) != DT_OK) return s;
+    return DT_OK;
+  }
+  DevCtx* dev = nullptr;
+  if ((s = dev_ctx(&dev)) != DT_OK) return s;
+  KParams p;
+  if ((s = rs_params(p, d, a_, b_, out, ws, 0)) != DT_OK) return s;
+  p.plain = 1;
+  const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  while (static_cast<int32_t>(dev->chunk_events.size()) < d.W) {
+    cudaEvent_t ev;
+    DT_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    dev->chunk_events.push_back(ev);
+  }
+  const float* recv = p.recv;
+  for (int32_t st = 0; st < d.W; ++st) {
+    // one GEMM launch for destination block st (all W sources), fp32 partials only
+    p.row_lo = static_cast<int64_t>(st) * d.Ms;
+    p.row_hi = p.row_lo + d.Ms;
+    p.Tm = static_cast<int32_t>(cdiv64(d.Ms, kBM));
+    p.T = d.W * p.Tm * d.Tn;
+    const int grid = std::min(p.T, sms);
+    cudaError_t e = launch_rs_kernel(p, d.f32, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "per-destination GEMM launch");
+    DT_CUDA(cudaEventRecord(dev->chunk_events[st], stream));
+    DT_CUDA(cudaStreamWaitEvent(dev->side, dev->chunk_events[st], 0));
+    // the reduction of block st runs on the second stream
+    const int64_t work = d.Ms * (d.N / 4);
+    const int rgrid = static_cast<int>(std::min<int64_t>(cdiv64(work, 256), 2 * sms));
+    reduce_slots_kernel<<<rgrid, 256, 0, dev->side>>>(recv, d.W, d.Ms, d.N, st, out[st], d.ldc,
+                                                      d.f32 ? 1 : 0);
+    DT_CUDA(cudaGetLastError());
+  }
+  DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
+  DT_CUDA(cudaStreamWaitEvent(stream, dev->ev_done, 0));
+  return DT_OK;
+}
+
+dt_status dt_debug_drop_transfer(int32_t step) {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  g_drop_transfer = step;
+  return DT_OK;
+}
+
+dt_status dt_check(void* ws, void* stream_, uint32_t* info) {
+  g_last_error.clear();
+  if (!ws) return fail(DT_ERR_WORKSPACE, "workspace is NULL");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  DT_CUDA(cudaStreamSynchronize(stream));
+  uint32_t h[4] = {0, 0, 0, 0};
+  DT_CUDA(cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost));
+  if (info) memcpy(info, h, sizeof(h));
+  if (h[0] == kDevOk) return DT_OK;
+  DT_CUDA(cudaMemset(ws, 0, sizeof(h)));
+  if (h[0] == kDevBadTile)
+    return fail(DT_ERR_INVALID, "device: tile id out of range at position %u", h[1]);
+  return fail(DT_ERR_TIMEOUT, "device: bounded wait ran out (code %u, site %u, cta %u, %u)", h[0],
+              h[1], h[2], h[3]);
+}
+
+}  // extern "C"

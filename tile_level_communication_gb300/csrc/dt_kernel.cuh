@@ -1,0 +1,665 @@
+// Persistent, warp-specialised tcgen05 GEMM with the chunk-centric AllGather and
+// ReduceScatter fused in.
+//
+// One CTA per SM, 8 warps:
+//   warp 0      TMA producer: per tile, waits (bounded) for the ready flags of the chunks
+//               the tile's rows live in, then streams A / B k-blocks into a 4-stage ring.
+//   warp 1      MMA issuer (one thread): tcgen05.mma 128x256x16 into one of two TMEM
+//               accumulators; also allocates / frees TMEM.
+//   warps 2-3   chunk transfer workers (AllGather, in-kernel backends): copy chunk pieces
+//               from the rank shards into the gather buffer (TMA bulk or 16-byte ld/st)
+//               and release each chunk's ready flag when its last piece has landed.
+//   warps 4-7   epilogue: TMEM -> registers -> global.  AllGather: bf16 / fp32 C.
+//               ReduceScatter: fp32 partial rows pushed into the destination's slot, then
+//               per (chunk, column tile) unit an arrival count; the last arrival reduces
+//               the W slots in rank order 0..W-1.
+//
+// Sources: AutoOverlap page sections 4-5 (chunks, per-chunk waits inserted before the
+// consuming tile, copy engine / TMA / ld-st lowerings with global-memory signals);
+// Triton-distributed talk (notify / wait pairs, pull for AllGather, push for
+// ReduceScatter); DITRON page section 3.2 (rank-aware tile order, see dt_plan.cuh).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "dt_plan.cuh"
+#include "dt_ptx.cuh"
+
+namespace dt {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
+constexpr int kAStage = kBM * kBK * 2;   // 16 KB: 128 rows x 64 bf16, 128-byte swizzle
+constexpr int kBSlab = kBK * 64 * 2;     // 8 KB: 64 k-rows x 64 bf16 columns
+constexpr int kBStage = 4 * kBSlab;      // 32 KB
+constexpr int kCopyBuf = 16384;          // TMA bulk copy staging, two buffers
+constexpr int kTmemCols = 512;           // two 128x256 fp32 accumulators
+constexpr int kMaxW = 16;
+constexpr int kReadyBitsWords = 128;     // producer's cache of seen chunk flags (4096)
+constexpr int kMiscBytes = 1024;
+
+enum CopyMode : int { kCopyNone = 0, kCopyTma = 1, kCopyLdst = 2 };
+
+enum DevCode : uint32_t {
+  kDevOk = 0,
+  kDevTimeoutFlag = 1,   // a chunk's ready flag did not flip in time
+  kDevTimeoutPipe = 2,   // a pipeline mbarrier did not complete in time
+  kDevBadTile = 3,       // a tile id from the plan was out of range (tile skipped)
+};
+
+__host__ __device__ constexpr int kernel_smem_bytes(int copy_mode) {
+  return 1024 + kStages * (kAStage + kBStage) + (copy_mode == kCopyTma ? 2 * kCopyBuf : 0) +
+         kMiscBytes;
+}
+
+struct KParams {
+  CUtensorMap tmA[kMaxW];  // AG: [0] = gather buffer; RS: A_q
+  CUtensorMap tmB[kMaxW];  // AG: [0] = B; RS: B_q
+  const uint8_t* shard[kMaxW];
+  void* out[kMaxW];        // AG: out[0] = C; RS: out[s]
+  uint8_t* gather;
+  float* recv;             // RS: W x W x Ms x N fp32 partial slots, [dest][src]
+  uint32_t* ready;         // AG: per chunk, = epoch once landed
+  uint32_t* pieces_done;   // AG: per chunk piece counter (back to 0 after the chunk)
+  uint32_t* unit_cnt;      // RS: per (chunk, column tile) arrival counter (back to 0)
+  const int32_t* order;    // tile order written by the plan kernel
+  uint32_t* err;           // 4 words: code, site, detail0, detail1
+  Geom g;
+  int64_t lda_src;         // AG: elements between shard rows
+  int64_t ld_gather;       // AG: elements between gather rows
+  int64_t ldc;
+  int64_t row_lo, row_hi;  // rows handled: [0, M) fused; one window in the baselines
+  int32_t Tm, KB, T;       // m-tiles in the window, k-blocks, tiles in the launch
+  int32_t plain;           // 1: identity order, no flags, no arrival counting
+  int32_t wait_flags;      // AG: the producer waits on ready flags
+  uint32_t epoch;
+  uint64_t timeout_ns;
+  // in-kernel chunk transfer (AG)
+  int64_t row_bytes;       // K * 2
+  int32_t rows_per_piece;  // > 0: whole rows per piece; 0: a row is split in segments
+  int32_t segs_per_row;
+  int32_t pieces_full;     // pieces of a chunk with Cr rows
+  int32_t pieces_last;     // pieces of the last chunk of a rank
+  int32_t src_rows_contig; // shard rows are back to back (lda == K)
+};
+
+struct SmemLayout {
+  uint8_t* a;
+  uint8_t* b;
+  uint8_t* copy;
+  uint64_t* bars;
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+  volatile int* unit_flag;
+  volatile int* vote;      // [2][4]
+  uint32_t* ready_bits;
+  __device__ uint32_t full(int s) const { return smem_u32(bars + s); }
+  __device__ uint32_t empty(int s) const { return smem_u32(bars + kStages + s); }
+  __device__ uint32_t tfull(int a) const { return smem_u32(bars + 2 * kStages + a); }
+  __device__ uint32_t tempty(int a) const { return smem_u32(bars + 2 * kStages + 2 + a); }
+  __device__ uint32_t copyb(int b) const { return smem_u32(bars + 2 * kStages + 4 + b); }
+  __device__ uint32_t fin() const { return smem_u32(bars + 2 * kStages + 6); }
+};
+
+__device__ __forceinline__ void raise_error(const KParams& p, uint32_t code, uint32_t site,
+                                            uint32_t d0, uint32_t d1) {
+  if (atomicCAS(p.err, 0u, code) == 0u) {
+    p.err[1] = site;
+    p.err[2] = d0;
+    p.err[3] = d1;
+    __threadfence();
+  }
+}
+
+// Bounded wait on an mbarrier phase.  On timeout records the error, raises the CTA's abort
+// flag and returns false; returns false at once when another role has aborted.
+static __device__ __noinline__ bool wait_bar(const KParams& p, const SmemLayout& L, uint32_t bar,
+                                      uint32_t parity, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0u) {
+      if (*L.abort_flag) return false;
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        raise_error(p, kDevTimeoutPipe, site, blockIdx.x, parity);
+        *L.abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded acquire-poll of a chunk's ready flag.
+static __device__ __noinline__ bool wait_flag(const KParams& p, const SmemLayout& L, int32_t c) {
+  const uint32_t* f = p.ready + c;
+  if (ld_acquire_gpu(f) == p.epoch) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(it < 64 ? 32 : 256);
+    if (ld_acquire_gpu(f) == p.epoch) return true;
+    if ((it & 7u) == 0u) {
+      if (*L.abort_flag) return false;
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        raise_error(p, kDevTimeoutFlag, static_cast<uint32_t>(c), blockIdx.x, p.epoch);
+        *L.abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+struct TileInfo {
+  int32_t q, i, n;
+  int64_t row0, row_end, col0;
+  bool valid;
+};
+
+template <bool RS>
+__device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
+  int32_t t = p.plain ? pos : __ldg(p.order + pos);
+  TileInfo ti;
+  ti.valid = (t >= 0 && t < p.T);
+  if (!ti.valid) t = 0;
+  const int32_t per_q = p.Tm * p.g.Tn;
+  ti.q = RS ? t / per_q : 0;
+  const int32_t rem = t - ti.q * per_q;
+  ti.i = rem / p.g.Tn;
+  ti.n = rem - ti.i * p.g.Tn;
+  ti.row0 = p.row_lo + static_cast<int64_t>(ti.i) * kBM;
+  ti.row_end = min64(ti.row0 + kBM, p.row_hi);
+  ti.col0 = static_cast<int64_t>(ti.n) * kBN;
+  return ti;
+}
+
+// ============================================================================ producer
+template <bool RS>
+__device__ void run_producer(const KParams& p, const SmemLayout& L) {
+  uint32_t kit = 0;
+  int64_t last_issue[kStages];
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) last_issue[s] = -1;
+  for (int32_t pos = blockIdx.x; pos < p.T; pos += gridDim.x) {
+    const TileInfo ti = decode_tile<RS>(p, pos);
+    if (!ti.valid) {
+      raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
+      continue;
+    }
+    if (!RS && p.wait_flags) {
+      // consumer_tile_wait: every chunk holding one of this tile's rows must have landed
+      bool ok = true;
+      for (int64_t g = ti.row0; g < ti.row_end && ok;) {
+        int32_t s, j;
+        row_chunk(p.g, g, s, j);
+        const int32_t c = s * p.g.nC + j;
+        const bool cached =
+            c < kReadyBitsWords * 32 && ((L.ready_bits[c >> 5] >> (c & 31)) & 1u);
+        if (!cached) {
+          ok = wait_flag(p, L, c);
+          if (ok && c < kReadyBitsWords * 32) L.ready_bits[c >> 5] |= 1u << (c & 31);
+        }
+        g = static_cast<int64_t>(s) * p.g.Ms + min64(static_cast<int64_t>(j + 1) * p.g.Cr, p.g.Ms);
+      }
+      if (!ok) break;
+      // the rows were written by other agents through the generic proxy (or the copy
+      // engine); the TMA loads below read through the async proxy
+      fence_proxy_async_global();
+    }
+    const CUtensorMap* tA = &p.tmA[RS ? ti.q : 0];
+    const CUtensorMap* tB = &p.tmB[RS ? ti.q : 0];
+    bool ok = true;
+    for (int32_t kb = 0; kb < p.KB; ++kb, ++kit) {
+      const int st = static_cast<int>(kit % kStages);
+      const uint32_t ph = (kit / kStages) & 1u;
+      if (!wait_bar(p, L, L.empty(st), ph ^ 1u, 100 + st)) { ok = false; break; }
+      mbar_expect_tx(L.full(st), kAStage + kBStage);
+      tma_load_2d(smem_u32(L.a + st * kAStage), tA, kb * kBK, static_cast<int32_t>(ti.row0),
+                  L.full(st));
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+        tma_load_2d(smem_u32(L.b + st * kBStage + jj * kBSlab), tB,
+                    static_cast<int32_t>(ti.col0) + jj * 64, kb * kBK, L.full(st));
+      last_issue[st] = kit;
+    }
+    if (!ok) break;
+  }
+  if (*L.abort_flag) {
+    // let every TMA load this thread issued land before the CTA can exit
+    for (int s = 0; s < kStages; ++s) {
+      if (last_issue[s] < 0) continue;
+      const uint32_t ph = static_cast<uint32_t>(last_issue[s] / kStages) & 1u;
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(L.full(s), ph) && globaltimer_ns() - t0 < p.timeout_ns) {
+      }
+    }
+  }
+}
+
+// ============================================================================ MMA issuer
+template <bool RS>
+__device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_base) {
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, /*B MN-major*/ 1);
+  uint32_t kit = 0;
+  int32_t tl = 0;
+  bool issued = false;
+  for (int32_t pos = blockIdx.x; pos < p.T; pos += gridDim.x) {
+    const TileInfo ti = decode_tile<RS>(p, pos);
+    if (!ti.valid) continue;
+    const int acc = tl & 1;
+    const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
+    if (!wait_bar(p, L, L.tempty(acc), aph ^ 1u, 200 + acc)) break;
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+    bool ok = true;
+    for (int32_t kb = 0; kb < p.KB; ++kb, ++kit) {
+      const int st = static_cast<int>(kit % kStages);
+      const uint32_t ph = (kit / kStages) & 1u;
+      if (!wait_bar(p, L, L.full(st), ph, 300 + st)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(L.a + st * kAStage);
+      const uint32_t b0 = smem_u32(L.b + st * kBStage);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        // A: K-major rows of 128 B, 8-row groups 1024 B apart; +32 B per 16 k
+        const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+        // B: MN-major; 64-column slabs 8 KB apart (LBO), 8 k-row groups 1 KB apart (SBO)
+        const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kBSlab, 1024);
+        umma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+      }
+      umma_commit(L.empty(st));  // frees the stage once these MMAs have read it
+      issued = true;
+    }
+    if (!ok) break;
+    umma_commit(L.tfull(acc));   // accumulator ready for the epilogue
+    ++tl;
+  }
+  if (*L.abort_flag && issued) {
+    umma_commit(L.fin());
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(L.fin(), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
+    }
+  }
+}
+
+// ============================================================================ epilogue
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <bool F32>
+__device__ __forceinline__ void store_row32(void* out, int64_t ldc, int64_t row, int64_t c0,
+                                            int64_t N, const uint32_t (&v)[32]) {
+  if (F32) {
+    float* dst = reinterpret_cast<float*>(out) + row * ldc + c0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (c0 + u * 8 < N) {
+        reinterpret_cast<float4*>(dst + u * 8)[0] =
+            make_float4(__uint_as_float(v[u * 8 + 0]), __uint_as_float(v[u * 8 + 1]),
+                        __uint_as_float(v[u * 8 + 2]), __uint_as_float(v[u * 8 + 3]));
+        reinterpret_cast<float4*>(dst + u * 8)[1] =
+            make_float4(__uint_as_float(v[u * 8 + 4]), __uint_as_float(v[u * 8 + 5]),
+                        __uint_as_float(v[u * 8 + 6]), __uint_as_float(v[u * 8 + 7]));
+      }
+    }
+  } else {
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out) + row * ldc + c0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (c0 + u * 8 < N) {
+        uint4 w;
+        w.x = pack_bf16x2(v[u * 8 + 0], v[u * 8 + 1]);
+        w.y = pack_bf16x2(v[u * 8 + 2], v[u * 8 + 3]);
+        w.z = pack_bf16x2(v[u * 8 + 4], v[u * 8 + 5]);
+        w.w = pack_bf16x2(v[u * 8 + 6], v[u * 8 + 7]);
+        *reinterpret_cast<uint4*>(dst) = w;
+      }
+      dst += 8;
+    }
+  }
+}
+
+__device__ __forceinline__ float4 ldcg_f4(const float* p) {
+  return __ldcg(reinterpret_cast<const float4*>(p));
+}
+
+// Sum the W partial slots of one unit (rows [lo, hi) of rank s, column tile n) in rank order
+// q = 0..W-1 and store the result rows of out_s.  Runs on the 128 epilogue threads.
+template <bool F32>
+__device__ void reduce_unit(const KParams& p, int32_t s, int64_t lo, int64_t hi, int32_t n,
+                            int et) {
+  const int64_t c0 = static_cast<int64_t>(n) * kBN;
+  const int32_t ncols = static_cast<int32_t>(min64(kBN, p.g.N - c0));
+  const int32_t nv = ncols >> 2;
+  const int32_t nrows = static_cast<int32_t>(hi - lo);
+  const int64_t lr0 = lo - static_cast<int64_t>(s) * p.g.Ms;
+  const size_t slot = static_cast<size_t>(p.g.Ms) * static_cast<size_t>(p.g.N);
+  const float* base = p.recv + static_cast<size_t>(s) * p.g.W * slot +
+                      static_cast<size_t>(lr0) * p.g.N + c0;
+  const int32_t W = p.g.W;
+  for (int32_t e = et; e < nrows * nv; e += 128) {
+    const int32_t r = e / nv;
+    const int32_t v = e - r * nv;
+    const float* src = base + static_cast<size_t>(r) * p.g.N + v * 4;
+    float4 x[kMaxW];
+#pragma unroll
+    for (int q = 0; q < kMaxW; ++q)
+      if (q < W) x[q] = ldcg_f4(src + q * slot);
+    float4 acc = x[0];
+#pragma unroll
+    for (int q = 1; q < kMaxW; ++q) {
+      if (q < W) {
+        acc.x += x[q].x;
+        acc.y += x[q].y;
+        acc.z += x[q].z;
+        acc.w += x[q].w;
+      }
+    }
+    const int64_t row = lr0 + r;
+    if (F32) {
+      float* dst = reinterpret_cast<float*>(p.out[s]) + row * p.ldc + c0 + v * 4;
+      *reinterpret_cast<float4*>(dst) = acc;
+    } else {
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out[s]) + row * p.ldc + c0 + v * 4;
+      uint2 w;
+      w.x = pack_bf16x2(__float_as_uint(acc.x), __float_as_uint(acc.y));
+      w.y = pack_bf16x2(__float_as_uint(acc.z), __float_as_uint(acc.w));
+      *reinterpret_cast<uint2*>(dst) = w;
+    }
+  }
+}
+
+template <bool RS, bool F32>
+__device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tmem_base,
+                             int warp, int lane) {
+  constexpr bool kStoreF32 = RS || F32;  // ReduceScatter partial slots are fp32
+  const int qd = warp - 4;  // TMEM lane quadrant this warp may read
+  const int et = threadIdx.x - 128;
+  int32_t tl = 0;
+  for (int32_t pos = blockIdx.x; pos < p.T; pos += gridDim.x) {
+    const TileInfo ti = decode_tile<RS>(p, pos);
+    if (!ti.valid) continue;
+    const int acc = tl & 1;
+    const uint32_t ph = (static_cast<uint32_t>(tl) >> 1) & 1u;
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(p, L, L.tfull(acc), ph, 400 + acc) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (RS && !p.plain) {
+      // all four epilogue warps agree before they meet at the named barriers below
+      if (lane == 0) L.vote[(tl & 1) * 4 + qd] = ok;
+      named_bar_sync(1, 128);
+      ok = L.vote[(tl & 1) * 4 + 0] & L.vote[(tl & 1) * 4 + 1] & L.vote[(tl & 1) * 4 + 2] &
+           L.vote[(tl & 1) * 4 + 3];
+    }
+    if (!ok) break;
+    tc_fence_after();
+    const int64_t row = ti.row0 + qd * 32 + lane;
+    const bool row_ok = row < ti.row_end;
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) +
+                           static_cast<uint32_t>(acc * kBN);
+    void* dst_base;
+    int64_t dst_row, dst_ld;
+    if (RS) {
+      const int32_t s = row_ok ? static_cast<int32_t>(row / p.g.Ms) : 0;
+      const size_t slot = static_cast<size_t>(s) * p.g.W + ti.q;
+      dst_base = p.recv + slot * static_cast<size_t>(p.g.Ms) * p.g.N;
+      dst_row = row - static_cast<int64_t>(s) * p.g.Ms;
+      dst_ld = p.g.N;
+    } else {
+      dst_base = p.out[0];
+      dst_row = row;
+      dst_ld = p.ldc;
+    }
+#pragma unroll 1
+    for (int cb = 0; cb < kBN / 32; ++cb) {
+      const int64_t c0 = ti.col0 + cb * 32;
+      if (c0 >= p.g.N) break;
+      uint32_t v[32];
+      tmem_ld32(tbase + cb * 32, v);
+      if (row_ok) store_row32<kStoreF32>(dst_base, dst_ld, dst_row, c0, p.g.N, v);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(L.tempty(acc));
+    ++tl;
+
+    if (RS && !p.plain) {
+      // notify: count this tile's arrival at every unit its rows belong to; the last
+      // arrival of a unit waits for nothing and reduces it
+      __threadfence();
+      named_bar_sync(1, 128);
+      for (int64_t g = ti.row0; g < ti.row_end;) {
+        int32_t s, j;
+        row_chunk(p.g, g, s, j);
+        const int64_t lo = static_cast<int64_t>(s) * p.g.Ms + static_cast<int64_t>(j) * p.g.Cr;
+        const int64_t hi =
+            static_cast<int64_t>(s) * p.g.Ms + min64(static_cast<int64_t>(j + 1) * p.g.Cr, p.g.Ms);
+        if (et == 0) {
+          uint32_t* cnt = p.unit_cnt + (static_cast<int64_t>(s) * p.g.nC + j) * p.g.Tn + ti.n;
+          const uint32_t old = atom_add_acq_rel_gpu(cnt, 1u);
+          const int last = (old + 1u == rs_unit_arrivals(p.g, lo, hi)) ? 1 : 0;
+          if (last) *cnt = 0u;  // every arrival of this call is in: ready for the next call
+          *L.unit_flag = last;
+        }
+        named_bar_sync(1, 128);
+        if (*L.unit_flag) {
+          __threadfence();
+          reduce_unit<F32>(p, s, lo, hi, ti.n, et);
+        }
+        named_bar_sync(1, 128);
+        g = hi;
+      }
+    }
+  }
+}
+
+// ============================================================================ chunk transfer
+__device__ __forceinline__ void signal_piece(const KParams& p, int32_t c, int32_t total) {
+  fence_proxy_async_global();
+  __threadfence();
+  const uint32_t old = atom_add_acq_rel_gpu(p.pieces_done + c, 1u);
+  if (old + 1u == static_cast<uint32_t>(total)) {
+    p.pieces_done[c] = 0u;
+    st_release_gpu(p.ready + c, p.epoch);  // notify: chunk c has landed
+  }
+}
+
+struct Piece {
+  int32_t r0, nr;   // rows of the chunk
+  int64_t boff;     // byte offset inside a row
+  uint32_t nbytes;  // bytes per row copied
+};
+
+__device__ __forceinline__ Piece piece_of(const KParams& p, int32_t pc, int32_t rows_c) {
+  Piece pc_;
+  if (p.rows_per_piece > 0) {
+    pc_.r0 = pc * p.rows_per_piece;
+    pc_.nr = min32(p.rows_per_piece, rows_c - pc_.r0);
+    pc_.boff = 0;
+    pc_.nbytes = static_cast<uint32_t>(p.row_bytes);
+  } else {
+    pc_.r0 = pc / p.segs_per_row;
+    pc_.nr = 1;
+    const int32_t seg = pc - pc_.r0 * p.segs_per_row;
+    pc_.boff = static_cast<int64_t>(seg) * kCopyBuf;
+    pc_.nbytes = static_cast<uint32_t>(min64(kCopyBuf, p.row_bytes - pc_.boff));
+  }
+  return pc_;
+}
+
+// Pieces are numbered along the transfer order (chunk by chunk); worker w takes the pieces
+// whose global number is w modulo the worker count, so every worker starts on the first
+// chunk of the order.
+template <typename Stop, typename F>
+__device__ __forceinline__ void for_each_piece(const KParams& p, int32_t wid, int32_t nw,
+                                               Stop&& stop, F&& f) {
+  const int32_t nchunks = p.g.W * p.g.nC;
+  const int64_t pieces_rank = static_cast<int64_t>(p.g.nC - 1) * p.pieces_full + p.pieces_last;
+  for (int32_t tc = 0; tc < nchunks; ++tc) {
+    if (stop()) return;
+    int32_t s, j;
+    ag_transfer_chunk(p.g, tc, s, j);
+    const int32_t u = tc / p.g.nC;
+    const int32_t rows_c =
+        static_cast<int32_t>(min64(p.g.Cr, p.g.Ms - static_cast<int64_t>(j) * p.g.Cr));
+    const int32_t total = (j == p.g.nC - 1) ? p.pieces_last : p.pieces_full;
+    const int64_t base = static_cast<int64_t>(u) * pieces_rank +
+                         static_cast<int64_t>(j) * p.pieces_full;
+    const int32_t first = static_cast<int32_t>(((wid - base) % nw + nw) % nw);
+    for (int32_t pc = first; pc < total; pc += nw) {
+      if (!f(s, j, s * p.g.nC + j, total, piece_of(p, pc, rows_c))) return;
+    }
+  }
+}
+
+static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L) {
+  const int32_t wid = blockIdx.x, nw = gridDim.x;
+  uint32_t k = 0;
+  int32_t prev_c = -1, prev_total = 0;
+  auto stop = [&]() { return *L.abort_flag != 0; };
+  for_each_piece(p, wid, nw, stop, [&](int32_t s, int32_t j, int32_t c, int32_t total,
+                                       const Piece& pc) -> bool {
+    const int64_t row_in_shard = static_cast<int64_t>(j) * p.g.Cr + pc.r0;
+    const uint8_t* src = p.shard[s] + row_in_shard * p.lda_src * 2 + pc.boff;
+    uint8_t* dst = p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard) * p.ld_gather * 2 +
+                   pc.boff;
+    const int b = static_cast<int>(k & 1u);
+    const uint32_t buf = smem_u32(L.copy + b * kCopyBuf);
+    const uint32_t tot = pc.nbytes * static_cast<uint32_t>(pc.nr);
+    const bool whole = pc.nbytes == static_cast<uint32_t>(p.row_bytes);
+    bulk_wait_read<1>();  // the store that last used this buffer has read it
+    mbar_expect_tx(L.copyb(b), tot);
+    if (p.src_rows_contig || pc.nr == 1) {
+      bulk_g2s(buf, src, tot, L.copyb(b));
+    } else {
+      for (int32_t r = 0; r < pc.nr; ++r)
+        bulk_g2s(buf + r * pc.nbytes, src + static_cast<int64_t>(r) * p.lda_src * 2, pc.nbytes,
+                 L.copyb(b));
+    }
+    if (!wait_bar(p, L, L.copyb(b), (k >> 1) & 1u, 500 + b)) return false;
+    if (whole || pc.nr == 1) {
+      bulk_s2g(dst, buf, tot);  // gather rows are back to back (ld_gather == K)
+    } else {
+      for (int32_t r = 0; r < pc.nr; ++r)
+        bulk_s2g(dst + static_cast<int64_t>(r) * p.ld_gather * 2, buf + r * pc.nbytes, pc.nbytes);
+    }
+    bulk_commit();
+    bulk_wait<1>();  // the previous piece's writes are complete
+    if (prev_c >= 0) signal_piece(p, prev_c, prev_total);
+    prev_c = c;
+    prev_total = total;
+    ++k;
+    return true;
+  });
+  bulk_wait<0>();
+  if (prev_c >= 0 && !*L.abort_flag) signal_piece(p, prev_c, prev_total);
+}
+
+static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int warp, int lane) {
+  const int32_t wid = blockIdx.x * 2 + (warp - 2), nw = gridDim.x * 2;
+  // the whole warp takes the same decision
+  auto stop = [&]() { return __shfl_sync(0xffffffffu, *L.abort_flag, 0) != 0; };
+  for_each_piece(p, wid, nw, stop, [&](int32_t s, int32_t j, int32_t c, int32_t total,
+                                       const Piece& pc) -> bool {
+    const int64_t row_in_shard = static_cast<int64_t>(j) * p.g.Cr + pc.r0;
+    const bool contig = pc.nr == 1 || (p.src_rows_contig && pc.nbytes == p.row_bytes);
+    const int32_t nrow = contig ? 1 : pc.nr;
+    const uint32_t nb = contig ? pc.nbytes * static_cast<uint32_t>(pc.nr) : pc.nbytes;
+    for (int32_t r = 0; r < nrow; ++r) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.shard[s] + (row_in_shard + r) * p.lda_src * 2 + pc.boff);
+      uint4* dst = reinterpret_cast<uint4*>(
+          p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard + r) * p.ld_gather * 2 +
+          pc.boff);
+      const int32_t nvec = static_cast<int32_t>(nb >> 4);
+      for (int32_t v = lane; v < nvec; v += 32 * 4) {
+        uint4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v + u * 32 < nvec) x[u] = __ldg(src + v + u * 32);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v + u * 32 < nvec) dst[v + u * 32] = x[u];
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) signal_piece(p, c, total);
+    __syncwarp();
+    return true;
+  });
+}
+
+// ============================================================================ kernel
+template <bool RS, int COPY, bool F32>
+__global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_constant__ KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  SmemLayout L;
+  L.a = base;
+  L.b = L.a + kStages * kAStage;
+  L.copy = L.b + kStages * kBStage;
+  uint8_t* misc = L.copy + (COPY == kCopyTma ? 2 * kCopyBuf : 0);
+  L.bars = reinterpret_cast<uint64_t*>(misc);  // 16 barriers
+  L.tmem_slot = reinterpret_cast<uint32_t*>(misc + 128);
+  L.abort_flag = reinterpret_cast<volatile int*>(misc + 132);
+  L.unit_flag = reinterpret_cast<volatile int*>(misc + 136);
+  L.vote = reinterpret_cast<volatile int*>(misc + 160);
+  L.ready_bits = reinterpret_cast<uint32_t*>(misc + 256);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < kReadyBitsWords) L.ready_bits[threadIdx.x] = 0u;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(L.full(s), 1);
+      mbar_init(L.empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(L.tfull(a), 1);
+      mbar_init(L.tempty(a), 4);
+      mbar_init(L.copyb(a), 1);
+    }
+    mbar_init(L.fin(), 1);
+    *L.abort_flag = 0;
+    *L.unit_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA[0]);
+    tma_prefetch_desc(&p.tmB[0]);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(L.tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *L.tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) run_producer<RS>(p, L);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<RS>(p, L, tmem_base);
+  } else if (warp < 4) {
+    if (!RS && !p.plain) {
+      if (COPY == kCopyTma && warp == 2 && lane == 0) run_copy_tma(p, L);
+      if (COPY == kCopyLdst) run_copy_ldst(p, L, warp, lane);
+    }
+  } else {
+    run_epilogue<RS, F32>(p, L, tmem_base, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace dt

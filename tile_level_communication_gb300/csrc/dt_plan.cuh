@@ -1,0 +1,173 @@
+// Rank-aware tile order (the distributed swizzle) as stateless position functions that run
+// on the host and on the device.
+//
+// DITRON page, section 3.2 (论文 §3.2, Fig. 3): swizzle_func maps the original tile id to a
+// new one with a rank-aware offset; rank r starts at r mod world_size.  Gather mode (AllGather
+// GEMM) treats local HBM as a cache of remote memory: own rows first, remote chunks in the
+// order they are fetched.  Scatter mode (GEMM ReduceScatter) computes first the rows that go
+// to the farthest rank; here rank q sends to q+1 first and keeps its own block for last.
+// Triton-distributed talk, "不完全なブロックスケジューリング": a tile that straddles ranks runs
+// after the data it waits for (AllGather) or before the tiles other ranks do not need
+// (ReduceScatter).  AutoOverlap page, section 5.4 / Fig. 6: across chunks the schedule follows
+// chunk arrival, inside a chunk bands of G m-tiles are swept column by column for locality.
+//
+// Definition (the same one the oracle sorts by):
+//   chunk (s, j) = rows [s*Ms + j*Cr, s*Ms + min((j+1)*Cr, Ms)),  nC = ceil(Ms / Cr)
+//   AG: pos(s, j) = ((s - r) mod W) * nC + j;  key(i) = max pos of the chunks m-tile i reads;
+//       order = sort (i, n) by (key(i), band(i), n, i)
+//   RS: dpos_q(s) = (s - q - 1) mod W;  key(q, i) = min over written chunks of dpos*nC + j;
+//       order = sort (q, i, n) by (key, q, band, n, i)
+// Evaluation here does not sort.  Along the m-tiles rotated to start at the first m-tile of
+// the own rank (AG) or of rank q+1 (RS) the key never decreases, so the key of an m-tile is
+// read off one row of it, and the number of m-tiles with a smaller key is a binary search.
+// A tile's position is then a closed expression of those counts.
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define DT_HD __host__ __device__ __forceinline__
+#else
+#define DT_HD inline
+#endif
+
+namespace dt {
+
+struct Geom {
+  int64_t M, N, Ms, Cr;
+  int32_t W, rank, BM, BN, nC, Tm, Tn, G, swizzle;
+};
+
+DT_HD int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+DT_HD int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+DT_HD int32_t min32(int32_t a, int32_t b) { return a < b ? a : b; }
+
+DT_HD Geom make_geom(int32_t W, int32_t rank, int64_t M, int64_t N, int64_t Cr, int32_t BM,
+                     int32_t BN, int32_t G, int32_t swizzle) {
+  Geom g;
+  g.M = M;
+  g.N = N;
+  g.W = W;
+  g.rank = rank;
+  g.Ms = M / W;
+  g.Cr = Cr;
+  g.BM = BM;
+  g.BN = BN;
+  g.G = G;
+  g.swizzle = swizzle;
+  g.nC = g.Ms > 0 ? static_cast<int32_t>(cdiv64(g.Ms, Cr)) : 0;
+  g.Tm = static_cast<int32_t>(cdiv64(M, BM));
+  g.Tn = static_cast<int32_t>(cdiv64(N, BN));
+  return g;
+}
+
+// rank s and chunk j of global row `row`
+DT_HD void row_chunk(const Geom& g, int64_t row, int32_t& s, int32_t& j) {
+  s = static_cast<int32_t>(row / g.Ms);
+  j = static_cast<int32_t>((row - static_cast<int64_t>(s) * g.Ms) / g.Cr);
+}
+
+// Offset of tile (u, n) inside its key group [ug, ue) of rotated m-tile indices: bands of
+// G m-tiles, each swept column by column.
+DT_HD int64_t band_offset(int32_t ug, int32_t ue, int32_t u, int32_t n, int32_t Tn, int32_t G) {
+  const int32_t b = (u - ug) / G;
+  const int32_t bs = ug + b * G;
+  const int32_t bsz = min32(G, ue - bs);
+  return static_cast<int64_t>(b) * G * Tn + static_cast<int64_t>(n) * bsz + (u - bs);
+}
+
+// ------------------------------------------------------------------ gather mode (AllGather)
+DT_HD int32_t ag_chunk_pos(const Geom& g, int32_t s, int32_t j) {
+  return ((s - g.rank + g.W) % g.W) * g.nC + j;
+}
+// first m-tile that lies wholly at or after the own rank's first row
+DT_HD int32_t ag_rot0(const Geom& g) {
+  return static_cast<int32_t>(cdiv64(static_cast<int64_t>(g.rank) * g.Ms, g.BM) % g.Tm);
+}
+// key of the m-tile at rotated index u
+DT_HD int32_t ag_key(const Geom& g, int32_t rot0, int32_t u) {
+  const int32_t i = (rot0 + u) % g.Tm;
+  const int64_t first = static_cast<int64_t>(i) * g.BM;
+  const int64_t last = min64(first + g.BM, g.M) - 1;
+  const int64_t own0 = static_cast<int64_t>(g.rank) * g.Ms;
+  // reads the last chunk of rank r-1: the latest chunk of the gather
+  if (g.rank > 0 && first < own0 && last >= own0) return g.W * g.nC - 1;
+  int32_t s, j;
+  row_chunk(g, last, s, j);
+  return ag_chunk_pos(g, s, j);
+}
+DT_HD int32_t ag_count_below(const Geom& g, int32_t rot0, int32_t k) {
+  int32_t lo = 0, hi = g.Tm;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (ag_key(g, rot0, mid) < k) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+// execution position of AllGather tile (i, n)
+DT_HD int64_t ag_position(const Geom& g, int32_t i, int32_t n) {
+  if (!g.swizzle) return static_cast<int64_t>(i) * g.Tn + n;
+  const int32_t rot0 = ag_rot0(g);
+  const int32_t u = (i - rot0 + g.Tm) % g.Tm;
+  const int32_t k = ag_key(g, rot0, u);
+  const int32_t ug = ag_count_below(g, rot0, k);
+  const int32_t ue = ag_count_below(g, rot0, k + 1);
+  return static_cast<int64_t>(ug) * g.Tn + band_offset(ug, ue, u, n, g.Tn, g.G);
+}
+// chunk moved at transfer step tc (own rank first, then r+1, r+2, ...)
+DT_HD void ag_transfer_chunk(const Geom& g, int32_t tc, int32_t& s, int32_t& j) {
+  const int32_t u = tc / g.nC;
+  j = tc - u * g.nC;
+  s = g.swizzle ? (g.rank + u) % g.W : u;
+}
+
+// ------------------------------------------------------------------ scatter mode (ReduceScatter)
+// m-tile holding the first row of rank q+1
+DT_HD int32_t rs_rot0(const Geom& g, int32_t q) {
+  const int32_t d1 = (q + 1) % g.W;
+  return static_cast<int32_t>((static_cast<int64_t>(d1) * g.Ms / g.BM) % g.Tm);
+}
+DT_HD int32_t rs_key(const Geom& g, int32_t q, int32_t rot0, int32_t u) {
+  const int32_t i = (rot0 + u) % g.Tm;
+  const int64_t first = static_cast<int64_t>(i) * g.BM;
+  const int64_t last = min64(first + g.BM, g.M) - 1;
+  const int64_t d1_first = static_cast<int64_t>((q + 1) % g.W) * g.Ms;
+  // feeds the first chunk of rank q+1, the most urgent destination
+  if (first < d1_first && last >= d1_first) return 0;
+  int32_t s, j;
+  row_chunk(g, first, s, j);
+  return ((s - q - 1 + 2 * g.W) % g.W) * g.nC + j;
+}
+DT_HD int32_t rs_count_below(const Geom& g, int32_t q, int32_t rot0, int32_t k) {
+  int32_t lo = 0, hi = g.Tm;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (rs_key(g, q, rot0, mid) < k) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+// execution position of ReduceScatter tile (q, i, n)
+DT_HD int64_t rs_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
+  if (!g.swizzle) return (static_cast<int64_t>(q) * g.Tm + i) * g.Tn + n;
+  const int32_t rot0 = rs_rot0(g, q);
+  const int32_t u = (i - rot0 + g.Tm) % g.Tm;
+  const int32_t k = rs_key(g, q, rot0, u);
+  int64_t before = 0;  // m-tiles of all ranks placed before this (q, key) group
+  for (int32_t qq = 0; qq < g.W; ++qq) {
+    const int32_t r0 = rs_rot0(g, qq);
+    const int32_t below = rs_count_below(g, qq, r0, k);
+    before += below;
+    if (qq < q) before += rs_count_below(g, qq, r0, k + 1) - below;
+  }
+  const int32_t ug = rs_count_below(g, q, rot0, k);
+  const int32_t ue = rs_count_below(g, q, rot0, k + 1);
+  return before * g.Tn + band_offset(ug, ue, u, n, g.Tn, g.G);
+}
+
+// partial tiles that must arrive before unit (chunk (s, j), column tile n) is complete
+DT_HD uint32_t rs_unit_arrivals(const Geom& g, int64_t lo, int64_t hi) {
+  return static_cast<uint32_t>(g.W) *
+         static_cast<uint32_t>((hi - 1) / g.BM - lo / g.BM + 1);
+}
+
+}  // namespace dt
