@@ -104,8 +104,9 @@ def test_edge_shapes(dt, case, out_dtype):
     w, m, n, k, cr = case
     inp = make_rs_inputs(w, m, n, k, seed=41 + m)
     ref = _oracle(inp)
+    lda = -(-k // 8) * 8  # 16-byte rows: K per rank need not be a multiple of 8
     for swizzle in [True, False]:
-        outs = _run(dt, inp, m, n, k, out_dtype, chunk_rows=cr, swizzle=swizzle)
+        outs = _run(dt, inp, m, n, k, out_dtype, lda=lda, chunk_rows=cr, swizzle=swizzle)
         _check_all(outs, ref, out_dtype, what=f"{case}")
 
 

@@ -213,9 +213,7 @@ struct LayoutKey {
 };
 
 struct WsState {
-  LayoutKey key;
   uint32_t epoch;
-  bool plan_ready;
 };
 
 std::mutex g_mu;
@@ -229,8 +227,25 @@ LayoutKey key_of(const Derived& d) {
   return LayoutKey{d.op, d.W, d.rank, d.G, d.swizzle ? 1 : 0, d.M, d.N, d.K, d.Cr};
 }
 
-// Bring the workspace to this call: clear its control block if it is new or was laid out
-// for another problem, bump the epoch, and write the tile order if it is not resident.
+// 64-bit tag of the workspace layout (FNV-1a over the key), never 0
+unsigned long long layout_tag(const Derived& d) {
+  const LayoutKey k = key_of(d);
+  const long long v[9] = {k.op, k.W, k.rank, k.G, k.swz, k.M, k.N, k.K, k.Cr};
+  unsigned long long h = 1469598103934665603ull;
+  for (long long x : v) {
+    for (int b = 0; b < 8; ++b) {
+      h ^= static_cast<unsigned long long>((x >> (8 * b)) & 0xff);
+      h *= 1099511628211ull;
+    }
+  }
+  return h | 1ull;
+}
+
+constexpr size_t kTagOffset = 16;  // after the 4-word error block
+
+// Bring the workspace to this call: bump the host-side epoch and launch the prepare kernel,
+// which rewrites the tile order and clears the control arrays unless the workspace already
+// carries this layout's tag and no recorded error.
 dt_status prepare_workspace(const Derived& d, void* ws, cudaStream_t stream, uint32_t* epoch);
 
 // ------------------------------------------------------------------------------ device info
@@ -272,6 +287,31 @@ __global__ void plan_kernel(Geom g, int op, int32_t* order, int32_t T) {
     pos = rs_position(g, q, rem / g.Tn, rem % g.Tn);
   }
   if (pos >= 0 && pos < T) order[pos] = t;
+}
+
+// Once per call before the fused kernel: if the workspace does not carry `tag` (new or
+// zero-filled memory, another problem, or a call that recorded an error), write the tile
+// order and zero the per-chunk flags and counters.  All blocks read the tag before anyone
+// can change it: only the fused kernel writes it, after this grid has finished.
+__global__ void prepare_kernel(Geom g, int op, int32_t* order, int32_t T, uint32_t* ctl,
+                               int64_t ctl_words, const uint32_t* err,
+                               const unsigned long long* tag, unsigned long long expected) {
+  if (*tag == expected && err[0] == 0u) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  for (int64_t w = t0; w < ctl_words; w += stride) ctl[w] = 0u;
+  for (int64_t t = t0; t < T; t += stride) {
+    int64_t pos;
+    if (op == DT_OP_AG_GEMM) {
+      pos = ag_position(g, static_cast<int32_t>(t / g.Tn), static_cast<int32_t>(t % g.Tn));
+    } else {
+      const int32_t per_q = g.Tm * g.Tn;
+      const int32_t q = static_cast<int32_t>(t / per_q);
+      const int32_t rem = static_cast<int32_t>(t - static_cast<int64_t>(q) * per_q);
+      pos = rs_position(g, q, rem / g.Tn, rem % g.Tn);
+    }
+    if (pos >= 0 && pos < T) order[pos] = static_cast<int32_t>(t);
+  }
 }
 
 __global__ void zero_rows_kernel(uint8_t* dst, int64_t rows, int64_t row_bytes, int64_t ld_bytes) {
@@ -326,35 +366,22 @@ dt_status launch_zero(void* dst, int64_t rows, int64_t row_bytes, int64_t ld_byt
 }
 
 dt_status prepare_workspace(const Derived& d, void* ws, cudaStream_t stream, uint32_t* epoch) {
-  bool need_plan = false;
-  bool need_clear = false;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_ws.find(ws);
-    const LayoutKey key = key_of(d);
-    if (it == g_ws.end() || !(it->second.key == key)) {
-      g_ws[ws] = WsState{key, 0u, false};
-      it = g_ws.find(ws);
-      need_clear = true;
-    }
-    WsState& st = it->second;
-    if (++st.epoch == 0u) st.epoch = 1u;
+    WsState& st = g_ws[ws];
+    if (++st.epoch == 0u) st.epoch = 1u;  // ready flags hold epochs; 0 means "never"
     *epoch = st.epoch;
-    need_plan = !st.plan_ready;
-    st.plan_ready = true;
   }
-  if (need_clear) DT_CUDA(cudaMemsetAsync(ws, 0, d.ctl_bytes, stream));
-  if (need_plan && d.T > 0) {
-    int32_t* order = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + d.off_order);
-    plan_kernel<<<static_cast<unsigned>(cdiv64(d.T, 256)), 256, 0, stream>>>(d.geom, d.op, order,
-                                                                              d.T);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-      std::lock_guard<std::mutex> lk(g_mu);
-      g_ws[ws].plan_ready = false;
-      return cuda_fail(e, "plan kernel launch");
-    }
-  }
+  uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+  const size_t ctl_begin = 256;
+  const int64_t ctl_words = static_cast<int64_t>((d.off_order - ctl_begin) / 4);
+  const int64_t work = std::max<int64_t>(d.T, ctl_words);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(cdiv64(work, 256), 1), 1024));
+  prepare_kernel<<<grid, 256, 0, stream>>>(
+      d.geom, d.op, reinterpret_cast<int32_t*>(w + d.off_order), d.T,
+      reinterpret_cast<uint32_t*>(w + ctl_begin), ctl_words, reinterpret_cast<uint32_t*>(w),
+      reinterpret_cast<unsigned long long*>(w + kTagOffset), layout_tag(d));
+  DT_CUDA(cudaGetLastError());
   return DT_OK;
 }
 
@@ -370,6 +397,8 @@ void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
   memset(&p, 0, sizeof(p));
   uint8_t* w = reinterpret_cast<uint8_t*>(ws);
   p.err = reinterpret_cast<uint32_t*>(w);
+  p.tag = reinterpret_cast<unsigned long long*>(w + kTagOffset);
+  p.tag_value = layout_tag(d);
   p.order = reinterpret_cast<const int32_t*>(w + d.off_order);
   p.g = d.geom;
   p.ldc = d.ldc;
@@ -606,6 +635,7 @@ dt_status dt_ag_gemm_kernel_overlap(const void* const* a_shards, const void* b, 
   uint8_t* gather = reinterpret_cast<uint8_t*>(ws) + d.off_data;
   KParams p;
   fill_common(p, d, ws, 0);
+  p.tag = nullptr;  // the baseline does not use (or vouch for) the tile order
   p.out[0] = c;
   p.plain = 1;
   p.wait_flags = 0;
@@ -718,6 +748,7 @@ dt_status dt_gemm_rs_kernel_overlap(const void* const* a_, const void* const* b_
   if ((s = dev_ctx(&dev)) != DT_OK) return s;
   KParams p;
   if ((s = rs_params(p, d, a_, b_, out, ws, 0)) != DT_OK) return s;
+  p.tag = nullptr;
   p.plain = 1;
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
   std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -765,7 +796,9 @@ dt_status dt_check(void* ws, void* stream_, uint32_t* info) {
   DT_CUDA(cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost));
   if (info) memcpy(info, h, sizeof(h));
   if (h[0] == kDevOk) return DT_OK;
-  DT_CUDA(cudaMemset(ws, 0, sizeof(h)));
+  // clear the error and the layout tag: the next call re-initialises the counters and flags
+  // that the failed call may have left behind
+  DT_CUDA(cudaMemset(ws, 0, kTagOffset + sizeof(unsigned long long)));
   if (h[0] == kDevBadTile)
     return fail(DT_ERR_INVALID, "device: tile id out of range at position %u", h[1]);
   return fail(DT_ERR_TIMEOUT, "device: bounded wait ran out (code %u, site %u, cta %u, %u)", h[0],

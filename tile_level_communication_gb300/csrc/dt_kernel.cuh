@@ -65,8 +65,10 @@ struct KParams {
   uint32_t* ready;         // AG: per chunk, = epoch once landed
   uint32_t* pieces_done;   // AG: per chunk piece counter (back to 0 after the chunk)
   uint32_t* unit_cnt;      // RS: per (chunk, column tile) arrival counter (back to 0)
-  const int32_t* order;    // tile order written by the plan kernel
+  const int32_t* order;    // tile order written by the prepare kernel
   uint32_t* err;           // 4 words: code, site, detail0, detail1
+  unsigned long long* tag; // workspace layout tag; written at exit when no error was seen
+  unsigned long long tag_value;
   Geom g;
   int64_t lda_src;         // AG: elements between shard rows
   int64_t ld_gather;       // AG: elements between gather rows
@@ -115,7 +117,9 @@ __device__ __forceinline__ void raise_error(const KParams& p, uint32_t code, uin
 }
 
 // Bounded wait on an mbarrier phase.  On timeout records the error, raises the CTA's abort
-// flag and returns false; returns false at once when another role has aborted.
+// flag and returns false; returns false at once when another role has aborted.  A pipeline
+// barrier only stalls when the role upstream of it stalls, so its bound is 4x the flag-wait
+// bound: the wait at the root of a stall reports first.
 static __device__ __noinline__ bool wait_bar(const KParams& p, const SmemLayout& L, uint32_t bar,
                                       uint32_t parity, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -124,7 +128,7 @@ static __device__ __noinline__ bool wait_bar(const KParams& p, const SmemLayout&
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0u) {
       if (*L.abort_flag) return false;
-      if (globaltimer_ns() - t0 > p.timeout_ns) {
+      if (globaltimer_ns() - t0 > 4 * p.timeout_ns) {
         raise_error(p, kDevTimeoutPipe, site, blockIdx.x, parity);
         *L.abort_flag = 1;
         return false;
@@ -660,6 +664,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  // the next call's prepare kernel (stream-ordered after this grid) may then skip rewriting
+  // the tile order and clearing the control arrays
+  if (p.tag != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && *(volatile uint32_t*)p.err == 0u)
+    *p.tag = p.tag_value;
 }
 
 }  // namespace dt
