@@ -179,6 +179,31 @@ dt_status dt_swizzle_plan_device(const dt_args* a, int op, int32_t* order_dev, i
  * {device code, site, detail0, detail1}. */
 dt_status dt_check(void* workspace, void* stream, uint32_t* info);
 
+/* Bytes of the fixed device scratch behind dt_ag_gemm_static_scratch. */
+#define DT_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* Fused AllGather-GEMM for callers that cannot allocate device memory: a plugin whose host
+ * framework owns all device memory and gives it no workspace, a process that reserved the
+ * whole GPU for its own allocator, or a latency-critical path that cannot afford
+ * cudaMalloc's device-wide synchronisation.  Same arguments and results as dt_ag_gemm
+ * without the workspace: the scratch is a fixed DT_STATIC_SCRATCH_BYTES device array inside
+ * the library, which every GPU that loads the library holds until the process exits.
+ *   - Problems with dt_workspace_size(a, DT_OP_AG_GEMM) > DT_STATIC_SCRATCH_BYTES are
+ *     rejected with DT_ERR_WORKSPACE; argument errors as in dt_ag_gemm.
+ *   - Transfer backends: DT_XFER_TMA or DT_XFER_LDST (DT_XFER_AUTO means TMA); the copy
+ *     engine needs a side stream and returns DT_ERR_UNSUPPORTED.
+ *   - Allocates nothing: no cudaMalloc / cudaFree, no stream or event creation.
+ *   - The first call on each device resolves the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture begins.
+ *   - All calls on a device share the one array and it keeps the last call's contents; each
+ *     call clears its error word and layout tag first, so the tile order, flags and counters
+ *     are rebuilt every call.  Calls that overlap on the GPU race: order them.
+ *   - Bounded device waits still end a stalled call, but there is no workspace to pass to
+ *     dt_check(), so a device-side timeout is not reported.
+ * The pages have no counterpart of this entry point. */
+dt_status dt_ag_gemm_static_scratch(const void* const* a_shards, const void* b, void* c,
+                                    const dt_args* a, void* stream);
+
 /* Failure-detection testing, host side only: the next copy-engine AllGather-GEMM call on
  * this process leaves out the copy and the ready-flag write of transfer step `step` (the
  * position in the gather order; -1 clears).  The tiles that need that chunk wait until

@@ -1,0 +1,71 @@
+"""The fixed-scratch AllGather-GEMM entry point, for callers that cannot allocate device
+memory (a plugin whose framework owns all device memory and passes no workspace, a process
+whose allocator reserved the whole GPU, a path that cannot afford cudaMalloc's
+synchronisation).  It must give the same results as dt_ag_gemm with a caller workspace, on
+consecutive calls that share its one scratch array, and reject problems that do not fit.
+
+This file is collected last so that a stop at the first failure has run every other test.
+"""
+import pytest
+
+from gpu_helpers import (assert_close, bits_equal, dev_bf16, load_dt, need_gpu, out_tensor,
+                         to_f64, workspace)
+from synth_inputs import WORKLOADS, make_ag_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dt():
+    need_gpu()
+    return load_dt()
+
+
+def _reference_call(dt, inp, args, m, n):
+    c = out_tensor(m, n, "bf16")
+    ws = workspace(dt.workspace_size(args, dt.OP_AG))
+    dt.ag_gemm([dev_bf16(s) for s in inp.shards], dev_bf16(inp.b), c, ws, args)
+    st, info = dt.check(ws)
+    assert st == 0, info
+    return c
+
+
+def test_static_scratch_matches_workspace_entry_on_consecutive_calls(dt):
+    import torch
+
+    wl = WORKLOADS["ag_w2_m512_n512_k512"]
+    small = wl.make()
+    ragged = make_ag_inputs(6, 6 * 100, 264, 1024, seed=12)
+    cases = [
+        (small, dt.make_args(2, wl.m, wl.n, wl.k, rank=1, chunk_rows=wl.chunk_rows, backend="tma"),
+         wl.m, wl.n),
+        (ragged, dt.make_args(6, 600, 264, 1024, rank=4, chunk_rows=37, backend="ldst"), 600, 264),
+        (small, dt.make_args(2, wl.m, wl.n, wl.k, rank=0, chunk_rows=64, backend="auto"),
+         wl.m, wl.n),
+    ]
+    for inp, args, m, n in cases:
+        want = _reference_call(dt, inp, args, m, n)
+        shards = [dev_bf16(s) for s in inp.shards]
+        b = dev_bf16(inp.b)
+        # two calls in a row on the shared scratch
+        for _ in range(2):
+            c = out_tensor(m, n, "bf16")
+            dt.ag_gemm_static_scratch(shards, b, c, args)
+            torch.cuda.synchronize()
+            assert_close(to_f64(c), to_f64(want), "bf16", "fixed scratch vs workspace entry")
+            assert bits_equal(c, want)
+
+
+def test_static_scratch_rejects_problems_that_do_not_fit(dt):
+    args = dt.make_args(8, 8192, 3584, 8192, chunk_rows=256, backend="tma")  # 128 MiB gather
+    assert dt.workspace_size(args, dt.OP_AG) > dt.capi.STATIC_SCRATCH_BYTES
+    with pytest.raises(dt.DtError) as ei:
+        dt.ag_gemm_static_scratch([0] * 8, 0, 0, args)
+    assert ei.value.status == dt.capi.DT_ERR_WORKSPACE
+    assert "32 MiB" in ei.value.message
+    ce = dt.make_args(2, 512, 512, 512, chunk_rows=128, backend="copy_engine")
+    inp = WORKLOADS["ag_w2_m512_n512_k512"].make()
+    with pytest.raises(dt.DtError) as ei:
+        dt.ag_gemm_static_scratch([dev_bf16(s) for s in inp.shards], dev_bf16(inp.b),
+                                  out_tensor(512, 512, "bf16"), ce)
+    assert ei.value.status == dt.capi.DT_ERR_UNSUPPORTED

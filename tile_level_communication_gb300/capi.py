@@ -40,7 +40,9 @@ _SIGS = {
     "dt_swizzle_plan_device": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64, _P]),
     "dt_check": (ctypes.c_int, [_P, _P, _P]),
     "dt_debug_drop_transfer": (ctypes.c_int, [ctypes.c_int32]),
+    "dt_ag_gemm_static_scratch": (ctypes.c_int, [_P, _P, _P, _P, _P]),
 }
+STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 class DtArgs(ctypes.Structure):
@@ -165,6 +167,13 @@ def gemm_rs(a_list, b_list, out_list, workspace, args: DtArgs, stream=None, ws_b
     _raise(lib().dt_gemm_rs(_ptr_array(a_list), _ptr_array(b_list), _ptr_array(out_list),
                             _ptr(workspace), _nbytes(workspace, ws_bytes), ctypes.byref(args),
                             _stream(stream)))
+
+
+def ag_gemm_static_scratch(shards, b, c, args: DtArgs, stream=None):
+    """dt_ag_gemm on the library's fixed device scratch: for callers that cannot allocate
+    device memory.  Problems needing more than STATIC_SCRATCH_BYTES are rejected."""
+    _raise(lib().dt_ag_gemm_static_scratch(_ptr_array(shards), _ptr(b), _ptr(c),
+                                           ctypes.byref(args), _stream(stream)))
 
 
 def ag_gemm_kernel_overlap(shards, b, c, workspace, args: DtArgs, stream=None, ws_bytes=None):

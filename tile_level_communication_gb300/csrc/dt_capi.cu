@@ -443,6 +443,75 @@ dt_status ce_copy_chunk(const Derived& d, const void* const* a_shards, uint8_t* 
 
 }  // namespace
 
+namespace dt {
+
+void set_last_error(const char* msg) { g_last_error = msg; }
+
+dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c, void* scratch,
+                             size_t scratch_bytes, const dt_args* a, cudaStream_t stream) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = ag_common(a_shards, b, c, scratch, scratch_bytes, a, &d);
+  if (s != DT_OK || d.M == 0 || d.N == 0) return s;
+  if (a->backend == DT_XFER_COPY_ENGINE)
+    return fail(DT_ERR_UNSUPPORTED,
+                "the copy-engine transfer needs a side stream; use DT_XFER_TMA or DT_XFER_LDST");
+  const int copy = a->backend == DT_XFER_LDST ? kCopyLdst : kCopyTma;
+  if (d.K == 0) return launch_zero(c, d.M, d.N * (d.f32 ? 4 : 2), d.ldc * (d.f32 ? 4 : 2), stream);
+  int dev = 0, sms = 0;
+  DT_CUDA(cudaGetDevice(&dev));
+  DT_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  uint8_t* w = reinterpret_cast<uint8_t*>(scratch);
+  // start from a cleared error word and tag: the prepare kernel below then rewrites the order
+  // and zeroes the flags and counters, whatever an earlier call left behind
+  DT_CUDA(cudaMemsetAsync(w, 0, kTagOffset + sizeof(unsigned long long), stream));
+  const size_t ctl_begin = 256;
+  const int64_t ctl_words = static_cast<int64_t>((d.off_order - ctl_begin) / 4);
+  const int64_t work = std::max<int64_t>(d.T, ctl_words);
+  const unsigned pgrid =
+      static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(cdiv64(work, 256), 1), 1024));
+  prepare_kernel<<<pgrid, 256, 0, stream>>>(
+      d.geom, d.op, reinterpret_cast<int32_t*>(w + d.off_order), d.T,
+      reinterpret_cast<uint32_t*>(w + ctl_begin), ctl_words, reinterpret_cast<uint32_t*>(w),
+      reinterpret_cast<unsigned long long*>(w + kTagOffset), layout_tag(d));
+  DT_CUDA(cudaGetLastError());
+  const uint32_t epoch = 1u;  // the flags were just zeroed
+  KParams p;
+  fill_common(p, d, scratch, epoch);
+  for (int i = 0; i < d.W; ++i) p.shard[i] = reinterpret_cast<const uint8_t*>(a_shards[i]);
+  p.out[0] = c;
+  p.gather = w + d.off_data;
+  p.ready = reinterpret_cast<uint32_t*>(w + d.off_ready);
+  p.pieces_done = reinterpret_cast<uint32_t*>(w + d.off_pieces);
+  p.lda_src = d.lda;
+  p.ld_gather = d.ld_gather;
+  p.wait_flags = 1;
+  p.row_bytes = d.K * 2;
+  if (p.row_bytes <= kCopyBuf) {
+    p.rows_per_piece = static_cast<int32_t>(kCopyBuf / p.row_bytes);
+    p.segs_per_row = 1;
+  } else {
+    p.rows_per_piece = 0;
+    p.segs_per_row = static_cast<int32_t>(cdiv64(p.row_bytes, kCopyBuf));
+  }
+  auto pieces = [&](int64_t rows) -> int32_t {
+    return p.rows_per_piece > 0 ? static_cast<int32_t>(cdiv64(rows, p.rows_per_piece))
+                                : static_cast<int32_t>(rows * p.segs_per_row);
+  };
+  p.pieces_full = pieces(std::min<int64_t>(d.Cr, d.Ms));
+  p.pieces_last = pieces(d.Ms - static_cast<int64_t>(d.nC - 1) * d.Cr);
+  p.src_rows_contig = d.lda == d.K ? 1 : 0;
+  if ((s = make_tmap(&p.tmA[0], p.gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
+  if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
+  const int use = a->num_sms > 0 ? std::min(a->num_sms, sms) : sms;
+  const int grid = static_cast<int>(std::min<int64_t>(d.T, use));
+  const cudaError_t e = launch_ag_kernel(p, copy, d.f32, grid, true, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
+  return DT_OK;
+}
+
+}  // namespace dt
+
 // ================================================================================ C ABI
 extern "C" {
 

@@ -3,9 +3,21 @@
 
 #include <cuda_runtime.h>
 
+#include "../../include/dt.h"
 #include "dt_kernel.cuh"
 
 namespace dt {
+
+// Fused AllGather-GEMM on a caller-supplied scratch buffer using only the in-kernel chunk
+// transfer (TMA bulk or ld/st; AUTO means TMA).  Creates no stream, event or host-side
+// record: every call clears the scratch's error word and layout tag, so the prepare kernel
+// rebuilds the tile order and zeroes the flags and counters, and the call runs with epoch 1.
+// Defined in dt_capi.cu; used by the fixed-scratch entry point in dt_static_ws.cu.
+dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c, void* scratch,
+                             size_t scratch_bytes, const dt_args* a, cudaStream_t stream);
+
+// Set the calling thread's dt_last_error() message.
+void set_last_error(const char* msg);
 
 // Launch the fused persistent kernel; defined in dt_ag.cu (AllGather variants) and
 // dt_rs.cu (ReduceScatter variants).  `cooperative` guarantees that every CTA is resident,
