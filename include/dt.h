@@ -22,9 +22,11 @@
  *     own block last) and waits per tile only for the chunks that tile reads;
  *   - the chunk transfer runs on the copy engine, on in-kernel TMA bulk copies, or on
  *     vectorised loads/stores (AutoOverlap page, Table 2 / Fig. 7);
- *   - GEMM-ReduceScatter scatters fp32 partial tiles into the destination's slots and the
- *     last arriving tile of a (chunk x column-tile) unit reduces the W partials in fixed
- *     rank order q = 0..W-1, so results do not depend on tile order, chunk size or backend.
+ *   - GEMM-ReduceScatter scatters fp32 partial tiles into the destination's slots; a
+ *     reduction unit is the part of a chunk that one m-tile covers, times one column tile,
+ *     and the last of its W arriving tiles reduces the partials in fixed rank order
+ *     q = 0..W-1 (its own term straight from its accumulator), so results do not depend on
+ *     tile order, chunk size or backend.
  *
  * Conventions
  *   - Matrices are row-major with explicit leading dimensions in ELEMENTS.
@@ -119,7 +121,7 @@ const char* dt_last_error(void);
 /* Bytes of device workspace that `op` (dt_op) needs for `a`; 0 if `a` is invalid.
  * AG: control block + per-chunk flags/counters + tile order + the gather buffer
  *     (M x K bf16).  RS: control block + per-unit counters + tile order + the fp32
- *     partial slots (W x W x M/W x N fp32). */
+ *     partial slots (W x W x M/W x N fp32; the last arriving partial is never stored). */
 size_t dt_workspace_size(const dt_args* a, int op);
 
 /* Zero the control block of a workspace laid out for (a, op) on `stream` and forget the
@@ -145,10 +147,12 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c,
  *   a   : host array of W device pointers, A_q [M x K] bf16 (K = per-rank K), ld = lda
  *   b   : host array of W device pointers, B_q [K x N] bf16, ld = ldb
  *   out : host array of W device pointers, out_s [M/W x N] (out_dtype), ld = ldc
- * Every tile (q, i, n) is one partial product; its fp32 rows are pushed into destination
- * s's slot q and the last of the W * (m-tiles per chunk) arrivals of a unit reduces the
- * slots in order q = 0..W-1 (DITRON page section 3.2 "Scatter模式"; Triton-distributed
- * talk, notify/wait of the GEMM-ReduceScatter example). */
+ * Every tile (q, i, n) is one partial product.  For each unit (rows of m-tile i inside one
+ * chunk, column tile n) the tile either pushes its fp32 rows into destination s's slot q and
+ * counts its arrival (notify), or, when the other W-1 partials are already in, sums all W in
+ * order q = 0..W-1 with its own term taken from its accumulator and writes out_s (DITRON page
+ * section 3.2 "Scatter模式"; Triton-distributed talk, notify/wait of the GEMM-ReduceScatter
+ * example). */
 dt_status dt_gemm_rs(const void* const* a, const void* const* b, void* const* out,
                      void* workspace, size_t ws_bytes, const dt_args* a_args, void* stream);
 

@@ -37,9 +37,10 @@ Tn = ceil(N/BN); group width G (default 8).
   dpos_q(s) * nC + j.  Tiles (q, i, n) sorted by (key, q, band, n, i), band taken
   among the m-tiles of the same (q, key).
 * ReduceScatter, swizzle off: lexicographic (q, i, n).
-* ReduceScatter arrivals: unit (s, j, n) = rows of chunk (s, j) x column tile n.
-  It is complete after W * (number of m-tiles that overlap chunk (s, j))
-  partial tiles have arrived.
+* ReduceScatter arrivals: a unit is the part of chunk (s, j) that m-tile i covers, times
+  column tile n (AutoOverlap section 4.1: a chunk is made of compute tiles; the reduction
+  is done per tile-sized piece of it).  Exactly the W source tiles (q, i, n), q = 0..W-1,
+  write its rows, so it is complete after W arrivals.
 """
 from __future__ import annotations
 
@@ -160,13 +161,19 @@ def rs_order(world_size, m, n, chunk_rows, bm, bn, swizzle=True, group=8):
 
 
 def rs_expected_arrivals(world_size, m, n, chunk_rows, bm, bn):
-    """{(s, j, n): partial tiles that must arrive before unit (s, j, n) is reduced}."""
+    """{(i, s, j, n): partial tiles that must arrive before that unit is reduced}.
+
+    A unit is (rows of m-tile i that lie in chunk (s, j)) x column tile n; the partial
+    tiles that write any of its rows are counted over every source rank and m-tile."""
     ms, nc, tm, tn = geometry(world_size, m, n, chunk_rows, bm, bn)
     out = {}
     for s in range(world_size):
         for j in range(nc):
             lo, hi = chunk_rows_range(s, j, ms, chunk_rows)
-            mtiles = {g // bm for g in range(lo, hi)}
-            for c in range(tn):
-                out[(s, j, c)] = world_size * len(mtiles)
+            for i in sorted({g // bm for g in range(lo, hi)}):
+                rows = set(range(max(lo, i * bm), min(hi, (i + 1) * bm)))
+                for c in range(tn):
+                    writers = [(q, i2) for q in range(world_size) for i2 in range(tm)
+                               if rows & set(range(i2 * bm, min(m, (i2 + 1) * bm)))]
+                    out[(i, s, j, c)] = len(writers)
     return out

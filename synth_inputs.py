@@ -159,8 +159,10 @@ WORKLOADS = {
     # Llama-70B-like TP=8 FFN pair, seed 2: activations N(0,1), weights N(0,0.02)
     "ag_w8_m8192_n3584_k8192": Workload("ag_w8_m8192_n3584_k8192", "ag", 8, 8192, 3584, 8192, 2,
                                         "normal(1.0)", "normal(0.02)", 256),
+    # (chunk rows for the ReduceScatter: one chunk per destination rank, the best of the
+    # 256 / 512 / 1024 sweep)
     "rs_w8_m8192_n8192_k3584": Workload("rs_w8_m8192_n8192_k3584", "rs", 8, 8192, 8192, 3584, 2,
-                                        "normal(1.0)", "normal(0.02)", 256),
+                                        "normal(1.0)", "normal(0.02)", 1024),
     # non-perfect tiling, W=6, U[-1,1], seed 3, chunk 192: every edge ragged
     "ag_w6_m6000_n3000_k5120": Workload("ag_w6_m6000_n3000_k5120", "ag", 6, 6000, 3000, 5120, 3,
                                         "uniform", "uniform", 192),

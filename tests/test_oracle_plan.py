@@ -196,8 +196,10 @@ def test_arrival_counts_brute_force(case):
     for t in plan.rs_order(w, m, n, cr, bm, bn, True):
         q, i, c = t // (tm * tn), (t // tn) % tm, t % tn
         for u in {plan.chunk_of_row(g, ms, cr) for g in _rows_of_mtile(i, m, bm)}:
-            counts[(u[0], u[1], c)] = counts.get((u[0], u[1], c), 0) + 1
-    assert counts == plan.rs_expected_arrivals(w, m, n, cr, bm, bn)
+            counts[(i, u[0], u[1], c)] = counts.get((i, u[0], u[1], c), 0) + 1
+    want = plan.rs_expected_arrivals(w, m, n, cr, bm, bn)
+    assert counts == want
+    assert set(want.values()) == {w}  # only the W source tiles of the same m-tile write a unit
 
 
 def test_chunk_map_covers_rows_once():

@@ -8,7 +8,7 @@ namespace {
 template <int COPY, bool F32>
 cudaError_t launch_one(const KParams& p, int grid, bool cooperative, cudaStream_t stream) {
   auto kern = fused_gemm_kernel<false, COPY, F32>;
-  const int smem = kernel_smem_bytes(COPY);
+  const int smem = kernel_smem_bytes(false, COPY);
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

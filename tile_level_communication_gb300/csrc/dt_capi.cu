@@ -16,7 +16,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/dt.h"
+#include "dt.h"
 #include "dt_internal.h"
 
 using namespace dt;
@@ -74,14 +74,15 @@ PfnWriteValue32 write_value32() {
 // 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per row, `outer`
 // rows `row_stride_bytes` apart; boxes of box_inner x box_outer elements.
 dt_status make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
-                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   PfnEncodeTiled enc = encode_tiled();
   if (!enc) return fail(DT_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_stride_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+  const CUresult r = enc(tm, dtype, 2, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -97,7 +98,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Derived {
   int op;
-  int32_t W, rank, G, Tm, Tn, KB, T, nC;
+  int32_t W, rank, G, Tm, Tn, KB, T, nC, pieces_max;
   int64_t M, N, K, Ms, Cr, lda, ldb, ldc, ld_gather;
   bool swizzle, f32;
   int backend;  // resolved for AG
@@ -166,6 +167,8 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   const int64_t T64 = (op == DT_OP_AG_GEMM ? 1 : d->W) * static_cast<int64_t>(d->Tm) * d->Tn;
   if (T64 >= (1ll << 31)) return fail(DT_ERR_UNSUPPORTED, "too many tiles");
   d->T = static_cast<int32_t>(T64);
+  if (op == DT_OP_GEMM_RS && static_cast<int64_t>(d->W - 1) * d->M >= (1ll << 31))
+    return fail(DT_ERR_UNSUPPORTED, "(W-1)*M must be below 2^31");
   if (static_cast<int64_t>(d->W) * d->nC >= (1ll << 24))
     return fail(DT_ERR_UNSUPPORTED, "too many chunks; raise chunk_rows");
   d->ld_gather = d->K;  // K % 8 == 0: 16-byte rows, back to back
@@ -182,14 +185,16 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   const size_t nchunks = static_cast<size_t>(d->W) * d->nC;
   size_t off = 256;
   d->off_ready = d->off_pieces = d->off_cnt = 0;
+  d->pieces_max = 0;
   if (op == DT_OP_AG_GEMM) {
     d->off_ready = off;
     off = align_up(off + 4 * nchunks, 256);
     d->off_pieces = off;
     off = align_up(off + 4 * nchunks, 256);
   } else {
+    d->pieces_max = d->Tm > 0 && d->Ms > 0 ? rs_pieces_max(d->geom) : 0;
     d->off_cnt = off;
-    off = align_up(off + 4 * nchunks * d->Tn, 256);
+    off = align_up(off + 4 * static_cast<size_t>(d->Tm) * d->Tn * d->pieces_max, 256);
   }
   d->off_order = off;
   off = align_up(off + 4 * static_cast<size_t>(d->T), 1024);
@@ -323,7 +328,8 @@ __global__ void zero_rows_kernel(uint8_t* dst, int64_t rows, int64_t row_bytes, 
   }
 }
 
-// out_s = sum over q (in order) of the fp32 partial slots recv[s][q]
+// out_s = the fp32 partial slots recv[s][q] summed in the fused path's fixed order: source
+// q_d = (s - d - 1) mod W for d = 0..W-1 (rank s-1 first, s itself last)
 __global__ void reduce_slots_kernel(const float* recv, int32_t W, int64_t Ms, int64_t N, int32_t s,
                                     void* out, int64_t ldc, int f32) {
   const int64_t nv = N / 4;
@@ -333,8 +339,9 @@ __global__ void reduce_slots_kernel(const float* recv, int32_t W, int64_t Ms, in
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = e / nv, v = e - r * nv;
     const float* src = base + r * N + v * 4;
-    float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
-    for (int32_t q = 1; q < W; ++q) {
+    float4 acc = __ldcg(reinterpret_cast<const float4*>(src + ((s - 1 + W) % W) * slot));
+    for (int32_t d = 1; d < W; ++d) {
+      const int32_t q = (s - d - 1 + 2 * W) % W;
       const float4 x = __ldcg(reinterpret_cast<const float4*>(src + q * slot));
       acc.x += x.x;
       acc.y += x.y;
@@ -764,6 +771,18 @@ static dt_status rs_params(KParams& p, const Derived& d, const void* const* a_,
   uint8_t* w = reinterpret_cast<uint8_t*>(ws);
   p.recv = reinterpret_cast<float*>(w + d.off_data);
   p.unit_cnt = reinterpret_cast<uint32_t*>(w + d.off_cnt);
+  p.pieces_max = d.pieces_max;
+  // running sums [M][N] fp32 and park slots [W (W-1) Ms][N] fp32, moved in 32 x 128 boxes
+  dt_status st = make_tmap(&p.tmAcc, p.recv, d.N, d.M, d.N * 4, 32, kBM, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+  if (st != DT_OK) return st;
+  if (d.W > 1) {
+    st = make_tmap(&p.tmPark, p.recv + static_cast<size_t>(d.M) * d.N, d.N,
+                   static_cast<uint64_t>(d.W - 1) * d.M, d.N * 4, 32, kBM,
+                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+    if (st != DT_OK) return st;
+  } else {
+    p.tmPark = p.tmAcc;  // one rank never parks
+  }
   for (int q = 0; q < d.W; ++q) {
     p.out[q] = out[q];
     dt_status s = make_tmap(&p.tmA[q], a_[q], d.K, d.M, d.lda * 2, 64, kBM);

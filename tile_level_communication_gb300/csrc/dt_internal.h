@@ -3,7 +3,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/dt.h"
+#include "dt.h"
 #include "dt_kernel.cuh"
 
 namespace dt {

@@ -50,21 +50,28 @@ enum DevCode : uint32_t {
   kDevBadTile = 3,       // a tile id from the plan was out of range (tile skipped)
 };
 
-__host__ __device__ constexpr int kernel_smem_bytes(int copy_mode) {
-  return 1024 + kStages * (kAStage + kBStage) + (copy_mode == kCopyTma ? 2 * kCopyBuf : 0) +
+// Dynamic shared memory of a kernel instance: alignment slack, the operand ring, two 16 KiB
+// staging buffers (AllGather TMA transfer, or ReduceScatter running-sum tiles), flags.
+__host__ __device__ constexpr bool has_staging(bool rs, int copy_mode) {
+  return rs || copy_mode == kCopyTma;
+}
+__host__ __device__ constexpr int kernel_smem_bytes(bool rs, int copy_mode) {
+  return 1024 + kStages * (kAStage + kBStage) + (has_staging(rs, copy_mode) ? 2 * kCopyBuf : 0) +
          kMiscBytes;
 }
 
 struct KParams {
   CUtensorMap tmA[kMaxW];  // AG: [0] = gather buffer; RS: A_q
   CUtensorMap tmB[kMaxW];  // AG: [0] = B; RS: B_q
+  CUtensorMap tmAcc;       // RS: running sums, fp32 [M][N], 32 x 128 boxes
+  CUtensorMap tmPark;      // RS: park slots, fp32 [W (W-1) M/W][N], 32 x 128 boxes
   const uint8_t* shard[kMaxW];
   void* out[kMaxW];        // AG: out[0] = C; RS: out[s]
   uint8_t* gather;
   float* recv;             // RS: W x W x Ms x N fp32 partial slots, [dest][src]
   uint32_t* ready;         // AG: per chunk, = epoch once landed
   uint32_t* pieces_done;   // AG: per chunk piece counter (back to 0 after the chunk)
-  uint32_t* unit_cnt;      // RS: per (chunk, column tile) arrival counter (back to 0)
+  uint32_t* unit_cnt;      // RS: per (m-tile, chunk piece, column tile) arrival counter
   const int32_t* order;    // tile order written by the prepare kernel
   uint32_t* err;           // 4 words: code, site, detail0, detail1
   unsigned long long* tag; // workspace layout tag; written at exit when no error was seen
@@ -75,6 +82,7 @@ struct KParams {
   int64_t ldc;
   int64_t row_lo, row_hi;  // rows handled: [0, M) fused; one window in the baselines
   int32_t Tm, KB, T;       // m-tiles in the window, k-blocks, tiles in the launch
+  int32_t pieces_max;      // RS: most chunks one m-tile's rows touch (counter stride)
   int32_t plain;           // 1: identity order, no flags, no arrival counting
   int32_t wait_flags;      // AG: the producer waits on ready flags
   uint32_t epoch;
@@ -97,6 +105,8 @@ struct SmemLayout {
   volatile int* abort_flag;
   volatile int* unit_flag;
   volatile int* vote;      // [2][4]
+  volatile uint32_t* last_mask;  // RS: pieces of the current tile folded in order [4]
+  volatile int8_t* chain;        // RS: per piece, first parked partial this tile folds (-1)
   uint32_t* ready_bits;
   __device__ uint32_t full(int s) const { return smem_u32(bars + s); }
   __device__ uint32_t empty(int s) const { return smem_u32(bars + kStages + s); }
@@ -331,59 +341,148 @@ __device__ __forceinline__ float4 ldcg_f4(const float* p) {
   return __ldcg(reinterpret_cast<const float4*>(p));
 }
 
-// Sum the W partial slots of one unit (rows [lo, hi) of rank s, column tile n) in rank order
-// q = 0..W-1 and store the result rows of out_s.  Runs on the 128 epilogue threads.
+// ---------------------------------------------------------------------------- RS folding
+// A ReduceScatter unit is (the rows of m-tile i inside one chunk of destination s) x column
+// tile n.  Its W partials are summed in a fixed order d = 0..W-1, partial d coming from source
+// rank q_d = (s - d - 1) mod W: the order in which the scatter schedule produces them (rank
+// s-1 first, the destination's own partial last).  The running fp32 sum S_d = S_{d-1} + P_{q_d}
+// lives in `acc` ([M][N], global rows); S_{W-1} is rounded once into out_s.  A partial that is
+// ready before its predecessors are folded waits in park slot (s, d).  One 32-bit word per unit
+// holds the number of partials folded so far (bits 0-7) and which ones are parked (bit 8+d);
+// whoever moves the count to d, or parks d after the count reached d, folds d: exactly one
+// tile does, and nobody waits.
+__device__ __forceinline__ int32_t fold_index(int32_t s, int32_t q, int32_t W) {
+  return (s - q - 1 + 2 * W) % W;
+}
+__device__ __forceinline__ float* acc_ptr(const KParams& p, int64_t row, int64_t col) {
+  return p.recv + row * p.g.N + col;
+}
+__device__ __forceinline__ float* park_ptr(const KParams& p, int32_t s, int32_t d, int64_t lr,
+                                           int64_t col) {
+  const size_t slot = static_cast<size_t>(s) * (p.g.W - 1) + (d - 1);  // d = 0 never parks
+  return p.recv + static_cast<size_t>(p.g.M) * p.g.N +
+         (slot * p.g.Ms + lr) * static_cast<size_t>(p.g.N) + col;
+}
+
 template <bool F32>
-__device__ void reduce_unit(const KParams& p, int32_t s, int64_t lo, int64_t hi, int32_t n,
-                            int et) {
-  const int64_t c0 = static_cast<int64_t>(n) * kBN;
-  const int32_t ncols = static_cast<int32_t>(min64(kBN, p.g.N - c0));
-  const int32_t nv = ncols >> 2;
-  const int32_t nrows = static_cast<int32_t>(hi - lo);
-  const int64_t lr0 = lo - static_cast<int64_t>(s) * p.g.Ms;
-  const size_t slot = static_cast<size_t>(p.g.Ms) * static_cast<size_t>(p.g.N);
-  const float* base = p.recv + static_cast<size_t>(s) * p.g.W * slot +
-                      static_cast<size_t>(lr0) * p.g.N + c0;
-  const int32_t W = p.g.W;
-  for (int32_t e = et; e < nrows * nv; e += 128) {
-    const int32_t r = e / nv;
-    const int32_t v = e - r * nv;
-    const float* src = base + static_cast<size_t>(r) * p.g.N + v * 4;
-    float4 x[kMaxW];
+__device__ __forceinline__ void store_out8(const KParams& p, int32_t s, int64_t lr, int64_t col,
+                                           const float (&a)[8]) {
+  if (F32) {
+    float* dst = reinterpret_cast<float*>(p.out[s]) + lr * p.ldc + col;
+    reinterpret_cast<float4*>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
+  } else {
+    uint4 w;
+    w.x = pack_bf16x2(__float_as_uint(a[0]), __float_as_uint(a[1]));
+    w.y = pack_bf16x2(__float_as_uint(a[2]), __float_as_uint(a[3]));
+    w.z = pack_bf16x2(__float_as_uint(a[4]), __float_as_uint(a[5]));
+    w.w = pack_bf16x2(__float_as_uint(a[6]), __float_as_uint(a[7]));
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out[s]) + lr * p.ldc + col) = w;
+  }
+}
+
+// One thread, one row, 32 columns: fold this tile's partial (index d, in registers) into the
+// running sum; the last fold writes out_s.
+template <bool F32>
+__device__ __forceinline__ void fold_row32(const KParams& p, int32_t s, int64_t row, int64_t lr,
+                                           int32_t d, int64_t c0, const uint32_t (&v)[32]) {
+  float* acc = acc_ptr(p, row, c0);
+  float4 x[8];
+  if (d > 0) {
 #pragma unroll
-    for (int q = 0; q < kMaxW; ++q)
-      if (q < W) x[q] = ldcg_f4(src + q * slot);
-    float4 acc = x[0];
+    for (int u = 0; u < 8; ++u)
+      if (c0 + u * 4 < p.g.N) x[u] = ldcg_f4(acc + u * 4);
+  }
 #pragma unroll
-    for (int q = 1; q < kMaxW; ++q) {
-      if (q < W) {
-        acc.x += x[q].x;
-        acc.y += x[q].y;
-        acc.z += x[q].z;
-        acc.w += x[q].w;
-      }
+  for (int u = 0; u < 4; ++u) {
+    if (c0 + u * 8 >= p.g.N) break;
+    float a[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a[e] = __uint_as_float(v[u * 8 + e]);
+    if (d > 0) {
+      a[0] = x[2 * u].x + a[0]; a[1] = x[2 * u].y + a[1];
+      a[2] = x[2 * u].z + a[2]; a[3] = x[2 * u].w + a[3];
+      a[4] = x[2 * u + 1].x + a[4]; a[5] = x[2 * u + 1].y + a[5];
+      a[6] = x[2 * u + 1].z + a[6]; a[7] = x[2 * u + 1].w + a[7];
     }
-    const int64_t row = lr0 + r;
-    if (F32) {
-      float* dst = reinterpret_cast<float*>(p.out[s]) + row * p.ldc + c0 + v * 4;
-      *reinterpret_cast<float4*>(dst) = acc;
+    if (d == p.g.W - 1) {
+      store_out8<F32>(p, s, lr, c0 + u * 8, a);
     } else {
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out[s]) + row * p.ldc + c0 + v * 4;
-      uint2 w;
-      w.x = pack_bf16x2(__float_as_uint(acc.x), __float_as_uint(acc.y));
-      w.y = pack_bf16x2(__float_as_uint(acc.z), __float_as_uint(acc.w));
-      *reinterpret_cast<uint2*>(dst) = w;
+      reinterpret_cast<float4*>(acc + u * 8)[0] = make_float4(a[0], a[1], a[2], a[3]);
+      reinterpret_cast<float4*>(acc + u * 8)[1] = make_float4(a[4], a[5], a[6], a[7]);
     }
+  }
+}
+
+// The 128 epilogue threads fold parked partial e of rows [lo, hi) (destination s), column tile n.
+template <bool F32>
+__device__ void fold_parked(const KParams& p, int32_t s, int64_t lo, int64_t hi, int32_t n,
+                            int32_t e, int et) {
+  const int64_t c0 = static_cast<int64_t>(n) * kBN;
+  const int32_t nv = static_cast<int32_t>(min64(kBN, p.g.N - c0)) >> 2;
+  const int32_t nrows = static_cast<int32_t>(hi - lo);
+  for (int32_t idx = et; idx < nrows * nv; idx += 128) {
+    const int32_t r = idx / nv;
+    const int32_t v = idx - r * nv;
+    const int64_t row = lo + r;
+    const int64_t lr = row - static_cast<int64_t>(s) * p.g.Ms;
+    const int64_t col = c0 + v * 4;
+    const float4 a = ldcg_f4(acc_ptr(p, row, col));
+    const float4 b = ldcg_f4(park_ptr(p, s, e, lr, col));
+    const float4 r4 = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    if (e == p.g.W - 1) {
+      if (F32) {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out[s]) + lr * p.ldc + col) = r4;
+      } else {
+        uint2 w;
+        w.x = pack_bf16x2(__float_as_uint(r4.x), __float_as_uint(r4.y));
+        w.y = pack_bf16x2(__float_as_uint(r4.z), __float_as_uint(r4.w));
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out[s]) + lr * p.ldc + col) = w;
+      }
+    } else {
+      *reinterpret_cast<float4*>(acc_ptr(p, row, col)) = r4;
+    }
+  }
+}
+
+// Fold parked partials e, e+1, ... of one unit while they are there (all 128 epilogue threads).
+template <bool F32>
+__device__ void fold_chain(const KParams& p, const SmemLayout& L, int32_t s, int64_t lo,
+                           int64_t hi, int32_t n, int32_t e, uint32_t* word, int et) {
+  for (;;) {
+    __threadfence();
+    fold_parked<F32>(p, s, lo, hi, n, e, et);
+    __threadfence();
+    named_bar_sync(1, 128);
+    if (et == 0) {
+      int next = -1;
+      if (e == p.g.W - 1) {
+        *word = 0u;  // all W folded: ready for the next call
+      } else {
+        // count one more folded, clear e's parked bit; is e+1 parked already?
+        const uint32_t old = atom_add_acq_rel_gpu(word, 1u - (1u << (8 + e)));
+        if ((old >> (8 + e + 1)) & 1u) next = e + 1;
+      }
+      *L.unit_flag = next;
+    }
+    named_bar_sync(1, 128);
+    const int next = *L.unit_flag;
+    named_bar_sync(1, 128);
+    if (next < 0) break;
+    e = next;
   }
 }
 
 template <bool RS, bool F32>
 __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tmem_base,
                              int warp, int lane) {
-  constexpr bool kStoreF32 = RS || F32;  // ReduceScatter partial slots are fp32
+  constexpr bool kStoreF32 = RS || F32;  // ReduceScatter partials are fp32
   const int qd = warp - 4;  // TMEM lane quadrant this warp may read
   const int et = threadIdx.x - 128;
+  const bool fused_rs = RS && !p.plain;
   int32_t tl = 0;
+  uint32_t stage_ctr = 0;           // running-sum staging buffer in use (alternates)
+  uint32_t ld_par[2] = {0u, 0u};    // phase of each staging buffer's load barrier
   for (int32_t pos = blockIdx.x; pos < p.T; pos += gridDim.x) {
     const TileInfo ti = decode_tile<RS>(p, pos);
     if (!ti.valid) continue;
@@ -392,7 +491,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
     int ok = 1;
     if (lane == 0) ok = wait_bar(p, L, L.tfull(acc), ph, 400 + acc) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (RS && !p.plain) {
+    if (fused_rs) {
       // all four epilogue warps agree before they meet at the named barriers below
       if (lane == 0) L.vote[(tl & 1) * 4 + qd] = ok;
       named_bar_sync(1, 128);
@@ -405,57 +504,214 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
     const bool row_ok = row < ti.row_end;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) +
                            static_cast<uint32_t>(acc * kBN);
-    void* dst_base;
-    int64_t dst_row, dst_ld;
-    if (RS) {
-      const int32_t s = row_ok ? static_cast<int32_t>(row / p.g.Ms) : 0;
-      const size_t slot = static_cast<size_t>(s) * p.g.W + ti.q;
-      dst_base = p.recv + slot * static_cast<size_t>(p.g.Ms) * p.g.N;
-      dst_row = row - static_cast<int64_t>(s) * p.g.Ms;
-      dst_ld = p.g.N;
-    } else {
-      dst_base = p.out[0];
-      dst_row = row;
-      dst_ld = p.ldc;
+    // ReduceScatter: the tile's rows split at chunk boundaries into units ("pieces"); find
+    // which of them this tile folds in order (all earlier partials folded already)
+    int32_t c_first = 0;
+    uint32_t* words = nullptr;
+    if (fused_rs) {
+      int32_t s0, j0;
+      row_chunk(p.g, ti.row0, s0, j0);
+      c_first = s0 * p.g.nC + j0;
+      words = p.unit_cnt +
+              (static_cast<int64_t>(ti.i) * p.g.Tn + ti.n) * static_cast<int64_t>(p.pieces_max);
+      if (et == 0) {
+        uint32_t m[4] = {0u, 0u, 0u, 0u};
+        int k = 0;
+        for (int64_t g = ti.row0; g < ti.row_end; ++k) {
+          int32_t s, j;
+          row_chunk(p.g, g, s, j);
+          const uint32_t st = ld_acquire_gpu(words + k);
+          if (static_cast<int32_t>(st & 0xffu) == fold_index(s, ti.q, p.g.W))
+            m[k >> 5] |= 1u << (k & 31);
+          g = static_cast<int64_t>(s) * p.g.Ms + min64(static_cast<int64_t>(j + 1) * p.g.Cr, p.g.Ms);
+        }
+        for (int w = 0; w < 4; ++w) L.last_mask[w] = m[w];
+      }
+      named_bar_sync(1, 128);
+      __threadfence();
+    }
+    int32_t s_row = 0, j_row = 0, d_row = 0;
+    bool in_order = false;
+    int64_t lr = 0;
+    if (RS && row_ok) {
+      row_chunk(p.g, row, s_row, j_row);
+      lr = row - static_cast<int64_t>(s_row) * p.g.Ms;
+      d_row = fold_index(s_row, ti.q, p.g.W);
+      if (fused_rs) {
+        const int32_t k = s_row * p.g.nC + j_row - c_first;
+        in_order = (L.last_mask[k >> 5] >> (k & 31)) & 1u;
+      }
+    }
+    // Whole 128-row tiles inside one unit move their running sums with TMA: a 128 x 32 fp32
+    // box of the running sum is loaded into a 128-byte-swizzled staging buffer, each thread
+    // adds its row of the accumulator, and the box goes back (or to a park slot) as one
+    // bulk store.  Other tiles (ragged, or cut by a chunk boundary) go row by row.
+    bool tma_tile = false;
+    int32_t t_s = 0, t_d = 0;
+    int64_t t_lr0 = 0;
+    bool t_in_order = false;
+    if (fused_rs && ti.row_end - ti.row0 == kBM) {
+      int32_t s0, j0, s1, j1;
+      row_chunk(p.g, ti.row0, s0, j0);
+      row_chunk(p.g, ti.row_end - 1, s1, j1);
+      if (s0 == s1 && j0 == j1) {
+        tma_tile = true;
+        t_s = s0;
+        t_d = fold_index(s0, ti.q, p.g.W);
+        t_lr0 = ti.row0 - static_cast<int64_t>(s0) * p.g.Ms;
+        t_in_order = L.last_mask[0] & 1u;
+      }
+    }
+    if (tma_tile) {
+      const bool load = t_in_order && t_d > 0;
+      const bool last = t_in_order && t_d == p.g.W - 1;
+      const CUtensorMap* store_map = t_in_order ? &p.tmAcc : &p.tmPark;
+      const int32_t store_y =
+          t_in_order ? static_cast<int32_t>(ti.row0)
+                     : static_cast<int32_t>((static_cast<int64_t>(t_s) * (p.g.W - 1) + t_d - 1) *
+                                                p.g.Ms + t_lr0);
+      const int r = qd * 32 + lane;  // this thread's row of the tile
+      // the unit's word was acquired through the generic proxy; the loads below are TMA
+      if (et == 0 && load) fence_proxy_async_global();
+#pragma unroll 1
+      for (int cb = 0; cb < kBN / 32; ++cb) {
+        const int64_t c0 = ti.col0 + cb * 32;
+        if (c0 >= p.g.N) break;
+        const int b = static_cast<int>(stage_ctr & 1u);
+        uint8_t* buf = L.copy + b * kCopyBuf;
+        if (et == 0) {
+          bulk_wait_read<1>();  // the store that last used this buffer has read it
+          if (load) {
+            mbar_expect_tx(L.copyb(b), kCopyBuf);
+            tma_load_2d(smem_u32(buf), &p.tmAcc, static_cast<int32_t>(c0),
+                        static_cast<int32_t>(ti.row0), L.copyb(b));
+          }
+        }
+        named_bar_sync(1, 128);
+        uint32_t v[32];
+        tmem_ld32(tbase + cb * 32, v);
+        if (load) {
+          wait_bar(p, L, L.copyb(b), ld_par[b], 600 + b);
+          ld_par[b] ^= 1u;
+        }
+        float4* rowp = reinterpret_cast<float4*>(buf + r * 128);
+        float a[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) a[e] = __uint_as_float(v[e]);
+        if (load) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 x = rowp[c ^ (r & 7)];
+            a[4 * c + 0] = x.x + a[4 * c + 0];
+            a[4 * c + 1] = x.y + a[4 * c + 1];
+            a[4 * c + 2] = x.z + a[4 * c + 2];
+            a[4 * c + 3] = x.w + a[4 * c + 3];
+          }
+        }
+        if (last) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (c0 + u * 8 < p.g.N) {
+              float o[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = a[u * 8 + e];
+              store_out8<F32>(p, t_s, t_lr0 + r, c0 + u * 8, o);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            rowp[c ^ (r & 7)] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+          fence_proxy_async_smem();
+        }
+        named_bar_sync(1, 128);
+        if (et == 0 && !last) {
+          tma_store_2d(store_map, smem_u32(buf), static_cast<int32_t>(c0), store_y);
+          bulk_commit();
+        }
+        ++stage_ctr;
+      }
+      if (et == 0) {
+        bulk_wait<0>();  // the running sum (or parked partial) is in global memory
+        fence_proxy_async_global();
+      }
     }
 #pragma unroll 1
     for (int cb = 0; cb < kBN / 32; ++cb) {
+      if (tma_tile) break;
       const int64_t c0 = ti.col0 + cb * 32;
       if (c0 >= p.g.N) break;
       uint32_t v[32];
       tmem_ld32(tbase + cb * 32, v);
-      if (row_ok) store_row32<kStoreF32>(dst_base, dst_ld, dst_row, c0, p.g.N, v);
+      if (!row_ok) continue;
+      if (!RS) {
+        store_row32<kStoreF32>(p.out[0], p.ldc, row, c0, p.g.N, v);
+      } else if (!fused_rs) {  // baseline: partial of source q into slot [s][q]
+        const size_t slot = static_cast<size_t>(s_row) * p.g.W + ti.q;
+        store_row32<true>(p.recv + slot * static_cast<size_t>(p.g.Ms) * p.g.N, p.g.N, lr, c0,
+                          p.g.N, v);
+      } else if (in_order) {
+        fold_row32<F32>(p, s_row, row, lr, d_row, c0, v);
+      } else {  // park: an earlier partial of this unit is not folded yet
+        store_row32<true>(park_ptr(p, s_row, d_row, 0, 0), p.g.N, lr, c0, p.g.N, v);
+      }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(L.tempty(acc));
     ++tl;
 
-    if (RS && !p.plain) {
-      // notify: count this tile's arrival at every unit its rows belong to; the last
-      // arrival of a unit waits for nothing and reduces it
+    if (fused_rs) {
+      // notify: publish this tile's fold or park of every piece
       __threadfence();
       named_bar_sync(1, 128);
-      for (int64_t g = ti.row0; g < ti.row_end;) {
+      if (et == 0) {
+        int k = 0;
+        for (int64_t g = ti.row0; g < ti.row_end; ++k) {
+          int32_t s, j;
+          row_chunk(p.g, g, s, j);
+          const int32_t d = fold_index(s, ti.q, p.g.W);
+          uint32_t* word = words + k;
+          int chain = -1;
+          if ((L.last_mask[k >> 5] >> (k & 31)) & 1u) {
+            if (d == p.g.W - 1) {
+              *word = 0u;  // the unit is complete: ready for the next call
+            } else {
+              const uint32_t old = atom_add_acq_rel_gpu(word, 1u);
+              if ((old >> (8 + d + 1)) & 1u) chain = d + 1;  // the next one is parked
+            }
+          } else {
+            const uint32_t old = atom_or_acq_rel_gpu(word, 1u << (8 + d));
+            if (static_cast<int32_t>(old & 0xffu) == d) chain = d;  // caught up meanwhile
+          }
+          L.chain[k] = static_cast<int8_t>(chain);
+          g = static_cast<int64_t>(s) * p.g.Ms + min64(static_cast<int64_t>(j + 1) * p.g.Cr, p.g.Ms);
+        }
+      }
+      named_bar_sync(1, 128);
+      int k = 0;
+      for (int64_t g = ti.row0; g < ti.row_end; ++k) {
         int32_t s, j;
         row_chunk(p.g, g, s, j);
-        const int64_t lo = static_cast<int64_t>(s) * p.g.Ms + static_cast<int64_t>(j) * p.g.Cr;
-        const int64_t hi =
-            static_cast<int64_t>(s) * p.g.Ms + min64(static_cast<int64_t>(j + 1) * p.g.Cr, p.g.Ms);
-        if (et == 0) {
-          uint32_t* cnt = p.unit_cnt + (static_cast<int64_t>(s) * p.g.nC + j) * p.g.Tn + ti.n;
-          const uint32_t old = atom_add_acq_rel_gpu(cnt, 1u);
-          const int last = (old + 1u == rs_unit_arrivals(p.g, lo, hi)) ? 1 : 0;
-          if (last) *cnt = 0u;  // every arrival of this call is in: ready for the next call
-          *L.unit_flag = last;
-        }
-        named_bar_sync(1, 128);
-        if (*L.unit_flag) {
-          __threadfence();
-          reduce_unit<F32>(p, s, lo, hi, ti.n, et);
-        }
-        named_bar_sync(1, 128);
+        const int64_t hi = min64(ti.row_end, static_cast<int64_t>(s) * p.g.Ms +
+                                                 min64(static_cast<int64_t>(j + 1) * p.g.Cr, p.g.Ms));
+        const int chain = L.chain[k];
+        if (chain >= 0) fold_chain<F32>(p, L, s, g, hi, ti.n, chain, words + k, et);
         g = hi;
+      }
+      named_bar_sync(1, 128);
+      // warm L2 with the running sums the next tile of this CTA will fold into
+      const int32_t npos = pos + static_cast<int32_t>(gridDim.x);
+      if (npos < p.T) {
+        const TileInfo nt = decode_tile<RS>(p, npos);
+        const int64_t nrow = nt.row0 + qd * 32 + lane;
+        if (nt.valid && nrow < nt.row_end) {
+          int32_t s, j;
+          row_chunk(p.g, nrow, s, j);
+          if (fold_index(s, nt.q, p.g.W) > 0)
+            prefetch_l2(acc_ptr(p, nrow, nt.col0),
+                        static_cast<uint32_t>(min64(kBN, p.g.N - nt.col0) * 4));
+        }
       }
     }
   }
@@ -608,13 +864,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   L.a = base;
   L.b = L.a + kStages * kAStage;
   L.copy = L.b + kStages * kBStage;
-  uint8_t* misc = L.copy + (COPY == kCopyTma ? 2 * kCopyBuf : 0);
-  L.bars = reinterpret_cast<uint64_t*>(misc);  // 16 barriers
-  L.tmem_slot = reinterpret_cast<uint32_t*>(misc + 128);
-  L.abort_flag = reinterpret_cast<volatile int*>(misc + 132);
-  L.unit_flag = reinterpret_cast<volatile int*>(misc + 136);
-  L.vote = reinterpret_cast<volatile int*>(misc + 160);
-  L.ready_bits = reinterpret_cast<uint32_t*>(misc + 256);
+  uint8_t* misc = L.copy + (has_staging(RS, COPY) ? 2 * kCopyBuf : 0);
+  L.bars = reinterpret_cast<uint64_t*>(misc);  // up to 32 barriers
+  L.tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
+  L.abort_flag = reinterpret_cast<volatile int*>(misc + 260);
+  L.unit_flag = reinterpret_cast<volatile int*>(misc + 264);
+  L.vote = reinterpret_cast<volatile int*>(misc + 288);
+  L.last_mask = reinterpret_cast<volatile uint32_t*>(misc + 320);
+  L.chain = reinterpret_cast<volatile int8_t*>(misc + 384);
+  L.ready_bits = reinterpret_cast<uint32_t*>(misc + 512);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

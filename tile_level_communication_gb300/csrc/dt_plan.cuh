@@ -164,10 +164,21 @@ DT_HD int64_t rs_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
   return before * g.Tn + band_offset(ug, ue, u, n, g.Tn, g.G);
 }
 
-// partial tiles that must arrive before unit (chunk (s, j), column tile n) is complete
-DT_HD uint32_t rs_unit_arrivals(const Geom& g, int64_t lo, int64_t hi) {
-  return static_cast<uint32_t>(g.W) *
-         static_cast<uint32_t>((hi - 1) / g.BM - lo / g.BM + 1);
+// Most chunks that the rows of one m-tile touch: each (m-tile, chunk) piece times a column
+// tile is one ReduceScatter reduction unit with its own arrival counter.
+inline int32_t rs_pieces_max(const Geom& g) {
+  int32_t best = 0;
+  for (int32_t i = 0; i < g.Tm; ++i) {
+    int32_t k = 0;
+    const int64_t end = min64(static_cast<int64_t>(i + 1) * g.BM, g.M);
+    for (int64_t r = static_cast<int64_t>(i) * g.BM; r < end; ++k) {
+      int32_t s, j;
+      row_chunk(g, r, s, j);
+      r = static_cast<int64_t>(s) * g.Ms + min64(static_cast<int64_t>(j + 1) * g.Cr, g.Ms);
+    }
+    best = k > best ? k : best;
+  }
+  return best;
 }
 
 }  // namespace dt

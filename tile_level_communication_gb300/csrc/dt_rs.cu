@@ -7,7 +7,7 @@ namespace {
 template <bool F32>
 cudaError_t launch_one(const KParams& p, int grid, cudaStream_t stream) {
   auto kern = fused_gemm_kernel<true, kCopyNone, F32>;
-  const int smem = kernel_smem_bytes(kCopyNone);
+  const int smem = kernel_smem_bytes(true, kCopyNone);
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -17,7 +17,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/dt.h"
+#include "dt.h"
 #include "dt_internal.h"
 
 // The scratch itself.  In host code this name is a host-side stand-in, never a device
