@@ -31,6 +31,24 @@ import numpy as np  # noqa: E402
 from synth_inputs import WORKLOADS, f64_from_bf16_bits  # noqa: E402
 
 METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU)"
+
+# DRAM bytes (read + write) per launch of the fused kernel, from one `ncu --set full` capture
+# of the named workload (profiles/), valid only for the kernel sources it was taken on.
+NCU_TRAFFIC = {
+    "rs_w8_m8192_n8192_k3584": {"csrc": "4352d877c48df460", "bytes": 6.181913e9 + 2.000587e9},
+    "ag_w8_m16384_n8192_k8192": {"csrc": "4352d877c48df460", "bytes": 4.250976e9 + 0.5306816e9},
+}
+
+
+def csrc_hash():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "tile_level_communication_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 FFN_PAIR = ("ag_w8_m8192_n3584_k8192", "rs_w8_m8192_n8192_k3584")
 L2_BYTES = 129 * 2 ** 20
 
@@ -341,7 +359,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": workload_desc(args.workload, ops, args.chunk_rows),
-        "gpu_launches": len(calls) * args.steps,
+        # per call: the prepare kernel and the fused kernel
+        "gpu_launches": 2 * len(calls) * args.steps,
     }
     line["config"].update({
         "parallelism": f"{ops[0].world_size} virtual ranks in one GPU's HBM; "
@@ -359,10 +378,13 @@ def main():
                       for cl, ms in zip(calls, per_call_ms)}
     dom = max(range(len(calls)), key=lambda j: per_call_ms[j])
     dom_achieved = calls[dom]["wl"].flops / (per_call_ms[dom] * 1e-3) / 1e12
+    tr = NCU_TRAFFIC.get(calls[dom]["wl"].name)
+    traffic = tr["bytes"] if tr and tr["csrc"] == csrc_hash() and \
+        (args.chunk_rows or calls[dom]["wl"].chunk_rows) == calls[dom]["wl"].chunk_rows else None
     line["roofline"] = {
         "bound": "tensor", "kernel": f"fused_gemm_kernel ({calls[dom]['op']})",
         "achieved": dom_achieved, "peak": peak, "unit": "TFLOP/s", "frac": dom_achieved / peak,
-        "traffic": None,
+        "traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read + write)",
         "peak_source": f"{pk['source']} bf16 sustained (cuBLAS, back to back under the power cap)",
         "algorithmic_flops_per_launch": calls[dom]["wl"].flops,
     }
@@ -457,7 +479,7 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
 
     # the CPU oracle on a bounded sample (rank 0, N=1 only)
     if world == 1:
-        f, s, desc = oracle_sample(ops, 2048, 1024, inputs)
+        f, s, desc = oracle_sample(ops, 1 << 30, 4096, inputs)
         out["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
                                "kind": "oracle", "sample": desc, "seconds": s}
     return out

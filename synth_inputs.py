@@ -157,8 +157,9 @@ WORKLOADS = {
     "rs_w4_m2048_n4096_k2048": Workload("rs_w4_m2048_n4096_k2048", "rs", 4, 2048, 4096, 2048, 1,
                                         "normal(0.02)", "normal(0.02)", 256),
     # Llama-70B-like TP=8 FFN pair, seed 2: activations N(0,1), weights N(0,0.02)
+    # (chunk rows: one chunk per rank, the best of the backend x chunk sweep)
     "ag_w8_m8192_n3584_k8192": Workload("ag_w8_m8192_n3584_k8192", "ag", 8, 8192, 3584, 8192, 2,
-                                        "normal(1.0)", "normal(0.02)", 256),
+                                        "normal(1.0)", "normal(0.02)", 1024),
     # (chunk rows for the ReduceScatter: one chunk per destination rank, the best of the
     # 256 / 512 / 1024 sweep)
     "rs_w8_m8192_n8192_k3584": Workload("rs_w8_m8192_n8192_k3584", "rs", 8, 8192, 8192, 3584, 2,
