@@ -66,6 +66,10 @@ def parse():
     ap.add_argument("--rank-view", type=int, default=0, help="AllGather rank whose view is computed")
     ap.add_argument("--skip-extras", action="store_true",
                     help="skip the baselines, e2e, CPU oracle and clock sampling")
+    ap.add_argument("--sweep", action="store_true",
+                    help="AllGather chunk x backend x swizzle sweep of --workload (default: the "
+                         "largest AllGather); one JSON line per point")
+    ap.add_argument("--sweep-chunks", default="64,128,256,512,2048")
     return ap.parse_args()
 
 
@@ -253,11 +257,58 @@ def peaks():
             "source": "fallback"}
 
 
+# ----------------------------------------------------------------------------- sweep
+def run_sweep(args):
+    """Chunk rows x transfer backend x swizzle on one AllGather workload (config 5 of the
+    benchmark plan): inputs generated and uploaded once, each point warmed up then timed."""
+    import torch
+
+    import tile_level_communication_gb300 as dt
+    name = args.workload if args.workload != "ffn_pair" else "ag_w8_m16384_n8192_k8192"
+    wl = WORKLOADS[name]
+    if wl.op != "ag":
+        raise SystemExit("--sweep takes an AllGather workload")
+    inp = wl.make()
+    up = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    shards = [up(x) for x in inp.shards]
+    b = up(inp.b)
+    c = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device="cuda")
+    peak = peaks()["bf16_tflops_sustained"]
+    chunks = [int(x) for x in args.sweep_chunks.split(",")]
+    ws = None
+    for cr in chunks:
+        for backend in ["copy_engine", "tma", "ldst"]:
+            for swizzle in [True, False]:
+                a = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, rank=args.rank_view,
+                                 chunk_rows=cr, swizzle=swizzle, backend=backend)
+                need = dt.workspace_size(a, dt.OP_AG)
+                if ws is None or ws.numel() < need:
+                    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+                for _ in range(max(3, args.warmup)):
+                    dt.ag_gemm(shards, b, c, ws, a)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record()
+                for _ in range(args.steps):
+                    dt.ag_gemm(shards, b, c, ws, a)
+                e1.record()
+                torch.cuda.synchronize()
+                st, info = dt.check(ws)
+                ms = e0.elapsed_time(e1) / args.steps
+                tf = wl.flops / (ms * 1e-3) / 1e12
+                print(json.dumps({"sweep": name, "chunk_rows": cr, "backend": backend,
+                                  "swizzle": swizzle, "ms": ms, "tflops": tf,
+                                  "frac_of_sustained_peak": tf / peak, "status": st}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- fused arm
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     import torch
 
     import tile_level_communication_gb300 as dt
