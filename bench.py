@@ -341,10 +341,12 @@ def main():
                              swizzle=not args.no_swizzle)
             A = [up(x) for x in inp.a]
             B = [up(x) for x in inp.b]
-            outs = [torch.empty((wl.m // wl.world_size, wl.n), dtype=torch.bfloat16, device=dev)
+            rows = wl.m // wl.world_size if wl.op == "rs" else wl.m  # AllReduce: every rank all rows
+            outs = [torch.empty((rows, wl.n), dtype=torch.bfloat16, device=dev)
                     for _ in range(wl.world_size)]
-            ws = torch.zeros(dt.workspace_size(a, dt.OP_RS), dtype=torch.uint8, device=dev)
-            calls.append(dict(op="rs", wl=wl, args=a, ins=A + B, A=A, B=B, outs=outs, ws=ws))
+            ws = torch.zeros(dt.workspace_size(a, dt.OP_RS if wl.op == "rs" else dt.OP_AR),
+                             dtype=torch.uint8, device=dev)
+            calls.append(dict(op=wl.op, wl=wl, args=a, ins=A + B, A=A, B=B, outs=outs, ws=ws))
         in_bytes += sum(t.numel() * 2 for t in calls[-1]["ins"])
         out_bytes += sum(t.numel() * 2 for t in calls[-1]["outs"])
 
@@ -352,8 +354,11 @@ def main():
         if cl["op"] == "ag":
             fn = dt.ag_gemm if fused else dt.ag_gemm_kernel_overlap
             fn(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], cl["args"])
-        else:
+        elif cl["op"] == "rs":
             fn = dt.gemm_rs if fused else dt.gemm_rs_kernel_overlap
+            fn(cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"])
+        else:
+            fn = dt.gemm_ar if fused else dt.gemm_ar_kernel_overlap
             fn(cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"])
 
     flops_step = sum(cl["wl"].flops for cl in calls)
@@ -505,7 +510,7 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
             a = torch.cat(cl["shards"], dim=0)[:256].float()
             ref = a @ cl["b"].float()
             got = cl["outs"][0][:256].float()
-        else:
+        else:  # ReduceScatter out_0 / AllReduce rank 0: rows 0..127 of the sum
             ref = sum(a_[:128].float() @ b_.float() for a_, b_ in zip(cl["A"], cl["B"]))
             got = cl["outs"][0][:128].float()
         errs.append(float((got - ref).abs().max() / ref.abs().max()))

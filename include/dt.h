@@ -76,7 +76,7 @@ typedef enum {
 
 typedef enum { DT_BF16 = 0, DT_F32 = 1 } dt_dtype;
 
-typedef enum { DT_OP_AG_GEMM = 0, DT_OP_GEMM_RS = 1 } dt_op;
+typedef enum { DT_OP_AG_GEMM = 0, DT_OP_GEMM_RS = 1, DT_OP_GEMM_AR = 2 } dt_op;
 
 /* Problem description shared by every call.  Fill with dt_args_default() first. */
 typedef struct dt_args {
@@ -156,6 +156,16 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c,
 dt_status dt_gemm_rs(const void* const* a, const void* const* b, void* const* out,
                      void* workspace, size_t ws_bytes, const dt_args* a_args, void* stream);
 
+/* Fused GEMM-AllReduce over all W virtual ranks (DITRON page, sections 4 and 5.1: GEMM-AR,
+ * the third tensor-parallel overlap kernel).  Same inputs, schedule and fixed-order running
+ * sums as dt_gemm_rs; the last fold of each unit writes its rows, rounded once, at their
+ * global row into every rank's output, so every rank receives all of S = sum_q A_q * B_q.
+ *   out : host array of W device pointers, out_r [M x N] (out_dtype), ld = ldc.  If all W
+ *         pointers are equal the result is written once.
+ * Workspace: dt_workspace_size(a, DT_OP_GEMM_AR) (the same layout as the ReduceScatter). */
+dt_status dt_gemm_ar(const void* const* a, const void* const* b, void* const* out,
+                     void* workspace, size_t ws_bytes, const dt_args* a_args, void* stream);
+
 /* Kernel-level-overlap baselines with the same arguments and results (AutoOverlap page,
  * section 2.1 / Fig. 2(b)): AG = per-chunk copies on a second stream and one launch of the
  * same GEMM per chunk, gated by events; RS = one GEMM launch per destination block writing
@@ -164,6 +174,9 @@ dt_status dt_ag_gemm_kernel_overlap(const void* const* a_shards, const void* b, 
                                     void* workspace, size_t ws_bytes, const dt_args* a,
                                     void* stream);
 dt_status dt_gemm_rs_kernel_overlap(const void* const* a, const void* const* b,
+                                    void* const* out, void* workspace, size_t ws_bytes,
+                                    const dt_args* a_args, void* stream);
+dt_status dt_gemm_ar_kernel_overlap(const void* const* a, const void* const* b,
                                     void* const* out, void* workspace, size_t ws_bytes,
                                     const dt_args* a_args, void* stream);
 

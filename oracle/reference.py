@@ -10,6 +10,7 @@ the reduced rows are scattered to their owner ranks):
 * AllGather-GEMM over W ranks: A = concat_rows(A_0, ..., A_{W-1}); C = A @ B.
 * GEMM-ReduceScatter over W ranks: P_q = A_q @ B_q (rank q holds a K slice);
   S = sum_q P_q; rank s receives rows s*M/W .. (s+1)*M/W - 1 of S.
+* GEMM-AllReduce over W ranks: the same S; every rank receives all of it.
 
 Inputs are float64 arrays holding exact bf16 values; outputs are float64.
 """
@@ -42,6 +43,22 @@ def gemm_rs(a_list, b_list):
         raise ValueError("M must be a multiple of W")
     ms = m // w
     return [s_full[s * ms:(s + 1) * ms] for s in range(w)]
+
+
+def gemm_ar(a_list, b_list):
+    """GEMM-AllReduce over W ranks: every rank receives S = sum_q A_q @ B_q (all M rows).
+
+    DITRON page, section 4 / 5.1 (GEMM-AR: GEMM followed by an AllReduce of the partial
+    products).  Returns a list of W float64 arrays, all equal to S.
+    """
+    w = len(a_list)
+    if w != len(b_list) or w < 1:
+        raise ValueError("need one A and one B per rank")
+    s_full = None
+    for q in range(w):
+        p_q = np.asarray(a_list[q], dtype=np.float64) @ np.asarray(b_list[q], dtype=np.float64)
+        s_full = p_q if s_full is None else s_full + p_q
+    return [s_full.copy() for _ in range(w)]
 
 
 def ag_gemm_entries(shards, b, rows, cols):

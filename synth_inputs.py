@@ -142,6 +142,7 @@ class Workload:
         return 2.0 * self.m * self.n * self.k * self.world_size
 
     def make(self):
+        # "rs" and "ar" (GEMM-AllReduce) take the same per-rank inputs
         if self.op == "ag":
             return make_ag_inputs(self.world_size, self.m, self.n, self.k, self.seed,
                                   self.dist_a, self.dist_b)
@@ -169,6 +170,9 @@ WORKLOADS = {
                                         "uniform", "uniform", 192),
     "rs_w6_m6000_n5120_k3000": Workload("rs_w6_m6000_n5120_k3000", "rs", 6, 6000, 5120, 3000, 3,
                                         "uniform", "uniform", 192),
+    # GEMM-AllReduce on the FFN pair's second GEMM (same inputs as the ReduceScatter)
+    "ar_w8_m8192_n8192_k3584": Workload("ar_w8_m8192_n8192_k3584", "ar", 8, 8192, 8192, 3584, 2,
+                                        "normal(1.0)", "normal(0.02)", 1024),
     # largest AllGather-GEMM (chunk/backend sweep), W=8, U[-1,1], seed 4
     "ag_w8_m16384_n8192_k8192": Workload("ag_w8_m16384_n8192_k8192", "ag", 8, 16384, 8192, 8192, 4,
                                          "uniform", "uniform", 256),

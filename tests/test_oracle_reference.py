@@ -179,6 +179,24 @@ PINS = [pin_ag_brute_force, pin_rs_brute_force, pin_ag_closed_form, pin_ag_shard
         pin_rs_row_scatter, pin_rs_k_split, pin_w1_is_plain_gemm, pin_integer_exact]
 
 
+def test_allreduce_brute_force_and_rank_copies():
+    """GEMM-AllReduce: every rank's result is the whole sum, equal (brute force) to the
+    concatenation of the ReduceScatter blocks; and integer inputs give exact sums."""
+    for seed, (w, m, n, k) in enumerate(RS_CASES):
+        inp = make_rs_inputs(w, m, n, k, seed=400 + seed)
+        a_list, b_list = _rs_f64(inp)
+        outs = reference.gemm_ar(a_list, b_list)
+        want = np.concatenate(_brute_rs(a_list, b_list), axis=0)
+        assert len(outs) == w
+        assert all(_close(o, want) for o in outs)
+    rng = np.random.Generator(np.random.PCG64(12))
+    a_list = [rng.integers(-5, 6, (6, 3)).astype(np.float64) for _ in range(3)]
+    b_list = [rng.integers(-5, 6, (3, 4)).astype(np.float64) for _ in range(3)]
+    exact = sum(np.array([[sum(int(a[i, t]) * int(b[t, c]) for t in range(3)) for c in range(4)]
+                          for i in range(6)], dtype=np.float64) for a, b in zip(a_list, b_list))
+    assert all(np.array_equal(o, exact) for o in reference.gemm_ar(a_list, b_list))
+
+
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
 def test_oracle_pin(pin):
     assert pin(reference.ag_gemm, reference.gemm_rs)

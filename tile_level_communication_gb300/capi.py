@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libdt.so")
 DT_OK, DT_ERR_INVALID, DT_ERR_UNSUPPORTED, DT_ERR_TIMEOUT, DT_ERR_CUDA, DT_ERR_WORKSPACE = range(6)
 BACKENDS = {"auto": 0, "copy_engine": 1, "tma": 2, "ldst": 3}
 DTYPES = {"bf16": 0, "f32": 1}
-OP_AG, OP_RS = 0, 1
+OP_AG, OP_RS, OP_AR = 0, 1, 2
 MAX_WORLD = 16
 
 # every function include/dt.h declares: name -> (restype, argtypes)
@@ -36,6 +36,8 @@ _SIGS = {
     "dt_gemm_rs": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_ag_gemm_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_gemm_rs_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_gemm_ar": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_gemm_ar_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_swizzle_plan": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64]),
     "dt_swizzle_plan_device": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64, _P]),
     "dt_check": (ctypes.c_int, [_P, _P, _P]),
@@ -176,6 +178,21 @@ def ag_gemm_static_scratch(shards, b, c, args: DtArgs, stream=None):
                                            ctypes.byref(args), _stream(stream)))
 
 
+def gemm_ar(a_list, b_list, out_list, workspace, args: DtArgs, stream=None, ws_bytes=None):
+    """Fused GEMM-AllReduce: out_list[r] ([M, N]) receives sum_q A_q @ B_q for every r."""
+    _raise(lib().dt_gemm_ar(_ptr_array(a_list), _ptr_array(b_list), _ptr_array(out_list),
+                            _ptr(workspace), _nbytes(workspace, ws_bytes), ctypes.byref(args),
+                            _stream(stream)))
+
+
+def gemm_ar_kernel_overlap(a_list, b_list, out_list, workspace, args: DtArgs, stream=None,
+                           ws_bytes=None):
+    _raise(lib().dt_gemm_ar_kernel_overlap(_ptr_array(a_list), _ptr_array(b_list),
+                                           _ptr_array(out_list), _ptr(workspace),
+                                           _nbytes(workspace, ws_bytes), ctypes.byref(args),
+                                           _stream(stream)))
+
+
 def ag_gemm_kernel_overlap(shards, b, c, workspace, args: DtArgs, stream=None, ws_bytes=None):
     _raise(lib().dt_ag_gemm_kernel_overlap(_ptr_array(shards), _ptr(b), _ptr(c), _ptr(workspace),
                                            _nbytes(workspace, ws_bytes), ctypes.byref(args),
@@ -193,7 +210,7 @@ def gemm_rs_kernel_overlap(a_list, b_list, out_list, workspace, args: DtArgs, st
 def tile_count(args: DtArgs, op: int) -> int:
     tm = -(-args.m // 128)
     tn = -(-args.n // 256)
-    return (1 if op == OP_AG else args.world_size) * tm * tn
+    return (1 if op == OP_AG else args.world_size) * tm * tn  # RS and AR: all W ranks' tiles
 
 
 def swizzle_plan(args: DtArgs, op: int) -> np.ndarray:

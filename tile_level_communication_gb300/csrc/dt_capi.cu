@@ -121,7 +121,8 @@ uint64_t default_timeout_ns() {
 
 dt_status derive(const dt_args* a, int op, Derived* d) {
   if (!a) return fail(DT_ERR_INVALID, "args is NULL");
-  if (op != DT_OP_AG_GEMM && op != DT_OP_GEMM_RS) return fail(DT_ERR_INVALID, "unknown op %d", op);
+  if (op != DT_OP_AG_GEMM && op != DT_OP_GEMM_RS && op != DT_OP_GEMM_AR)
+    return fail(DT_ERR_INVALID, "unknown op %d", op);
   d->op = op;
   d->W = a->world_size;
   if (d->W < 1 || d->W > DT_MAX_WORLD)
@@ -129,7 +130,7 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   d->rank = a->rank;
   if (op == DT_OP_AG_GEMM && (d->rank < 0 || d->rank >= d->W))
     return fail(DT_ERR_INVALID, "rank %d outside 0..%d", d->rank, d->W - 1);
-  if (op == DT_OP_GEMM_RS) d->rank = 0;
+  if (op != DT_OP_AG_GEMM) d->rank = 0;
   d->M = a->m;
   d->N = a->n;
   d->K = a->k;
@@ -167,7 +168,7 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   const int64_t T64 = (op == DT_OP_AG_GEMM ? 1 : d->W) * static_cast<int64_t>(d->Tm) * d->Tn;
   if (T64 >= (1ll << 31)) return fail(DT_ERR_UNSUPPORTED, "too many tiles");
   d->T = static_cast<int32_t>(T64);
-  if (op == DT_OP_GEMM_RS && static_cast<int64_t>(d->W - 1) * d->M >= (1ll << 31))
+  if (op != DT_OP_AG_GEMM && static_cast<int64_t>(d->W - 1) * d->M >= (1ll << 31))
     return fail(DT_ERR_UNSUPPORTED, "(W-1)*M must be below 2^31");
   if (static_cast<int64_t>(d->W) * d->nC >= (1ll << 24))
     return fail(DT_ERR_UNSUPPORTED, "too many chunks; raise chunk_rows");
@@ -330,8 +331,14 @@ __global__ void zero_rows_kernel(uint8_t* dst, int64_t rows, int64_t row_bytes, 
 
 // out_s = the fp32 partial slots recv[s][q] summed in the fused path's fixed order: source
 // q_d = (s - d - 1) mod W for d = 0..W-1 (rank s-1 first, s itself last)
+struct OutRows {
+  void* p[DT_MAX_WORLD];  // ReduceScatter: out_s; AllReduce: every rank's output
+  int32_t n;
+  int64_t row0;            // first output row of this destination block
+};
+
 __global__ void reduce_slots_kernel(const float* recv, int32_t W, int64_t Ms, int64_t N, int32_t s,
-                                    void* out, int64_t ldc, int f32) {
+                                    OutRows out, int64_t ldc, int f32) {
   const int64_t nv = N / 4;
   const size_t slot = static_cast<size_t>(Ms) * N;
   const float* base = recv + static_cast<size_t>(s) * W * slot;
@@ -348,15 +355,17 @@ __global__ void reduce_slots_kernel(const float* recv, int32_t W, int64_t Ms, in
       acc.z += x.z;
       acc.w += x.w;
     }
-    if (f32) {
-      reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + r * ldc)[v] = acc;
-    } else {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 w;
-      w.x = *reinterpret_cast<uint32_t*>(&lo);
-      w.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + r * ldc)[v] = w;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&lo);
+    w.y = *reinterpret_cast<uint32_t*>(&hi);
+    for (int32_t c = 0; c < out.n; ++c) {
+      const int64_t row = out.row0 + r;
+      if (f32)
+        reinterpret_cast<float4*>(reinterpret_cast<float*>(out.p[c]) + row * ldc)[v] = acc;
+      else
+        reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out.p[c]) + row * ldc)[v] = w;
     }
   }
 }
@@ -749,10 +758,10 @@ dt_status dt_ag_gemm_kernel_overlap(const void* const* a_shards, const void* b, 
   return DT_OK;
 }
 
-// ------------------------------------------------------------------------------ ReduceScatter
+// ------------------------------------------------------------------------------ ReduceScatter / AllReduce
 static dt_status rs_common(const void* const* a_, const void* const* b_, void* const* out, void* ws,
-                           size_t ws_bytes, const dt_args* a, Derived* d) {
-  dt_status s = derive(a, DT_OP_GEMM_RS, d);
+                           size_t ws_bytes, const dt_args* a, int op, Derived* d) {
+  dt_status s = derive(a, op, d);
   if (s != DT_OK) return s;
   if (!a_ || !b_ || !out) return fail(DT_ERR_INVALID, "a, b and out arrays must be non-NULL");
   if (d->M == 0 || d->N == 0) return DT_OK;
@@ -765,6 +774,13 @@ static dt_status rs_common(const void* const* a_, const void* const* b_, void* c
   return check_ws(*d, ws, ws_bytes);
 }
 
+// AllReduce: one output copy when every rank's pointer is the same buffer, else W
+static int32_t ar_copies_of(const Derived& d, void* const* out) {
+  for (int i = 1; i < d.W; ++i)
+    if (out[i] != out[0]) return d.W;
+  return 1;
+}
+
 static dt_status rs_params(KParams& p, const Derived& d, const void* const* a_,
                            const void* const* b_, void* const* out, void* ws, uint32_t epoch) {
   fill_common(p, d, ws, epoch);
@@ -772,6 +788,7 @@ static dt_status rs_params(KParams& p, const Derived& d, const void* const* a_,
   p.recv = reinterpret_cast<float*>(w + d.off_data);
   p.unit_cnt = reinterpret_cast<uint32_t*>(w + d.off_cnt);
   p.pieces_max = d.pieces_max;
+  p.ar_copies = d.op == DT_OP_GEMM_AR ? ar_copies_of(d, out) : 0;
   // running sums [M][N] fp32 and park slots [W (W-1) Ms][N] fp32, moved in 32 x 128 boxes
   dt_status st = make_tmap(&p.tmAcc, p.recv, d.N, d.M, d.N * 4, 32, kBM, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
   if (st != DT_OK) return st;
@@ -793,19 +810,25 @@ static dt_status rs_params(KParams& p, const Derived& d, const void* const* a_,
   return DT_OK;
 }
 
-dt_status dt_gemm_rs(const void* const* a_, const void* const* b_, void* const* out, void* ws,
-                     size_t ws_bytes, const dt_args* a, void* stream_) {
+static dt_status zero_reduce_outputs(const Derived& d, void* const* out, cudaStream_t stream) {
+  const int64_t eb = d.f32 ? 4 : 2;
+  const bool ar = d.op == DT_OP_GEMM_AR;
+  const int n = ar ? ar_copies_of(d, out) : d.W;
+  for (int q = 0; q < n; ++q) {
+    const dt_status s = launch_zero(out[q], ar ? d.M : d.Ms, d.N * eb, d.ldc * eb, stream);
+    if (s != DT_OK) return s;
+  }
+  return DT_OK;
+}
+
+static dt_status reduce_fused(const void* const* a_, const void* const* b_, void* const* out,
+                              void* ws, size_t ws_bytes, const dt_args* a, void* stream_, int op) {
   g_last_error.clear();
   Derived d;
-  dt_status s = rs_common(a_, b_, out, ws, ws_bytes, a, &d);
+  dt_status s = rs_common(a_, b_, out, ws, ws_bytes, a, op, &d);
   if (s != DT_OK || d.M == 0 || d.N == 0) return s;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  const int64_t eb = d.f32 ? 4 : 2;
-  if (d.K == 0) {
-    for (int q = 0; q < d.W; ++q)
-      if ((s = launch_zero(out[q], d.Ms, d.N * eb, d.ldc * eb, stream)) != DT_OK) return s;
-    return DT_OK;
-  }
+  if (d.K == 0) return zero_reduce_outputs(d, out, stream);
   DevCtx* dev = nullptr;
   if ((s = dev_ctx(&dev)) != DT_OK) return s;
   uint32_t epoch = 0;
@@ -815,29 +838,26 @@ dt_status dt_gemm_rs(const void* const* a_, const void* const* b_, void* const* 
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
   const int grid = static_cast<int>(std::min<int64_t>(d.T, sms));
   cudaError_t e = launch_rs_kernel(p, d.f32, grid, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "fused GEMM-ReduceScatter launch");
+  if (e != cudaSuccess) return cuda_fail(e, "fused GEMM-ReduceScatter / AllReduce launch");
   return DT_OK;
 }
 
-dt_status dt_gemm_rs_kernel_overlap(const void* const* a_, const void* const* b_, void* const* out,
-                                    void* ws, size_t ws_bytes, const dt_args* a, void* stream_) {
+static dt_status reduce_kernel_overlap(const void* const* a_, const void* const* b_,
+                                       void* const* out, void* ws, size_t ws_bytes,
+                                       const dt_args* a, void* stream_, int op) {
   g_last_error.clear();
   Derived d;
-  dt_status s = rs_common(a_, b_, out, ws, ws_bytes, a, &d);
+  dt_status s = rs_common(a_, b_, out, ws, ws_bytes, a, op, &d);
   if (s != DT_OK || d.M == 0 || d.N == 0) return s;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  const int64_t eb = d.f32 ? 4 : 2;
-  if (d.K == 0) {
-    for (int q = 0; q < d.W; ++q)
-      if ((s = launch_zero(out[q], d.Ms, d.N * eb, d.ldc * eb, stream)) != DT_OK) return s;
-    return DT_OK;
-  }
+  if (d.K == 0) return zero_reduce_outputs(d, out, stream);
   DevCtx* dev = nullptr;
   if ((s = dev_ctx(&dev)) != DT_OK) return s;
   KParams p;
   if ((s = rs_params(p, d, a_, b_, out, ws, 0)) != DT_OK) return s;
   p.tag = nullptr;
   p.plain = 1;
+  const bool ar = op == DT_OP_GEMM_AR;
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   while (static_cast<int32_t>(dev->chunk_events.size()) < d.W) {
@@ -858,15 +878,46 @@ dt_status dt_gemm_rs_kernel_overlap(const void* const* a_, const void* const* b_
     DT_CUDA(cudaEventRecord(dev->chunk_events[st], stream));
     DT_CUDA(cudaStreamWaitEvent(dev->side, dev->chunk_events[st], 0));
     // the reduction of block st runs on the second stream
+    OutRows rows;
+    memset(&rows, 0, sizeof(rows));
+    if (ar) {
+      rows.n = p.ar_copies;
+      for (int c = 0; c < rows.n; ++c) rows.p[c] = out[c];
+      rows.row0 = static_cast<int64_t>(st) * d.Ms;
+    } else {
+      rows.n = 1;
+      rows.p[0] = out[st];
+      rows.row0 = 0;
+    }
     const int64_t work = d.Ms * (d.N / 4);
     const int rgrid = static_cast<int>(std::min<int64_t>(cdiv64(work, 256), 2 * sms));
-    reduce_slots_kernel<<<rgrid, 256, 0, dev->side>>>(recv, d.W, d.Ms, d.N, st, out[st], d.ldc,
+    reduce_slots_kernel<<<rgrid, 256, 0, dev->side>>>(recv, d.W, d.Ms, d.N, st, rows, d.ldc,
                                                       d.f32 ? 1 : 0);
     DT_CUDA(cudaGetLastError());
   }
   DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
   DT_CUDA(cudaStreamWaitEvent(stream, dev->ev_done, 0));
   return DT_OK;
+}
+
+dt_status dt_gemm_rs(const void* const* a_, const void* const* b_, void* const* out, void* ws,
+                     size_t ws_bytes, const dt_args* a, void* stream) {
+  return reduce_fused(a_, b_, out, ws, ws_bytes, a, stream, DT_OP_GEMM_RS);
+}
+
+dt_status dt_gemm_ar(const void* const* a_, const void* const* b_, void* const* out, void* ws,
+                     size_t ws_bytes, const dt_args* a, void* stream) {
+  return reduce_fused(a_, b_, out, ws, ws_bytes, a, stream, DT_OP_GEMM_AR);
+}
+
+dt_status dt_gemm_rs_kernel_overlap(const void* const* a_, const void* const* b_, void* const* out,
+                                    void* ws, size_t ws_bytes, const dt_args* a, void* stream) {
+  return reduce_kernel_overlap(a_, b_, out, ws, ws_bytes, a, stream, DT_OP_GEMM_RS);
+}
+
+dt_status dt_gemm_ar_kernel_overlap(const void* const* a_, const void* const* b_, void* const* out,
+                                    void* ws, size_t ws_bytes, const dt_args* a, void* stream) {
+  return reduce_kernel_overlap(a_, b_, out, ws, ws_bytes, a, stream, DT_OP_GEMM_AR);
 }
 
 dt_status dt_debug_drop_transfer(int32_t step) {

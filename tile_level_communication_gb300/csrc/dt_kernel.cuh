@@ -66,7 +66,7 @@ struct KParams {
   CUtensorMap tmAcc;       // RS: running sums, fp32 [M][N], 32 x 128 boxes
   CUtensorMap tmPark;      // RS: park slots, fp32 [W (W-1) M/W][N], 32 x 128 boxes
   const uint8_t* shard[kMaxW];
-  void* out[kMaxW];        // AG: out[0] = C; RS: out[s]
+  void* out[kMaxW];        // AG: out[0] = C; RS: out[s] ([M/W][N]); AR: out[r] ([M][N])
   uint8_t* gather;
   float* recv;             // RS: W x W x Ms x N fp32 partial slots, [dest][src]
   uint32_t* ready;         // AG: per chunk, = epoch once landed
@@ -83,6 +83,7 @@ struct KParams {
   int64_t row_lo, row_hi;  // rows handled: [0, M) fused; one window in the baselines
   int32_t Tm, KB, T;       // m-tiles in the window, k-blocks, tiles in the launch
   int32_t pieces_max;      // RS: most chunks one m-tile's rows touch (counter stride)
+  int32_t ar_copies;       // 0: ReduceScatter; > 0: AllReduce into out[0 .. ar_copies-1]
   int32_t plain;           // 1: identity order, no flags, no arrival counting
   int32_t wait_flags;      // AG: the producer waits on ready flags
   uint32_t epoch;
@@ -364,20 +365,46 @@ __device__ __forceinline__ float* park_ptr(const KParams& p, int32_t s, int32_t 
          (slot * p.g.Ms + lr) * static_cast<size_t>(p.g.N) + col;
 }
 
+// Final result of 8 columns of row lr of destination s: into out_s (ReduceScatter), or at
+// global row s*Ms + lr into every rank's output (AllReduce).
 template <bool F32>
 __device__ __forceinline__ void store_out8(const KParams& p, int32_t s, int64_t lr, int64_t col,
                                            const float (&a)[8]) {
-  if (F32) {
-    float* dst = reinterpret_cast<float*>(p.out[s]) + lr * p.ldc + col;
-    reinterpret_cast<float4*>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
-    reinterpret_cast<float4*>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
-  } else {
-    uint4 w;
+  const int ncopy = p.ar_copies > 0 ? p.ar_copies : 1;
+  const int64_t row = p.ar_copies > 0 ? static_cast<int64_t>(s) * p.g.Ms + lr : lr;
+  uint4 w;
+  if (!F32) {
     w.x = pack_bf16x2(__float_as_uint(a[0]), __float_as_uint(a[1]));
     w.y = pack_bf16x2(__float_as_uint(a[2]), __float_as_uint(a[3]));
     w.z = pack_bf16x2(__float_as_uint(a[4]), __float_as_uint(a[5]));
     w.w = pack_bf16x2(__float_as_uint(a[6]), __float_as_uint(a[7]));
-    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out[s]) + lr * p.ldc + col) = w;
+  }
+  for (int r = 0; r < ncopy; ++r) {
+    void* out = p.out[p.ar_copies > 0 ? r : s];
+    if (F32) {
+      float* dst = reinterpret_cast<float*>(out) + row * p.ldc + col;
+      reinterpret_cast<float4*>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
+    } else {
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + row * p.ldc + col) = w;
+    }
+  }
+}
+template <bool F32>
+__device__ __forceinline__ void store_out4(const KParams& p, int32_t s, int64_t lr, int64_t col,
+                                           const float4& r4) {
+  const int ncopy = p.ar_copies > 0 ? p.ar_copies : 1;
+  const int64_t row = p.ar_copies > 0 ? static_cast<int64_t>(s) * p.g.Ms + lr : lr;
+  for (int r = 0; r < ncopy; ++r) {
+    void* out = p.out[p.ar_copies > 0 ? r : s];
+    if (F32) {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * p.ldc + col) = r4;
+    } else {
+      uint2 w;
+      w.x = pack_bf16x2(__float_as_uint(r4.x), __float_as_uint(r4.y));
+      w.y = pack_bf16x2(__float_as_uint(r4.z), __float_as_uint(r4.w));
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + row * p.ldc + col) = w;
+    }
   }
 }
 
@@ -431,14 +458,7 @@ __device__ void fold_parked(const KParams& p, int32_t s, int64_t lo, int64_t hi,
     const float4 b = ldcg_f4(park_ptr(p, s, e, lr, col));
     const float4 r4 = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
     if (e == p.g.W - 1) {
-      if (F32) {
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out[s]) + lr * p.ldc + col) = r4;
-      } else {
-        uint2 w;
-        w.x = pack_bf16x2(__float_as_uint(r4.x), __float_as_uint(r4.y));
-        w.y = pack_bf16x2(__float_as_uint(r4.z), __float_as_uint(r4.w));
-        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out[s]) + lr * p.ldc + col) = w;
-      }
+      store_out4<F32>(p, s, lr, col, r4);
     } else {
       *reinterpret_cast<float4*>(acc_ptr(p, row, col)) = r4;
     }
