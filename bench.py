@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--rank-view", type=int, default=0, help="AllGather rank whose view is computed")
     ap.add_argument("--skip-extras", action="store_true",
                     help="skip the baselines, e2e, CPU oracle and clock sampling")
+    ap.add_argument("--no-tune", action="store_true",
+                    help="skip the enumerate-and-measure tuner and use the workload's knobs")
     ap.add_argument("--sweep", action="store_true",
                     help="AllGather chunk x backend x swizzle sweep of --workload (default: the "
                          "largest AllGather); one JSON line per point")
@@ -333,7 +335,9 @@ def main():
             shards = [up(s) for s in inp.shards]
             b = up(inp.b)
             c = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device=dev)
-            ws = torch.zeros(dt.workspace_size(a, dt.OP_AG), dtype=torch.uint8, device=dev)
+            probe = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=64)
+            need = max(dt.workspace_size(a, dt.OP_AG), dt.workspace_size(probe, dt.OP_AG))
+            ws = torch.zeros(need, dtype=torch.uint8, device=dev)
             calls.append(dict(op="ag", wl=wl, args=a, ins=shards + [b], shards=shards, b=b,
                               outs=[c], ws=ws))
         else:
@@ -344,8 +348,10 @@ def main():
             rows = wl.m // wl.world_size if wl.op == "rs" else wl.m  # AllReduce: every rank all rows
             outs = [torch.empty((rows, wl.n), dtype=torch.bfloat16, device=dev)
                     for _ in range(wl.world_size)]
-            ws = torch.zeros(dt.workspace_size(a, dt.OP_RS if wl.op == "rs" else dt.OP_AR),
-                             dtype=torch.uint8, device=dev)
+            op_id = dt.OP_RS if wl.op == "rs" else dt.OP_AR
+            probe = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=64)
+            need = max(dt.workspace_size(a, op_id), dt.workspace_size(probe, op_id))
+            ws = torch.zeros(need, dtype=torch.uint8, device=dev)
             calls.append(dict(op=wl.op, wl=wl, args=a, ins=A + B, A=A, B=B, outs=outs, ws=ws))
         in_bytes += sum(t.numel() * 2 for t in calls[-1]["ins"])
         out_bytes += sum(t.numel() * 2 for t in calls[-1]["outs"])
@@ -363,6 +369,21 @@ def main():
 
     flops_step = sum(cl["wl"].flops for cl in calls)
     stream = torch.cuda.current_stream(dev)
+
+    # enumerate-and-measure tuning of every call's knobs (not timed)
+    tuned = {}
+    if not args.no_tune and args.chunk_rows == 0 and args.backend == "auto":
+        for cl in calls:
+            if cl["op"] == "ag":
+                pts = dt.tune_ag_gemm(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], cl["args"])
+            else:
+                pts = dt.tune_reduce(dt.OP_RS if cl["op"] == "rs" else dt.OP_AR, cl["A"], cl["B"],
+                                     cl["outs"], cl["ws"], cl["args"])
+            a = cl["args"]
+            tuned[cl["op"]] = {"chunk_rows": int(a.chunk_rows),
+                               "backend": [k for k, v in dt.BACKENDS.items() if v == a.backend][0],
+                               "copy_ctas": int(a.copy_ctas), "group": int(a.group),
+                               "candidates": len(pts)}
 
     # warm-up (also writes each workspace's tile order once)
     for _ in range(max(3, args.warmup)):
@@ -425,7 +446,10 @@ def main():
         "l2": f"inputs larger than L2: {in_bytes / 2**20:.0f} MiB read per step vs "
               f"{L2_BYTES / 2**20:.0f} MiB L2",
         "accumulate": "fp32", "out_dtype": "bf16",
+        "tuned": tuned or None,
     })
+    for op_name, t in tuned.items():
+        line["config"][op_name]["chunk_rows"] = t["chunk_rows"]
     pk = peaks()
     peak = pk["bf16_tflops_sustained"]
     line["frac_of_peak"] = value / world / peak
@@ -435,8 +459,9 @@ def main():
     dom = max(range(len(calls)), key=lambda j: per_call_ms[j])
     dom_achieved = calls[dom]["wl"].flops / (per_call_ms[dom] * 1e-3) / 1e12
     tr = NCU_TRAFFIC.get(calls[dom]["wl"].name)
+    used = calls[dom]["args"]  # the knobs actually timed (after tuning)
     traffic = tr["bytes"] if tr and tr["csrc"] == csrc_hash() and \
-        (args.chunk_rows or calls[dom]["wl"].chunk_rows) == calls[dom]["wl"].chunk_rows else None
+        used.chunk_rows == calls[dom]["wl"].chunk_rows and used.group == 8 else None
     line["roofline"] = {
         "bound": "tensor", "kernel": f"fused_gemm_kernel ({calls[dom]['op']})",
         "achieved": dom_achieved, "peak": peak, "unit": "TFLOP/s", "frac": dom_achieved / peak,

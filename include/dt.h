@@ -98,7 +98,9 @@ typedef struct dt_args {
   int64_t ldc;         /* of C / every out_s                     (0 = N)                   */
   int64_t timeout_us;  /* bound of every device wait; 0 = 2 s (env DT_WAIT_TIMEOUT_US)     */
   int32_t num_sms;     /* persistent grid size; 0 = all SMs                                */
-  int32_t reserved;
+  int32_t copy_ctas;   /* AG with DT_XFER_TMA / DT_XFER_LDST: CTAs of the grid that only move
+                          chunks (dedicated SMs); 0 = transfer warps inside every compute CTA
+                          (co-located).  AutoOverlap page section 5.3, lowerings 2-5.        */
 } dt_args;
 
 /* Fill `a` with defaults: W=1, rank 0, swizzle on, AUTO backend, bf16 output, 128x256
@@ -220,6 +222,38 @@ dt_status dt_check(void* workspace, void* stream, uint32_t* info);
  * The pages have no counterpart of this entry point. */
 dt_status dt_ag_gemm_static_scratch(const void* const* a_shards, const void* b, void* c,
                                     const dt_args* a, void* stream);
+
+/* One candidate of the tuner: its knobs, mean time per call (ms, < 0 if it did not run) and
+ * the status of its calls. */
+typedef struct dt_tune_point {
+  int64_t chunk_rows;
+  int32_t backend;    /* dt_xfer as requested (AllGather)       */
+  int32_t copy_ctas;
+  int32_t swizzle;
+  int32_t group;
+  float ms;
+  int32_t status;     /* dt_status of the candidate's calls      */
+} dt_tune_point;
+
+/* Enumerate-and-measure tuner (AutoOverlap page, section 6: the inter-chunk tuner picks chunk
+ * size / split factor, the intra-chunk tuner the transfer backend, the SMs given to
+ * communication and the tile order, all by measuring the generated variants).
+ * AllGather-GEMM candidates: chunk rows {64 .. 4096, M/W} x {copy engine (when the chunk count
+ * stays <= 512), TMA and ld/st with co-located transfer warps, TMA and ld/st on 8 or 16
+ * dedicated CTAs}; then group widths {4, 16} around the best.  Reduce candidates
+ * (op DT_OP_GEMM_RS or DT_OP_GEMM_AR): chunk rows x group widths.  Each candidate runs once as
+ * warm-up and `reps` times timed with CUDA events on `stream` (synchronising); candidates
+ * whose workspace exceeds ws_bytes are skipped.  The fastest knobs are written into *a
+ * (chunk_rows, backend, copy_ctas, group; swizzle stays on).  `points` (may be NULL) receives
+ * up to max_points candidates and *n_points their number.  The inputs are read and the
+ * outputs written by every candidate; all candidates give bit-identical outputs. */
+dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, void* workspace,
+                          size_t ws_bytes, dt_args* a, int32_t reps, dt_tune_point* points,
+                          int32_t max_points, int32_t* n_points, void* stream);
+dt_status dt_tune_reduce(int op, const void* const* a, const void* const* b, void* const* out,
+                         void* workspace, size_t ws_bytes, dt_args* a_args, int32_t reps,
+                         dt_tune_point* points, int32_t max_points, int32_t* n_points,
+                         void* stream);
 
 /* Failure-detection testing, host side only: the next copy-engine AllGather-GEMM call on
  * this process leaves out the copy and the ready-flag write of transfer step `step` (the

@@ -205,3 +205,39 @@ def test_full_size_sampled(dt, name, backend, chunk):
     # the tolerance scale is the largest |C| over the sample
     assert_close(got.cpu().numpy(), ref, "bf16", name)
     assert torch.isfinite(c.float()).all()
+
+
+@pytest.mark.parametrize("backend", ["tma", "ldst"])
+@pytest.mark.parametrize("copy_ctas", [1, 8, 16])
+def test_dedicated_transfer_ctas(dt, small, ragged, backend, copy_ctas):
+    """CTAs that only move chunks (dedicated SMs) give the same bits as co-located warps."""
+    for wl, inp, ref in (small, ragged):
+        base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, backend=backend, rank=1)
+        c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, backend=backend, rank=1,
+                 copy_ctas=copy_ctas)
+        assert_close(to_f64(c), ref, "bf16", f"{backend} dedicated {copy_ctas}")
+        assert bits_equal(c, base)
+
+
+def test_tuner_picks_a_measured_candidate_with_identical_output(dt, ragged):
+    wl, inp, ref = ragged
+    args = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, rank=2, chunk_rows=wl.chunk_rows)
+    shards = [dev_bf16(s) for s in inp.shards]
+    b = dev_bf16(inp.b)
+    c = out_tensor(wl.m, wl.n, "bf16")
+    probe = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, rank=2, chunk_rows=64)
+    ws = workspace(max(dt.workspace_size(probe, dt.OP_AG), dt.workspace_size(args, dt.OP_AG)))
+    pts = dt.tune_ag_gemm(shards, b, c, ws, args, reps=2)
+    ran = [p for p in pts if p["status"] == 0 and p["ms"] > 0]
+    assert len(ran) >= 10
+    best = min(ran, key=lambda p: p["ms"])
+    assert (args.chunk_rows, args.copy_ctas, args.group) == (best["chunk_rows"], best["copy_ctas"],
+                                                             best["group"])
+    assert {p["backend"] for p in ran} >= {"tma", "ldst", "copy_engine"}
+    assert any(p["copy_ctas"] > 0 for p in ran)
+    tuned = out_tensor(wl.m, wl.n, "bf16")
+    dt.ag_gemm(shards, b, tuned, ws, args)
+    assert dt.check(ws)[0] == 0
+    assert_close(to_f64(tuned), ref, "bf16", "tuned")
+    default = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, rank=2)
+    assert bits_equal(tuned, default)

@@ -169,3 +169,22 @@ def test_full_size_sampled(dt):
     got = np.array([float(outs[int(d)][int(r), int(c)].float()) for d, r, c in zip(dest, rows, cols)])
     assert_close(got, ref, "bf16", "rs full")
     assert all(torch.isfinite(o.float()).all() for o in outs)
+
+
+def test_tuner_reduce_identical_output(dt, w4):
+    wl, inp, ref = w4
+    args = dt.make_args(4, wl.m, wl.n, wl.k, chunk_rows=256)
+    a = [dev_bf16(x) for x in inp.a]
+    b = [dev_bf16(x) for x in inp.b]
+    outs = [out_tensor(wl.m // 4, wl.n, "bf16") for _ in range(4)]
+    probe = dt.make_args(4, wl.m, wl.n, wl.k, chunk_rows=64)
+    ws = workspace(max(dt.workspace_size(probe, dt.OP_RS), dt.workspace_size(args, dt.OP_RS)))
+    pts = dt.tune_reduce(dt.OP_RS, a, b, outs, ws, args, reps=2)
+    ran = [p for p in pts if p["status"] == 0 and p["ms"] > 0]
+    assert len(ran) >= 9 and args.chunk_rows in {p["chunk_rows"] for p in ran}
+    tuned = [out_tensor(wl.m // 4, wl.n, "bf16") for _ in range(4)]
+    dt.gemm_rs(a, b, tuned, ws, args)
+    assert dt.check(ws)[0] == 0
+    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256)
+    assert all(bits_equal(t, x) for t, x in zip(tuned, base))
+    _check_all(tuned, ref, "bf16", what="tuned")

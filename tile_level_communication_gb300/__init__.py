@@ -8,4 +8,5 @@ from .capi import (BACKENDS, OP_AG, OP_AR, OP_RS, DtArgs, DtError, ag_gemm,  # n
                    ag_gemm_static_scratch,
                    ag_gemm_kernel_overlap, check, debug_drop_transfer, gemm_ar,
                    gemm_ar_kernel_overlap, gemm_rs, gemm_rs_kernel_overlap, make_args,
-                   swizzle_plan, swizzle_plan_device, tile_count, workspace_init, workspace_size)
+                   swizzle_plan, swizzle_plan_device, tile_count, tune_ag_gemm, tune_reduce,
+                   workspace_init, workspace_size)

@@ -43,6 +43,10 @@ _SIGS = {
     "dt_check": (ctypes.c_int, [_P, _P, _P]),
     "dt_debug_drop_transfer": (ctypes.c_int, [ctypes.c_int32]),
     "dt_ag_gemm_static_scratch": (ctypes.c_int, [_P, _P, _P, _P, _P]),
+    "dt_tune_ag_gemm": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_int32, _P,
+                                       ctypes.c_int32, _P, _P]),
+    "dt_tune_reduce": (ctypes.c_int, [ctypes.c_int, _P, _P, _P, _P, ctypes.c_size_t, _P,
+                                      ctypes.c_int32, _P, ctypes.c_int32, _P, _P]),
 }
 STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 
@@ -57,8 +61,15 @@ class DtArgs(ctypes.Structure):
         ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("group", ctypes.c_int32),
         ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
         ("timeout_us", ctypes.c_int64),
-        ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32), ("copy_ctas", ctypes.c_int32),
     ]
+
+
+class DtTunePoint(ctypes.Structure):
+    """Mirror of ``dt_tune_point``."""
+    _fields_ = [("chunk_rows", ctypes.c_int64), ("backend", ctypes.c_int32),
+                ("copy_ctas", ctypes.c_int32), ("swizzle", ctypes.c_int32),
+                ("group", ctypes.c_int32), ("ms", ctypes.c_float), ("status", ctypes.c_int32)]
 
 
 class DtError(RuntimeError):
@@ -128,7 +139,7 @@ def _ptr_array(xs):
 def make_args(world_size: int, m: int, n: int, k: int, *, rank: int = 0, chunk_rows: int = 128,
               swizzle: bool = True, backend: str = "auto", out_dtype: str = "bf16",
               lda: int = 0, ldb: int = 0, ldc: int = 0, timeout_us: int = 0, num_sms: int = 0,
-              group: int = 8) -> DtArgs:
+              group: int = 8, copy_ctas: int = 0) -> DtArgs:
     a = DtArgs()
     lib().dt_args_default(ctypes.byref(a))
     a.world_size, a.rank, a.m, a.n, a.k = world_size, rank, m, n, k
@@ -140,6 +151,7 @@ def make_args(world_size: int, m: int, n: int, k: int, *, rank: int = 0, chunk_r
     a.timeout_us = timeout_us
     a.num_sms = num_sms
     a.group = group
+    a.copy_ctas = copy_ctas
     return a
 
 
@@ -225,6 +237,37 @@ def swizzle_plan_device(args: DtArgs, op: int, order_dev, stream=None):
     """Device evaluation into ``order_dev`` (int32 device buffer of tile_count entries)."""
     _raise(lib().dt_swizzle_plan_device(ctypes.byref(args), op, _ptr(order_dev),
                                         tile_count(args, op), _stream(stream)))
+
+
+_BACKEND_NAMES = {v: k for k, v in BACKENDS.items()}
+
+
+def _points(buf, n):
+    return [dict(chunk_rows=int(p.chunk_rows), backend=_BACKEND_NAMES.get(p.backend, p.backend),
+                 copy_ctas=int(p.copy_ctas), swizzle=bool(p.swizzle), group=int(p.group),
+                 ms=float(p.ms), status=int(p.status)) for p in buf[:n]]
+
+
+def tune_ag_gemm(shards, b, c, workspace, args: DtArgs, reps: int = 3, stream=None,
+                 ws_bytes=None, max_points: int = 128):
+    """Enumerate-and-measure tuner; writes the fastest knobs into `args`, returns the points."""
+    buf = (DtTunePoint * max_points)()
+    n = ctypes.c_int32(0)
+    _raise(lib().dt_tune_ag_gemm(_ptr_array(shards), _ptr(b), _ptr(c), _ptr(workspace),
+                                 _nbytes(workspace, ws_bytes), ctypes.byref(args), reps, buf,
+                                 max_points, ctypes.byref(n), _stream(stream)))
+    return _points(buf, min(n.value, max_points))
+
+
+def tune_reduce(op: int, a_list, b_list, out_list, workspace, args: DtArgs, reps: int = 3,
+                stream=None, ws_bytes=None, max_points: int = 128):
+    """Tuner of dt_gemm_rs (op OP_RS) or dt_gemm_ar (op OP_AR); writes the best into `args`."""
+    buf = (DtTunePoint * max_points)()
+    n = ctypes.c_int32(0)
+    _raise(lib().dt_tune_reduce(op, _ptr_array(a_list), _ptr_array(b_list), _ptr_array(out_list),
+                                _ptr(workspace), _nbytes(workspace, ws_bytes), ctypes.byref(args),
+                                reps, buf, max_points, ctypes.byref(n), _stream(stream)))
+    return _points(buf, min(n.value, max_points))
 
 
 def debug_drop_transfer(step: int):

@@ -102,6 +102,7 @@ struct Derived {
   int64_t M, N, K, Ms, Cr, lda, ldb, ldc, ld_gather;
   bool swizzle, f32;
   int backend;  // resolved for AG
+  int32_t copy_ctas;
   uint64_t timeout_ns;
   Geom geom;
   size_t off_ready, off_pieces, off_cnt, off_order, ctl_bytes, off_data, total;
@@ -179,9 +180,14 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     // large chunks amortise the copy engine's per-transfer launch cost; smaller ones move
     // on in-kernel TMA bulk copies
     const int64_t chunk_bytes = std::min<int64_t>(d->Cr, d->Ms) * d->K * 2;
-    be = chunk_bytes >= (8ll << 20) ? DT_XFER_COPY_ENGINE : DT_XFER_TMA;
+    be = chunk_bytes >= (8ll << 20) && a->copy_ctas == 0 ? DT_XFER_COPY_ENGINE : DT_XFER_TMA;
   }
   d->backend = be;
+  d->copy_ctas = op == DT_OP_AG_GEMM ? a->copy_ctas : 0;
+  if (d->copy_ctas < 0 || d->copy_ctas > 64)
+    return fail(DT_ERR_INVALID, "copy_ctas %d outside 0..64", d->copy_ctas);
+  if (d->copy_ctas > 0 && be == DT_XFER_COPY_ENGINE)
+    return fail(DT_ERR_INVALID, "dedicated transfer CTAs need DT_XFER_TMA or DT_XFER_LDST");
   // workspace layout: error word | control arrays | tile order || data
   const size_t nchunks = static_cast<size_t>(d->W) * d->nC;
   size_t off = 256;
@@ -259,6 +265,7 @@ struct DevCtx {
   int sms = 0;
   cudaStream_t side = nullptr;
   cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+  cudaEvent_t tune_t0 = nullptr, tune_t1 = nullptr;  // timing events of the tuner
   std::vector<cudaEvent_t> chunk_events;
 };
 std::mutex g_dev_mu;
@@ -520,7 +527,9 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
   if ((s = make_tmap(&p.tmA[0], p.gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
   if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
   const int use = a->num_sms > 0 ? std::min(a->num_sms, sms) : sms;
-  const int grid = static_cast<int>(std::min<int64_t>(d.T, use));
+  if (d.copy_ctas >= use) return fail(DT_ERR_INVALID, "copy_ctas must leave SMs for the GEMM");
+  p.copy_ctas = d.copy_ctas;
+  const int grid = d.copy_ctas + static_cast<int>(std::min<int64_t>(d.T, use - d.copy_ctas));
   const cudaError_t e = launch_ag_kernel(p, copy, d.f32, grid, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
   return DT_OK;
@@ -702,7 +711,10 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
     return DT_OK;
   }
   const int copy = d.backend == DT_XFER_TMA ? kCopyTma : kCopyLdst;
-  cudaError_t e = launch_ag_kernel(p, copy, d.f32, grid, true, stream);
+  p.copy_ctas = d.copy_ctas;
+  if (d.copy_ctas >= sms) return fail(DT_ERR_INVALID, "copy_ctas must leave SMs for the GEMM");
+  const int grid_ded = d.copy_ctas + static_cast<int>(std::min<int64_t>(d.T, sms - d.copy_ctas));
+  cudaError_t e = launch_ag_kernel(p, copy, d.f32, d.copy_ctas ? grid_ded : grid, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
   return DT_OK;
 }
@@ -918,6 +930,181 @@ dt_status dt_gemm_rs_kernel_overlap(const void* const* a_, const void* const* b_
 dt_status dt_gemm_ar_kernel_overlap(const void* const* a_, const void* const* b_, void* const* out,
                                     void* ws, size_t ws_bytes, const dt_args* a, void* stream) {
   return reduce_kernel_overlap(a_, b_, out, ws, ws_bytes, a, stream, DT_OP_GEMM_AR);
+}
+
+// ------------------------------------------------------------------------------ tuner
+}  // extern "C"
+
+namespace {
+
+struct TuneCtx {
+  cudaStream_t stream;
+  void* ws;
+  size_t ws_bytes;
+  int32_t reps;
+  cudaEvent_t t0, t1;
+};
+
+// Time one candidate: one warm-up call, then `reps` calls between two events.
+template <typename Call>
+void tune_one(const TuneCtx& t, dt_args& cand, int op, Call&& call, dt_tune_point* pt) {
+  pt->chunk_rows = cand.chunk_rows;
+  pt->backend = cand.backend;
+  pt->copy_ctas = cand.copy_ctas;
+  pt->swizzle = cand.swizzle;
+  pt->group = cand.group;
+  pt->ms = -1.0f;
+  const size_t need = dt_workspace_size(&cand, op);
+  if (need == 0 || need > t.ws_bytes) {
+    pt->status = need == 0 ? DT_ERR_INVALID : DT_ERR_WORKSPACE;
+    return;
+  }
+  dt_status st = call(cand);
+  if (st == DT_OK) st = dt_check(t.ws, t.stream, nullptr);
+  if (st != DT_OK) {
+    pt->status = st;
+    return;
+  }
+  cudaEventRecord(t.t0, t.stream);
+  for (int32_t r = 0; r < t.reps && st == DT_OK; ++r) st = call(cand);
+  cudaEventRecord(t.t1, t.stream);
+  if (st == DT_OK) st = dt_check(t.ws, t.stream, nullptr);
+  float ms = 0.f;
+  if (st == DT_OK && cudaEventElapsedTime(&ms, t.t0, t.t1) == cudaSuccess) pt->ms = ms / t.reps;
+  pt->status = st;
+}
+
+std::vector<int64_t> chunk_candidates(int64_t ms) {
+  std::vector<int64_t> v;
+  for (int64_t c : {64, 128, 256, 512, 1024, 2048, 4096})
+    if (c < ms) v.push_back(c);
+  v.push_back(std::max<int64_t>(ms, 1));
+  return v;
+}
+
+dt_status tune_setup(int op, const dt_args* a, void* ws, size_t ws_bytes, int32_t reps,
+                     void* stream, TuneCtx* t, Derived* d) {
+  dt_status s = derive(a, op, d);
+  if (s != DT_OK) return s;
+  if (reps < 1) return fail(DT_ERR_INVALID, "reps must be >= 1");
+  DevCtx* dev = nullptr;
+  if ((s = dev_ctx(&dev)) != DT_OK) return s;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!dev->tune_t0) {
+      DT_CUDA(cudaEventCreate(&dev->tune_t0));
+      DT_CUDA(cudaEventCreate(&dev->tune_t1));
+    }
+  }
+  *t = TuneCtx{reinterpret_cast<cudaStream_t>(stream), ws, ws_bytes, reps, dev->tune_t0,
+               dev->tune_t1};
+  return DT_OK;
+}
+
+// Pick the fastest point that ran, copy its knobs into *a.
+dt_status tune_finish(std::vector<dt_tune_point>& pts, dt_args* a, dt_tune_point* out,
+                      int32_t max_points, int32_t* n_points) {
+  int best = -1;
+  for (int i = 0; i < static_cast<int>(pts.size()); ++i)
+    if (pts[i].status == DT_OK && pts[i].ms >= 0 && (best < 0 || pts[i].ms < pts[best].ms)) best = i;
+  if (n_points) *n_points = static_cast<int32_t>(pts.size());
+  if (out)
+    for (int i = 0; i < static_cast<int>(pts.size()) && i < max_points; ++i) out[i] = pts[i];
+  if (best < 0) return fail(DT_ERR_UNSUPPORTED, "no tuner candidate ran");
+  a->chunk_rows = pts[best].chunk_rows;
+  a->backend = pts[best].backend;
+  a->copy_ctas = pts[best].copy_ctas;
+  a->swizzle = pts[best].swizzle;
+  a->group = pts[best].group;
+  return DT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, void* ws,
+                          size_t ws_bytes, dt_args* a, int32_t reps, dt_tune_point* points,
+                          int32_t max_points, int32_t* n_points, void* stream) {
+  g_last_error.clear();
+  TuneCtx t;
+  Derived d;
+  dt_status s = tune_setup(DT_OP_AG_GEMM, a, ws, ws_bytes, reps, stream, &t, &d);
+  if (s != DT_OK) return s;
+  DevCtx* dev = nullptr;
+  if ((s = dev_ctx(&dev)) != DT_OK) return s;
+  auto call = [&](dt_args& cand) { return dt_ag_gemm(a_shards, b, c, ws, ws_bytes, &cand, stream); };
+  std::vector<dt_tune_point> pts;
+  for (int64_t cr : chunk_candidates(d.Ms)) {
+    const int64_t nchunks = d.W * cdiv64(d.Ms, cr);
+    struct V { int be; int copy; };
+    std::vector<V> vs = {{DT_XFER_TMA, 0}, {DT_XFER_LDST, 0}};
+    if (nchunks <= 512) vs.push_back({DT_XFER_COPY_ENGINE, 0});
+    for (int n : {8, 16})
+      if (dev->sms > 4 * n) {
+        vs.push_back({DT_XFER_TMA, n});
+        vs.push_back({DT_XFER_LDST, n});
+      }
+    for (const V& v : vs) {
+      dt_args cand = *a;
+      cand.chunk_rows = cr;
+      cand.backend = v.be;
+      cand.copy_ctas = v.copy;
+      cand.swizzle = 1;
+      cand.group = a->group > 0 ? a->group : 8;
+      dt_tune_point pt;
+      tune_one(t, cand, DT_OP_AG_GEMM, call, &pt);
+      pts.push_back(pt);
+    }
+  }
+  // tile order inside a chunk: group widths around the best point
+  int best = -1;
+  for (int i = 0; i < static_cast<int>(pts.size()); ++i)
+    if (pts[i].status == DT_OK && pts[i].ms >= 0 && (best < 0 || pts[i].ms < pts[best].ms)) best = i;
+  if (best >= 0) {
+    const dt_tune_point base = pts[best];
+    for (int g : {4, 16}) {
+      dt_args cand = *a;
+      cand.chunk_rows = base.chunk_rows;
+      cand.backend = base.backend;
+      cand.copy_ctas = base.copy_ctas;
+      cand.swizzle = 1;
+      cand.group = g;
+      dt_tune_point pt;
+      tune_one(t, cand, DT_OP_AG_GEMM, call, &pt);
+      pts.push_back(pt);
+    }
+  }
+  return tune_finish(pts, a, points, max_points, n_points);
+}
+
+dt_status dt_tune_reduce(int op, const void* const* a_, const void* const* b_, void* const* out,
+                         void* ws, size_t ws_bytes, dt_args* a, int32_t reps, dt_tune_point* points,
+                         int32_t max_points, int32_t* n_points, void* stream) {
+  g_last_error.clear();
+  if (op != DT_OP_GEMM_RS && op != DT_OP_GEMM_AR)
+    return fail(DT_ERR_INVALID, "dt_tune_reduce takes DT_OP_GEMM_RS or DT_OP_GEMM_AR");
+  TuneCtx t;
+  Derived d;
+  dt_status s = tune_setup(op, a, ws, ws_bytes, reps, stream, &t, &d);
+  if (s != DT_OK) return s;
+  auto call = [&](dt_args& cand) {
+    return op == DT_OP_GEMM_RS ? dt_gemm_rs(a_, b_, out, ws, ws_bytes, &cand, stream)
+                               : dt_gemm_ar(a_, b_, out, ws, ws_bytes, &cand, stream);
+  };
+  std::vector<dt_tune_point> pts;
+  for (int64_t cr : chunk_candidates(d.Ms)) {
+    for (int g : {4, 8, 16}) {
+      dt_args cand = *a;
+      cand.chunk_rows = cr;
+      cand.swizzle = 1;
+      cand.group = g;
+      dt_tune_point pt;
+      tune_one(t, cand, op, call, &pt);
+      pts.push_back(pt);
+    }
+  }
+  return tune_finish(pts, a, points, max_points, n_points);
 }
 
 dt_status dt_debug_drop_transfer(int32_t step) {

@@ -84,6 +84,8 @@ struct KParams {
   int32_t Tm, KB, T;       // m-tiles in the window, k-blocks, tiles in the launch
   int32_t pieces_max;      // RS: most chunks one m-tile's rows touch (counter stride)
   int32_t ar_copies;       // 0: ReduceScatter; > 0: AllReduce into out[0 .. ar_copies-1]
+  int32_t copy_ctas;       // AG in-kernel transfer: CTAs 0..copy_ctas-1 only move chunks
+                           // (dedicated SMs); 0: transfer warps inside every compute CTA
   int32_t plain;           // 1: identity order, no flags, no arrival counting
   int32_t wait_flags;      // AG: the producer waits on ready flags
   uint32_t epoch;
@@ -190,6 +192,14 @@ __device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
   return ti;
 }
 
+// Compute CTAs are blockIdx.x >= copy_ctas; they take the tile order round robin.
+__device__ __forceinline__ int32_t first_pos(const KParams& p) {
+  return static_cast<int32_t>(blockIdx.x) - p.copy_ctas;
+}
+__device__ __forceinline__ int32_t pos_stride(const KParams& p) {
+  return static_cast<int32_t>(gridDim.x) - p.copy_ctas;
+}
+
 // ============================================================================ producer
 template <bool RS>
 __device__ void run_producer(const KParams& p, const SmemLayout& L) {
@@ -197,7 +207,7 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
   int64_t last_issue[kStages];
 #pragma unroll
   for (int s = 0; s < kStages; ++s) last_issue[s] = -1;
-  for (int32_t pos = blockIdx.x; pos < p.T; pos += gridDim.x) {
+  for (int32_t pos = first_pos(p); pos < p.T; pos += pos_stride(p)) {
     const TileInfo ti = decode_tile<RS>(p, pos);
     if (!ti.valid) {
       raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
@@ -260,7 +270,7 @@ __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_bas
   uint32_t kit = 0;
   int32_t tl = 0;
   bool issued = false;
-  for (int32_t pos = blockIdx.x; pos < p.T; pos += gridDim.x) {
+  for (int32_t pos = first_pos(p); pos < p.T; pos += pos_stride(p)) {
     const TileInfo ti = decode_tile<RS>(p, pos);
     if (!ti.valid) continue;
     const int acc = tl & 1;
@@ -503,7 +513,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
   int32_t tl = 0;
   uint32_t stage_ctr = 0;           // running-sum staging buffer in use (alternates)
   uint32_t ld_par[2] = {0u, 0u};    // phase of each staging buffer's load barrier
-  for (int32_t pos = blockIdx.x; pos < p.T; pos += gridDim.x) {
+  for (int32_t pos = first_pos(p); pos < p.T; pos += pos_stride(p)) {
     const TileInfo ti = decode_tile<RS>(p, pos);
     if (!ti.valid) continue;
     const int acc = tl & 1;
@@ -721,7 +731,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
       }
       named_bar_sync(1, 128);
       // warm L2 with the running sums the next tile of this CTA will fold into
-      const int32_t npos = pos + static_cast<int32_t>(gridDim.x);
+      const int32_t npos = pos + pos_stride(p);
       if (npos < p.T) {
         const TileInfo nt = decode_tile<RS>(p, npos);
         const int64_t nrow = nt.row0 + qd * 32 + lane;
@@ -796,8 +806,10 @@ __device__ __forceinline__ void for_each_piece(const KParams& p, int32_t wid, in
   }
 }
 
-static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L) {
-  const int32_t wid = blockIdx.x, nw = gridDim.x;
+// One TMA bulk-copy worker (one thread): staging buffers `stage` and `stage + kCopyBuf`,
+// completion barriers bar0 / bar1.
+static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32_t wid, int32_t nw,
+                                    uint8_t* stage, uint32_t bar0, uint32_t bar1) {
   uint32_t k = 0;
   int32_t prev_c = -1, prev_total = 0;
   auto stop = [&]() { return *L.abort_flag != 0; };
@@ -808,19 +820,19 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L) {
     uint8_t* dst = p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard) * p.ld_gather * 2 +
                    pc.boff;
     const int b = static_cast<int>(k & 1u);
-    const uint32_t buf = smem_u32(L.copy + b * kCopyBuf);
+    const uint32_t buf = smem_u32(stage + b * kCopyBuf);
+    const uint32_t bar = b ? bar1 : bar0;
     const uint32_t tot = pc.nbytes * static_cast<uint32_t>(pc.nr);
     const bool whole = pc.nbytes == static_cast<uint32_t>(p.row_bytes);
     bulk_wait_read<1>();  // the store that last used this buffer has read it
-    mbar_expect_tx(L.copyb(b), tot);
+    mbar_expect_tx(bar, tot);
     if (p.src_rows_contig || pc.nr == 1) {
-      bulk_g2s(buf, src, tot, L.copyb(b));
+      bulk_g2s(buf, src, tot, bar);
     } else {
       for (int32_t r = 0; r < pc.nr; ++r)
-        bulk_g2s(buf + r * pc.nbytes, src + static_cast<int64_t>(r) * p.lda_src * 2, pc.nbytes,
-                 L.copyb(b));
+        bulk_g2s(buf + r * pc.nbytes, src + static_cast<int64_t>(r) * p.lda_src * 2, pc.nbytes, bar);
     }
-    if (!wait_bar(p, L, L.copyb(b), (k >> 1) & 1u, 500 + b)) return false;
+    if (!wait_bar(p, L, bar, (k >> 1) & 1u, 500 + b)) return false;
     if (whole || pc.nr == 1) {
       bulk_s2g(dst, buf, tot);  // gather rows are back to back (ld_gather == K)
     } else {
@@ -839,8 +851,9 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L) {
   if (prev_c >= 0 && !*L.abort_flag) signal_piece(p, prev_c, prev_total);
 }
 
-static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int warp, int lane) {
-  const int32_t wid = blockIdx.x * 2 + (warp - 2), nw = gridDim.x * 2;
+// One vector ld/st copy worker (one warp).
+static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int lane, int32_t wid,
+                                     int32_t nw) {
   // the whole warp takes the same decision
   auto stop = [&]() { return __shfl_sync(0xffffffffu, *L.abort_flag, 0) != 0; };
   for_each_piece(p, wid, nw, stop, [&](int32_t s, int32_t j, int32_t c, int32_t total,
@@ -908,6 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
       mbar_init(L.copyb(a), 1);
     }
     mbar_init(L.fin(), 1);
+    for (int w = 0; w < 8; ++w) mbar_init(smem_u32(L.bars + 16 + w), 1);  // dedicated workers
     *L.abort_flag = 0;
     *L.unit_flag = 0;
     mbar_init_fence();
@@ -916,20 +930,35 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     tma_prefetch_desc(&p.tmA[0]);
     tma_prefetch_desc(&p.tmB[0]);
   }
-  if (warp == 1) tmem_alloc(smem_u32(L.tmem_slot), kTmemCols);
+  const bool copier = static_cast<int32_t>(blockIdx.x) < p.copy_ctas;
+  if (warp == 1 && !copier) tmem_alloc(smem_u32(L.tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *L.tmem_slot;
+  const uint32_t tmem_base = copier ? 0u : *L.tmem_slot;
 
-  if (warp == 0) {
+  if (copier) {
+    // dedicated transfer CTA: no GEMM; the operand ring becomes four 32 KiB staging pairs
+    if (!RS && !p.plain) {
+      if (COPY == kCopyTma && warp < 4 && lane == 0)
+        run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x) * 4 + warp, p.copy_ctas * 4,
+                     L.a + warp * 2 * kCopyBuf, smem_u32(L.bars + 16 + 2 * warp),
+                     smem_u32(L.bars + 17 + 2 * warp));
+      if (COPY == kCopyLdst)
+        run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 8 + warp, p.copy_ctas * 8);
+    }
+  } else if (warp == 0) {
     if (lane == 0) run_producer<RS>(p, L);
   } else if (warp == 1) {
     if (lane == 0) run_mma<RS>(p, L, tmem_base);
   } else if (warp < 4) {
-    if (!RS && !p.plain) {
-      if (COPY == kCopyTma && warp == 2 && lane == 0) run_copy_tma(p, L);
-      if (COPY == kCopyLdst) run_copy_ldst(p, L, warp, lane);
+    if (!RS && !p.plain && p.copy_ctas == 0) {  // co-located transfer warps
+      if (COPY == kCopyTma && warp == 2 && lane == 0)
+        run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x), static_cast<int32_t>(gridDim.x),
+                     L.copy, L.copyb(0), L.copyb(1));
+      if (COPY == kCopyLdst)
+        run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 2 + (warp - 2),
+                      static_cast<int32_t>(gridDim.x) * 2);
     }
   } else {
     run_epilogue<RS, F32>(p, L, tmem_base, warp, lane);
@@ -937,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 1 && !copier) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
