@@ -85,6 +85,12 @@ def workload_desc(name, ops, chunk_override):
     d = {"workload": name if name != "ffn_pair" else
          "llama70b_like_tp8_ffn_pair (AG-GEMM then GEMM-RS, W=8 virtual ranks)"}
     for wl in ops:
+        if wl.op == "ffn":
+            d["ffn"] = {"name": wl.name, "world_size": wl.world_size, "m": wl.m, "k": wl.k,
+                        "f_per_rank": wl.f_rank, "n": wl.n, "act": wl.act, "seed": wl.seed,
+                        "chunk_rows": chunk_override or wl.chunk_rows, "gflop": wl.flops / 1e9,
+                        "dist_x": wl.dist_a, "dist_w": wl.dist_b}
+            continue
         d[wl.op] = {"name": wl.name, "world_size": wl.world_size, "m": wl.m, "n": wl.n,
                     "k" if wl.op == "ag" else "k_per_rank": wl.k,
                     "chunk_rows": chunk_override or wl.chunk_rows, "seed": wl.seed,
@@ -129,6 +135,20 @@ def oracle_sample(ops, ag_rows, rs_rows, inputs):
     desc = []
     for wl, inp in zip(ops, inputs):
         ms = wl.m // wl.world_size
+        if wl.op == "ffn":
+            # the block is row-independent: run it on the first rows, split over W ranks
+            w = wl.world_size
+            rows = max(w, min(rs_rows, wl.m) // w * w)
+            x = np.concatenate([f64_from_bf16_bits(sh) for sh in inp.x_shards])[:rows]
+            pieces = [x[q * rows // w:(q + 1) * rows // w] for q in range(w)]
+            w1 = f64_from_bf16_bits(inp.w1)
+            w2 = [f64_from_bf16_bits(t) for t in inp.w2]
+            t0 = time.perf_counter()
+            reference.ffn_tp(pieces, w1, w2, wl.act)
+            secs += time.perf_counter() - t0
+            flops += 2.0 * rows * w * wl.f_rank * (wl.k + wl.n)
+            desc.append(f"FFN block on rows 0..{rows}")
+            continue
         if wl.op == "ag":
             rows = min(ag_rows, wl.m)
             nsh = -(-rows // ms)
@@ -329,6 +349,36 @@ def main():
     in_bytes = out_bytes = 0
     for wl, inp in zip(ops, inputs):
         cr = args.chunk_rows or wl.chunk_rows
+        if wl.op == "ffn":
+            # chained block: AllGather-GEMM (+ activation) into H, GEMM-ReduceScatter reads H
+            import dataclasses
+            w, fr = wl.world_size, wl.f_rank
+            ag_wl = dataclasses.replace(wl, name=wl.name + "/ag", op="ag", n=w * fr)
+            rs_wl = dataclasses.replace(wl, name=wl.name + "/rs", op="rs", k=fr)
+            x = [up(s_) for s_ in inp.x_shards]
+            w1 = up(inp.w1)
+            h = torch.empty((wl.m, w * fr), dtype=torch.bfloat16, device=dev)
+            a_ag = dt.make_args(w, wl.m, w * fr, wl.k, chunk_rows=cr, act=wl.act,
+                                swizzle=not args.no_swizzle, backend=args.backend)
+            probe = dt.make_args(w, wl.m, w * fr, wl.k, chunk_rows=64)
+            ws_ag = torch.zeros(max(dt.workspace_size(a_ag, dt.OP_AG),
+                                    dt.workspace_size(probe, dt.OP_AG)), dtype=torch.uint8, device=dev)
+            calls.append(dict(op="ag", wl=ag_wl, args=a_ag, ins=x + [w1], shards=x, b=w1, outs=[h],
+                              ws=ws_ag, act=wl.act))
+            w2 = [up(t) for t in inp.w2]
+            a_rs = dt.make_args(w, wl.m, wl.n, fr, chunk_rows=cr, lda=w * fr,
+                                swizzle=not args.no_swizzle)
+            probe = dt.make_args(w, wl.m, wl.n, fr, chunk_rows=64, lda=w * fr)
+            ws_rs = torch.zeros(max(dt.workspace_size(a_rs, dt.OP_RS),
+                                    dt.workspace_size(probe, dt.OP_RS)), dtype=torch.uint8, device=dev)
+            outs = [torch.empty((wl.m // w, wl.n), dtype=torch.bfloat16, device=dev)
+                    for _ in range(w)]
+            calls.append(dict(op="rs", wl=rs_wl, args=a_rs, ins=w2,
+                              A=[h[:, q * fr:(q + 1) * fr] for q in range(w)], B=w2, outs=outs,
+                              ws=ws_rs))
+            in_bytes += sum(t.numel() * 2 for t in x + [w1] + w2)
+            out_bytes += sum(t.numel() * 2 for t in outs)
+            continue
         if wl.op == "ag":
             a = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, rank=args.rank_view, chunk_rows=cr,
                              swizzle=not args.no_swizzle, backend=args.backend)
@@ -449,7 +499,8 @@ def main():
         "tuned": tuned or None,
     })
     for op_name, t in tuned.items():
-        line["config"][op_name]["chunk_rows"] = t["chunk_rows"]
+        if op_name in line["config"]:
+            line["config"][op_name]["chunk_rows"] = t["chunk_rows"]
     pk = peaks()
     peak = pk["bf16_tflops_sustained"]
     line["frac_of_peak"] = value / world / peak
@@ -534,6 +585,10 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
         if cl["op"] == "ag":
             a = torch.cat(cl["shards"], dim=0)[:256].float()
             ref = a @ cl["b"].float()
+            if cl.get("act") == "gelu_tanh":
+                ref = torch.nn.functional.gelu(ref, approximate="tanh")
+            elif cl.get("act") == "silu":
+                ref = torch.nn.functional.silu(ref)
             got = cl["outs"][0][:256].float()
         else:  # ReduceScatter out_0 / AllReduce rank 0: rows 0..127 of the sum
             ref = sum(a_[:128].float() @ b_.float() for a_, b_ in zip(cl["A"], cl["B"]))

@@ -101,7 +101,11 @@ typedef struct dt_args {
   int32_t copy_ctas;   /* AG with DT_XFER_TMA / DT_XFER_LDST: CTAs of the grid that only move
                           chunks (dedicated SMs); 0 = transfer warps inside every compute CTA
                           (co-located).  AutoOverlap page section 5.3, lowerings 2-5.        */
+  int32_t act;         /* AG only: dt_act applied to the fp32 result before it is stored     */
+  int32_t reserved;
 } dt_args;
+
+typedef enum { DT_ACT_NONE = 0, DT_ACT_GELU_TANH = 1, DT_ACT_SILU = 2 } dt_act;
 
 /* Fill `a` with defaults: W=1, rank 0, swizzle on, AUTO backend, bf16 output, 128x256
  * tiles, group 8.  Sizes are zero and must be set by the caller. */
@@ -167,6 +171,21 @@ dt_status dt_gemm_rs(const void* const* a, const void* const* b, void* const* ou
  * Workspace: dt_workspace_size(a, DT_OP_GEMM_AR) (the same layout as the ReduceScatter). */
 dt_status dt_gemm_ar(const void* const* a, const void* const* b, void* const* out,
                      void* workspace, size_t ws_bytes, const dt_args* a_args, void* stream);
+
+/* Tensor-parallel feed-forward block, AllGather + ReduceScatter form, over W virtual ranks
+ * (DITRON page, section 5.1 "FFN模块"; Triton-distributed talk: the AllGather-GEMM feeds the
+ * GEMM-ReduceScatter).  Rank q holds column block q of W1 (F_r = F/W columns) and W2_q.
+ *   1. h = act(AllGather(x) * W1), all ranks' blocks at once (every rank gathers the same X):
+ *      dt_ag_gemm with `ag` (m = M, k = model dim, n = W*F_r, act, out_dtype bf16, ldc = n).
+ *   2. out_s = rows s of sum_q h[:, q*F_r .. (q+1)*F_r) * W2_q: dt_gemm_rs with `rs`
+ *      (m = M, k = F_r, n = N, lda = W*F_r), A_q = h + q*F_r.
+ *   x_shards : W device pointers [M/W x K] bf16;  w1 : [K x W*F_r] bf16;
+ *   w2       : W device pointers [F_r x N] bf16;  h : [M x W*F_r] bf16 (written, then read);
+ *   out      : W device pointers [M/W x N].
+ * Requires ag.world_size == rs.world_size, ag.m == rs.m, ag.n == W * rs.k, rs.k % 8 == 0. */
+dt_status dt_ffn_ag_rs(const void* const* x_shards, const void* w1, const void* const* w2,
+                       void* h, void* const* out, void* ws_ag, size_t ws_ag_bytes, void* ws_rs,
+                       size_t ws_rs_bytes, const dt_args* ag, const dt_args* rs, void* stream);
 
 /* Kernel-level-overlap baselines with the same arguments and results (AutoOverlap page,
  * section 2.1 / Fig. 2(b)): AG = per-chunk copies on a second stream and one launch of the

@@ -61,6 +61,50 @@ def gemm_ar(a_list, b_list):
     return [s_full.copy() for _ in range(w)]
 
 
+ACTIVATIONS = ("none", "gelu_tanh", "silu")
+
+
+def activation(x, act):
+    """Elementwise activation in float64.
+
+    gelu_tanh: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), the tanh form of GELU used by
+    GPT / Megatron feed-forward blocks; silu: x / (1 + exp(-x)).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if act == "none":
+        return x.copy()
+    if act == "gelu_tanh":
+        return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)))
+    if act == "silu":
+        return x / (1.0 + np.exp(-x))
+    raise ValueError(act)
+
+
+def round_bf16_via_f32(x):
+    """float64 -> float32 (nearest) -> bfloat16 (nearest, ties to even), returned as float64:
+    how the CUDA epilogue stores an fp32 value as bf16."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def ffn_tp(x_shards, w1, w2_list, act):
+    """Tensor-parallel feed-forward block over W ranks, AllGather + ReduceScatter form.
+
+    Rank q holds the column block q of W1 (F/W columns) and W2_q (F/W x N).  Every rank
+    gathers X, computes H_q = act(X W1_q), stored as bf16, and the partial H_q W2_q; the
+    partials are reduce-scattered by rows.  (DITRON page, section 5.1 "FFN模块": AllGather +
+    ReduceScatter around the two GEMMs.)  Returns (H as float64 [M, F], list of W out_s).
+    """
+    w = len(x_shards)
+    x = np.concatenate([np.asarray(s, dtype=np.float64) for s in x_shards], axis=0)
+    h = round_bf16_via_f32(activation(x @ np.asarray(w1, dtype=np.float64), act))
+    fr = h.shape[1] // w
+    outs = gemm_rs([h[:, q * fr:(q + 1) * fr] for q in range(w)], w2_list)
+    return h, outs
+
+
 def ag_gemm_entries(shards, b, rows, cols):
     """Selected entries C[rows[t], cols[t]] of the AllGather-GEMM, one dot each.
 

@@ -120,6 +120,29 @@ def make_rs_inputs(world_size: int, m: int, n: int, k_rank: int, seed: int,
     return RSInputs(world_size, a, b)
 
 
+@dataclass
+class FFNInputs:
+    world_size: int
+    x_shards: list          # W arrays uint16 [M/W, K]
+    w1: np.ndarray          # uint16 [K, W*F_r]  (rank q's block = columns q*F_r ..)
+    w2: list                # W arrays uint16 [F_r, N]
+
+
+def make_ffn_inputs(world_size: int, m: int, k: int, f_rank: int, n: int, seed: int,
+                    dist_x: str = "normal(1.0)", dist_w: str = "normal(0.02)") -> FFNInputs:
+    """Inputs of one tensor-parallel feed-forward block: X (M x K, row shards), W1
+    (K x W*F_r), W2_0 .. W2_{W-1} (F_r x N each); drawn in that order."""
+    if m % world_size:
+        raise ValueError("M must be a multiple of the world size")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = _draw_bf16(rng, dist_x, (m, k))
+    w1 = _draw_bf16(rng, dist_w, (k, world_size * f_rank))
+    w2 = [_draw_bf16(rng, dist_w, (f_rank, n)) for _ in range(world_size)]
+    ms = m // world_size
+    return FFNInputs(world_size, [np.ascontiguousarray(x[s * ms:(s + 1) * ms])
+                                  for s in range(world_size)], w1, w2)
+
+
 @dataclass(frozen=True)
 class Workload:
     """One benchmark / parity workload: shapes, seed, distributions, chunking."""
@@ -133,16 +156,22 @@ class Workload:
     dist_a: str
     dist_b: str
     chunk_rows: int
-    note: str = ""
+    f_rank: int = 0         # feed-forward block: hidden columns per rank
+    act: str = "none"       # feed-forward block: activation between the GEMMs
 
     @property
     def flops(self) -> float:
         if self.op == "ag":
             return 2.0 * self.m * self.n * self.k
+        if self.op == "ffn":
+            return 2.0 * self.m * self.world_size * self.f_rank * (self.k + self.n)
         return 2.0 * self.m * self.n * self.k * self.world_size
 
     def make(self):
         # "rs" and "ar" (GEMM-AllReduce) take the same per-rank inputs
+        if self.op == "ffn":
+            return make_ffn_inputs(self.world_size, self.m, self.k, self.f_rank, self.n, self.seed,
+                                   self.dist_a, self.dist_b)
         if self.op == "ag":
             return make_ag_inputs(self.world_size, self.m, self.n, self.k, self.seed,
                                   self.dist_a, self.dist_b)
@@ -173,6 +202,11 @@ WORKLOADS = {
     # GEMM-AllReduce on the FFN pair's second GEMM (same inputs as the ReduceScatter)
     "ar_w8_m8192_n8192_k3584": Workload("ar_w8_m8192_n8192_k3584", "ar", 8, 8192, 8192, 3584, 2,
                                         "normal(1.0)", "normal(0.02)", 1024),
+    # the whole Llama-70B-like TP=8 feed-forward block, chained: X 8192 x 8192 gathered,
+    # H = GELU(X W1) with W1 8192 x (8 x 3584), then out = ReduceScatter(H W2), W2_q 3584 x 8192
+    "ffn_w8_m8192_k8192_f3584_n8192": Workload("ffn_w8_m8192_k8192_f3584_n8192", "ffn", 8, 8192,
+                                               8192, 8192, 2, "normal(1.0)", "normal(0.02)", 1024,
+                                               f_rank=3584, act="gelu_tanh"),
     # largest AllGather-GEMM (chunk/backend sweep), W=8, U[-1,1], seed 4
     "ag_w8_m16384_n8192_k8192": Workload("ag_w8_m16384_n8192_k8192", "ag", 8, 16384, 8192, 8192, 4,
                                          "uniform", "uniform", 256),

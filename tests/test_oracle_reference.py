@@ -314,3 +314,52 @@ def test_generator_is_seeded_and_ordered():
     rng = np.random.Generator(np.random.PCG64(3))
     a_full = bf16_bits_from_f64(rng.uniform(-1, 1, (4, 5)))
     assert np.array_equal(a.shards[0], a_full[:2]) and np.array_equal(a.shards[1], a_full[2:])
+
+
+# ---------------------------------------------------------------- activations and the FFN block
+
+def test_gelu_tanh_is_close_to_exact_gelu():
+    """The tanh form stays within 5e-4 of x * Phi(x) (exact GELU, via the error function)."""
+    from scipy.special import erf
+    x = np.linspace(-8, 8, 4001)
+    exact = 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+    assert np.max(np.abs(reference.activation(x, "gelu_tanh") - exact)) < 5e-4
+    assert reference.activation(np.array([0.0]), "gelu_tanh")[0] == 0.0
+
+
+def test_silu_identities():
+    x = np.linspace(-20, 20, 801)
+    s = reference.activation(x, "silu")
+    assert np.allclose(s - reference.activation(-x, "silu"), x, atol=1e-12)  # x*sig(x)+x*sig(-x)=x
+    nz = x != 0
+    assert np.allclose(s[nz] / x[nz], 1.0 / (1.0 + np.exp(-x[nz])), atol=1e-12)  # silu = x sig(x)
+    assert np.array_equal(reference.activation(x, "none"), x)
+
+
+def test_bf16_rounding_of_the_block_matches_the_generator():
+    rng = np.random.Generator(np.random.PCG64(3))
+    x = rng.normal(0, 3, 20000).astype(np.float32).astype(np.float64)  # exact in float32
+    got = reference.round_bf16_via_f32(x)
+    want = f64_from_bf16_bits(bf16_bits_from_f64(x))  # independent rounding of the same values
+    assert np.array_equal(got, want)
+
+
+def test_ffn_block_reduces_to_two_plain_products():
+    """act = none, bf16-exact H: the block equals X W1 W2 split by rank (brute force)."""
+    rng = np.random.Generator(np.random.PCG64(21))
+    w, ms, k, fr, n = 2, 3, 4, 2, 5
+    xs = [rng.integers(-3, 4, (ms, k)).astype(np.float64) for _ in range(w)]
+    w1 = rng.integers(-3, 4, (k, w * fr)).astype(np.float64)
+    w2 = [rng.integers(-3, 4, (fr, n)).astype(np.float64) for _ in range(w)]
+    h, outs = reference.ffn_tp(xs, w1, w2, "none")
+    x = np.concatenate(xs)
+    want_h = np.array([[sum(x[i, t] * w1[t, c] for t in range(k)) for c in range(w * fr)]
+                       for i in range(w * ms)])
+    assert np.array_equal(h, want_h)
+    w2_full = np.concatenate(w2, axis=0)
+    want = np.array([[sum(want_h[i, t] * w2_full[t, c] for t in range(w * fr)) for c in range(n)]
+                     for i in range(w * ms)])
+    assert np.array_equal(np.concatenate(outs), want)
+    # with an activation, H is act(X W1) rounded to bf16
+    h2, _ = reference.ffn_tp(xs, w1, w2, "silu")
+    assert np.array_equal(h2, reference.round_bf16_via_f32(reference.activation(want_h, "silu")))

@@ -6,7 +6,7 @@ the library is loaded on first use and every call fails loudly if it is not buil
 """
 from .capi import (BACKENDS, OP_AG, OP_AR, OP_RS, DtArgs, DtError, ag_gemm,  # noqa: F401
                    ag_gemm_static_scratch,
-                   ag_gemm_kernel_overlap, check, debug_drop_transfer, gemm_ar,
+                   ag_gemm_kernel_overlap, check, debug_drop_transfer, ffn_ag_rs, gemm_ar,
                    gemm_ar_kernel_overlap, gemm_rs, gemm_rs_kernel_overlap, make_args,
                    swizzle_plan, swizzle_plan_device, tile_count, tune_ag_gemm, tune_reduce,
                    workspace_init, workspace_size)

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libdt.so")
 DT_OK, DT_ERR_INVALID, DT_ERR_UNSUPPORTED, DT_ERR_TIMEOUT, DT_ERR_CUDA, DT_ERR_WORKSPACE = range(6)
 BACKENDS = {"auto": 0, "copy_engine": 1, "tma": 2, "ldst": 3}
 DTYPES = {"bf16": 0, "f32": 1}
+ACTS = {"none": 0, "gelu_tanh": 1, "silu": 2}
 OP_AG, OP_RS, OP_AR = 0, 1, 2
 MAX_WORLD = 16
 
@@ -43,6 +44,8 @@ _SIGS = {
     "dt_check": (ctypes.c_int, [_P, _P, _P]),
     "dt_debug_drop_transfer": (ctypes.c_int, [ctypes.c_int32]),
     "dt_ag_gemm_static_scratch": (ctypes.c_int, [_P, _P, _P, _P, _P]),
+    "dt_ffn_ag_rs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_size_t,
+                                    _P, _P, _P]),
     "dt_tune_ag_gemm": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_int32, _P,
                                        ctypes.c_int32, _P, _P]),
     "dt_tune_reduce": (ctypes.c_int, [ctypes.c_int, _P, _P, _P, _P, ctypes.c_size_t, _P,
@@ -62,6 +65,7 @@ class DtArgs(ctypes.Structure):
         ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
         ("timeout_us", ctypes.c_int64),
         ("num_sms", ctypes.c_int32), ("copy_ctas", ctypes.c_int32),
+        ("act", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -139,7 +143,7 @@ def _ptr_array(xs):
 def make_args(world_size: int, m: int, n: int, k: int, *, rank: int = 0, chunk_rows: int = 128,
               swizzle: bool = True, backend: str = "auto", out_dtype: str = "bf16",
               lda: int = 0, ldb: int = 0, ldc: int = 0, timeout_us: int = 0, num_sms: int = 0,
-              group: int = 8, copy_ctas: int = 0) -> DtArgs:
+              group: int = 8, copy_ctas: int = 0, act: str = "none") -> DtArgs:
     a = DtArgs()
     lib().dt_args_default(ctypes.byref(a))
     a.world_size, a.rank, a.m, a.n, a.k = world_size, rank, m, n, k
@@ -152,6 +156,7 @@ def make_args(world_size: int, m: int, n: int, k: int, *, rank: int = 0, chunk_r
     a.num_sms = num_sms
     a.group = group
     a.copy_ctas = copy_ctas
+    a.act = ACTS[act]
     return a
 
 
@@ -268,6 +273,15 @@ def tune_reduce(op: int, a_list, b_list, out_list, workspace, args: DtArgs, reps
                                 _ptr(workspace), _nbytes(workspace, ws_bytes), ctypes.byref(args),
                                 reps, buf, max_points, ctypes.byref(n), _stream(stream)))
     return _points(buf, min(n.value, max_points))
+
+
+def ffn_ag_rs(x_shards, w1, w2_list, h, out_list, ws_ag, ws_rs, ag: DtArgs, rs: DtArgs,
+              stream=None, ws_ag_bytes=None, ws_rs_bytes=None):
+    """Tensor-parallel feed-forward block: h = act(AllGather(x) W1), out = ReduceScatter(h W2)."""
+    _raise(lib().dt_ffn_ag_rs(_ptr_array(x_shards), _ptr(w1), _ptr_array(w2_list), _ptr(h),
+                              _ptr_array(out_list), _ptr(ws_ag), _nbytes(ws_ag, ws_ag_bytes),
+                              _ptr(ws_rs), _nbytes(ws_rs, ws_rs_bytes), ctypes.byref(ag),
+                              ctypes.byref(rs), _stream(stream)))
 
 
 def debug_drop_transfer(step: int):

@@ -103,6 +103,7 @@ struct Derived {
   bool swizzle, f32;
   int backend;  // resolved for AG
   int32_t copy_ctas;
+  int32_t act;
   uint64_t timeout_ns;
   Geom geom;
   size_t off_ready, off_pieces, off_cnt, off_order, ctl_bytes, off_data, total;
@@ -183,6 +184,10 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     be = chunk_bytes >= (8ll << 20) && a->copy_ctas == 0 ? DT_XFER_COPY_ENGINE : DT_XFER_TMA;
   }
   d->backend = be;
+  if (a->act < DT_ACT_NONE || a->act > DT_ACT_SILU) return fail(DT_ERR_INVALID, "unknown act %d", a->act);
+  if (a->act != DT_ACT_NONE && op != DT_OP_AG_GEMM)
+    return fail(DT_ERR_UNSUPPORTED, "activations apply to the AllGather-GEMM only");
+  d->act = a->act;
   d->copy_ctas = op == DT_OP_AG_GEMM ? a->copy_ctas : 0;
   if (d->copy_ctas < 0 || d->copy_ctas > 64)
     return fail(DT_ERR_INVALID, "copy_ctas %d outside 0..64", d->copy_ctas);
@@ -432,6 +437,7 @@ void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
   p.T = d.T;
   p.epoch = epoch;
   p.timeout_ns = d.timeout_ns;
+  p.act = d.act;
 }
 
 // ------------------------------------------------------------------------------ AllGather
@@ -1105,6 +1111,30 @@ dt_status dt_tune_reduce(int op, const void* const* a_, const void* const* b_, v
     }
   }
   return tune_finish(pts, a, points, max_points, n_points);
+}
+
+dt_status dt_ffn_ag_rs(const void* const* x_shards, const void* w1, const void* const* w2,
+                       void* h, void* const* out, void* ws_ag, size_t ws_ag_bytes, void* ws_rs,
+                       size_t ws_rs_bytes, const dt_args* ag, const dt_args* rs, void* stream) {
+  g_last_error.clear();
+  if (!ag || !rs || !w2 || !out) return fail(DT_ERR_INVALID, "NULL argument");
+  const int32_t W = ag->world_size;
+  if (rs->world_size != W || ag->m != rs->m || ag->n != static_cast<int64_t>(W) * rs->k)
+    return fail(DT_ERR_INVALID, "the two GEMMs do not chain: need equal W and M, ag.n == W * rs.k");
+  if (rs->k % 8) return fail(DT_ERR_UNSUPPORTED, "F per rank must be a multiple of 8");
+  if (ag->out_dtype != DT_BF16 || (ag->ldc != 0 && ag->ldc != ag->n))
+    return fail(DT_ERR_INVALID, "h must be bf16 with ldc == ag.n");
+  if ((rs->lda != 0 && rs->lda != ag->n))
+    return fail(DT_ERR_INVALID, "rs.lda must be ag.n (the row stride of h)");
+  if (W < 1 || W > DT_MAX_WORLD) return fail(DT_ERR_INVALID, "world_size out of range");
+  dt_status s = dt_ag_gemm(x_shards, w1, h, ws_ag, ws_ag_bytes, ag, stream);
+  if (s != DT_OK) return s;
+  dt_args r = *rs;
+  r.lda = ag->n;
+  const void* a_blocks[DT_MAX_WORLD];
+  for (int q = 0; q < W; ++q)
+    a_blocks[q] = reinterpret_cast<const uint8_t*>(h) + static_cast<size_t>(q) * rs->k * 2;
+  return dt_gemm_rs(a_blocks, w2, out, ws_rs, ws_rs_bytes, &r, stream);
 }
 
 dt_status dt_debug_drop_transfer(int32_t step) {

@@ -84,6 +84,7 @@ struct KParams {
   int32_t Tm, KB, T;       // m-tiles in the window, k-blocks, tiles in the launch
   int32_t pieces_max;      // RS: most chunks one m-tile's rows touch (counter stride)
   int32_t ar_copies;       // 0: ReduceScatter; > 0: AllReduce into out[0 .. ar_copies-1]
+  int32_t act;             // AG epilogue activation: 0 none, 1 GELU (tanh form), 2 SiLU
   int32_t copy_ctas;       // AG in-kernel transfer: CTAs 0..copy_ctas-1 only move chunks
                            // (dedicated SMs); 0: transfer warps inside every compute CTA
   int32_t plain;           // 1: identity order, no flags, no arrival counting
@@ -310,6 +311,22 @@ __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_bas
 }
 
 // ============================================================================ epilogue
+// Activation of the fp32 accumulator before it is stored (the first GEMM of a feed-forward
+// block): GELU in its tanh form, 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), or SiLU,
+// x / (1 + exp(-x)); CUDA's tanhf / expf.
+__device__ __forceinline__ void apply_activation(uint32_t (&v)[32], int act) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float x = __uint_as_float(v[e]);
+    float y;
+    if (act == 1)
+      y = 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x)));
+    else
+      y = x / (1.0f + expf(-x));
+    v[e] = __float_as_uint(y);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -675,6 +692,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
       tmem_ld32(tbase + cb * 32, v);
       if (!row_ok) continue;
       if (!RS) {
+        if (p.act) apply_activation(v, p.act);
         store_row32<kStoreF32>(p.out[0], p.ldc, row, c0, p.g.N, v);
       } else if (!fused_rs) {  // baseline: partial of source q into slot [s][q]
         const size_t slot = static_cast<size_t>(s_row) * p.g.W + ti.q;
