@@ -72,6 +72,9 @@ def parse():
                     help="AllGather chunk x backend x swizzle sweep of --workload (default: the "
                          "largest AllGather); one JSON line per point")
     ap.add_argument("--sweep-chunks", default="64,128,256,512,2048")
+    ap.add_argument("--ffn-crossover", action="store_true",
+                    help="time the feed-forward block in AllGather+ReduceScatter form and in "
+                         "AllReduce form over a range of token counts M (one JSON line per M)")
     return ap.parse_args()
 
 
@@ -324,6 +327,80 @@ def run_sweep(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- FFN forms
+def run_ffn_crossover(args):
+    """The Llama-70B-like TP=8 feed-forward block (K=8192, F=8x3584, N=8192, GELU) for several
+    token counts M, in its two tensor-parallel forms (DITRON page, section 5.1, FFN module):
+    AG+RS: sequence-sharded X is gathered, out is reduce-scattered (dt_ffn_ag_rs);
+    AR:    X is replicated, H = act(X W1) needs no communication, out is all-reduced
+           (GEMM then dt_gemm_ar), with W output copies, or one shared output buffer."""
+    import torch
+
+    import tile_level_communication_gb300 as dt
+    from synth_inputs import make_ffn_inputs
+    w, k, fr, n = 8, 8192, 3584, 8192
+    ms_list = [1024, 2048, 4096, 8192, 16384]
+    inp = make_ffn_inputs(w, max(ms_list), k, fr, n, seed=2)
+    up = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    x_all = up(np.concatenate(inp.x_shards))
+    w1 = up(inp.w1)
+    w2 = [up(t) for t in inp.w2]
+    peak = peaks()["bf16_tflops_sustained"]
+
+    def timed(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    for m in ms_list:
+        x = x_all[:m]
+        ms_ = m // w
+        flops = 2.0 * m * w * fr * (k + n)
+        cr = max(ms_ // 1, 1)
+        h = torch.empty((m, w * fr), dtype=torch.bfloat16, device="cuda")
+        # AG + RS
+        ag = dt.make_args(w, m, w * fr, k, chunk_rows=cr, act="gelu_tanh")
+        rs = dt.make_args(w, m, n, fr, chunk_rows=cr, lda=w * fr)
+        ws_ag = torch.zeros(dt.workspace_size(ag, dt.OP_AG), dtype=torch.uint8, device="cuda")
+        ws_rs = torch.zeros(dt.workspace_size(rs, dt.OP_RS), dtype=torch.uint8, device="cuda")
+        shards = [x[q * ms_:(q + 1) * ms_] for q in range(w)]
+        outs_rs = [torch.empty((ms_, n), dtype=torch.bfloat16, device="cuda") for _ in range(w)]
+        t_agrs = timed(lambda: dt.ffn_ag_rs(shards, w1, w2, h, outs_rs, ws_ag, ws_rs, ag, rs),
+                       args.steps)
+        # AR: replicated X, plain GEMM with the activation, then GEMM-AllReduce
+        g1 = dt.make_args(1, m, w * fr, k, chunk_rows=m, act="gelu_tanh")
+        ws_g1 = torch.zeros(dt.workspace_size(g1, dt.OP_AG), dtype=torch.uint8, device="cuda")
+        ar = dt.make_args(w, m, n, fr, chunk_rows=cr, lda=w * fr)
+        ws_ar = torch.zeros(dt.workspace_size(ar, dt.OP_AR), dtype=torch.uint8, device="cuda")
+        a_blocks = [h[:, q * fr:(q + 1) * fr] for q in range(w)]
+        outs_ar = [torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for _ in range(w)]
+        shared = [outs_ar[0]] * w
+
+        def ar_form(outs):
+            dt.ag_gemm([x], w1, h, ws_g1, g1)
+            dt.gemm_ar(a_blocks, w2, outs, ws_ar, ar)
+        t_ar = timed(lambda: ar_form(outs_ar), args.steps)
+        t_ar1 = timed(lambda: ar_form(shared), args.steps)
+        for ws in (ws_ag, ws_rs, ws_g1, ws_ar):
+            if dt.check(ws)[0] != 0:
+                raise RuntimeError("device error in the crossover run")
+        print(json.dumps({"ffn_crossover_m": m, "gflop": flops / 1e9,
+                          "ag_rs_ms": t_agrs, "ar_copies_ms": t_ar, "ar_shared_ms": t_ar1,
+                          "ag_rs_tflops": flops / t_agrs / 1e9,
+                          "ar_shared_tflops": flops / t_ar1 / 1e9,
+                          "ag_rs_frac_of_sustained_peak": flops / t_agrs / 1e9 / peak}),
+              flush=True)
+        del h, ws_ag, ws_rs, ws_g1, ws_ar, outs_rs, outs_ar, shared, a_blocks
+        torch.cuda.empty_cache()
+    return 0
+
+
 # ----------------------------------------------------------------------------- fused arm
 def main():
     args = parse()
@@ -331,6 +408,8 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.ffn_crossover:
+        return run_ffn_crossover(args)
     import torch
 
     import tile_level_communication_gb300 as dt

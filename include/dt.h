@@ -144,8 +144,9 @@ dt_status dt_workspace_init(const dt_args* a, int op, void* workspace, size_t ws
  *              aligned, used by one call at a time.
  * Rows of shard s are gathered into the workspace chunk by chunk (own rank first, then
  * r+1, r+2, ...), each chunk's ready flag is released, and the persistent GEMM waits per
- * tile for the chunks of its rows (DITRON page section 3.2 "Gather模式").  K == 0 writes
- * zeros; M == 0 or N == 0 does nothing. */
+ * tile for the chunks of its rows (DITRON page section 3.2 "Gather模式").  With W == 1 there
+ * is nothing to gather and the GEMM reads the one shard in place (a plain GEMM).  K == 0
+ * writes zeros; M == 0 or N == 0 does nothing. */
 dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c,
                      void* workspace, size_t ws_bytes, const dt_args* a, void* stream);
 

@@ -241,3 +241,13 @@ def test_tuner_picks_a_measured_candidate_with_identical_output(dt, ragged):
     assert_close(to_f64(tuned), ref, "bf16", "tuned")
     default = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, rank=2)
     assert bits_equal(tuned, default)
+
+
+def test_single_rank_reads_its_shard_in_place(dt):
+    """W = 1: nothing to gather; a plain GEMM on the shard, padded rows included."""
+    inp = make_ag_inputs(1, 200, 40, 96, seed=91)
+    ref = _oracle(inp)
+    for act in ("none",):
+        c = _run(dt, inp, 200, 40, 96, lda=104, ldc=48, chunk_rows=64, backend="tma")
+        assert_close(to_f64(c, 40), ref, "bf16", "W=1")
+        assert torch.isnan(c[:, 40:].float()).all()

@@ -683,6 +683,14 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
 
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
   const int grid = static_cast<int>(std::min<int64_t>(d.T, sms));
+  if (d.W == 1) {
+    // one rank gathers nothing: the GEMM reads its shard where it is
+    if ((s = make_tmap(&p.tmA[0], a_shards[0], d.K, d.M, d.lda * 2, 64, kBM)) != DT_OK) return s;
+    p.wait_flags = 0;
+    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+    return DT_OK;
+  }
   if (d.backend == DT_XFER_COPY_ENGINE) {
     PfnWriteValue32 wv = write_value32();
     if (!wv) return fail(DT_ERR_CUDA, "cuStreamWriteValue32 entry point unavailable");
