@@ -455,6 +455,14 @@ dt_status ag_common(const void* const* a_shards, const void* b, void* c, void* w
   return check_ws(*d, ws, ws_bytes);
 }
 
+// The own rank's block is tile-aligned (no tile straddles it): its tiles can read the shard
+// in place and its chunks need no transfer.
+bool own_in_place(const Derived& d) {
+  if (d.W < 2) return false;
+  const int64_t lo = static_cast<int64_t>(d.rank) * d.Ms, hi = lo + d.Ms;
+  return lo % kBM == 0 && (hi % kBM == 0 || hi == d.M);
+}
+
 // copy chunk (s, j) of shard s into the gather buffer on `st`
 dt_status ce_copy_chunk(const Derived& d, const void* const* a_shards, uint8_t* gather, int32_t s,
                         int32_t j, cudaStream_t st) {
@@ -532,6 +540,10 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
   p.src_rows_contig = d.lda == d.K ? 1 : 0;
   if ((s = make_tmap(&p.tmA[0], p.gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
   if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
+  p.own_in_place = own_in_place(d) ? 1 : 0;
+  if (p.own_in_place &&
+      (s = make_tmap(&p.tmA[1], a_shards[d.rank], d.K, d.Ms, d.lda * 2, 64, kBM)) != DT_OK)
+    return s;
   const int use = a->num_sms > 0 ? std::min(a->num_sms, sms) : sms;
   if (d.copy_ctas >= use) return fail(DT_ERR_INVALID, "copy_ctas must leave SMs for the GEMM");
   p.copy_ctas = d.copy_ctas;
@@ -680,6 +692,10 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
   p.src_rows_contig = d.lda == d.K ? 1 : 0;
   if ((s = make_tmap(&p.tmA[0], gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
   if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
+  p.own_in_place = own_in_place(d) ? 1 : 0;
+  if (p.own_in_place &&
+      (s = make_tmap(&p.tmA[1], a_shards[d.rank], d.K, d.Ms, d.lda * 2, 64, kBM)) != DT_OK)
+    return s;
 
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
   const int grid = static_cast<int>(std::min<int64_t>(d.T, sms));
@@ -702,13 +718,16 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
     g_drop_transfer = -1;
     bool launched = false;
     for (int32_t tc = 0; tc < nchunks; ++tc) {
-      if (tc == d.nC && !launched) {  // own chunks are queued; start the GEMM
+      // start the GEMM once the chunks its first tiles need are queued (at once when the own
+      // rank's tiles read in place)
+      if ((tc == d.nC || p.own_in_place) && !launched) {
         cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream);
         if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
         launched = true;
       }
       int32_t cs, cj;
       ag_transfer_chunk(d.geom, tc, cs, cj);
+      if (p.own_in_place && cs == d.rank) continue;  // read in place
       if (tc == drop) continue;  // the message never arrives: its consumers time out
       if ((s = ce_copy_chunk(d, a_shards, gather, cs, cj, dev->side)) != DT_OK) return s;
       const CUdeviceptr flag =

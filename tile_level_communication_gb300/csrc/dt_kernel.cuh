@@ -85,6 +85,8 @@ struct KParams {
   int32_t pieces_max;      // RS: most chunks one m-tile's rows touch (counter stride)
   int32_t ar_copies;       // 0: ReduceScatter; > 0: AllReduce into out[0 .. ar_copies-1]
   int32_t act;             // AG epilogue activation: 0 none, 1 GELU (tanh form), 2 SiLU
+  int32_t own_in_place;    // AG: the own rank's tiles read its shard in place (tmA[1]) and
+                           // its chunks are not transferred (its block is tile-aligned)
   int32_t copy_ctas;       // AG in-kernel transfer: CTAs 0..copy_ctas-1 only move chunks
                            // (dedicated SMs); 0: transfer warps inside every compute CTA
   int32_t plain;           // 1: identity order, no flags, no arrival counting
@@ -214,7 +216,10 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
       raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
       continue;
     }
-    if (!RS && p.wait_flags) {
+    // local HBM as the cache of remote memory: the own rank's rows need no transfer
+    const int64_t own0 = static_cast<int64_t>(p.g.rank) * p.g.Ms;
+    const bool own_tile = !RS && p.own_in_place && ti.row0 >= own0 && ti.row_end <= own0 + p.g.Ms;
+    if (!RS && p.wait_flags && !own_tile) {
       // consumer_tile_wait: every chunk holding one of this tile's rows must have landed
       bool ok = true;
       for (int64_t g = ti.row0; g < ti.row_end && ok;) {
@@ -234,16 +239,16 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
       // engine); the TMA loads below read through the async proxy
       fence_proxy_async_global();
     }
-    const CUtensorMap* tA = &p.tmA[RS ? ti.q : 0];
+    const CUtensorMap* tA = &p.tmA[RS ? ti.q : (own_tile ? 1 : 0)];
     const CUtensorMap* tB = &p.tmB[RS ? ti.q : 0];
+    const int32_t a_row = static_cast<int32_t>(own_tile ? ti.row0 - own0 : ti.row0);
     bool ok = true;
     for (int32_t kb = 0; kb < p.KB; ++kb, ++kit) {
       const int st = static_cast<int>(kit % kStages);
       const uint32_t ph = (kit / kStages) & 1u;
       if (!wait_bar(p, L, L.empty(st), ph ^ 1u, 100 + st)) { ok = false; break; }
       mbar_expect_tx(L.full(st), kAStage + kBStage);
-      tma_load_2d(smem_u32(L.a + st * kAStage), tA, kb * kBK, static_cast<int32_t>(ti.row0),
-                  L.full(st));
+      tma_load_2d(smem_u32(L.a + st * kAStage), tA, kb * kBK, a_row, L.full(st));
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
         tma_load_2d(smem_u32(L.b + st * kBStage + jj * kBSlab), tB,
@@ -818,6 +823,7 @@ __device__ __forceinline__ void for_each_piece(const KParams& p, int32_t wid, in
     const int64_t base = static_cast<int64_t>(u) * pieces_rank +
                          static_cast<int64_t>(j) * p.pieces_full;
     const int32_t first = static_cast<int32_t>(((wid - base) % nw + nw) % nw);
+    if (p.own_in_place && s == p.g.rank) continue;  // read in place, never transferred
     for (int32_t pc = first; pc < total; pc += nw) {
       if (!f(s, j, s * p.g.nC + j, total, piece_of(p, pc, rows_c))) return;
     }
