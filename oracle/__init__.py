@@ -1,4 +1,5 @@
-"""CPU oracle for the chunk-centric fused AllGather-GEMM and GEMM-ReduceScatter.
+"""CPU oracle for the chunk-centric fused AllGather-GEMM, GEMM-ReduceScatter,
+GEMM-AllReduce and GEMM-AllToAll.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports, calls or links
 anything here: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline

@@ -41,6 +41,16 @@ Tn = ceil(N/BN); group width G (default 8).
   column tile n (AutoOverlap section 4.1: a chunk is made of compute tiles; the reduction
   is done per tile-sized piece of it).  Exactly the W source tiles (q, i, n), q = 0..W-1,
   write its rows, so it is complete after W arrivals.
+* AllToAll (GEMM-AllToAll, scatter mode by columns): rank q holds Ms rows of its own,
+  m-tiles i = 0 .. ceil(Ms/BM)-1 of those rows, and Y_q's N = W * Nw columns are
+  tiled per destination: Tnw = ceil(Nw/BN) column tiles c inside block h, tile column
+  n = h * Tnw + c, tile id (q * Tm + i) * (W * Tnw) + n.  Chunk (q, j) = rows
+  [j*Cr, min((j+1)*Cr, Ms)) of rank q; what goes to destination h is signalled per
+  (h, q, j).  Swizzle on: key(q, i, h) = dpos_q(h) * nC + (first chunk m-tile i
+  writes), dpos as in ReduceScatter (the next rank first, the own block last);
+  tiles sorted by (key, q, band, c, i), band taken among the m-tiles of the same
+  (q, key).  Swizzle off: lexicographic (q, i, n).  Chunk (h, q, j) is complete
+  when every tile of source q, destination h whose rows touch it has been stored.
 """
 from __future__ import annotations
 
@@ -176,4 +186,55 @@ def rs_expected_arrivals(world_size, m, n, chunk_rows, bm, bn):
                     writers = [(q, i2) for q in range(world_size) for i2 in range(tm)
                                if rows & set(range(i2 * bm, min(m, (i2 + 1) * bm)))]
                     out[(i, s, j, c)] = len(writers)
+    return out
+
+
+def a2a_geometry(world_size, ms, n, chunk_rows, bm, bn):
+    """Return (Nw, nC, Tm, Tnw): columns per destination, chunks per rank, m-tiles per
+    rank, column tiles per destination."""
+    if world_size < 1 or n % world_size:
+        raise ValueError("N must be a positive multiple of W")
+    nw = n // world_size
+    nc = cdiv(ms, chunk_rows) if ms > 0 else 0
+    return nw, nc, cdiv(ms, bm), cdiv(nw, bn)
+
+
+def a2a_mtile_chunks(i, ms, chunk_rows, bm):
+    """Chunks j of a rank that its m-tile i writes, by visiting every row."""
+    return {r // chunk_rows for r in range(i * bm, min((i + 1) * bm, ms))}
+
+
+def a2a_order(world_size, ms, n, chunk_rows, bm, bn, swizzle=True, group=8):
+    """Tile ids ((q * Tm + i) * W * Tnw + h * Tnw + c) of the GEMM-AllToAll in execution
+    order, all W source ranks interleaved step by step like the ReduceScatter."""
+    nw, nc, tm, tnw = a2a_geometry(world_size, ms, n, chunk_rows, bm, bn)
+    tn = world_size * tnw
+    if tm == 0 or tnw == 0:
+        return []
+    if not swizzle:
+        return list(range(world_size * tm * tn))
+    entries = []
+    for q in range(world_size):
+        for h in range(world_size):
+            keys = {i: rs_dpos(q, h, world_size) * nc + min(a2a_mtile_chunks(i, ms, chunk_rows, bm))
+                    for i in range(tm)}
+            band = _bands(keys, group)
+            for i in range(tm):
+                for c in range(tnw):
+                    entries.append((keys[i], q, band[i], c, i, h))
+    entries.sort()
+    return [(q * tm + i) * tn + h * tnw + c for (_, q, _, c, i, h) in entries]
+
+
+def a2a_expected_counts(world_size, ms, n, chunk_rows, bm, bn):
+    """{(h, q, j): tiles of source q, destination h whose rows touch chunk j}."""
+    nw, nc, tm, tnw = a2a_geometry(world_size, ms, n, chunk_rows, bm, bn)
+    out = {}
+    for h in range(world_size):
+        for q in range(world_size):
+            for j in range(nc):
+                rows = set(range(j * chunk_rows, min((j + 1) * chunk_rows, ms)))
+                writers = [(i, c) for i in range(tm) for c in range(tnw)
+                           if rows & set(range(i * bm, min(ms, (i + 1) * bm)))]
+                out[(h, q, j)] = len(writers)
     return out

@@ -11,6 +11,10 @@ the reduced rows are scattered to their owner ranks):
 * GEMM-ReduceScatter over W ranks: P_q = A_q @ B_q (rank q holds a K slice);
   S = sum_q P_q; rank s receives rows s*M/W .. (s+1)*M/W - 1 of S.
 * GEMM-AllReduce over W ranks: the same S; every rank receives all of it.
+* GEMM-AllToAll over W ranks (sequence parallelism, DITRON page section 4: SP uses
+  GEMM+AllToAll): rank q holds the sequence rows A_q and computes Y_q = A_q @ B_q; the
+  AllToAll sends column block h of Y_q to rank h, which stacks what it receives by source
+  rank.
 
 Inputs are float64 arrays holding exact bf16 values; outputs are float64.
 """
@@ -137,4 +141,44 @@ def gemm_rs_entries(a_list, b_list, dest, rows, cols):
             acc += float(np.dot(np.asarray(a_list[q][g], dtype=np.float64),
                                 np.asarray(b_list[q][:, int(cols[t])], dtype=np.float64)))
         out[t] = acc
+    return out
+
+
+def gemm_a2a(a_list, b_list):
+    """GEMM-AllToAll over W ranks, the sequence-parallel kernel of the DITRON page (section 4,
+    "序列并行SP: GEMMAllToAll"; section 4.2, weak scaling with a fixed sequence length per rank).
+
+    Rank q holds A_q [Ms, K] (its Ms sequence rows) and B_q [K, N], N = W * Nw.  It computes
+    Y_q = A_q @ B_q; the all-to-all moves column block h of Y_q (columns h*Nw .. (h+1)*Nw - 1,
+    e.g. the heads that rank h owns) to rank h, where the blocks are stacked in source-rank
+    order:  out_h[q*Ms + r, c] = Y_q[r, h*Nw + c].  Returns a list of W float64 arrays
+    [W*Ms, Nw].
+    """
+    w = len(a_list)
+    if w != len(b_list) or w < 1:
+        raise ValueError("need one A and one B per rank")
+    ys = [np.asarray(a_list[q], dtype=np.float64) @ np.asarray(b_list[q], dtype=np.float64)
+          for q in range(w)]
+    n = ys[0].shape[1]
+    if n % w:
+        raise ValueError("N must be a multiple of W")
+    nw = n // w
+    return [np.concatenate([ys[q][:, h * nw:(h + 1) * nw] for q in range(w)], axis=0)
+            for h in range(w)]
+
+
+def gemm_a2a_entries(a_list, b_list, dest, rows, cols):
+    """Selected entries out_dest[t][rows[t], cols[t]] of the GEMM-AllToAll, one dot each.
+
+    Row m of out_h is row m - q*Ms of source q = m // Ms; column c is column h*Nw + c of B_q.
+    """
+    w = len(a_list)
+    ms = a_list[0].shape[0]
+    nw = b_list[0].shape[1] // w
+    out = np.empty(len(rows), dtype=np.float64)
+    for t in range(len(rows)):
+        h, m, c = int(dest[t]), int(rows[t]), int(cols[t])
+        q = m // ms
+        out[t] = float(np.dot(np.asarray(a_list[q][m - q * ms], dtype=np.float64),
+                              np.asarray(b_list[q][:, h * nw + c], dtype=np.float64)))
     return out

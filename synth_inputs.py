@@ -121,6 +121,32 @@ def make_rs_inputs(world_size: int, m: int, n: int, k_rank: int, seed: int,
 
 
 @dataclass
+class A2AInputs:
+    world_size: int
+    a: list                 # W arrays uint16 [M/W, K]: each rank's sequence rows
+    b: list                 # W arrays uint16 [K, N] (the same array W times when shared)
+
+
+def make_a2a_inputs(world_size: int, m: int, n: int, k: int, seed: int,
+                    dist_a: str = "uniform", dist_b: str = "uniform",
+                    shared_b: bool = True) -> A2AInputs:
+    """Inputs of one GEMM-AllToAll: per rank A_q (M/W x K); one B (K x N) that every rank
+    holds (a replicated projection weight), or one per rank.  Draw order: A_0 .. A_{W-1},
+    then B (or B_0 .. B_{W-1})."""
+    if m % world_size or n % world_size:
+        raise ValueError("M and N must be multiples of the world size")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ms = m // world_size
+    a = [_draw_bf16(rng, dist_a, (ms, k)) for _ in range(world_size)]
+    if shared_b:
+        b0 = _draw_bf16(rng, dist_b, (k, n))
+        b = [b0] * world_size
+    else:
+        b = [_draw_bf16(rng, dist_b, (k, n)) for _ in range(world_size)]
+    return A2AInputs(world_size, a, b)
+
+
+@dataclass
 class FFNInputs:
     world_size: int
     x_shards: list          # W arrays uint16 [M/W, K]
@@ -147,9 +173,9 @@ def make_ffn_inputs(world_size: int, m: int, k: int, f_rank: int, n: int, seed: 
 class Workload:
     """One benchmark / parity workload: shapes, seed, distributions, chunking."""
     name: str
-    op: str                 # "ag" or "rs"
+    op: str                 # "ag", "rs", "ar", "ffn" or "a2a"
     world_size: int
-    m: int                  # total rows (gathered M for AG; M for RS)
+    m: int                  # total rows (gathered M for AG; M for RS; W x rows per rank for A2A)
     n: int
     k: int                  # AG: full K; RS: K per rank
     seed: int
@@ -161,7 +187,7 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        if self.op == "ag":
+        if self.op in ("ag", "a2a"):
             return 2.0 * self.m * self.n * self.k
         if self.op == "ffn":
             return 2.0 * self.m * self.world_size * self.f_rank * (self.k + self.n)
@@ -171,6 +197,9 @@ class Workload:
         # "rs" and "ar" (GEMM-AllReduce) take the same per-rank inputs
         if self.op == "ffn":
             return make_ffn_inputs(self.world_size, self.m, self.k, self.f_rank, self.n, self.seed,
+                                   self.dist_a, self.dist_b)
+        if self.op == "a2a":
+            return make_a2a_inputs(self.world_size, self.m, self.n, self.k, self.seed,
                                    self.dist_a, self.dist_b)
         if self.op == "ag":
             return make_ag_inputs(self.world_size, self.m, self.n, self.k, self.seed,
@@ -207,6 +236,15 @@ WORKLOADS = {
     "ffn_w8_m8192_k8192_f3584_n8192": Workload("ffn_w8_m8192_k8192_f3584_n8192", "ffn", 8, 8192,
                                                8192, 8192, 2, "normal(1.0)", "normal(0.02)", 1024,
                                                f_rank=3584, act="gelu_tanh"),
+    # GEMM-AllToAll (sequence parallelism), W=4, every edge ragged: 300 rows per rank, 200
+    # columns per destination, K=520, chunk 96; U[-1,1], seed 5
+    "a2a_w4_m1200_n800_k520": Workload("a2a_w4_m1200_n800_k520", "a2a", 4, 1200, 800, 520, 5,
+                                       "uniform", "uniform", 96),
+    # Llama-70B-like QKV projection under 8-way sequence parallelism: 2048 tokens per rank,
+    # hidden 8192, N = 64 query + 2 x 8 key/value heads of 128 = 10240 (1280 per rank after
+    # the all-to-all); activations N(0,1), weight N(0,0.02), seed 6
+    "a2a_w8_m16384_n10240_k8192": Workload("a2a_w8_m16384_n10240_k8192", "a2a", 8, 16384, 10240,
+                                           8192, 6, "normal(1.0)", "normal(0.02)", 512),
     # largest AllGather-GEMM (chunk/backend sweep), W=8, U[-1,1], seed 4
     "ag_w8_m16384_n8192_k8192": Workload("ag_w8_m16384_n8192_k8192", "ag", 8, 16384, 8192, 8192, 4,
                                          "uniform", "uniform", 256),
