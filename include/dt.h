@@ -1,12 +1,15 @@
 /*
- * dt.h - C ABI of the chunk-centric fused AllGather-GEMM and GEMM-ReduceScatter
- *        for one GB300 (sm_103a).
+ * dt.h - C ABI of the chunk-centric fused AllGather-GEMM, GEMM-ReduceScatter,
+ *        GEMM-AllReduce and GEMM-AllToAll for one GB300 (sm_103a).
  *
  * What is computed (DITRON page, section 4 "支持的并行策略": tensor parallelism overlaps
  * AllGather with GEMM and GEMM with ReduceScatter; Triton-distributed talk, "GEMM
  * ReduceScatter" paragraph):
  *   AllGather-GEMM     C   = concat_rows(A_0 .. A_{W-1}) * B
  *   GEMM-ReduceScatter out_s = rows [s*M/W, (s+1)*M/W) of  sum_q A_q * B_q
+ *   GEMM-AllReduce     out_r = sum_q A_q * B_q  (every rank)
+ *   GEMM-AllToAll      out_h = rows stacked by source q of columns [h*N/W, (h+1)*N/W) of
+ *                              A_q * B_q  (sequence parallelism, section 4 "序列并行SP")
  * W tensor-parallel ranks are emulated as W "virtual ranks" whose buffers live in the
  * one GPU's HBM.  The user-facing signature is the local GEMM's plus rank and world size
  * (AutoOverlap page, section 3: the fused operator keeps the local kernel's signature and
@@ -22,10 +25,10 @@
  *     own block last) and waits per tile only for the chunks that tile reads;
  *   - the chunk transfer runs on the copy engine, on in-kernel TMA bulk copies, or on
  *     vectorised loads/stores (AutoOverlap page, Table 2 / Fig. 7);
- *   - GEMM-ReduceScatter scatters fp32 partial tiles into the destination's slots; a
- *     reduction unit is the part of a chunk that one m-tile covers, times one column tile,
- *     and the last of its W arriving tiles reduces the partials in fixed rank order
- *     q = 0..W-1 (its own term straight from its accumulator), so results do not depend on
+ *   - GEMM-ReduceScatter: a reduction unit is the part of a chunk that one m-tile covers,
+ *     times one column tile; its W partial tiles are folded into an fp32 running sum in the
+ *     fixed order q = s-1, s-2, ..., s (the scatter schedule's own order; a partial that
+ *     arrives early waits in a park slot) and rounded once, so results do not depend on
  *     tile order, chunk size or backend.
  *
  * Conventions
@@ -76,16 +79,17 @@ typedef enum {
 
 typedef enum { DT_BF16 = 0, DT_F32 = 1 } dt_dtype;
 
-typedef enum { DT_OP_AG_GEMM = 0, DT_OP_GEMM_RS = 1, DT_OP_GEMM_AR = 2 } dt_op;
+typedef enum { DT_OP_AG_GEMM = 0, DT_OP_GEMM_RS = 1, DT_OP_GEMM_AR = 2, DT_OP_GEMM_A2A = 3 } dt_op;
 
 /* Problem description shared by every call.  Fill with dt_args_default() first. */
 typedef struct dt_args {
   int32_t world_size;  /* W, 1..DT_MAX_WORLD                                               */
   int32_t rank;        /* AllGather-GEMM: the rank whose view is computed (0..W-1);
                           its own shard is "local", the other W-1 are "remote".  RS: unused */
-  int64_t m;           /* rows: gathered M for AG, M for RS; M % W == 0                    */
-  int64_t n;           /* columns of B and C; multiple of 8                                */
-  int64_t k;           /* AG: full K (multiple of 8); RS: K per rank                       */
+  int64_t m;           /* rows: gathered M for AG, M for RS, W x rows per rank for A2A;
+                          M % W == 0                                                       */
+  int64_t n;           /* columns of B and C; multiple of 8 (A2A: N/W multiple of 8)       */
+  int64_t k;           /* AG: full K (multiple of 8); RS: K per rank; A2A: K               */
   int64_t chunk_rows;  /* rows per communication chunk, >= 1                               */
   int32_t swizzle;     /* 1: rank-aware swizzle order; 0: naive order (all ranks tile 0)   */
   int32_t backend;     /* dt_xfer, AllGather chunk transfer                                */
@@ -95,7 +99,7 @@ typedef struct dt_args {
   int32_t group;       /* m-tiles per band of the in-chunk raster; 0 = 8                   */
   int64_t lda;         /* AG: of every shard; RS: of every A_q   (0 = K)                   */
   int64_t ldb;         /* of B / every B_q                       (0 = N)                   */
-  int64_t ldc;         /* of C / every out_s                     (0 = N)                   */
+  int64_t ldc;         /* of C / every out_s (0 = N); A2A: of every out_h (0 = N/W)        */
   int64_t timeout_us;  /* bound of every device wait; 0 = 2 s (env DT_WAIT_TIMEOUT_US)     */
   int32_t num_sms;     /* persistent grid size; 0 = all SMs                                */
   int32_t copy_ctas;   /* AG with DT_XFER_TMA / DT_XFER_LDST: CTAs of the grid that only move
@@ -126,8 +130,9 @@ const char* dt_last_error(void);
 
 /* Bytes of device workspace that `op` (dt_op) needs for `a`; 0 if `a` is invalid.
  * AG: control block + per-chunk flags/counters + tile order + the gather buffer
- *     (M x K bf16).  RS: control block + per-unit counters + tile order + the fp32
- *     partial slots (W x W x M/W x N fp32; the last arriving partial is never stored). */
+ *     (M x K bf16).  RS / AR: control block + per-unit words + tile order + the fp32
+ *     running sums (M x N) and park slots (W-1 per destination, M/W x N each).
+ *     A2A: control block + per-chunk counters and flags + tile order. */
 size_t dt_workspace_size(const dt_args* a, int op);
 
 /* Zero the control block of a workspace laid out for (a, op) on `stream` and forget the
@@ -155,11 +160,12 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c,
  *   b   : host array of W device pointers, B_q [K x N] bf16, ld = ldb
  *   out : host array of W device pointers, out_s [M/W x N] (out_dtype), ld = ldc
  * Every tile (q, i, n) is one partial product.  For each unit (rows of m-tile i inside one
- * chunk, column tile n) the tile either pushes its fp32 rows into destination s's slot q and
- * counts its arrival (notify), or, when the other W-1 partials are already in, sums all W in
- * order q = 0..W-1 with its own term taken from its accumulator and writes out_s (DITRON page
- * section 3.2 "Scatter模式"; Triton-distributed talk, notify/wait of the GEMM-ReduceScatter
- * example). */
+ * chunk, column tile n) the partials are folded in the fixed order d = 0..W-1, partial d from
+ * source q = (s - d - 1) mod W: a tile whose partial is next in order adds it to the fp32
+ * running sum (the last one rounds into out_s); one that arrives early parks it, and whoever
+ * advances the unit past it folds it (notify through one atomic word per unit; nobody
+ * waits).  DITRON page section 3.2 "Scatter模式"; Triton-distributed talk, notify/wait of
+ * the GEMM-ReduceScatter example. */
 dt_status dt_gemm_rs(const void* const* a, const void* const* b, void* const* out,
                      void* workspace, size_t ws_bytes, const dt_args* a_args, void* stream);
 
@@ -172,6 +178,36 @@ dt_status dt_gemm_rs(const void* const* a, const void* const* b, void* const* ou
  * Workspace: dt_workspace_size(a, DT_OP_GEMM_AR) (the same layout as the ReduceScatter). */
 dt_status dt_gemm_ar(const void* const* a, const void* const* b, void* const* out,
                      void* workspace, size_t ws_bytes, const dt_args* a_args, void* stream);
+
+/* Fused GEMM-AllToAll over all W virtual ranks (sequence parallelism: DITRON page, section 4
+ * "序列并行SP: GEMMAllToAll", section 4.2 weak scaling with a fixed sequence length per rank).
+ * Rank q holds its M/W sequence rows A_q and computes Y_q = A_q * B_q (N = W*Nw columns, e.g.
+ * the attention heads of all ranks, block h being those that rank h owns); the all-to-all
+ * gives rank h columns [h*Nw, (h+1)*Nw) of every Y_q, stacked by source rank:
+ *     out_h[q*M/W + r, c] = Y_q[r, h*Nw + c].
+ *   a   : host array of W device pointers, A_q [M/W x K] bf16, ld = lda
+ *   b   : host array of W device pointers, B_q [K x N] bf16, ld = ldb (a replicated weight
+ *         passes the same pointer W times)
+ *   out : host array of W device pointers, out_h [M x N/W] (out_dtype), ld = ldc (0 = N/W)
+ * Requires N % W == 0 and (N/W) % 8 == 0.  Column tiles never cross a destination's block;
+ * every tile's epilogue stores its rows straight into out_h (push, scatter mode: rank q
+ * computes destination q+1's block first and its own last, chunk by chunk in row order) and
+ * counts itself on chunk (h, q, j) = rows [j*chunk_rows, ..) of source q; the count's last
+ * tile releases that chunk's ready flag (notify).  Results do not depend on the order, chunk
+ * size or group width (each output is one product).  Workspace:
+ * dt_workspace_size(a, DT_OP_GEMM_A2A) (control block, counters, flags, tile order only).
+ * K == 0 writes zeros; M == 0 or N == 0 does nothing. */
+dt_status dt_gemm_a2a(const void* const* a, const void* const* b, void* const* out,
+                      void* workspace, size_t ws_bytes, const dt_args* a_args, void* stream);
+
+/* The AllToAll's chunk signals after the last dt_gemm_a2a call on `workspace`: synchronises
+ * `stream`, then copies the W*W*nC ready flags and completion counters, index
+ * (h*W + q)*nC + j with nC = ceil((M/W)/chunk_rows), to the host arrays `flags` and
+ * `counts` (either may be NULL), and the call's epoch to *epoch (may be NULL).  After a
+ * completed call every flag equals the epoch and every counter is back to 0.  `len` must
+ * equal W*W*nC. */
+dt_status dt_a2a_signals(const dt_args* a, void* workspace, void* stream, uint32_t* flags,
+                         uint32_t* counts, int64_t len, uint32_t* epoch);
 
 /* Tensor-parallel feed-forward block, AllGather + ReduceScatter form, over W virtual ranks
  * (DITRON page, section 5.1 "FFN模块"; Triton-distributed talk: the AllGather-GEMM feeds the
@@ -201,10 +237,21 @@ dt_status dt_gemm_rs_kernel_overlap(const void* const* a, const void* const* b,
 dt_status dt_gemm_ar_kernel_overlap(const void* const* a, const void* const* b,
                                     void* const* out, void* workspace, size_t ws_bytes,
                                     const dt_args* a_args, void* stream);
+/* GEMM-AllToAll baseline: W GEMM launches, step d computing on every rank q the column
+ * block of destination (q + d + 1) mod W into the rank's own buffer y_q, each followed on a
+ * second stream by the W copy-engine copies of that step's blocks into out_h; the copies of
+ * step d overlap the GEMM of step d+1.
+ *   y : host array of W device pointers, y_q [M/W x N] (out_dtype), ld = N, scratch owned
+ *       by the caller (each rank's local GEMM output). */
+dt_status dt_gemm_a2a_kernel_overlap(const void* const* a, const void* const* b,
+                                     void* const* y, void* const* out, void* workspace,
+                                     size_t ws_bytes, const dt_args* a_args, void* stream);
 
 /* Tile execution order of `op` for `a` computed on the host: order[p] is the tile run at
- * position p.  AG tile id = i*Tn + n; RS tile id = (q*Tm + i)*Tn + n, with
- * Tm = ceil(M/tile_m), Tn = ceil(N/tile_n).  `len` must equal the tile count.
+ * position p.  AG tile id = i*Tn + n; RS / AR tile id = (q*Tm + i)*Tn + n, with
+ * Tm = ceil(M/tile_m), Tn = ceil(N/tile_n); A2A tile id = (q*Tm + i)*Tn + h*Tnw + c with
+ * Tm = ceil((M/W)/tile_m), Tnw = ceil((N/W)/tile_n), Tn = W*Tnw.  `len` must equal the tile
+ * count.
  * (DITRON page section 3.2: swizzle_func maps the original tile id to the new one.) */
 dt_status dt_swizzle_plan(const dt_args* a, int op, int32_t* order_host, int64_t len);
 

@@ -142,3 +142,58 @@ def test_host_plan_random_sweep(dt):
         a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr)
         assert dt.swizzle_plan(a, dt.OP_AG).tolist() == oplan.ag_order(w, r, m, n, cr, 128, 256)
         assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(w, m, n, cr, 128, 256)
+
+
+# ----------------------------------------------------------------------------- AllToAll
+
+A2A_GRID = [
+    # (W, Ms, Nw, Cr): each rank's Ms rows tiled on their own, Nw columns per destination
+    (1, 100, 264, 64), (2, 256, 512, 128), (2, 3, 8, 1), (4, 300, 200, 96), (3, 130, 8, 1000),
+    (8, 2048, 1280, 512), (8, 2048, 1280, 100), (5, 7, 520, 3), (16, 256, 16, 64),
+]
+
+
+@pytest.mark.parametrize("case", A2A_GRID)
+@pytest.mark.parametrize("swizzle", [True, False])
+def test_host_plan_matches_oracle_a2a(dt, case, swizzle):
+    w, ms, nw, cr = case
+    a = dt.make_args(w, w * ms, w * nw, 8, chunk_rows=cr, swizzle=swizzle)
+    got = dt.swizzle_plan(a, dt.OP_A2A)
+    assert got.tolist() == oplan.a2a_order(w, ms, w * nw, cr, 128, 256, swizzle), case
+
+
+def test_host_plan_a2a_random_sweep(dt):
+    rng = np.random.Generator(np.random.PCG64(6))
+    for _ in range(40):
+        w = int(rng.integers(1, 9))
+        ms = int(rng.integers(1, 600))
+        nw = 8 * int(rng.integers(1, 90))
+        cr = int(rng.integers(1, 2 * ms + 2))
+        g = int(rng.integers(1, 10))
+        a = dt.make_args(w, w * ms, w * nw, 8, chunk_rows=cr, group=g)
+        assert dt.swizzle_plan(a, dt.OP_A2A).tolist() == \
+            oplan.a2a_order(w, ms, w * nw, cr, 128, 256, True, g)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(world_size=3, m=9, n=16, k=8), "DT_ERR_INVALID"),        # N % W
+    (dict(world_size=2, m=8, n=24, k=8), "DT_ERR_UNSUPPORTED"),    # N/W % 8
+    (dict(world_size=2, m=7, n=16, k=8), "DT_ERR_INVALID"),        # M % W
+    (dict(world_size=2, m=8, n=32, k=8, ldc=8), "DT_ERR_INVALID"),  # ldc < N/W
+])
+def test_a2a_argument_errors_are_synchronous(dt, kw, status):
+    w = kw.pop("world_size")
+    m, n, k = kw.pop("m"), kw.pop("n"), kw.pop("k")
+    a = dt.make_args(w, m, n, k, **kw)
+    assert dt.capi.lib().dt_workspace_size(ctypes.byref(a), dt.OP_A2A) == 0
+    with pytest.raises(dt.DtError) as ei:
+        dt.gemm_a2a([16] * w, [16] * w, [16] * w, 256, a, stream=0, ws_bytes=1 << 30)
+    assert ei.value.status == getattr(dt.capi, status)
+
+
+def test_a2a_workspace_holds_only_control(dt):
+    # K is not restricted (lda pads the rows); the workspace is the control block alone
+    a = dt.make_args(8, 16384, 10240, 8190, chunk_rows=512, lda=8192)
+    need = dt.workspace_size(a, dt.OP_A2A)
+    assert 0 < need < (1 << 20)
+    assert dt.a2a_chunks(a) == 8 * 8 * 4

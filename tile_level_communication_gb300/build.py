@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdt.so")
-SOURCES = ["dt_capi.cu", "dt_ag.cu", "dt_rs.cu", "dt_static_ws.cu"]
+SOURCES = ["dt_capi.cu", "dt_ag.cu", "dt_rs.cu", "dt_a2a.cu", "dt_static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

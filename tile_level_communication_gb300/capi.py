@@ -1,6 +1,7 @@
 """ctypes binding of libdt.so (include/dt.h): argument marshalling only.
 
-Every step of the fused AllGather-GEMM / GEMM-ReduceScatter runs in the library's CUDA
+Every step of the fused AllGather-GEMM / GEMM-ReduceScatter / GEMM-AllReduce /
+GEMM-AllToAll runs in the library's CUDA
 kernels; this module converts Python arguments into the C structs and pointers, calls the
 C entry point with the same name, and raises ``DtError`` on a non-OK status.  Tensors may be
 anything with ``data_ptr()`` (torch tensors) or plain integer addresses.  When the library
@@ -20,7 +21,7 @@ DT_OK, DT_ERR_INVALID, DT_ERR_UNSUPPORTED, DT_ERR_TIMEOUT, DT_ERR_CUDA, DT_ERR_W
 BACKENDS = {"auto": 0, "copy_engine": 1, "tma": 2, "ldst": 3}
 DTYPES = {"bf16": 0, "f32": 1}
 ACTS = {"none": 0, "gelu_tanh": 1, "silu": 2}
-OP_AG, OP_RS, OP_AR = 0, 1, 2
+OP_AG, OP_RS, OP_AR, OP_A2A = 0, 1, 2, 3
 MAX_WORLD = 16
 
 # every function include/dt.h declares: name -> (restype, argtypes)
@@ -39,6 +40,9 @@ _SIGS = {
     "dt_gemm_rs_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_gemm_ar": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_gemm_ar_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_gemm_a2a": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_gemm_a2a_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_a2a_signals": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int64, _P]),
     "dt_swizzle_plan": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64]),
     "dt_swizzle_plan_device": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64, _P]),
     "dt_check": (ctypes.c_int, [_P, _P, _P]),
@@ -224,7 +228,45 @@ def gemm_rs_kernel_overlap(a_list, b_list, out_list, workspace, args: DtArgs, st
                                            _stream(stream)))
 
 
+def gemm_a2a(a_list, b_list, out_list, workspace, args: DtArgs, stream=None, ws_bytes=None):
+    """Fused GEMM-AllToAll: out_list[h] ([M, N/W]) receives columns h*N/W .. of every
+    A_q @ B_q, rows stacked by source rank q."""
+    _raise(lib().dt_gemm_a2a(_ptr_array(a_list), _ptr_array(b_list), _ptr_array(out_list),
+                             _ptr(workspace), _nbytes(workspace, ws_bytes), ctypes.byref(args),
+                             _stream(stream)))
+
+
+def gemm_a2a_kernel_overlap(a_list, b_list, y_list, out_list, workspace, args: DtArgs,
+                            stream=None, ws_bytes=None):
+    """Baseline: per-step GEMMs into the ranks' own y_q ([M/W, N]) and copy-engine copies."""
+    _raise(lib().dt_gemm_a2a_kernel_overlap(_ptr_array(a_list), _ptr_array(b_list),
+                                            _ptr_array(y_list), _ptr_array(out_list),
+                                            _ptr(workspace), _nbytes(workspace, ws_bytes),
+                                            ctypes.byref(args), _stream(stream)))
+
+
+def a2a_chunks(args: DtArgs) -> int:
+    ms = args.m // args.world_size
+    nc = -(-ms // args.chunk_rows) if ms > 0 else 0
+    return args.world_size * args.world_size * nc
+
+
+def a2a_signals(args: DtArgs, workspace, stream=None):
+    """(flags, counts, epoch) of the last GEMM-AllToAll call on ``workspace``: uint32 arrays
+    indexed (h * W + q) * nC + j (synchronises ``stream``)."""
+    n = a2a_chunks(args)
+    flags = np.zeros(n, dtype=np.uint32)
+    counts = np.zeros(n, dtype=np.uint32)
+    epoch = ctypes.c_uint32(0)
+    _raise(lib().dt_a2a_signals(ctypes.byref(args), _ptr(workspace), _stream(stream),
+                                flags.ctypes.data, counts.ctypes.data, n, ctypes.byref(epoch)))
+    return flags, counts, int(epoch.value)
+
+
 def tile_count(args: DtArgs, op: int) -> int:
+    if op == OP_A2A:  # each rank's rows tiled on their own, columns per destination block
+        w = args.world_size
+        return w * -(-(args.m // w) // 128) * w * -(-(args.n // w) // 256)
     tm = -(-args.m // 128)
     tn = -(-args.n // 256)
     return (1 if op == OP_AG else args.world_size) * tm * tn  # RS and AR: all W ranks' tiles

@@ -7,7 +7,7 @@ namespace dt {
 namespace {
 template <int COPY, bool F32>
 cudaError_t launch_one(const KParams& p, int grid, bool cooperative, cudaStream_t stream) {
-  auto kern = fused_gemm_kernel<false, COPY, F32>;
+  auto kern = fused_gemm_kernel<kOpAG, COPY, F32>;
   const int smem = kernel_smem_bytes(false, COPY);
   static bool configured = false;
   if (!configured) {

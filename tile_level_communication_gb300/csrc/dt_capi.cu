@@ -123,8 +123,9 @@ uint64_t default_timeout_ns() {
 
 dt_status derive(const dt_args* a, int op, Derived* d) {
   if (!a) return fail(DT_ERR_INVALID, "args is NULL");
-  if (op != DT_OP_AG_GEMM && op != DT_OP_GEMM_RS && op != DT_OP_GEMM_AR)
+  if (op != DT_OP_AG_GEMM && op != DT_OP_GEMM_RS && op != DT_OP_GEMM_AR && op != DT_OP_GEMM_A2A)
     return fail(DT_ERR_INVALID, "unknown op %d", op);
+  const bool a2a = op == DT_OP_GEMM_A2A;
   d->op = op;
   d->W = a->world_size;
   if (d->W < 1 || d->W > DT_MAX_WORLD)
@@ -143,12 +144,18 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   if (d->N % 8) return fail(DT_ERR_UNSUPPORTED, "N=%lld must be a multiple of 8", (long long)d->N);
   if (op == DT_OP_AG_GEMM && d->K % 8)
     return fail(DT_ERR_UNSUPPORTED, "AllGather K=%lld must be a multiple of 8", (long long)d->K);
+  if (a2a && d->N % d->W)
+    return fail(DT_ERR_INVALID, "AllToAll N=%lld is not a multiple of W=%d", (long long)d->N, d->W);
+  if (a2a && (d->N / d->W) % 8)
+    return fail(DT_ERR_UNSUPPORTED, "AllToAll N/W=%lld must be a multiple of 8 (16-byte column blocks)",
+                (long long)(d->N / d->W));
   d->Cr = a->chunk_rows;
   if (d->Cr < 1) return fail(DT_ERR_INVALID, "chunk_rows must be >= 1");
   d->lda = a->lda ? a->lda : d->K;
   d->ldb = a->ldb ? a->ldb : d->N;
-  d->ldc = a->ldc ? a->ldc : d->N;
-  if (d->lda < d->K || d->ldb < d->N || d->ldc < d->N)
+  const int64_t out_cols = a2a ? d->N / d->W : d->N;  // columns of each output
+  d->ldc = a->ldc ? a->ldc : out_cols;
+  if (d->lda < d->K || d->ldb < d->N || d->ldc < out_cols)
     return fail(DT_ERR_INVALID, "leading dimension smaller than the row length");
   if ((d->lda % 8) || (d->ldb % 8) || (d->ldc % 8))
     return fail(DT_ERR_INVALID, "leading dimensions must be multiples of 8 elements (16-byte rows)");
@@ -162,7 +169,8 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   d->timeout_ns = a->timeout_us > 0 ? static_cast<uint64_t>(a->timeout_us) * 1000ull
                                     : default_timeout_ns();
   d->Ms = d->M / d->W;
-  d->geom = make_geom(d->W, d->rank, d->M, d->N, d->Cr, kBM, kBN, d->G, d->swizzle ? 1 : 0);
+  d->geom = a2a ? make_geom_a2a(d->W, d->M, d->N, d->Cr, kBM, kBN, d->G, d->swizzle ? 1 : 0)
+              : make_geom(d->W, d->rank, d->M, d->N, d->Cr, kBM, kBN, d->G, d->swizzle ? 1 : 0);
   d->nC = d->geom.nC;
   d->Tm = d->geom.Tm;
   d->Tn = d->geom.Tn;
@@ -170,9 +178,9 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   const int64_t T64 = (op == DT_OP_AG_GEMM ? 1 : d->W) * static_cast<int64_t>(d->Tm) * d->Tn;
   if (T64 >= (1ll << 31)) return fail(DT_ERR_UNSUPPORTED, "too many tiles");
   d->T = static_cast<int32_t>(T64);
-  if (op != DT_OP_AG_GEMM && static_cast<int64_t>(d->W - 1) * d->M >= (1ll << 31))
+  if ((op == DT_OP_GEMM_RS || op == DT_OP_GEMM_AR) && static_cast<int64_t>(d->W - 1) * d->M >= (1ll << 31))
     return fail(DT_ERR_UNSUPPORTED, "(W-1)*M must be below 2^31");
-  if (static_cast<int64_t>(d->W) * d->nC >= (1ll << 24))
+  if (static_cast<int64_t>(d->W) * d->W * d->nC >= (1ll << 24))
     return fail(DT_ERR_UNSUPPORTED, "too many chunks; raise chunk_rows");
   d->ld_gather = d->K;  // K % 8 == 0: 16-byte rows, back to back
   int be = a->backend;
@@ -203,6 +211,12 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     off = align_up(off + 4 * nchunks, 256);
     d->off_pieces = off;
     off = align_up(off + 4 * nchunks, 256);
+  } else if (a2a) {
+    // per (destination h, source q, chunk j): count of stored tiles, then the ready flag
+    d->off_cnt = off;
+    off = align_up(off + 4 * nchunks * d->W, 256);
+    d->off_ready = off;
+    off = align_up(off + 4 * nchunks * d->W, 256);
   } else {
     d->pieces_max = d->Tm > 0 && d->Ms > 0 ? rs_pieces_max(d->geom) : 0;
     d->off_cnt = off;
@@ -214,6 +228,8 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   d->off_data = off;
   if (op == DT_OP_AG_GEMM)
     d->total = off + static_cast<size_t>(d->M) * d->ld_gather * 2;
+  else if (a2a)
+    d->total = off;
   else
     d->total = off + static_cast<size_t>(d->W) * d->W * d->Ms * d->N * 4;
   return DT_OK;
@@ -295,15 +311,7 @@ dt_status dev_ctx(DevCtx** out) {
 __global__ void plan_kernel(Geom g, int op, int32_t* order, int32_t T) {
   const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
-  int64_t pos;
-  if (op == DT_OP_AG_GEMM) {
-    pos = ag_position(g, t / g.Tn, t % g.Tn);
-  } else {
-    const int32_t per_q = g.Tm * g.Tn;
-    const int32_t q = t / per_q;
-    const int32_t rem = t - q * per_q;
-    pos = rs_position(g, q, rem / g.Tn, rem % g.Tn);
-  }
+  const int64_t pos = tile_position(g, op, t);
   if (pos >= 0 && pos < T) order[pos] = t;
 }
 
@@ -319,15 +327,7 @@ __global__ void prepare_kernel(Geom g, int op, int32_t* order, int32_t T, uint32
   const int64_t t0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   for (int64_t w = t0; w < ctl_words; w += stride) ctl[w] = 0u;
   for (int64_t t = t0; t < T; t += stride) {
-    int64_t pos;
-    if (op == DT_OP_AG_GEMM) {
-      pos = ag_position(g, static_cast<int32_t>(t / g.Tn), static_cast<int32_t>(t % g.Tn));
-    } else {
-      const int32_t per_q = g.Tm * g.Tn;
-      const int32_t q = static_cast<int32_t>(t / per_q);
-      const int32_t rem = static_cast<int32_t>(t - static_cast<int64_t>(q) * per_q);
-      pos = rs_position(g, q, rem / g.Tn, rem % g.Tn);
-    }
+    const int64_t pos = tile_position(g, op, t);
     if (pos >= 0 && pos < T) order[pos] = static_cast<int32_t>(t);
   }
 }
@@ -620,14 +620,7 @@ dt_status dt_swizzle_plan(const dt_args* a, int op, int32_t* order, int64_t len)
   if (!order) return fail(DT_ERR_INVALID, "order is NULL");
   std::vector<uint8_t> seen(d.T, 0);
   for (int32_t t = 0; t < d.T; ++t) {
-    int64_t pos;
-    if (op == DT_OP_AG_GEMM) {
-      pos = ag_position(d.geom, t / d.Tn, t % d.Tn);
-    } else {
-      const int32_t per_q = d.Tm * d.Tn;
-      const int32_t q = t / per_q, rem = t - q * per_q;
-      pos = rs_position(d.geom, q, rem / d.Tn, rem % d.Tn);
-    }
+    const int64_t pos = tile_position(d.geom, op, t);
     if (pos < 0 || pos >= d.T || seen[pos]) return fail(DT_ERR_INVALID, "plan is not a bijection");
     seen[pos] = 1;
     order[pos] = t;
@@ -963,6 +956,142 @@ dt_status dt_gemm_rs_kernel_overlap(const void* const* a_, const void* const* b_
 dt_status dt_gemm_ar_kernel_overlap(const void* const* a_, const void* const* b_, void* const* out,
                                     void* ws, size_t ws_bytes, const dt_args* a, void* stream) {
   return reduce_kernel_overlap(a_, b_, out, ws, ws_bytes, a, stream, DT_OP_GEMM_AR);
+}
+
+// ------------------------------------------------------------------------------ AllToAll
+static dt_status a2a_common(const void* const* a_, const void* const* b_, void* const* out,
+                            void* ws, size_t ws_bytes, const dt_args* a, Derived* d) {
+  dt_status s = derive(a, DT_OP_GEMM_A2A, d);
+  if (s != DT_OK) return s;
+  if (!a_ || !b_ || !out) return fail(DT_ERR_INVALID, "a, b and out arrays must be non-NULL");
+  if (d->M == 0 || d->N == 0) return DT_OK;
+  for (int i = 0; i < d->W; ++i) {
+    if (!a_[i] || !is_aligned(a_[i], 16) || !b_[i] || !is_aligned(b_[i], 16))
+      return fail(DT_ERR_INVALID, "A_%d / B_%d NULL or not 16-byte aligned", i, i);
+    if (!out[i] || !is_aligned(out[i], 16))
+      return fail(DT_ERR_INVALID, "out_%d NULL or not 16-byte aligned", i);
+  }
+  return check_ws(*d, ws, ws_bytes);
+}
+
+static dt_status a2a_params(KParams& p, const Derived& d, const void* const* a_,
+                            const void* const* b_, void* ws, uint32_t epoch) {
+  fill_common(p, d, ws, epoch);
+  uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+  p.unit_cnt = reinterpret_cast<uint32_t*>(w + d.off_cnt);
+  p.ready = reinterpret_cast<uint32_t*>(w + d.off_ready);
+  p.row_hi = d.Ms;  // each rank's rows are tiled on their own
+  p.a2a_step = -1;
+  for (int q = 0; q < d.W; ++q) {
+    dt_status s = make_tmap(&p.tmA[q], a_[q], d.K, d.Ms, d.lda * 2, 64, kBM);
+    if (s != DT_OK) return s;
+    s = make_tmap(&p.tmB[q], b_[q], d.N, d.K, d.ldb * 2, 64, kBK);
+    if (s != DT_OK) return s;
+  }
+  return DT_OK;
+}
+
+static dt_status zero_a2a_outputs(const Derived& d, void* const* out, cudaStream_t stream) {
+  const int64_t eb = d.f32 ? 4 : 2;
+  for (int h = 0; h < d.W; ++h) {
+    const dt_status s = launch_zero(out[h], d.M, d.geom.Nw * eb, d.ldc * eb, stream);
+    if (s != DT_OK) return s;
+  }
+  return DT_OK;
+}
+
+dt_status dt_gemm_a2a(const void* const* a_, const void* const* b_, void* const* out, void* ws,
+                      size_t ws_bytes, const dt_args* a, void* stream_) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = a2a_common(a_, b_, out, ws, ws_bytes, a, &d);
+  if (s != DT_OK || d.M == 0 || d.N == 0) return s;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (d.K == 0) return zero_a2a_outputs(d, out, stream);
+  DevCtx* dev = nullptr;
+  if ((s = dev_ctx(&dev)) != DT_OK) return s;
+  uint32_t epoch = 0;
+  if ((s = prepare_workspace(d, ws, stream, &epoch)) != DT_OK) return s;
+  KParams p;
+  if ((s = a2a_params(p, d, a_, b_, ws, epoch)) != DT_OK) return s;
+  for (int h = 0; h < d.W; ++h) p.out[h] = out[h];
+  const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
+  const int grid = static_cast<int>(std::min<int64_t>(d.T, sms));
+  cudaError_t e = launch_a2a_kernel(p, d.f32, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fused GEMM-AllToAll launch");
+  return DT_OK;
+}
+
+dt_status dt_gemm_a2a_kernel_overlap(const void* const* a_, const void* const* b_,
+                                     void* const* y, void* const* out, void* ws, size_t ws_bytes,
+                                     const dt_args* a, void* stream_) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = a2a_common(a_, b_, out, ws, ws_bytes, a, &d);
+  if (s != DT_OK || d.M == 0 || d.N == 0) return s;
+  if (!y) return fail(DT_ERR_INVALID, "y array must be non-NULL");
+  for (int q = 0; q < d.W; ++q)
+    if (!y[q] || !is_aligned(y[q], 16)) return fail(DT_ERR_INVALID, "y_%d NULL or not 16-byte aligned", q);
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (d.K == 0) return zero_a2a_outputs(d, out, stream);
+  DevCtx* dev = nullptr;
+  if ((s = dev_ctx(&dev)) != DT_OK) return s;
+  KParams p;
+  if ((s = a2a_params(p, d, a_, b_, ws, 0)) != DT_OK) return s;
+  p.tag = nullptr;
+  p.plain = 1;
+  p.ldc = d.N;  // the ranks' own Y_q
+  for (int q = 0; q < d.W; ++q) p.out[q] = y[q];
+  p.T = d.W * d.Tm * d.geom.Tnw;
+  const int eb = d.f32 ? 4 : 2;
+  const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  while (static_cast<int32_t>(dev->chunk_events.size()) < d.W) {
+    cudaEvent_t ev;
+    DT_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    dev->chunk_events.push_back(ev);
+  }
+  for (int32_t st = 0; st < d.W; ++st) {
+    // step st: every rank q computes the block of destination (q + st + 1) mod W
+    p.a2a_step = st;
+    cudaError_t e = launch_a2a_kernel(p, d.f32, std::min(p.T, sms), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "per-step GEMM launch");
+    DT_CUDA(cudaEventRecord(dev->chunk_events[st], stream));
+    DT_CUDA(cudaStreamWaitEvent(dev->side, dev->chunk_events[st], 0));
+    // the all-to-all of this step on the copy engine, overlapping the next step's GEMM
+    for (int32_t q = 0; q < d.W; ++q) {
+      const int32_t h = (q + st + 1) % d.W;
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(y[q]) + h * d.geom.Nw * eb;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(out[h]) + static_cast<size_t>(q) * d.Ms * d.ldc * eb;
+      DT_CUDA(cudaMemcpy2DAsync(dst, d.ldc * eb, src, d.N * eb, d.geom.Nw * eb, d.Ms,
+                                cudaMemcpyDeviceToDevice, dev->side));
+    }
+  }
+  DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
+  DT_CUDA(cudaStreamWaitEvent(stream, dev->ev_done, 0));
+  return DT_OK;
+}
+
+dt_status dt_a2a_signals(const dt_args* a, void* ws, void* stream_, uint32_t* flags,
+                         uint32_t* counts, int64_t len, uint32_t* epoch) {
+  g_last_error.clear();
+  Derived d;
+  dt_status s = derive(a, DT_OP_GEMM_A2A, &d);
+  if (s != DT_OK) return s;
+  const int64_t n = static_cast<int64_t>(d.W) * d.W * d.nC;
+  if (len != n) return fail(DT_ERR_INVALID, "len %lld != W*W*nC = %lld", (long long)len, (long long)n);
+  if (!ws) return fail(DT_ERR_WORKSPACE, "workspace is NULL");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  DT_CUDA(cudaStreamSynchronize(stream));
+  const uint8_t* w = reinterpret_cast<const uint8_t*>(ws);
+  if (flags && n > 0) DT_CUDA(cudaMemcpy(flags, w + d.off_ready, 4 * n, cudaMemcpyDeviceToHost));
+  if (counts && n > 0) DT_CUDA(cudaMemcpy(counts, w + d.off_cnt, 4 * n, cudaMemcpyDeviceToHost));
+  if (epoch) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_ws.find(ws);
+    *epoch = it == g_ws.end() ? 0u : it->second.epoch;
+  }
+  return DT_OK;
 }
 
 // ------------------------------------------------------------------------------ tuner

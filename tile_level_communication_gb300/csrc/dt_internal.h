@@ -19,11 +19,12 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
 // Set the calling thread's dt_last_error() message.
 void set_last_error(const char* msg);
 
-// Launch the fused persistent kernel; defined in dt_ag.cu (AllGather variants) and
-// dt_rs.cu (ReduceScatter variants).  `cooperative` guarantees that every CTA is resident,
+// Launch the fused persistent kernel; defined in dt_ag.cu (AllGather variants), dt_rs.cu
+// (ReduceScatter / AllReduce variants) and dt_a2a.cu (AllToAll variants).  `cooperative` guarantees that every CTA is resident,
 // which the in-kernel chunk transfer relies on.
 cudaError_t launch_ag_kernel(const KParams& p, int copy_mode, bool f32, int grid,
                              bool cooperative, cudaStream_t stream);
 cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream);
+cudaError_t launch_a2a_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream);
 
 }  // namespace dt

@@ -10,9 +10,10 @@
 //               from the rank shards into the gather buffer (TMA bulk or 16-byte ld/st)
 //               and release each chunk's ready flag when its last piece has landed.
 //   warps 4-7   epilogue: TMEM -> registers -> global.  AllGather: bf16 / fp32 C.
-//               ReduceScatter: fp32 partial rows pushed into the destination's slot, then
-//               per (chunk, column tile) unit an arrival count; the last arrival reduces
-//               the W slots in rank order 0..W-1.
+//               ReduceScatter / AllReduce: per (chunk piece, column tile) unit the
+//               partial is folded into an fp32 running sum in the fixed source order, or
+//               parked until its turn.  AllToAll: the tile's rows go straight into the
+//               destination's block, then the chunk's count of stored tiles is notified.
 //
 // Sources: AutoOverlap page sections 4-5 (chunks, per-chunk waits inserted before the
 // consuming tile, copy engine / TMA / ld-st lowerings with global-memory signals);
@@ -42,6 +43,10 @@ constexpr int kReadyBitsWords = 128;     // producer's cache of seen chunk flags
 constexpr int kMiscBytes = 1024;
 
 enum CopyMode : int { kCopyNone = 0, kCopyTma = 1, kCopyLdst = 2 };
+// Which collective is fused: AllGather (gather mode, one A and B), ReduceScatter /
+// AllReduce (scatter mode by rows, per-rank A_q and B_q), AllToAll (scatter mode by
+// columns, per-rank A_q and B_q with each rank's rows tiled on their own).
+enum OpKind : int { kOpAG = 0, kOpRS = 1, kOpA2A = 2 };
 
 enum DevCode : uint32_t {
   kDevOk = 0,
@@ -61,17 +66,20 @@ __host__ __device__ constexpr int kernel_smem_bytes(bool rs, int copy_mode) {
 }
 
 struct KParams {
-  CUtensorMap tmA[kMaxW];  // AG: [0] = gather buffer; RS: A_q
-  CUtensorMap tmB[kMaxW];  // AG: [0] = B; RS: B_q
+  CUtensorMap tmA[kMaxW];  // AG: [0] = gather buffer, [1] = own shard; RS / A2A: A_q
+  CUtensorMap tmB[kMaxW];  // AG: [0] = B; RS / A2A: B_q
   CUtensorMap tmAcc;       // RS: running sums, fp32 [M][N], 32 x 128 boxes
   CUtensorMap tmPark;      // RS: park slots, fp32 [W (W-1) M/W][N], 32 x 128 boxes
   const uint8_t* shard[kMaxW];
-  void* out[kMaxW];        // AG: out[0] = C; RS: out[s] ([M/W][N]); AR: out[r] ([M][N])
+  void* out[kMaxW];        // AG: out[0] = C; RS: out[s] ([M/W][N]); AR: out[r] ([M][N]);
+                           // A2A: out[h] ([M][N/W]), or the ranks' own Y_q in the baseline
   uint8_t* gather;
-  float* recv;             // RS: W x W x Ms x N fp32 partial slots, [dest][src]
-  uint32_t* ready;         // AG: per chunk, = epoch once landed
+  float* recv;             // RS: running sums [M][N] fp32, then the park slots
+  uint32_t* ready;         // AG: per chunk, = epoch once landed; A2A: per (h, q, j), = epoch
+                           // once every tile of that chunk has been stored
   uint32_t* pieces_done;   // AG: per chunk piece counter (back to 0 after the chunk)
-  uint32_t* unit_cnt;      // RS: per (m-tile, chunk piece, column tile) arrival counter
+  uint32_t* unit_cnt;      // RS: per (m-tile, chunk piece, column tile) arrival counter;
+                           // A2A: per (h, q, j) count of stored tiles (back to 0 when done)
   const int32_t* order;    // tile order written by the prepare kernel
   uint32_t* err;           // 4 words: code, site, detail0, detail1
   unsigned long long* tag; // workspace layout tag; written at exit when no error was seen
@@ -90,6 +98,8 @@ struct KParams {
   int32_t copy_ctas;       // AG in-kernel transfer: CTAs 0..copy_ctas-1 only move chunks
                            // (dedicated SMs); 0: transfer warps inside every compute CTA
   int32_t plain;           // 1: identity order, no flags, no arrival counting
+  int32_t a2a_step;        // A2A baseline launch: step d, every rank q computes destination
+                           // (q + d + 1) mod W into out[q]; -1 in the fused kernel
   int32_t wait_flags;      // AG: the producer waits on ready flags
   uint32_t epoch;
   uint64_t timeout_ns;
@@ -173,25 +183,42 @@ static __device__ __noinline__ bool wait_flag(const KParams& p, const SmemLayout
 }
 
 struct TileInfo {
-  int32_t q, i, n;
-  int64_t row0, row_end, col0;
+  int32_t q, i, n, h;
+  int64_t row0, row_end, col0, col_end;
   bool valid;
 };
 
-template <bool RS>
+template <int OP>
 __device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
   int32_t t = p.plain ? pos : __ldg(p.order + pos);
   TileInfo ti;
   ti.valid = (t >= 0 && t < p.T);
   if (!ti.valid) t = 0;
-  const int32_t per_q = p.Tm * p.g.Tn;
-  ti.q = RS ? t / per_q : 0;
+  // an AllToAll baseline launch holds one destination block (Tnw column tiles) per rank
+  const int32_t tn = (OP == kOpA2A && p.a2a_step >= 0) ? p.g.Tnw : p.g.Tn;
+  const int32_t per_q = p.Tm * tn;
+  ti.q = OP != kOpAG ? t / per_q : 0;
   const int32_t rem = t - ti.q * per_q;
-  ti.i = rem / p.g.Tn;
-  ti.n = rem - ti.i * p.g.Tn;
+  ti.i = rem / tn;
+  ti.n = rem - ti.i * tn;
   ti.row0 = p.row_lo + static_cast<int64_t>(ti.i) * kBM;
   ti.row_end = min64(ti.row0 + kBM, p.row_hi);
-  ti.col0 = static_cast<int64_t>(ti.n) * kBN;
+  if (OP == kOpA2A) {
+    int32_t c;
+    if (p.a2a_step >= 0) {
+      ti.h = (ti.q + p.a2a_step + 1) % p.g.W;
+      c = ti.n;
+    } else {
+      ti.h = ti.n / p.g.Tnw;
+      c = ti.n - ti.h * p.g.Tnw;
+    }
+    ti.col0 = static_cast<int64_t>(ti.h) * p.g.Nw + static_cast<int64_t>(c) * kBN;
+    ti.col_end = static_cast<int64_t>(ti.h + 1) * p.g.Nw;
+  } else {
+    ti.h = 0;
+    ti.col0 = static_cast<int64_t>(ti.n) * kBN;
+    ti.col_end = p.g.N;
+  }
   return ti;
 }
 
@@ -204,22 +231,23 @@ __device__ __forceinline__ int32_t pos_stride(const KParams& p) {
 }
 
 // ============================================================================ producer
-template <bool RS>
+template <int OP>
 __device__ void run_producer(const KParams& p, const SmemLayout& L) {
   uint32_t kit = 0;
   int64_t last_issue[kStages];
 #pragma unroll
   for (int s = 0; s < kStages; ++s) last_issue[s] = -1;
   for (int32_t pos = first_pos(p); pos < p.T; pos += pos_stride(p)) {
-    const TileInfo ti = decode_tile<RS>(p, pos);
+    const TileInfo ti = decode_tile<OP>(p, pos);
     if (!ti.valid) {
       raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
       continue;
     }
     // local HBM as the cache of remote memory: the own rank's rows need no transfer
     const int64_t own0 = static_cast<int64_t>(p.g.rank) * p.g.Ms;
-    const bool own_tile = !RS && p.own_in_place && ti.row0 >= own0 && ti.row_end <= own0 + p.g.Ms;
-    if (!RS && p.wait_flags && !own_tile) {
+    const bool own_tile =
+        OP == kOpAG && p.own_in_place && ti.row0 >= own0 && ti.row_end <= own0 + p.g.Ms;
+    if (OP == kOpAG && p.wait_flags && !own_tile) {
       // consumer_tile_wait: every chunk holding one of this tile's rows must have landed
       bool ok = true;
       for (int64_t g = ti.row0; g < ti.row_end && ok;) {
@@ -239,8 +267,8 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
       // engine); the TMA loads below read through the async proxy
       fence_proxy_async_global();
     }
-    const CUtensorMap* tA = &p.tmA[RS ? ti.q : (own_tile ? 1 : 0)];
-    const CUtensorMap* tB = &p.tmB[RS ? ti.q : 0];
+    const CUtensorMap* tA = &p.tmA[OP != kOpAG ? ti.q : (own_tile ? 1 : 0)];
+    const CUtensorMap* tB = &p.tmB[OP != kOpAG ? ti.q : 0];
     const int32_t a_row = static_cast<int32_t>(own_tile ? ti.row0 - own0 : ti.row0);
     bool ok = true;
     for (int32_t kb = 0; kb < p.KB; ++kb, ++kit) {
@@ -270,14 +298,14 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
 }
 
 // ============================================================================ MMA issuer
-template <bool RS>
+template <int OP>
 __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_base) {
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, /*B MN-major*/ 1);
   uint32_t kit = 0;
   int32_t tl = 0;
   bool issued = false;
   for (int32_t pos = first_pos(p); pos < p.T; pos += pos_stride(p)) {
-    const TileInfo ti = decode_tile<RS>(p, pos);
+    const TileInfo ti = decode_tile<OP>(p, pos);
     if (!ti.valid) continue;
     const int acc = tl & 1;
     const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
@@ -525,25 +553,28 @@ __device__ void fold_chain(const KParams& p, const SmemLayout& L, int32_t s, int
   }
 }
 
-template <bool RS, bool F32>
+template <int OP, bool F32>
 __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tmem_base,
                              int warp, int lane) {
+  constexpr bool RS = OP == kOpRS;
+  constexpr bool A2A = OP == kOpA2A;
   constexpr bool kStoreF32 = RS || F32;  // ReduceScatter partials are fp32
   const int qd = warp - 4;  // TMEM lane quadrant this warp may read
   const int et = threadIdx.x - 128;
   const bool fused_rs = RS && !p.plain;
+  const bool fused_a2a = A2A && !p.plain;
   int32_t tl = 0;
   uint32_t stage_ctr = 0;           // running-sum staging buffer in use (alternates)
   uint32_t ld_par[2] = {0u, 0u};    // phase of each staging buffer's load barrier
   for (int32_t pos = first_pos(p); pos < p.T; pos += pos_stride(p)) {
-    const TileInfo ti = decode_tile<RS>(p, pos);
+    const TileInfo ti = decode_tile<OP>(p, pos);
     if (!ti.valid) continue;
     const int acc = tl & 1;
     const uint32_t ph = (static_cast<uint32_t>(tl) >> 1) & 1u;
     int ok = 1;
     if (lane == 0) ok = wait_bar(p, L, L.tfull(acc), ph, 400 + acc) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (fused_rs) {
+    if (fused_rs || fused_a2a) {
       // all four epilogue warps agree before they meet at the named barriers below
       if (lane == 0) L.vote[(tl & 1) * 4 + qd] = ok;
       named_bar_sync(1, 128);
@@ -692,13 +723,19 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
     for (int cb = 0; cb < kBN / 32; ++cb) {
       if (tma_tile) break;
       const int64_t c0 = ti.col0 + cb * 32;
-      if (c0 >= p.g.N) break;
+      if (c0 >= ti.col_end) break;
       uint32_t v[32];
       tmem_ld32(tbase + cb * 32, v);
       if (!row_ok) continue;
-      if (!RS) {
+      if (OP == kOpAG) {
         if (p.act) apply_activation(v, p.act);
         store_row32<kStoreF32>(p.out[0], p.ldc, row, c0, p.g.N, v);
+      } else if (A2A) {
+        if (fused_a2a)  // push: row q*Ms + row, column c0 - h*Nw of destination h's block
+          store_row32<F32>(p.out[ti.h], p.ldc, static_cast<int64_t>(ti.q) * p.g.Ms + row,
+                           c0 - static_cast<int64_t>(ti.h) * p.g.Nw, p.g.Nw, v);
+        else            // baseline: into the rank's own Y_q
+          store_row32<F32>(p.out[ti.q], p.ldc, row, c0, ti.col_end, v);
       } else if (!fused_rs) {  // baseline: partial of source q into slot [s][q]
         const size_t slot = static_cast<size_t>(s_row) * p.g.W + ti.q;
         store_row32<true>(p.recv + slot * static_cast<size_t>(p.g.Ms) * p.g.N, p.g.N, lr, c0,
@@ -713,6 +750,25 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
     __syncwarp();
     if (lane == 0) mbar_arrive(L.tempty(acc));
     ++tl;
+
+    if (fused_a2a) {
+      // notify: once all 128 rows are stored, count the tile on every chunk (h, q, j) its
+      // rows touch; the last tile of a chunk releases the chunk's ready flag
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (et == 0) {
+        const int32_t j0 = static_cast<int32_t>(ti.row0 / p.g.Cr);
+        const int32_t j1 = static_cast<int32_t>((ti.row_end - 1) / p.g.Cr);
+        for (int32_t j = j0; j <= j1; ++j) {
+          const int64_t c = (static_cast<int64_t>(ti.h) * p.g.W + ti.q) * p.g.nC + j;
+          const uint32_t old = atom_add_acq_rel_gpu(p.unit_cnt + c, 1u);
+          if (old + 1u == static_cast<uint32_t>(a2a_chunk_tiles(p.g, j))) {
+            p.unit_cnt[c] = 0u;  // ready for the next call
+            st_release_gpu(p.ready + c, p.epoch);
+          }
+        }
+      }
+    }
 
     if (fused_rs) {
       // notify: publish this tile's fold or park of every piece
@@ -756,7 +812,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
       // warm L2 with the running sums the next tile of this CTA will fold into
       const int32_t npos = pos + pos_stride(p);
       if (npos < p.T) {
-        const TileInfo nt = decode_tile<RS>(p, npos);
+        const TileInfo nt = decode_tile<OP>(p, npos);
         const int64_t nrow = nt.row0 + qd * 32 + lane;
         if (nt.valid && nrow < nt.row_end) {
           int32_t s, j;
@@ -912,7 +968,7 @@ static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int 
 }
 
 // ============================================================================ kernel
-template <bool RS, int COPY, bool F32>
+template <int OP, int COPY, bool F32>
 __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_constant__ KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -921,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   L.a = base;
   L.b = L.a + kStages * kAStage;
   L.copy = L.b + kStages * kBStage;
-  uint8_t* misc = L.copy + (has_staging(RS, COPY) ? 2 * kCopyBuf : 0);
+  uint8_t* misc = L.copy + (has_staging(OP == kOpRS, COPY) ? 2 * kCopyBuf : 0);
   L.bars = reinterpret_cast<uint64_t*>(misc);  // up to 32 barriers
   L.tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   L.abort_flag = reinterpret_cast<volatile int*>(misc + 260);
@@ -963,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 
   if (copier) {
     // dedicated transfer CTA: no GEMM; the operand ring becomes four 32 KiB staging pairs
-    if (!RS && !p.plain) {
+    if (OP == kOpAG && !p.plain) {
       if (COPY == kCopyTma && warp < 4 && lane == 0)
         run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x) * 4 + warp, p.copy_ctas * 4,
                      L.a + warp * 2 * kCopyBuf, smem_u32(L.bars + 16 + 2 * warp),
@@ -972,11 +1028,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 8 + warp, p.copy_ctas * 8);
     }
   } else if (warp == 0) {
-    if (lane == 0) run_producer<RS>(p, L);
+    if (lane == 0) run_producer<OP>(p, L);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<RS>(p, L, tmem_base);
+    if (lane == 0) run_mma<OP>(p, L, tmem_base);
   } else if (warp < 4) {
-    if (!RS && !p.plain && p.copy_ctas == 0) {  // co-located transfer warps
+    if (OP == kOpAG && !p.plain && p.copy_ctas == 0) {  // co-located transfer warps
       if (COPY == kCopyTma && warp == 2 && lane == 0)
         run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x), static_cast<int32_t>(gridDim.x),
                      L.copy, L.copyb(0), L.copyb(1));
@@ -985,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
                       static_cast<int32_t>(gridDim.x) * 2);
     }
   } else {
-    run_epilogue<RS, F32>(p, L, tmem_base, warp, lane);
+    run_epilogue<OP, F32>(p, L, tmem_base, warp, lane);
   }
 
   tc_fence_before();

@@ -17,6 +17,9 @@
 //       order = sort (i, n) by (key(i), band(i), n, i)
 //   RS: dpos_q(s) = (s - q - 1) mod W;  key(q, i) = min over written chunks of dpos*nC + j;
 //       order = sort (q, i, n) by (key, q, band, n, i)
+//   A2A (GEMM-AllToAll, rows local to each rank, columns split by destination h):
+//       key(q, i, h) = dpos_q(h)*nC + (first chunk of m-tile i);
+//       order = sort (q, i, h, c) by (key, q, band, c, i)
 // Evaluation here does not sort.  Along the m-tiles rotated to start at the first m-tile of
 // the own rank (AG) or of rank q+1 (RS) the key never decreases, so the key of an m-tile is
 // read off one row of it, and the number of m-tiles with a smaller key is a binary search.
@@ -36,6 +39,8 @@ namespace dt {
 struct Geom {
   int64_t M, N, Ms, Cr;
   int32_t W, rank, BM, BN, nC, Tm, Tn, G, swizzle;
+  int64_t Nw;   // AllToAll: columns per destination (N / W); 0 otherwise
+  int32_t Tnw;  // AllToAll: column tiles per destination; 0 otherwise
 };
 
 DT_HD int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -58,6 +63,20 @@ DT_HD Geom make_geom(int32_t W, int32_t rank, int64_t M, int64_t N, int64_t Cr, 
   g.nC = g.Ms > 0 ? static_cast<int32_t>(cdiv64(g.Ms, Cr)) : 0;
   g.Tm = static_cast<int32_t>(cdiv64(M, BM));
   g.Tn = static_cast<int32_t>(cdiv64(N, BN));
+  g.Nw = 0;
+  g.Tnw = 0;
+  return g;
+}
+
+// GEMM-AllToAll: every rank's Ms rows are tiled on their own (Tm m-tiles per rank) and the N
+// columns block by block, one block of Nw = N / W per destination (Tnw column tiles each).
+DT_HD Geom make_geom_a2a(int32_t W, int64_t M, int64_t N, int64_t Cr, int32_t BM, int32_t BN,
+                         int32_t G, int32_t swizzle) {
+  Geom g = make_geom(W, 0, M, N, Cr, BM, BN, G, swizzle);
+  g.Nw = N / W;
+  g.Tm = static_cast<int32_t>(cdiv64(g.Ms, BM));
+  g.Tnw = static_cast<int32_t>(cdiv64(g.Nw, BN));
+  g.Tn = W * g.Tnw;
   return g;
 }
 
@@ -162,6 +181,47 @@ DT_HD int64_t rs_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
   const int32_t ug = rs_count_below(g, q, rot0, k);
   const int32_t ue = rs_count_below(g, q, rot0, k + 1);
   return before * g.Tn + band_offset(ug, ue, u, n, g.Tn, g.G);
+}
+
+// ------------------------------------------------------------------ all-to-all (GEMM-AllToAll)
+// Scatter mode by columns: rank q sends column block h in the order dpos_q(h) = (h - q - 1)
+// mod W (rank q+1 first, its own block last), and inside one destination its chunks in row
+// order.  The key of m-tile i is dpos*nC + (first chunk it writes), so for one (q, d) the
+// m-tiles keyed j are exactly those whose first row lies in chunk j: [first_mtile(j),
+// first_mtile(j+1)).  Every (q, d) holds Tm m-tiles and all W ranks share the group sizes.
+DT_HD int32_t a2a_first_mtile(const Geom& g, int32_t j) {
+  const int64_t t = cdiv64(static_cast<int64_t>(j) * g.Cr, g.BM);
+  return static_cast<int32_t>(t < g.Tm ? t : g.Tm);
+}
+// execution position of AllToAll tile (q, i, n), n = h * Tnw + c
+DT_HD int64_t a2a_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
+  if (!g.swizzle) return (static_cast<int64_t>(q) * g.Tm + i) * g.Tn + n;
+  const int32_t h = n / g.Tnw;
+  const int32_t c = n - h * g.Tnw;
+  const int32_t d = (h - q - 1 + 2 * g.W) % g.W;
+  const int32_t j = static_cast<int32_t>(static_cast<int64_t>(i) * g.BM / g.Cr);
+  const int32_t ug = a2a_first_mtile(g, j);
+  const int32_t ue = a2a_first_mtile(g, j + 1);
+  return static_cast<int64_t>(g.W) * g.Tnw * (static_cast<int64_t>(d) * g.Tm + ug) +
+         static_cast<int64_t>(q) * (ue - ug) * g.Tnw + band_offset(ug, ue, i, c, g.Tnw, g.G);
+}
+// tiles of one (destination, source) pair whose rows touch chunk j: its m-tiles x Tnw
+DT_HD int32_t a2a_chunk_tiles(const Geom& g, int32_t j) {
+  const int64_t lo = static_cast<int64_t>(j) * g.Cr;
+  const int64_t hi = min64(lo + g.Cr, g.Ms);
+  return static_cast<int32_t>((hi - 1) / g.BM - lo / g.BM + 1) * g.Tnw;
+}
+
+// Execution position of tile id t of an operation with the dt_op numbering (0 AllGather:
+// t = i*Tn + n; 1 ReduceScatter, 2 AllReduce, 3 AllToAll: t = (q*Tm + i)*Tn + n).
+DT_HD int64_t tile_position(const Geom& g, int op, int64_t t) {
+  if (op == 0) return ag_position(g, static_cast<int32_t>(t / g.Tn), static_cast<int32_t>(t % g.Tn));
+  const int64_t per_q = static_cast<int64_t>(g.Tm) * g.Tn;
+  const int32_t q = static_cast<int32_t>(t / per_q);
+  const int64_t rem = t - q * per_q;
+  const int32_t i = static_cast<int32_t>(rem / g.Tn);
+  const int32_t n = static_cast<int32_t>(rem - static_cast<int64_t>(i) * g.Tn);
+  return op == 3 ? a2a_position(g, q, i, n) : rs_position(g, q, i, n);
 }
 
 // Most chunks that the rows of one m-tile touch: each (m-tile, chunk) piece times a column

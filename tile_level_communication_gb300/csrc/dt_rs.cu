@@ -6,7 +6,7 @@ namespace dt {
 namespace {
 template <bool F32>
 cudaError_t launch_one(const KParams& p, int grid, cudaStream_t stream) {
-  auto kern = fused_gemm_kernel<true, kCopyNone, F32>;
+  auto kern = fused_gemm_kernel<kOpRS, kCopyNone, F32>;
   const int smem = kernel_smem_bytes(true, kCopyNone);
   static bool configured = false;
   if (!configured) {
