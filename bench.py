@@ -95,7 +95,7 @@ def workload_desc(name, ops, chunk_override):
                         "dist_x": wl.dist_a, "dist_w": wl.dist_b}
             continue
         d[wl.op] = {"name": wl.name, "world_size": wl.world_size, "m": wl.m, "n": wl.n,
-                    "k" if wl.op == "ag" else "k_per_rank": wl.k,
+                    "k" if wl.op in ("ag", "a2a") else "k_per_rank": wl.k,
                     "chunk_rows": chunk_override or wl.chunk_rows, "seed": wl.seed,
                     "dist_a": wl.dist_a, "dist_b": wl.dist_b, "gflop": wl.flops / 1e9}
     return d
@@ -151,6 +151,18 @@ def oracle_sample(ops, ag_rows, rs_rows, inputs):
             secs += time.perf_counter() - t0
             flops += 2.0 * rows * w * wl.f_rank * (wl.k + wl.n)
             desc.append(f"FFN block on rows 0..{rows}")
+            continue
+        if wl.op == "a2a":
+            # the first r rows of every rank, all W destinations
+            w = wl.world_size
+            r = max(1, min(rs_rows, wl.m) // w)
+            a = [f64_from_bf16_bits(x[:r]) for x in inp.a]
+            b = [f64_from_bf16_bits(inp.b[0])] * w
+            t0 = time.perf_counter()
+            reference.gemm_a2a(a, b)
+            secs += time.perf_counter() - t0
+            flops += 2.0 * w * r * wl.n * wl.k
+            desc.append(f"A2A rows 0..{r} of every rank, all destinations")
             continue
         if wl.op == "ag":
             rows = min(ag_rows, wl.m)
@@ -469,6 +481,20 @@ def main():
             ws = torch.zeros(need, dtype=torch.uint8, device=dev)
             calls.append(dict(op="ag", wl=wl, args=a, ins=shards + [b], shards=shards, b=b,
                               outs=[c], ws=ws))
+        elif wl.op == "a2a":
+            w = wl.world_size
+            a = dt.make_args(w, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=not args.no_swizzle)
+            A = [up(x) for x in inp.a]
+            b = up(inp.b[0])  # the replicated weight, held once
+            outs = [torch.empty((wl.m, wl.n // w), dtype=torch.bfloat16, device=dev)
+                    for _ in range(w)]
+            y = [torch.empty((wl.m // w, wl.n), dtype=torch.bfloat16, device=dev)
+                 for _ in range(w)]  # the baseline's per-rank GEMM outputs
+            probe = dt.make_args(w, wl.m, wl.n, wl.k, chunk_rows=64)
+            need = max(dt.workspace_size(a, dt.OP_A2A), dt.workspace_size(probe, dt.OP_A2A))
+            ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+            calls.append(dict(op="a2a", wl=wl, args=a, ins=A + [b], A=A, B=[b] * w, outs=outs,
+                              y=y, ws=ws))
         else:
             a = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=cr,
                              swizzle=not args.no_swizzle)
@@ -492,6 +518,12 @@ def main():
         elif cl["op"] == "rs":
             fn = dt.gemm_rs if fused else dt.gemm_rs_kernel_overlap
             fn(cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"])
+        elif cl["op"] == "a2a":
+            if fused:
+                dt.gemm_a2a(cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"])
+            else:
+                dt.gemm_a2a_kernel_overlap(cl["A"], cl["B"], cl["y"], cl["outs"], cl["ws"],
+                                           cl["args"])
         else:
             fn = dt.gemm_ar if fused else dt.gemm_ar_kernel_overlap
             fn(cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"])
@@ -506,8 +538,8 @@ def main():
             if cl["op"] == "ag":
                 pts = dt.tune_ag_gemm(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], cl["args"])
             else:
-                pts = dt.tune_reduce(dt.OP_RS if cl["op"] == "rs" else dt.OP_AR, cl["A"], cl["B"],
-                                     cl["outs"], cl["ws"], cl["args"])
+                op_id = {"rs": dt.OP_RS, "ar": dt.OP_AR, "a2a": dt.OP_A2A}[cl["op"]]
+                pts = dt.tune_reduce(op_id, cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"])
             a = cl["args"]
             tuned[cl["op"]] = {"chunk_rows": int(a.chunk_rows),
                                "backend": [k for k, v in dt.BACKENDS.items() if v == a.backend][0],
@@ -644,6 +676,13 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
             if cl["op"] == "ag":
                 a = torch.cat(cl["shards"], dim=0)
                 torch.matmul(a, cl["b"])
+            elif cl["op"] == "a2a":
+                w = len(cl["A"])
+                ms, nw = cl["A"][0].shape[0], cl["outs"][0].shape[1]
+                for q, a_ in enumerate(cl["A"]):
+                    y = torch.mm(a_, cl["B"][q])
+                    for h in range(w):
+                        cl["outs"][h][q * ms:(q + 1) * ms].copy_(y[:, h * nw:(h + 1) * nw])
             else:
                 acc = None
                 for a_, b_ in zip(cl["A"], cl["B"]):
@@ -653,7 +692,8 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     ms_c = timed(cublas_step, max(3, k_side // 2))
     out["cublas_nonoverlapped_context"] = {
         "value": flops_step / (ms_c * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_c,
-        "note": "torch.cat gather + torch.matmul (AG); per-rank torch.mm, fp32 sum (RS)"}
+        "note": "torch.cat gather + torch.matmul (AG); per-rank torch.mm, fp32 sum (RS); "
+                "per-rank torch.mm then block copies (A2A)"}
 
     # spot check of the fused result against cuBLAS on a row sample
     for cl in calls:
@@ -669,6 +709,10 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
             elif cl.get("act") == "silu":
                 ref = torch.nn.functional.silu(ref)
             got = cl["outs"][0][:256].float()
+        elif cl["op"] == "a2a":  # out_0 rows 0..127: source 0's rows, destination 0's columns
+            nw = cl["outs"][0].shape[1]
+            ref = cl["A"][0][:128].float() @ cl["B"][0][:, :nw].float()
+            got = cl["outs"][0][:128].float()
         else:  # ReduceScatter out_0 / AllReduce rank 0: rows 0..127 of the sum
             ref = sum(a_[:128].float() @ b_.float() for a_, b_ in zip(cl["A"], cl["B"]))
             got = cl["outs"][0][:128].float()

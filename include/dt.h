@@ -307,8 +307,9 @@ typedef struct dt_tune_point {
  * communication and the tile order, all by measuring the generated variants).
  * AllGather-GEMM candidates: chunk rows {64 .. 4096, M/W} x {copy engine (when the chunk count
  * stays <= 512), TMA and ld/st with co-located transfer warps, TMA and ld/st on 8 or 16
- * dedicated CTAs}; then group widths {4, 16} around the best.  Reduce candidates
- * (op DT_OP_GEMM_RS or DT_OP_GEMM_AR): chunk rows x group widths.  Each candidate runs once as
+ * dedicated CTAs}; then group widths {4, 16} around the best.  Scatter-mode candidates
+ * (dt_tune_reduce with op DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A): chunk rows x group
+ * widths {4, 8, 16}.  Each candidate runs once as
  * warm-up and `reps` times timed with CUDA events on `stream` (synchronising); candidates
  * whose workspace exceeds ws_bytes are skipped.  The fastest knobs are written into *a
  * (chunk_rows, backend, copy_ctas, group; swizzle stays on).  `points` (may be NULL) receives

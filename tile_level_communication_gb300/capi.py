@@ -308,7 +308,8 @@ def tune_ag_gemm(shards, b, c, workspace, args: DtArgs, reps: int = 3, stream=No
 
 def tune_reduce(op: int, a_list, b_list, out_list, workspace, args: DtArgs, reps: int = 3,
                 stream=None, ws_bytes=None, max_points: int = 128):
-    """Tuner of dt_gemm_rs (op OP_RS) or dt_gemm_ar (op OP_AR); writes the best into `args`."""
+    """Tuner of dt_gemm_rs (op OP_RS), dt_gemm_ar (OP_AR) or dt_gemm_a2a (OP_A2A); writes the
+    best into `args`."""
     buf = (DtTunePoint * max_points)()
     n = ctypes.c_int32(0)
     _raise(lib().dt_tune_reduce(op, _ptr_array(a_list), _ptr_array(b_list), _ptr_array(out_list),

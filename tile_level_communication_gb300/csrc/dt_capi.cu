@@ -1244,13 +1244,14 @@ dt_status dt_tune_reduce(int op, const void* const* a_, const void* const* b_, v
                          void* ws, size_t ws_bytes, dt_args* a, int32_t reps, dt_tune_point* points,
                          int32_t max_points, int32_t* n_points, void* stream) {
   g_last_error.clear();
-  if (op != DT_OP_GEMM_RS && op != DT_OP_GEMM_AR)
-    return fail(DT_ERR_INVALID, "dt_tune_reduce takes DT_OP_GEMM_RS or DT_OP_GEMM_AR");
+  if (op != DT_OP_GEMM_RS && op != DT_OP_GEMM_AR && op != DT_OP_GEMM_A2A)
+    return fail(DT_ERR_INVALID, "dt_tune_reduce takes DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A");
   TuneCtx t;
   Derived d;
   dt_status s = tune_setup(op, a, ws, ws_bytes, reps, stream, &t, &d);
   if (s != DT_OK) return s;
   auto call = [&](dt_args& cand) {
+    if (op == DT_OP_GEMM_A2A) return dt_gemm_a2a(a_, b_, out, ws, ws_bytes, &cand, stream);
     return op == DT_OP_GEMM_RS ? dt_gemm_rs(a_, b_, out, ws, ws_bytes, &cand, stream)
                                : dt_gemm_ar(a_, b_, out, ws, ws_bytes, &cand, stream);
   };
