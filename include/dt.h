@@ -94,7 +94,11 @@ typedef struct dt_args {
   int32_t swizzle;     /* 1: rank-aware swizzle order; 0: naive order (all ranks tile 0)   */
   int32_t backend;     /* dt_xfer, AllGather chunk transfer                                */
   int32_t out_dtype;   /* dt_dtype of C / out_s                                            */
-  int32_t tile_m;      /* 0 or 128                                                         */
+  int32_t tile_m;      /* rows of a tile: 128 (one CTA, tcgen05 cta_group::1), 256 (a cluster
+                          of two CTAs on two SMs, cta_group::2: each stages 128 rows of A and
+                          half of the 256 columns of B, 6 pipeline stages), 0 = 256 when that
+                          leaves at least 76 tiles (one per SM pair) and copy_ctas is even,
+                          else 128                                                          */
   int32_t tile_n;      /* 0 or 256                                                         */
   int32_t group;       /* m-tiles per band of the in-chunk raster; 0 = 8                   */
   int64_t lda;         /* AG: of every shard; RS: of every A_q   (0 = K)                   */
@@ -111,8 +115,8 @@ typedef struct dt_args {
 
 typedef enum { DT_ACT_NONE = 0, DT_ACT_GELU_TANH = 1, DT_ACT_SILU = 2 } dt_act;
 
-/* Fill `a` with defaults: W=1, rank 0, swizzle on, AUTO backend, bf16 output, 128x256
- * tiles, group 8.  Sizes are zero and must be set by the caller. */
+/* Fill `a` with defaults: W=1, rank 0, swizzle on, AUTO backend, bf16 output, automatic tile
+ * rows (tile_m = 0) x 256 columns, group 8.  Sizes are zero and must be set by the caller. */
 void dt_args_default(dt_args* a);
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -247,11 +251,16 @@ dt_status dt_gemm_a2a_kernel_overlap(const void* const* a, const void* const* b,
                                      void* const* y, void* const* out, void* workspace,
                                      size_t ws_bytes, const dt_args* a_args, void* stream);
 
+/* Tiles of the execution order of `op` for `a` (-1 if `a` is invalid), and the rows of one
+ * tile (128 or 256, tile_m resolved). */
+int64_t dt_tile_count(const dt_args* a, int op);
+int32_t dt_tile_rows(const dt_args* a, int op);
+
 /* Tile execution order of `op` for `a` computed on the host: order[p] is the tile run at
  * position p.  AG tile id = i*Tn + n; RS / AR tile id = (q*Tm + i)*Tn + n, with
  * Tm = ceil(M/tile_m), Tn = ceil(N/tile_n); A2A tile id = (q*Tm + i)*Tn + h*Tnw + c with
- * Tm = ceil((M/W)/tile_m), Tnw = ceil((N/W)/tile_n), Tn = W*Tnw.  `len` must equal the tile
- * count.
+ * Tm = ceil((M/W)/tile_m), Tnw = ceil((N/W)/tile_n), Tn = W*Tnw; tile_m as resolved by
+ * dt_tile_rows.  `len` must equal dt_tile_count.
  * (DITRON page section 3.2: swizzle_func maps the original tile id to the new one.) */
 dt_status dt_swizzle_plan(const dt_args* a, int op, int32_t* order_host, int64_t len);
 

@@ -99,35 +99,42 @@ PLAN_GRID = [
 ]
 
 
+# the order's tile rows: one CTA (128) or a CTA pair (256); the oracle takes them as BM
+TILE_M = [128, 256]
+
+
 @pytest.mark.parametrize("case", PLAN_GRID)
 @pytest.mark.parametrize("swizzle", [True, False])
-def test_host_plan_matches_oracle_ag(dt, case, swizzle):
+@pytest.mark.parametrize("bm", TILE_M)
+def test_host_plan_matches_oracle_ag(dt, case, swizzle, bm):
     w, m, n, cr = case
     for r in range(w):
-        a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr, swizzle=swizzle)
+        a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr, swizzle=swizzle, tile_m=bm)
         got = dt.swizzle_plan(a, dt.OP_AG)
-        want = oplan.ag_order(w, r, m, n, cr, 128, 256, swizzle)
+        want = oplan.ag_order(w, r, m, n, cr, bm, 256, swizzle)
         assert got.tolist() == want, (case, r)
 
 
 @pytest.mark.parametrize("case", PLAN_GRID)
 @pytest.mark.parametrize("swizzle", [True, False])
-def test_host_plan_matches_oracle_rs(dt, case, swizzle):
+@pytest.mark.parametrize("bm", TILE_M)
+def test_host_plan_matches_oracle_rs(dt, case, swizzle, bm):
     w, m, n, cr = case
-    a = dt.make_args(w, m, n, 8, chunk_rows=cr, swizzle=swizzle)
+    a = dt.make_args(w, m, n, 8, chunk_rows=cr, swizzle=swizzle, tile_m=bm)
     got = dt.swizzle_plan(a, dt.OP_RS)
-    want = oplan.rs_order(w, m, n, cr, 128, 256, swizzle)
+    want = oplan.rs_order(w, m, n, cr, bm, 256, swizzle)
     assert got.tolist() == want, case
 
 
 @pytest.mark.parametrize("group", [1, 3, 8, 64])
-def test_host_plan_group_width(dt, group):
+@pytest.mark.parametrize("bm", TILE_M)
+def test_host_plan_group_width(dt, group, bm):
     for (w, m, n, cr) in [(4, 2048, 4096, 256), (6, 6000, 3000, 192)]:
-        a = dt.make_args(w, m, n, 8, rank=w - 1, chunk_rows=cr, group=group)
+        a = dt.make_args(w, m, n, 8, rank=w - 1, chunk_rows=cr, group=group, tile_m=bm)
         assert dt.swizzle_plan(a, dt.OP_AG).tolist() == oplan.ag_order(
-            w, w - 1, m, n, cr, 128, 256, True, group)
+            w, w - 1, m, n, cr, bm, 256, True, group)
         assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(
-            w, m, n, cr, 128, 256, True, group)
+            w, m, n, cr, bm, 256, True, group)
 
 
 def test_host_plan_random_sweep(dt):
@@ -140,8 +147,23 @@ def test_host_plan_random_sweep(dt):
         cr = int(rng.integers(1, 2 * ms + 2))
         r = int(rng.integers(0, w))
         a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr)
-        assert dt.swizzle_plan(a, dt.OP_AG).tolist() == oplan.ag_order(w, r, m, n, cr, 128, 256)
-        assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(w, m, n, cr, 128, 256)
+        bm = dt.tile_rows(a, dt.OP_AG)
+        assert dt.swizzle_plan(a, dt.OP_AG).tolist() == oplan.ag_order(w, r, m, n, cr, bm, 256)
+        bm = dt.tile_rows(a, dt.OP_RS)
+        assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(w, m, n, cr, bm, 256)
+
+
+def test_tile_rows_auto_rule(dt):
+    """tile_m = 0: a CTA pair (256 rows) when that leaves at least 76 tiles, else one CTA."""
+    big = dt.make_args(8, 8192, 3584, 8192, chunk_rows=1024)   # 32 x 14 = 448 pair tiles
+    small = dt.make_args(2, 512, 512, 512, chunk_rows=128)     # 2 x 2 = 4 pair tiles
+    assert dt.tile_rows(big, dt.OP_AG) == 256 and dt.tile_rows(small, dt.OP_AG) == 128
+    assert dt.tile_count(big, dt.OP_AG) == 32 * 14
+    assert dt.tile_rows(dt.make_args(4, 2048, 4096, 2048, chunk_rows=256), dt.OP_RS) == 256
+    for bm in TILE_M:
+        a = dt.make_args(2, 512, 512, 512, chunk_rows=128, tile_m=bm)
+        assert dt.tile_rows(a, dt.OP_AG) == bm
+        assert dt.tile_count(a, dt.OP_AG) == (512 // bm) * 2
 
 
 # ----------------------------------------------------------------------------- AllToAll
@@ -155,11 +177,12 @@ A2A_GRID = [
 
 @pytest.mark.parametrize("case", A2A_GRID)
 @pytest.mark.parametrize("swizzle", [True, False])
-def test_host_plan_matches_oracle_a2a(dt, case, swizzle):
+@pytest.mark.parametrize("bm", TILE_M)
+def test_host_plan_matches_oracle_a2a(dt, case, swizzle, bm):
     w, ms, nw, cr = case
-    a = dt.make_args(w, w * ms, w * nw, 8, chunk_rows=cr, swizzle=swizzle)
+    a = dt.make_args(w, w * ms, w * nw, 8, chunk_rows=cr, swizzle=swizzle, tile_m=bm)
     got = dt.swizzle_plan(a, dt.OP_A2A)
-    assert got.tolist() == oplan.a2a_order(w, ms, w * nw, cr, 128, 256, swizzle), case
+    assert got.tolist() == oplan.a2a_order(w, ms, w * nw, cr, bm, 256, swizzle), case
 
 
 def test_host_plan_a2a_random_sweep(dt):
@@ -170,9 +193,10 @@ def test_host_plan_a2a_random_sweep(dt):
         nw = 8 * int(rng.integers(1, 90))
         cr = int(rng.integers(1, 2 * ms + 2))
         g = int(rng.integers(1, 10))
-        a = dt.make_args(w, w * ms, w * nw, 8, chunk_rows=cr, group=g)
+        bm = 128 * int(rng.integers(1, 3))
+        a = dt.make_args(w, w * ms, w * nw, 8, chunk_rows=cr, group=g, tile_m=bm)
         assert dt.swizzle_plan(a, dt.OP_A2A).tolist() == \
-            oplan.a2a_order(w, ms, w * nw, cr, 128, 256, True, g)
+            oplan.a2a_order(w, ms, w * nw, cr, bm, 256, True, g)
 
 
 @pytest.mark.parametrize("kw,status", [

@@ -67,11 +67,13 @@ def small():
 
 
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-def test_small_parity_and_padding_untouched(dt, small, out_dtype):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_small_parity_and_padding_untouched(dt, small, out_dtype, tile_m):
     wl, inp, ref = small
     nw = wl.n // wl.world_size
     ldc = nw + 24
-    outs, _, _ = _run(dt, inp, wl.m, wl.n, wl.k, out_dtype, ldc=ldc, chunk_rows=wl.chunk_rows)
+    outs, _, _ = _run(dt, inp, wl.m, wl.n, wl.k, out_dtype, ldc=ldc, chunk_rows=wl.chunk_rows,
+                      tile_m=tile_m)
     for h, o in enumerate(outs):
         assert_close(to_f64(o, nw), ref[h], out_dtype, f"out_{h}")
         assert torch.isnan(o[:, nw:].float()).all(), f"out_{h}: padding written"
@@ -80,10 +82,12 @@ def test_small_parity_and_padding_untouched(dt, small, out_dtype):
 def test_small_bit_identical_across_orders_chunks_groups_and_baseline(dt, small):
     wl, inp, _ = small
     dev = _upload(inp)
-    base, _, _ = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, dev=dev)
+    base, _, _ = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, dev=dev, tile_m=128)
     variants = [dict(swizzle=False), dict(chunk_rows=1), dict(chunk_rows=64),
                 dict(chunk_rows=300), dict(chunk_rows=1000), dict(group=1),
-                dict(group=3, chunk_rows=128), dict(num_sms=7)]
+                dict(group=3, chunk_rows=128), dict(num_sms=7), dict(tile_m=256),
+                dict(tile_m=256, chunk_rows=1), dict(tile_m=256, swizzle=False),
+                dict(tile_m=256, num_sms=7)]
     for kw in variants:
         kw.setdefault("chunk_rows", wl.chunk_rows)
         outs, _, _ = _run(dt, inp, wl.m, wl.n, wl.k, dev=dev, **kw)
@@ -93,13 +97,15 @@ def test_small_bit_identical_across_orders_chunks_groups_and_baseline(dt, small)
 
 
 @pytest.mark.parametrize("chunk_rows", [96, 1, 300])
-def test_signals_after_each_call(dt, small, chunk_rows):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_signals_after_each_call(dt, small, chunk_rows, tile_m):
     wl, inp, _ = small
     dev = _upload(inp)
-    outs, args, ws = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=chunk_rows, dev=dev)
+    outs, args, ws = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=chunk_rows, dev=dev,
+                          tile_m=tile_m)
     flags, counts, e1 = dt.a2a_signals(args, ws)
     assert e1 > 0 and (flags == e1).all() and (counts == 0).all()
-    _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=chunk_rows, dev=dev, ws=ws)
+    _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=chunk_rows, dev=dev, ws=ws, tile_m=tile_m)
     flags, counts, e2 = dt.a2a_signals(args, ws)
     assert e2 == e1 + 1 and (flags == e2).all() and (counts == 0).all()
 

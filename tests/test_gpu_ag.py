@@ -53,24 +53,27 @@ def small():
 @pytest.mark.parametrize("swizzle", [True, False])
 @pytest.mark.parametrize("rank", [0, 1])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-def test_small_parity(dt, small, backend, swizzle, rank, out_dtype):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_small_parity(dt, small, backend, swizzle, rank, out_dtype, tile_m):
     wl, inp, ref = small
     c = _run(dt, inp, wl.m, wl.n, wl.k, out_dtype, chunk_rows=wl.chunk_rows, backend=backend,
-             swizzle=swizzle, rank=rank)
+             swizzle=swizzle, rank=rank, tile_m=tile_m)
     assert_close(to_f64(c), ref, out_dtype, f"{backend} swz={swizzle} r={rank}")
 
 
 def test_small_bit_identical_across_variants(dt, small):
     wl, inp, ref = small
-    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=128, backend="tma")
-    for backend in ["copy_engine", "tma", "ldst"]:
-        for swizzle in [True, False]:
-            for cr in [1, 64, 100, 128, 256, 1000]:
-                c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, backend=backend, swizzle=swizzle,
-                         rank=1)
-                assert bits_equal(c, base), (backend, swizzle, cr)
-    c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=128, fn=dt.ag_gemm_kernel_overlap)
-    assert bits_equal(c, base)
+    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=128, backend="tma", tile_m=128)
+    for tile_m in [128, 256]:  # one CTA or a CTA pair per tile: the same bits
+        for backend in ["copy_engine", "tma", "ldst"]:
+            for swizzle in [True, False]:
+                for cr in [1, 64, 100, 128, 256, 1000]:
+                    c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, backend=backend,
+                             swizzle=swizzle, rank=1, tile_m=tile_m)
+                    assert bits_equal(c, base), (tile_m, backend, swizzle, cr)
+        c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=128, fn=dt.ag_gemm_kernel_overlap,
+                 tile_m=tile_m)
+        assert bits_equal(c, base), tile_m
 
 
 @pytest.fixture(scope="module")
@@ -81,18 +84,19 @@ def ragged():
 
 
 @pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
-def test_ragged_parity_and_identity(dt, ragged, backend):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_ragged_parity_and_identity(dt, ragged, backend, tile_m):
     wl, inp, ref = ragged
     outs = []
     for rank, swizzle, cr in [(0, True, wl.chunk_rows), (5, True, wl.chunk_rows), (3, False, 77),
                               (2, True, 1000)]:
         c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, backend=backend, swizzle=swizzle,
-                 rank=rank)
+                 rank=rank, tile_m=tile_m)
         assert_close(to_f64(c), ref, "bf16", f"{backend} r={rank}")
         outs.append(c)
     assert all(bits_equal(outs[0], o) for o in outs[1:])
     c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, rank=4,
-             fn=dt.ag_gemm_kernel_overlap)
+             fn=dt.ag_gemm_kernel_overlap, tile_m=tile_m)
     assert bits_equal(outs[0], c)
 
 
@@ -107,24 +111,26 @@ def test_ragged_parity_and_identity(dt, ragged, backend):
     (16, 16 * 9, 16, 16, 4),
 ])
 @pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
-def test_edge_shapes(dt, case, backend):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_edge_shapes(dt, case, backend, tile_m):
     w, m, n, k, cr = case
     inp = make_ag_inputs(w, m, n, k, seed=31 + m)
     ref = _oracle(inp)
     for rank in sorted({0, w - 1}):
-        c = _run(dt, inp, m, n, k, chunk_rows=cr, backend=backend, rank=rank)
+        c = _run(dt, inp, m, n, k, chunk_rows=cr, backend=backend, rank=rank, tile_m=tile_m)
         assert_close(to_f64(c), ref, "bf16", f"{case} {backend} r={rank}")
 
 
 @pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
-def test_padded_leading_dims_and_canaries(dt, backend):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_padded_leading_dims_and_canaries(dt, backend, tile_m):
     w, m, n, k = 3, 3 * 50, 72, 96
     inp = make_ag_inputs(w, m, n, k, seed=77)
     ref = _oracle(inp)
     lda, ldb, ldc = 104, 80, 88
     for out_dtype in ["bf16", "f32"]:
         c = _run(dt, inp, m, n, k, out_dtype, lda=lda, ldb=ldb, ldc=ldc, chunk_rows=16,
-                 backend=backend, rank=1)
+                 backend=backend, rank=1, tile_m=tile_m)
         assert_close(to_f64(c, n), ref, out_dtype)
         # the padding columns of C were filled with NaN and must be untouched
         assert torch.isnan(c[:, n:].float()).all()
@@ -158,12 +164,14 @@ def test_workspace_reuse_across_problems(dt):
             assert_close(to_f64(c), ref_small, "bf16")
 
 
-def test_lost_chunk_times_out_and_context_survives(dt, small):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_lost_chunk_times_out_and_context_survives(dt, small, tile_m):
     """Host-made fault: one chunk's copy and flag are never issued; the consumer tiles'
-    bounded waits run out, the error comes back through dt_check, and the next call works."""
+    bounded waits run out, the error comes back through dt_check, and the next call works
+    (with a CTA pair per tile too: the partner CTA's waits run out as well)."""
     wl, inp, ref = small
     args = dt.make_args(2, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, backend="copy_engine",
-                        rank=0, timeout_us=200_000)
+                        rank=0, timeout_us=200_000, tile_m=tile_m)
     shards = [dev_bf16(s) for s in inp.shards]
     b = dev_bf16(inp.b)
     c = out_tensor(wl.m, wl.n, "bf16")
@@ -192,11 +200,14 @@ def _sampled_indices(m, n, rng, count=1500):
     ("ag_w8_m16384_n8192_k8192", "auto", 256),
     ("ag_w8_m16384_n8192_k8192", "copy_engine", 2048),
     ("ag_w8_m16384_n8192_k8192", "ldst", 64),
+    ("ag_w8_m16384_n8192_k8192", "tma", -256),   # one CTA per tile (tile_m = 128)
 ])
 def test_full_size_sampled(dt, name, backend, chunk):
     wl = WORKLOADS[name]
     inp = wl.make()
-    c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=chunk, backend=backend, rank=3)
+    tile_m = 128 if chunk < 0 else 0
+    c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=abs(chunk), backend=backend, rank=3,
+             tile_m=tile_m)
     rng = np.random.Generator(np.random.PCG64(9))
     rows, cols = _sampled_indices(wl.m, wl.n, rng)
     ref = reference.ag_gemm_entries([f64_from_bf16_bits(s) for s in inp.shards],
@@ -209,12 +220,16 @@ def test_full_size_sampled(dt, name, backend, chunk):
 
 @pytest.mark.parametrize("backend", ["tma", "ldst"])
 @pytest.mark.parametrize("copy_ctas", [1, 8, 16])
-def test_dedicated_transfer_ctas(dt, small, ragged, backend, copy_ctas):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_dedicated_transfer_ctas(dt, small, ragged, backend, copy_ctas, tile_m):
     """CTAs that only move chunks (dedicated SMs) give the same bits as co-located warps."""
+    if tile_m == 256 and copy_ctas % 2:
+        pytest.skip("CTA pairs take an even number of dedicated CTAs")
     for wl, inp, ref in (small, ragged):
-        base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, backend=backend, rank=1)
+        base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, backend=backend, rank=1,
+                    tile_m=tile_m)
         c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, backend=backend, rank=1,
-                 copy_ctas=copy_ctas)
+                 copy_ctas=copy_ctas, tile_m=tile_m)
         assert_close(to_f64(c), ref, "bf16", f"{backend} dedicated {copy_ctas}")
         assert bits_equal(c, base)
 

@@ -19,16 +19,23 @@ def dt():
 
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("swizzle", [True, False])
-def test_device_plan_matches_oracle(dt, case, swizzle):
+@pytest.mark.parametrize("bm", [128, 256])
+def test_device_plan_matches_oracle(dt, case, swizzle, bm):
     w, m, n, cr = case
     for r in sorted({0, 1 % w, w - 1}):
-        a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr, swizzle=swizzle)
+        a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr, swizzle=swizzle, tile_m=bm)
         t = dt.tile_count(a, dt.OP_AG)
         buf = torch.full((t,), -1, dtype=torch.int32, device="cuda")
         dt.swizzle_plan_device(a, dt.OP_AG, buf)
-        assert buf.cpu().tolist() == oplan.ag_order(w, r, m, n, cr, 128, 256, swizzle)
-    a = dt.make_args(w, m, n, 8, chunk_rows=cr, swizzle=swizzle)
+        assert buf.cpu().tolist() == oplan.ag_order(w, r, m, n, cr, bm, 256, swizzle)
+    a = dt.make_args(w, m, n, 8, chunk_rows=cr, swizzle=swizzle, tile_m=bm)
     t = dt.tile_count(a, dt.OP_RS)
     buf = torch.full((t,), -1, dtype=torch.int32, device="cuda")
     dt.swizzle_plan_device(a, dt.OP_RS, buf)
-    assert buf.cpu().tolist() == oplan.rs_order(w, m, n, cr, 128, 256, swizzle)
+    assert buf.cpu().tolist() == oplan.rs_order(w, m, n, cr, bm, 256, swizzle)
+    if n % (8 * w) == 0:  # the AllToAll over the same rows, each rank's M/W of them
+        a = dt.make_args(w, m, n, 8, chunk_rows=cr, swizzle=swizzle, tile_m=bm)
+        t = dt.tile_count(a, dt.OP_A2A)
+        buf = torch.full((t,), -1, dtype=torch.int32, device="cuda")
+        dt.swizzle_plan_device(a, dt.OP_A2A, buf)
+        assert buf.cpu().tolist() == oplan.a2a_order(w, m // w, n, cr, bm, 256, swizzle)

@@ -55,36 +55,43 @@ def w4():
 
 @pytest.mark.parametrize("swizzle", [True, False])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-def test_w4_parity(dt, w4, swizzle, out_dtype):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_w4_parity(dt, w4, swizzle, out_dtype, tile_m):
     wl, inp, ref = w4
-    outs = _run(dt, inp, wl.m, wl.n, wl.k, out_dtype, chunk_rows=wl.chunk_rows, swizzle=swizzle)
+    outs = _run(dt, inp, wl.m, wl.n, wl.k, out_dtype, chunk_rows=wl.chunk_rows, swizzle=swizzle,
+                tile_m=tile_m)
     _check_all(outs, ref, out_dtype, what=f"swz={swizzle}")
 
 
 def test_w4_bit_identical_across_variants(dt, w4):
     wl, inp, ref = w4
-    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256)
-    for swizzle in [True, False]:
-        for cr in [1, 64, 100, 512, 4096]:
-            outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=swizzle)
-            assert all(bits_equal(o, b) for o, b in zip(outs, base)), (swizzle, cr)
-    for group in [1, 3]:
-        outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, group=group)
+    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, tile_m=128)
+    for tile_m in [128, 256]:  # one CTA or a CTA pair per tile: the same bits
+        for swizzle in [True, False]:
+            for cr in [1, 64, 100, 512, 4096]:
+                outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=swizzle,
+                            tile_m=tile_m)
+                assert all(bits_equal(o, b) for o, b in zip(outs, base)), (tile_m, swizzle, cr)
+        for group in [1, 3]:
+            outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, group=group, tile_m=tile_m)
+            assert all(bits_equal(o, b) for o, b in zip(outs, base))
+        outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, fn=dt.gemm_rs_kernel_overlap,
+                    tile_m=tile_m)
         assert all(bits_equal(o, b) for o, b in zip(outs, base))
-    outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, fn=dt.gemm_rs_kernel_overlap)
-    assert all(bits_equal(o, b) for o, b in zip(outs, base))
 
 
-def test_ragged_parity_and_identity(dt):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_ragged_parity_and_identity(dt, tile_m):
     wl = WORKLOADS["rs_w6_m6000_n5120_k3000"]
     inp = wl.make()
     ref = _oracle(inp)
-    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows)
+    base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, tile_m=tile_m)
     _check_all(base, ref, "bf16", what="ragged")
     for swizzle, cr in [(False, wl.chunk_rows), (True, 77), (True, 1000)]:
-        outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=swizzle)
+        outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=swizzle, tile_m=tile_m)
         assert all(bits_equal(o, b) for o, b in zip(outs, base)), (swizzle, cr)
-    outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, fn=dt.gemm_rs_kernel_overlap)
+    outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, fn=dt.gemm_rs_kernel_overlap,
+                tile_m=tile_m)
     assert all(bits_equal(o, b) for o, b in zip(outs, base))
 
 
@@ -100,13 +107,15 @@ def test_ragged_parity_and_identity(dt):
     (5, 5 * 130, 256, 20, 130),
 ])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-def test_edge_shapes(dt, case, out_dtype):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_edge_shapes(dt, case, out_dtype, tile_m):
     w, m, n, k, cr = case
     inp = make_rs_inputs(w, m, n, k, seed=41 + m)
     ref = _oracle(inp)
     lda = -(-k // 8) * 8  # 16-byte rows: K per rank need not be a multiple of 8
     for swizzle in [True, False]:
-        outs = _run(dt, inp, m, n, k, out_dtype, lda=lda, chunk_rows=cr, swizzle=swizzle)
+        outs = _run(dt, inp, m, n, k, out_dtype, lda=lda, chunk_rows=cr, swizzle=swizzle,
+                    tile_m=tile_m)
         _check_all(outs, ref, out_dtype, what=f"{case}")
 
 
@@ -133,11 +142,12 @@ def test_k_zero(dt):
     assert all((o == 0).all() for o in outs)
 
 
-def test_repeated_calls_reuse_counters(dt, w4):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_repeated_calls_reuse_counters(dt, w4, tile_m):
     """Arrival counters return to zero inside each call, so back-to-back calls on one
     workspace keep reducing correctly."""
     wl, inp, ref = w4
-    args = dt.make_args(4, wl.m, wl.n, wl.k, chunk_rows=128)
+    args = dt.make_args(4, wl.m, wl.n, wl.k, chunk_rows=128, tile_m=tile_m)
     ws = workspace(dt.workspace_size(args, dt.OP_RS))
     a = [dev_bf16(x) for x in inp.a]
     b = [dev_bf16(x) for x in inp.b]

@@ -10,4 +10,4 @@ from .capi import (BACKENDS, OP_A2A, OP_AG, OP_AR, OP_RS, DtArgs, DtError,  # no
                    ag_gemm_static_scratch, check, debug_drop_transfer, ffn_ag_rs, gemm_a2a,
                    gemm_a2a_kernel_overlap, gemm_ar, gemm_ar_kernel_overlap, gemm_rs,
                    gemm_rs_kernel_overlap, make_args, swizzle_plan, swizzle_plan_device,
-                   tile_count, tune_ag_gemm, tune_reduce, workspace_init, workspace_size)
+                   tile_count, tile_rows, tune_ag_gemm, tune_reduce, workspace_init, workspace_size)

@@ -43,6 +43,8 @@ _SIGS = {
     "dt_gemm_a2a": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_gemm_a2a_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_a2a_signals": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int64, _P]),
+    "dt_tile_count": (ctypes.c_int64, [_P, ctypes.c_int]),
+    "dt_tile_rows": (ctypes.c_int32, [_P, ctypes.c_int]),
     "dt_swizzle_plan": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64]),
     "dt_swizzle_plan_device": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64, _P]),
     "dt_check": (ctypes.c_int, [_P, _P, _P]),
@@ -147,7 +149,7 @@ def _ptr_array(xs):
 def make_args(world_size: int, m: int, n: int, k: int, *, rank: int = 0, chunk_rows: int = 128,
               swizzle: bool = True, backend: str = "auto", out_dtype: str = "bf16",
               lda: int = 0, ldb: int = 0, ldc: int = 0, timeout_us: int = 0, num_sms: int = 0,
-              group: int = 8, copy_ctas: int = 0, act: str = "none") -> DtArgs:
+              group: int = 8, copy_ctas: int = 0, act: str = "none", tile_m: int = 0) -> DtArgs:
     a = DtArgs()
     lib().dt_args_default(ctypes.byref(a))
     a.world_size, a.rank, a.m, a.n, a.k = world_size, rank, m, n, k
@@ -161,6 +163,7 @@ def make_args(world_size: int, m: int, n: int, k: int, *, rank: int = 0, chunk_r
     a.group = group
     a.copy_ctas = copy_ctas
     a.act = ACTS[act]
+    a.tile_m = tile_m
     return a
 
 
@@ -264,12 +267,19 @@ def a2a_signals(args: DtArgs, workspace, stream=None):
 
 
 def tile_count(args: DtArgs, op: int) -> int:
-    if op == OP_A2A:  # each rank's rows tiled on their own, columns per destination block
-        w = args.world_size
-        return w * -(-(args.m // w) // 128) * w * -(-(args.n // w) // 256)
-    tm = -(-args.m // 128)
-    tn = -(-args.n // 256)
-    return (1 if op == OP_AG else args.world_size) * tm * tn  # RS and AR: all W ranks' tiles
+    """Tiles of the execution order (the library's count, tile rows resolved)."""
+    t = lib().dt_tile_count(ctypes.byref(args), op)
+    if t < 0:
+        _raise(DT_ERR_INVALID)
+    return int(t)
+
+
+def tile_rows(args: DtArgs, op: int) -> int:
+    """Rows of one tile of the order: 128 (one CTA) or 256 (a CTA pair)."""
+    r = lib().dt_tile_rows(ctypes.byref(args), op)
+    if r < 0:
+        _raise(DT_ERR_INVALID)
+    return int(r)
 
 
 def swizzle_plan(args: DtArgs, op: int) -> np.ndarray:

@@ -99,6 +99,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Derived {
   int op;
   int32_t W, rank, G, Tm, Tn, KB, T, nC, pieces_max;
+  int32_t bm;    // rows of a tile in the order: 128 (one CTA) or 256 (a CTA pair)
+  bool pair;
+  int32_t Tm128; // 128-row m-tiles (one CTA's rows): the ReduceScatter's unit granularity
   int64_t M, N, K, Ms, Cr, lda, ldb, ldc, ld_gather;
   bool swizzle, f32;
   int backend;  // resolved for AG
@@ -159,8 +162,10 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     return fail(DT_ERR_INVALID, "leading dimension smaller than the row length");
   if ((d->lda % 8) || (d->ldb % 8) || (d->ldc % 8))
     return fail(DT_ERR_INVALID, "leading dimensions must be multiples of 8 elements (16-byte rows)");
-  if ((a->tile_m != 0 && a->tile_m != kBM) || (a->tile_n != 0 && a->tile_n != kBN))
-    return fail(DT_ERR_UNSUPPORTED, "tiles other than %dx%d are not built", kBM, kBN);
+  if ((a->tile_m != 0 && a->tile_m != kBM && a->tile_m != 2 * kBM) ||
+      (a->tile_n != 0 && a->tile_n != kBN))
+    return fail(DT_ERR_UNSUPPORTED, "tiles other than %dx%d and %dx%d are not built", kBM, kBN,
+                2 * kBM, kBN);
   if (a->out_dtype != DT_BF16 && a->out_dtype != DT_F32)
     return fail(DT_ERR_INVALID, "unknown out_dtype %d", a->out_dtype);
   d->f32 = a->out_dtype == DT_F32;
@@ -169,8 +174,22 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   d->timeout_ns = a->timeout_us > 0 ? static_cast<uint64_t>(a->timeout_us) * 1000ull
                                     : default_timeout_ns();
   d->Ms = d->M / d->W;
-  d->geom = a2a ? make_geom_a2a(d->W, d->M, d->N, d->Cr, kBM, kBN, d->G, d->swizzle ? 1 : 0)
-              : make_geom(d->W, d->rank, d->M, d->N, d->Cr, kBM, kBN, d->G, d->swizzle ? 1 : 0);
+  // tile rows: as asked, or a CTA pair (256 rows) when that still gives every pair of SMs a
+  // tile (at least 76 pair tiles), else one CTA (128 rows)
+  const int64_t rows_tiled = a2a ? d->Ms : d->M;  // rows one rank's tiles cover
+  const int64_t copies = op == DT_OP_AG_GEMM ? 1 : d->W;
+  if (a->tile_m != 0) {
+    d->bm = a->tile_m;
+  } else {
+    const int64_t t256 = copies * cdiv64(rows_tiled, 2 * kBM) * cdiv64(a2a ? d->N / d->W : d->N, kBN) *
+                         (a2a ? d->W : 1);
+    const bool odd_copiers = op == DT_OP_AG_GEMM && (a->copy_ctas % 2) != 0;
+    d->bm = t256 >= 76 && !odd_copiers ? 2 * kBM : kBM;
+  }
+  d->pair = d->bm == 2 * kBM;
+  d->Tm128 = static_cast<int32_t>(cdiv64(rows_tiled, kBM));
+  d->geom = a2a ? make_geom_a2a(d->W, d->M, d->N, d->Cr, d->bm, kBN, d->G, d->swizzle ? 1 : 0)
+              : make_geom(d->W, d->rank, d->M, d->N, d->Cr, d->bm, kBN, d->G, d->swizzle ? 1 : 0);
   d->nC = d->geom.nC;
   d->Tm = d->geom.Tm;
   d->Tn = d->geom.Tn;
@@ -201,6 +220,8 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     return fail(DT_ERR_INVALID, "copy_ctas %d outside 0..64", d->copy_ctas);
   if (d->copy_ctas > 0 && be == DT_XFER_COPY_ENGINE)
     return fail(DT_ERR_INVALID, "dedicated transfer CTAs need DT_XFER_TMA or DT_XFER_LDST");
+  if (d->pair && d->copy_ctas % 2)
+    return fail(DT_ERR_INVALID, "CTA-pair tiles need an even copy_ctas");
   // workspace layout: error word | control arrays | tile order || data
   const size_t nchunks = static_cast<size_t>(d->W) * d->nC;
   size_t off = 256;
@@ -218,9 +239,11 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     d->off_ready = off;
     off = align_up(off + 4 * nchunks * d->W, 256);
   } else {
-    d->pieces_max = d->Tm > 0 && d->Ms > 0 ? rs_pieces_max(d->geom) : 0;
+    // reduction units live on one CTA's 128 rows, whatever the tile of the order
+    const Geom g128 = make_geom(d->W, 0, d->M, d->N, d->Cr, kBM, kBN, d->G, 1);
+    d->pieces_max = d->Tm128 > 0 && d->Ms > 0 ? rs_pieces_max(g128) : 0;
     d->off_cnt = off;
-    off = align_up(off + 4 * static_cast<size_t>(d->Tm) * d->Tn * d->pieces_max, 256);
+    off = align_up(off + 4 * static_cast<size_t>(d->Tm128) * d->Tn * d->pieces_max, 256);
   }
   d->off_order = off;
   off = align_up(off + 4 * static_cast<size_t>(d->T), 1024);
@@ -237,11 +260,11 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
 
 // ------------------------------------------------------------------------------ per-workspace state
 struct LayoutKey {
-  int op, W, rank, G, swz;
+  int op, W, rank, G, swz, bm;
   long long M, N, K, Cr;
   bool operator==(const LayoutKey& o) const {
-    return op == o.op && W == o.W && rank == o.rank && G == o.G && swz == o.swz && M == o.M &&
-           N == o.N && K == o.K && Cr == o.Cr;
+    return op == o.op && W == o.W && rank == o.rank && G == o.G && swz == o.swz && bm == o.bm &&
+           M == o.M && N == o.N && K == o.K && Cr == o.Cr;
   }
 };
 
@@ -257,13 +280,13 @@ std::map<const void*, WsState> g_ws;
 int32_t g_drop_transfer = -1;
 
 LayoutKey key_of(const Derived& d) {
-  return LayoutKey{d.op, d.W, d.rank, d.G, d.swizzle ? 1 : 0, d.M, d.N, d.K, d.Cr};
+  return LayoutKey{d.op, d.W, d.rank, d.G, d.swizzle ? 1 : 0, d.bm, d.M, d.N, d.K, d.Cr};
 }
 
 // 64-bit tag of the workspace layout (FNV-1a over the key), never 0
 unsigned long long layout_tag(const Derived& d) {
   const LayoutKey k = key_of(d);
-  const long long v[9] = {k.op, k.W, k.rank, k.G, k.swz, k.M, k.N, k.K, k.Cr};
+  const long long v[10] = {k.op, k.W, k.rank, k.G, k.swz, k.bm, k.M, k.N, k.K, k.Cr};
   unsigned long long h = 1469598103934665603ull;
   for (long long x : v) {
     for (int b = 0; b < 8; ++b) {
@@ -421,6 +444,13 @@ dt_status check_ws(const Derived& d, void* ws, size_t bytes) {
   return DT_OK;
 }
 
+// Persistent grid over `tiles` tiles of the order with `sms` SMs to use: one CTA per SM, or
+// one cluster of two per pair of SMs.
+int grid_for(const Derived& d, int64_t tiles, int sms) {
+  if (d.pair) return 2 * static_cast<int>(std::min<int64_t>(tiles, std::max(sms / 2, 1)));
+  return static_cast<int>(std::min<int64_t>(tiles, sms));
+}
+
 void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
   memset(&p, 0, sizeof(p));
   uint8_t* w = reinterpret_cast<uint8_t*>(ws);
@@ -547,8 +577,8 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
   const int use = a->num_sms > 0 ? std::min(a->num_sms, sms) : sms;
   if (d.copy_ctas >= use) return fail(DT_ERR_INVALID, "copy_ctas must leave SMs for the GEMM");
   p.copy_ctas = d.copy_ctas;
-  const int grid = d.copy_ctas + static_cast<int>(std::min<int64_t>(d.T, use - d.copy_ctas));
-  const cudaError_t e = launch_ag_kernel(p, copy, d.f32, grid, true, stream);
+  const int grid = d.copy_ctas + grid_for(d, d.T, use - d.copy_ctas);
+  const cudaError_t e = launch_ag_kernel(p, copy, d.f32, grid, true, stream, d.pair);
   if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
   return DT_OK;
 }
@@ -565,7 +595,7 @@ void dt_args_default(dt_args* a) {
   a->swizzle = 1;
   a->backend = DT_XFER_AUTO;
   a->out_dtype = DT_BF16;
-  a->tile_m = kBM;
+  a->tile_m = 0;  // CTA pairs when the problem has enough 256-row tiles
   a->tile_n = kBN;
   a->group = 8;
   a->chunk_rows = 128;
@@ -608,6 +638,18 @@ dt_status dt_workspace_init(const dt_args* a, int op, void* ws, size_t ws_bytes,
   }
   DT_CUDA(cudaMemsetAsync(ws, 0, d.ctl_bytes, reinterpret_cast<cudaStream_t>(stream)));
   return DT_OK;
+}
+
+int64_t dt_tile_count(const dt_args* a, int op) {
+  Derived d;
+  if (derive(a, op, &d) != DT_OK) return -1;
+  return d.T;
+}
+
+int32_t dt_tile_rows(const dt_args* a, int op) {
+  Derived d;
+  if (derive(a, op, &d) != DT_OK) return -1;
+  return d.bm;
 }
 
 dt_status dt_swizzle_plan(const dt_args* a, int op, int32_t* order, int64_t len) {
@@ -691,12 +733,12 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
     return s;
 
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
-  const int grid = static_cast<int>(std::min<int64_t>(d.T, sms));
+  const int grid = grid_for(d, d.T, sms);
   if (d.W == 1) {
     // one rank gathers nothing: the GEMM reads its shard where it is
     if ((s = make_tmap(&p.tmA[0], a_shards[0], d.K, d.M, d.lda * 2, 64, kBM)) != DT_OK) return s;
     p.wait_flags = 0;
-    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream);
+    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.pair);
     if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
     return DT_OK;
   }
@@ -714,7 +756,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
       // start the GEMM once the chunks its first tiles need are queued (at once when the own
       // rank's tiles read in place)
       if ((tc == d.nC || p.own_in_place) && !launched) {
-        cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream);
+        cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.pair);
         if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
         launched = true;
       }
@@ -729,7 +771,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
       if (r != CUDA_SUCCESS) return fail(DT_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)r);
     }
     if (!launched) {
-      cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream);
+      cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.pair);
       if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
     }
     DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
@@ -739,8 +781,9 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
   const int copy = d.backend == DT_XFER_TMA ? kCopyTma : kCopyLdst;
   p.copy_ctas = d.copy_ctas;
   if (d.copy_ctas >= sms) return fail(DT_ERR_INVALID, "copy_ctas must leave SMs for the GEMM");
-  const int grid_ded = d.copy_ctas + static_cast<int>(std::min<int64_t>(d.T, sms - d.copy_ctas));
-  cudaError_t e = launch_ag_kernel(p, copy, d.f32, d.copy_ctas ? grid_ded : grid, true, stream);
+  const int grid_ded = d.copy_ctas + grid_for(d, d.T, sms - d.copy_ctas);
+  cudaError_t e =
+      launch_ag_kernel(p, copy, d.f32, d.copy_ctas ? grid_ded : grid, true, stream, d.pair);
   if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
   return DT_OK;
 }
@@ -785,10 +828,9 @@ dt_status dt_ag_gemm_kernel_overlap(const void* const* a_shards, const void* b, 
     const int64_t hi = static_cast<int64_t>(cs) * d.Ms + std::min<int64_t>((cj + 1) * d.Cr, d.Ms);
     p.row_lo = lo;
     p.row_hi = hi;
-    p.Tm = static_cast<int32_t>(cdiv64(hi - lo, kBM));
+    p.Tm = static_cast<int32_t>(cdiv64(hi - lo, d.bm));
     p.T = p.Tm * d.Tn;
-    const int grid = std::min(p.T, sms);
-    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream);
+    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid_for(d, p.T, sms), false, stream, d.pair);
     if (e != cudaSuccess) return cuda_fail(e, "per-chunk GEMM launch");
   }
   DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
@@ -874,8 +916,7 @@ static dt_status reduce_fused(const void* const* a_, const void* const* b_, void
   KParams p;
   if ((s = rs_params(p, d, a_, b_, out, ws, epoch)) != DT_OK) return s;
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
-  const int grid = static_cast<int>(std::min<int64_t>(d.T, sms));
-  cudaError_t e = launch_rs_kernel(p, d.f32, grid, stream);
+  cudaError_t e = launch_rs_kernel(p, d.f32, grid_for(d, d.T, sms), stream, d.pair);
   if (e != cudaSuccess) return cuda_fail(e, "fused GEMM-ReduceScatter / AllReduce launch");
   return DT_OK;
 }
@@ -908,10 +949,9 @@ static dt_status reduce_kernel_overlap(const void* const* a_, const void* const*
     // one GEMM launch for destination block st (all W sources), fp32 partials only
     p.row_lo = static_cast<int64_t>(st) * d.Ms;
     p.row_hi = p.row_lo + d.Ms;
-    p.Tm = static_cast<int32_t>(cdiv64(d.Ms, kBM));
+    p.Tm = static_cast<int32_t>(cdiv64(d.Ms, d.bm));
     p.T = d.W * p.Tm * d.Tn;
-    const int grid = std::min(p.T, sms);
-    cudaError_t e = launch_rs_kernel(p, d.f32, grid, stream);
+    cudaError_t e = launch_rs_kernel(p, d.f32, grid_for(d, p.T, sms), stream, d.pair);
     if (e != cudaSuccess) return cuda_fail(e, "per-destination GEMM launch");
     DT_CUDA(cudaEventRecord(dev->chunk_events[st], stream));
     DT_CUDA(cudaStreamWaitEvent(dev->side, dev->chunk_events[st], 0));
@@ -1016,8 +1056,7 @@ dt_status dt_gemm_a2a(const void* const* a_, const void* const* b_, void* const*
   if ((s = a2a_params(p, d, a_, b_, ws, epoch)) != DT_OK) return s;
   for (int h = 0; h < d.W; ++h) p.out[h] = out[h];
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
-  const int grid = static_cast<int>(std::min<int64_t>(d.T, sms));
-  cudaError_t e = launch_a2a_kernel(p, d.f32, grid, stream);
+  cudaError_t e = launch_a2a_kernel(p, d.f32, grid_for(d, d.T, sms), stream, d.pair);
   if (e != cudaSuccess) return cuda_fail(e, "fused GEMM-AllToAll launch");
   return DT_OK;
 }
@@ -1054,7 +1093,7 @@ dt_status dt_gemm_a2a_kernel_overlap(const void* const* a_, const void* const* b
   for (int32_t st = 0; st < d.W; ++st) {
     // step st: every rank q computes the block of destination (q + st + 1) mod W
     p.a2a_step = st;
-    cudaError_t e = launch_a2a_kernel(p, d.f32, std::min(p.T, sms), stream);
+    cudaError_t e = launch_a2a_kernel(p, d.f32, grid_for(d, p.T, sms), stream, d.pair);
     if (e != cudaSuccess) return cuda_fail(e, "per-step GEMM launch");
     DT_CUDA(cudaEventRecord(dev->chunk_events[st], stream));
     DT_CUDA(cudaStreamWaitEvent(dev->side, dev->chunk_events[st], 0));

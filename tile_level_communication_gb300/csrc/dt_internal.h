@@ -20,11 +20,48 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
 void set_last_error(const char* msg);
 
 // Launch the fused persistent kernel; defined in dt_ag.cu (AllGather variants), dt_rs.cu
-// (ReduceScatter / AllReduce variants) and dt_a2a.cu (AllToAll variants).  `cooperative` guarantees that every CTA is resident,
-// which the in-kernel chunk transfer relies on.
+// (ReduceScatter / AllReduce variants) and dt_a2a.cu (AllToAll variants).  `cooperative`
+// guarantees that every CTA is resident, which the in-kernel chunk transfer relies on.
+// `pair`: 256-row tiles on clusters of two CTAs (grid and copy_ctas even).
 cudaError_t launch_ag_kernel(const KParams& p, int copy_mode, bool f32, int grid,
-                             bool cooperative, cudaStream_t stream);
-cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream);
-cudaError_t launch_a2a_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream);
+                             bool cooperative, cudaStream_t stream, bool pair);
+cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream, bool pair);
+cudaError_t launch_a2a_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream,
+                              bool pair);
+
+// One launch of an instance of the fused kernel (dynamic shared memory raised once).
+template <int OP, int COPY, bool F32, bool PAIR>
+cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStream_t stream) {
+  auto kern = fused_gemm_kernel<OP, COPY, F32, PAIR>;
+  const int smem = kernel_smem_bytes(OP == kOpRS, COPY, PAIR);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  if (PAIR) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
 
 }  // namespace dt

@@ -28,14 +28,18 @@
 
 namespace dt {
 
-constexpr int kBM = 128;
+constexpr int kBM = 128;                 // rows of A per CTA (a CTA pair's tile has 256)
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
 constexpr int kThreads = 256;
 constexpr int kAStage = kBM * kBK * 2;   // 16 KB: 128 rows x 64 bf16, 128-byte swizzle
 constexpr int kBSlab = kBK * 64 * 2;     // 8 KB: 64 k-rows x 64 bf16 columns
-constexpr int kBStage = 4 * kBSlab;      // 32 KB
+// Operand ring per CTA: one CTA per tile stages all 256 columns of B (4 slabs, 32 KB) in 4
+// stages; a CTA pair splits them (2 slabs, 16 KB each) and affords 6 stages.
+__host__ __device__ constexpr int stages(bool pair) { return pair ? 6 : 4; }
+__host__ __device__ constexpr int b_slabs(bool pair) { return pair ? 2 : 4; }
+__host__ __device__ constexpr int b_stage_bytes(bool pair) { return b_slabs(pair) * kBSlab; }
+constexpr int kMaxStages = 6;
 constexpr int kCopyBuf = 16384;          // TMA bulk copy staging, two buffers
 constexpr int kTmemCols = 512;           // two 128x256 fp32 accumulators
 constexpr int kMaxW = 16;
@@ -60,9 +64,9 @@ enum DevCode : uint32_t {
 __host__ __device__ constexpr bool has_staging(bool rs, int copy_mode) {
   return rs || copy_mode == kCopyTma;
 }
-__host__ __device__ constexpr int kernel_smem_bytes(bool rs, int copy_mode) {
-  return 1024 + kStages * (kAStage + kBStage) + (has_staging(rs, copy_mode) ? 2 * kCopyBuf : 0) +
-         kMiscBytes;
+__host__ __device__ constexpr int kernel_smem_bytes(bool rs, int copy_mode, bool pair) {
+  return 1024 + stages(pair) * (kAStage + b_stage_bytes(pair)) +
+         (has_staging(rs, copy_mode) ? 2 * kCopyBuf : 0) + kMiscBytes;
 }
 
 struct KParams {
@@ -124,12 +128,16 @@ struct SmemLayout {
   volatile uint32_t* last_mask;  // RS: pieces of the current tile folded in order [4]
   volatile int8_t* chain;        // RS: per piece, first parked partial this tile folds (-1)
   uint32_t* ready_bits;
+  int ns;  // pipeline stages
+  // barrier slots: full[ns], empty[ns], tfull[2], tempty[2], copyb[2], fin (at most 19);
+  // slots 24..31 belong to the dedicated transfer CTAs' workers
   __device__ uint32_t full(int s) const { return smem_u32(bars + s); }
-  __device__ uint32_t empty(int s) const { return smem_u32(bars + kStages + s); }
-  __device__ uint32_t tfull(int a) const { return smem_u32(bars + 2 * kStages + a); }
-  __device__ uint32_t tempty(int a) const { return smem_u32(bars + 2 * kStages + 2 + a); }
-  __device__ uint32_t copyb(int b) const { return smem_u32(bars + 2 * kStages + 4 + b); }
-  __device__ uint32_t fin() const { return smem_u32(bars + 2 * kStages + 6); }
+  __device__ uint32_t empty(int s) const { return smem_u32(bars + ns + s); }
+  __device__ uint32_t tfull(int a) const { return smem_u32(bars + 2 * ns + a); }
+  __device__ uint32_t tempty(int a) const { return smem_u32(bars + 2 * ns + 2 + a); }
+  __device__ uint32_t copyb(int b) const { return smem_u32(bars + 2 * ns + 4 + b); }
+  __device__ uint32_t fin() const { return smem_u32(bars + 2 * ns + 6); }
+  __device__ uint32_t worker(int w) const { return smem_u32(bars + 24 + w); }
 };
 
 __device__ __forceinline__ void raise_error(const KParams& p, uint32_t code, uint32_t site,
@@ -146,9 +154,8 @@ __device__ __forceinline__ void raise_error(const KParams& p, uint32_t code, uin
 // flag and returns false; returns false at once when another role has aborted.  A pipeline
 // barrier only stalls when the role upstream of it stalls, so its bound is 4x the flag-wait
 // bound: the wait at the root of a stall reports first.
-static __device__ __noinline__ bool wait_bar(const KParams& p, const SmemLayout& L, uint32_t bar,
-                                      uint32_t parity, uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool wait_bar_slow(const KParams& p, const SmemLayout& L,
+                                                 uint32_t bar, uint32_t parity, uint32_t site) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -161,6 +168,13 @@ static __device__ __noinline__ bool wait_bar(const KParams& p, const SmemLayout&
       }
     }
   }
+}
+// The issuing threads wait once per k-block: the first test is inline (a call per wait costs
+// the MMA issue loop about an eighth of its rate); the timed retry loop is out of line.
+__device__ __forceinline__ bool wait_bar(const KParams& p, const SmemLayout& L, uint32_t bar,
+                                        uint32_t parity, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(p, L, bar, parity, site);
 }
 
 // Bounded acquire-poll of a chunk's ready flag.
@@ -183,12 +197,19 @@ static __device__ __noinline__ bool wait_flag(const KParams& p, const SmemLayout
 }
 
 struct TileInfo {
-  int32_t q, i, n, h;
+  int32_t q, i, n, h;  // i: index of this CTA's 128-row m-tile
   int64_t row0, row_end, col0, col_end;
   bool valid;
 };
 
-template <int OP>
+// CTA pairs: the two CTAs of a cluster work on the same tile of the order, each on its own
+// 128 of the tile's 256 rows (cluster rank 0: the upper half).
+template <bool PAIR>
+__device__ __forceinline__ uint32_t pair_rank() {
+  return PAIR ? (blockIdx.x & 1u) : 0u;
+}
+
+template <int OP, bool PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
   int32_t t = p.plain ? pos : __ldg(p.order + pos);
   TileInfo ti;
@@ -199,8 +220,9 @@ __device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
   const int32_t per_q = p.Tm * tn;
   ti.q = OP != kOpAG ? t / per_q : 0;
   const int32_t rem = t - ti.q * per_q;
-  ti.i = rem / tn;
-  ti.n = rem - ti.i * tn;
+  const int32_t it = rem / tn;
+  ti.n = rem - it * tn;
+  ti.i = PAIR ? 2 * it + static_cast<int32_t>(pair_rank<PAIR>()) : it;
   ti.row0 = p.row_lo + static_cast<int64_t>(ti.i) * kBM;
   ti.row_end = min64(ti.row0 + kBM, p.row_hi);
   if (OP == kOpA2A) {
@@ -222,23 +244,30 @@ __device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
   return ti;
 }
 
-// Compute CTAs are blockIdx.x >= copy_ctas; they take the tile order round robin.
+// Compute CTAs are blockIdx.x >= copy_ctas; they (or their pairs) take the tile order round
+// robin.
+template <bool PAIR>
 __device__ __forceinline__ int32_t first_pos(const KParams& p) {
-  return static_cast<int32_t>(blockIdx.x) - p.copy_ctas;
+  return (static_cast<int32_t>(blockIdx.x) - p.copy_ctas) / (PAIR ? 2 : 1);
 }
+template <bool PAIR>
 __device__ __forceinline__ int32_t pos_stride(const KParams& p) {
-  return static_cast<int32_t>(gridDim.x) - p.copy_ctas;
+  return (static_cast<int32_t>(gridDim.x) - p.copy_ctas) / (PAIR ? 2 : 1);
 }
 
 // ============================================================================ producer
-template <int OP>
+template <int OP, bool PAIR>
 __device__ void run_producer(const KParams& p, const SmemLayout& L) {
+  constexpr int NS = stages(PAIR);
+  constexpr int NB = b_slabs(PAIR);
+  // a pair's loads complete on the even CTA's barriers; it expects both CTAs' bytes
+  const bool leader = pair_rank<PAIR>() == 0;
   uint32_t kit = 0;
-  int64_t last_issue[kStages];
+  int64_t last_issue[NS];
 #pragma unroll
-  for (int s = 0; s < kStages; ++s) last_issue[s] = -1;
-  for (int32_t pos = first_pos(p); pos < p.T; pos += pos_stride(p)) {
-    const TileInfo ti = decode_tile<OP>(p, pos);
+  for (int s = 0; s < NS; ++s) last_issue[s] = -1;
+  for (int32_t pos = first_pos<PAIR>(p); pos < p.T; pos += pos_stride<PAIR>(p)) {
+    const TileInfo ti = decode_tile<OP, PAIR>(p, pos);
     if (!ti.valid) {
       raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
       continue;
@@ -270,26 +299,40 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
     const CUtensorMap* tA = &p.tmA[OP != kOpAG ? ti.q : (own_tile ? 1 : 0)];
     const CUtensorMap* tB = &p.tmB[OP != kOpAG ? ti.q : 0];
     const int32_t a_row = static_cast<int32_t>(own_tile ? ti.row0 - own0 : ti.row0);
+    // this CTA's columns of B: all 256, or its half of the pair's
+    const int32_t b_col = static_cast<int32_t>(ti.col0) +
+                          static_cast<int32_t>(pair_rank<PAIR>()) * (NB * 64);
     bool ok = true;
     for (int32_t kb = 0; kb < p.KB; ++kb, ++kit) {
-      const int st = static_cast<int>(kit % kStages);
-      const uint32_t ph = (kit / kStages) & 1u;
+      const int st = static_cast<int>(kit % NS);
+      const uint32_t ph = (kit / NS) & 1u;
       if (!wait_bar(p, L, L.empty(st), ph ^ 1u, 100 + st)) { ok = false; break; }
-      mbar_expect_tx(L.full(st), kAStage + kBStage);
-      tma_load_2d(smem_u32(L.a + st * kAStage), tA, kb * kBK, a_row, L.full(st));
+      const uint32_t a_dst = smem_u32(L.a + st * kAStage);
+      const uint32_t b_dst = smem_u32(L.b + st * b_stage_bytes(PAIR));
+      if constexpr (PAIR) {
+        const uint32_t bar = mapa_shared(L.full(st), 0);
+        if (leader) mbar_expect_tx(L.full(st), 2 * (kAStage + b_stage_bytes(PAIR)));
+        tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-        tma_load_2d(smem_u32(L.b + st * kBStage + jj * kBSlab), tB,
-                    static_cast<int32_t>(ti.col0) + jj * 64, kb * kBK, L.full(st));
+        for (int jj = 0; jj < NB; ++jj)
+          tma_load_2d_pair(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, bar);
+      } else {
+        mbar_expect_tx(L.full(st), kAStage + b_stage_bytes(PAIR));
+        tma_load_2d(a_dst, tA, kb * kBK, a_row, L.full(st));
+#pragma unroll
+        for (int jj = 0; jj < NB; ++jj)
+          tma_load_2d(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, L.full(st));
+      }
       last_issue[st] = kit;
     }
     if (!ok) break;
   }
-  if (*L.abort_flag) {
-    // let every TMA load this thread issued land before the CTA can exit
-    for (int s = 0; s < kStages; ++s) {
+  if (*L.abort_flag && leader) {
+    // let every TMA load issued into this stage ring land before the CTA can exit (a pair's
+    // leader barrier counts the other CTA's bytes as well)
+    for (int s = 0; s < NS; ++s) {
       if (last_issue[s] < 0) continue;
-      const uint32_t ph = static_cast<uint32_t>(last_issue[s] / kStages) & 1u;
+      const uint32_t ph = static_cast<uint32_t>(last_issue[s] / NS) & 1u;
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(L.full(s), ph) && globaltimer_ns() - t0 < p.timeout_ns) {
       }
@@ -298,14 +341,16 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
 }
 
 // ============================================================================ MMA issuer
-template <int OP>
+template <int OP, bool PAIR>
 __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_base) {
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, /*B MN-major*/ 1);
+  constexpr int NS = stages(PAIR);
+  // a pair's MMA has M = 256: rows 0-127 from the even CTA, 128-255 from the odd one
+  constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, kBN, /*B MN-major*/ 1);
   uint32_t kit = 0;
   int32_t tl = 0;
   bool issued = false;
-  for (int32_t pos = first_pos(p); pos < p.T; pos += pos_stride(p)) {
-    const TileInfo ti = decode_tile<OP>(p, pos);
+  for (int32_t pos = first_pos<PAIR>(p); pos < p.T; pos += pos_stride<PAIR>(p)) {
+    const TileInfo ti = decode_tile<OP, PAIR>(p, pos);
     if (!ti.valid) continue;
     const int acc = tl & 1;
     const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
@@ -314,29 +359,36 @@ __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_bas
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
     bool ok = true;
     for (int32_t kb = 0; kb < p.KB; ++kb, ++kit) {
-      const int st = static_cast<int>(kit % kStages);
-      const uint32_t ph = (kit / kStages) & 1u;
+      const int st = static_cast<int>(kit % NS);
+      const uint32_t ph = (kit / NS) & 1u;
+      // the stage was filled by TMA (async proxy) and is read by the MMAs (async proxy): the
+      // barrier's completion orders them; no tcgen05 fence here, which would hold the issue
+      // of this k-block until the MMAs in flight have finished
       if (!wait_bar(p, L, L.full(st), ph, 300 + st)) { ok = false; break; }
-      tc_fence_after();
       const uint32_t a0 = smem_u32(L.a + st * kAStage);
-      const uint32_t b0 = smem_u32(L.b + st * kBStage);
+      const uint32_t b0 = smem_u32(L.b + st * b_stage_bytes(PAIR));
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
         // A: K-major rows of 128 B, 8-row groups 1024 B apart; +32 B per 16 k
         const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
         // B: MN-major; 64-column slabs 8 KB apart (LBO), 8 k-row groups 1 KB apart (SBO)
         const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kBSlab, 1024);
-        umma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+        if constexpr (PAIR)
+          umma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+        else
+          umma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
       }
-      umma_commit(L.empty(st));  // frees the stage once these MMAs have read it
+      // frees the stage (in both CTAs of a pair) once these MMAs have read it
+      if constexpr (PAIR) umma_commit_pair(L.empty(st), 3); else umma_commit(L.empty(st));
       issued = true;
     }
     if (!ok) break;
-    umma_commit(L.tfull(acc));   // accumulator ready for the epilogue
+    // accumulator ready for the epilogue (of both CTAs)
+    if constexpr (PAIR) umma_commit_pair(L.tfull(acc), 3); else umma_commit(L.tfull(acc));
     ++tl;
   }
   if (*L.abort_flag && issued) {
-    umma_commit(L.fin());
+    if constexpr (PAIR) umma_commit_pair(L.fin(), 1); else umma_commit(L.fin());
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(L.fin(), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
     }
@@ -553,7 +605,7 @@ __device__ void fold_chain(const KParams& p, const SmemLayout& L, int32_t s, int
   }
 }
 
-template <int OP, bool F32>
+template <int OP, bool F32, bool PAIR>
 __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tmem_base,
                              int warp, int lane) {
   constexpr bool RS = OP == kOpRS;
@@ -566,8 +618,14 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
   int32_t tl = 0;
   uint32_t stage_ctr = 0;           // running-sum staging buffer in use (alternates)
   uint32_t ld_par[2] = {0u, 0u};    // phase of each staging buffer's load barrier
-  for (int32_t pos = first_pos(p); pos < p.T; pos += pos_stride(p)) {
-    const TileInfo ti = decode_tile<OP>(p, pos);
+  // a pair's accumulator is released on the even CTA's barrier, by the warps of both CTAs
+  uint32_t tempty_bar0 = L.tempty(0), tempty_bar1 = L.tempty(1);
+  if constexpr (PAIR) {
+    tempty_bar0 = mapa_shared(tempty_bar0, 0);
+    tempty_bar1 = mapa_shared(tempty_bar1, 0);
+  }
+  for (int32_t pos = first_pos<PAIR>(p); pos < p.T; pos += pos_stride<PAIR>(p)) {
+    const TileInfo ti = decode_tile<OP, PAIR>(p, pos);
     if (!ti.valid) continue;
     const int acc = tl & 1;
     const uint32_t ph = (static_cast<uint32_t>(tl) >> 1) & 1u;
@@ -748,7 +806,12 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(L.tempty(acc));
+    if (lane == 0) {
+      if constexpr (PAIR)
+        mbar_arrive_cluster(acc ? tempty_bar1 : tempty_bar0);
+      else
+        mbar_arrive(L.tempty(acc));
+    }
     ++tl;
 
     if (fused_a2a) {
@@ -756,13 +819,13 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
       // rows touch; the last tile of a chunk releases the chunk's ready flag
       __threadfence();
       named_bar_sync(1, 128);
-      if (et == 0) {
+      if (et == 0 && ti.row_end > ti.row0) {
         const int32_t j0 = static_cast<int32_t>(ti.row0 / p.g.Cr);
         const int32_t j1 = static_cast<int32_t>((ti.row_end - 1) / p.g.Cr);
         for (int32_t j = j0; j <= j1; ++j) {
           const int64_t c = (static_cast<int64_t>(ti.h) * p.g.W + ti.q) * p.g.nC + j;
           const uint32_t old = atom_add_acq_rel_gpu(p.unit_cnt + c, 1u);
-          if (old + 1u == static_cast<uint32_t>(a2a_chunk_tiles(p.g, j))) {
+          if (old + 1u == static_cast<uint32_t>(a2a_chunk_tiles(p.g, j, kBM))) {
             p.unit_cnt[c] = 0u;  // ready for the next call
             st_release_gpu(p.ready + c, p.epoch);
           }
@@ -810,9 +873,9 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
       }
       named_bar_sync(1, 128);
       // warm L2 with the running sums the next tile of this CTA will fold into
-      const int32_t npos = pos + pos_stride(p);
+      const int32_t npos = pos + pos_stride<PAIR>(p);
       if (npos < p.T) {
-        const TileInfo nt = decode_tile<OP>(p, npos);
+        const TileInfo nt = decode_tile<OP, PAIR>(p, npos);
         const int64_t nrow = nt.row0 + qd * 32 + lane;
         if (nt.valid && nrow < nt.row_end) {
           int32_t s, j;
@@ -968,15 +1031,19 @@ static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int 
 }
 
 // ============================================================================ kernel
-template <int OP, int COPY, bool F32>
+// PAIR: launched in clusters of two CTAs that share each 256-row tile (tcgen05 cta_group::2);
+// copy_ctas is then even, so dedicated transfer CTAs form whole clusters.
+template <int OP, int COPY, bool F32, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_constant__ KParams p) {
+  constexpr int NS = stages(PAIR);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   SmemLayout L;
+  L.ns = NS;
   L.a = base;
-  L.b = L.a + kStages * kAStage;
-  L.copy = L.b + kStages * kBStage;
+  L.b = L.a + NS * kAStage;
+  L.copy = L.b + NS * b_stage_bytes(PAIR);
   uint8_t* misc = L.copy + (has_staging(OP == kOpRS, COPY) ? 2 * kCopyBuf : 0);
   L.bars = reinterpret_cast<uint64_t*>(misc);  // up to 32 barriers
   L.tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
@@ -991,17 +1058,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < kReadyBitsWords) L.ready_bits[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(L.full(s), 1);
       mbar_init(L.empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(L.tfull(a), 1);
-      mbar_init(L.tempty(a), 4);
+      mbar_init(L.tempty(a), PAIR ? 8 : 4);  // the epilogue warps of the tile's CTA(s)
       mbar_init(L.copyb(a), 1);
     }
     mbar_init(L.fin(), 1);
-    for (int w = 0; w < 8; ++w) mbar_init(smem_u32(L.bars + 16 + w), 1);  // dedicated workers
+    for (int w = 0; w < 8; ++w) mbar_init(L.worker(w), 1);  // dedicated workers
     *L.abort_flag = 0;
     *L.unit_flag = 0;
     mbar_init_fence();
@@ -1011,9 +1078,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     tma_prefetch_desc(&p.tmB[0]);
   }
   const bool copier = static_cast<int32_t>(blockIdx.x) < p.copy_ctas;
-  if (warp == 1 && !copier) tmem_alloc(smem_u32(L.tmem_slot), kTmemCols);
+  if (warp == 1 && !copier) {
+    if constexpr (PAIR) tmem_alloc_pair(smem_u32(L.tmem_slot), kTmemCols);
+    else tmem_alloc(smem_u32(L.tmem_slot), kTmemCols);
+  }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the pair's barriers exist before either signals them
   tc_fence_after();
   const uint32_t tmem_base = copier ? 0u : *L.tmem_slot;
 
@@ -1022,15 +1093,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     if (OP == kOpAG && !p.plain) {
       if (COPY == kCopyTma && warp < 4 && lane == 0)
         run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x) * 4 + warp, p.copy_ctas * 4,
-                     L.a + warp * 2 * kCopyBuf, smem_u32(L.bars + 16 + 2 * warp),
-                     smem_u32(L.bars + 17 + 2 * warp));
+                     L.a + warp * 2 * kCopyBuf, L.worker(2 * warp), L.worker(2 * warp + 1));
       if (COPY == kCopyLdst)
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 8 + warp, p.copy_ctas * 8);
     }
   } else if (warp == 0) {
-    if (lane == 0) run_producer<OP>(p, L);
+    if (lane == 0) run_producer<OP, PAIR>(p, L);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<OP>(p, L, tmem_base);
+    if (lane == 0 && pair_rank<PAIR>() == 0) run_mma<OP, PAIR>(p, L, tmem_base);
   } else if (warp < 4) {
     if (OP == kOpAG && !p.plain && p.copy_ctas == 0) {  // co-located transfer warps
       if (COPY == kCopyTma && warp == 2 && lane == 0)
@@ -1041,15 +1111,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
                       static_cast<int32_t>(gridDim.x) * 2);
     }
   } else {
-    run_epilogue<OP, F32>(p, L, tmem_base, warp, lane);
+    run_epilogue<OP, F32, PAIR>(p, L, tmem_base, warp, lane);
   }
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair leaves while the other may still read its shared memory or TMEM
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1 && !copier) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
   // the next call's prepare kernel (stream-ordered after this grid) may then skip rewriting
   // the tile order and clearing the control arrays

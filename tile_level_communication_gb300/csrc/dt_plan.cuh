@@ -205,11 +205,12 @@ DT_HD int64_t a2a_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
   return static_cast<int64_t>(g.W) * g.Tnw * (static_cast<int64_t>(d) * g.Tm + ug) +
          static_cast<int64_t>(q) * (ue - ug) * g.Tnw + band_offset(ug, ue, i, c, g.Tnw, g.G);
 }
-// tiles of one (destination, source) pair whose rows touch chunk j: its m-tiles x Tnw
-DT_HD int32_t a2a_chunk_tiles(const Geom& g, int32_t j) {
+// stores counted on chunk j of one (destination, source) pair: the bm-row tiles (one CTA's
+// rows) whose rows touch it, times Tnw
+DT_HD int32_t a2a_chunk_tiles(const Geom& g, int32_t j, int32_t bm) {
   const int64_t lo = static_cast<int64_t>(j) * g.Cr;
   const int64_t hi = min64(lo + g.Cr, g.Ms);
-  return static_cast<int32_t>((hi - 1) / g.BM - lo / g.BM + 1) * g.Tnw;
+  return static_cast<int32_t>((hi - 1) / bm - lo / bm + 1) * g.Tnw;
 }
 
 // Execution position of tile id t of an operation with the dt_op numbering (0 AllGather:
