@@ -34,9 +34,17 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 
 # DRAM bytes (read + write) per launch of the fused kernel, from one `ncu --set full` capture
 # of the named workload (profiles/), valid only for the kernel sources it was taken on.
+# DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
+# kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "4352d877c48df460", "bytes": 6.181913e9 + 2.000587e9},
-    "ag_w8_m16384_n8192_k8192": {"csrc": "4352d877c48df460", "bytes": 4.250976e9 + 0.5306816e9},
+    "rs_w8_m8192_n8192_k3584": {"csrc": "23830aa3046508ed", "points": {
+        "1024/8/256": 7.495026e9 + 2.007133e9,     # --set full capture
+        "1024/4/256": 6481171200 + 1999900160,     # dram metrics only
+        "1024/16/256": 6651609088 + 1999531520,    # dram metrics only
+    }},
+    "ag_w8_m8192_n3584_k8192": {"csrc": "23830aa3046508ed", "points": {
+        "256/8/256": 565.70368e6 + 168.374784e6,   # --set full capture, TMA transfer
+    }},
 }
 
 
@@ -56,13 +64,18 @@ L2_BYTES = 129 * 2 ** 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=1000,
+                    help="timed steps; >= 2 s of them is measured against the sustained peak")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
     ap.add_argument("--workload", default="ffn_pair")
     ap.add_argument("--backend", default="auto", choices=["auto", "copy_engine", "tma", "ldst"])
     ap.add_argument("--chunk-rows", type=int, default=0, help="0 = the workload's")
     ap.add_argument("--no-swizzle", action="store_true")
+    ap.add_argument("--group", type=int, default=0, help="m-tiles per band of the in-chunk "
+                    "raster (0 = the library's 8; fixed, not tuned, when given)")
+    ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256],
+                    help="tile rows: 128 (one CTA), 256 (a CTA pair), 0 = the library's choice")
     ap.add_argument("--rank-view", type=int, default=0, help="AllGather rank whose view is computed")
     ap.add_argument("--skip-extras", action="store_true",
                     help="skip the baselines, e2e, CPU oracle and clock sampling")
@@ -436,6 +449,9 @@ def main():
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
 
     # device-resident inputs, outputs, workspaces, argument structs
+    knobs = {"tile_m": args.tile_m}
+    if args.group:
+        knobs["group"] = args.group
     calls = []
     in_bytes = out_bytes = 0
     for wl, inp in zip(ops, inputs):
@@ -450,7 +466,7 @@ def main():
             w1 = up(inp.w1)
             h = torch.empty((wl.m, w * fr), dtype=torch.bfloat16, device=dev)
             a_ag = dt.make_args(w, wl.m, w * fr, wl.k, chunk_rows=cr, act=wl.act,
-                                swizzle=not args.no_swizzle, backend=args.backend)
+                                swizzle=not args.no_swizzle, backend=args.backend, **knobs)
             probe = dt.make_args(w, wl.m, w * fr, wl.k, chunk_rows=64)
             ws_ag = torch.zeros(max(dt.workspace_size(a_ag, dt.OP_AG),
                                     dt.workspace_size(probe, dt.OP_AG)), dtype=torch.uint8, device=dev)
@@ -458,7 +474,7 @@ def main():
                               ws=ws_ag, act=wl.act))
             w2 = [up(t) for t in inp.w2]
             a_rs = dt.make_args(w, wl.m, wl.n, fr, chunk_rows=cr, lda=w * fr,
-                                swizzle=not args.no_swizzle)
+                                swizzle=not args.no_swizzle, **knobs)
             probe = dt.make_args(w, wl.m, wl.n, fr, chunk_rows=64, lda=w * fr)
             ws_rs = torch.zeros(max(dt.workspace_size(a_rs, dt.OP_RS),
                                     dt.workspace_size(probe, dt.OP_RS)), dtype=torch.uint8, device=dev)
@@ -472,7 +488,7 @@ def main():
             continue
         if wl.op == "ag":
             a = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, rank=args.rank_view, chunk_rows=cr,
-                             swizzle=not args.no_swizzle, backend=args.backend)
+                             swizzle=not args.no_swizzle, backend=args.backend, **knobs)
             shards = [up(s) for s in inp.shards]
             b = up(inp.b)
             c = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device=dev)
@@ -483,7 +499,8 @@ def main():
                               outs=[c], ws=ws))
         elif wl.op == "a2a":
             w = wl.world_size
-            a = dt.make_args(w, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=not args.no_swizzle)
+            a = dt.make_args(w, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=not args.no_swizzle,
+                             **knobs)
             A = [up(x) for x in inp.a]
             b = up(inp.b[0])  # the replicated weight, held once
             outs = [torch.empty((wl.m, wl.n // w), dtype=torch.bfloat16, device=dev)
@@ -497,7 +514,7 @@ def main():
                               y=y, ws=ws))
         else:
             a = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=cr,
-                             swizzle=not args.no_swizzle)
+                             swizzle=not args.no_swizzle, **knobs)
             A = [up(x) for x in inp.a]
             B = [up(x) for x in inp.b]
             rows = wl.m // wl.world_size if wl.op == "rs" else wl.m  # AllReduce: every rank all rows
@@ -533,7 +550,7 @@ def main():
 
     # enumerate-and-measure tuning of every call's knobs (not timed)
     tuned = {}
-    if not args.no_tune and args.chunk_rows == 0 and args.backend == "auto":
+    if not args.no_tune and args.chunk_rows == 0 and args.backend == "auto" and not args.group:
         for cl in calls:
             if cl["op"] == "ag":
                 pts = dt.tune_ag_gemm(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], cl["args"])
@@ -613,7 +630,10 @@ def main():
         if op_name in line["config"]:
             line["config"][op_name]["chunk_rows"] = t["chunk_rows"]
     pk = peaks()
-    peak = pk["bf16_tflops_sustained"]
+    # the timed region's own regime: seconds of back-to-back steps settle under the power cap
+    # (the sustained cuBLAS figure); a short region runs at boost clocks (the burst figure)
+    regime = "sustained" if (w1 - w0) >= 2.0 else "burst"
+    peak = pk["bf16_tflops_sustained"] if regime == "sustained" else pk["bf16_tflops"]
     line["frac_of_peak"] = value / world / peak
     line["per_op"] = {cl["op"]: {"ms": ms, "tflops": cl["wl"].flops / (ms * 1e-3) / 1e12,
                                  "frac_of_peak": cl["wl"].flops / (ms * 1e-3) / 1e12 / peak}
@@ -622,13 +642,20 @@ def main():
     dom_achieved = calls[dom]["wl"].flops / (per_call_ms[dom] * 1e-3) / 1e12
     tr = NCU_TRAFFIC.get(calls[dom]["wl"].name)
     used = calls[dom]["args"]  # the knobs actually timed (after tuning)
-    traffic = tr["bytes"] if tr and tr["csrc"] == csrc_hash() and \
-        used.chunk_rows == calls[dom]["wl"].chunk_rows and used.group == 8 else None
+    op_id = {"ag": dt.OP_AG, "rs": dt.OP_RS, "ar": dt.OP_AR, "a2a": dt.OP_A2A}[calls[dom]["op"]]
+    knob_key = f"{used.chunk_rows}/{used.group}/{dt.tile_rows(used, op_id)}"
+    traffic = tr["points"].get(knob_key) if tr and tr["csrc"] == csrc_hash() else None
     line["roofline"] = {
         "bound": "tensor", "kernel": f"fused_gemm_kernel ({calls[dom]['op']})",
         "achieved": dom_achieved, "peak": peak, "unit": "TFLOP/s", "frac": dom_achieved / peak,
+        "regime": regime,
         "traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read + write)",
-        "peak_source": f"{pk['source']} bf16 sustained (cuBLAS, back to back under the power cap)",
+        "knobs": knob_key,
+        "peak_source": (f"{pk['source']} bf16 sustained (cuBLAS back to back for seconds, under the "
+                        f"power cap): the timed region ran {w1 - w0:.2f} s"
+                        if regime == "sustained" else
+                        f"{pk['source']} bf16 burst (cuBLAS best of 10): the timed region ran "
+                        f"{w1 - w0:.2f} s, too short to settle under the power cap"),
         "algorithmic_flops_per_launch": calls[dom]["wl"].flops,
     }
 

@@ -22,7 +22,8 @@ void set_last_error(const char* msg);
 // Launch the fused persistent kernel; defined in dt_ag.cu (AllGather variants), dt_rs.cu
 // (ReduceScatter / AllReduce variants) and dt_a2a.cu (AllToAll variants).  `cooperative`
 // guarantees that every CTA is resident, which the in-kernel chunk transfer relies on.
-// `pair`: 256-row tiles on clusters of two CTAs (grid and copy_ctas even).
+// `pair`: 256-row tiles on clusters of two CTAs (grid and copy_ctas even); the grid is capped
+// at the clusters the GPU holds at once.
 cudaError_t launch_ag_kernel(const KParams& p, int copy_mode, bool f32, int grid,
                              bool cooperative, cudaStream_t stream, bool pair);
 cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream, bool pair);
@@ -45,22 +46,35 @@ cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStrea
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  int n = 0;
-  if (cooperative) {
-    attr[n].id = cudaLaunchAttributeCooperative;
-    attr[n].val.cooperative = 1;
-    ++n;
-  }
+  cudaLaunchAttribute attr[1];
   if (PAIR) {
-    attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = 2;
-    attr[n].val.clusterDim.y = 1;
-    attr[n].val.clusterDim.z = 1;
-    ++n;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a persistent cluster launch is sized to the clusters the GPU holds at once, so every CTA
+    // is resident (what the in-kernel chunk transfer needs; checked here rather than with the
+    // cooperative attribute, which a profiler cannot replay together with clusters); the
+    // tiles are spread over whatever grid runs
+    static int max_clusters = -1;
+    if (max_clusters < 0) {
+      cudaLaunchConfig_t probe = cfg;
+      probe.gridDim = dim3(2);
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &probe);
+      if (e != cudaSuccess) return e;
+      if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    }
+    if (grid > 2 * max_clusters) cfg.gridDim = dim3(2 * max_clusters);
+    if (cooperative && p.copy_ctas >= static_cast<int>(cfg.gridDim.x))
+      return cudaErrorCooperativeLaunchTooLarge;
+  } else if (cooperative) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
-  cfg.attrs = attr;
-  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

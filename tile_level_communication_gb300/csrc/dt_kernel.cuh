@@ -262,10 +262,7 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
   constexpr int NB = b_slabs(PAIR);
   // a pair's loads complete on the even CTA's barriers; it expects both CTAs' bytes
   const bool leader = pair_rank<PAIR>() == 0;
-  uint32_t kit = 0;
-  int64_t last_issue[NS];
-#pragma unroll
-  for (int s = 0; s < NS; ++s) last_issue[s] = -1;
+  uint32_t kit = 0;  // k-blocks issued so far (the last one, if any, is kit - 1)
   for (int32_t pos = first_pos<PAIR>(p); pos < p.T; pos += pos_stride<PAIR>(p)) {
     const TileInfo ti = decode_tile<OP, PAIR>(p, pos);
     if (!ti.valid) {
@@ -323,16 +320,17 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
         for (int jj = 0; jj < NB; ++jj)
           tma_load_2d(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, L.full(st));
       }
-      last_issue[st] = kit;
     }
     if (!ok) break;
   }
   if (*L.abort_flag && leader) {
     // let every TMA load issued into this stage ring land before the CTA can exit (a pair's
     // leader barrier counts the other CTA's bytes as well)
+    // the last k-block issued into stage s is the largest k < kit with k % NS == s
     for (int s = 0; s < NS; ++s) {
-      if (last_issue[s] < 0) continue;
-      const uint32_t ph = static_cast<uint32_t>(last_issue[s] / NS) & 1u;
+      if (kit <= static_cast<uint32_t>(s)) continue;
+      const uint32_t last = (kit - 1u) - ((kit - 1u - static_cast<uint32_t>(s)) % NS);
+      const uint32_t ph = (last / NS) & 1u;
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(L.full(s), ph) && globaltimer_ns() - t0 < p.timeout_ns) {
       }
