@@ -710,20 +710,29 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
                      : static_cast<int32_t>((static_cast<int64_t>(t_s) * (p.g.W - 1) + t_d - 1) *
                                                 p.g.Ms + t_lr0);
       const int r = qd * 32 + lane;  // this thread's row of the tile
-      // the unit's word was acquired through the generic proxy; the loads below are TMA
-      if (et == 0 && load) fence_proxy_async_global();
+      const int ncb = static_cast<int>(min64(kBN, p.g.N - ti.col0) + 31) / 32;  // 32-column boxes
+      // Box cb+1's running sum is loaded into the other buffer while box cb is processed.  The
+      // buffers are free at the start of a tile (its predecessor waited for all its stores).
+      if (et == 0 && load) {
+        // the unit's word was acquired through the generic proxy; the loads below are TMA
+        fence_proxy_async_global();
+        const int b0 = static_cast<int>(stage_ctr & 1u);
+        mbar_expect_tx(L.copyb(b0), kCopyBuf);
+        tma_load_2d(smem_u32(L.copy + b0 * kCopyBuf), &p.tmAcc, static_cast<int32_t>(ti.col0),
+                    static_cast<int32_t>(ti.row0), L.copyb(b0));
+      }
 #pragma unroll 1
-      for (int cb = 0; cb < kBN / 32; ++cb) {
+      for (int cb = 0; cb < ncb; ++cb) {
         const int64_t c0 = ti.col0 + cb * 32;
-        if (c0 >= p.g.N) break;
         const int b = static_cast<int>(stage_ctr & 1u);
         uint8_t* buf = L.copy + b * kCopyBuf;
         if (et == 0) {
-          bulk_wait_read<1>();  // the store that last used this buffer has read it
-          if (load) {
-            mbar_expect_tx(L.copyb(b), kCopyBuf);
-            tma_load_2d(smem_u32(buf), &p.tmAcc, static_cast<int32_t>(c0),
-                        static_cast<int32_t>(ti.row0), L.copyb(b));
+          bulk_wait_read<0>();  // box cb-1's store has read the other buffer
+          if (load && cb + 1 < ncb) {
+            mbar_expect_tx(L.copyb(b ^ 1), kCopyBuf);
+            tma_load_2d(smem_u32(L.copy + (b ^ 1) * kCopyBuf), &p.tmAcc,
+                        static_cast<int32_t>(c0 + 32), static_cast<int32_t>(ti.row0),
+                        L.copyb(b ^ 1));
           }
         }
         named_bar_sync(1, 128);
@@ -870,19 +879,6 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
         g = hi;
       }
       named_bar_sync(1, 128);
-      // warm L2 with the running sums the next tile of this CTA will fold into
-      const int32_t npos = pos + pos_stride<PAIR>(p);
-      if (npos < p.T) {
-        const TileInfo nt = decode_tile<OP, PAIR>(p, npos);
-        const int64_t nrow = nt.row0 + qd * 32 + lane;
-        if (nt.valid && nrow < nt.row_end) {
-          int32_t s, j;
-          row_chunk(p.g, nrow, s, j);
-          if (fold_index(s, nt.q, p.g.W) > 0)
-            prefetch_l2(acc_ptr(p, nrow, nt.col0),
-                        static_cast<uint32_t>(min64(kBN, p.g.N - nt.col0) * 4));
-        }
-      }
     }
   }
 }
