@@ -99,8 +99,9 @@ PLAN_GRID = [
 ]
 
 
-# the order's tile rows: one CTA (128) or a CTA pair (256); the oracle takes them as BM
-TILE_M = [128, 256]
+# the order's tile rows: one CTA (128), a CTA pair (256) or two pairs (512); the oracle takes
+# them as BM
+TILE_M = [128, 256, 512]
 
 
 @pytest.mark.parametrize("case", PLAN_GRID)
@@ -193,7 +194,7 @@ def test_host_plan_a2a_random_sweep(dt):
         nw = 8 * int(rng.integers(1, 90))
         cr = int(rng.integers(1, 2 * ms + 2))
         g = int(rng.integers(1, 10))
-        bm = 128 * int(rng.integers(1, 3))
+        bm = 128 * int(rng.choice([1, 2, 4]))
         a = dt.make_args(w, w * ms, w * nw, 8, chunk_rows=cr, group=g, tile_m=bm)
         assert dt.swizzle_plan(a, dt.OP_A2A).tolist() == \
             oplan.a2a_order(w, ms, w * nw, cr, bm, 256, True, g)

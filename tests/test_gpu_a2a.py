@@ -67,7 +67,7 @@ def small():
 
 
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("tile_m", [128, 256, 512])
 def test_small_parity_and_padding_untouched(dt, small, out_dtype, tile_m):
     wl, inp, ref = small
     nw = wl.n // wl.world_size
@@ -87,7 +87,8 @@ def test_small_bit_identical_across_orders_chunks_groups_and_baseline(dt, small)
                 dict(chunk_rows=300), dict(chunk_rows=1000), dict(group=1),
                 dict(group=3, chunk_rows=128), dict(num_sms=7), dict(tile_m=256),
                 dict(tile_m=256, chunk_rows=1), dict(tile_m=256, swizzle=False),
-                dict(tile_m=256, num_sms=7)]
+                dict(tile_m=256, num_sms=7), dict(tile_m=512), dict(tile_m=512, chunk_rows=1),
+                dict(tile_m=512, num_sms=9)]
     for kw in variants:
         kw.setdefault("chunk_rows", wl.chunk_rows)
         outs, _, _ = _run(dt, inp, wl.m, wl.n, wl.k, dev=dev, **kw)
@@ -97,7 +98,7 @@ def test_small_bit_identical_across_orders_chunks_groups_and_baseline(dt, small)
 
 
 @pytest.mark.parametrize("chunk_rows", [96, 1, 300])
-@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("tile_m", [128, 256, 512])
 def test_signals_after_each_call(dt, small, chunk_rows, tile_m):
     wl, inp, _ = small
     dev = _upload(inp)

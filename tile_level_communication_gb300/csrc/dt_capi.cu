@@ -99,8 +99,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Derived {
   int op;
   int32_t W, rank, G, Tm, Tn, KB, T, nC, pieces_max;
-  int32_t bm;    // rows of a tile in the order: 128 (one CTA) or 256 (a CTA pair)
-  bool pair;
+  int32_t bm;    // rows of a tile in the order: 128 (one CTA), 256 (a CTA pair), 512 (two pairs)
+  int32_t cl;    // CTAs per cluster: bm / 128
   int32_t Tm128; // 128-row m-tiles (one CTA's rows): the ReduceScatter's unit granularity
   int64_t M, N, K, Ms, Cr, lda, ldb, ldc, ld_gather;
   bool swizzle, f32;
@@ -162,10 +162,10 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     return fail(DT_ERR_INVALID, "leading dimension smaller than the row length");
   if ((d->lda % 8) || (d->ldb % 8) || (d->ldc % 8))
     return fail(DT_ERR_INVALID, "leading dimensions must be multiples of 8 elements (16-byte rows)");
-  if ((a->tile_m != 0 && a->tile_m != kBM && a->tile_m != 2 * kBM) ||
+  if ((a->tile_m != 0 && a->tile_m != kBM && a->tile_m != 2 * kBM && a->tile_m != 4 * kBM) ||
       (a->tile_n != 0 && a->tile_n != kBN))
-    return fail(DT_ERR_UNSUPPORTED, "tiles other than %dx%d and %dx%d are not built", kBM, kBN,
-                2 * kBM, kBN);
+    return fail(DT_ERR_UNSUPPORTED, "tiles other than %d, %d or %d x %d are not built", kBM,
+                2 * kBM, 4 * kBM, kBN);
   if (a->out_dtype != DT_BF16 && a->out_dtype != DT_F32)
     return fail(DT_ERR_INVALID, "unknown out_dtype %d", a->out_dtype);
   d->f32 = a->out_dtype == DT_F32;
@@ -186,7 +186,7 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     const bool odd_copiers = op == DT_OP_AG_GEMM && (a->copy_ctas % 2) != 0;
     d->bm = t256 >= 76 && !odd_copiers ? 2 * kBM : kBM;
   }
-  d->pair = d->bm == 2 * kBM;
+  d->cl = d->bm / kBM;
   d->Tm128 = static_cast<int32_t>(cdiv64(rows_tiled, kBM));
   d->geom = a2a ? make_geom_a2a(d->W, d->M, d->N, d->Cr, d->bm, kBN, d->G, d->swizzle ? 1 : 0)
               : make_geom(d->W, d->rank, d->M, d->N, d->Cr, d->bm, kBN, d->G, d->swizzle ? 1 : 0);
@@ -220,8 +220,9 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     return fail(DT_ERR_INVALID, "copy_ctas %d outside 0..64", d->copy_ctas);
   if (d->copy_ctas > 0 && be == DT_XFER_COPY_ENGINE)
     return fail(DT_ERR_INVALID, "dedicated transfer CTAs need DT_XFER_TMA or DT_XFER_LDST");
-  if (d->pair && d->copy_ctas % 2)
-    return fail(DT_ERR_INVALID, "CTA-pair tiles need an even copy_ctas");
+  if (d->copy_ctas % d->cl)
+    return fail(DT_ERR_INVALID, "copy_ctas must be a multiple of the %d CTAs of a %d-row tile",
+                d->cl, d->bm);
   // workspace layout: error word | control arrays | tile order || data
   const size_t nchunks = static_cast<size_t>(d->W) * d->nC;
   size_t off = 256;
@@ -447,8 +448,7 @@ dt_status check_ws(const Derived& d, void* ws, size_t bytes) {
 // Persistent grid over `tiles` tiles of the order with `sms` SMs to use: one CTA per SM, or
 // one cluster of two per pair of SMs.
 int grid_for(const Derived& d, int64_t tiles, int sms) {
-  if (d.pair) return 2 * static_cast<int>(std::min<int64_t>(tiles, std::max(sms / 2, 1)));
-  return static_cast<int>(std::min<int64_t>(tiles, sms));
+  return d.cl * static_cast<int>(std::min<int64_t>(tiles, std::max(sms / d.cl, 1)));
 }
 
 void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
@@ -578,7 +578,7 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
   if (d.copy_ctas >= use) return fail(DT_ERR_INVALID, "copy_ctas must leave SMs for the GEMM");
   p.copy_ctas = d.copy_ctas;
   const int grid = d.copy_ctas + grid_for(d, d.T, use - d.copy_ctas);
-  const cudaError_t e = launch_ag_kernel(p, copy, d.f32, grid, true, stream, d.pair);
+  const cudaError_t e = launch_ag_kernel(p, copy, d.f32, grid, true, stream, d.cl);
   if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
   return DT_OK;
 }
@@ -738,7 +738,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
     // one rank gathers nothing: the GEMM reads its shard where it is
     if ((s = make_tmap(&p.tmA[0], a_shards[0], d.K, d.M, d.lda * 2, 64, kBM)) != DT_OK) return s;
     p.wait_flags = 0;
-    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.pair);
+    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.cl);
     if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
     return DT_OK;
   }
@@ -756,7 +756,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
       // start the GEMM once the chunks its first tiles need are queued (at once when the own
       // rank's tiles read in place)
       if ((tc == d.nC || p.own_in_place) && !launched) {
-        cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.pair);
+        cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.cl);
         if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
         launched = true;
       }
@@ -771,7 +771,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
       if (r != CUDA_SUCCESS) return fail(DT_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)r);
     }
     if (!launched) {
-      cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.pair);
+      cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.cl);
       if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
     }
     DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
@@ -783,7 +783,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
   if (d.copy_ctas >= sms) return fail(DT_ERR_INVALID, "copy_ctas must leave SMs for the GEMM");
   const int grid_ded = d.copy_ctas + grid_for(d, d.T, sms - d.copy_ctas);
   cudaError_t e =
-      launch_ag_kernel(p, copy, d.f32, d.copy_ctas ? grid_ded : grid, true, stream, d.pair);
+      launch_ag_kernel(p, copy, d.f32, d.copy_ctas ? grid_ded : grid, true, stream, d.cl);
   if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
   return DT_OK;
 }
@@ -830,7 +830,7 @@ dt_status dt_ag_gemm_kernel_overlap(const void* const* a_shards, const void* b, 
     p.row_hi = hi;
     p.Tm = static_cast<int32_t>(cdiv64(hi - lo, d.bm));
     p.T = p.Tm * d.Tn;
-    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid_for(d, p.T, sms), false, stream, d.pair);
+    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid_for(d, p.T, sms), false, stream, d.cl);
     if (e != cudaSuccess) return cuda_fail(e, "per-chunk GEMM launch");
   }
   DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
@@ -916,7 +916,7 @@ static dt_status reduce_fused(const void* const* a_, const void* const* b_, void
   KParams p;
   if ((s = rs_params(p, d, a_, b_, out, ws, epoch)) != DT_OK) return s;
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
-  cudaError_t e = launch_rs_kernel(p, d.f32, grid_for(d, d.T, sms), stream, d.pair);
+  cudaError_t e = launch_rs_kernel(p, d.f32, grid_for(d, d.T, sms), stream, d.cl);
   if (e != cudaSuccess) return cuda_fail(e, "fused GEMM-ReduceScatter / AllReduce launch");
   return DT_OK;
 }
@@ -951,7 +951,7 @@ static dt_status reduce_kernel_overlap(const void* const* a_, const void* const*
     p.row_hi = p.row_lo + d.Ms;
     p.Tm = static_cast<int32_t>(cdiv64(d.Ms, d.bm));
     p.T = d.W * p.Tm * d.Tn;
-    cudaError_t e = launch_rs_kernel(p, d.f32, grid_for(d, p.T, sms), stream, d.pair);
+    cudaError_t e = launch_rs_kernel(p, d.f32, grid_for(d, p.T, sms), stream, d.cl);
     if (e != cudaSuccess) return cuda_fail(e, "per-destination GEMM launch");
     DT_CUDA(cudaEventRecord(dev->chunk_events[st], stream));
     DT_CUDA(cudaStreamWaitEvent(dev->side, dev->chunk_events[st], 0));
@@ -1056,7 +1056,7 @@ dt_status dt_gemm_a2a(const void* const* a_, const void* const* b_, void* const*
   if ((s = a2a_params(p, d, a_, b_, ws, epoch)) != DT_OK) return s;
   for (int h = 0; h < d.W; ++h) p.out[h] = out[h];
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
-  cudaError_t e = launch_a2a_kernel(p, d.f32, grid_for(d, d.T, sms), stream, d.pair);
+  cudaError_t e = launch_a2a_kernel(p, d.f32, grid_for(d, d.T, sms), stream, d.cl);
   if (e != cudaSuccess) return cuda_fail(e, "fused GEMM-AllToAll launch");
   return DT_OK;
 }
@@ -1093,7 +1093,7 @@ dt_status dt_gemm_a2a_kernel_overlap(const void* const* a_, const void* const* b
   for (int32_t st = 0; st < d.W; ++st) {
     // step st: every rank q computes the block of destination (q + st + 1) mod W
     p.a2a_step = st;
-    cudaError_t e = launch_a2a_kernel(p, d.f32, grid_for(d, p.T, sms), stream, d.pair);
+    cudaError_t e = launch_a2a_kernel(p, d.f32, grid_for(d, p.T, sms), stream, d.cl);
     if (e != cudaSuccess) return cuda_fail(e, "per-step GEMM launch");
     DT_CUDA(cudaEventRecord(dev->chunk_events[st], stream));
     DT_CUDA(cudaStreamWaitEvent(dev->side, dev->chunk_events[st], 0));

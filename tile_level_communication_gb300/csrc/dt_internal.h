@@ -22,19 +22,19 @@ void set_last_error(const char* msg);
 // Launch the fused persistent kernel; defined in dt_ag.cu (AllGather variants), dt_rs.cu
 // (ReduceScatter / AllReduce variants) and dt_a2a.cu (AllToAll variants).  `cooperative`
 // guarantees that every CTA is resident, which the in-kernel chunk transfer relies on.
-// `pair`: 256-row tiles on clusters of two CTAs (grid and copy_ctas even); the grid is capped
-// at the clusters the GPU holds at once.
+// `cl`: CTAs per cluster, 1, 2 (a CTA pair per 256-row tile) or 4 (two pairs per 512-row tile
+// sharing B); grid and copy_ctas are multiples of it and the grid is capped at the clusters the
+// GPU holds at once.
 cudaError_t launch_ag_kernel(const KParams& p, int copy_mode, bool f32, int grid,
-                             bool cooperative, cudaStream_t stream, bool pair);
-cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream, bool pair);
-cudaError_t launch_a2a_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream,
-                              bool pair);
+                             bool cooperative, cudaStream_t stream, int cl);
+cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream, int cl);
+cudaError_t launch_a2a_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream, int cl);
 
 // One launch of an instance of the fused kernel (dynamic shared memory raised once).
-template <int OP, int COPY, bool F32, bool PAIR>
+template <int OP, int COPY, bool F32, int CL>
 cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStream_t stream) {
-  auto kern = fused_gemm_kernel<OP, COPY, F32, PAIR>;
-  const int smem = kernel_smem_bytes(OP == kOpRS, COPY, PAIR);
+  auto kern = fused_gemm_kernel<OP, COPY, F32, CL>;
+  const int smem = kernel_smem_bytes(OP == kOpRS, COPY, CL);
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -47,9 +47,9 @@ cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStrea
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  if (PAIR) {
+  if (CL > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -61,12 +61,12 @@ cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStrea
     static int max_clusters = -1;
     if (max_clusters < 0) {
       cudaLaunchConfig_t probe = cfg;
-      probe.gridDim = dim3(2);
+      probe.gridDim = dim3(CL);
       cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &probe);
       if (e != cudaSuccess) return e;
       if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     }
-    if (grid > 2 * max_clusters) cfg.gridDim = dim3(2 * max_clusters);
+    if (grid > CL * max_clusters) cfg.gridDim = dim3(CL * max_clusters);
     if (cooperative && p.copy_ctas >= static_cast<int>(cfg.gridDim.x))
       return cudaErrorCooperativeLaunchTooLarge;
   } else if (cooperative) {

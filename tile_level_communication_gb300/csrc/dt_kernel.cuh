@@ -35,11 +35,14 @@ constexpr int kThreads = 256;
 constexpr int kAStage = kBM * kBK * 2;   // 16 KB: 128 rows x 64 bf16, 128-byte swizzle
 constexpr int kBSlab = kBK * 64 * 2;     // 8 KB: 64 k-rows x 64 bf16 columns
 // Operand ring per CTA: one CTA per tile stages all 256 columns of B (4 slabs, 32 KB) in 4
-// stages; a CTA pair splits them (2 slabs, 16 KB each) and affords 6 stages.
-__host__ __device__ constexpr int stages(bool pair) { return pair ? 6 : 4; }
+// stages; a CTA pair splits them (2 slabs, 16 KB each) and affords 6 stages next to the 32 KB
+// staging buffers, 7 without them.
+__host__ __device__ constexpr int stages(bool pair, bool staging) {
+  return pair ? (staging ? 6 : 7) : 4;
+}
 __host__ __device__ constexpr int b_slabs(bool pair) { return pair ? 2 : 4; }
 __host__ __device__ constexpr int b_stage_bytes(bool pair) { return b_slabs(pair) * kBSlab; }
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 7;
 constexpr int kCopyBuf = 16384;          // TMA bulk copy staging, two buffers
 constexpr int kTmemCols = 512;           // two 128x256 fp32 accumulators
 constexpr int kMaxW = 16;
@@ -64,8 +67,10 @@ enum DevCode : uint32_t {
 __host__ __device__ constexpr bool has_staging(bool rs, int copy_mode) {
   return rs || copy_mode == kCopyTma;
 }
-__host__ __device__ constexpr int kernel_smem_bytes(bool rs, int copy_mode, bool pair) {
-  return 1024 + stages(pair) * (kAStage + b_stage_bytes(pair)) +
+// cl: CTAs per cluster (1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile; 4: two
+// pairs per 512-row tile sharing B)
+__host__ __device__ constexpr int kernel_smem_bytes(bool rs, int copy_mode, int cl) {
+  return 1024 + stages(cl > 1, has_staging(rs, copy_mode)) * (kAStage + b_stage_bytes(cl > 1)) +
          (has_staging(rs, copy_mode) ? 2 * kCopyBuf : 0) + kMiscBytes;
 }
 
@@ -129,7 +134,7 @@ struct SmemLayout {
   volatile int8_t* chain;        // RS: per piece, first parked partial this tile folds (-1)
   uint32_t* ready_bits;
   int ns;  // pipeline stages
-  // barrier slots: full[ns], empty[ns], tfull[2], tempty[2], copyb[2], fin (at most 19);
+  // barrier slots: full[ns], empty[ns], tfull[2], tempty[2], copyb[2], fin (at most 21);
   // slots 24..31 belong to the dedicated transfer CTAs' workers
   __device__ uint32_t full(int s) const { return smem_u32(bars + s); }
   __device__ uint32_t empty(int s) const { return smem_u32(bars + ns + s); }
@@ -202,14 +207,15 @@ struct TileInfo {
   bool valid;
 };
 
-// CTA pairs: the two CTAs of a cluster work on the same tile of the order, each on its own
-// 128 of the tile's 256 rows (cluster rank 0: the upper half).
-template <bool PAIR>
-__device__ __forceinline__ uint32_t pair_rank() {
-  return PAIR ? (blockIdx.x & 1u) : 0u;
+// Clusters: the CL CTAs of a cluster work on the same tile of the order, each on its own 128 of
+// the tile's CL * 128 rows, in cluster-rank order.  CTAs 2k and 2k+1 form a pair (tcgen05
+// cta_group::2) whose even CTA issues the MMAs; with CL = 4 the two pairs share B.
+template <int CL>
+__device__ __forceinline__ uint32_t cl_rank() {
+  return CL > 1 ? (blockIdx.x % static_cast<uint32_t>(CL)) : 0u;
 }
 
-template <int OP, bool PAIR>
+template <int OP, int CL>
 __device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
   int32_t t = p.plain ? pos : __ldg(p.order + pos);
   TileInfo ti;
@@ -222,7 +228,7 @@ __device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
   const int32_t rem = t - ti.q * per_q;
   const int32_t it = rem / tn;
   ti.n = rem - it * tn;
-  ti.i = PAIR ? 2 * it + static_cast<int32_t>(pair_rank<PAIR>()) : it;
+  ti.i = CL * it + static_cast<int32_t>(cl_rank<CL>());
   ti.row0 = p.row_lo + static_cast<int64_t>(ti.i) * kBM;
   ti.row_end = min64(ti.row0 + kBM, p.row_hi);
   if (OP == kOpA2A) {
@@ -246,25 +252,31 @@ __device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
 
 // Compute CTAs are blockIdx.x >= copy_ctas; they (or their pairs) take the tile order round
 // robin.
-template <bool PAIR>
+template <int CL>
 __device__ __forceinline__ int32_t first_pos(const KParams& p) {
-  return (static_cast<int32_t>(blockIdx.x) - p.copy_ctas) / (PAIR ? 2 : 1);
+  return (static_cast<int32_t>(blockIdx.x) - p.copy_ctas) / CL;
 }
-template <bool PAIR>
+template <int CL>
 __device__ __forceinline__ int32_t pos_stride(const KParams& p) {
-  return (static_cast<int32_t>(gridDim.x) - p.copy_ctas) / (PAIR ? 2 : 1);
+  return (static_cast<int32_t>(gridDim.x) - p.copy_ctas) / CL;
 }
 
 // ============================================================================ producer
-template <int OP, bool PAIR>
+template <int OP, int CL, int NS>
 __device__ void run_producer(const KParams& p, const SmemLayout& L) {
-  constexpr int NS = stages(PAIR);
+  constexpr bool PAIR = CL > 1;
   constexpr int NB = b_slabs(PAIR);
-  // a pair's loads complete on the even CTA's barriers; it expects both CTAs' bytes
-  const bool leader = pair_rank<PAIR>() == 0;
+  // a pair's loads complete on its even CTA's barriers; that CTA expects both CTAs' bytes
+  const uint32_t rank = cl_rank<CL>();
+  const bool leader = (rank & 1u) == 0u;
+  // stage s: barriers 8 s bytes after stage 0's, buffers s stages after stage 0's
+  const uint32_t full0 = L.full(0), empty0 = L.empty(0);
+  const uint32_t a_smem0 = smem_u32(L.a), b_smem0 = smem_u32(L.b);
+  uint32_t full0_lead = full0;  // stage 0's full barrier in the pair leader (cluster address)
+  if constexpr (PAIR) full0_lead = mapa_shared(full0, rank & ~1u);
   uint32_t kit = 0;  // k-blocks issued so far (the last one, if any, is kit - 1)
-  for (int32_t pos = first_pos<PAIR>(p); pos < p.T; pos += pos_stride<PAIR>(p)) {
-    const TileInfo ti = decode_tile<OP, PAIR>(p, pos);
+  for (int32_t pos = first_pos<CL>(p); pos < p.T; pos += pos_stride<CL>(p)) {
+    const TileInfo ti = decode_tile<OP, CL>(p, pos);
     if (!ti.valid) {
       raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
       continue;
@@ -297,28 +309,38 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
     const CUtensorMap* tB = &p.tmB[OP != kOpAG ? ti.q : 0];
     const int32_t a_row = static_cast<int32_t>(own_tile ? ti.row0 - own0 : ti.row0);
     // this CTA's columns of B: all 256, or its half of the pair's
-    const int32_t b_col = static_cast<int32_t>(ti.col0) +
-                          static_cast<int32_t>(pair_rank<PAIR>()) * (NB * 64);
+    const int32_t b_col = static_cast<int32_t>(ti.col0) + static_cast<int32_t>(rank & 1u) * (NB * 64);
     bool ok = true;
     for (int32_t kb = 0; kb < p.KB; ++kb, ++kit) {
       const int st = static_cast<int>(kit % NS);
       const uint32_t ph = (kit / NS) & 1u;
-      if (!wait_bar(p, L, L.empty(st), ph ^ 1u, 100 + st)) { ok = false; break; }
-      const uint32_t a_dst = smem_u32(L.a + st * kAStage);
-      const uint32_t b_dst = smem_u32(L.b + st * b_stage_bytes(PAIR));
-      if constexpr (PAIR) {
-        const uint32_t bar = mapa_shared(L.full(st), 0);
-        if (leader) mbar_expect_tx(L.full(st), 2 * (kAStage + b_stage_bytes(PAIR)));
+      const uint32_t sst = static_cast<uint32_t>(st);
+      if (!wait_bar(p, L, empty0 + 8u * sst, ph ^ 1u, 100 + st)) { ok = false; break; }
+      const uint32_t a_dst = a_smem0 + sst * kAStage;
+      const uint32_t b_dst = b_smem0 + sst * b_stage_bytes(PAIR);
+      const uint32_t fb = full0 + 8u * sst;
+      if constexpr (CL == 4) {
+        // both pairs use the same columns: this CTA loads slab (rank >> 1) of its half of B
+        // for itself and for its counterpart in the other pair
+        const uint32_t bar = full0_lead + 8u * sst;
+        if (leader) mbar_expect_tx(fb, 2 * (kAStage + b_stage_bytes(PAIR)));
+        tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
+        const uint32_t sl = rank >> 1;
+        tma_load_2d_pair_mc(b_dst + sl * kBSlab, tB, b_col + static_cast<int32_t>(sl) * 64,
+                            kb * kBK, bar, static_cast<uint16_t>(0x5u << (rank & 1u)));
+      } else if constexpr (PAIR) {
+        const uint32_t bar = full0_lead + 8u * sst;
+        if (leader) mbar_expect_tx(fb, 2 * (kAStage + b_stage_bytes(PAIR)));
         tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
 #pragma unroll
         for (int jj = 0; jj < NB; ++jj)
           tma_load_2d_pair(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, bar);
       } else {
-        mbar_expect_tx(L.full(st), kAStage + b_stage_bytes(PAIR));
-        tma_load_2d(a_dst, tA, kb * kBK, a_row, L.full(st));
+        mbar_expect_tx(fb, kAStage + b_stage_bytes(PAIR));
+        tma_load_2d(a_dst, tA, kb * kBK, a_row, fb);
 #pragma unroll
         for (int jj = 0; jj < NB; ++jj)
-          tma_load_2d(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, L.full(st));
+          tma_load_2d(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, fb);
       }
     }
     if (!ok) break;
@@ -339,16 +361,27 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
 }
 
 // ============================================================================ MMA issuer
-template <int OP, bool PAIR>
+template <int OP, int CL, int NS>
 __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_base) {
-  constexpr int NS = stages(PAIR);
+  constexpr bool PAIR = CL > 1;
+  // commit masks: a stage is refilled by both pairs of a 4-CTA cluster (B is shared), an
+  // accumulator belongs to this pair
+  const uint32_t rank = cl_rank<CL>();
+  const uint16_t stage_mask = CL == 4 ? 0xF : 0x3;
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & ~1u));
   // a pair's MMA has M = 256: rows 0-127 from the even CTA, 128-255 from the odd one
   constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, kBN, /*B MN-major*/ 1);
   uint32_t kit = 0;
   int32_t tl = 0;
   bool issued = false;
-  for (int32_t pos = first_pos<PAIR>(p); pos < p.T; pos += pos_stride<PAIR>(p)) {
-    const TileInfo ti = decode_tile<OP, PAIR>(p, pos);
+  // what the k-loop touches, in registers: stage s's barriers are 8 s bytes after stage 0's,
+  // its descriptors (s * stage bytes) >> 4 after stage 0's (the start-address field, which
+  // cannot carry: shared addresses stay below 256 KB)
+  const uint32_t full0 = L.full(0), empty0 = L.empty(0);
+  const uint64_t adesc0 = smem_desc_sw128(smem_u32(L.a), 16, 1024);
+  const uint64_t bdesc0 = smem_desc_sw128(smem_u32(L.b), kBSlab, 1024);
+  for (int32_t pos = first_pos<CL>(p); pos < p.T; pos += pos_stride<CL>(p)) {
+    const TileInfo ti = decode_tile<OP, CL>(p, pos);
     if (!ti.valid) continue;
     const int acc = tl & 1;
     const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
@@ -362,31 +395,37 @@ __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_bas
       // the stage was filled by TMA (async proxy) and is read by the MMAs (async proxy): the
       // barrier's completion orders them; no tcgen05 fence here, which would hold the issue
       // of this k-block until the MMAs in flight have finished
-      if (!wait_bar(p, L, L.full(st), ph, 300 + st)) { ok = false; break; }
-      const uint32_t a0 = smem_u32(L.a + st * kAStage);
-      const uint32_t b0 = smem_u32(L.b + st * b_stage_bytes(PAIR));
+      const uint32_t fb = full0 + 8u * static_cast<uint32_t>(st);
+      if (!wait_bar(p, L, fb, ph, 300 + st)) { ok = false; break; }
+      const uint64_t ad0 =
+          adesc0 + static_cast<uint64_t>((static_cast<uint32_t>(st) * kAStage) >> 4);
+      const uint64_t bd0 =
+          bdesc0 + static_cast<uint64_t>((static_cast<uint32_t>(st) * b_stage_bytes(PAIR)) >> 4);
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
-        // A: K-major rows of 128 B, 8-row groups 1024 B apart; +32 B per 16 k
-        const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-        // B: MN-major; 64-column slabs 8 KB apart (LBO), 8 k-row groups 1 KB apart (SBO)
-        const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kBSlab, 1024);
+        // A: K-major rows of 128 B, 8-row groups 1024 B apart (SBO); +32 B per 16 k
+        const uint64_t ad = ad0 + static_cast<uint64_t>(kk * (32 >> 4));
+        // B: MN-major; 64-column slabs 8 KB apart (LBO), 8 k-row groups 1 KB apart (SBO);
+        // +2 KB per 16 k
+        const uint64_t bd = bd0 + static_cast<uint64_t>(kk * (2048 >> 4));
         if constexpr (PAIR)
           umma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
         else
           umma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
       }
       // frees the stage (in both CTAs of a pair) once these MMAs have read it
-      if constexpr (PAIR) umma_commit_pair(L.empty(st), 3); else umma_commit(L.empty(st));
+      const uint32_t eb = empty0 + 8u * static_cast<uint32_t>(st);
+      if constexpr (PAIR) umma_commit_pair(eb, stage_mask); else umma_commit(eb);
       issued = true;
     }
     if (!ok) break;
     // accumulator ready for the epilogue (of both CTAs)
-    if constexpr (PAIR) umma_commit_pair(L.tfull(acc), 3); else umma_commit(L.tfull(acc));
+    if constexpr (PAIR) umma_commit_pair(L.tfull(acc), pair_mask); else umma_commit(L.tfull(acc));
     ++tl;
   }
   if (*L.abort_flag && issued) {
-    if constexpr (PAIR) umma_commit_pair(L.fin(), 1); else umma_commit(L.fin());
+    if constexpr (PAIR) umma_commit_pair(L.fin(), static_cast<uint16_t>(1u << rank));
+    else umma_commit(L.fin());
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(L.fin(), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
     }
@@ -603,9 +642,10 @@ __device__ void fold_chain(const KParams& p, const SmemLayout& L, int32_t s, int
   }
 }
 
-template <int OP, bool F32, bool PAIR>
+template <int OP, bool F32, int CL>
 __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tmem_base,
                              int warp, int lane) {
+  constexpr bool PAIR = CL > 1;
   constexpr bool RS = OP == kOpRS;
   constexpr bool A2A = OP == kOpA2A;
   constexpr bool kStoreF32 = RS || F32;  // ReduceScatter partials are fp32
@@ -619,11 +659,12 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
   // a pair's accumulator is released on the even CTA's barrier, by the warps of both CTAs
   uint32_t tempty_bar0 = L.tempty(0), tempty_bar1 = L.tempty(1);
   if constexpr (PAIR) {
-    tempty_bar0 = mapa_shared(tempty_bar0, 0);
-    tempty_bar1 = mapa_shared(tempty_bar1, 0);
+    const uint32_t lead = cl_rank<CL>() & ~1u;
+    tempty_bar0 = mapa_shared(tempty_bar0, lead);
+    tempty_bar1 = mapa_shared(tempty_bar1, lead);
   }
-  for (int32_t pos = first_pos<PAIR>(p); pos < p.T; pos += pos_stride<PAIR>(p)) {
-    const TileInfo ti = decode_tile<OP, PAIR>(p, pos);
+  for (int32_t pos = first_pos<CL>(p); pos < p.T; pos += pos_stride<CL>(p)) {
+    const TileInfo ti = decode_tile<OP, CL>(p, pos);
     if (!ti.valid) continue;
     const int acc = tl & 1;
     const uint32_t ph = (static_cast<uint32_t>(tl) >> 1) & 1u;
@@ -1025,11 +1066,13 @@ static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int 
 }
 
 // ============================================================================ kernel
-// PAIR: launched in clusters of two CTAs that share each 256-row tile (tcgen05 cta_group::2);
-// copy_ctas is then even, so dedicated transfer CTAs form whole clusters.
-template <int OP, int COPY, bool F32, bool PAIR>
+// CL > 1: launched in clusters of CL CTAs that share each CL * 128-row tile (tcgen05
+// cta_group::2 pairs); copy_ctas is then a multiple of CL, so dedicated transfer CTAs form
+// whole clusters.
+template <int OP, int COPY, bool F32, int CL>
 __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_constant__ KParams p) {
-  constexpr int NS = stages(PAIR);
+  constexpr bool PAIR = CL > 1;
+  constexpr int NS = stages(PAIR, has_staging(OP == kOpRS, COPY));
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1054,7 +1097,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(L.full(s), 1);
-      mbar_init(L.empty(s), 1);
+      mbar_init(L.empty(s), CL == 4 ? 2 : 1);  // both pairs' MMAs release a shared-B stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(L.tfull(a), 1);
@@ -1078,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (PAIR) cluster_sync();  // the pair's barriers exist before either signals them
+  if constexpr (PAIR) cluster_sync();  // the cluster's barriers exist before any CTA signals them
   tc_fence_after();
   const uint32_t tmem_base = copier ? 0u : *L.tmem_slot;
 
@@ -1092,9 +1135,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 8 + warp, p.copy_ctas * 8);
     }
   } else if (warp == 0) {
-    if (lane == 0) run_producer<OP, PAIR>(p, L);
+    if (lane == 0) run_producer<OP, CL, NS>(p, L);
   } else if (warp == 1) {
-    if (lane == 0 && pair_rank<PAIR>() == 0) run_mma<OP, PAIR>(p, L, tmem_base);
+    if (lane == 0 && (cl_rank<CL>() & 1u) == 0u) run_mma<OP, CL, NS>(p, L, tmem_base);
   } else if (warp < 4) {
     if (OP == kOpAG && !p.plain && p.copy_ctas == 0) {  // co-located transfer warps
       if (COPY == kCopyTma && warp == 2 && lane == 0)
@@ -1105,12 +1148,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
                       static_cast<int32_t>(gridDim.x) * 2);
     }
   } else {
-    run_epilogue<OP, F32, PAIR>(p, L, tmem_base, warp, lane);
+    run_epilogue<OP, F32, CL>(p, L, tmem_base, warp, lane);
   }
 
   tc_fence_before();
   __syncthreads();
-  // neither CTA of a pair leaves while the other may still read its shared memory or TMEM
+  // no CTA of a cluster leaves while another may still read or write its shared memory or TMEM
   if constexpr (PAIR) cluster_sync();
   if (warp == 1 && !copier) {
     __syncwarp();

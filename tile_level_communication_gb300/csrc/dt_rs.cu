@@ -1,15 +1,23 @@
 // GEMM-ReduceScatter / GEMM-AllReduce instantiations of the fused kernel (bf16 or fp32
-// out, one CTA or a CTA pair per tile).
+// out, one CTA, a CTA pair or two pairs per tile).
 #include "dt_internal.h"
 
 namespace dt {
 
-cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream, bool pair) {
-  if (pair)
-    return f32 ? launch_fused<kOpRS, kCopyNone, true, true>(p, grid, false, stream)
-               : launch_fused<kOpRS, kCopyNone, false, true>(p, grid, false, stream);
-  return f32 ? launch_fused<kOpRS, kCopyNone, true, false>(p, grid, false, stream)
-             : launch_fused<kOpRS, kCopyNone, false, false>(p, grid, false, stream);
+namespace {
+template <bool F32>
+cudaError_t launch_cl(const KParams& p, int grid, cudaStream_t stream, int cl) {
+  switch (cl) {
+    case 1: return launch_fused<kOpRS, kCopyNone, F32, 1>(p, grid, false, stream);
+    case 2: return launch_fused<kOpRS, kCopyNone, F32, 2>(p, grid, false, stream);
+    case 4: return launch_fused<kOpRS, kCopyNone, F32, 4>(p, grid, false, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+}  // namespace
+
+cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream, int cl) {
+  return f32 ? launch_cl<true>(p, grid, stream, cl) : launch_cl<false>(p, grid, stream, cl);
 }
 
 }  // namespace dt
