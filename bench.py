@@ -37,13 +37,13 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 # DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
 # kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "23830aa3046508ed", "points": {
-        "1024/8/256": 7.495026e9 + 2.007133e9,     # --set full capture
-        "1024/4/256": 6481171200 + 1999900160,     # dram metrics only
-        "1024/16/256": 6651609088 + 1999531520,    # dram metrics only
+    "rs_w8_m8192_n8192_k3584": {"csrc": "85a774d459cc0eba", "points": {
+        "1024/8/256": 7.467960e9 + 2.009302e9,     # --set full capture
+        "1024/4/256": 7019597568 + 2005891072,     # dram metrics only
+        "1024/16/256": 6938266112 + 2005884416,    # dram metrics only
     }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "23830aa3046508ed", "points": {
-        "256/8/256": 565.70368e6 + 168.374784e6,   # --set full capture, TMA transfer
+    "ag_w8_m8192_n3584_k8192": {"csrc": "85a774d459cc0eba", "points": {
+        "256/8/256": 580.155392e6 + 168.795136e6,  # --set full capture, TMA transfer
     }},
 }
 
