@@ -41,6 +41,12 @@ NCU_TRAFFIC = {
         "1024/8/256": 7.467960e9 + 2.009302e9,     # --set full capture
         "1024/4/256": 7019597568 + 2005891072,     # dram metrics only
         "1024/16/256": 6938266112 + 2005884416,    # dram metrics only
+        # chunks of 512 / 256 rows: two / one pair m-tiles per chunk, the same order at every
+        # group width (dram metrics only)
+        "512/4/256": 10256476928 + 2010745856, "512/8/256": 10256476928 + 2010745856,
+        "512/16/256": 10256476928 + 2010745856,
+        "256/4/256": 17776413952 + 2021791744, "256/8/256": 17776413952 + 2021791744,
+        "256/16/256": 17776413952 + 2021791744,
     }},
     "ag_w8_m8192_n3584_k8192": {"csrc": "85a774d459cc0eba", "points": {
         "256/8/256": 580.155392e6 + 168.795136e6,  # --set full capture, TMA transfer
@@ -558,10 +564,12 @@ def main():
     if not args.no_tune and args.chunk_rows == 0 and args.backend == "auto" and not args.group:
         for cl in calls:
             if cl["op"] == "ag":
-                pts = dt.tune_ag_gemm(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], cl["args"])
+                pts = dt.tune_ag_gemm(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], cl["args"],
+                                      reps=8)
             else:
                 op_id = {"rs": dt.OP_RS, "ar": dt.OP_AR, "a2a": dt.OP_A2A}[cl["op"]]
-                pts = dt.tune_reduce(op_id, cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"])
+                pts = dt.tune_reduce(op_id, cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"],
+                                     reps=8)
             a = cl["args"]
             tuned[cl["op"]] = {"chunk_rows": int(a.chunk_rows),
                                "backend": [k for k, v in dt.BACKENDS.items() if v == a.backend][0],
