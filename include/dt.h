@@ -319,12 +319,13 @@ typedef struct dt_tune_point {
  * communication and the tile order, all by measuring the generated variants).
  * AllGather-GEMM candidates: chunk rows {64 .. 4096, M/W} x {copy engine (when the chunk count
  * stays <= 512), TMA and ld/st with co-located transfer warps, TMA and ld/st on 8 or 16
- * dedicated CTAs}; then group widths {4, 16} around the best.  Scatter-mode candidates
+ * dedicated CTAs}; then group widths {4, 8, 16} at the best point.  Scatter-mode candidates
  * (dt_tune_reduce with op DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A): chunk rows x group
  * widths {4, 8, 16}.  Each candidate runs once as
- * warm-up and `reps` times timed with CUDA events on `stream` (synchronising); candidates
- * whose workspace exceeds ws_bytes are skipped.  The fastest knobs are written into *a
- * (chunk_rows, backend, copy_ctas, group; swizzle stays on).  `points` (may be NULL) receives
+ * warm-up and `reps` times timed with CUDA events on `stream` (synchronising), in a forward
+ * and again in a reverse pass over the candidates, keeping its faster time (the GPU slows as
+ * it warms under the power cap); candidates whose workspace exceeds ws_bytes are skipped.  The
+ * fastest knobs are written into *a (chunk_rows, backend, copy_ctas, group; swizzle stays on).  `points` (may be NULL) receives
  * up to max_points candidates and *n_points their number.  The inputs are read and the
  * outputs written by every candidate; all candidates give bit-identical outputs. */
 dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, void* workspace,
