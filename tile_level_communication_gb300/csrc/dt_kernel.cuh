@@ -215,9 +215,16 @@ __device__ __forceinline__ uint32_t cl_rank() {
   return CL > 1 ? (blockIdx.x % static_cast<uint32_t>(CL)) : 0u;
 }
 
+// Tile id at position pos of the order (identity in the baselines' plain launches); -1 past the
+// end.  Each role fetches the next tile's id while it works on the current one, so the load's
+// latency does not sit between two tiles.
+__device__ __forceinline__ int32_t tile_id(const KParams& p, int32_t pos) {
+  if (pos >= p.T) return -1;
+  return p.plain ? pos : __ldg(p.order + pos);
+}
+
 template <int OP, int CL>
-__device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t pos) {
-  int32_t t = p.plain ? pos : __ldg(p.order + pos);
+__device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t t) {
   TileInfo ti;
   ti.valid = (t >= 0 && t < p.T);
   if (!ti.valid) t = 0;
@@ -275,8 +282,11 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
   uint32_t full0_lead = full0;  // stage 0's full barrier in the pair leader (cluster address)
   if constexpr (PAIR) full0_lead = mapa_shared(full0, rank & ~1u);
   uint32_t kit = 0;  // k-blocks issued so far (the last one, if any, is kit - 1)
+  int32_t t_next = tile_id(p, first_pos<CL>(p));
   for (int32_t pos = first_pos<CL>(p); pos < p.T; pos += pos_stride<CL>(p)) {
-    const TileInfo ti = decode_tile<OP, CL>(p, pos);
+    const int32_t t_cur = t_next;
+    t_next = tile_id(p, pos + pos_stride<CL>(p));
+    const TileInfo ti = decode_tile<OP, CL>(p, t_cur);
     if (!ti.valid) {
       raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
       continue;
@@ -380,8 +390,11 @@ __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_bas
   const uint32_t full0 = L.full(0), empty0 = L.empty(0);
   const uint64_t adesc0 = smem_desc_sw128(smem_u32(L.a), 16, 1024);
   const uint64_t bdesc0 = smem_desc_sw128(smem_u32(L.b), kBSlab, 1024);
+  int32_t t_next = tile_id(p, first_pos<CL>(p));
   for (int32_t pos = first_pos<CL>(p); pos < p.T; pos += pos_stride<CL>(p)) {
-    const TileInfo ti = decode_tile<OP, CL>(p, pos);
+    const int32_t t_cur = t_next;
+    t_next = tile_id(p, pos + pos_stride<CL>(p));
+    const TileInfo ti = decode_tile<OP, CL>(p, t_cur);
     if (!ti.valid) continue;
     const int acc = tl & 1;
     const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
@@ -663,8 +676,11 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
     tempty_bar0 = mapa_shared(tempty_bar0, lead);
     tempty_bar1 = mapa_shared(tempty_bar1, lead);
   }
+  int32_t t_next = tile_id(p, first_pos<CL>(p));
   for (int32_t pos = first_pos<CL>(p); pos < p.T; pos += pos_stride<CL>(p)) {
-    const TileInfo ti = decode_tile<OP, CL>(p, pos);
+    const int32_t t_cur = t_next;
+    t_next = tile_id(p, pos + pos_stride<CL>(p));
+    const TileInfo ti = decode_tile<OP, CL>(p, t_cur);
     if (!ti.valid) continue;
     const int acc = tl & 1;
     const uint32_t ph = (static_cast<uint32_t>(tl) >> 1) & 1u;
