@@ -37,19 +37,19 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 # DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
 # kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "f0350d344fb34a5f", "points": {
-        "1024/8/256": 7.467960e9 + 2.009302e9,     # --set full capture
-        "1024/4/256": 7019597568 + 2005891072,     # dram metrics only
-        "1024/16/256": 6938266112 + 2005884416,    # dram metrics only
+    "rs_w8_m8192_n8192_k3584": {"csrc": "9fa5006f81a033a5", "points": {
+        "1024/8/256": 6.308888e9 + 2.000354e9,     # --set full capture
+        "1024/4/256": 6289709312 + 2000205056,     # dram metrics only
+        "1024/16/256": 6307103232 + 2000097792,    # dram metrics only
         # chunks of 512 / 256 rows: two / one pair m-tiles per chunk, the same order at every
         # group width (dram metrics only)
-        "512/4/256": 10256476928 + 2010745856, "512/8/256": 10256476928 + 2010745856,
-        "512/16/256": 10256476928 + 2010745856,
-        "256/4/256": 17776413952 + 2021791744, "256/8/256": 17776413952 + 2021791744,
-        "256/16/256": 17776413952 + 2021791744,
+        "512/4/256": 10012182528 + 2009983232, "512/8/256": 10012182528 + 2009983232,
+        "512/16/256": 10012182528 + 2009983232,
+        "256/4/256": 17825377024 + 2022490112, "256/8/256": 17825377024 + 2022490112,
+        "256/16/256": 17825377024 + 2022490112,
     }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "f0350d344fb34a5f", "points": {
-        "256/8/256": 580.155392e6 + 168.795136e6,  # --set full capture, TMA transfer
+    "ag_w8_m8192_n3584_k8192": {"csrc": "9fa5006f81a033a5", "points": {
+        "256/8/256": 564.260096e6 + 168.435968e6,  # --set full capture, TMA transfer
     }},
 }
 
