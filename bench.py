@@ -37,7 +37,7 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 # DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
 # kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "9fa5006f81a033a5", "points": {
+    "rs_w8_m8192_n8192_k3584": {"csrc": "d060726ad4a8e25f", "points": {
         "1024/8/256": 6.308888e9 + 2.000354e9,     # --set full capture
         "1024/4/256": 6289709312 + 2000205056,     # dram metrics only
         "1024/16/256": 6307103232 + 2000097792,    # dram metrics only
@@ -48,7 +48,7 @@ NCU_TRAFFIC = {
         "256/4/256": 17825377024 + 2022490112, "256/8/256": 17825377024 + 2022490112,
         "256/16/256": 17825377024 + 2022490112,
     }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "9fa5006f81a033a5", "points": {
+    "ag_w8_m8192_n3584_k8192": {"csrc": "d060726ad4a8e25f", "points": {
         "256/8/256": 564.260096e6 + 168.435968e6,  # --set full capture, TMA transfer
     }},
 }
@@ -61,12 +61,17 @@ KERNEL_SOURCES = ("dt_kernel.cuh", "dt_ptx.cuh", "dt_plan.cuh", "dt_internal.h",
 
 
 def csrc_hash():
+    """Hash of the kernel sources' code: comments and whitespace do not count."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
         h.update(name.encode())
-        with open(os.path.join(ROOT, "tile_level_communication_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "tile_level_communication_gb300", "csrc", name)) as fh:
+            code = fh.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 FFN_PAIR = ("ag_w8_m8192_n3584_k8192", "rs_w8_m8192_n8192_k3584")
 L2_BYTES = 129 * 2 ** 20

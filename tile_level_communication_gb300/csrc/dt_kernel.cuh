@@ -1,11 +1,13 @@
-// Persistent, warp-specialised tcgen05 GEMM with the chunk-centric AllGather and
-// ReduceScatter fused in.
+// Persistent, warp-specialised tcgen05 GEMM with the chunk-centric AllGather,
+// ReduceScatter / AllReduce or AllToAll fused in.
 //
-// One CTA per SM, 8 warps:
+// One CTA per SM, 8 warps; CL CTAs per cluster share a tile of CL x 128 rows (CL = 1: one
+// CTA, tcgen05 cta_group::1; CL = 2: a CTA pair, cta_group::2; CL = 4: two pairs sharing B):
 //   warp 0      TMA producer: per tile, waits (bounded) for the ready flags of the chunks
-//               the tile's rows live in, then streams A / B k-blocks into a 4-stage ring.
-//   warp 1      MMA issuer (one thread): tcgen05.mma 128x256x16 into one of two TMEM
-//               accumulators; also allocates / frees TMEM.
+//               this CTA's rows live in, then streams A / B k-blocks into a 4- to 7-stage
+//               ring (a pair's stages complete on its even CTA's barriers).
+//   warp 1      MMA issuer (one thread; the even CTA of a pair): tcgen05.mma 128x256x16 or
+//               256x256x16 into one of two TMEM accumulators; allocates / frees TMEM.
 //   warps 2-3   chunk transfer workers (AllGather, in-kernel backends): copy chunk pieces
 //               from the rank shards into the gather buffer (TMA bulk or 16-byte ld/st)
 //               and release each chunk's ready flag when its last piece has landed.
