@@ -37,7 +37,7 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 # DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
 # kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "d060726ad4a8e25f", "points": {
+    "rs_w8_m8192_n8192_k3584": {"csrc": "c578d47a50fd557d", "points": {
         "1024/8/256": 6.308888e9 + 2.000354e9,     # --set full capture
         "1024/4/256": 6289709312 + 2000205056,     # dram metrics only
         "1024/16/256": 6307103232 + 2000097792,    # dram metrics only
@@ -48,7 +48,7 @@ NCU_TRAFFIC = {
         "256/4/256": 17825377024 + 2022490112, "256/8/256": 17825377024 + 2022490112,
         "256/16/256": 17825377024 + 2022490112,
     }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "d060726ad4a8e25f", "points": {
+    "ag_w8_m8192_n3584_k8192": {"csrc": "c578d47a50fd557d", "points": {
         "256/8/256": 564.260096e6 + 168.435968e6,  # --set full capture, TMA transfer
     }},
 }

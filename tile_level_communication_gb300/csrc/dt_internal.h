@@ -31,15 +31,28 @@ cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t 
 cudaError_t launch_a2a_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream, int cl);
 
 // One launch of an instance of the fused kernel (dynamic shared memory raised once).
+// Per device and kernel instance: the dynamic shared memory limit raised, and how many of its
+// clusters the device holds at once (0 until known).
+constexpr int kMaxDevices = 64;
+template <int OP, int COPY, bool F32, int CL>
+struct LaunchState {
+  bool configured[kMaxDevices];
+  int max_clusters[kMaxDevices];
+};
+
 template <int OP, int COPY, bool F32, int CL>
 cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStream_t stream) {
   auto kern = fused_gemm_kernel<OP, COPY, F32, CL>;
   const int smem = kernel_smem_bytes(OP == kOpRS, COPY, CL);
-  static bool configured = false;
-  if (!configured) {
+  static LaunchState<OP, COPY, F32, CL> state = {};
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return de;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!state.configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    state.configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -58,8 +71,8 @@ cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStrea
     // is resident (what the in-kernel chunk transfer needs; checked here rather than with the
     // cooperative attribute, which a profiler cannot replay together with clusters); the
     // tiles are spread over whatever grid runs
-    static int max_clusters = -1;
-    if (max_clusters < 0) {
+    int& max_clusters = state.max_clusters[dev];
+    if (max_clusters < 1) {
       cudaLaunchConfig_t probe = cfg;
       probe.gridDim = dim3(CL);
       cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &probe);
