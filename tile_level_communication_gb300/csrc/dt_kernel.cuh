@@ -373,6 +373,15 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
 }
 
 // ============================================================================ MMA issuer
+// The whole MMA warp runs the loop, so it stays converged, and one elected lane issues the
+// MMAs and commits: issued by a lone lane of a diverged warp, CTA-pair MMAs (M = 256, N = 256,
+// K = 16) go out every 135 clocks instead of every 128.  Waits are polled by every lane and
+// agreed by a vote, so all lanes leave the loop together.
+__device__ __forceinline__ bool warp_wait_bar(const KParams& p, const SmemLayout& L, uint32_t bar,
+                                             uint32_t parity, uint32_t site) {
+  return __all_sync(0xffffffffu, wait_bar(p, L, bar, parity, site));
+}
+
 template <int OP, int CL, int NS>
 __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_base) {
   constexpr bool PAIR = CL > 1;
@@ -400,7 +409,7 @@ __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_bas
     if (!ti.valid) continue;
     const int acc = tl & 1;
     const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
-    if (!wait_bar(p, L, L.tempty(acc), aph ^ 1u, 200 + acc)) break;
+    if (!warp_wait_bar(p, L, L.tempty(acc), aph ^ 1u, 200 + acc)) break;
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
     bool ok = true;
@@ -411,36 +420,45 @@ __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_bas
       // barrier's completion orders them; no tcgen05 fence here, which would hold the issue
       // of this k-block until the MMAs in flight have finished
       const uint32_t fb = full0 + 8u * static_cast<uint32_t>(st);
-      if (!wait_bar(p, L, fb, ph, 300 + st)) { ok = false; break; }
+      if (!warp_wait_bar(p, L, fb, ph, 300 + st)) { ok = false; break; }
       const uint64_t ad0 =
           adesc0 + static_cast<uint64_t>((static_cast<uint32_t>(st) * kAStage) >> 4);
       const uint64_t bd0 =
           bdesc0 + static_cast<uint64_t>((static_cast<uint32_t>(st) * b_stage_bytes(PAIR)) >> 4);
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        // A: K-major rows of 128 B, 8-row groups 1024 B apart (SBO); +32 B per 16 k
-        const uint64_t ad = ad0 + static_cast<uint64_t>(kk * (32 >> 4));
-        // B: MN-major; 64-column slabs 8 KB apart (LBO), 8 k-row groups 1 KB apart (SBO);
-        // +2 KB per 16 k
-        const uint64_t bd = bd0 + static_cast<uint64_t>(kk * (2048 >> 4));
-        if constexpr (PAIR)
-          umma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
-        else
-          umma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // A: K-major rows of 128 B, 8-row groups 1024 B apart (SBO); +32 B per 16 k
+          const uint64_t ad = ad0 + static_cast<uint64_t>(kk * (32 >> 4));
+          // B: MN-major; 64-column slabs 8 KB apart (LBO), 8 k-row groups 1 KB apart (SBO);
+          // +2 KB per 16 k
+          const uint64_t bd = bd0 + static_cast<uint64_t>(kk * (2048 >> 4));
+          if constexpr (PAIR)
+            umma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          else
+            umma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        // frees the stage (in both CTAs of a pair) once these MMAs have read it
+        const uint32_t eb = empty0 + 8u * static_cast<uint32_t>(st);
+        if constexpr (PAIR) umma_commit_pair(eb, stage_mask); else umma_commit(eb);
       }
-      // frees the stage (in both CTAs of a pair) once these MMAs have read it
-      const uint32_t eb = empty0 + 8u * static_cast<uint32_t>(st);
-      if constexpr (PAIR) umma_commit_pair(eb, stage_mask); else umma_commit(eb);
+      __syncwarp();
       issued = true;
     }
     if (!ok) break;
     // accumulator ready for the epilogue (of both CTAs)
-    if constexpr (PAIR) umma_commit_pair(L.tfull(acc), pair_mask); else umma_commit(L.tfull(acc));
+    if (elect_one()) {
+      if constexpr (PAIR) umma_commit_pair(L.tfull(acc), pair_mask); else umma_commit(L.tfull(acc));
+    }
+    __syncwarp();
     ++tl;
   }
-  if (*L.abort_flag && issued) {
-    if constexpr (PAIR) umma_commit_pair(L.fin(), static_cast<uint16_t>(1u << rank));
-    else umma_commit(L.fin());
+  if (__any_sync(0xffffffffu, *L.abort_flag != 0) && issued) {
+    if (elect_one()) {
+      if constexpr (PAIR) umma_commit_pair(L.fin(), static_cast<uint16_t>(1u << rank));
+      else umma_commit(L.fin());
+    }
+    __syncwarp();
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(L.fin(), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
     }
@@ -1155,7 +1173,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   } else if (warp == 0) {
     if (lane == 0) run_producer<OP, CL, NS>(p, L);
   } else if (warp == 1) {
-    if (lane == 0 && (cl_rank<CL>() & 1u) == 0u) run_mma<OP, CL, NS>(p, L, tmem_base);
+    if ((cl_rank<CL>() & 1u) == 0u) run_mma<OP, CL, NS>(p, L, tmem_base);
   } else if (warp < 4) {
     if (OP == kOpAG && !p.plain && p.copy_ctas == 0) {  // co-located transfer warps
       if (COPY == kCopyTma && warp == 2 && lane == 0)
