@@ -270,6 +270,14 @@ __device__ __forceinline__ int32_t pos_stride(const KParams& p) {
   return (static_cast<int32_t>(gridDim.x) - p.copy_ctas) / CL;
 }
 
+// Warp-wide bounded wait: every lane polls, a vote makes the outcome the warp's, so all lanes
+// leave a loop together (the producer and MMA roles run as whole warps that stay converged;
+// one elected lane issues the TMA loads or MMAs).
+__device__ __forceinline__ bool warp_wait_bar(const KParams& p, const SmemLayout& L, uint32_t bar,
+                                             uint32_t parity, uint32_t site) {
+  return __all_sync(0xffffffffu, wait_bar(p, L, bar, parity, site));
+}
+
 // ============================================================================ producer
 template <int OP, int CL, int NS>
 __device__ void run_producer(const KParams& p, const SmemLayout& L) {
@@ -290,7 +298,8 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
     t_next = tile_id(p, pos + pos_stride<CL>(p));
     const TileInfo ti = decode_tile<OP, CL>(p, t_cur);
     if (!ti.valid) {
-      raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
+      if (elect_one()) raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
+      __syncwarp();
       continue;
     }
     // local HBM as the cache of remote memory: the own rank's rows need no transfer
@@ -299,23 +308,27 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
         OP == kOpAG && p.own_in_place && ti.row0 >= own0 && ti.row_end <= own0 + p.g.Ms;
     if (OP == kOpAG && p.wait_flags && !own_tile) {
       // consumer_tile_wait: every chunk holding one of this tile's rows must have landed
+      // (polled by the lane that issues the loads)
       bool ok = true;
-      for (int64_t g = ti.row0; g < ti.row_end && ok;) {
-        int32_t s, j;
-        row_chunk(p.g, g, s, j);
-        const int32_t c = s * p.g.nC + j;
-        const bool cached =
-            c < kReadyBitsWords * 32 && ((L.ready_bits[c >> 5] >> (c & 31)) & 1u);
-        if (!cached) {
-          ok = wait_flag(p, L, c);
-          if (ok && c < kReadyBitsWords * 32) L.ready_bits[c >> 5] |= 1u << (c & 31);
+      if (elect_one()) {
+        for (int64_t g = ti.row0; g < ti.row_end && ok;) {
+          int32_t s, j;
+          row_chunk(p.g, g, s, j);
+          const int32_t c = s * p.g.nC + j;
+          const bool cached =
+              c < kReadyBitsWords * 32 && ((L.ready_bits[c >> 5] >> (c & 31)) & 1u);
+          if (!cached) {
+            ok = wait_flag(p, L, c);
+            if (ok && c < kReadyBitsWords * 32) L.ready_bits[c >> 5] |= 1u << (c & 31);
+          }
+          g = static_cast<int64_t>(s) * p.g.Ms +
+              min64(static_cast<int64_t>(j + 1) * p.g.Cr, p.g.Ms);
         }
-        g = static_cast<int64_t>(s) * p.g.Ms + min64(static_cast<int64_t>(j + 1) * p.g.Cr, p.g.Ms);
+        // the rows were written by other agents through the generic proxy (or the copy
+        // engine); the TMA loads below read through the async proxy
+        if (ok) fence_proxy_async_global();
       }
-      if (!ok) break;
-      // the rows were written by other agents through the generic proxy (or the copy
-      // engine); the TMA loads below read through the async proxy
-      fence_proxy_async_global();
+      if (__any_sync(0xffffffffu, !ok)) break;
     }
     const CUtensorMap* tA = &p.tmA[OP != kOpAG ? ti.q : (own_tile ? 1 : 0)];
     const CUtensorMap* tB = &p.tmB[OP != kOpAG ? ti.q : 0];
@@ -327,37 +340,40 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
       const int st = static_cast<int>(kit % NS);
       const uint32_t ph = (kit / NS) & 1u;
       const uint32_t sst = static_cast<uint32_t>(st);
-      if (!wait_bar(p, L, empty0 + 8u * sst, ph ^ 1u, 100 + st)) { ok = false; break; }
-      const uint32_t a_dst = a_smem0 + sst * kAStage;
-      const uint32_t b_dst = b_smem0 + sst * b_stage_bytes(PAIR);
-      const uint32_t fb = full0 + 8u * sst;
-      if constexpr (CL == 4) {
-        // both pairs use the same columns: this CTA loads slab (rank >> 1) of its half of B
-        // for itself and for its counterpart in the other pair
-        const uint32_t bar = full0_lead + 8u * sst;
-        if (leader) mbar_expect_tx(fb, 2 * (kAStage + b_stage_bytes(PAIR)));
-        tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
-        const uint32_t sl = rank >> 1;
-        tma_load_2d_pair_mc(b_dst + sl * kBSlab, tB, b_col + static_cast<int32_t>(sl) * 64,
-                            kb * kBK, bar, static_cast<uint16_t>(0x5u << (rank & 1u)));
-      } else if constexpr (PAIR) {
-        const uint32_t bar = full0_lead + 8u * sst;
-        if (leader) mbar_expect_tx(fb, 2 * (kAStage + b_stage_bytes(PAIR)));
-        tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
+      if (!warp_wait_bar(p, L, empty0 + 8u * sst, ph ^ 1u, 100 + st)) { ok = false; break; }
+      if (elect_one()) {
+        const uint32_t a_dst = a_smem0 + sst * kAStage;
+        const uint32_t b_dst = b_smem0 + sst * b_stage_bytes(PAIR);
+        const uint32_t fb = full0 + 8u * sst;
+        if constexpr (CL == 4) {
+          // both pairs use the same columns: this CTA loads slab (rank >> 1) of its half of B
+          // for itself and for its counterpart in the other pair
+          const uint32_t bar = full0_lead + 8u * sst;
+          if (leader) mbar_expect_tx(fb, 2 * (kAStage + b_stage_bytes(PAIR)));
+          tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
+          const uint32_t sl = rank >> 1;
+          tma_load_2d_pair_mc(b_dst + sl * kBSlab, tB, b_col + static_cast<int32_t>(sl) * 64,
+                              kb * kBK, bar, static_cast<uint16_t>(0x5u << (rank & 1u)));
+        } else if constexpr (PAIR) {
+          const uint32_t bar = full0_lead + 8u * sst;
+          if (leader) mbar_expect_tx(fb, 2 * (kAStage + b_stage_bytes(PAIR)));
+          tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
 #pragma unroll
-        for (int jj = 0; jj < NB; ++jj)
-          tma_load_2d_pair(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, bar);
-      } else {
-        mbar_expect_tx(fb, kAStage + b_stage_bytes(PAIR));
-        tma_load_2d(a_dst, tA, kb * kBK, a_row, fb);
+          for (int jj = 0; jj < NB; ++jj)
+            tma_load_2d_pair(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, bar);
+        } else {
+          mbar_expect_tx(fb, kAStage + b_stage_bytes(PAIR));
+          tma_load_2d(a_dst, tA, kb * kBK, a_row, fb);
 #pragma unroll
-        for (int jj = 0; jj < NB; ++jj)
-          tma_load_2d(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, fb);
+          for (int jj = 0; jj < NB; ++jj)
+            tma_load_2d(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, fb);
+        }
       }
+      __syncwarp();
     }
     if (!ok) break;
   }
-  if (*L.abort_flag && leader) {
+  if (__any_sync(0xffffffffu, *L.abort_flag != 0) && leader) {
     // let every TMA load issued into this stage ring land before the CTA can exit (a pair's
     // leader barrier counts the other CTA's bytes as well)
     // the last k-block issued into stage s is the largest k < kit with k % NS == s
@@ -375,12 +391,7 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
 // ============================================================================ MMA issuer
 // The whole MMA warp runs the loop, so it stays converged, and one elected lane issues the
 // MMAs and commits: issued by a lone lane of a diverged warp, CTA-pair MMAs (M = 256, N = 256,
-// K = 16) go out every 135 clocks instead of every 128.  Waits are polled by every lane and
-// agreed by a vote, so all lanes leave the loop together.
-__device__ __forceinline__ bool warp_wait_bar(const KParams& p, const SmemLayout& L, uint32_t bar,
-                                             uint32_t parity, uint32_t site) {
-  return __all_sync(0xffffffffu, wait_bar(p, L, bar, parity, site));
-}
+// K = 16) go out every 135 clocks instead of every 128.
 
 template <int OP, int CL, int NS>
 __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_base) {
@@ -1171,7 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 8 + warp, p.copy_ctas * 8);
     }
   } else if (warp == 0) {
-    if (lane == 0) run_producer<OP, CL, NS>(p, L);
+    run_producer<OP, CL, NS>(p, L);
   } else if (warp == 1) {
     if ((cl_rank<CL>() & 1u) == 0u) run_mma<OP, CL, NS>(p, L, tmem_base);
   } else if (warp < 4) {
