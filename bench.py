@@ -37,19 +37,19 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 # DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
 # kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "c578d47a50fd557d", "points": {
-        "1024/8/256": 6.308888e9 + 2.000354e9,     # --set full capture
-        "1024/4/256": 6289709312 + 2000205056,     # dram metrics only
-        "1024/16/256": 6307103232 + 2000097792,    # dram metrics only
+    "rs_w8_m8192_n8192_k3584": {"csrc": "6087463d16bb5c0f", "points": {
+        "1024/8/256": 6.313576e9 + 2.000093e9,     # --set full capture
+        "1024/4/256": 6272429056 + 1999698944,     # dram metrics only
+        "1024/16/256": 6263151616 + 1999620352,    # dram metrics only
         # chunks of 512 / 256 rows: two / one pair m-tiles per chunk, the same order at every
         # group width (dram metrics only)
-        "512/4/256": 10012182528 + 2009983232, "512/8/256": 10012182528 + 2009983232,
-        "512/16/256": 10012182528 + 2009983232,
-        "256/4/256": 17825377024 + 2022490112, "256/8/256": 17825377024 + 2022490112,
-        "256/16/256": 17825377024 + 2022490112,
+        "512/4/256": 10104554240 + 2008636672, "512/8/256": 10104554240 + 2008636672,
+        "512/16/256": 10104554240 + 2008636672,
+        "256/4/256": 17956824064 + 2023083008, "256/8/256": 17956824064 + 2023083008,
+        "256/16/256": 17956824064 + 2023083008,
     }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "c578d47a50fd557d", "points": {
-        "256/8/256": 564.260096e6 + 168.435968e6,  # --set full capture, TMA transfer
+    "ag_w8_m8192_n3584_k8192": {"csrc": "6087463d16bb5c0f", "points": {
+        "256/8/256": 568.476672e6 + 168.011008e6,  # --set full capture, TMA transfer
     }},
 }
 
