@@ -839,10 +839,39 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
         for d_, h_ in zip(cl["outs"], hs):
             if not torch.equal(d_.cpu().view(torch.int16), h_.view(torch.int16)):
                 raise RuntimeError("end-to-end outputs differ from the device's")
+    # the host link's own rate, measured here: one 512 MiB pinned copy each way, best of 3; the
+    # step's inputs cannot arrive faster than in_bytes at the host-to-device rate
+    link_bytes = 1 << 29
+    h_buf = torch.empty(link_bytes, dtype=torch.uint8).pin_memory()
+    d_buf = torch.empty(link_bytes, dtype=torch.uint8, device=dev)
+
+    def link_ms(h2d):
+        best = 1e9
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(s_main)
+            if h2d:
+                d_buf.copy_(h_buf, non_blocking=True)
+            else:
+                h_buf.copy_(d_buf, non_blocking=True)
+            e1.record(s_main)
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        return best
+
+    h2d_gbs = link_bytes / (link_ms(True) * 1e-3) / 1e9
+    d2h_gbs = link_bytes / (link_ms(False) * 1e-3) / 1e9
+    del h_buf, d_buf
+    floor_ms = max(in_bytes / (h2d_gbs * 1e9) * 1e3, t_max / args.steps)
     out["e2e"] = {"value": world * flops_step / (ms_e * 1e-3) / 1e12, "unit": "TFLOP/s",
                   "ms_per_step": ms_e, "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                   "pipelined": "step i+1's inputs in and step i-1's outputs out overlap step i, "
-                               f"each spread over {n_cs} copy streams"}
+                               f"each spread over {n_cs} copy streams",
+                  "link": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+                           "floor_ms_per_step": floor_ms, "frac_of_floor": floor_ms / ms_e,
+                           "note": "floor = the larger of the step's input bytes at the measured "
+                                   "pinned host-to-device rate and the device step time"}}
 
     # the CPU oracle on a bounded sample (rank 0, N=1 only)
     if world == 1:
