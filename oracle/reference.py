@@ -7,6 +7,8 @@ tensor parallelism uses AllGather+GEMM and GEMM+ReduceScatter; Triton-distribute
 talk, "GEMM ReduceScatter" paragraph: every rank computes a partial product and
 the reduced rows are scattered to their owner ranks):
 
+* AllGather over W ranks (the collective on its own): every rank receives
+  concat_rows(A_0, ..., A_{W-1}), shard s at rows s*M/W .. (s+1)*M/W - 1.
 * AllGather-GEMM over W ranks: A = concat_rows(A_0, ..., A_{W-1}); C = A @ B.
 * GEMM-ReduceScatter over W ranks: P_q = A_q @ B_q (rank q holds a K slice);
   S = sum_q P_q; rank s receives rows s*M/W .. (s+1)*M/W - 1 of S.
@@ -21,6 +23,17 @@ Inputs are float64 arrays holding exact bf16 values; outputs are float64.
 from __future__ import annotations
 
 import numpy as np
+
+
+def allgather(shards):
+    """The gathered matrix: shard s's rows at rows s*M/W .. of the result, any dtype kept
+    (a copy is exact, so bf16 bit patterns pass through unchanged)."""
+    if len(shards) < 1:
+        raise ValueError("need at least one shard")
+    rows = {np.asarray(x).shape[0] for x in shards}
+    if len(rows) != 1:
+        raise ValueError("every rank holds M/W rows")
+    return np.concatenate([np.asarray(x) for x in shards], axis=0)
 
 
 def ag_gemm(shards, b):

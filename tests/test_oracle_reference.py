@@ -363,3 +363,28 @@ def test_ffn_block_reduces_to_two_plain_products():
     # with an activation, H is act(X W1) rounded to bf16
     h2, _ = reference.ffn_tp(xs, w1, w2, "silu")
     assert np.array_equal(h2, reference.round_bf16_via_f32(reference.activation(want_h, "silu")))
+
+
+def test_allgather_places_each_shard_and_composes_with_the_gemm():
+    inp = make_ag_inputs(3, 12, 8, 16, seed=11)
+    shards = [f64_from_bf16_bits(s) for s in inp.shards]
+    g = reference.allgather(shards)
+    # brute force: row s*Ms + r of the gathered matrix is shard s's row r
+    assert g.shape == (12, 16)
+    for s in range(3):
+        for r in range(4):
+            assert np.array_equal(g[s * 4 + r], shards[s][r])
+    # gathering then multiplying is the AllGather-GEMM (pinned on its own above)
+    b = f64_from_bf16_bits(inp.b)
+    assert np.array_equal(g @ b, reference.ag_gemm(shards, b))
+    # one rank: the identity; bf16 bit patterns pass through unchanged
+    assert np.array_equal(reference.allgather([inp.shards[0]]), inp.shards[0])
+    bits = reference.allgather(inp.shards)
+    assert bits.dtype == np.uint16 and np.array_equal(bits[4:8], inp.shards[1])
+    # a reversed rank order (a plausible mistake) is caught by the row check
+    rev = np.concatenate(shards[::-1], axis=0)
+    assert not np.array_equal(rev, g)
+    with pytest.raises(ValueError):
+        reference.allgather([np.zeros((2, 8)), np.zeros((3, 8))])
+    with pytest.raises(ValueError):
+        reference.allgather([])
