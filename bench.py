@@ -37,19 +37,19 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 # DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
 # kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "6087463d16bb5c0f", "points": {
-        "1024/8/256": 6.313576e9 + 2.000093e9,     # --set full capture
-        "1024/4/256": 6272429056 + 1999698944,     # dram metrics only
-        "1024/16/256": 6263151616 + 1999620352,    # dram metrics only
+    "rs_w8_m8192_n8192_k3584": {"csrc": "386d5ed2b1b86eac", "points": {
+        "1024/8/256": 6.278112e9 + 2.002142e9,     # --set full capture
+        "1024/4/256": 6349637632 + 2001186304,     # dram metrics only
+        "1024/16/256": 6412386816 + 2001429248,    # dram metrics only
         # chunks of 512 / 256 rows: two / one pair m-tiles per chunk, the same order at every
         # group width (dram metrics only)
-        "512/4/256": 10104554240 + 2008636672, "512/8/256": 10104554240 + 2008636672,
-        "512/16/256": 10104554240 + 2008636672,
-        "256/4/256": 17956824064 + 2023083008, "256/8/256": 17956824064 + 2023083008,
-        "256/16/256": 17956824064 + 2023083008,
+        "512/4/256": 10003929600 + 2006697984, "512/8/256": 10003929600 + 2006697984,
+        "512/16/256": 10003929600 + 2006697984,
+        "256/4/256": 17727164928 + 2020683264, "256/8/256": 17727164928 + 2020683264,
+        "256/16/256": 17727164928 + 2020683264,
     }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "6087463d16bb5c0f", "points": {
-        "256/8/256": 568.476672e6 + 168.011008e6,  # --set full capture, TMA transfer
+    "ag_w8_m8192_n3584_k8192": {"csrc": "386d5ed2b1b86eac", "points": {
+        "256/8/256": 657.1712e6 + 168.678144e6,    # --set full capture, TMA transfer
     }},
 }
 
@@ -720,6 +720,50 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
         "value": flops_step / (ms_b * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_b,
         "fused_speedup": ms_b / (flops_step / (value / world * 1e12) * 1e3)}
 
+    # the copy path on its own: the AllGather's chunk transfer of every shard into one [M, K]
+    # buffer, per backend; 2 x bytes (read + write) over the time, against the measured HBM
+    # copy rate; L2 flushed before each timed copy (the shards fit in L2 otherwise)
+    ag_calls = [cl for cl in calls if cl["op"] == "ag"]
+    if ag_calls:
+        cl = ag_calls[0]
+        wl = cl["wl"]
+        hbm = peaks()["hbm_gbs"]
+        gathered = torch.empty((wl.m, wl.k), dtype=torch.bfloat16, device=dev)
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        nbytes = wl.m * wl.k * 2
+        res = {}
+        for be in ("copy_engine", "tma", "ldst"):
+            ga = dt.make_args(wl.world_size, wl.m, 8, wl.k, chunk_rows=cl["args"].chunk_rows,
+                              backend=be)
+            gws = torch.zeros(dt.workspace_size(ga, dt.OP_AG), dtype=torch.uint8, device=dev)
+            dt.allgather(cl["shards"], gathered, gws, ga)
+            times = []
+            for _ in range(k_side):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                dt.allgather(cl["shards"], gathered, gws, ga)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                times.append(e0.elapsed_time(e1))
+            code, info = dt.check(gws)
+            if code != 0:
+                raise RuntimeError(f"AllGather device error {info}")
+            t = statistics.median(times)
+            res[be] = {"ms": t, "gbs": 2 * nbytes / (t * 1e-3) / 1e9,
+                       "frac": 2 * nbytes / (t * 1e-3) / 1e9 / hbm}
+        if not torch.equal(gathered.view(torch.int16),
+                           torch.cat(cl["shards"], dim=0).view(torch.int16)):
+            raise RuntimeError("AllGather result differs from the shards")
+        del gathered, flush
+        out["copy_path"] = {
+            "what": f"AllGather alone of {wl.name}'s {wl.world_size} shards "
+                    f"({nbytes / 2**20:.0f} MiB, chunk {cl['args'].chunk_rows} rows), L2 flushed "
+                    "before each copy; gbs = 2 x bytes / time (read + write)",
+            "unit": "GB/s", "peak": hbm, "peak_source": "measured HBM copy" if
+            peaks()["source"] == "measured" else "fallback", "backends": res}
+
     # context: non-overlapped gather + cuBLAS (AG); cuBLAS partial products + sum (RS)
     def cublas_step():
         for cl in calls:
@@ -863,7 +907,8 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     h2d_gbs = link_bytes / (link_ms(True) * 1e-3) / 1e9
     d2h_gbs = link_bytes / (link_ms(False) * 1e-3) / 1e9
     del h_buf, d_buf
-    floor_ms = max(in_bytes / (h2d_gbs * 1e9) * 1e3, t_max / args.steps)
+    ms_dev = flops_step / (value / world * 1e12) * 1e3  # the device-resident step
+    floor_ms = max(in_bytes / (h2d_gbs * 1e9) * 1e3, ms_dev)
     out["e2e"] = {"value": world * flops_step / (ms_e * 1e-3) / 1e12, "unit": "TFLOP/s",
                   "ms_per_step": ms_e, "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                   "pipelined": "step i+1's inputs in and step i-1's outputs out overlap step i, "

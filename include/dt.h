@@ -231,6 +231,27 @@ dt_status dt_ffn_ag_rs(const void* const* x_shards, const void* w1, const void* 
                        void* h, void* const* out, void* ws_ag, size_t ws_ag_bytes, void* ws_rs,
                        size_t ws_rs_bytes, const dt_args* ag, const dt_args* rs, void* stream);
 
+/* AllGather alone: the chunk transfer of dt_ag_gemm without the GEMM (Triton-distributed
+ * talk, "AllGather" producer side; TileLink page, section 3.2, tile-level pull of remote
+ * chunks).  out = concat_rows(A_0, .., A_{W-1}), [M x K] bf16 with leading dimension
+ * a->ldc (0 = K); every shard, the own one included, is copied chunk by chunk (chunk_rows
+ * rows, ragged last chunk) in the AllGather's transfer order (own rank first when swizzle is
+ * on, then rank+1, ..).  Backends:
+ *   DT_XFER_COPY_ENGINE : one (2-D) copy per chunk on `stream`; any ldc.
+ *   DT_XFER_TMA / LDST  : one launch of the fused kernel with no GEMM tiles, every CTA (all
+ *                         SMs, or a->num_sms) running the transfer workers (4 TMA bulk-copy
+ *                         threads or 8 vector ld/st warps per CTA); each chunk's ready flag in
+ *                         the workspace is released with the call's epoch.  Needs ldc == K
+ *                         (rows land back to back).
+ *   DT_XFER_AUTO        : the AllGather-GEMM's rule (copy engine for chunks of >= 8 MiB, else
+ *                         TMA), and the copy engine whenever ldc != K.
+ * Uses world_size, rank, M, K, chunk_rows, swizzle, backend, lda, ldc, num_sms; N, ldb,
+ * out_dtype, tile_m, act and copy_ctas are ignored.  Workspace: dt_workspace_size(a,
+ * DT_OP_AG_GEMM) with any N >= 8 suffices (its gather area is not used).  Inputs and `out`
+ * must not overlap.  M == 0 or K == 0 does nothing. */
+dt_status dt_allgather(const void* const* a_shards, void* out, void* workspace, size_t ws_bytes,
+                       const dt_args* a, void* stream);
+
 /* Kernel-level-overlap baselines with the same arguments and results (AutoOverlap page,
  * section 2.1 / Fig. 2(b)): AG = per-chunk copies on a second stream and one launch of the
  * same GEMM per chunk, gated by events; RS = one GEMM launch per destination block writing

@@ -222,3 +222,45 @@ def test_a2a_workspace_holds_only_control(dt):
     need = dt.workspace_size(a, dt.OP_A2A)
     assert 0 < need < (1 << 20)
     assert dt.a2a_chunks(a) == 8 * 8 * 4
+
+
+# ----------------------------------------------------------------------------- AllGather alone
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(world_size=0, m=512, k=512), "DT_ERR_INVALID"),
+    (dict(world_size=3, m=512, k=512), "DT_ERR_INVALID"),            # M % W
+    (dict(world_size=2, m=512, k=500), "DT_ERR_UNSUPPORTED"),        # K % 8
+    (dict(world_size=2, m=512, k=512, chunk_rows=0), "DT_ERR_INVALID"),
+    (dict(world_size=2, m=512, k=512, ldc=504), "DT_ERR_INVALID"),   # out rows shorter than K
+    (dict(world_size=2, m=512, k=512, ldc=516), "DT_ERR_INVALID"),   # not 16-byte rows
+    (dict(world_size=2, m=512, k=512, ldc=520, backend="tma"), "DT_ERR_UNSUPPORTED"),
+    (dict(world_size=2, m=512, k=512, ldc=520, backend="ldst"), "DT_ERR_UNSUPPORTED"),
+    (dict(world_size=2, m=512, k=512, lda=500), "DT_ERR_INVALID"),
+])
+def test_allgather_argument_errors_are_synchronous(dt, kw, status):
+    w = kw.pop("world_size")
+    m, k = kw.pop("m"), kw.pop("k")
+    a = dt.make_args(w, m, 0, k, **kw)  # N plays no part
+    with pytest.raises(dt.DtError) as ei:
+        dt.allgather([256] * max(1, min(w, 16)), 4096, 8192, a, stream=0, ws_bytes=1 << 30)
+    assert ei.value.status == getattr(dt.capi, status)
+
+
+def test_allgather_pointer_and_workspace_errors(dt):
+    a = dt.make_args(2, 512, 8, 512, chunk_rows=128, backend="tma")
+    need = dt.workspace_size(a, dt.OP_AG)
+    with pytest.raises(dt.DtError) as ei:
+        dt.allgather([256, 8], 4096, 8192, a, stream=0, ws_bytes=need)     # shard misaligned
+    assert ei.value.status == dt.capi.DT_ERR_INVALID
+    with pytest.raises(dt.DtError) as ei:
+        dt.allgather([256, 512], 4104, 8192, a, stream=0, ws_bytes=need)   # out misaligned
+    assert ei.value.status == dt.capi.DT_ERR_INVALID
+    with pytest.raises(dt.DtError) as ei:
+        dt.allgather([256, 512], 4096, 8192, a, stream=0, ws_bytes=need - 1)
+    assert ei.value.status == dt.capi.DT_ERR_WORKSPACE
+    # N does not enter the workspace an AllGather needs
+    b = dt.make_args(2, 512, 4096, 512, chunk_rows=128, backend="tma")
+    assert dt.workspace_size(b, dt.OP_AG) >= need
+    # nothing to move: no pointer is touched
+    dt.allgather([0, 0], 0, 0, dt.make_args(2, 0, 8, 512), stream=0, ws_bytes=0)
+    dt.allgather([0, 0], 0, 0, dt.make_args(2, 512, 8, 0), stream=0, ws_bytes=0)

@@ -36,6 +36,7 @@ _SIGS = {
     "dt_workspace_init": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "dt_ag_gemm": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_gemm_rs": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "dt_allgather": (ctypes.c_int, [_P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_ag_gemm_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_gemm_rs_kernel_overlap": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "dt_gemm_ar": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
@@ -187,6 +188,13 @@ def _nbytes(workspace, nbytes):
 def ag_gemm(shards, b, c, workspace, args: DtArgs, stream=None, ws_bytes=None):
     _raise(lib().dt_ag_gemm(_ptr_array(shards), _ptr(b), _ptr(c), _ptr(workspace),
                             _nbytes(workspace, ws_bytes), ctypes.byref(args), _stream(stream)))
+
+
+def allgather(shards, out, workspace, args: DtArgs, stream=None, ws_bytes=None):
+    """AllGather alone (the fused op's chunk transfer): out ([M, K], ld args.ldc or K)
+    receives every shard's rows in rank order."""
+    _raise(lib().dt_allgather(_ptr_array(shards), _ptr(out), _ptr(workspace),
+                              _nbytes(workspace, ws_bytes), ctypes.byref(args), _stream(stream)))
 
 
 def gemm_rs(a_list, b_list, out_list, workspace, args: DtArgs, stream=None, ws_bytes=None):

@@ -306,9 +306,15 @@ constexpr size_t kTagOffset = 16;  // after the 4-word error block
 dt_status prepare_workspace(const Derived& d, void* ws, cudaStream_t stream, uint32_t* epoch);
 
 // ------------------------------------------------------------------------------ device info
+// Copy-engine chunk copies are spread round-robin over this many streams: one stream moves
+// 8 MiB device-to-device copies at ~2.7 TB/s (read + write), four at ~5 TB/s.
+constexpr int kCopyStreams = 4;
+
 struct DevCtx {
   int sms = 0;
   cudaStream_t side = nullptr;
+  cudaStream_t copy[kCopyStreams] = {};
+  cudaEvent_t copy_done[kCopyStreams] = {};
   cudaEvent_t ev_start = nullptr, ev_done = nullptr;
   cudaEvent_t tune_t0 = nullptr, tune_t1 = nullptr;  // timing events of the tuner
   std::vector<cudaEvent_t> chunk_events;
@@ -324,10 +330,29 @@ dt_status dev_ctx(DevCtx** out) {
   if (c.sms == 0) {
     DT_CUDA(cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev));
     DT_CUDA(cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking));
+    for (int i = 0; i < kCopyStreams; ++i) {
+      DT_CUDA(cudaStreamCreateWithFlags(&c.copy[i], cudaStreamNonBlocking));
+      DT_CUDA(cudaEventCreateWithFlags(&c.copy_done[i], cudaEventDisableTiming));
+    }
     DT_CUDA(cudaEventCreateWithFlags(&c.ev_start, cudaEventDisableTiming));
     DT_CUDA(cudaEventCreateWithFlags(&c.ev_done, cudaEventDisableTiming));
   }
   *out = &c;
+  return DT_OK;
+}
+
+// The copy streams start after `stream`'s work so far (fork) and `stream` continues after
+// theirs (join); the caller holds g_dev_mu in between.
+dt_status fork_copies(DevCtx* dev, cudaStream_t stream) {
+  DT_CUDA(cudaEventRecord(dev->ev_start, stream));
+  for (int i = 0; i < kCopyStreams; ++i) DT_CUDA(cudaStreamWaitEvent(dev->copy[i], dev->ev_start, 0));
+  return DT_OK;
+}
+dt_status join_copies(DevCtx* dev, cudaStream_t stream) {
+  for (int i = 0; i < kCopyStreams; ++i) {
+    DT_CUDA(cudaEventRecord(dev->copy_done[i], dev->copy[i]));
+    DT_CUDA(cudaStreamWaitEvent(stream, dev->copy_done[i], 0));
+  }
   return DT_OK;
 }
 
@@ -471,6 +496,26 @@ void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
 }
 
 // ------------------------------------------------------------------------------ AllGather
+// How the in-kernel transfer cuts a chunk into pieces of at most one 16 KiB staging buffer:
+// whole rows when a row fits (rows_per_piece of them), else 16 KiB segments of one row.
+void set_pieces(KParams& p, const Derived& d) {
+  p.row_bytes = d.K * 2;
+  if (p.row_bytes <= kCopyBuf) {
+    p.rows_per_piece = static_cast<int32_t>(kCopyBuf / p.row_bytes);
+    p.segs_per_row = 1;
+  } else {
+    p.rows_per_piece = 0;
+    p.segs_per_row = static_cast<int32_t>(cdiv64(p.row_bytes, kCopyBuf));
+  }
+  auto pieces = [&](int64_t rows) -> int32_t {
+    return p.rows_per_piece > 0 ? static_cast<int32_t>(cdiv64(rows, p.rows_per_piece))
+                                : static_cast<int32_t>(rows * p.segs_per_row);
+  };
+  p.pieces_full = pieces(std::min<int64_t>(d.Cr, d.Ms));
+  p.pieces_last = pieces(d.Ms - static_cast<int64_t>(d.nC - 1) * d.Cr);
+  p.src_rows_contig = d.lda == d.K ? 1 : 0;
+}
+
 dt_status ag_common(const void* const* a_shards, const void* b, void* c, void* ws,
                     size_t ws_bytes, const dt_args* a, Derived* d) {
   dt_status s = derive(a, DT_OP_AG_GEMM, d);
@@ -500,7 +545,7 @@ dt_status ce_copy_chunk(const Derived& d, const void* const* a_shards, uint8_t* 
   const int64_t rows = std::min<int64_t>(d.Cr, d.Ms - r0);
   const uint8_t* src = reinterpret_cast<const uint8_t*>(a_shards[s]) + r0 * d.lda * 2;
   uint8_t* dst = gather + (static_cast<int64_t>(s) * d.Ms + r0) * d.ld_gather * 2;
-  if (d.lda == d.K)
+  if (d.lda == d.K && d.ld_gather == d.K)  // rows back to back on both sides
     DT_CUDA(cudaMemcpyAsync(dst, src, static_cast<size_t>(rows * d.K * 2), cudaMemcpyDeviceToDevice, st));
   else
     DT_CUDA(cudaMemcpy2DAsync(dst, d.ld_gather * 2, src, d.lda * 2, d.K * 2, rows,
@@ -710,21 +755,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
   p.lda_src = d.lda;
   p.ld_gather = d.ld_gather;
   p.wait_flags = 1;
-  p.row_bytes = d.K * 2;
-  if (p.row_bytes <= kCopyBuf) {
-    p.rows_per_piece = static_cast<int32_t>(kCopyBuf / p.row_bytes);
-    p.segs_per_row = 1;
-  } else {
-    p.rows_per_piece = 0;
-    p.segs_per_row = static_cast<int32_t>(cdiv64(p.row_bytes, kCopyBuf));
-  }
-  auto pieces = [&](int64_t rows) -> int32_t {
-    return p.rows_per_piece > 0 ? static_cast<int32_t>(cdiv64(rows, p.rows_per_piece))
-                                : static_cast<int32_t>(rows * p.segs_per_row);
-  };
-  p.pieces_full = pieces(std::min<int64_t>(d.Cr, d.Ms));
-  p.pieces_last = pieces(d.Ms - static_cast<int64_t>(d.nC - 1) * d.Cr);
-  p.src_rows_contig = d.lda == d.K ? 1 : 0;
+  set_pieces(p, d);
   if ((s = make_tmap(&p.tmA[0], gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
   if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
   p.own_in_place = own_in_place(d) ? 1 : 0;
@@ -746,12 +777,12 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
     PfnWriteValue32 wv = write_value32();
     if (!wv) return fail(DT_ERR_CUDA, "cuStreamWriteValue32 entry point unavailable");
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    DT_CUDA(cudaEventRecord(dev->ev_start, stream));
-    DT_CUDA(cudaStreamWaitEvent(dev->side, dev->ev_start, 0));
+    if ((s = fork_copies(dev, stream)) != DT_OK) return s;
     const int32_t nchunks = d.W * d.nC;
     const int32_t drop = g_drop_transfer;
     g_drop_transfer = -1;
     bool launched = false;
+    int32_t queued = 0;  // chunks queued so far: chunk n goes to copy stream n % kCopyStreams
     for (int32_t tc = 0; tc < nchunks; ++tc) {
       // start the GEMM once the chunks its first tiles need are queued (at once when the own
       // rank's tiles read in place)
@@ -764,19 +795,19 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
       ag_transfer_chunk(d.geom, tc, cs, cj);
       if (p.own_in_place && cs == d.rank) continue;  // read in place
       if (tc == drop) continue;  // the message never arrives: its consumers time out
-      if ((s = ce_copy_chunk(d, a_shards, gather, cs, cj, dev->side)) != DT_OK) return s;
+      cudaStream_t cst = dev->copy[queued++ % kCopyStreams];
+      if ((s = ce_copy_chunk(d, a_shards, gather, cs, cj, cst)) != DT_OK) return s;
+      // the chunk's flag, written by the copy's own stream once the copy is complete
       const CUdeviceptr flag =
           reinterpret_cast<CUdeviceptr>(p.ready + (static_cast<int64_t>(cs) * d.nC + cj));
-      const CUresult r = wv(reinterpret_cast<CUstream>(dev->side), flag, epoch, 0);
+      const CUresult r = wv(reinterpret_cast<CUstream>(cst), flag, epoch, 0);
       if (r != CUDA_SUCCESS) return fail(DT_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)r);
     }
     if (!launched) {
       cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.cl);
       if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
     }
-    DT_CUDA(cudaEventRecord(dev->ev_done, dev->side));
-    DT_CUDA(cudaStreamWaitEvent(stream, dev->ev_done, 0));
-    return DT_OK;
+    return join_copies(dev, stream);
   }
   const int copy = d.backend == DT_XFER_TMA ? kCopyTma : kCopyLdst;
   p.copy_ctas = d.copy_ctas;
@@ -785,6 +816,77 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
   cudaError_t e =
       launch_ag_kernel(p, copy, d.f32, d.copy_ctas ? grid_ded : grid, true, stream, d.cl);
   if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
+  return DT_OK;
+}
+
+dt_status dt_allgather(const void* const* a_shards, void* out, void* ws, size_t ws_bytes,
+                       const dt_args* a, void* stream_) {
+  g_last_error.clear();
+  if (!a) return fail(DT_ERR_INVALID, "args is NULL");
+  // the GEMM's N, B and C play no part: the geometry is derived with a placeholder N
+  dt_args x = *a;
+  x.n = 8;
+  x.ldb = 0;
+  x.ldc = 0;
+  x.out_dtype = DT_BF16;
+  x.tile_m = 0;
+  x.copy_ctas = 0;
+  x.act = DT_ACT_NONE;
+  const int64_t ldo = a->ldc ? a->ldc : a->k;
+  if (a->backend == DT_XFER_AUTO && ldo != a->k) x.backend = DT_XFER_COPY_ENGINE;  // strided rows
+  Derived d;
+  dt_status s = derive(&x, DT_OP_AG_GEMM, &d);
+  if (s != DT_OK) return s;
+  if (!a_shards) return fail(DT_ERR_INVALID, "a_shards is NULL");
+  if (d.M == 0 || d.K == 0) return DT_OK;
+  if (ldo < d.K || ldo % 8)
+    return fail(DT_ERR_INVALID, "out's leading dimension (ldc) must be >= K and a multiple of 8");
+  for (int i = 0; i < d.W; ++i)
+    if (!a_shards[i] || !is_aligned(a_shards[i], 16))
+      return fail(DT_ERR_INVALID, "shard %d is NULL or not 16-byte aligned", i);
+  if (!out || !is_aligned(out, 16)) return fail(DT_ERR_INVALID, "out must be non-NULL and 16-byte aligned");
+  if (d.backend != DT_XFER_COPY_ENGINE && ldo != d.K)
+    return fail(DT_ERR_UNSUPPORTED,
+                "the in-kernel transfers write rows back to back: out's leading dimension must be K");
+  if ((s = check_ws(d, ws, ws_bytes)) != DT_OK) return s;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint8_t* dst = reinterpret_cast<uint8_t*>(out);
+  d.ld_gather = ldo;  // the copies land in `out`
+  DevCtx* dev = nullptr;
+  if ((s = dev_ctx(&dev)) != DT_OK) return s;
+  if (d.backend == DT_XFER_COPY_ENGINE) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if ((s = fork_copies(dev, stream)) != DT_OK) return s;
+    for (int32_t tc = 0; tc < d.W * d.nC; ++tc) {
+      int32_t cs, cj;
+      ag_transfer_chunk(d.geom, tc, cs, cj);
+      if ((s = ce_copy_chunk(d, a_shards, dst, cs, cj, dev->copy[tc % kCopyStreams])) != DT_OK)
+        return s;
+    }
+    return join_copies(dev, stream);
+  }
+  uint32_t epoch = 0;
+  if ((s = prepare_workspace(d, ws, stream, &epoch)) != DT_OK) return s;
+  uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+  KParams p;
+  fill_common(p, d, ws, epoch);
+  p.T = 0;  // no GEMM tiles: every CTA is a transfer CTA
+  for (int i = 0; i < d.W; ++i) p.shard[i] = reinterpret_cast<const uint8_t*>(a_shards[i]);
+  p.gather = dst;
+  p.ready = reinterpret_cast<uint32_t*>(w + d.off_ready);
+  p.pieces_done = reinterpret_cast<uint32_t*>(w + d.off_pieces);
+  p.lda_src = d.lda;
+  p.ld_gather = ldo;
+  p.own_in_place = 0;  // the own shard is copied too
+  set_pieces(p, d);
+  // descriptors the kernel prefetches at start (unused without tiles)
+  if ((s = make_tmap(&p.tmA[0], out, d.K, d.M, ldo * 2, 64, kBM)) != DT_OK) return s;
+  p.tmB[0] = p.tmA[0];
+  const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
+  p.copy_ctas = sms;
+  const int copy = d.backend == DT_XFER_LDST ? kCopyLdst : kCopyTma;
+  cudaError_t e = launch_ag_kernel(p, copy, false, sms, false, stream, 1);
+  if (e != cudaSuccess) return cuda_fail(e, "AllGather launch");
   return DT_OK;
 }
 

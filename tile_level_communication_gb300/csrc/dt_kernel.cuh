@@ -972,9 +972,11 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
 }
 
 // ============================================================================ chunk transfer
+// The piece's writes (bulk stores, complete; or the warp's fenced vector stores) are ordered
+// before the count by the proxy fence and the count's release; the last piece's worker, which
+// acquired every other count, releases the flag.
 __device__ __forceinline__ void signal_piece(const KParams& p, int32_t c, int32_t total) {
   fence_proxy_async_global();
-  __threadfence();
   const uint32_t old = atom_add_acq_rel_gpu(p.pieces_done + c, 1u);
   if (old + 1u == static_cast<uint32_t>(total)) {
     p.pieces_done[c] = 0u;
@@ -1032,24 +1034,57 @@ __device__ __forceinline__ void for_each_piece(const KParams& p, int32_t wid, in
 }
 
 // One TMA bulk-copy worker (one thread): staging buffers `stage` and `stage + kCopyBuf`,
-// completion barriers bar0 / bar1.
+// completion barriers bar0 / bar1.  Piece i is loaded into buffer i & 1 before the worker waits
+// for piece i - 1's load, so a load is always in flight while the previous piece is stored; a
+// piece is counted towards its chunk once its store's writes are complete, which the worker
+// checks one store later.
+struct CopyJob {
+  uint8_t* dst;
+  Piece pc;
+  int32_t c, total;
+};
+
 static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32_t wid, int32_t nw,
                                     uint8_t* stage, uint32_t bar0, uint32_t bar1) {
-  uint32_t k = 0;
-  int32_t prev_c = -1, prev_total = 0;
+  uint32_t issued = 0;  // loads issued
+  uint32_t landed = 0;  // loads waited for (and their pieces stored)
+  CopyJob prev = {};    // the piece of load issued - 1
+  int32_t st_c = -1, st_total = 0;  // the piece stored last, not yet counted
+  auto bar_of = [&](uint32_t i) { return (i & 1u) ? bar1 : bar0; };
+  auto buf_of = [&](uint32_t i) { return smem_u32(stage + (i & 1u) * kCopyBuf); };
+  auto store_piece = [&](uint32_t i, const CopyJob& job) -> bool {
+    if (!wait_bar(p, L, bar_of(i), (i >> 1) & 1u, 500 + (i & 1u))) return false;
+    landed = i + 1;
+    const uint32_t buf = buf_of(i);
+    const uint32_t tot = job.pc.nbytes * static_cast<uint32_t>(job.pc.nr);
+    if (job.pc.nbytes == static_cast<uint32_t>(p.row_bytes) || job.pc.nr == 1) {
+      bulk_s2g(job.dst, buf, tot);  // gather rows are back to back (ld_gather == K)
+    } else {
+      for (int32_t r = 0; r < job.pc.nr; ++r)
+        bulk_s2g(job.dst + static_cast<int64_t>(r) * p.ld_gather * 2, buf + r * job.pc.nbytes,
+                 job.pc.nbytes);
+    }
+    bulk_commit();
+    bulk_wait<1>();  // the previous piece's writes are complete
+    if (st_c >= 0) signal_piece(p, st_c, st_total);
+    st_c = job.c;
+    st_total = job.total;
+    return true;
+  };
   auto stop = [&]() { return *L.abort_flag != 0; };
   for_each_piece(p, wid, nw, stop, [&](int32_t s, int32_t j, int32_t c, int32_t total,
                                        const Piece& pc) -> bool {
     const int64_t row_in_shard = static_cast<int64_t>(j) * p.g.Cr + pc.r0;
     const uint8_t* src = p.shard[s] + row_in_shard * p.lda_src * 2 + pc.boff;
-    uint8_t* dst = p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard) * p.ld_gather * 2 +
-                   pc.boff;
-    const int b = static_cast<int>(k & 1u);
-    const uint32_t buf = smem_u32(stage + b * kCopyBuf);
-    const uint32_t bar = b ? bar1 : bar0;
+    const CopyJob cur = {
+        p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard) * p.ld_gather * 2 + pc.boff,
+        pc, c, total};
+    // buffer issued & 1 was last read by the store of piece issued - 2, the only store that
+    // may still be in flight
+    bulk_wait_read<0>();
+    const uint32_t i = issued;
+    const uint32_t buf = buf_of(i), bar = bar_of(i);
     const uint32_t tot = pc.nbytes * static_cast<uint32_t>(pc.nr);
-    const bool whole = pc.nbytes == static_cast<uint32_t>(p.row_bytes);
-    bulk_wait_read<1>();  // the store that last used this buffer has read it
     mbar_expect_tx(bar, tot);
     if (p.src_rows_contig || pc.nr == 1) {
       bulk_g2s(buf, src, tot, bar);
@@ -1057,23 +1092,20 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32
       for (int32_t r = 0; r < pc.nr; ++r)
         bulk_g2s(buf + r * pc.nbytes, src + static_cast<int64_t>(r) * p.lda_src * 2, pc.nbytes, bar);
     }
-    if (!wait_bar(p, L, bar, (k >> 1) & 1u, 500 + b)) return false;
-    if (whole || pc.nr == 1) {
-      bulk_s2g(dst, buf, tot);  // gather rows are back to back (ld_gather == K)
-    } else {
-      for (int32_t r = 0; r < pc.nr; ++r)
-        bulk_s2g(dst + static_cast<int64_t>(r) * p.ld_gather * 2, buf + r * pc.nbytes, pc.nbytes);
-    }
-    bulk_commit();
-    bulk_wait<1>();  // the previous piece's writes are complete
-    if (prev_c >= 0) signal_piece(p, prev_c, prev_total);
-    prev_c = c;
-    prev_total = total;
-    ++k;
-    return true;
+    ++issued;
+    const bool ok = i == 0 || store_piece(i - 1, prev);
+    prev = cur;
+    return ok;
   });
+  if (!*L.abort_flag && landed < issued) store_piece(issued - 1, prev);
   bulk_wait<0>();
-  if (prev_c >= 0 && !*L.abort_flag) signal_piece(p, prev_c, prev_total);
+  if (!*L.abort_flag && st_c >= 0) signal_piece(p, st_c, st_total);
+  // after an abort, the loads still in flight (at most two) land before the CTA can exit
+  for (uint32_t i = landed; i < issued; ++i) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar_of(i), (i >> 1) & 1u) && globaltimer_ns() - t0 < p.timeout_ns) {
+    }
+  }
 }
 
 // One vector ld/st copy worker (one warp).
@@ -1093,14 +1125,16 @@ static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int 
       uint4* dst = reinterpret_cast<uint4*>(
           p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard + r) * p.ld_gather * 2 +
           pc.boff);
+      // 8 vectors per lane in flight (4 KiB per warp): a copy at HBM rate needs ~32 KiB in
+      // flight per SM
       const int32_t nvec = static_cast<int32_t>(nb >> 4);
-      for (int32_t v = lane; v < nvec; v += 32 * 4) {
-        uint4 x[4];
+      for (int32_t v = lane; v < nvec; v += 32 * 8) {
+        uint4 x[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 8; ++u)
           if (v + u * 32 < nvec) x[u] = __ldg(src + v + u * 32);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 8; ++u)
           if (v + u * 32 < nvec) dst[v + u * 32] = x[u];
       }
     }
