@@ -206,7 +206,11 @@ def a2a_mtile_chunks(i, ms, chunk_rows, bm):
 
 def a2a_order(world_size, ms, n, chunk_rows, bm, bn, swizzle=True, group=8):
     """Tile ids ((q * Tm + i) * W * Tnw + h * Tnw + c) of the GEMM-AllToAll in execution
-    order, all W source ranks interleaved step by step like the ReduceScatter."""
+    order: source rank after source rank, each rank's tiles in its own scatter order
+    (destination q+1 first, its own block last; chunk order inside a destination; grouped
+    raster inside a chunk).  Reading: the pages fix each rank's order only; how W virtual
+    ranks share one GPU is ours, and rank after rank keeps one rank's A_q and B columns in
+    L2 the way separate GPUs would (no result depends on it: each output is one product)."""
     nw, nc, tm, tnw = a2a_geometry(world_size, ms, n, chunk_rows, bm, bn)
     tn = world_size * tnw
     if tm == 0 or tnw == 0:
@@ -221,9 +225,9 @@ def a2a_order(world_size, ms, n, chunk_rows, bm, bn, swizzle=True, group=8):
             band = _bands(keys, group)
             for i in range(tm):
                 for c in range(tnw):
-                    entries.append((keys[i], q, band[i], c, i, h))
+                    entries.append((q, keys[i], band[i], c, i, h))
     entries.sort()
-    return [(q * tm + i) * tn + h * tnw + c for (_, q, _, c, i, h) in entries]
+    return [(q * tm + i) * tn + h * tnw + c for (q, _, _, c, i, h) in entries]
 
 
 def a2a_expected_counts(world_size, ms, n, chunk_rows, bm, bn):

@@ -234,16 +234,16 @@ def test_a2a_order_is_a_bijection(case, swizzle):
 
 @pytest.mark.parametrize("case", GRID)
 def test_a2a_next_rank_first_own_last(case):
-    """Per source rank the destinations come in ring order q+1, q+2, ..., q, and every step
-    d holds exactly one destination per source (the ranks interleave step by step)."""
+    """Per source rank the destinations come in ring order q+1, q+2, ..., q, each
+    destination's tiles together; the source ranks run one after another."""
     w, ms, n, cr, bm, bn = case
     _, nc, tm, tnw = plan.a2a_geometry(w, ms, n, cr, bm, bn)
     order = plan.a2a_order(w, ms, n, cr, bm, bn)
-    step_of = []
+    rank_step = []
     for t in order:
         q, i, h, c = _decode(t, w, tm, tnw)
-        step_of.append((h - q - 1) % w)
-    assert step_of == sorted(step_of)
+        rank_step.append((q, (h - q - 1) % w))
+    assert rank_step == sorted(rank_step)
     for q in range(w):
         dests = [_decode(t, w, tm, tnw)[2] for t in order if _decode(t, w, tm, tnw)[0] == q]
         firsts = [d for idx, d in enumerate(dests) if idx == 0 or dests[idx - 1] != d]
@@ -252,7 +252,7 @@ def test_a2a_next_rank_first_own_last(case):
 
 @pytest.mark.parametrize("case", GRID)
 def test_a2a_chunks_complete_in_order(case):
-    """Inside one step a source's chunks complete in ascending chunk order: the last tile of
+    """Inside one destination a source's chunks complete in ascending chunk order: the last tile of
     chunk j comes no later than the last tile of chunk j+1 (AutoOverlap section 5.4)."""
     w, ms, n, cr, bm, bn = case
     _, nc, tm, tnw = plan.a2a_geometry(w, ms, n, cr, bm, bn)
