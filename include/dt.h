@@ -198,7 +198,8 @@ dt_status dt_gemm_ar(const void* const* a, const void* const* b, void* const* ou
  *   out : host array of W device pointers, out_h [M x N/W] (out_dtype), ld = ldc (0 = N/W)
  * Requires N % W == 0 and (N/W) % 8 == 0.  Column tiles never cross a destination's block;
  * every tile's epilogue stores its rows straight into out_h (push, scatter mode: rank q
- * computes destination q+1's block first and its own last, chunk by chunk in row order) and
+ * computes destination q+1's block first and its own last, chunk by chunk in row order; the
+ * W virtual source ranks run one after another) and
  * counts itself on chunk (h, q, j) = rows [j*chunk_rows, ..) of source q; the count's last
  * tile releases that chunk's ready flag (notify).  Results do not depend on the order, chunk
  * size or group width (each output is one product).  Workspace:

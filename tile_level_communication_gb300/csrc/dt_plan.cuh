@@ -19,7 +19,9 @@
 //       order = sort (q, i, n) by (key, q, band, n, i)
 //   A2A (GEMM-AllToAll, rows local to each rank, columns split by destination h):
 //       key(q, i, h) = dpos_q(h)*nC + (first chunk of m-tile i);
-//       order = sort (q, i, h, c) by (key, q, band, c, i)
+//       order = sort (q, i, h, c) by (q, key, band, c, i): the virtual source ranks one after
+//       another, each in its own scatter order (each output is one product, so nothing but
+//       L2 reuse depends on how they interleave: one rank's A_q and B columns stay in L2)
 // Evaluation here does not sort.  Along the m-tiles rotated to start at the first m-tile of
 // the own rank (AG) or of rank q+1 (RS) the key never decreases, so the key of an m-tile is
 // read off one row of it, and the number of m-tiles with a smaller key is a binary search.
@@ -188,7 +190,8 @@ DT_HD int64_t rs_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
 // mod W (rank q+1 first, its own block last), and inside one destination its chunks in row
 // order.  The key of m-tile i is dpos*nC + (first chunk it writes), so for one (q, d) the
 // m-tiles keyed j are exactly those whose first row lies in chunk j: [first_mtile(j),
-// first_mtile(j+1)).  Every (q, d) holds Tm m-tiles and all W ranks share the group sizes.
+// first_mtile(j+1)).  Every (q, d) holds Tm m-tiles x Tnw column tiles; rank q's tiles fill
+// positions [q*Tm*Tn, (q+1)*Tm*Tn).
 DT_HD int32_t a2a_first_mtile(const Geom& g, int32_t j) {
   const int64_t t = cdiv64(static_cast<int64_t>(j) * g.Cr, g.BM);
   return static_cast<int32_t>(t < g.Tm ? t : g.Tm);
@@ -202,8 +205,8 @@ DT_HD int64_t a2a_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
   const int32_t j = static_cast<int32_t>(static_cast<int64_t>(i) * g.BM / g.Cr);
   const int32_t ug = a2a_first_mtile(g, j);
   const int32_t ue = a2a_first_mtile(g, j + 1);
-  return static_cast<int64_t>(g.W) * g.Tnw * (static_cast<int64_t>(d) * g.Tm + ug) +
-         static_cast<int64_t>(q) * (ue - ug) * g.Tnw + band_offset(ug, ue, i, c, g.Tnw, g.G);
+  return static_cast<int64_t>(g.Tnw) * g.Tm * (static_cast<int64_t>(q) * g.W + d) +
+         static_cast<int64_t>(g.Tnw) * ug + band_offset(ug, ue, i, c, g.Tnw, g.G);
 }
 // stores counted on chunk j of one (destination, source) pair: the bm-row tiles (one CTA's
 // rows) whose rows touch it, times Tnw
