@@ -37,19 +37,19 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 # DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
 # kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "386d5ed2b1b86eac", "points": {
-        "1024/8/256": 6.278112e9 + 2.002142e9,     # --set full capture
-        "1024/4/256": 6349637632 + 2001186304,     # dram metrics only
-        "1024/16/256": 6412386816 + 2001429248,    # dram metrics only
+    "rs_w8_m8192_n8192_k3584": {"csrc": "fb69fc9f27987ca0", "points": {
+        "1024/8/256": 8.794246e9 + 2.015441e9,     # --set full capture
+        "1024/4/256": 8603513088 + 2015194112,     # dram metrics only
+        "1024/16/256": 8666231296 + 2015441408,    # dram metrics only
         # chunks of 512 / 256 rows: two / one pair m-tiles per chunk, the same order at every
         # group width (dram metrics only)
-        "512/4/256": 10003929600 + 2006697984, "512/8/256": 10003929600 + 2006697984,
-        "512/16/256": 10003929600 + 2006697984,
-        "256/4/256": 17727164928 + 2020683264, "256/8/256": 17727164928 + 2020683264,
-        "256/16/256": 17727164928 + 2020683264,
+        "512/4/256": 10215056640 + 2007790848, "512/8/256": 10215056640 + 2007790848,
+        "512/16/256": 10215056640 + 2007790848,
+        "256/4/256": 17989725184 + 2024065536, "256/8/256": 17989725184 + 2024065536,
+        "256/16/256": 17989725184 + 2024065536,
     }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "386d5ed2b1b86eac", "points": {
-        "256/8/256": 657.1712e6 + 168.678144e6,    # --set full capture, TMA transfer
+    "ag_w8_m8192_n3584_k8192": {"csrc": "fb69fc9f27987ca0", "points": {
+        "256/8/256": 693.589248e6 + 168.359168e6,  # --set full capture, TMA transfer
     }},
 }
 
