@@ -119,6 +119,20 @@ def test_per_rank_b_parity(dt):
         assert_close(to_f64(o), ref[h], "f32", f"out_{h}")
 
 
+@pytest.mark.parametrize("tile_m", [128, 256, 512])
+def test_sixteen_ranks_tiny_blocks(dt, tile_m):
+    # the largest world size: 9 rows per rank, 16 columns per destination, K not a multiple of 8
+    inp = make_a2a_inputs(16, 16 * 9, 16 * 16, 20, seed=44)
+    ref = reference.gemm_a2a(*_f64(inp))
+    a = [dev_bf16(x, 24) for x in inp.a]
+    b0 = dev_bf16(inp.b[0])
+    for swizzle in (True, False):
+        outs, _, _ = _run(dt, inp, 16 * 9, 16 * 16, 20, "f32", chunk_rows=4, lda=24,
+                          dev=(a, [b0] * 16), tile_m=tile_m, swizzle=swizzle)
+        for h, o in enumerate(outs):
+            assert_close(to_f64(o), ref[h], "f32", f"out_{h}")
+
+
 def test_w1_is_a_plain_gemm(dt):
     inp = make_a2a_inputs(1, 257, 264, 200, seed=42)
     ref = reference.gemm_a2a(*_f64(inp))

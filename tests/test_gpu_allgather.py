@@ -2,7 +2,7 @@
 ABI) against the oracle's row concatenation: a copy, so bit for bit.
 
 Every backend (copy engine, in-kernel TMA bulk copies, in-kernel vector ld/st) over world sizes
-1, 3 and 8, ragged chunks (1 row, 96 rows, 1000 rows against 300-row shards), padded source
+1, 3, 8 and 16, ragged chunks (1 row, 96 rows, 1000 rows against 300-row shards), padded source
 rows, padded destination rows (copy engine; the padding stays untouched), few SMs, swizzle off
 and a nonzero rank; then the FFN pair's shards (W = 8, 1024 x 8192 each) on every backend.
 """
@@ -39,7 +39,7 @@ def _gather(dt, shards_dev, m, k, ldc=0, **kw):
 
 
 CASES = [  # (W, Ms, K)
-    (1, 300, 136), (3, 300, 520), (8, 128, 8192 + 64),
+    (1, 300, 136), (3, 300, 520), (8, 128, 8192 + 64), (16, 9, 64),
 ]
 
 
