@@ -75,7 +75,8 @@ PfnWriteValue32 write_value32() {
 // rows `row_stride_bytes` apart; boxes of box_inner x box_outer elements.
 dt_status make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
-                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   PfnEncodeTiled enc = encode_tiled();
   if (!enc) return fail(DT_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const cuuint64_t dims[2] = {inner, outer};
@@ -84,7 +85,7 @@ dt_status make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t 
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(tm, dtype, 2, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(DT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %llu x %llu, stride %llu",
@@ -981,6 +982,18 @@ static dt_status rs_params(KParams& p, const Derived& d, const void* const* a_,
     if (st != DT_OK) return st;
   } else {
     p.tmPark = p.tmAcc;  // one rank never parks
+  }
+  // the final sums go out as 32 x 128 boxes: bf16 boxes are dense 64-byte rows, fp32 boxes
+  // keep the running sums' swizzled layout
+  const CUtensorMapDataType odt =
+      d.f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle oswz = d.f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const uint64_t orow_bytes = static_cast<uint64_t>(d.ldc) * (d.f32 ? 4 : 2);
+  const int nout = p.ar_copies > 0 ? p.ar_copies : d.W;
+  for (int q = 0; q < nout; ++q) {
+    const dt_status s = make_tmap(&p.tmOut[q], out[q], d.N, p.ar_copies > 0 ? d.M : d.Ms,
+                                  orow_bytes, 32, kBM, odt, oswz);
+    if (s != DT_OK) return s;
   }
   for (int q = 0; q < d.W; ++q) {
     p.out[q] = out[q];

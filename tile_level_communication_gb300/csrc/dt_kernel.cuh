@@ -81,6 +81,8 @@ struct KParams {
   CUtensorMap tmB[kMaxW];  // AG: [0] = B; RS / A2A: B_q
   CUtensorMap tmAcc;       // RS: running sums, fp32 [M][N], 32 x 128 boxes
   CUtensorMap tmPark;      // RS: park slots, fp32 [W (W-1) M/W][N], 32 x 128 boxes
+  CUtensorMap tmOut[kMaxW];  // RS: out[s]; AR: out[r]; 32 x 128 boxes (bf16 dense rows, or
+                             // fp32 in the running sums' 128-byte-swizzled layout)
   const uint8_t* shard[kMaxW];
   void* out[kMaxW];        // AG: out[0] = C; RS: out[s] ([M/W][N]); AR: out[r] ([M][N]);
                            // A2A: out[h] ([M][N/W]), or the ranks' own Y_q in the baseline
@@ -844,25 +846,39 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
             a[4 * c + 3] = x.w + a[4 * c + 3];
           }
         }
-        if (last) {
+        if (last && !F32) {
+          // the final sum, rounded to bf16, as dense 64-byte rows of the box once every thread
+          // has read its running-sum row out of the same buffer
+          named_bar_sync(1, 128);
+          uint4* orow = reinterpret_cast<uint4*>(buf + r * 64);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            if (c0 + u * 8 < p.g.N) {
-              float o[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] = a[u * 8 + e];
-              store_out8<F32>(p, t_s, t_lr0 + r, c0 + u * 8, o);
-            }
+            uint4 w;
+            w.x = pack_bf16x2(__float_as_uint(a[8 * u + 0]), __float_as_uint(a[8 * u + 1]));
+            w.y = pack_bf16x2(__float_as_uint(a[8 * u + 2]), __float_as_uint(a[8 * u + 3]));
+            w.z = pack_bf16x2(__float_as_uint(a[8 * u + 4]), __float_as_uint(a[8 * u + 5]));
+            w.w = pack_bf16x2(__float_as_uint(a[8 * u + 6]), __float_as_uint(a[8 * u + 7]));
+            orow[u] = w;
           }
         } else {
+          // the running sum (or the fp32 final sum) in the box's swizzled layout
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             rowp[c ^ (r & 7)] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
-          fence_proxy_async_smem();
         }
+        fence_proxy_async_smem();
         named_bar_sync(1, 128);
-        if (et == 0 && !last) {
-          tma_store_2d(store_map, smem_u32(buf), static_cast<int32_t>(c0), store_y);
+        if (et == 0) {
+          if (!last) {
+            tma_store_2d(store_map, smem_u32(buf), static_cast<int32_t>(c0), store_y);
+          } else {
+            // one TMA store per output: out_s (ReduceScatter), every rank's copy (AllReduce)
+            const int ncopy = p.ar_copies > 0 ? p.ar_copies : 1;
+            const int32_t oy = static_cast<int32_t>(p.ar_copies > 0 ? ti.row0 : t_lr0);
+            for (int cp = 0; cp < ncopy; ++cp)
+              tma_store_2d(&p.tmOut[p.ar_copies > 0 ? cp : t_s], smem_u32(buf),
+                           static_cast<int32_t>(c0), oy);
+          }
           bulk_commit();
         }
         ++stage_ctr;
