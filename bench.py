@@ -37,19 +37,19 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 # DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
 # kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "fb69fc9f27987ca0", "points": {
-        "1024/8/256": 8.794246e9 + 2.015441e9,     # --set full capture
-        "1024/4/256": 8603513088 + 2015194112,     # dram metrics only
-        "1024/16/256": 8666231296 + 2015441408,    # dram metrics only
+    "rs_w8_m8192_n8192_k3584": {"csrc": "e05a1df3319b9a9b", "points": {
+        "1024/8/256": 9.73036e9 + 2.019329e9,      # --set full capture
+        "1024/4/256": 9660946688 + 2018318080,     # dram metrics only
+        "1024/16/256": 9815673600 + 2017504512,    # dram metrics only
         # chunks of 512 / 256 rows: two / one pair m-tiles per chunk, the same order at every
         # group width (dram metrics only)
-        "512/4/256": 10215056640 + 2007790848, "512/8/256": 10215056640 + 2007790848,
-        "512/16/256": 10215056640 + 2007790848,
-        "256/4/256": 17989725184 + 2024065536, "256/8/256": 17989725184 + 2024065536,
-        "256/16/256": 17989725184 + 2024065536,
+        "512/4/256": 10523545344 + 2014522624, "512/8/256": 10523545344 + 2014522624,
+        "512/16/256": 10523545344 + 2014522624,
+        "256/4/256": 17615243008 + 2023023616, "256/8/256": 17615243008 + 2023023616,
+        "256/16/256": 17615243008 + 2023023616,
     }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "fb69fc9f27987ca0", "points": {
-        "256/8/256": 693.589248e6 + 168.359168e6,  # --set full capture, TMA transfer
+    "ag_w8_m8192_n3584_k8192": {"csrc": "e05a1df3319b9a9b", "points": {
+        "256/8/256": 706.54592e6 + 168.447232e6,   # --set full capture, TMA transfer
     }},
 }
 
