@@ -552,7 +552,8 @@ def main():
     def run_call(cl, fused=True):
         if cl["op"] == "ag":
             fn = dt.ag_gemm if fused else dt.ag_gemm_kernel_overlap
-            fn(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], cl["args"])
+            fn(cl["shards"], cl["b"], cl["outs"][0], cl["ws"],
+               cl["args"] if fused else cl.get("base_args", cl["args"]))
         elif cl["op"] == "rs":
             fn = dt.gemm_rs if fused else dt.gemm_rs_kernel_overlap
             fn(cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"])
@@ -710,7 +711,28 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) / k
 
-    # kernel-level-overlap baseline: same GEMM kernel, per-chunk / per-destination launches
+    # kernel-level-overlap baseline: same GEMM kernel, per-chunk / per-destination launches.
+    # Its AllGather launches one GEMM per chunk, so it runs at its own best chunk size rather
+    # than the fused kernel's.
+    base_chunks = {}
+    for cl in calls:
+        if cl["op"] != "ag":
+            continue
+        ms_rank = cl["wl"].m // cl["wl"].world_size
+        best = None
+        for cr in sorted({int(cl["args"].chunk_rows), 256, 512, 1024, 2048, ms_rank}):
+            if cr > ms_rank:
+                continue
+            a = dt.DtArgs.from_buffer_copy(cl["args"])
+            a.chunk_rows = cr
+            if dt.workspace_size(a, dt.OP_AG) > cl["ws"].numel():
+                continue
+            cl["base_args"] = a
+            t = timed(lambda: run_call(cl, fused=False), 3)
+            if best is None or t < best[0]:
+                best = (t, a)
+        cl["base_args"] = best[1]
+        base_chunks[cl["op"]] = int(best[1].chunk_rows)
     ms_b = timed(lambda: [run_call(cl, fused=False) for cl in calls], k_side)
     for cl in calls:
         st, info = dt.check(cl["ws"])
@@ -718,7 +740,8 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
             raise RuntimeError(f"baseline device error {info}")
     out["kernel_overlap_baseline"] = {
         "value": flops_step / (ms_b * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_b,
-        "fused_speedup": ms_b / (flops_step / (value / world * 1e12) * 1e3)}
+        "fused_speedup": ms_b / (flops_step / (value / world * 1e12) * 1e3),
+        "chunk_rows": base_chunks or None}
 
     # the copy path on its own: the AllGather's chunk transfer of every shard into one [M, K]
     # buffer, per backend; 2 x bytes (read + write) over the time, against the measured HBM

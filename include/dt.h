@@ -344,9 +344,12 @@ typedef struct dt_tune_point {
  * dedicated CTAs}; then group widths {4, 8, 16} at the best point.  Scatter-mode candidates
  * (dt_tune_reduce with op DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A): chunk rows x group
  * widths {4, 8, 16}.  Each candidate runs once as
- * warm-up and `reps` times timed with CUDA events on `stream` (synchronising), in a forward
- * and again in a reverse pass over the candidates, keeping its faster time (the GPU slows as
- * it warms under the power cap); candidates whose workspace exceeds ws_bytes are skipped.  The
+ * warm-up and `reps` times timed with CUDA events on `stream` (synchronising).  A forward
+ * pass times every candidate and takes the fastest as the reference; a reverse pass times each
+ * other candidate between two timings of the reference and scores it by its time over their
+ * mean (the GPU's clock drifts as it warms under the power cap; the ratio cancels the drift);
+ * a point's reported ms is its score times the reference's median time.  Candidates whose
+ * workspace exceeds ws_bytes are skipped.  The
  * fastest knobs are written into *a (chunk_rows, backend, copy_ctas, group; swizzle stays on).  `points` (may be NULL) receives
  * up to max_points candidates and *n_points their number.  The inputs are read and the
  * outputs written by every candidate; all candidates give bit-identical outputs. */

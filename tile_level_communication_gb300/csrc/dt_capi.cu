@@ -1290,22 +1290,50 @@ void tune_one(const TuneCtx& t, dt_args& cand, int op, Call&& call, dt_tune_poin
   pt->status = st;
 }
 
-// Time every candidate twice, once in a forward and once in a reverse pass, and keep each
-// one's faster time: under the power cap the GPU slows down as it warms, which would favour
-// whatever is timed first.
+// Under the power cap the GPU's clock drifts as it warms, which would favour whatever is timed
+// first.  A forward pass times every candidate and picks the fastest as the reference; a
+// reverse pass then times each candidate between two timings of the reference and scores it
+// by its time over the mean of those two, which cancels the drift.  A point's reported time is
+// its score times the median of the reference's timings.
 template <typename Call>
 std::vector<dt_tune_point> tune_all(const TuneCtx& t, std::vector<dt_args>& cands, int op,
                                     Call&& call) {
   std::vector<dt_tune_point> pts(cands.size());
   const int n = static_cast<int>(cands.size());
-  for (int i = 0; i < n; ++i) tune_one(t, cands[i], op, call, &pts[i]);
-  for (int i = n - 1; i >= 0; --i) {
-    if (pts[i].status != DT_OK) continue;
+  int ref = -1;
+  for (int i = 0; i < n; ++i) {
+    tune_one(t, cands[i], op, call, &pts[i]);
+    if (pts[i].status == DT_OK && pts[i].ms >= 0 && (ref < 0 || pts[i].ms < pts[ref].ms)) ref = i;
+  }
+  if (ref < 0 || n < 2) return pts;
+  std::vector<float> ref_ms;
+  auto time_ref = [&]() -> float {
+    dt_tune_point r;
+    tune_one(t, cands[ref], op, call, &r);
+    if (r.status == DT_OK && r.ms > 0) ref_ms.push_back(r.ms);
+    return r.status == DT_OK ? r.ms : -1.0f;
+  };
+  std::vector<float> score(n, -1.0f);
+  score[ref] = 1.0f;
+  float before = time_ref();
+  for (int i = n - 1; i >= 0 && before > 0; --i) {
+    if (i == ref || pts[i].status != DT_OK) continue;
     dt_tune_point again;
     tune_one(t, cands[i], op, call, &again);
-    if (again.status != DT_OK) pts[i] = again;
-    else if (again.ms >= 0 && again.ms < pts[i].ms) pts[i].ms = again.ms;
+    const float after = time_ref();
+    if (again.status != DT_OK) {
+      pts[i] = again;
+    } else if (after > 0 && again.ms >= 0) {
+      score[i] = again.ms / (0.5f * (before + after));
+    }
+    if (after <= 0) break;
+    before = after;
   }
+  if (ref_ms.empty()) return pts;
+  std::sort(ref_ms.begin(), ref_ms.end());
+  const float ref_med = ref_ms[ref_ms.size() / 2];
+  for (int i = 0; i < n; ++i)
+    if (pts[i].status == DT_OK && score[i] > 0) pts[i].ms = score[i] * ref_med;
   return pts;
 }
 
