@@ -488,7 +488,7 @@ def main():
                 probe = dt.make_args(w, wl.m, w * fr, wl.k, chunk_rows=64)
                 ws_ag = torch.zeros(max(dt.workspace_size(a_ag, dt.OP_AG),
                                         dt.workspace_size(probe, dt.OP_AG)), dtype=torch.uint8, device=dev)
-                calls.append(dict(op="ag", wl=ag_wl, args=a_ag, ins=x + [w1], shards=x, b=w1, outs=[h],
+                calls.append(dict(op="ag", wl=ag_wl, args=a_ag, ins=x + [w1], acts=x, shards=x, b=w1, outs=[h],
                                   ws=ws_ag, act=wl.act))
                 w2 = [up(t) for t in inp.w2]
                 a_rs = dt.make_args(w, wl.m, wl.n, fr, chunk_rows=cr, lda=w * fr,
@@ -498,7 +498,7 @@ def main():
                                         dt.workspace_size(probe, dt.OP_RS)), dtype=torch.uint8, device=dev)
                 outs = [torch.empty((wl.m // w, wl.n), dtype=torch.bfloat16, device=dev)
                         for _ in range(w)]
-                calls.append(dict(op="rs", wl=rs_wl, args=a_rs, ins=w2,
+                calls.append(dict(op="rs", wl=rs_wl, args=a_rs, ins=w2, acts=[],
                                   A=[h[:, q * fr:(q + 1) * fr] for q in range(w)], B=w2, outs=outs,
                                   ws=ws_rs))
                 in_bytes += sum(t.numel() * 2 for t in x + [w1] + w2)
@@ -513,7 +513,7 @@ def main():
                 probe = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=64)
                 need = max(dt.workspace_size(a, dt.OP_AG), dt.workspace_size(probe, dt.OP_AG))
                 ws = torch.zeros(need, dtype=torch.uint8, device=dev)
-                calls.append(dict(op="ag", wl=wl, args=a, ins=shards + [b], shards=shards, b=b,
+                calls.append(dict(op="ag", wl=wl, args=a, ins=shards + [b], acts=shards, shards=shards, b=b,
                                   outs=[c], ws=ws))
             elif wl.op == "a2a":
                 w = wl.world_size
@@ -528,7 +528,7 @@ def main():
                 probe = dt.make_args(w, wl.m, wl.n, wl.k, chunk_rows=64)
                 need = max(dt.workspace_size(a, dt.OP_A2A), dt.workspace_size(probe, dt.OP_A2A))
                 ws = torch.zeros(need, dtype=torch.uint8, device=dev)
-                calls.append(dict(op="a2a", wl=wl, args=a, ins=A + [b], A=A, B=[b] * w, outs=outs,
+                calls.append(dict(op="a2a", wl=wl, args=a, ins=A + [b], acts=A, A=A, B=[b] * w, outs=outs,
                                   y=y, ws=ws))
             else:
                 a = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=cr,
@@ -542,7 +542,7 @@ def main():
                 probe = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=64)
                 need = max(dt.workspace_size(a, op_id), dt.workspace_size(probe, op_id))
                 ws = torch.zeros(need, dtype=torch.uint8, device=dev)
-                calls.append(dict(op=wl.op, wl=wl, args=a, ins=A + B, A=A, B=B, outs=outs, ws=ws))
+                calls.append(dict(op=wl.op, wl=wl, args=a, ins=A + B, acts=A, A=A, B=B, outs=outs, ws=ws))
             in_bytes += sum(t.numel() * 2 for t in calls[-1]["ins"])
             out_bytes += sum(t.numel() * 2 for t in calls[-1]["outs"])
         return calls, in_bytes, out_bytes
@@ -858,7 +858,12 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     pairs_out = [[(d_, h_) for cl, hs in zip(sets[k], host_out[k])
                   for d_, h_ in zip(cl["outs"], hs)] for k in range(2)]
 
-    def e2e_steps(n):
+    # the same with the weights resident in HBM: only the activations cross the link each step
+    pairs_act = [[(d_, h_) for cl, hs in zip(sets[k], host_in) for d_, h_ in zip(cl["ins"], hs)
+                  if any(d_ is x for x in cl["acts"])] for k in range(2)]
+    act_bytes = sum(d_.numel() * d_.element_size() for d_, _ in pairs_act[0])
+
+    def e2e_steps(n, pairs_in=pairs_in):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         e0.record(s_main)
@@ -895,6 +900,7 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     e2e_steps(2)  # warm-up (second set's tile orders, pinned pages)
     n_e = max(4, min(args.steps, 20))
     ms_e = e2e_steps(n_e) / n_e
+    ms_act = e2e_steps(n_e, pairs_act) / n_e
     for st in sets:
         for cl in st:
             code, info = dt.check(cl["ws"])
@@ -939,7 +945,13 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
                   "link": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
                            "floor_ms_per_step": floor_ms, "frac_of_floor": floor_ms / ms_e,
                            "note": "floor = the larger of the step's input bytes at the measured "
-                                   "pinned host-to-device rate and the device step time"}}
+                                   "pinned host-to-device rate and the device step time"},
+                  "weights_resident": {
+                      "value": world * flops_step / (ms_act * 1e-3) / 1e12, "ms_per_step": ms_act,
+                      "h2d_bytes_per_step": act_bytes, "d2h_bytes_per_step": out_bytes,
+                      "floor_ms_per_step": max(act_bytes / (h2d_gbs * 1e9) * 1e3, ms_dev),
+                      "note": "the weights (B, B_q, W1, W2) stay in HBM; the activations are "
+                              "copied in and the outputs out every step"}}
 
     # the CPU oracle on a bounded sample (rank 0, N=1 only)
     if world == 1:
