@@ -34,8 +34,12 @@ Tn = ceil(N/BN); group width G (default 8).
 * ReduceScatter, swizzle on: source rank q sends to s in the order
   dpos_q(s) = (s - q - 1) mod W (next rank first, its own block last).
   key(q, i) = min over the chunks (s, j) that m-tile i writes of
-  dpos_q(s) * nC + j.  Tiles (q, i, n) sorted by (key, q, band, n, i), band taken
-  among the m-tiles of the same (q, key).
+  dpos_q(s) * nC + j.  Tiles (q, i, n) sorted by (q, key, band, n, i), band taken
+  among the m-tiles of the same (q, key): the virtual source ranks run one after
+  another, each in its own scatter order.  The pages fix only one rank's order;
+  rank after rank is how W ranks that each own an SM array run on one GPU (one
+  rank's B_q stays in L2 for all its send steps), and each destination then
+  receives its partials in source order q = 0, 1, ..., W-1.
 * ReduceScatter, swizzle off: lexicographic (q, i, n).
 * ReduceScatter arrivals: a unit is the part of chunk (s, j) that m-tile i covers, times
   column tile n (AutoOverlap section 4.1: a chunk is made of compute tiles; the reduction
@@ -165,9 +169,9 @@ def rs_order(world_size, m, n, chunk_rows, bm, bn, swizzle=True, group=8):
         band = _bands(keys, group)
         for i in range(tm):
             for c in range(tn):
-                entries.append((keys[i], q, band[i], c, i))
+                entries.append((q, keys[i], band[i], c, i))
     entries.sort()
-    return [(q * tm + i) * tn + c for (_, q, _, c, i) in entries]
+    return [(q * tm + i) * tn + c for (q, _, _, c, i) in entries]
 
 
 def rs_expected_arrivals(world_size, m, n, chunk_rows, bm, bn):

@@ -154,17 +154,33 @@ def test_scatter_next_rank_first_own_last(case):
 
 
 @pytest.mark.parametrize("case", GRID)
-def test_scatter_steps_interleave_ranks(case):
-    """Within one send step all ranks' tiles are interleaved: the key sequence is
-    non-decreasing along the order and, at equal key, the source ranks ascend."""
+def test_scatter_ranks_one_after_another(case):
+    """The virtual source ranks run one after another (q ascending) and, inside one
+    rank, the send keys never decrease."""
     w, m, n, cr, bm, bn = case
     ms, nc, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
     keys = {q: plan.rs_keys(w, q, m, cr, bm) for q in range(w)}
     seq = []
     for t in plan.rs_order(w, m, n, cr, bm, bn, True):
         q, i = t // (tm * tn), (t // tn) % tm
-        seq.append((keys[q][i], q))
+        seq.append((q, keys[q][i]))
     assert seq == sorted(seq)
+
+
+@pytest.mark.parametrize("case", GRID)
+@pytest.mark.parametrize("swizzle", [True, False])
+def test_scatter_units_receive_sources_in_rank_order(case, swizzle):
+    """Executed one tile at a time, every reduction unit receives its W partials from
+    sources 0, 1, ..., W-1 in that order, the order in which they are summed."""
+    w, m, n, cr, bm, bn = case
+    ms, nc, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    seen = {}
+    for t in plan.rs_order(w, m, n, cr, bm, bn, swizzle):
+        q, i, c = t // (tm * tn), (t // tn) % tm, t % tn
+        for u in {plan.chunk_of_row(g, ms, cr) for g in _rows_of_mtile(i, m, bm)}:
+            got = seen.setdefault((i, u, c), [])
+            assert len(got) == q
+            got.append(q)
 
 
 @pytest.mark.parametrize("case", GRID)
@@ -232,9 +248,43 @@ def _mut_ag_order_min_key(w, r, m, n, cr, bm, bn, swizzle=True, group=8):
     return [i * tn + c for (_, c, i) in ent]
 
 
-@pytest.mark.parametrize("mutant", [_mut_ag_order_negative_offset, _mut_ag_order_min_key])
-def test_plan_pins_catch_planted_mistakes(mutant, monkeypatch):
-    monkeypatch.setattr(plan, "ag_order", mutant)
+_ORIG_RS_ORDER = plan.rs_order
+
+
+def _mut_rs_order_ranks_interleaved(w, m, n, cr, bm, bn, swizzle=True, group=8):
+    """Steps interleaved across ranks (key before q) instead of rank after rank."""
+    _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    ent = []
+    for q in range(w):
+        keys = plan.rs_keys(w, q, m, cr, bm)
+        for i in range(tm):
+            for c in range(tn):
+                ent.append((keys[i], q, c, i))
+    ent.sort()
+    return [(q * tm + i) * tn + c for (_, q, c, i) in ent]
+
+
+def _mut_rs_order_own_first(w, m, n, cr, bm, bn, swizzle=True, group=8):
+    """Each rank keeps its own block first (dpos = (s - q) mod W)."""
+    _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    ms = m // w
+    nc = plan.cdiv(ms, cr)
+    ent = []
+    for q in range(w):
+        for i in range(tm):
+            key = min(((s - q) % w) * nc + j for (s, j) in plan.tile_chunks(i, m, ms, cr, bm))
+            for c in range(tn):
+                ent.append((q, key, c, i))
+    ent.sort()
+    return [(q * tm + i) * tn + c for (q, _, c, i) in ent]
+
+
+@pytest.mark.parametrize("name,mutant", [("ag_order", _mut_ag_order_negative_offset),
+                                         ("ag_order", _mut_ag_order_min_key),
+                                         ("rs_order", _mut_rs_order_ranks_interleaved),
+                                         ("rs_order", _mut_rs_order_own_first)])
+def test_plan_pins_catch_planted_mistakes(name, mutant, monkeypatch):
+    monkeypatch.setattr(plan, name, mutant)
     caught = False
     for fn in (test_golden_rank_offset_orders, test_golden_nonperfect_tiling):
         try:
