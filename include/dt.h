@@ -27,7 +27,8 @@
  *     vectorised loads/stores (AutoOverlap page, Table 2 / Fig. 7);
  *   - GEMM-ReduceScatter: a reduction unit is the part of a chunk that one m-tile covers,
  *     times one column tile; its W partial tiles are folded into an fp32 running sum in the
- *     fixed order q = s-1, s-2, ..., s (the scatter schedule's own order; a partial that
+ *     fixed source order q = 0, 1, ..., W-1 (the order the schedule produces them: the
+ *     virtual ranks run one after another, each in its own scatter order; a partial that
  *     arrives early waits in a park slot) and rounded once, so results do not depend on
  *     tile order, chunk size or backend.
  *
@@ -167,8 +168,10 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c,
  *   b   : host array of W device pointers, B_q [K x N] bf16, ld = ldb
  *   out : host array of W device pointers, out_s [M/W x N] (out_dtype), ld = ldc
  * Every tile (q, i, n) is one partial product.  For each unit (rows of m-tile i inside one
- * chunk, column tile n) the partials are folded in the fixed order d = 0..W-1, partial d from
- * source q = (s - d - 1) mod W: a tile whose partial is next in order adds it to the fp32
+ * chunk, column tile n) the partials are folded in the fixed source order q = 0..W-1 (the
+ * virtual ranks run one after another, each sending to rank q+1 first and keeping its own
+ * block for last, so each unit receives them in that order): a tile whose partial is next
+ * in order adds it to the fp32
  * running sum (the last one rounds into out_s); one that arrives early parks it, and whoever
  * advances the unit past it folds it (notify through one atomic word per unit; nobody
  * waits).  DITRON page section 3.2 "Scatter模式"; Triton-distributed talk, notify/wait of

@@ -391,8 +391,8 @@ __global__ void zero_rows_kernel(uint8_t* dst, int64_t rows, int64_t row_bytes, 
   }
 }
 
-// out_s = the fp32 partial slots recv[s][q] summed in the fused path's fixed order: source
-// q_d = (s - d - 1) mod W for d = 0..W-1 (rank s-1 first, s itself last)
+// out_s = the fp32 partial slots recv[s][q] summed in the fused path's fixed source order
+// q = 0..W-1
 struct OutRows {
   void* p[DT_MAX_WORLD];  // ReduceScatter: out_s; AllReduce: every rank's output
   int32_t n;
@@ -408,9 +408,8 @@ __global__ void reduce_slots_kernel(const float* recv, int32_t W, int64_t Ms, in
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = e / nv, v = e - r * nv;
     const float* src = base + r * N + v * 4;
-    float4 acc = __ldcg(reinterpret_cast<const float4*>(src + ((s - 1 + W) % W) * slot));
-    for (int32_t d = 1; d < W; ++d) {
-      const int32_t q = (s - d - 1 + 2 * W) % W;
+    float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
+    for (int32_t q = 1; q < W; ++q) {
       const float4 x = __ldcg(reinterpret_cast<const float4*>(src + q * slot));
       acc.x += x.x;
       acc.y += x.y;

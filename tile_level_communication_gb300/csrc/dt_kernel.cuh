@@ -539,16 +539,18 @@ __device__ __forceinline__ float4 ldcg_f4(const float* p) {
 
 // ---------------------------------------------------------------------------- RS folding
 // A ReduceScatter unit is (the rows of m-tile i inside one chunk of destination s) x column
-// tile n.  Its W partials are summed in a fixed order d = 0..W-1, partial d coming from source
-// rank q_d = (s - d - 1) mod W: the order in which the scatter schedule produces them (rank
-// s-1 first, the destination's own partial last).  The running fp32 sum S_d = S_{d-1} + P_{q_d}
-// lives in `acc` ([M][N], global rows); S_{W-1} is rounded once into out_s.  A partial that is
+// tile n.  Its W partials are summed in the fixed source order d = q = 0..W-1: the order in
+// which the schedule produces them (the virtual ranks run one after another, each in its own
+// scatter order).  The running fp32 sum S_d = S_{d-1} + P_d lives in `acc` ([M][N], global
+// rows); S_{W-1} is rounded once into out_s.  A partial that is
 // ready before its predecessors are folded waits in park slot (s, d).  One 32-bit word per unit
 // holds the number of partials folded so far (bits 0-7) and which ones are parked (bit 8+d);
 // whoever moves the count to d, or parks d after the count reached d, folds d: exactly one
 // tile does, and nobody waits.
 __device__ __forceinline__ int32_t fold_index(int32_t s, int32_t q, int32_t W) {
-  return (s - q - 1 + 2 * W) % W;
+  (void)s;
+  (void)W;
+  return q;
 }
 __device__ __forceinline__ float* acc_ptr(const KParams& p, int64_t row, int64_t col) {
   return p.recv + row * p.g.N + col;

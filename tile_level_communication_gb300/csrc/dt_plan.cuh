@@ -16,7 +16,9 @@
 //   AG: pos(s, j) = ((s - r) mod W) * nC + j;  key(i) = max pos of the chunks m-tile i reads;
 //       order = sort (i, n) by (key(i), band(i), n, i)
 //   RS: dpos_q(s) = (s - q - 1) mod W;  key(q, i) = min over written chunks of dpos*nC + j;
-//       order = sort (q, i, n) by (key, q, band, n, i)
+//       order = sort (q, i, n) by (q, key, band, n, i): the virtual source ranks one after
+//       another, each in its own scatter order, so every destination receives its partials
+//       in source order q = 0 .. W-1 and one rank's B_q stays in L2 for all its send steps
 //   A2A (GEMM-AllToAll, rows local to each rank, columns split by destination h):
 //       key(q, i, h) = dpos_q(h)*nC + (first chunk of m-tile i);
 //       order = sort (q, i, h, c) by (q, key, band, c, i): the virtual source ranks one after
@@ -173,16 +175,9 @@ DT_HD int64_t rs_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
   const int32_t rot0 = rs_rot0(g, q);
   const int32_t u = (i - rot0 + g.Tm) % g.Tm;
   const int32_t k = rs_key(g, q, rot0, u);
-  int64_t before = 0;  // m-tiles of all ranks placed before this (q, key) group
-  for (int32_t qq = 0; qq < g.W; ++qq) {
-    const int32_t r0 = rs_rot0(g, qq);
-    const int32_t below = rs_count_below(g, qq, r0, k);
-    before += below;
-    if (qq < q) before += rs_count_below(g, qq, r0, k + 1) - below;
-  }
   const int32_t ug = rs_count_below(g, q, rot0, k);
   const int32_t ue = rs_count_below(g, q, rot0, k + 1);
-  return before * g.Tn + band_offset(ug, ue, u, n, g.Tn, g.G);
+  return (static_cast<int64_t>(q) * g.Tm + ug) * g.Tn + band_offset(ug, ue, u, n, g.Tn, g.G);
 }
 
 // ------------------------------------------------------------------ all-to-all (GEMM-AllToAll)
