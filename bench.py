@@ -96,8 +96,9 @@ def parse():
     ap.add_argument("--no-swizzle", action="store_true")
     ap.add_argument("--group", type=int, default=0, help="m-tiles per band of the in-chunk "
                     "raster (0 = the library's 8; fixed, not tuned, when given)")
-    ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256],
-                    help="tile rows: 128 (one CTA), 256 (a CTA pair), 0 = the library's choice")
+    ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256, 512],
+                    help="tile rows: 128 (one CTA), 256 (a CTA pair), 512 (two pairs sharing B), "
+                         "0 = the library's choice")
     ap.add_argument("--rank-view", type=int, default=0, help="AllGather rank whose view is computed")
     ap.add_argument("--skip-extras", action="store_true",
                     help="skip the baselines, e2e, CPU oracle and clock sampling")
