@@ -218,13 +218,14 @@ def test_full_size_sampled(dt, name, backend, chunk):
     assert torch.isfinite(c.float()).all()
 
 
+# dedicated CTAs come in whole clusters: a multiple of tile_m / 128
+_DEDICATED = [(c, t) for c in (1, 8, 16) for t in (128, 256, 512) if c % (t // 128) == 0]
+
+
 @pytest.mark.parametrize("backend", ["tma", "ldst"])
-@pytest.mark.parametrize("copy_ctas", [1, 8, 16])
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("copy_ctas,tile_m", _DEDICATED)
 def test_dedicated_transfer_ctas(dt, small, ragged, backend, copy_ctas, tile_m):
     """CTAs that only move chunks (dedicated SMs) give the same bits as co-located warps."""
-    if copy_ctas % (tile_m // 128):
-        pytest.skip("dedicated CTAs come in whole clusters")
     for wl, inp, ref in (small, ragged):
         base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows, backend=backend, rank=1,
                     tile_m=tile_m)
