@@ -108,6 +108,10 @@ def parse():
                     help="AllGather chunk x backend x swizzle sweep of --workload (default: the "
                          "largest AllGather); one JSON line per point")
     ap.add_argument("--sweep-chunks", default="64,128,256,512,2048")
+    ap.add_argument("--allgather-only", action="store_true",
+                    help="time the AllGather's chunk transfer alone (dt_allgather) on the shards "
+                         "of --workload's AllGather, per backend (or --backend), L2 flushed by "
+                         "reading before each call; one JSON line per backend")
     ap.add_argument("--ffn-crossover", action="store_true",
                     help="time the feed-forward block in AllGather+ReduceScatter form and in "
                          "AllReduce form over a range of token counts M (one JSON line per M)")
@@ -449,6 +453,53 @@ def run_ffn_crossover(args):
     return 0
 
 
+def run_allgather_only(args):
+    """The copy path alone: every shard of the AllGather's workload gathered into one [M, K]
+    buffer by dt_allgather; 2 x bytes (read + write) over the time per call."""
+    import statistics
+
+    import torch
+
+    import tile_level_communication_gb300 as dt
+    ag = [wl for wl in workload_ops(args.workload) if wl.op in ("ag", "ffn")]
+    if not ag:
+        raise SystemExit("--allgather-only takes a workload with an AllGather")
+    wl = ag[0]
+    inp = wl.make()
+    up = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    shards = [up(x) for x in (inp.x_shards if wl.op == "ffn" else inp.shards)]
+    m, k = sum(t.shape[0] for t in shards), shards[0].shape[1]
+    out = torch.empty((m, k), dtype=torch.bfloat16, device="cuda")
+    flush = torch.zeros(2 * L2_BYTES // 8, dtype=torch.int64, device="cuda")
+    hbm = peaks()["hbm_gbs"]
+    cr = args.chunk_rows or wl.chunk_rows
+    for be in ([args.backend] if args.backend != "auto" else ["copy_engine", "tma", "ldst"]):
+        a = dt.make_args(wl.world_size, m, 8, k, chunk_rows=cr, backend=be)
+        ws = torch.zeros(dt.workspace_size(a, dt.OP_AG), dtype=torch.uint8, device="cuda")
+        for _ in range(max(3, args.warmup)):
+            dt.allgather(shards, out, ws, a)
+        times = []
+        for _ in range(args.steps):
+            torch.amax(flush)  # reads twice L2's size: evicts the shards, leaves clean lines
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dt.allgather(shards, out, ws, a)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        st, info = dt.check(ws)
+        if st != 0:
+            raise RuntimeError(f"AllGather device error {info}")
+        if not torch.equal(out.view(torch.int16), torch.cat(shards).view(torch.int16)):
+            raise RuntimeError("AllGather result differs from the shards")
+        ms = statistics.median(times)
+        gbs = 2 * m * k * 2 / (ms * 1e-3) / 1e9
+        print(json.dumps({"allgather": wl.name, "bytes": m * k * 2, "chunk_rows": cr,
+                          "backend": be, "ms": ms, "gbs": gbs, "frac_of_hbm_copy": gbs / hbm}),
+              flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- fused arm
 def main():
     args = parse()
@@ -458,6 +509,8 @@ def main():
         return run_sweep(args)
     if args.ffn_crossover:
         return run_ffn_crossover(args)
+    if args.allgather_only:
+        return run_allgather_only(args)
     import torch
 
     import tile_level_communication_gb300 as dt
