@@ -53,6 +53,18 @@ NCU_TRAFFIC = {
         "128/16/256": 5969986560 + 2005768704,
         "64/4/256": 5301320192 + 2003131648, "64/8/256": 5301320192 + 2003131648,
         "64/16/256": 5301320192 + 2003131648,
+        # 512-row tiles (two CTA pairs sharing B), every group width the same order (dram
+        # metrics only)
+        "1024/4/512": 5535062016 + 2000622336, "1024/8/512": 5535062016 + 2000622336,
+        "1024/16/512": 5535062016 + 2000622336,
+        "512/4/512": 5679610624 + 2002911744, "512/8/512": 5679610624 + 2002911744,
+        "512/16/512": 5679610624 + 2002911744,
+        "256/4/512": 5714238464 + 2002917888, "256/8/512": 5714238464 + 2002917888,
+        "256/16/512": 5714238464 + 2002917888,
+        "128/4/512": 5667729152 + 2003435264, "128/8/512": 5667729152 + 2003435264,
+        "128/16/512": 5667729152 + 2003435264,
+        "64/4/512": 5032781056 + 2001794304, "64/8/512": 5032781056 + 2001794304,
+        "64/16/512": 5032781056 + 2001794304,
     }},
     "ag_w8_m8192_n3584_k8192": {"csrc": "ea0d680da8286dbb", "points": {
         "256/8/256": 692.992512e6 + 168.30976e6,   # --set full capture, TMA transfer
@@ -645,7 +657,7 @@ def main():
             tuned[cl["op"]] = {"chunk_rows": int(a.chunk_rows),
                                "backend": [k for k, v in dt.BACKENDS.items() if v == a.backend][0],
                                "copy_ctas": int(a.copy_ctas), "group": int(a.group),
-                               "candidates": len(pts)}
+                               "tile_m": int(a.tile_m), "candidates": len(pts)}
 
     # warm-up (also writes each workspace's tile order once)
     for _ in range(max(3, args.warmup)):

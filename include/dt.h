@@ -335,9 +335,13 @@ typedef struct dt_tune_point {
   int32_t copy_ctas;
   int32_t swizzle;
   int32_t group;
+  int32_t tile_m;     /* tile rows as requested (0 = the library's choice) */
   float ms;
   int32_t status;     /* dt_status of the candidate's calls      */
 } dt_tune_point;
+
+/* sizeof(dt_tune_point) as compiled into the library, for bindings to check their mirror. */
+size_t dt_sizeof_tune_point(void);
 
 /* Enumerate-and-measure tuner (AutoOverlap page, section 6: the inter-chunk tuner picks chunk
  * size / split factor, the intra-chunk tuner the transfer backend, the SMs given to
@@ -346,14 +350,17 @@ typedef struct dt_tune_point {
  * stays <= 512), TMA and ld/st with co-located transfer warps, TMA and ld/st on 8 or 16
  * dedicated CTAs}; then group widths {4, 8, 16} at the best point.  Scatter-mode candidates
  * (dt_tune_reduce with op DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A): chunk rows x group
- * widths {4, 8, 16}.  Each candidate runs once as
+ * widths {4, 8, 16}, and for DT_OP_GEMM_RS / DT_OP_GEMM_AR x tile rows {as given, 512 (two CTA
+ * pairs sharing B)} when the problem has at least 38 tiles of 512 rows (one per four SMs).
+ * Each candidate runs once as
  * warm-up and `reps` times timed with CUDA events on `stream` (synchronising).  A forward
  * pass times every candidate and takes the fastest as the reference; a reverse pass times each
  * other candidate between two timings of the reference and scores it by its time over their
  * mean (the GPU's clock drifts as it warms under the power cap; the ratio cancels the drift);
  * a point's reported ms is its score times the reference's median time.  Candidates whose
  * workspace exceeds ws_bytes are skipped.  The
- * fastest knobs are written into *a (chunk_rows, backend, copy_ctas, group; swizzle stays on).  `points` (may be NULL) receives
+ * fastest knobs are written into *a (chunk_rows, backend, copy_ctas, group, tile_m; swizzle
+ * stays on).  `points` (may be NULL) receives
  * up to max_points candidates and *n_points their number.  The inputs are read and the
  * outputs written by every candidate; all candidates give bit-identical outputs. */
 dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, void* workspace,

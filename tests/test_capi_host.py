@@ -44,6 +44,7 @@ def test_library_exports_every_declared_symbol(dt):
 
 def test_args_layout_matches(dt):
     assert dt.capi.lib().dt_sizeof_args() == ctypes.sizeof(dt.capi.DtArgs)
+    assert dt.capi.lib().dt_sizeof_tune_point() == ctypes.sizeof(dt.capi.DtTunePoint)
     assert dt.capi.lib().dt_version() >= 100
 
 

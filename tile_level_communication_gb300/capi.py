@@ -30,6 +30,7 @@ _SIGS = {
     "dt_args_default": (None, [_P]),
     "dt_version": (ctypes.c_int, []),
     "dt_sizeof_args": (ctypes.c_size_t, []),
+    "dt_sizeof_tune_point": (ctypes.c_size_t, []),
     "dt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dt_last_error": (ctypes.c_char_p, []),
     "dt_workspace_size": (ctypes.c_size_t, [_P, ctypes.c_int]),
@@ -80,7 +81,8 @@ class DtTunePoint(ctypes.Structure):
     """Mirror of ``dt_tune_point``."""
     _fields_ = [("chunk_rows", ctypes.c_int64), ("backend", ctypes.c_int32),
                 ("copy_ctas", ctypes.c_int32), ("swizzle", ctypes.c_int32),
-                ("group", ctypes.c_int32), ("ms", ctypes.c_float), ("status", ctypes.c_int32)]
+                ("group", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("ms", ctypes.c_float),
+                ("status", ctypes.c_int32)]
 
 
 class DtError(RuntimeError):
@@ -107,6 +109,8 @@ def lib():
             fn.argtypes = argt
         if h.dt_sizeof_args() != ctypes.sizeof(DtArgs):
             raise RuntimeError("dt_args layout mismatch between libdt.so and the binding")
+        if h.dt_sizeof_tune_point() != ctypes.sizeof(DtTunePoint):
+            raise RuntimeError("dt_tune_point layout mismatch between libdt.so and the binding")
         _lib = h
     return _lib
 
@@ -310,7 +314,7 @@ _BACKEND_NAMES = {v: k for k, v in BACKENDS.items()}
 def _points(buf, n):
     return [dict(chunk_rows=int(p.chunk_rows), backend=_BACKEND_NAMES.get(p.backend, p.backend),
                  copy_ctas=int(p.copy_ctas), swizzle=bool(p.swizzle), group=int(p.group),
-                 ms=float(p.ms), status=int(p.status)) for p in buf[:n]]
+                 tile_m=int(p.tile_m), ms=float(p.ms), status=int(p.status)) for p in buf[:n]]
 
 
 def tune_ag_gemm(shards, b, c, workspace, args: DtArgs, reps: int = 3, stream=None,

@@ -646,9 +646,10 @@ void dt_args_default(dt_args* a) {
   a->chunk_rows = 128;
 }
 
-int dt_version(void) { return 100; }
+int dt_version(void) { return 200; }  // 2.0.0: dt_tune_point carries tile_m
 
 size_t dt_sizeof_args(void) { return sizeof(dt_args); }
+size_t dt_sizeof_tune_point(void) { return sizeof(dt_tune_point); }
 
 const char* dt_status_string(dt_status s) {
   switch (s) {
@@ -1268,6 +1269,7 @@ void tune_one(const TuneCtx& t, dt_args& cand, int op, Call&& call, dt_tune_poin
   pt->copy_ctas = cand.copy_ctas;
   pt->swizzle = cand.swizzle;
   pt->group = cand.group;
+  pt->tile_m = cand.tile_m;
   pt->ms = -1.0f;
   const size_t need = dt_workspace_size(&cand, op);
   if (need == 0 || need > t.ws_bytes) {
@@ -1378,6 +1380,7 @@ dt_status tune_finish(std::vector<dt_tune_point>& pts, dt_args* a, dt_tune_point
   a->copy_ctas = pts[best].copy_ctas;
   a->swizzle = pts[best].swizzle;
   a->group = pts[best].group;
+  a->tile_m = pts[best].tile_m;
   return DT_OK;
 }
 
@@ -1455,14 +1458,23 @@ dt_status dt_tune_reduce(int op, const void* const* a_, const void* const* b_, v
     return op == DT_OP_GEMM_RS ? dt_gemm_rs(a_, b_, out, ws, ws_bytes, &cand, stream)
                                : dt_gemm_ar(a_, b_, out, ws, ws_bytes, &cand, stream);
   };
+  // tile rows: as given, and for the ReduceScatter / AllReduce also 512 (two CTA pairs sharing
+  // B: a quarter fewer operand bytes from L2) when that still gives every four SMs a tile
+  std::vector<int32_t> tiles = {a->tile_m};
+  if (op != DT_OP_GEMM_A2A && a->tile_m != 4 * kBM &&
+      static_cast<int64_t>(d.W) * cdiv64(d.M, 4 * kBM) * cdiv64(d.N, kBN) >= 38)
+    tiles.push_back(4 * kBM);
   std::vector<dt_args> cands;
-  for (int64_t cr : chunk_candidates(d.Ms)) {
-    for (int g : {4, 8, 16}) {
-      dt_args cand = *a;
-      cand.chunk_rows = cr;
-      cand.swizzle = 1;
-      cand.group = g;
-      cands.push_back(cand);
+  for (int32_t tm : tiles) {
+    for (int64_t cr : chunk_candidates(d.Ms)) {
+      for (int g : {4, 8, 16}) {
+        dt_args cand = *a;
+        cand.chunk_rows = cr;
+        cand.swizzle = 1;
+        cand.group = g;
+        cand.tile_m = tm;
+        cands.push_back(cand);
+      }
     }
   }
   std::vector<dt_tune_point> pts = tune_all(t, cands, op, call);
