@@ -65,7 +65,7 @@ extern "C" {
 typedef enum {
   DT_OK = 0,
   DT_ERR_INVALID = 1,      /* bad argument (message: dt_last_error())                    */
-  DT_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement                 */
+  DT_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement               */
   DT_ERR_TIMEOUT = 3,      /* a bounded device wait ran out (from dt_check)               */
   DT_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed                         */
   DT_ERR_WORKSPACE = 5     /* workspace missing, misaligned or smaller than required      */
