@@ -15,6 +15,7 @@ replica (weak scaling); there is no data-path collective.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -681,6 +682,7 @@ def main():
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(pg)
     torch.cuda.synchronize(dev)
+    gc.disable()  # a collector pause on the host would leave the GPU idle (as timeit does)
     w0 = time.time()
     ev0.record(stream)
     for s in range(args.steps):
@@ -691,6 +693,7 @@ def main():
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     w1 = time.time()
+    gc.enable()
     barrier(pg)
     if sampler:
         sampler.stop()
@@ -949,6 +952,7 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     def e2e_steps(n, pairs_in=pairs_in):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
+        gc.disable()  # the host enqueues only a few steps ahead: a collector pause idles the GPU
         e0.record(s_main)
         for st in s_h2d:
             st.wait_event(e0)
@@ -978,6 +982,7 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
                 s_main.wait_event(ev)
         e1.record(s_main)
         torch.cuda.synchronize(dev)
+        gc.enable()
         return e0.elapsed_time(e1)
 
     e2e_steps(2)  # warm-up (second set's tile orders, pinned pages)
