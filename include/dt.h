@@ -236,8 +236,9 @@ dt_status dt_ffn_ag_rs(const void* const* x_shards, const void* w1, const void* 
                        size_t ws_rs_bytes, const dt_args* ag, const dt_args* rs, void* stream);
 
 /* AllGather alone: the chunk transfer of dt_ag_gemm without the GEMM (Triton-distributed
- * talk, "AllGather" producer side; TileLink page, section 3.2, tile-level pull of remote
- * chunks).  out = concat_rows(A_0, .., A_{W-1}), [M x K] bf16 with leading dimension
+ * talk, "AllGather" producer side; AutoOverlap page, section 4: a P2P op defined at the
+ * destination pulls a chunk; DITRON page, section 3.1: device-level chunks move by DMA-style
+ * getmem).  out = concat_rows(A_0, .., A_{W-1}), [M x K] bf16 with leading dimension
  * a->ldc (0 = K); every shard, the own one included, is copied chunk by chunk (chunk_rows
  * rows, ragged last chunk) in the AllGather's transfer order (own rank first when swizzle is
  * on, then rank+1, ..).  Backends:
