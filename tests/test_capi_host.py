@@ -88,6 +88,20 @@ def test_workspace_errors(dt):
     assert dt.workspace_size(r, dt.OP_RS) >= 4 * 4 * 512 * 4096 * 4
 
 
+@pytest.mark.parametrize("op", ["OP_RS", "OP_AR"])
+@pytest.mark.parametrize("case", [(8, 8192, 8192, 3584), (4, 2048, 4096, 2048), (6, 6000, 5120, 3000),
+                                  (2, 6, 8, 8)])
+def test_reduce_workspace_does_not_grow_with_tile_rows(dt, op, case):
+    """The reduce tuner sizes one workspace for the library's tile rows and also tries 512-row
+    tiles in it: a larger tile needs no more workspace (only the tile order shrinks)."""
+    w, m, n, k = case
+    for cr in (1, 64, 256, 1024):
+        sizes = [dt.workspace_size(dt.make_args(w, m, n, k, chunk_rows=cr, tile_m=t),
+                                   getattr(dt, op)) for t in (128, 256, 512)]
+        assert sizes[0] >= sizes[1] >= sizes[2] > 0
+        assert dt.workspace_size(dt.make_args(w, m, n, k, chunk_rows=cr), getattr(dt, op)) >= sizes[2]
+
+
 # ----------------------------------------------------------------------------- plan parity
 
 PLAN_GRID = [
