@@ -329,14 +329,17 @@ dt_status dev_ctx(DevCtx** out) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DevCtx& c = g_dev[dev];
   if (c.sms == 0) {
-    DT_CUDA(cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev));
-    DT_CUDA(cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking));
+    // sms is set last: a set-up that fails part way is redone by the next call
+    int sms = 0;
+    DT_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (!c.side) DT_CUDA(cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking));
     for (int i = 0; i < kCopyStreams; ++i) {
-      DT_CUDA(cudaStreamCreateWithFlags(&c.copy[i], cudaStreamNonBlocking));
-      DT_CUDA(cudaEventCreateWithFlags(&c.copy_done[i], cudaEventDisableTiming));
+      if (!c.copy[i]) DT_CUDA(cudaStreamCreateWithFlags(&c.copy[i], cudaStreamNonBlocking));
+      if (!c.copy_done[i]) DT_CUDA(cudaEventCreateWithFlags(&c.copy_done[i], cudaEventDisableTiming));
     }
-    DT_CUDA(cudaEventCreateWithFlags(&c.ev_start, cudaEventDisableTiming));
-    DT_CUDA(cudaEventCreateWithFlags(&c.ev_done, cudaEventDisableTiming));
+    if (!c.ev_start) DT_CUDA(cudaEventCreateWithFlags(&c.ev_start, cudaEventDisableTiming));
+    if (!c.ev_done) DT_CUDA(cudaEventCreateWithFlags(&c.ev_done, cudaEventDisableTiming));
+    c.sms = sms;
   }
   *out = &c;
   return DT_OK;
