@@ -41,3 +41,23 @@ def test_reference_arm_names_the_default_workload():
     d = _run_reference("--steps", "1", "--warmup", "0")
     assert d["config"]["workload"].startswith("llama70b_like_tp8_ffn_pair")
     assert set(d["config"]) >= {"ag", "rs"}
+
+
+def test_traffic_table_covers_every_reduce_tuner_candidate():
+    """The roofline's DRAM traffic of the benchmark's dominant launch (the FFN pair's
+    ReduceScatter) is looked up by the tuned knobs: every candidate the reduce tuner can pick
+    (chunk rows 64 .. M/W, group widths 4 / 8 / 16, tile rows 256 or 512) has an entry."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    from synth_inputs import WORKLOADS
+    wl = WORKLOADS[bench.FFN_PAIR[1]]
+    ms = wl.m // wl.world_size
+    chunks = [c for c in (64, 128, 256, 512, 1024, 2048, 4096) if c < ms] + [ms]
+    points = bench.NCU_TRAFFIC[wl.name]["points"]
+    for cr in chunks:
+        for g in (4, 8, 16):
+            for t in (256, 512):
+                key = f"{cr}/{g}/{t}"
+                assert key in points, key
+                assert points[key] > 0
