@@ -5,8 +5,10 @@ One step is one pass of the whole hot path over one batch of synthetic input: th
 Llama-70B-like tensor-parallel (W=8) FFN pair -- a fused AllGather-GEMM (gathered M=8192,
 K=8192, N=3584; chunk transfer, ready flags, swizzled persistent tcgen05 GEMM) followed by
 a fused GEMM-ReduceScatter over all 8 virtual ranks (M=8192, K=3584 per rank, N=8192;
-swizzled GEMM, fp32 scatter epilogue, last-arriver fixed-order reduction).  Other
-workloads: --workload <name> from synth_inputs.WORKLOADS (one operation per step).
+the ranks one after another in their scatter order, each tile's fp32 partial folded into its
+unit's running sum in source order).  Other workloads: --workload <name> from
+synth_inputs.WORKLOADS (one operation per step); --allgather-only times the chunk transfer
+alone; --sweep and --ffn-crossover print one line per point.
 
 Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle on a bounded
 row sample of the same workload instead.  Under torchrun every GPU runs an independent
