@@ -35,12 +35,14 @@ from synth_inputs import WORKLOADS, f64_from_bf16_bits  # noqa: E402
 
 METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU)"
 
-# DRAM bytes (read + write) per launch of the fused kernel, from one `ncu --set full` capture
-# of the named workload (profiles/), valid only for the kernel sources it was taken on.
-# DRAM bytes (read + write) of one launch of the dominant kernel, from `ncu` captures of these
-# kernel sources (csrc hash) at the knobs "chunk_rows/group/tile_rows"; see profiles/
+# Recorded DRAM bytes (read + write) of one launch of the dominant kernel: figures copied from
+# earlier `ncu` captures (the profile named beside each workload), not measured by this run.
+# They hold only for the kernel sources they were taken on (csrc hash) and the knobs
+# "chunk_rows/group/tile_rows"; otherwise the roofline's traffic is null.
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "ea0d680da8286dbb", "points": {
+    "rs_w8_m8192_n8192_k3584": {"csrc": "ea0d680da8286dbb",
+                                "profile": "profiles/fused_gemm_rs_w8_m8192_n8192_k3584.md",
+                                "points": {
         "1024/8/256": 6.454941e9 + 2.010043e9,     # --set full capture
         # with 1024-row chunks a destination block is 4 pair m-tiles, so groups 4, 8 and 16
         # give the same tile order as group 8
@@ -56,20 +58,10 @@ NCU_TRAFFIC = {
         "128/16/256": 5969986560 + 2005768704,
         "64/4/256": 5301320192 + 2003131648, "64/8/256": 5301320192 + 2003131648,
         "64/16/256": 5301320192 + 2003131648,
-        # 512-row tiles (two CTA pairs sharing B), every group width the same order (dram
-        # metrics only)
-        "1024/4/512": 5535062016 + 2000622336, "1024/8/512": 5535062016 + 2000622336,
-        "1024/16/512": 5535062016 + 2000622336,
-        "512/4/512": 5679610624 + 2002911744, "512/8/512": 5679610624 + 2002911744,
-        "512/16/512": 5679610624 + 2002911744,
-        "256/4/512": 5714238464 + 2002917888, "256/8/512": 5714238464 + 2002917888,
-        "256/16/512": 5714238464 + 2002917888,
-        "128/4/512": 5667729152 + 2003435264, "128/8/512": 5667729152 + 2003435264,
-        "128/16/512": 5667729152 + 2003435264,
-        "64/4/512": 5032781056 + 2001794304, "64/8/512": 5032781056 + 2001794304,
-        "64/16/512": 5032781056 + 2001794304,
     }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "ea0d680da8286dbb", "points": {
+    "ag_w8_m8192_n3584_k8192": {"csrc": "ea0d680da8286dbb",
+                                "profile": "profiles/fused_gemm_ag_w8_m8192_n3584_k8192.md",
+                                "points": {
         "256/8/256": 692.992512e6 + 168.30976e6,   # --set full capture, TMA transfer
     }},
 }
@@ -111,9 +103,8 @@ def parse():
     ap.add_argument("--no-swizzle", action="store_true")
     ap.add_argument("--group", type=int, default=0, help="m-tiles per band of the in-chunk "
                     "raster (0 = the library's 8; fixed, not tuned, when given)")
-    ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256, 512],
-                    help="tile rows: 128 (one CTA), 256 (a CTA pair), 512 (two pairs sharing B), "
-                         "0 = the library's choice")
+    ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256],
+                    help="tile rows: 128 (one CTA), 256 (a CTA pair), 0 = the library's choice")
     ap.add_argument("--rank-view", type=int, default=0, help="AllGather rank whose view is computed")
     ap.add_argument("--skip-extras", action="store_true",
                     help="skip the baselines, e2e, CPU oracle and clock sampling")
@@ -751,6 +742,9 @@ def main():
         "achieved": dom_achieved, "peak": peak, "unit": "TFLOP/s", "frac": dom_achieved / peak,
         "regime": regime,
         "traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read + write)",
+        "traffic_source": (f"recorded ncu capture of these kernel sources ({tr['profile']}), not "
+                           "measured in this run" if traffic is not None else
+                           "none recorded for these kernel sources and knobs"),
         "knobs": knob_key,
         "peak_source": (f"{pk['source']} bf16 sustained (cuBLAS back to back for seconds, under the "
                         f"power cap): the timed region ran {w1 - w0:.2f} s"

@@ -97,9 +97,7 @@ typedef struct dt_args {
   int32_t out_dtype;   /* dt_dtype of C / out_s                                            */
   int32_t tile_m;      /* rows of a tile: 128 (one CTA, tcgen05 cta_group::1), 256 (a cluster
                           of two CTAs on two SMs, cta_group::2: each stages 128 rows of A and
-                          half of the 256 columns of B, 6-7 pipeline stages), 512 (a cluster
-                          of two such pairs on the same columns: each CTA loads one of its two
-                          B slabs and multicasts it to its counterpart in the other pair),
+                          half of the 256 columns of B, 6-7 pipeline stages),
                           0 = 256 when that leaves at least 76 tiles (one per SM pair) and
                           copy_ctas is even, else 128; copy_ctas must be a multiple of
                           tile_m / 128                                                      */
@@ -351,9 +349,7 @@ size_t dt_sizeof_tune_point(void);
  * stays <= 512), TMA and ld/st with co-located transfer warps, TMA and ld/st on 8 or 16
  * dedicated CTAs}; then group widths {4, 8, 16} at the best point.  Scatter-mode candidates
  * (dt_tune_reduce with op DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A): chunk rows x group
- * widths {4, 8, 16}, and for DT_OP_GEMM_RS / DT_OP_GEMM_AR x tile rows {as given, 512 (two CTA
- * pairs sharing B)} when the problem has at least 38 tiles of 512 rows (one per four SMs).
- * Each candidate runs once as
+ * widths {4, 8, 16}, at the tile rows given.  Each candidate runs once as
  * warm-up and `reps` times timed with CUDA events on `stream` (synchronising).  A forward
  * pass times every candidate and takes the fastest as the reference; a reverse pass times each
  * other candidate between two timings of the reference and scores it by its time over their

@@ -46,7 +46,8 @@ def test_reference_arm_names_the_default_workload():
 def test_traffic_table_covers_every_reduce_tuner_candidate():
     """The roofline's DRAM traffic of the benchmark's dominant launch (the FFN pair's
     ReduceScatter) is looked up by the tuned knobs: every candidate the reduce tuner can pick
-    (chunk rows 64 .. M/W, group widths 4 / 8 / 16, tile rows 256 or 512) has an entry."""
+    (chunk rows 64 .. M/W, group widths 4 / 8 / 16, at the library's 256-row tiles) has an
+    entry, and each workload names the profile its figures come from."""
     import sys
     sys.path.insert(0, ROOT)
     import bench
@@ -57,7 +58,8 @@ def test_traffic_table_covers_every_reduce_tuner_candidate():
     points = bench.NCU_TRAFFIC[wl.name]["points"]
     for cr in chunks:
         for g in (4, 8, 16):
-            for t in (256, 512):
-                key = f"{cr}/{g}/{t}"
-                assert key in points, key
-                assert points[key] > 0
+            key = f"{cr}/{g}/256"
+            assert key in points, key
+            assert points[key] > 0
+    for entry in bench.NCU_TRAFFIC.values():
+        assert os.path.exists(os.path.join(ROOT, entry["profile"])), entry["profile"]

@@ -92,14 +92,16 @@ def test_workspace_errors(dt):
 @pytest.mark.parametrize("case", [(8, 8192, 8192, 3584), (4, 2048, 4096, 2048), (6, 6000, 5120, 3000),
                                   (2, 6, 8, 8)])
 def test_reduce_workspace_does_not_grow_with_tile_rows(dt, op, case):
-    """The reduce tuner sizes one workspace for the library's tile rows and also tries 512-row
-    tiles in it: a larger tile needs no more workspace (only the tile order shrinks)."""
+    """A larger tile needs no more workspace (only the tile order shrinks), and 512-row tiles
+    are not built."""
     w, m, n, k = case
     for cr in (1, 64, 256, 1024):
         sizes = [dt.workspace_size(dt.make_args(w, m, n, k, chunk_rows=cr, tile_m=t),
-                                   getattr(dt, op)) for t in (128, 256, 512)]
-        assert sizes[0] >= sizes[1] >= sizes[2] > 0
-        assert dt.workspace_size(dt.make_args(w, m, n, k, chunk_rows=cr), getattr(dt, op)) >= sizes[2]
+                                   getattr(dt, op)) for t in (128, 256)]
+        assert sizes[0] >= sizes[1] > 0
+        assert dt.workspace_size(dt.make_args(w, m, n, k, chunk_rows=cr), getattr(dt, op)) >= sizes[1]
+        with pytest.raises(dt.DtError, match="not built"):
+            dt.workspace_size(dt.make_args(w, m, n, k, chunk_rows=cr, tile_m=512), getattr(dt, op))
 
 
 # ----------------------------------------------------------------------------- plan parity
@@ -114,9 +116,8 @@ PLAN_GRID = [
 ]
 
 
-# the order's tile rows: one CTA (128), a CTA pair (256) or two pairs (512); the oracle takes
-# them as BM
-TILE_M = [128, 256, 512]
+# the order's tile rows: one CTA (128) or a CTA pair (256); the oracle takes them as BM
+TILE_M = [128, 256]
 
 
 @pytest.mark.parametrize("case", PLAN_GRID)
@@ -209,7 +210,7 @@ def test_host_plan_a2a_random_sweep(dt):
         nw = 8 * int(rng.integers(1, 90))
         cr = int(rng.integers(1, 2 * ms + 2))
         g = int(rng.integers(1, 10))
-        bm = 128 * int(rng.choice([1, 2, 4]))
+        bm = 128 * int(rng.choice([1, 2]))
         a = dt.make_args(w, w * ms, w * nw, 8, chunk_rows=cr, group=g, tile_m=bm)
         assert dt.swizzle_plan(a, dt.OP_A2A).tolist() == \
             oplan.a2a_order(w, ms, w * nw, cr, bm, 256, True, g)

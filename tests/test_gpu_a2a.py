@@ -67,7 +67,7 @@ def small():
 
 
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_small_parity_and_padding_untouched(dt, small, out_dtype, tile_m):
     wl, inp, ref = small
     nw = wl.n // wl.world_size
@@ -87,8 +87,7 @@ def test_small_bit_identical_across_orders_chunks_groups_and_baseline(dt, small)
                 dict(chunk_rows=300), dict(chunk_rows=1000), dict(group=1),
                 dict(group=3, chunk_rows=128), dict(num_sms=7), dict(tile_m=256),
                 dict(tile_m=256, chunk_rows=1), dict(tile_m=256, swizzle=False),
-                dict(tile_m=256, num_sms=7), dict(tile_m=512), dict(tile_m=512, chunk_rows=1),
-                dict(tile_m=512, num_sms=9)]
+                dict(tile_m=256, num_sms=7)]
     for kw in variants:
         kw.setdefault("chunk_rows", wl.chunk_rows)
         outs, _, _ = _run(dt, inp, wl.m, wl.n, wl.k, dev=dev, **kw)
@@ -98,7 +97,7 @@ def test_small_bit_identical_across_orders_chunks_groups_and_baseline(dt, small)
 
 
 @pytest.mark.parametrize("chunk_rows", [96, 1, 300])
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_signals_after_each_call(dt, small, chunk_rows, tile_m):
     wl, inp, _ = small
     dev = _upload(inp)
@@ -119,7 +118,7 @@ def test_per_rank_b_parity(dt):
         assert_close(to_f64(o), ref[h], "f32", f"out_{h}")
 
 
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_sixteen_ranks_tiny_blocks(dt, tile_m):
     # the largest world size: 9 rows per rank, 16 columns per destination, K not a multiple of 8
     inp = make_a2a_inputs(16, 16 * 9, 16 * 16, 20, seed=44)

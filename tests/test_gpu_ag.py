@@ -53,7 +53,7 @@ def small():
 @pytest.mark.parametrize("swizzle", [True, False])
 @pytest.mark.parametrize("rank", [0, 1])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_small_parity(dt, small, backend, swizzle, rank, out_dtype, tile_m):
     wl, inp, ref = small
     c = _run(dt, inp, wl.m, wl.n, wl.k, out_dtype, chunk_rows=wl.chunk_rows, backend=backend,
@@ -64,7 +64,7 @@ def test_small_parity(dt, small, backend, swizzle, rank, out_dtype, tile_m):
 def test_small_bit_identical_across_variants(dt, small):
     wl, inp, ref = small
     base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=128, backend="tma", tile_m=128)
-    for tile_m in [128, 256, 512]:  # one CTA, a pair or two pairs per tile: the same bits
+    for tile_m in [128, 256]:  # one CTA or a pair per tile: the same bits
         for backend in ["copy_engine", "tma", "ldst"]:
             for swizzle in [True, False]:
                 for cr in [1, 64, 100, 128, 256, 1000]:
@@ -84,7 +84,7 @@ def ragged():
 
 
 @pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_ragged_parity_and_identity(dt, ragged, backend, tile_m):
     wl, inp, ref = ragged
     outs = []
@@ -111,7 +111,7 @@ def test_ragged_parity_and_identity(dt, ragged, backend, tile_m):
     (16, 16 * 9, 16, 16, 4),
 ])
 @pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_edge_shapes(dt, case, backend, tile_m):
     w, m, n, k, cr = case
     inp = make_ag_inputs(w, m, n, k, seed=31 + m)
@@ -122,7 +122,7 @@ def test_edge_shapes(dt, case, backend, tile_m):
 
 
 @pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_padded_leading_dims_and_canaries(dt, backend, tile_m):
     w, m, n, k = 3, 3 * 50, 72, 96
     inp = make_ag_inputs(w, m, n, k, seed=77)
@@ -164,7 +164,7 @@ def test_workspace_reuse_across_problems(dt):
             assert_close(to_f64(c), ref_small, "bf16")
 
 
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_lost_chunk_times_out_and_context_survives(dt, small, tile_m):
     """Host-made fault: one chunk's copy and flag are never issued; the consumer tiles'
     bounded waits run out, the error comes back through dt_check, and the next call works

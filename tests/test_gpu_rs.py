@@ -55,7 +55,7 @@ def w4():
 
 @pytest.mark.parametrize("swizzle", [True, False])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_w4_parity(dt, w4, swizzle, out_dtype, tile_m):
     wl, inp, ref = w4
     outs = _run(dt, inp, wl.m, wl.n, wl.k, out_dtype, chunk_rows=wl.chunk_rows, swizzle=swizzle,
@@ -66,7 +66,7 @@ def test_w4_parity(dt, w4, swizzle, out_dtype, tile_m):
 def test_w4_bit_identical_across_variants(dt, w4):
     wl, inp, ref = w4
     base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, tile_m=128)
-    for tile_m in [128, 256, 512]:  # one CTA, a pair or two pairs per tile: the same bits
+    for tile_m in [128, 256]:  # one CTA or a pair per tile: the same bits
         for swizzle in [True, False]:
             for cr in [1, 64, 100, 512, 4096]:
                 outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, swizzle=swizzle,
@@ -80,7 +80,7 @@ def test_w4_bit_identical_across_variants(dt, w4):
         assert all(bits_equal(o, b) for o, b in zip(outs, base))
 
 
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_ragged_parity_and_identity(dt, tile_m):
     wl = WORKLOADS["rs_w6_m6000_n5120_k3000"]
     inp = wl.make()
@@ -107,7 +107,7 @@ def test_ragged_parity_and_identity(dt, tile_m):
     (5, 5 * 130, 256, 20, 130),
 ])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_edge_shapes(dt, case, out_dtype, tile_m):
     w, m, n, k, cr = case
     inp = make_rs_inputs(w, m, n, k, seed=41 + m)
@@ -142,7 +142,7 @@ def test_k_zero(dt):
     assert all((o == 0).all() for o in outs)
 
 
-@pytest.mark.parametrize("tile_m", [128, 256, 512])
+@pytest.mark.parametrize("tile_m", [128, 256])
 def test_repeated_calls_reuse_counters(dt, w4, tile_m):
     """Arrival counters return to zero inside each call, so back-to-back calls on one
     workspace keep reducing correctly."""

@@ -1,5 +1,5 @@
-// GEMM-AllToAll instantiations of the fused kernel (bf16 or fp32 out_h, one CTA, a CTA pair or
-// two pairs per tile), also used by the baseline's per-step launches.
+// GEMM-AllToAll instantiations of the fused kernel (bf16 or fp32 out_h, one CTA or a CTA pair
+// per tile), also used by the baseline's per-step launches.
 #include "dt_internal.h"
 
 namespace dt {
@@ -10,7 +10,6 @@ cudaError_t launch_cl(const KParams& p, int grid, cudaStream_t stream, int cl) {
   switch (cl) {
     case 1: return launch_fused<kOpA2A, kCopyNone, F32, 1>(p, grid, false, stream);
     case 2: return launch_fused<kOpA2A, kCopyNone, F32, 2>(p, grid, false, stream);
-    case 4: return launch_fused<kOpA2A, kCopyNone, F32, 4>(p, grid, false, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,6 +1,6 @@
 // AllGather-GEMM instantiations of the fused kernel: chunk transfer on the copy engine
 // (no in-kernel workers), on TMA bulk copies, or on vector loads/stores; bf16 or fp32 C;
-// one CTA, a CTA pair or two pairs per tile.
+// one CTA or a CTA pair per tile.
 #include "dt_internal.h"
 
 namespace dt {
@@ -11,7 +11,6 @@ cudaError_t launch_copy(const KParams& p, int grid, bool cooperative, cudaStream
   switch (cl) {
     case 1: return launch_fused<kOpAG, COPY, F32, 1>(p, grid, cooperative, stream);
     case 2: return launch_fused<kOpAG, COPY, F32, 2>(p, grid, cooperative, stream);
-    case 4: return launch_fused<kOpAG, COPY, F32, 4>(p, grid, cooperative, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -100,7 +100,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Derived {
   int op;
   int32_t W, rank, G, Tm, Tn, KB, T, nC, pieces_max;
-  int32_t bm;    // rows of a tile in the order: 128 (one CTA), 256 (a CTA pair), 512 (two pairs)
+  int32_t bm;    // rows of a tile in the order: 128 (one CTA), 256 (a CTA pair)
   int32_t cl;    // CTAs per cluster: bm / 128
   int32_t Tm128; // 128-row m-tiles (one CTA's rows): the ReduceScatter's unit granularity
   int64_t M, N, K, Ms, Cr, lda, ldb, ldc, ld_gather;
@@ -163,10 +163,10 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     return fail(DT_ERR_INVALID, "leading dimension smaller than the row length");
   if ((d->lda % 8) || (d->ldb % 8) || (d->ldc % 8))
     return fail(DT_ERR_INVALID, "leading dimensions must be multiples of 8 elements (16-byte rows)");
-  if ((a->tile_m != 0 && a->tile_m != kBM && a->tile_m != 2 * kBM && a->tile_m != 4 * kBM) ||
+  if ((a->tile_m != 0 && a->tile_m != kBM && a->tile_m != 2 * kBM) ||
       (a->tile_n != 0 && a->tile_n != kBN))
-    return fail(DT_ERR_UNSUPPORTED, "tiles other than %d, %d or %d x %d are not built", kBM,
-                2 * kBM, 4 * kBM, kBN);
+    return fail(DT_ERR_UNSUPPORTED, "tiles other than %d or %d x %d are not built", kBM, 2 * kBM,
+                kBN);
   if (a->out_dtype != DT_BF16 && a->out_dtype != DT_F32)
     return fail(DT_ERR_INVALID, "unknown out_dtype %d", a->out_dtype);
   d->f32 = a->out_dtype == DT_F32;
@@ -1461,23 +1461,14 @@ dt_status dt_tune_reduce(int op, const void* const* a_, const void* const* b_, v
     return op == DT_OP_GEMM_RS ? dt_gemm_rs(a_, b_, out, ws, ws_bytes, &cand, stream)
                                : dt_gemm_ar(a_, b_, out, ws, ws_bytes, &cand, stream);
   };
-  // tile rows: as given, and for the ReduceScatter / AllReduce also 512 (two CTA pairs sharing
-  // B: a quarter fewer operand bytes from L2) when that still gives every four SMs a tile
-  std::vector<int32_t> tiles = {a->tile_m};
-  if (op != DT_OP_GEMM_A2A && a->tile_m != 4 * kBM &&
-      static_cast<int64_t>(d.W) * cdiv64(d.M, 4 * kBM) * cdiv64(d.N, kBN) >= 38)
-    tiles.push_back(4 * kBM);
   std::vector<dt_args> cands;
-  for (int32_t tm : tiles) {
-    for (int64_t cr : chunk_candidates(d.Ms)) {
-      for (int g : {4, 8, 16}) {
-        dt_args cand = *a;
-        cand.chunk_rows = cr;
-        cand.swizzle = 1;
-        cand.group = g;
-        cand.tile_m = tm;
-        cands.push_back(cand);
-      }
+  for (int64_t cr : chunk_candidates(d.Ms)) {
+    for (int g : {4, 8, 16}) {
+      dt_args cand = *a;
+      cand.chunk_rows = cr;
+      cand.swizzle = 1;
+      cand.group = g;
+      cands.push_back(cand);
     }
   }
   std::vector<dt_tune_point> pts = tune_all(t, cands, op, call);

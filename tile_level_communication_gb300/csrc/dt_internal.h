@@ -22,9 +22,8 @@ void set_last_error(const char* msg);
 // Launch the fused persistent kernel; defined in dt_ag.cu (AllGather variants), dt_rs.cu
 // (ReduceScatter / AllReduce variants) and dt_a2a.cu (AllToAll variants).  `cooperative`
 // guarantees that every CTA is resident, which the in-kernel chunk transfer relies on.
-// `cl`: CTAs per cluster, 1, 2 (a CTA pair per 256-row tile) or 4 (two pairs per 512-row tile
-// sharing B); grid and copy_ctas are multiples of it and the grid is capped at the clusters the
-// GPU holds at once.
+// `cl`: CTAs per cluster, 1 or 2 (a CTA pair per 256-row tile); grid and copy_ctas are
+// multiples of it and the grid is capped at the clusters the GPU holds at once.
 cudaError_t launch_ag_kernel(const KParams& p, int copy_mode, bool f32, int grid,
                              bool cooperative, cudaStream_t stream, int cl);
 cudaError_t launch_rs_kernel(const KParams& p, bool f32, int grid, cudaStream_t stream, int cl);

@@ -2,7 +2,7 @@
 // ReduceScatter / AllReduce or AllToAll fused in.
 //
 // One CTA per SM, 8 warps; CL CTAs per cluster share a tile of CL x 128 rows (CL = 1: one
-// CTA, tcgen05 cta_group::1; CL = 2: a CTA pair, cta_group::2; CL = 4: two pairs sharing B):
+// CTA, tcgen05 cta_group::1; CL = 2: a CTA pair, cta_group::2):
 //   warp 0      TMA producer: per tile, waits (bounded) for the ready flags of the chunks
 //               this CTA's rows live in, then streams A / B k-blocks into a 4- to 7-stage
 //               ring (a pair's stages complete on its even CTA's barriers).
@@ -69,8 +69,7 @@ enum DevCode : uint32_t {
 __host__ __device__ constexpr bool has_staging(bool rs, int copy_mode) {
   return rs || copy_mode == kCopyTma;
 }
-// cl: CTAs per cluster (1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile; 4: two
-// pairs per 512-row tile sharing B)
+// cl: CTAs per cluster (1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile)
 __host__ __device__ constexpr int kernel_smem_bytes(bool rs, int copy_mode, int cl) {
   return 1024 + stages(cl > 1, has_staging(rs, copy_mode)) * (kAStage + b_stage_bytes(cl > 1)) +
          (has_staging(rs, copy_mode) ? 2 * kCopyBuf : 0) + kMiscBytes;
@@ -213,7 +212,7 @@ struct TileInfo {
 
 // Clusters: the CL CTAs of a cluster work on the same tile of the order, each on its own 128 of
 // the tile's CL * 128 rows, in cluster-rank order.  CTAs 2k and 2k+1 form a pair (tcgen05
-// cta_group::2) whose even CTA issues the MMAs; with CL = 4 the two pairs share B.
+// cta_group::2) whose even CTA issues the MMAs.
 template <int CL>
 __device__ __forceinline__ uint32_t cl_rank() {
   return CL > 1 ? (blockIdx.x % static_cast<uint32_t>(CL)) : 0u;
@@ -347,16 +346,7 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
         const uint32_t a_dst = a_smem0 + sst * kAStage;
         const uint32_t b_dst = b_smem0 + sst * b_stage_bytes(PAIR);
         const uint32_t fb = full0 + 8u * sst;
-        if constexpr (CL == 4) {
-          // both pairs use the same columns: this CTA loads slab (rank >> 1) of its half of B
-          // for itself and for its counterpart in the other pair
-          const uint32_t bar = full0_lead + 8u * sst;
-          if (leader) mbar_expect_tx(fb, 2 * (kAStage + b_stage_bytes(PAIR)));
-          tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
-          const uint32_t sl = rank >> 1;
-          tma_load_2d_pair_mc(b_dst + sl * kBSlab, tB, b_col + static_cast<int32_t>(sl) * 64,
-                              kb * kBK, bar, static_cast<uint16_t>(0x5u << (rank & 1u)));
-        } else if constexpr (PAIR) {
+        if constexpr (PAIR) {
           const uint32_t bar = full0_lead + 8u * sst;
           if (leader) mbar_expect_tx(fb, 2 * (kAStage + b_stage_bytes(PAIR)));
           tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
@@ -398,10 +388,9 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
 template <int OP, int CL, int NS>
 __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_base) {
   constexpr bool PAIR = CL > 1;
-  // commit masks: a stage is refilled by both pairs of a 4-CTA cluster (B is shared), an
-  // accumulator belongs to this pair
+  // commit masks: a stage and an accumulator belong to both CTAs of the pair
   const uint32_t rank = cl_rank<CL>();
-  const uint16_t stage_mask = CL == 4 ? 0xF : 0x3;
+  const uint16_t stage_mask = 0x3;
   const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & ~1u));
   // a pair's MMA has M = 256: rows 0-127 from the even CTA, 128-255 from the odd one
   constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, kBN, /*B MN-major*/ 1);
@@ -1170,6 +1159,7 @@ static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int 
 // whole clusters.
 template <int OP, int COPY, bool F32, int CL>
 __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_constant__ KParams p) {
+  static_assert(CL == 1 || CL == 2, "one CTA or a CTA pair per tile");
   constexpr bool PAIR = CL > 1;
   constexpr int NS = stages(PAIR, has_staging(OP == kOpRS, COPY));
   extern __shared__ uint8_t smem_raw[];
@@ -1196,7 +1186,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(L.full(s), 1);
-      mbar_init(L.empty(s), CL == 4 ? 2 : 1);  // both pairs' MMAs release a shared-B stage
+      mbar_init(L.empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(L.tfull(a), 1);

@@ -224,17 +224,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
 }
-// The same load multicast to the CTAs in `mask` (same shared-memory offset in each); every
-// destination's bytes complete on the barrier at offset `bar_cluster` of that destination's
-// pair leader.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* tm, int32_t x,
-                                                    int32_t y, uint32_t bar_cluster, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster), "h"(mask)
-      : "memory");
-}
 // Whole warp, in both CTAs of the pair: allocate `ncols` TMEM columns in each.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),

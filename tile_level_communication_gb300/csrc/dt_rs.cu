@@ -1,5 +1,5 @@
 // GEMM-ReduceScatter / GEMM-AllReduce instantiations of the fused kernel (bf16 or fp32
-// out, one CTA, a CTA pair or two pairs per tile).
+// out, one CTA or a CTA pair per tile).
 #include "dt_internal.h"
 
 namespace dt {
@@ -10,7 +10,6 @@ cudaError_t launch_cl(const KParams& p, int grid, cudaStream_t stream, int cl) {
   switch (cl) {
     case 1: return launch_fused<kOpRS, kCopyNone, F32, 1>(p, grid, false, stream);
     case 2: return launch_fused<kOpRS, kCopyNone, F32, 2>(p, grid, false, stream);
-    case 4: return launch_fused<kOpRS, kCopyNone, F32, 4>(p, grid, false, stream);
     default: return cudaErrorInvalidValue;
   }
 }
