@@ -320,11 +320,18 @@ dt_status dt_check(void* workspace, void* stream, uint32_t* info);
  *   - All calls on a device share the one array and it keeps the last call's contents; each
  *     call clears its error word and layout tag first, so the tile order, flags and counters
  *     are rebuilt every call.  Calls that overlap on the GPU race: order them.
- *   - Bounded device waits still end a stalled call, but there is no workspace to pass to
- *     dt_check(), so a device-side timeout is not reported.
+ *   - Bounded device waits still end a stalled call; the error they record stays in the
+ *     array until dt_static_scratch_check() reads it (the next call clears it first).
  * The pages have no counterpart of this entry point. */
 dt_status dt_ag_gemm_static_scratch(const void* const* a_shards, const void* b, void* c,
                                     const dt_args* a, void* stream);
+
+/* dt_check() for the fixed scratch of the current device: synchronise `stream`, read and clear
+ * the error block that the last dt_ag_gemm_static_scratch call on this device left in the
+ * array.  Returns DT_OK, DT_ERR_TIMEOUT (a bounded device wait ran out: C is incomplete) or
+ * DT_ERR_INVALID; `info` (may be NULL) receives {device code, site, detail0, detail1}.
+ * Allocates nothing.  Call it after the static-scratch call it checks and before the next one. */
+dt_status dt_static_scratch_check(void* stream, uint32_t* info);
 
 /* One candidate of the tuner: its knobs, mean time per call (ms, < 0 if it did not run) and
  * the status of its calls. */
@@ -368,11 +375,12 @@ dt_status dt_tune_reduce(int op, const void* const* a, const void* const* b, voi
                          dt_tune_point* points, int32_t max_points, int32_t* n_points,
                          void* stream);
 
-/* Failure-detection testing, host side only: the next copy-engine AllGather-GEMM call on
- * this process leaves out the copy and the ready-flag write of transfer step `step` (the
- * position in the gather order; -1 clears).  The tiles that need that chunk wait until
- * `timeout_us`, record DT_ERR_TIMEOUT in the workspace and exit; the CUDA context stays
- * usable.  (Syncopate summary page, "局限与后续工作": fault injection for lost signals and
+/* Failure-detection testing, host side only: the next AllGather-GEMM call on this process
+ * (dt_ag_gemm on any backend, or dt_ag_gemm_static_scratch) leaves out the copy and the
+ * ready-flag write of transfer step `step` (the position in the gather order; -1 clears): the
+ * copy engine is not given that copy, or the in-kernel transfer is told to skip that chunk.
+ * The tiles that need that chunk wait until `timeout_us`, record DT_ERR_TIMEOUT in the
+ * workspace (or the fixed scratch) and exit; the CUDA context stays usable.  (Syncopate summary page, "局限与后续工作": fault injection for lost signals and
  * timeouts.) */
 dt_status dt_debug_drop_transfer(int32_t step);
 

@@ -327,6 +327,35 @@ def test_gelu_tanh_is_close_to_exact_gelu():
     assert reference.activation(np.array([0.0]), "gelu_tanh")[0] == 0.0
 
 
+# points exactly representable in binary64 (and in bf16), over the range the activations see
+_ACT_POINTS = [-6.0, -3.0, -1.5, -1.0, -0.5, -0.125, 0.0, 0.0625, 0.25, 0.75, 1.0, 2.0, 3.5, 8.0]
+
+
+def test_gelu_tanh_matches_its_formula_in_high_precision():
+    """The float64 oracle agrees with the tanh form of GELU evaluated with 50 significant digits
+    (mpmath, with the decimal constant 0.044715 taken exactly) to 1e-12: a wrong constant, a
+    dropped cubic term or a sign slip moves at least one point by far more."""
+    mpmath = pytest.importorskip("mpmath")
+    mp = mpmath.mp
+    mp.dps = 50
+    got = reference.activation(np.array(_ACT_POINTS), "gelu_tanh")
+    for x, g in zip(_ACT_POINTS, got):
+        xm = mpmath.mpf(x)
+        want = mpmath.mpf("0.5") * xm * (1 + mpmath.tanh(mpmath.sqrt(2 / mp.pi) *
+                                                         (xm + mpmath.mpf("0.044715") * xm ** 3)))
+        assert abs(mpmath.mpf(float(g)) - want) <= mpmath.mpf("1e-12") * max(1, abs(want)), x
+
+
+def test_silu_matches_its_formula_in_high_precision():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    got = reference.activation(np.array(_ACT_POINTS), "silu")
+    for x, g in zip(_ACT_POINTS, got):
+        xm = mpmath.mpf(x)
+        want = xm / (1 + mpmath.exp(-xm))
+        assert abs(mpmath.mpf(float(g)) - want) <= mpmath.mpf("1e-12") * max(1, abs(want)), x
+
+
 def test_silu_identities():
     x = np.linspace(-20, 20, 801)
     s = reference.activation(x, "silu")

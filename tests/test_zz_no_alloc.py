@@ -47,13 +47,49 @@ def test_static_scratch_matches_workspace_entry_on_consecutive_calls(dt):
         want = _reference_call(dt, inp, args, m, n)
         shards = [dev_bf16(s) for s in inp.shards]
         b = dev_bf16(inp.b)
-        # two calls in a row on the shared scratch
-        for _ in range(2):
-            c = out_tensor(m, n, "bf16")
+        outs = [out_tensor(m, n, "bf16") for _ in range(3)]
+        dt.ag_gemm_static_scratch(shards, b, outs[0], args)  # first call: set-up, kernel loads
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        torch_bytes0 = torch.cuda.memory_allocated()
+        # two calls in a row on the shared scratch: nothing is allocated on the device
+        for c in outs[1:]:
             dt.ag_gemm_static_scratch(shards, b, c, args)
             torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert torch.cuda.memory_allocated() == torch_bytes0
+        assert dt.static_scratch_check() == (0, [0, 0, 0, 0])
+        for c in outs:
             assert_close(to_f64(c), to_f64(want), "bf16", "fixed scratch vs workspace entry")
             assert bits_equal(c, want)
+
+
+@pytest.mark.parametrize("backend", ["tma", "ldst"])
+def test_static_scratch_reports_a_lost_chunk(dt, backend):
+    """A chunk the host drops never lands: the bounded waits run out, the error stays in the
+    fixed scratch until dt_static_scratch_check reads and clears it, and the next call on the
+    same scratch gives the exact result."""
+    import torch
+
+    wl = WORKLOADS["ag_w2_m512_n512_k512"]
+    inp = wl.make()
+    args = dt.make_args(2, wl.m, wl.n, wl.k, rank=0, chunk_rows=wl.chunk_rows, backend=backend,
+                        timeout_us=200_000)
+    want = _reference_call(dt, inp, args, wl.m, wl.n)
+    shards = [dev_bf16(s) for s in inp.shards]
+    b = dev_bf16(inp.b)
+    c = out_tensor(wl.m, wl.n, "bf16")
+    dt.debug_drop_transfer(3)  # the second chunk of rank 1
+    dt.ag_gemm_static_scratch(shards, b, c, args)
+    st, info = dt.static_scratch_check()
+    assert st == dt.capi.DT_ERR_TIMEOUT, (st, info)
+    assert info[0] == 1  # a chunk's ready flag did not flip
+    assert dt.static_scratch_check() == (0, [0, 0, 0, 0])  # read once, then cleared
+    c2 = out_tensor(wl.m, wl.n, "bf16")
+    dt.ag_gemm_static_scratch(shards, b, c2, args)
+    torch.cuda.synchronize()
+    assert dt.static_scratch_check()[0] == 0
+    assert bits_equal(c2, want)
 
 
 def test_static_scratch_rejects_problems_that_do_not_fit(dt):

@@ -52,6 +52,7 @@ _SIGS = {
     "dt_check": (ctypes.c_int, [_P, _P, _P]),
     "dt_debug_drop_transfer": (ctypes.c_int, [ctypes.c_int32]),
     "dt_ag_gemm_static_scratch": (ctypes.c_int, [_P, _P, _P, _P, _P]),
+    "dt_static_scratch_check": (ctypes.c_int, [_P, _P]),
     "dt_ffn_ag_rs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_size_t,
                                     _P, _P, _P]),
     "dt_tune_ag_gemm": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_int32, _P,
@@ -350,7 +351,8 @@ def ffn_ag_rs(x_shards, w1, w2_list, h, out_list, ws_ag, ws_rs, ag: DtArgs, rs: 
 
 
 def debug_drop_transfer(step: int):
-    """Host-side fault injection: the next copy-engine AllGather call skips transfer `step`."""
+    """Host-side fault injection: the next AllGather-GEMM call (any backend) leaves out the
+    copy and the ready flag of transfer step `step`."""
     _raise(lib().dt_debug_drop_transfer(step))
 
 
@@ -358,4 +360,11 @@ def check(workspace, stream=None):
     """Synchronise, read and clear the device error word; returns (status, info[4])."""
     info = (ctypes.c_uint32 * 4)()
     st = lib().dt_check(_ptr(workspace), _stream(stream), info)
+    return st, list(info)
+
+
+def static_scratch_check(stream=None):
+    """check() for the fixed scratch of the current device; returns (status, info[4])."""
+    info = (ctypes.c_uint32 * 4)()
+    st = lib().dt_static_scratch_check(_stream(stream), info)
     return st, list(info)

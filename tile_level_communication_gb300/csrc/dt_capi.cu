@@ -445,13 +445,8 @@ dt_status launch_zero(void* dst, int64_t rows, int64_t row_bytes, int64_t ld_byt
   return DT_OK;
 }
 
-dt_status prepare_workspace(const Derived& d, void* ws, cudaStream_t stream, uint32_t* epoch) {
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    WsState& st = g_ws[ws];
-    if (++st.epoch == 0u) st.epoch = 1u;  // ready flags hold epochs; 0 means "never"
-    *epoch = st.epoch;
-  }
+// The prepare kernel of one call on `ws` (see prepare_kernel).
+dt_status launch_prepare(const Derived& d, void* ws, cudaStream_t stream) {
   uint8_t* w = reinterpret_cast<uint8_t*>(ws);
   const size_t ctl_begin = 256;
   const int64_t ctl_words = static_cast<int64_t>((d.off_order - ctl_begin) / 4);
@@ -463,6 +458,33 @@ dt_status prepare_workspace(const Derived& d, void* ws, cudaStream_t stream, uin
       reinterpret_cast<unsigned long long*>(w + kTagOffset), layout_tag(d));
   DT_CUDA(cudaGetLastError());
   return DT_OK;
+}
+
+dt_status prepare_workspace(const Derived& d, void* ws, cudaStream_t stream, uint32_t* epoch) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    WsState& st = g_ws[ws];
+    if (++st.epoch == 0u) st.epoch = 1u;  // ready flags hold epochs; 0 means "never"
+    *epoch = st.epoch;
+  }
+  return launch_prepare(d, ws, stream);
+}
+
+// The transfer step that dt_debug_drop_transfer asked the next AllGather to leave out (-1:
+// none); reading it clears it.
+int32_t take_drop_transfer() {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  const int32_t drop = g_drop_transfer;
+  g_drop_transfer = -1;
+  return drop;
+}
+
+// The in-kernel transfer leaves out the chunk of transfer step `drop` (no copy, no flag).
+void set_drop_chunk(KParams& p, const Derived& d, int32_t drop) {
+  if (drop < 0 || drop >= d.W * d.nC) return;
+  int32_t s, j;
+  ag_transfer_chunk(d.geom, drop, s, j);
+  p.drop_chunk = s * d.nC + j;
 }
 
 dt_status check_ws(const Derived& d, void* ws, size_t bytes) {
@@ -496,6 +518,7 @@ void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
   p.epoch = epoch;
   p.timeout_ns = d.timeout_ns;
   p.act = d.act;
+  p.drop_chunk = -1;
 }
 
 // ------------------------------------------------------------------------------ AllGather
@@ -580,16 +603,7 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
   // start from a cleared error word and tag: the prepare kernel below then rewrites the order
   // and zeroes the flags and counters, whatever an earlier call left behind
   DT_CUDA(cudaMemsetAsync(w, 0, kTagOffset + sizeof(unsigned long long), stream));
-  const size_t ctl_begin = 256;
-  const int64_t ctl_words = static_cast<int64_t>((d.off_order - ctl_begin) / 4);
-  const int64_t work = std::max<int64_t>(d.T, ctl_words);
-  const unsigned pgrid =
-      static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(cdiv64(work, 256), 1), 1024));
-  prepare_kernel<<<pgrid, 256, 0, stream>>>(
-      d.geom, d.op, reinterpret_cast<int32_t*>(w + d.off_order), d.T,
-      reinterpret_cast<uint32_t*>(w + ctl_begin), ctl_words, reinterpret_cast<uint32_t*>(w),
-      reinterpret_cast<unsigned long long*>(w + kTagOffset), layout_tag(d));
-  DT_CUDA(cudaGetLastError());
+  if ((s = launch_prepare(d, scratch, stream)) != DT_OK) return s;
   const uint32_t epoch = 1u;  // the flags were just zeroed
   KParams p;
   fill_common(p, d, scratch, epoch);
@@ -601,21 +615,8 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
   p.lda_src = d.lda;
   p.ld_gather = d.ld_gather;
   p.wait_flags = 1;
-  p.row_bytes = d.K * 2;
-  if (p.row_bytes <= kCopyBuf) {
-    p.rows_per_piece = static_cast<int32_t>(kCopyBuf / p.row_bytes);
-    p.segs_per_row = 1;
-  } else {
-    p.rows_per_piece = 0;
-    p.segs_per_row = static_cast<int32_t>(cdiv64(p.row_bytes, kCopyBuf));
-  }
-  auto pieces = [&](int64_t rows) -> int32_t {
-    return p.rows_per_piece > 0 ? static_cast<int32_t>(cdiv64(rows, p.rows_per_piece))
-                                : static_cast<int32_t>(rows * p.segs_per_row);
-  };
-  p.pieces_full = pieces(std::min<int64_t>(d.Cr, d.Ms));
-  p.pieces_last = pieces(d.Ms - static_cast<int64_t>(d.nC - 1) * d.Cr);
-  p.src_rows_contig = d.lda == d.K ? 1 : 0;
+  set_pieces(p, d);
+  set_drop_chunk(p, d, take_drop_transfer());
   if ((s = make_tmap(&p.tmA[0], p.gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
   if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
   p.own_in_place = own_in_place(d) ? 1 : 0;
@@ -780,11 +781,10 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
   if (d.backend == DT_XFER_COPY_ENGINE) {
     PfnWriteValue32 wv = write_value32();
     if (!wv) return fail(DT_ERR_CUDA, "cuStreamWriteValue32 entry point unavailable");
+    const int32_t drop = take_drop_transfer();
     std::lock_guard<std::mutex> lk(g_dev_mu);
     if ((s = fork_copies(dev, stream)) != DT_OK) return s;
     const int32_t nchunks = d.W * d.nC;
-    const int32_t drop = g_drop_transfer;
-    g_drop_transfer = -1;
     bool launched = false;
     int32_t queued = 0;  // chunks queued so far: chunk n goes to copy stream n % kCopyStreams
     for (int32_t tc = 0; tc < nchunks; ++tc) {
@@ -816,6 +816,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
   const int copy = d.backend == DT_XFER_TMA ? kCopyTma : kCopyLdst;
   p.copy_ctas = d.copy_ctas;
   if (d.copy_ctas >= sms) return fail(DT_ERR_INVALID, "copy_ctas must leave SMs for the GEMM");
+  set_drop_chunk(p, d, take_drop_transfer());
   const int grid_ded = d.copy_ctas + grid_for(d, d.T, sms - d.copy_ctas);
   cudaError_t e =
       launch_ag_kernel(p, copy, d.f32, d.copy_ctas ? grid_ded : grid, true, stream, d.cl);

@@ -122,6 +122,8 @@ struct KParams {
   int32_t pieces_full;     // pieces of a chunk with Cr rows
   int32_t pieces_last;     // pieces of the last chunk of a rank
   int32_t src_rows_contig; // shard rows are back to back (lda == K)
+  int32_t drop_chunk;      // failure-detection testing: chunk the host told the in-kernel
+                           // transfer to leave out (its flag never flips); -1: none
 };
 
 struct SmemLayout {
@@ -1034,6 +1036,7 @@ __device__ __forceinline__ void for_each_piece(const KParams& p, int32_t wid, in
                          static_cast<int64_t>(j) * p.pieces_full;
     const int32_t first = static_cast<int32_t>(((wid - base) % nw + nw) % nw);
     if (p.own_in_place && s == p.g.rank) continue;  // read in place, never transferred
+    if (s * p.g.nC + j == p.drop_chunk) continue;     // the host dropped this message
     for (int32_t pc = first; pc < total; pc += nw) {
       if (!f(s, j, s * p.g.nC + j, total, piece_of(p, pc, rows_c))) return;
     }

@@ -70,3 +70,13 @@ extern "C" dt_status dt_ag_gemm_static_scratch(const void* const* a_shards, cons
   return dt::ag_gemm_on_scratch(a_shards, b, c, scratch, DT_STATIC_SCRATCH_BYTES, a,
                                 reinterpret_cast<cudaStream_t>(stream));
 }
+
+// The array starts with the same error block as a workspace, so dt_check reads and clears it.
+extern "C" dt_status dt_static_scratch_check(void* stream, uint32_t* info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DT_ERR_CUDA;
+  void* scratch = nullptr;
+  const dt_status s = scratch_address(dev, &scratch);
+  if (s != DT_OK) return s;
+  return dt_check(scratch, stream, info);
+}
