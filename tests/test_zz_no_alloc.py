@@ -31,6 +31,8 @@ def _reference_call(dt, inp, args, m, n):
 
 
 def test_static_scratch_matches_workspace_entry_on_consecutive_calls(dt):
+    import gc
+
     import torch
 
     wl = WORKLOADS["ag_w2_m512_n512_k512"]
@@ -50,14 +52,17 @@ def test_static_scratch_matches_workspace_entry_on_consecutive_calls(dt):
         outs = [out_tensor(m, n, "bf16") for _ in range(3)]
         dt.ag_gemm_static_scratch(shards, b, outs[0], args)  # first call: set-up, kernel loads
         torch.cuda.synchronize()
+        gc.collect()
         free0, _ = torch.cuda.mem_get_info()
+        torch.cuda.reset_peak_memory_stats()
         torch_bytes0 = torch.cuda.memory_allocated()
-        # two calls in a row on the shared scratch: nothing is allocated on the device
+        # two calls in a row on the shared scratch: nothing is allocated on the device, by the
+        # driver or through torch's allocator (its peak stays where it was)
         for c in outs[1:]:
             dt.ag_gemm_static_scratch(shards, b, c, args)
             torch.cuda.synchronize()
         assert torch.cuda.mem_get_info()[0] == free0
-        assert torch.cuda.memory_allocated() == torch_bytes0
+        assert torch.cuda.max_memory_allocated() == torch_bytes0
         assert dt.static_scratch_check() == (0, [0, 0, 0, 0])
         for c in outs:
             assert_close(to_f64(c), to_f64(want), "bf16", "fixed scratch vs workspace entry")

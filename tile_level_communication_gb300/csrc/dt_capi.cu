@@ -125,6 +125,15 @@ uint64_t default_timeout_ns() {
   return v;
 }
 
+// L2 cache policies of the fused kernels (KParams::l2_hints); DT_L2_HINTS overrides.
+int32_t l2_hints_setting() {
+  static int32_t v = [] {
+    const char* e = getenv("DT_L2_HINTS");
+    return e ? static_cast<int32_t>(atoi(e)) & 3 : 0;
+  }();
+  return v;
+}
+
 dt_status derive(const dt_args* a, int op, Derived* d) {
   if (!a) return fail(DT_ERR_INVALID, "args is NULL");
   if (op != DT_OP_AG_GEMM && op != DT_OP_GEMM_RS && op != DT_OP_GEMM_AR && op != DT_OP_GEMM_A2A)
@@ -519,6 +528,7 @@ void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
   p.timeout_ns = d.timeout_ns;
   p.act = d.act;
   p.drop_chunk = -1;
+  p.l2_hints = l2_hints_setting();
 }
 
 // ------------------------------------------------------------------------------ AllGather

@@ -124,6 +124,9 @@ struct KParams {
   int32_t src_rows_contig; // shard rows are back to back (lda == K)
   int32_t drop_chunk;      // failure-detection testing: chunk the host told the in-kernel
                            // transfer to leave out (its flag never flips); -1: none
+  int32_t l2_hints;        // L2 cache policies: bit 0, ReduceScatter running sums, park slots
+                           // and final sums stream through L2 (evict first); bit 1, B's k-blocks
+                           // stay (evict last)
 };
 
 struct SmemLayout {
@@ -292,6 +295,8 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
   // stage s: barriers 8 s bytes after stage 0's, buffers s stages after stage 0's
   const uint32_t full0 = L.full(0), empty0 = L.empty(0);
   const uint32_t a_smem0 = smem_u32(L.a), b_smem0 = smem_u32(L.b);
+  const bool b_keep = (p.l2_hints & 2) != 0;
+  const uint64_t pol_b = l2_policy_evict_last();
   uint32_t full0_lead = full0;  // stage 0's full barrier in the pair leader (cluster address)
   if constexpr (PAIR) full0_lead = mapa_shared(full0, rank & ~1u);
   uint32_t kit = 0;  // k-blocks issued so far (the last one, if any, is kit - 1)
@@ -352,15 +357,27 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
           const uint32_t bar = full0_lead + 8u * sst;
           if (leader) mbar_expect_tx(fb, 2 * (kAStage + b_stage_bytes(PAIR)));
           tma_load_2d_pair(a_dst, tA, kb * kBK, a_row, bar);
+          if (b_keep) {
 #pragma unroll
-          for (int jj = 0; jj < NB; ++jj)
-            tma_load_2d_pair(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, bar);
+            for (int jj = 0; jj < NB; ++jj)
+              tma_load_2d_pair_hint(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, bar, pol_b);
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < NB; ++jj)
+              tma_load_2d_pair(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, bar);
+          }
         } else {
           mbar_expect_tx(fb, kAStage + b_stage_bytes(PAIR));
           tma_load_2d(a_dst, tA, kb * kBK, a_row, fb);
+          if (b_keep) {
 #pragma unroll
-          for (int jj = 0; jj < NB; ++jj)
-            tma_load_2d(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, fb);
+            for (int jj = 0; jj < NB; ++jj)
+              tma_load_2d_hint(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, fb, pol_b);
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < NB; ++jj)
+              tma_load_2d(b_dst + jj * kBSlab, tB, b_col + jj * 64, kb * kBK, fb);
+          }
         }
       }
       __syncwarp();
@@ -693,6 +710,8 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
   const bool fused_rs = RS && !p.plain;
   const bool fused_a2a = A2A && !p.plain;
   int32_t tl = 0;
+  const bool stream_sums = (p.l2_hints & 1) != 0;  // running sums pass through L2 once
+  const uint64_t pol_s = l2_policy_evict_first();
   uint32_t stage_ctr = 0;           // running-sum staging buffer in use (alternates)
   uint32_t ld_par[2] = {0u, 0u};    // phase of each staging buffer's load barrier
   // a pair's accumulator is released on the even CTA's barrier, by the warps of both CTAs
@@ -801,8 +820,12 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
         fence_proxy_async_global();
         const int b0 = static_cast<int>(stage_ctr & 1u);
         mbar_expect_tx(L.copyb(b0), kCopyBuf);
-        tma_load_2d(smem_u32(L.copy + b0 * kCopyBuf), &p.tmAcc, static_cast<int32_t>(ti.col0),
-                    static_cast<int32_t>(ti.row0), L.copyb(b0));
+        if (stream_sums)
+          tma_load_2d_hint(smem_u32(L.copy + b0 * kCopyBuf), &p.tmAcc, static_cast<int32_t>(ti.col0),
+                           static_cast<int32_t>(ti.row0), L.copyb(b0), pol_s);
+        else
+          tma_load_2d(smem_u32(L.copy + b0 * kCopyBuf), &p.tmAcc, static_cast<int32_t>(ti.col0),
+                      static_cast<int32_t>(ti.row0), L.copyb(b0));
       }
 #pragma unroll 1
       for (int cb = 0; cb < ncb; ++cb) {
@@ -813,9 +836,14 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
           bulk_wait_read<0>();  // box cb-1's store has read the other buffer
           if (load && cb + 1 < ncb) {
             mbar_expect_tx(L.copyb(b ^ 1), kCopyBuf);
-            tma_load_2d(smem_u32(L.copy + (b ^ 1) * kCopyBuf), &p.tmAcc,
-                        static_cast<int32_t>(c0 + 32), static_cast<int32_t>(ti.row0),
-                        L.copyb(b ^ 1));
+            if (stream_sums)
+              tma_load_2d_hint(smem_u32(L.copy + (b ^ 1) * kCopyBuf), &p.tmAcc,
+                               static_cast<int32_t>(c0 + 32), static_cast<int32_t>(ti.row0),
+                               L.copyb(b ^ 1), pol_s);
+            else
+              tma_load_2d(smem_u32(L.copy + (b ^ 1) * kCopyBuf), &p.tmAcc,
+                          static_cast<int32_t>(c0 + 32), static_cast<int32_t>(ti.row0),
+                          L.copyb(b ^ 1));
           }
         }
         named_bar_sync(1, 128);
@@ -863,14 +891,21 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
         named_bar_sync(1, 128);
         if (et == 0) {
           if (!last) {
-            tma_store_2d(store_map, smem_u32(buf), static_cast<int32_t>(c0), store_y);
+            if (stream_sums)
+              tma_store_2d_hint(store_map, smem_u32(buf), static_cast<int32_t>(c0), store_y, pol_s);
+            else
+              tma_store_2d(store_map, smem_u32(buf), static_cast<int32_t>(c0), store_y);
           } else {
             // one TMA store per output: out_s (ReduceScatter), every rank's copy (AllReduce)
             const int ncopy = p.ar_copies > 0 ? p.ar_copies : 1;
             const int32_t oy = static_cast<int32_t>(p.ar_copies > 0 ? ti.row0 : t_lr0);
-            for (int cp = 0; cp < ncopy; ++cp)
-              tma_store_2d(&p.tmOut[p.ar_copies > 0 ? cp : t_s], smem_u32(buf),
-                           static_cast<int32_t>(c0), oy);
+            for (int cp = 0; cp < ncopy; ++cp) {
+              const CUtensorMap* om = &p.tmOut[p.ar_copies > 0 ? cp : t_s];
+              if (stream_sums)
+                tma_store_2d_hint(om, smem_u32(buf), static_cast<int32_t>(c0), oy, pol_s);
+              else
+                tma_store_2d(om, smem_u32(buf), static_cast<int32_t>(c0), oy);
+            }
           }
           bulk_commit();
         }
