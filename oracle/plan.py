@@ -40,6 +40,12 @@ Tn = ceil(N/BN); group width G (default 8).
   rank after rank is how W ranks that each own an SM array run on one GPU (one
   rank's B_q stays in L2 for all its send steps), and each destination then
   receives its partials in source order q = 0, 1, ..., W-1.
+* ReduceScatter column bands (col_band tiles wide; one band = all Tn when B_q fits the
+  cache): inside rank q's pass the column bands run one after another, and each band
+  repeats the scatter order over all destinations: sort by (q, n // col_band, key, band,
+  n, i).  A wide B_q no longer streams once per destination step: only one band of it
+  is in use at a time (AutoOverlap section 5.4: the order inside the schedule keeps
+  locality).  Destinations still receive their partials in source order.
 * ReduceScatter, swizzle off: lexicographic (q, i, n).
 * ReduceScatter arrivals: a unit is the part of chunk (s, j) that m-tile i covers, times
   column tile n (AutoOverlap section 4.1: a chunk is made of compute tiles; the reduction
@@ -156,22 +162,29 @@ def rs_keys(world_size, q, m, chunk_rows, bm):
             for i in range(tm)}
 
 
-def rs_order(world_size, m, n, chunk_rows, bm, bn, swizzle=True, group=8):
-    """Tile ids ((q * Tm + i) * Tn + n) of the GEMM-ReduceScatter in execution order."""
+def rs_order(world_size, m, n, chunk_rows, bm, bn, swizzle=True, group=8, col_band=None):
+    """Tile ids ((q * Tm + i) * Tn + n) of the GEMM-ReduceScatter in execution order.
+
+    col_band: column tiles per column band (None: all Tn, one band).  Rank q's pass takes the
+    bands one after another and repeats its scatter order inside each: sort by
+    (q, n // col_band, key, band, n, i)."""
     _, _, tm, tn = geometry(world_size, m, n, chunk_rows, bm, bn)
     if tm == 0 or tn == 0:
         return []
     if not swizzle:
         return list(range(world_size * tm * tn))
+    nb = tn if col_band is None else col_band
+    if nb < 1:
+        raise ValueError("col_band must be >= 1")
     entries = []
     for q in range(world_size):
         keys = rs_keys(world_size, q, m, chunk_rows, bm)
         band = _bands(keys, group)
         for i in range(tm):
             for c in range(tn):
-                entries.append((q, keys[i], band[i], c, i))
+                entries.append((q, c // nb, keys[i], band[i], c, i))
     entries.sort()
-    return [(q * tm + i) * tn + c for (q, _, _, c, i) in entries]
+    return [(q * tm + i) * tn + c for (q, _, _, _, c, i) in entries]
 
 
 def rs_expected_arrivals(world_size, m, n, chunk_rows, bm, bn):

@@ -48,6 +48,37 @@ def test_golden_nonperfect_tiling():
             assert plan.rs_order(2, 6, 1, 3, 2, 1) == order
 
 
+def test_golden_column_bands():
+    for head, order in _read_golden("rs_column_bands.txt"):
+        ms, cr, tn, g, nb = (int(x) for x in head[1:])
+        assert plan.rs_order(2, 2 * ms, tn, cr, 1, 1, group=g, col_band=nb) == order, head[0]
+
+
+@pytest.mark.parametrize("w,m,n,cr,bm,bn", [(2, 512, 2048, 128, 128, 256), (3, 390, 520, 50, 128, 96),
+                                            (4, 2048, 4096, 256, 128, 256), (5, 35, 17, 3, 4, 1)])
+@pytest.mark.parametrize("nb", [1, 2, 3, 5, 1000])
+def test_column_bands_keep_each_rank_and_unit_in_order(w, m, n, cr, bm, bn, nb):
+    """Column bands reorder tiles inside a rank's pass only: the order is a bijection, rank q's
+    tiles still come as one block, inside a band the order is the band-less order restricted
+    to it, the bands come one after another, and every unit still receives its partials in
+    source order q = 0..W-1."""
+    _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    o = plan.rs_order(w, m, n, cr, bm, bn, col_band=nb)
+    assert sorted(o) == list(range(w * tm * tn))
+    base = plan.rs_order(w, m, n, cr, bm, bn)
+    per_q = tm * tn
+    for q in range(w):
+        mine = o[q * per_q:(q + 1) * per_q]
+        assert all(t // per_q == q for t in mine)
+        bands = [(t % tn) // nb for t in mine]
+        assert bands == sorted(bands)
+        for b in set(bands):
+            assert [t for t in mine if (t % tn) // nb == b] == \
+                [t for t in base[q * per_q:(q + 1) * per_q] if (t % tn) // nb == b]
+    if nb >= tn:
+        assert o == base
+
+
 GRID = [
     # (W, M, N, Cr, BM, BN)
     (1, 100, 300, 64, 128, 256),
@@ -251,7 +282,7 @@ def _mut_ag_order_min_key(w, r, m, n, cr, bm, bn, swizzle=True, group=8):
 _ORIG_RS_ORDER = plan.rs_order
 
 
-def _mut_rs_order_ranks_interleaved(w, m, n, cr, bm, bn, swizzle=True, group=8):
+def _mut_rs_order_ranks_interleaved(w, m, n, cr, bm, bn, swizzle=True, group=8, col_band=None):
     """Steps interleaved across ranks (key before q) instead of rank after rank."""
     _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
     ent = []
@@ -264,7 +295,7 @@ def _mut_rs_order_ranks_interleaved(w, m, n, cr, bm, bn, swizzle=True, group=8):
     return [(q * tm + i) * tn + c for (_, q, c, i) in ent]
 
 
-def _mut_rs_order_own_first(w, m, n, cr, bm, bn, swizzle=True, group=8):
+def _mut_rs_order_own_first(w, m, n, cr, bm, bn, swizzle=True, group=8, col_band=None):
     """Each rank keeps its own block first (dpos = (s - q) mod W)."""
     _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
     ms = m // w
@@ -279,14 +310,37 @@ def _mut_rs_order_own_first(w, m, n, cr, bm, bn, swizzle=True, group=8):
     return [(q * tm + i) * tn + c for (q, _, c, i) in ent]
 
 
+def _mut_rs_order_bands_ignored(w, m, n, cr, bm, bn, swizzle=True, group=8, col_band=None):
+    """Column bands ignored: the band-less order."""
+    return _ORIG_RS_ORDER(w, m, n, cr, bm, bn, swizzle, group)
+
+
+def _mut_rs_order_band_inside_key(w, m, n, cr, bm, bn, swizzle=True, group=8, col_band=None):
+    """Column band taken inside each destination step instead of around the whole pass."""
+    _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    nb = col_band or tn
+    ent = []
+    for q in range(w):
+        keys = plan.rs_keys(w, q, m, cr, bm)
+        band = plan._bands(keys, group)
+        for i in range(tm):
+            for c in range(tn):
+                ent.append((q, keys[i], c // nb, band[i], c, i))
+    ent.sort()
+    return [(q * tm + i) * tn + c for (q, _, _, _, c, i) in ent]
+
+
 @pytest.mark.parametrize("name,mutant", [("ag_order", _mut_ag_order_negative_offset),
                                          ("ag_order", _mut_ag_order_min_key),
                                          ("rs_order", _mut_rs_order_ranks_interleaved),
-                                         ("rs_order", _mut_rs_order_own_first)])
+                                         ("rs_order", _mut_rs_order_own_first),
+                                         ("rs_order", _mut_rs_order_bands_ignored),
+                                         ("rs_order", _mut_rs_order_band_inside_key)])
 def test_plan_pins_catch_planted_mistakes(name, mutant, monkeypatch):
     monkeypatch.setattr(plan, name, mutant)
     caught = False
-    for fn in (test_golden_rank_offset_orders, test_golden_nonperfect_tiling):
+    for fn in (test_golden_rank_offset_orders, test_golden_nonperfect_tiling,
+               test_golden_column_bands):
         try:
             fn()
         except AssertionError:
