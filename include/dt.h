@@ -112,7 +112,12 @@ typedef struct dt_args {
                           chunks (dedicated SMs); 0 = transfer warps inside every compute CTA
                           (co-located).  AutoOverlap page section 5.3, lowerings 2-5.        */
   int32_t act;         /* AG only: dt_act applied to the fp32 result before it is stored     */
-  int32_t reserved;
+  int32_t col_band;    /* ReduceScatter / AllReduce tile order: column tiles per column band
+                          (rank q's pass takes the bands one after another, each repeating
+                          the scatter order over every destination); 0 = automatic: one band
+                          when B_q (K x N bf16) fits in 32 MiB, else the fewest equal bands
+                          whose share of B_q does; >= Tn: one band.  AllGather / AllToAll:
+                          unused                                                          */
 } dt_args;
 
 typedef enum { DT_ACT_NONE = 0, DT_ACT_GELU_TANH = 1, DT_ACT_SILU = 2 } dt_act;
@@ -278,10 +283,12 @@ dt_status dt_gemm_a2a_kernel_overlap(const void* const* a, const void* const* b,
                                      void* const* y, void* const* out, void* workspace,
                                      size_t ws_bytes, const dt_args* a_args, void* stream);
 
-/* Tiles of the execution order of `op` for `a` (-1 if `a` is invalid), and the rows of one
- * tile (128 or 256, tile_m resolved). */
+/* Tiles of the execution order of `op` for `a` (-1 if `a` is invalid), the rows of one
+ * tile (128 or 256, tile_m resolved), and the column tiles per column band of the
+ * ReduceScatter / AllReduce order (col_band resolved; the tile count Tn for other ops). */
 int64_t dt_tile_count(const dt_args* a, int op);
 int32_t dt_tile_rows(const dt_args* a, int op);
+int32_t dt_col_band(const dt_args* a, int op);
 
 /* Tile execution order of `op` for `a` computed on the host: order[p] is the tile run at
  * position p.  AG tile id = i*Tn + n; RS / AR tile id = (q*Tm + i)*Tn + n, with
@@ -342,6 +349,7 @@ typedef struct dt_tune_point {
   int32_t swizzle;
   int32_t group;
   int32_t tile_m;     /* tile rows as requested (0 = the library's choice) */
+  int32_t col_band;   /* column band as requested (0 = automatic) */
   float ms;
   int32_t status;     /* dt_status of the candidate's calls      */
 } dt_tune_point;
@@ -356,7 +364,9 @@ size_t dt_sizeof_tune_point(void);
  * stays <= 512), TMA and ld/st with co-located transfer warps, TMA and ld/st on 8 or 16
  * dedicated CTAs}; then group widths {4, 8, 16} at the best point.  Scatter-mode candidates
  * (dt_tune_reduce with op DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A): chunk rows x group
- * widths {4, 8, 16}, at the tile rows given.  Each candidate runs once as
+ * widths {4, 8, 16}, at the tile rows given, and for DT_OP_GEMM_RS / DT_OP_GEMM_AR x column
+ * bands {as given, one band} when the given (or automatic) bands are more than one.  Each
+ * candidate runs once as
  * warm-up and `reps` times timed with CUDA events on `stream` (synchronising).  A forward
  * pass times every candidate and takes the fastest as the reference; a reverse pass times each
  * other candidate between two timings of the reference and scores it by its time over their
@@ -383,6 +393,24 @@ dt_status dt_tune_reduce(int op, const void* const* a, const void* const* b, voi
  * workspace (or the fixed scratch) and exit; the CUDA context stays usable.  (Syncopate summary page, "局限与后续工作": fault injection for lost signals and
  * timeouts.) */
 dt_status dt_debug_drop_transfer(int32_t step);
+
+/* Debug timeline of the fused AllGather-GEMM: how much of the chunk transfer the GEMM hid.
+ * (DITRON page, paper section 4.1: most of the communication of a large AllGather-GEMM is
+ * hidden behind the GEMM; AutoOverlap page, section 2: what kernel-level overlap leaves
+ * exposed.)  While a buffer is attached, every dt_ag_gemm call resets it on its stream and its
+ * kernel records, in 64-bit global-timer nanoseconds:
+ *   [0] first CTA start, [1] last CTA exit, [2] total time the GEMM's producers spent waiting
+ *   for ready flags (summed over waits), [3] how many waits found their chunk missing;
+ *   then per chunk c = s * nC + j (rank s, chunk j):
+ *   [4 + 3c] release of its ready flag by the in-kernel transfer (all ones on the copy engine,
+ *            whose stream writes the flag), [5 + 3c] the first wait that found it missing
+ *            began (all ones if none did), [6 + 3c] the first tile read past its flag (all ones
+ *            for chunks read in place or never waited for).
+ * `trace` is caller-owned device memory of at least dt_trace_bytes(a) bytes, 8-byte aligned;
+ * NULL detaches.  A call whose problem needs more bytes than attached returns DT_ERR_INVALID.
+ * Tracing adds a few global atomics per chunk and per CTA; it is off unless attached. */
+size_t dt_trace_bytes(const dt_args* a);
+dt_status dt_trace_attach(void* trace, size_t bytes);
 
 #ifdef __cplusplus
 }

@@ -143,6 +143,36 @@ def test_host_plan_matches_oracle_rs(dt, case, swizzle, bm):
     assert got.tolist() == want, case
 
 
+@pytest.mark.parametrize("case", PLAN_GRID)
+@pytest.mark.parametrize("nb", [1, 2, 3, 7])
+@pytest.mark.parametrize("bm", TILE_M)
+def test_host_plan_matches_oracle_rs_column_bands(dt, case, nb, bm):
+    w, m, n, cr = case
+    for op in (dt.OP_RS, dt.OP_AR):
+        a = dt.make_args(w, m, n, 8, chunk_rows=cr, tile_m=bm, col_band=nb)
+        tn = -(-n // 256)
+        assert dt.col_band(a, op) == min(nb, tn)
+        assert dt.swizzle_plan(a, op).tolist() == oplan.rs_order(w, m, n, cr, bm, 256,
+                                                                 col_band=nb), (case, nb)
+
+
+@pytest.mark.parametrize("w,m,n,k,want", [
+    (8, 8192, 8192, 3584, 16),    # B_q 56 MiB: two bands of 16 column tiles
+    (4, 2048, 4096, 2048, 16),    # B_q 16 MiB: one band (all 16 column tiles)
+    (6, 6000, 5120, 3000, 20),    # B_q 29.3 MiB: one band
+    (2, 512, 8192, 16384, 4),     # B_q 256 MiB: eight bands of 4
+    (2, 512, 2000, 16384, 4),     # 8 column tiles, B_q 62.5 MiB: two bands of 4
+])
+def test_automatic_column_bands(dt, w, m, n, k, want):
+    a = dt.make_args(w, m, n, k, chunk_rows=128)
+    assert dt.col_band(a, dt.OP_RS) == want
+    assert dt.col_band(a, dt.OP_AR) == want
+    assert dt.col_band(a, dt.OP_AG) == -(-n // 256)   # other ops: one band
+    bm = dt.tile_rows(a, dt.OP_RS)
+    assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(w, m, n, 128, bm, 256,
+                                                                   col_band=want)
+
+
 @pytest.mark.parametrize("group", [1, 3, 8, 64])
 @pytest.mark.parametrize("bm", TILE_M)
 def test_host_plan_group_width(dt, group, bm):
@@ -168,6 +198,10 @@ def test_host_plan_random_sweep(dt):
         assert dt.swizzle_plan(a, dt.OP_AG).tolist() == oplan.ag_order(w, r, m, n, cr, bm, 256)
         bm = dt.tile_rows(a, dt.OP_RS)
         assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(w, m, n, cr, bm, 256)
+        nb = int(rng.integers(1, 12))
+        a = dt.make_args(w, m, n, 8, chunk_rows=cr, col_band=nb, group=int(rng.integers(1, 9)))
+        assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(
+            w, m, n, cr, dt.tile_rows(a, dt.OP_RS), 256, group=a.group, col_band=nb)
 
 
 def test_tile_rows_auto_rule(dt):

@@ -269,3 +269,41 @@ def test_single_rank_reads_its_shard_in_place(dt):
         c = _run(dt, inp, 200, 40, 96, lda=104, ldc=48, chunk_rows=64, backend="tma")
         assert_close(to_f64(c, 40), ref, "bf16", "W=1")
         assert torch.isnan(c[:, 40:].float()).all()
+
+
+@pytest.mark.parametrize("backend", ["tma", "ldst", "copy_engine"])
+def test_trace_records_release_before_first_read(dt, backend):
+    """The debug timeline: every chunk the kernel transfers is released before any tile reads
+    past its flag, chunks read in place are never released, and tracing changes no bit."""
+    inp = make_ag_inputs(8, 8 * 512, 1024, 2048, seed=13)
+    args = dt.make_args(8, 8 * 512, 1024, 2048, rank=2, chunk_rows=128, backend=backend)
+    shards = [dev_bf16(s) for s in inp.shards]
+    b = dev_bf16(inp.b)
+    ws = workspace(dt.workspace_size(args, dt.OP_AG))
+    base = out_tensor(8 * 512, 1024, "bf16")
+    dt.ag_gemm(shards, b, base, ws, args)
+    assert dt.check(ws)[0] == 0
+    buf = torch.zeros(dt.trace_bytes(args) // 8, dtype=torch.int64, device="cuda")
+    dt.trace_attach(buf)
+    try:
+        c = out_tensor(8 * 512, 1024, "bf16")
+        dt.ag_gemm(shards, b, c, ws, args)
+        assert dt.check(ws)[0] == 0
+    finally:
+        dt.trace_attach(None)
+    assert bits_equal(c, base)
+    tr = dt.trace_decode(buf.cpu().tolist(), args)
+    assert tr["kernel_us"] is not None and tr["kernel_us"] > 0
+    for (s, j), ev in tr["chunks"].items():
+        if s == 2:   # the own block is tile-aligned: read in place, never transferred
+            assert ev["released_us"] is None and ev["first_read_us"] is None, (s, j, ev)
+            continue
+        assert ev["first_read_us"] is not None, (s, j, ev)
+        if backend == "copy_engine":
+            assert ev["released_us"] is None   # the copy's stream writes the flag
+        else:
+            assert ev["released_us"] is not None
+            assert 0 <= ev["released_us"] <= ev["first_read_us"] <= tr["kernel_us"], (s, j, ev)
+        if ev["first_miss_us"] is not None:
+            assert ev["first_miss_us"] <= ev["first_read_us"]
+    assert tr["stall_us_total"] >= 0 and tr["stalled_waits"] >= 0

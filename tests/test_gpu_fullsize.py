@@ -29,8 +29,9 @@ def dt():
 # ----------------------------------------------------------------------------- ReduceScatter
 
 RS_NAME = "rs_w8_m8192_n8192_k3584"
-RS_VARIANTS = [dict(chunk_rows=c, tile_m=t, swizzle=s)
-               for c in (128, 256, 1024) for t in (128, 256) for s in (True, False)]
+RS_VARIANTS = ([dict(chunk_rows=c, tile_m=t, swizzle=s)
+                for c in (128, 256, 1024) for t in (128, 256) for s in (True, False)] +
+               [dict(chunk_rows=c, col_band=nb) for c in (256, 1024) for nb in (3, 32)])
 
 
 @pytest.fixture(scope="module")
@@ -57,7 +58,8 @@ def rs_full(dt):
 
 
 @pytest.mark.parametrize("variant", RS_VARIANTS,
-                         ids=[f"c{v['chunk_rows']}-t{v['tile_m']}-{'sw' if v['swizzle'] else 'nosw'}"
+                         ids=[f"c{v['chunk_rows']}-t{v.get('tile_m', 0)}-"
+                              f"{'sw' if v.get('swizzle', True) else 'nosw'}-b{v.get('col_band', 0)}"
                               for v in RS_VARIANTS])
 def test_rs_full_size_bit_identical_across_variants(rs_full, variant):
     wl, inp, run, base = rs_full

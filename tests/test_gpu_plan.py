@@ -33,6 +33,11 @@ def test_device_plan_matches_oracle(dt, case, swizzle, bm):
     buf = torch.full((t,), -1, dtype=torch.int32, device="cuda")
     dt.swizzle_plan_device(a, dt.OP_RS, buf)
     assert buf.cpu().tolist() == oplan.rs_order(w, m, n, cr, bm, 256, swizzle)
+    for nb in (1, 3, 5):  # column bands
+        a = dt.make_args(w, m, n, 8, chunk_rows=cr, swizzle=swizzle, tile_m=bm, col_band=nb)
+        buf.fill_(-1)
+        dt.swizzle_plan_device(a, dt.OP_RS, buf)
+        assert buf.cpu().tolist() == oplan.rs_order(w, m, n, cr, bm, 256, swizzle, col_band=nb)
     if n % (8 * w) == 0:  # the AllToAll over the same rows, each rank's M/W of them
         a = dt.make_args(w, m, n, 8, chunk_rows=cr, swizzle=swizzle, tile_m=bm)
         t = dt.tile_count(a, dt.OP_A2A)

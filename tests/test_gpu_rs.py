@@ -75,6 +75,9 @@ def test_w4_bit_identical_across_variants(dt, w4):
         for group in [1, 3]:
             outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, group=group, tile_m=tile_m)
             assert all(bits_equal(o, b) for o, b in zip(outs, base))
+        for nb in [1, 3, 5]:  # column bands
+            outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, col_band=nb, tile_m=tile_m)
+            assert all(bits_equal(o, b) for o, b in zip(outs, base)), nb
         outs = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=256, fn=dt.gemm_rs_kernel_overlap,
                     tile_m=tile_m)
         assert all(bits_equal(o, b) for o, b in zip(outs, base))

@@ -47,10 +47,13 @@ _SIGS = {
     "dt_a2a_signals": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int64, _P]),
     "dt_tile_count": (ctypes.c_int64, [_P, ctypes.c_int]),
     "dt_tile_rows": (ctypes.c_int32, [_P, ctypes.c_int]),
+    "dt_col_band": (ctypes.c_int32, [_P, ctypes.c_int]),
     "dt_swizzle_plan": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64]),
     "dt_swizzle_plan_device": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int64, _P]),
     "dt_check": (ctypes.c_int, [_P, _P, _P]),
     "dt_debug_drop_transfer": (ctypes.c_int, [ctypes.c_int32]),
+    "dt_trace_bytes": (ctypes.c_size_t, [_P]),
+    "dt_trace_attach": (ctypes.c_int, [_P, ctypes.c_size_t]),
     "dt_ag_gemm_static_scratch": (ctypes.c_int, [_P, _P, _P, _P, _P]),
     "dt_static_scratch_check": (ctypes.c_int, [_P, _P]),
     "dt_ffn_ag_rs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_size_t,
@@ -74,7 +77,7 @@ class DtArgs(ctypes.Structure):
         ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
         ("timeout_us", ctypes.c_int64),
         ("num_sms", ctypes.c_int32), ("copy_ctas", ctypes.c_int32),
-        ("act", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("act", ctypes.c_int32), ("col_band", ctypes.c_int32),
     ]
 
 
@@ -82,8 +85,8 @@ class DtTunePoint(ctypes.Structure):
     """Mirror of ``dt_tune_point``."""
     _fields_ = [("chunk_rows", ctypes.c_int64), ("backend", ctypes.c_int32),
                 ("copy_ctas", ctypes.c_int32), ("swizzle", ctypes.c_int32),
-                ("group", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("ms", ctypes.c_float),
-                ("status", ctypes.c_int32)]
+                ("group", ctypes.c_int32), ("tile_m", ctypes.c_int32),
+                ("col_band", ctypes.c_int32), ("ms", ctypes.c_float), ("status", ctypes.c_int32)]
 
 
 class DtError(RuntimeError):
@@ -155,7 +158,8 @@ def _ptr_array(xs):
 def make_args(world_size: int, m: int, n: int, k: int, *, rank: int = 0, chunk_rows: int = 128,
               swizzle: bool = True, backend: str = "auto", out_dtype: str = "bf16",
               lda: int = 0, ldb: int = 0, ldc: int = 0, timeout_us: int = 0, num_sms: int = 0,
-              group: int = 8, copy_ctas: int = 0, act: str = "none", tile_m: int = 0) -> DtArgs:
+              group: int = 8, copy_ctas: int = 0, act: str = "none", tile_m: int = 0,
+              col_band: int = 0) -> DtArgs:
     a = DtArgs()
     lib().dt_args_default(ctypes.byref(a))
     a.world_size, a.rank, a.m, a.n, a.k = world_size, rank, m, n, k
@@ -170,6 +174,7 @@ def make_args(world_size: int, m: int, n: int, k: int, *, rank: int = 0, chunk_r
     a.copy_ctas = copy_ctas
     a.act = ACTS[act]
     a.tile_m = tile_m
+    a.col_band = col_band
     return a
 
 
@@ -295,6 +300,14 @@ def tile_rows(args: DtArgs, op: int) -> int:
     return int(r)
 
 
+def col_band(args: DtArgs, op: int) -> int:
+    """Column tiles per column band of the ReduceScatter / AllReduce order (Tn: one band)."""
+    r = lib().dt_col_band(ctypes.byref(args), op)
+    if r < 0:
+        _raise(DT_ERR_INVALID)
+    return int(r)
+
+
 def swizzle_plan(args: DtArgs, op: int) -> np.ndarray:
     """Host evaluation of the tile order (order[p] = tile run at position p)."""
     t = tile_count(args, op)
@@ -315,7 +328,8 @@ _BACKEND_NAMES = {v: k for k, v in BACKENDS.items()}
 def _points(buf, n):
     return [dict(chunk_rows=int(p.chunk_rows), backend=_BACKEND_NAMES.get(p.backend, p.backend),
                  copy_ctas=int(p.copy_ctas), swizzle=bool(p.swizzle), group=int(p.group),
-                 tile_m=int(p.tile_m), ms=float(p.ms), status=int(p.status)) for p in buf[:n]]
+                 tile_m=int(p.tile_m), col_band=int(p.col_band), ms=float(p.ms),
+                 status=int(p.status)) for p in buf[:n]]
 
 
 def tune_ag_gemm(shards, b, c, workspace, args: DtArgs, reps: int = 3, stream=None,
@@ -361,6 +375,44 @@ def check(workspace, stream=None):
     info = (ctypes.c_uint32 * 4)()
     st = lib().dt_check(_ptr(workspace), _stream(stream), info)
     return st, list(info)
+
+
+def trace_bytes(args: DtArgs) -> int:
+    n = lib().dt_trace_bytes(ctypes.byref(args))
+    if n == 0:
+        raise DtError(DT_ERR_INVALID, lib().dt_last_error().decode())
+    return int(n)
+
+
+def trace_attach(buf, nbytes=None):
+    """Attach a device buffer (int64 / uint8 tensor or pointer) for the AllGather-GEMM's debug
+    timeline; None detaches."""
+    if buf is None:
+        _raise(lib().dt_trace_attach(None, 0))
+    else:
+        _raise(lib().dt_trace_attach(_ptr(buf), _nbytes(buf, nbytes)))
+
+
+def trace_decode(words, args: DtArgs) -> dict:
+    """The timeline read back (a sequence of uint64 words) as times in microseconds from the
+    first CTA's start; None where nothing was recorded."""
+    none = (1 << 64) - 1
+    w = [int(x) & none for x in words]
+    t0 = w[0]
+
+    def rel(x):
+        return None if x == none else (x - t0) / 1e3
+
+    ms = args.m // args.world_size
+    nc = -(-ms // args.chunk_rows) if ms else 0
+    chunks = {}
+    for s in range(args.world_size):
+        for j in range(nc):
+            c = s * nc + j
+            chunks[(s, j)] = {"released_us": rel(w[4 + 3 * c]), "first_miss_us": rel(w[5 + 3 * c]),
+                              "first_read_us": rel(w[6 + 3 * c])}
+    return {"kernel_us": rel(w[1]), "stall_us_total": w[2] / 1e3, "stalled_waits": w[3],
+            "chunks": chunks}
 
 
 def static_scratch_check(stream=None):

@@ -5,6 +5,7 @@
 // copy-engine chunk transfer, kernel launches, and the kernel-level-overlap baselines.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstdarg>
@@ -45,6 +46,15 @@ dt_status cuda_fail(cudaError_t e, const char* what) {
     cudaError_t e_ = (call);                             \
     if (e_ != cudaSuccess) return cuda_fail(e_, #call);  \
   } while (0)
+
+// One NVTX range per library call (named after the call), visible to a profiler's timeline;
+// without a tool attached the push and pop do nothing.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ------------------------------------------------------------------------------ driver entry points
 typedef CUresult (*PfnEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -125,6 +135,9 @@ uint64_t default_timeout_ns() {
   return v;
 }
 
+// Bytes of B_q that one column band of the ReduceScatter order may use (automatic col_band).
+constexpr int64_t kBandBytes = 32ll << 20;
+
 // L2 cache policies of the fused kernels (KParams::l2_hints); DT_L2_HINTS overrides.
 int32_t l2_hints_setting() {
   static int32_t v = [] {
@@ -200,6 +213,19 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   d->Tm128 = static_cast<int32_t>(cdiv64(rows_tiled, kBM));
   d->geom = a2a ? make_geom_a2a(d->W, d->M, d->N, d->Cr, d->bm, kBN, d->G, d->swizzle ? 1 : 0)
               : make_geom(d->W, d->rank, d->M, d->N, d->Cr, d->bm, kBN, d->G, d->swizzle ? 1 : 0);
+  if (a->col_band < 0) return fail(DT_ERR_INVALID, "col_band must be >= 0");
+  if (op == DT_OP_GEMM_RS || op == DT_OP_GEMM_AR) {
+    // column bands: one band of B_q (K x band columns, bf16) within kBandBytes, so that it
+    // stays in L2 while the pass visits every destination
+    const int32_t tn = d->geom.Tn;
+    int32_t nb = a->col_band;
+    if (nb == 0) {
+      const int64_t b_bytes = d->K * d->N * 2;
+      const int64_t bands = std::max<int64_t>(1, cdiv64(b_bytes, kBandBytes));
+      nb = static_cast<int32_t>(cdiv64(tn, std::min<int64_t>(bands, std::max(tn, 1))));
+    }
+    d->geom.Nb = std::max(1, std::min(nb, std::max(tn, 1)));
+  }
   d->nC = d->geom.nC;
   d->Tm = d->geom.Tm;
   d->Tn = d->geom.Tn;
@@ -271,12 +297,8 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
 
 // ------------------------------------------------------------------------------ per-workspace state
 struct LayoutKey {
-  int op, W, rank, G, swz, bm;
+  int op, W, rank, G, swz, bm, nb;
   long long M, N, K, Cr;
-  bool operator==(const LayoutKey& o) const {
-    return op == o.op && W == o.W && rank == o.rank && G == o.G && swz == o.swz && bm == o.bm &&
-           M == o.M && N == o.N && K == o.K && Cr == o.Cr;
-  }
 };
 
 struct WsState {
@@ -287,17 +309,27 @@ std::mutex g_mu;
 std::map<const void*, WsState> g_ws;
 
 // host-side fault injection for failure-detection tests: transfer step whose copy and flag
-// write the next copy-engine AllGather call leaves out (-1: none)
+// write the next AllGather call leaves out (-1: none)
 int32_t g_drop_transfer = -1;
 
+// debug timeline of the fused AllGather-GEMM calls (dt_trace_attach), caller-owned device
+// memory; null when tracing is off
+std::mutex g_trace_mu;
+void* g_trace = nullptr;
+size_t g_trace_bytes = 0;
+
+size_t trace_bytes_for(int32_t W, int32_t nC) {
+  return (static_cast<size_t>(kTraceHead) + 3 * static_cast<size_t>(W) * nC) * 8;
+}
+
 LayoutKey key_of(const Derived& d) {
-  return LayoutKey{d.op, d.W, d.rank, d.G, d.swizzle ? 1 : 0, d.bm, d.M, d.N, d.K, d.Cr};
+  return LayoutKey{d.op, d.W, d.rank, d.G, d.swizzle ? 1 : 0, d.bm, d.geom.Nb, d.M, d.N, d.K, d.Cr};
 }
 
 // 64-bit tag of the workspace layout (FNV-1a over the key), never 0
 unsigned long long layout_tag(const Derived& d) {
   const LayoutKey k = key_of(d);
-  const long long v[10] = {k.op, k.W, k.rank, k.G, k.swz, k.bm, k.M, k.N, k.K, k.Cr};
+  const long long v[11] = {k.op, k.W, k.rank, k.G, k.swz, k.bm, k.nb, k.M, k.N, k.K, k.Cr};
   unsigned long long h = 1469598103934665603ull;
   for (long long x : v) {
     for (int b = 0; b < 8; ++b) {
@@ -529,6 +561,22 @@ void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
   p.act = d.act;
   p.drop_chunk = -1;
   p.l2_hints = l2_hints_setting();
+  p.trace = nullptr;
+}
+
+// Point the kernel at the attached timeline (if any) and reset it on `stream`: the min words to
+// all ones, the sums to zero.
+dt_status attach_trace(KParams& p, const Derived& d, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (g_trace == nullptr) return DT_OK;
+  const size_t need = trace_bytes_for(d.W, d.nC);
+  if (g_trace_bytes < need)
+    return fail(DT_ERR_INVALID, "the attached trace buffer holds %zu bytes, this call needs %zu",
+                g_trace_bytes, need);
+  DT_CUDA(cudaMemsetAsync(g_trace, 0xff, need, stream));
+  DT_CUDA(cudaMemsetAsync(reinterpret_cast<uint8_t*>(g_trace) + 8, 0, 24, stream));
+  p.trace = reinterpret_cast<unsigned long long*>(g_trace);
+  return DT_OK;
 }
 
 // ------------------------------------------------------------------------------ AllGather
@@ -660,7 +708,7 @@ void dt_args_default(dt_args* a) {
   a->chunk_rows = 128;
 }
 
-int dt_version(void) { return 200; }  // 2.0.0: dt_tune_point carries tile_m
+int dt_version(void) { return 300; }  // 3.0.0: dt_args.col_band, dt_tune_point carries col_band
 
 size_t dt_sizeof_args(void) { return sizeof(dt_args); }
 size_t dt_sizeof_tune_point(void) { return sizeof(dt_tune_point); }
@@ -712,6 +760,12 @@ int32_t dt_tile_rows(const dt_args* a, int op) {
   return d.bm;
 }
 
+int32_t dt_col_band(const dt_args* a, int op) {
+  Derived d;
+  if (derive(a, op, &d) != DT_OK) return -1;
+  return d.geom.Nb;
+}
+
 dt_status dt_swizzle_plan(const dt_args* a, int op, int32_t* order, int64_t len) {
   g_last_error.clear();
   Derived d;
@@ -747,6 +801,7 @@ dt_status dt_swizzle_plan_device(const dt_args* a, int op, int32_t* order_dev, i
 
 dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* ws,
                      size_t ws_bytes, const dt_args* a, void* stream_) {
+  NvtxRange range("dt_ag_gemm");
   g_last_error.clear();
   Derived d;
   dt_status s = ag_common(a_shards, b, c, ws, ws_bytes, a, &d);
@@ -777,6 +832,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
   if (p.own_in_place &&
       (s = make_tmap(&p.tmA[1], a_shards[d.rank], d.K, d.Ms, d.lda * 2, 64, kBM)) != DT_OK)
     return s;
+  if ((s = attach_trace(p, d, stream)) != DT_OK) return s;
 
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
   const int grid = grid_for(d, d.T, sms);
@@ -836,6 +892,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
 
 dt_status dt_allgather(const void* const* a_shards, void* out, void* ws, size_t ws_bytes,
                        const dt_args* a, void* stream_) {
+  NvtxRange range("dt_allgather");
   g_last_error.clear();
   if (!a) return fail(DT_ERR_INVALID, "args is NULL");
   // the GEMM's N, B and C play no part: the geometry is derived with a placeholder N
@@ -907,6 +964,7 @@ dt_status dt_allgather(const void* const* a_shards, void* out, void* ws, size_t 
 
 dt_status dt_ag_gemm_kernel_overlap(const void* const* a_shards, const void* b, void* c,
                                     void* ws, size_t ws_bytes, const dt_args* a, void* stream_) {
+  NvtxRange range("dt_ag_gemm_kernel_overlap");
   g_last_error.clear();
   Derived d;
   dt_status s = ag_common(a_shards, b, c, ws, ws_bytes, a, &d);
@@ -1032,6 +1090,7 @@ static dt_status zero_reduce_outputs(const Derived& d, void* const* out, cudaStr
 
 static dt_status reduce_fused(const void* const* a_, const void* const* b_, void* const* out,
                               void* ws, size_t ws_bytes, const dt_args* a, void* stream_, int op) {
+  NvtxRange range(op == DT_OP_GEMM_RS ? "dt_gemm_rs" : "dt_gemm_ar");
   g_last_error.clear();
   Derived d;
   dt_status s = rs_common(a_, b_, out, ws, ws_bytes, a, op, &d);
@@ -1053,6 +1112,7 @@ static dt_status reduce_fused(const void* const* a_, const void* const* b_, void
 static dt_status reduce_kernel_overlap(const void* const* a_, const void* const* b_,
                                        void* const* out, void* ws, size_t ws_bytes,
                                        const dt_args* a, void* stream_, int op) {
+  NvtxRange range(op == DT_OP_GEMM_RS ? "dt_gemm_rs_kernel_overlap" : "dt_gemm_ar_kernel_overlap");
   g_last_error.clear();
   Derived d;
   dt_status s = rs_common(a_, b_, out, ws, ws_bytes, a, op, &d);
@@ -1171,6 +1231,7 @@ static dt_status zero_a2a_outputs(const Derived& d, void* const* out, cudaStream
 
 dt_status dt_gemm_a2a(const void* const* a_, const void* const* b_, void* const* out, void* ws,
                       size_t ws_bytes, const dt_args* a, void* stream_) {
+  NvtxRange range("dt_gemm_a2a");
   g_last_error.clear();
   Derived d;
   dt_status s = a2a_common(a_, b_, out, ws, ws_bytes, a, &d);
@@ -1193,6 +1254,7 @@ dt_status dt_gemm_a2a(const void* const* a_, const void* const* b_, void* const*
 dt_status dt_gemm_a2a_kernel_overlap(const void* const* a_, const void* const* b_,
                                      void* const* y, void* const* out, void* ws, size_t ws_bytes,
                                      const dt_args* a, void* stream_) {
+  NvtxRange range("dt_gemm_a2a_kernel_overlap");
   g_last_error.clear();
   Derived d;
   dt_status s = a2a_common(a_, b_, out, ws, ws_bytes, a, &d);
@@ -1284,6 +1346,7 @@ void tune_one(const TuneCtx& t, dt_args& cand, int op, Call&& call, dt_tune_poin
   pt->swizzle = cand.swizzle;
   pt->group = cand.group;
   pt->tile_m = cand.tile_m;
+  pt->col_band = cand.col_band;
   pt->ms = -1.0f;
   const size_t need = dt_workspace_size(&cand, op);
   if (need == 0 || need > t.ws_bytes) {
@@ -1395,6 +1458,7 @@ dt_status tune_finish(std::vector<dt_tune_point>& pts, dt_args* a, dt_tune_point
   a->swizzle = pts[best].swizzle;
   a->group = pts[best].group;
   a->tile_m = pts[best].tile_m;
+  a->col_band = pts[best].col_band;
   return DT_OK;
 }
 
@@ -1472,14 +1536,20 @@ dt_status dt_tune_reduce(int op, const void* const* a_, const void* const* b_, v
     return op == DT_OP_GEMM_RS ? dt_gemm_rs(a_, b_, out, ws, ws_bytes, &cand, stream)
                                : dt_gemm_ar(a_, b_, out, ws, ws_bytes, &cand, stream);
   };
+  // column bands (ReduceScatter / AllReduce): as given, and one band when that differs
+  std::vector<int32_t> bands = {a->col_band};
+  if (op != DT_OP_GEMM_A2A && d.geom.Nb < d.Tn) bands.push_back(d.Tn);
   std::vector<dt_args> cands;
-  for (int64_t cr : chunk_candidates(d.Ms)) {
-    for (int g : {4, 8, 16}) {
-      dt_args cand = *a;
-      cand.chunk_rows = cr;
-      cand.swizzle = 1;
-      cand.group = g;
-      cands.push_back(cand);
+  for (int32_t nb : bands) {
+    for (int64_t cr : chunk_candidates(d.Ms)) {
+      for (int g : {4, 8, 16}) {
+        dt_args cand = *a;
+        cand.chunk_rows = cr;
+        cand.swizzle = 1;
+        cand.group = g;
+        cand.col_band = nb;
+        cands.push_back(cand);
+      }
     }
   }
   std::vector<dt_tune_point> pts = tune_all(t, cands, op, call);
@@ -1508,6 +1578,21 @@ dt_status dt_ffn_ag_rs(const void* const* x_shards, const void* w1, const void* 
   for (int q = 0; q < W; ++q)
     a_blocks[q] = reinterpret_cast<const uint8_t*>(h) + static_cast<size_t>(q) * rs->k * 2;
   return dt_gemm_rs(a_blocks, w2, out, ws_rs, ws_rs_bytes, &r, stream);
+}
+
+size_t dt_trace_bytes(const dt_args* a) {
+  Derived d;
+  if (derive(a, DT_OP_AG_GEMM, &d) != DT_OK) return 0;
+  return trace_bytes_for(d.W, d.nC);
+}
+
+dt_status dt_trace_attach(void* trace, size_t bytes) {
+  g_last_error.clear();
+  if (trace != nullptr && !is_aligned(trace, 8)) return fail(DT_ERR_INVALID, "trace must be 8-byte aligned");
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace = trace;
+  g_trace_bytes = trace ? bytes : 0;
+  return DT_OK;
 }
 
 dt_status dt_debug_drop_transfer(int32_t step) {

@@ -127,7 +127,18 @@ struct KParams {
   int32_t l2_hints;        // L2 cache policies: bit 0, ReduceScatter running sums, park slots
                            // and final sums stream through L2 (evict first); bit 1, B's k-blocks
                            // stay (evict last)
+  unsigned long long* trace;  // AG debug timeline (global timer, ns), or null; see trace_*
 };
+
+// AG debug timeline, in 64-bit words: [0] first CTA start (min), [1] last CTA exit (max),
+// [2] time the producers spent waiting for ready flags (sum over waits), [3] waits that had to
+// wait; then per chunk c: [4 + 3c] release of its ready flag by the in-kernel transfer (min),
+// [5 + 3c] first wait that found it missing began (min), [6 + 3c] first consumer passed its
+// flag (min).  The host fills the min words with all ones and the others with zero.
+constexpr int kTraceHead = 4;
+__device__ __forceinline__ void trace_min(unsigned long long* tr, int64_t w) {
+  if (tr != nullptr) atomicMin(tr + w, static_cast<unsigned long long>(globaltimer_ns()));
+}
 
 struct SmemLayout {
   uint8_t* a;
@@ -193,11 +204,25 @@ __device__ __forceinline__ bool wait_bar(const KParams& p, const SmemLayout& L, 
 // Bounded acquire-poll of a chunk's ready flag.
 static __device__ __noinline__ bool wait_flag(const KParams& p, const SmemLayout& L, int32_t c) {
   const uint32_t* f = p.ready + c;
-  if (ld_acquire_gpu(f) == p.epoch) return true;
+  unsigned long long* tr = p.trace;
+  const int64_t tw = kTraceHead + 3 * static_cast<int64_t>(c);
+  if (ld_acquire_gpu(f) == p.epoch) {
+    trace_min(tr, tw + 2);
+    return true;
+  }
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     __nanosleep(it < 64 ? 32 : 256);
-    if (ld_acquire_gpu(f) == p.epoch) return true;
+    if (ld_acquire_gpu(f) == p.epoch) {
+      if (tr != nullptr) {
+        const uint64_t t1 = globaltimer_ns();
+        atomicMin(tr + tw + 1, static_cast<unsigned long long>(t0));
+        atomicMin(tr + tw + 2, static_cast<unsigned long long>(t1));
+        atomicAdd(tr + 2, static_cast<unsigned long long>(t1 - t0));
+        atomicAdd(tr + 3, 1ull);
+      }
+      return true;
+    }
     if ((it & 7u) == 0u) {
       if (*L.abort_flag) return false;
       if (globaltimer_ns() - t0 > p.timeout_ns) {
@@ -1025,6 +1050,7 @@ __device__ __forceinline__ void signal_piece(const KParams& p, int32_t c, int32_
   if (old + 1u == static_cast<uint32_t>(total)) {
     p.pieces_done[c] = 0u;
     st_release_gpu(p.ready + c, p.epoch);  // notify: chunk c has landed
+    trace_min(p.trace, kTraceHead + 3 * static_cast<int64_t>(c));
   }
 }
 
@@ -1220,6 +1246,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) trace_min(p.trace, 0);
   if (threadIdx.x < kReadyBitsWords) L.ready_bits[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -1292,6 +1319,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   // the tile order and clearing the control arrays
   if (p.tag != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && *(volatile uint32_t*)p.err == 0u)
     *p.tag = p.tag_value;
+  if (p.trace != nullptr && threadIdx.x == 0)
+    atomicMax(p.trace + 1, static_cast<unsigned long long>(globaltimer_ns()));
 }
 
 }  // namespace dt

@@ -16,9 +16,11 @@
 //   AG: pos(s, j) = ((s - r) mod W) * nC + j;  key(i) = max pos of the chunks m-tile i reads;
 //       order = sort (i, n) by (key(i), band(i), n, i)
 //   RS: dpos_q(s) = (s - q - 1) mod W;  key(q, i) = min over written chunks of dpos*nC + j;
-//       order = sort (q, i, n) by (q, key, band, n, i): the virtual source ranks one after
-//       another, each in its own scatter order, so every destination receives its partials
-//       in source order q = 0 .. W-1 and one rank's B_q stays in L2 for all its send steps
+//       order = sort (q, i, n) by (q, n / Nb, key, band, n, i): the virtual source ranks one
+//       after another, each in its own scatter order, so every destination receives its
+//       partials in source order q = 0 .. W-1; inside a rank's pass the column tiles go in
+//       bands of Nb, each band repeating the scatter order over every destination, so only
+//       one band of B_q is in use at a time (Nb = Tn: one band)
 //   A2A (GEMM-AllToAll, rows local to each rank, columns split by destination h):
 //       key(q, i, h) = dpos_q(h)*nC + (first chunk of m-tile i);
 //       order = sort (q, i, h, c) by (q, key, band, c, i): the virtual source ranks one after
@@ -45,6 +47,7 @@ struct Geom {
   int32_t W, rank, BM, BN, nC, Tm, Tn, G, swizzle;
   int64_t Nw;   // AllToAll: columns per destination (N / W); 0 otherwise
   int32_t Tnw;  // AllToAll: column tiles per destination; 0 otherwise
+  int32_t Nb;   // ReduceScatter: column tiles per column band (Tn: one band)
 };
 
 DT_HD int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -69,6 +72,7 @@ DT_HD Geom make_geom(int32_t W, int32_t rank, int64_t M, int64_t N, int64_t Cr, 
   g.Tn = static_cast<int32_t>(cdiv64(N, BN));
   g.Nw = 0;
   g.Tnw = 0;
+  g.Nb = g.Tn;
   return g;
 }
 
@@ -81,6 +85,7 @@ DT_HD Geom make_geom_a2a(int32_t W, int64_t M, int64_t N, int64_t Cr, int32_t BM
   g.Tm = static_cast<int32_t>(cdiv64(g.Ms, BM));
   g.Tnw = static_cast<int32_t>(cdiv64(g.Nw, BN));
   g.Tn = W * g.Tnw;
+  g.Nb = g.Tn;
   return g;
 }
 
@@ -169,7 +174,9 @@ DT_HD int32_t rs_count_below(const Geom& g, int32_t q, int32_t rot0, int32_t k) 
   }
   return lo;
 }
-// execution position of ReduceScatter tile (q, i, n)
+// execution position of ReduceScatter tile (q, i, n): rank q's block of Tm*Tn positions, the
+// full column bands before n's (Tm*Nb each), then n's band (Nbw columns wide) laid out like a
+// band-less order over those columns
 DT_HD int64_t rs_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
   if (!g.swizzle) return (static_cast<int64_t>(q) * g.Tm + i) * g.Tn + n;
   const int32_t rot0 = rs_rot0(g, q);
@@ -177,7 +184,10 @@ DT_HD int64_t rs_position(const Geom& g, int32_t q, int32_t i, int32_t n) {
   const int32_t k = rs_key(g, q, rot0, u);
   const int32_t ug = rs_count_below(g, q, rot0, k);
   const int32_t ue = rs_count_below(g, q, rot0, k + 1);
-  return (static_cast<int64_t>(q) * g.Tm + ug) * g.Tn + band_offset(ug, ue, u, n, g.Tn, g.G);
+  const int32_t b = n / g.Nb;
+  const int32_t nbw = min32(g.Nb, g.Tn - b * g.Nb);
+  return static_cast<int64_t>(q) * g.Tm * g.Tn + static_cast<int64_t>(b) * g.Tm * g.Nb +
+         static_cast<int64_t>(ug) * nbw + band_offset(ug, ue, u, n - b * g.Nb, nbw, g.G);
 }
 
 // ------------------------------------------------------------------ all-to-all (GEMM-AllToAll)
