@@ -135,6 +135,19 @@ uint64_t default_timeout_ns() {
   return v;
 }
 
+// The fused AllGather-GEMM stores C through TMA (1) or per thread (0); DT_C_TMA overrides.
+int32_t c_tma_setting() {
+  static int32_t v = [] {
+    const char* e = getenv("DT_C_TMA");
+    return e ? (atoi(e) != 0 ? 1 : 0) : 1;
+  }();
+  return v;
+}
+
+// C's tensor map for the TMA-store epilogue: 32-column x 128-row boxes; bf16 boxes are dense
+// 64-byte rows, fp32 boxes 128-byte rows in the 128-byte swizzle.
+dt_status make_c_tmap(CUtensorMap* tm, void* c, int64_t rows, int64_t cols, int64_t ldc, bool f32);
+
 // Bytes of B_q that one column band of the ReduceScatter order may use (automatic col_band).
 constexpr int64_t kBandBytes = 32ll << 20;
 
@@ -528,6 +541,12 @@ void set_drop_chunk(KParams& p, const Derived& d, int32_t drop) {
   p.drop_chunk = s * d.nC + j;
 }
 
+dt_status make_c_tmap(CUtensorMap* tm, void* c, int64_t rows, int64_t cols, int64_t ldc, bool f32) {
+  return make_tmap(tm, c, cols, rows, static_cast<uint64_t>(ldc) * (f32 ? 4 : 2), 32, kBM,
+                   f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 dt_status check_ws(const Derived& d, void* ws, size_t bytes) {
   if (!ws) return fail(DT_ERR_WORKSPACE, "workspace is NULL");
   if (!is_aligned(ws, 256)) return fail(DT_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -833,6 +852,8 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
       (s = make_tmap(&p.tmA[1], a_shards[d.rank], d.K, d.Ms, d.lda * 2, 64, kBM)) != DT_OK)
     return s;
   if ((s = attach_trace(p, d, stream)) != DT_OK) return s;
+  p.c_tma = c_tma_setting();
+  if (p.c_tma && (s = make_c_tmap(&p.tmOut[0], c, d.M, d.N, d.ldc, d.f32)) != DT_OK) return s;
 
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
   const int grid = grid_for(d, d.T, sms);

@@ -65,14 +65,15 @@ enum DevCode : uint32_t {
 };
 
 // Dynamic shared memory of a kernel instance: alignment slack, the operand ring, two 16 KiB
-// staging buffers (AllGather TMA transfer, or ReduceScatter running-sum tiles), flags.
-__host__ __device__ constexpr bool has_staging(bool rs, int copy_mode) {
-  return rs || copy_mode == kCopyTma;
+// staging buffers (AllGather: the co-located TMA transfer, else C's boxes on their way to a
+// TMA store; ReduceScatter: running-sum tiles), flags.
+__host__ __device__ constexpr bool has_staging(int op, int copy_mode) {
+  return op != 2 /* kOpA2A */ || copy_mode == kCopyTma;
 }
 // cl: CTAs per cluster (1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile)
-__host__ __device__ constexpr int kernel_smem_bytes(bool rs, int copy_mode, int cl) {
-  return 1024 + stages(cl > 1, has_staging(rs, copy_mode)) * (kAStage + b_stage_bytes(cl > 1)) +
-         (has_staging(rs, copy_mode) ? 2 * kCopyBuf : 0) + kMiscBytes;
+__host__ __device__ constexpr int kernel_smem_bytes(int op, int copy_mode, int cl) {
+  return 1024 + stages(cl > 1, has_staging(op, copy_mode)) * (kAStage + b_stage_bytes(cl > 1)) +
+         (has_staging(op, copy_mode) ? 2 * kCopyBuf : 0) + kMiscBytes;
 }
 
 struct KParams {
@@ -128,6 +129,8 @@ struct KParams {
                            // and final sums stream through L2 (evict first); bit 1, B's k-blocks
                            // stay (evict last)
   unsigned long long* trace;  // AG debug timeline (global timer, ns), or null; see trace_*
+  int32_t c_tma;           // AG: C leaves through the staging buffers as TMA stores (tmOut[0],
+                           // 32-column boxes clipped at M and N); 0: each thread stores its row
 };
 
 // AG debug timeline, in 64-bit words: [0] first CTA start (min), [1] last CTA exit (max),
@@ -153,15 +156,14 @@ struct SmemLayout {
   volatile int8_t* chain;        // RS: per piece, first parked partial this tile folds (-1)
   uint32_t* ready_bits;
   int ns;  // pipeline stages
-  // barrier slots: full[ns], empty[ns], tfull[2], tempty[2], copyb[2], fin (at most 21);
-  // slots 24..31 belong to the dedicated transfer CTAs' workers
+  // barrier slots: full[ns], empty[ns], tfull[2], tempty[2], copyb[2], fin (at most 21); on a
+  // dedicated transfer CTA all 32 slots belong to its copy workers
   __device__ uint32_t full(int s) const { return smem_u32(bars + s); }
   __device__ uint32_t empty(int s) const { return smem_u32(bars + ns + s); }
   __device__ uint32_t tfull(int a) const { return smem_u32(bars + 2 * ns + a); }
   __device__ uint32_t tempty(int a) const { return smem_u32(bars + 2 * ns + 2 + a); }
   __device__ uint32_t copyb(int b) const { return smem_u32(bars + 2 * ns + 4 + b); }
   __device__ uint32_t fin() const { return smem_u32(bars + 2 * ns + 6); }
-  __device__ uint32_t worker(int w) const { return smem_u32(bars + 24 + w); }
 };
 
 __device__ __forceinline__ void raise_error(const KParams& p, uint32_t code, uint32_t site,
@@ -725,11 +727,14 @@ __device__ void fold_chain(const KParams& p, const SmemLayout& L, int32_t s, int
 
 template <int OP, bool F32, int CL>
 __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tmem_base,
-                             int warp, int lane) {
+                             int warp, int lane, bool staging_free) {
   constexpr bool PAIR = CL > 1;
   constexpr bool RS = OP == kOpRS;
   constexpr bool A2A = OP == kOpA2A;
   constexpr bool kStoreF32 = RS || F32;  // ReduceScatter partials are fp32
+  // AllGather: C's 32-column boxes go out as TMA stores from the staging buffers (which the
+  // co-located TMA transfer, when there is one, needs for itself)
+  const bool c_tma = OP == kOpAG && p.c_tma != 0 && staging_free;
   const int qd = warp - 4;  // TMEM lane quadrant this warp may read
   const int et = threadIdx.x - 128;
   const bool fused_rs = RS && !p.plain;
@@ -941,9 +946,52 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
         fence_proxy_async_global();
       }
     }
+    if (c_tma) {
+      // Each thread writes its row of the box into a staging buffer (bf16: dense 64-byte rows;
+      // fp32: 128-byte rows in the 128-byte swizzle), then one thread stores the box; the
+      // tensor map clips rows at M and columns at N.  A buffer is rewritten once the store
+      // issued from it two boxes earlier has read it.
+      const int r = qd * 32 + lane;
+      const int ncb = static_cast<int>(min64(kBN, p.g.N - ti.col0) + 31) / 32;
+#pragma unroll 1
+      for (int cb = 0; cb < ncb; ++cb) {
+        uint8_t* buf = L.copy + (stage_ctr & 1u) * kCopyBuf;
+        uint32_t v[32];
+        tmem_ld32(tbase + cb * 32, v);
+        if (p.act) apply_activation(v, p.act);
+        if (et == 0) bulk_wait_read<1>();
+        named_bar_sync(1, 128);
+        if (F32) {
+          float4* rowp = reinterpret_cast<float4*>(buf + r * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            rowp[c ^ (r & 7)] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                            __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+        } else {
+          uint4* orow = reinterpret_cast<uint4*>(buf + r * 64);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(v[8 * u + 0], v[8 * u + 1]);
+            w.y = pack_bf16x2(v[8 * u + 2], v[8 * u + 3]);
+            w.z = pack_bf16x2(v[8 * u + 4], v[8 * u + 5]);
+            w.w = pack_bf16x2(v[8 * u + 6], v[8 * u + 7]);
+            orow[u] = w;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (et == 0) {
+          tma_store_2d(&p.tmOut[0], smem_u32(buf), static_cast<int32_t>(ti.col0 + cb * 32),
+                       static_cast<int32_t>(ti.row0));
+          bulk_commit();
+        }
+        ++stage_ctr;
+      }
+    }
 #pragma unroll 1
     for (int cb = 0; cb < kBN / 32; ++cb) {
-      if (tma_tile) break;
+      if (tma_tile || c_tma) break;
       const int64_t c0 = ti.col0 + cb * 32;
       if (c0 >= ti.col_end) break;
       uint32_t v[32];
@@ -1038,6 +1086,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
       named_bar_sync(1, 128);
     }
   }
+  if (c_tma && et == 0) bulk_wait<0>();  // C's last boxes are in global memory
 }
 
 // ============================================================================ chunk transfer
@@ -1104,28 +1153,32 @@ __device__ __forceinline__ void for_each_piece(const KParams& p, int32_t wid, in
   }
 }
 
-// One TMA bulk-copy worker (one thread): staging buffers `stage` and `stage + kCopyBuf`,
-// completion barriers bar0 / bar1.  Piece i is loaded into buffer i & 1 before the worker waits
-// for piece i - 1's load, so a load is always in flight while the previous piece is stored; a
-// piece is counted towards its chunk once its store's writes are complete, which the worker
-// checks one store later.
+// One TMA bulk-copy worker (one thread): `nbuf` staging buffers of kCopyBuf bytes at `stage`,
+// completion barriers bar0, bar0 + 8, ... (one per buffer).  Piece i goes through buffer
+// i % nbuf; the worker keeps nbuf - 1 loads in flight and stores the oldest piece once its load
+// has landed, so loads and stores overlap; a piece is counted towards its chunk once its
+// store's writes are complete, which the worker checks one store later.
 struct CopyJob {
   uint8_t* dst;
   Piece pc;
   int32_t c, total;
 };
+constexpr uint32_t kMaxCopyBufs = 4;
+constexpr uint32_t kDedicatedCopyBufs = 3;  // per worker on a dedicated transfer CTA (48 KiB)
 
 static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32_t wid, int32_t nw,
-                                    uint8_t* stage, uint32_t bar0, uint32_t bar1) {
+                                    uint8_t* stage, uint32_t bar0, uint32_t nbuf) {
   uint32_t issued = 0;  // loads issued
-  uint32_t landed = 0;  // loads waited for (and their pieces stored)
-  CopyJob prev = {};    // the piece of load issued - 1
+  uint32_t stored = 0;  // loads waited for and their pieces' stores issued
+  CopyJob jobs[kMaxCopyBufs] = {};  // the piece in each buffer
   int32_t st_c = -1, st_total = 0;  // the piece stored last, not yet counted
-  auto bar_of = [&](uint32_t i) { return (i & 1u) ? bar1 : bar0; };
-  auto buf_of = [&](uint32_t i) { return smem_u32(stage + (i & 1u) * kCopyBuf); };
-  auto store_piece = [&](uint32_t i, const CopyJob& job) -> bool {
-    if (!wait_bar(p, L, bar_of(i), (i >> 1) & 1u, 500 + (i & 1u))) return false;
-    landed = i + 1;
+  auto bar_of = [&](uint32_t i) { return bar0 + 8u * (i % nbuf); };
+  auto buf_of = [&](uint32_t i) { return smem_u32(stage + (i % nbuf) * kCopyBuf); };
+  auto par_of = [&](uint32_t i) { return (i / nbuf) & 1u; };  // use i / nbuf of its barrier
+  auto store_oldest = [&]() -> bool {
+    const uint32_t i = stored;
+    if (!wait_bar(p, L, bar_of(i), par_of(i), 500 + (i % nbuf))) return false;
+    const CopyJob& job = jobs[i % nbuf];
     const uint32_t buf = buf_of(i);
     const uint32_t tot = job.pc.nbytes * static_cast<uint32_t>(job.pc.nr);
     if (job.pc.nbytes == static_cast<uint32_t>(p.row_bytes) || job.pc.nr == 1) {
@@ -1136,6 +1189,7 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32
                  job.pc.nbytes);
     }
     bulk_commit();
+    ++stored;
     bulk_wait<1>();  // the previous piece's writes are complete
     if (st_c >= 0) signal_piece(p, st_c, st_total);
     st_c = job.c;
@@ -1147,11 +1201,9 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32
                                        const Piece& pc) -> bool {
     const int64_t row_in_shard = static_cast<int64_t>(j) * p.g.Cr + pc.r0;
     const uint8_t* src = p.shard[s] + row_in_shard * p.lda_src * 2 + pc.boff;
-    const CopyJob cur = {
-        p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard) * p.ld_gather * 2 + pc.boff,
-        pc, c, total};
-    // buffer issued & 1 was last read by the store of piece issued - 2, the only store that
-    // may still be in flight
+    // buffer issued % nbuf was last read by the store of piece issued - nbuf, which has been
+    // issued (at most nbuf - 1 pieces are loaded but not stored) and in steady state is the
+    // newest store: wait until every issued store has read its shared memory
     bulk_wait_read<0>();
     const uint32_t i = issued;
     const uint32_t buf = buf_of(i), bar = bar_of(i);
@@ -1163,18 +1215,21 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32
       for (int32_t r = 0; r < pc.nr; ++r)
         bulk_g2s(buf + r * pc.nbytes, src + static_cast<int64_t>(r) * p.lda_src * 2, pc.nbytes, bar);
     }
+    jobs[i % nbuf] = {
+        p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard) * p.ld_gather * 2 + pc.boff,
+        pc, c, total};
     ++issued;
-    const bool ok = i == 0 || store_piece(i - 1, prev);
-    prev = cur;
-    return ok;
+    // keep nbuf - 1 loads in flight: store the oldest piece once nbuf are outstanding
+    return issued - stored < nbuf || store_oldest();
   });
-  if (!*L.abort_flag && landed < issued) store_piece(issued - 1, prev);
+  while (!*L.abort_flag && stored < issued && store_oldest()) {
+  }
   bulk_wait<0>();
   if (!*L.abort_flag && st_c >= 0) signal_piece(p, st_c, st_total);
-  // after an abort, the loads still in flight (at most two) land before the CTA can exit
-  for (uint32_t i = landed; i < issued; ++i) {
+  // after an abort, the loads still in flight (at most nbuf) land before the CTA can exit
+  for (uint32_t i = stored; i < issued; ++i) {
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar_of(i), (i >> 1) & 1u) && globaltimer_ns() - t0 < p.timeout_ns) {
+    while (!mbar_try_wait(bar_of(i), par_of(i)) && globaltimer_ns() - t0 < p.timeout_ns) {
     }
   }
 }
@@ -1225,7 +1280,10 @@ template <int OP, int COPY, bool F32, int CL>
 __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_constant__ KParams p) {
   static_assert(CL == 1 || CL == 2, "one CTA or a CTA pair per tile");
   constexpr bool PAIR = CL > 1;
-  constexpr int NS = stages(PAIR, has_staging(OP == kOpRS, COPY));
+  constexpr int NS = stages(PAIR, has_staging(OP, COPY));
+  static_assert(COPY != kCopyTma ||
+                    4 * kDedicatedCopyBufs * kCopyBuf <= NS * (kAStage + b_stage_bytes(PAIR)),
+                "the dedicated TMA workers' buffers fit in the operand ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1234,7 +1292,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   L.a = base;
   L.b = L.a + NS * kAStage;
   L.copy = L.b + NS * b_stage_bytes(PAIR);
-  uint8_t* misc = L.copy + (has_staging(OP == kOpRS, COPY) ? 2 * kCopyBuf : 0);
+  uint8_t* misc = L.copy + (has_staging(OP, COPY) ? 2 * kCopyBuf : 0);
   L.bars = reinterpret_cast<uint64_t*>(misc);  // up to 32 barriers
   L.tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   L.abort_flag = reinterpret_cast<volatile int*>(misc + 260);
@@ -1248,18 +1306,23 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) trace_min(p.trace, 0);
   if (threadIdx.x < kReadyBitsWords) L.ready_bits[threadIdx.x] = 0u;
+  const bool copier = static_cast<int32_t>(blockIdx.x) < p.copy_ctas;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(L.full(s), 1);
-      mbar_init(L.empty(s), 1);
+    if (copier) {
+      // a dedicated transfer CTA runs no GEMM: every barrier slot is a copy worker's
+      for (int s = 0; s < 32; ++s) mbar_init(smem_u32(L.bars + s), 1);
+    } else {
+      for (int s = 0; s < NS; ++s) {
+        mbar_init(L.full(s), 1);
+        mbar_init(L.empty(s), 1);
+      }
+      for (int a = 0; a < 2; ++a) {
+        mbar_init(L.tfull(a), 1);
+        mbar_init(L.tempty(a), PAIR ? 8 : 4);  // the epilogue warps of the tile's CTA(s)
+        mbar_init(L.copyb(a), 1);
+      }
+      mbar_init(L.fin(), 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(L.tfull(a), 1);
-      mbar_init(L.tempty(a), PAIR ? 8 : 4);  // the epilogue warps of the tile's CTA(s)
-      mbar_init(L.copyb(a), 1);
-    }
-    mbar_init(L.fin(), 1);
-    for (int w = 0; w < 8; ++w) mbar_init(L.worker(w), 1);  // dedicated workers
     *L.abort_flag = 0;
     *L.unit_flag = 0;
     mbar_init_fence();
@@ -1268,7 +1331,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     tma_prefetch_desc(&p.tmA[0]);
     tma_prefetch_desc(&p.tmB[0]);
   }
-  const bool copier = static_cast<int32_t>(blockIdx.x) < p.copy_ctas;
   if (warp == 1 && !copier) {
     if constexpr (PAIR) tmem_alloc_pair(smem_u32(L.tmem_slot), kTmemCols);
     else tmem_alloc(smem_u32(L.tmem_slot), kTmemCols);
@@ -1280,11 +1342,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   const uint32_t tmem_base = copier ? 0u : *L.tmem_slot;
 
   if (copier) {
-    // dedicated transfer CTA: no GEMM; the operand ring becomes four 32 KiB staging pairs
+    // dedicated transfer CTA: no GEMM; the operand ring becomes four workers' staging rings
+    // of kDedicatedCopyBufs 16 KiB buffers
     if (OP == kOpAG && !p.plain) {
       if (COPY == kCopyTma && warp < 4 && lane == 0)
         run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x) * 4 + warp, p.copy_ctas * 4,
-                     L.a + warp * 2 * kCopyBuf, L.worker(2 * warp), L.worker(2 * warp + 1));
+                     L.a + warp * kDedicatedCopyBufs * kCopyBuf,
+                     smem_u32(L.bars + warp * kDedicatedCopyBufs), kDedicatedCopyBufs);
       if (COPY == kCopyLdst)
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 8 + warp, p.copy_ctas * 8);
     }
@@ -1296,13 +1360,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     if (OP == kOpAG && !p.plain && p.copy_ctas == 0) {  // co-located transfer warps
       if (COPY == kCopyTma && warp == 2 && lane == 0)
         run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x), static_cast<int32_t>(gridDim.x),
-                     L.copy, L.copyb(0), L.copyb(1));
+                     L.copy, L.copyb(0), 2);
       if (COPY == kCopyLdst)
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 2 + (warp - 2),
                       static_cast<int32_t>(gridDim.x) * 2);
     }
   } else {
-    run_epilogue<OP, F32, CL>(p, L, tmem_base, warp, lane);
+    run_epilogue<OP, F32, CL>(p, L, tmem_base, warp, lane, COPY != kCopyTma || p.copy_ctas > 0);
   }
 
   tc_fence_before();
