@@ -75,7 +75,12 @@ typedef enum {
   DT_XFER_AUTO = 0,        /* pick per chunk size                                          */
   DT_XFER_COPY_ENGINE = 1, /* host-issued cudaMemcpy2DAsync + stream flag write per chunk  */
   DT_XFER_TMA = 2,         /* in-kernel cp.async.bulk, global -> shared -> global          */
-  DT_XFER_LDST = 3         /* in-kernel 16-byte vector loads/stores                        */
+  DT_XFER_LDST = 3,        /* in-kernel 16-byte vector loads/stores                        */
+  DT_XFER_TMA_TILE = 4     /* AllGather-GEMM only: every compute CTA pulls exactly the A rows
+                              of its own tiles from the owning shard into its shared-memory
+                              operand ring with TMA, and its MMAs wait on that ring's
+                              mbarriers (no gather buffer, no global flags); needs every
+                              128-row m-tile inside one shard: (M/W) % 128 == 0             */
 } dt_xfer;
 
 typedef enum { DT_BF16 = 0, DT_F32 = 1 } dt_dtype;
@@ -160,7 +165,12 @@ dt_status dt_workspace_init(const dt_args* a, int op, void* workspace, size_t ws
  *              aligned, used by one call at a time.
  * Rows of shard s are gathered into the workspace chunk by chunk (own rank first, then
  * r+1, r+2, ...), each chunk's ready flag is released, and the persistent GEMM waits per
- * tile for the chunks of its rows (DITRON page section 3.2 "Gather模式").  With W == 1 there
+ * tile for the chunks of its rows (DITRON page section 3.2 "Gather模式").  With
+ * DT_XFER_TMA_TILE there is no gather buffer and no flag: each tile's A rows come straight
+ * from the shard that owns them into the consuming CTA's shared memory, synchronised by the
+ * pipeline's mbarriers (AutoOverlap page, section 5.3: the co-located lowering coordinates
+ * communication and computation on one SM through shared-memory barriers); the tile order
+ * still visits the own rank's rows first and then rank r+1, r+2, ...  With W == 1 there
  * is nothing to gather and the GEMM reads the one shard in place (a plain GEMM).  K == 0
  * writes zeros; M == 0 or N == 0 does nothing. */
 dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c,
@@ -362,7 +372,8 @@ size_t dt_sizeof_tune_point(void);
  * communication and the tile order, all by measuring the generated variants).
  * AllGather-GEMM candidates: chunk rows {64 .. 4096, M/W} x {copy engine (when the chunk count
  * stays <= 512), TMA and ld/st with co-located transfer warps, TMA and ld/st on 8 or 16
- * dedicated CTAs}; then group widths {4, 8, 16} at the best point.  Scatter-mode candidates
+ * dedicated CTAs, the per-tile pull DT_XFER_TMA_TILE when (M/W) % 128 == 0}; then group widths
+ * {4, 8, 16} at the best point.  Scatter-mode candidates
  * (dt_tune_reduce with op DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A): chunk rows x group
  * widths {4, 8, 16}, at the tile rows given, and for DT_OP_GEMM_RS / DT_OP_GEMM_AR x column
  * bands {as given, one band} when the given (or automatic) bands are more than one.  Each

@@ -49,7 +49,7 @@ def small():
     return wl, inp, _oracle(inp)
 
 
-@pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])
+@pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst", "tma_tile"])
 @pytest.mark.parametrize("swizzle", [True, False])
 @pytest.mark.parametrize("rank", [0, 1])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
@@ -65,7 +65,7 @@ def test_small_bit_identical_across_variants(dt, small):
     wl, inp, ref = small
     base = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=128, backend="tma", tile_m=128)
     for tile_m in [128, 256]:  # one CTA or a pair per tile: the same bits
-        for backend in ["copy_engine", "tma", "ldst"]:
+        for backend in ["copy_engine", "tma", "ldst", "tma_tile"]:
             for swizzle in [True, False]:
                 for cr in [1, 64, 100, 128, 256, 1000]:
                     c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, backend=backend,
@@ -81,6 +81,16 @@ def ragged():
     wl = WORKLOADS["ag_w6_m6000_n3000_k5120"]
     inp = wl.make()
     return wl, inp, _oracle(inp)
+
+
+def test_tile_pull_needs_tile_aligned_shards(dt, ragged):
+    """Shards of 1000 rows put m-tiles across two shards: the per-tile pull refuses them."""
+    wl, inp, ref = ragged
+    args = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=wl.chunk_rows,
+                        backend="tma_tile")
+    with pytest.raises(dt.DtError) as ei:
+        dt.workspace_size(args, dt.OP_AG)
+    assert "multiple of 128" in ei.value.message
 
 
 @pytest.mark.parametrize("backend", ["copy_engine", "tma", "ldst"])

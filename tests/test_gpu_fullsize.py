@@ -4,8 +4,8 @@ The FFN pair's GEMM-ReduceScatter (W=8, M=8192, N=8192, K=3584 per rank) and the
 AllGather-GEMM (W=8, M=16384, N=8192, K=8192):
 
 * every output entry is bit-identical across chunk rows, tile rows (one CTA or a CTA pair),
-  swizzle on / off and, for the AllGather, the three transfer backends (DITRON page, section 6:
-  the adapted kernels give bit-identical results);
+  swizzle on / off, for the ReduceScatter column bands and for the AllGather every transfer
+  backend (DITRON page, section 6: the adapted kernels give bit-identical results);
 * whole 128-row strips of every destination (ReduceScatter) or source block (AllGather), and
   one strip that crosses a block boundary, match the float64 oracle element by element within
   the bf16 tolerance.
@@ -100,7 +100,9 @@ AG_VARIANTS = ([dict(chunk_rows=c, backend=be, tile_m=256, swizzle=True)
                 for c in (128, 256, 1024) for be in ("copy_engine", "tma", "ldst")] +
                [dict(chunk_rows=c, backend="tma", tile_m=t, swizzle=s)
                 for c in (256, 1024) for t in (128, 256) for s in (True, False)
-                if (t, s) != (256, True)])
+                if (t, s) != (256, True)] +
+               [dict(chunk_rows=c, backend="tma_tile", tile_m=t, swizzle=True)
+                for c in (256, 2048) for t in (128, 256)])
 
 
 @pytest.fixture(scope="module")

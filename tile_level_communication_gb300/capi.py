@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdt.so")
 
 DT_OK, DT_ERR_INVALID, DT_ERR_UNSUPPORTED, DT_ERR_TIMEOUT, DT_ERR_CUDA, DT_ERR_WORKSPACE = range(6)
-BACKENDS = {"auto": 0, "copy_engine": 1, "tma": 2, "ldst": 3}
+BACKENDS = {"auto": 0, "copy_engine": 1, "tma": 2, "ldst": 3, "tma_tile": 4}
 DTYPES = {"bf16": 0, "f32": 1}
 ACTS = {"none": 0, "gelu_tanh": 1, "silu": 2}
 OP_AG, OP_RS, OP_AR, OP_A2A = 0, 1, 2, 3

@@ -155,7 +155,7 @@ constexpr int64_t kBandBytes = 32ll << 20;
 int32_t l2_hints_setting() {
   static int32_t v = [] {
     const char* e = getenv("DT_L2_HINTS");
-    return e ? static_cast<int32_t>(atoi(e)) & 3 : 0;
+    return e ? static_cast<int32_t>(atoi(e)) & 3 : 3;
   }();
   return v;
 }
@@ -252,7 +252,17 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
     return fail(DT_ERR_UNSUPPORTED, "too many chunks; raise chunk_rows");
   d->ld_gather = d->K;  // K % 8 == 0: 16-byte rows, back to back
   int be = a->backend;
-  if (be < DT_XFER_AUTO || be > DT_XFER_LDST) return fail(DT_ERR_INVALID, "unknown backend %d", be);
+  if (be < DT_XFER_AUTO || be > DT_XFER_TMA_TILE)
+    return fail(DT_ERR_INVALID, "unknown backend %d", be);
+  if (be == DT_XFER_TMA_TILE) {
+    if (op != DT_OP_AG_GEMM)
+      return fail(DT_ERR_INVALID, "DT_XFER_TMA_TILE applies to the AllGather-GEMM only");
+    if (d->Ms % kBM)
+      return fail(DT_ERR_UNSUPPORTED,
+                  "DT_XFER_TMA_TILE needs M/W (%lld) to be a multiple of %d (no tile across shards)",
+                  (long long)d->Ms, kBM);
+    if (a->copy_ctas != 0) return fail(DT_ERR_INVALID, "DT_XFER_TMA_TILE uses no transfer CTAs");
+  }
   if (op == DT_OP_AG_GEMM && be == DT_XFER_AUTO) {
     // large chunks amortise the copy engine's per-transfer launch cost; smaller ones move
     // on in-kernel TMA bulk copies
@@ -299,8 +309,10 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   off = align_up(off + 4 * static_cast<size_t>(d->T), 1024);
   d->ctl_bytes = off;
   d->off_data = off;
-  if (op == DT_OP_AG_GEMM)
+  if (op == DT_OP_AG_GEMM && be != DT_XFER_TMA_TILE)
     d->total = off + static_cast<size_t>(d->M) * d->ld_gather * 2;
+  else if (op == DT_OP_AG_GEMM)
+    d->total = off;  // the tiles read the shards in place: no gather buffer
   else if (a2a)
     d->total = off;
   else
@@ -668,9 +680,9 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
   Derived d;
   dt_status s = ag_common(a_shards, b, c, scratch, scratch_bytes, a, &d);
   if (s != DT_OK || d.M == 0 || d.N == 0) return s;
-  if (a->backend == DT_XFER_COPY_ENGINE)
+  if (a->backend == DT_XFER_COPY_ENGINE || a->backend == DT_XFER_TMA_TILE)
     return fail(DT_ERR_UNSUPPORTED,
-                "the copy-engine transfer needs a side stream; use DT_XFER_TMA or DT_XFER_LDST");
+                "the fixed scratch runs the in-kernel transfer: use DT_XFER_TMA or DT_XFER_LDST");
   const int copy = a->backend == DT_XFER_LDST ? kCopyLdst : kCopyTma;
   if (d.K == 0) return launch_zero(c, d.M, d.N * (d.f32 ? 4 : 2), d.ldc * (d.f32 ? 4 : 2), stream);
   int dev = 0, sms = 0;
@@ -865,6 +877,17 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
     if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
     return DT_OK;
   }
+  if (d.backend == DT_XFER_TMA_TILE) {
+    // every tile loads its A rows from the owning shard (tmA[s]); no transfer, no flags
+    for (int q = 0; q < d.W; ++q)
+      if ((s = make_tmap(&p.tmA[q], a_shards[q], d.K, d.Ms, d.lda * 2, 64, kBM)) != DT_OK) return s;
+    p.a_from_shards = 1;
+    p.wait_flags = 0;
+    p.own_in_place = 0;
+    cudaError_t e = launch_ag_kernel(p, kCopyNone, d.f32, grid, false, stream, d.cl);
+    if (e != cudaSuccess) return cuda_fail(e, "fused AllGather-GEMM launch");
+    return DT_OK;
+  }
   if (d.backend == DT_XFER_COPY_ENGINE) {
     PfnWriteValue32 wv = write_value32();
     if (!wv) return fail(DT_ERR_CUDA, "cuStreamWriteValue32 entry point unavailable");
@@ -927,6 +950,8 @@ dt_status dt_allgather(const void* const* a_shards, void* out, void* ws, size_t 
   x.act = DT_ACT_NONE;
   const int64_t ldo = a->ldc ? a->ldc : a->k;
   if (a->backend == DT_XFER_AUTO && ldo != a->k) x.backend = DT_XFER_COPY_ENGINE;  // strided rows
+  if (a->backend == DT_XFER_TMA_TILE)
+    return fail(DT_ERR_INVALID, "DT_XFER_TMA_TILE moves tiles into shared memory, not an AllGather");
   Derived d;
   dt_status s = derive(&x, DT_OP_AG_GEMM, &d);
   if (s != DT_OK) return s;
@@ -1509,6 +1534,7 @@ dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, v
         vs.push_back({DT_XFER_TMA, n});
         vs.push_back({DT_XFER_LDST, n});
       }
+    if (d.Ms % kBM == 0) vs.push_back({DT_XFER_TMA_TILE, 0});  // per-tile pull, co-located
     for (const V& v : vs) {
       dt_args cand = *a;
       cand.chunk_rows = cr;

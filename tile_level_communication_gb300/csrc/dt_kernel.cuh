@@ -125,12 +125,13 @@ struct KParams {
   int32_t src_rows_contig; // shard rows are back to back (lda == K)
   int32_t drop_chunk;      // failure-detection testing: chunk the host told the in-kernel
                            // transfer to leave out (its flag never flips); -1: none
-  int32_t l2_hints;        // L2 cache policies: bit 0, ReduceScatter running sums, park slots
-                           // and final sums stream through L2 (evict first); bit 1, B's k-blocks
-                           // stay (evict last)
+  int32_t l2_hints;        // ReduceScatter / AllReduce L2 cache policies: bit 0, running sums,
+                           // park slots and final sums stream through L2 (evict first); bit 1,
+                           // B_q's k-blocks stay (evict last)
   unsigned long long* trace;  // AG debug timeline (global timer, ns), or null; see trace_*
   int32_t c_tma;           // AG: C leaves through the staging buffers as TMA stores (tmOut[0],
                            // 32-column boxes clipped at M and N); 0: each thread stores its row
+  int32_t a_from_shards;   // AG: each tile's A rows are loaded from the owning shard (tmA[s])
 };
 
 // AG debug timeline, in 64-bit words: [0] first CTA start (min), [1] last CTA exit (max),
@@ -322,7 +323,7 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
   // stage s: barriers 8 s bytes after stage 0's, buffers s stages after stage 0's
   const uint32_t full0 = L.full(0), empty0 = L.empty(0);
   const uint32_t a_smem0 = smem_u32(L.a), b_smem0 = smem_u32(L.b);
-  const bool b_keep = (p.l2_hints & 2) != 0;
+  const bool b_keep = OP == kOpRS && (p.l2_hints & 2) != 0;
   const uint64_t pol_b = l2_policy_evict_last();
   uint32_t full0_lead = full0;  // stage 0's full barrier in the pair leader (cluster address)
   if constexpr (PAIR) full0_lead = mapa_shared(full0, rank & ~1u);
@@ -367,7 +368,14 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
     }
     const CUtensorMap* tA = &p.tmA[OP != kOpAG ? ti.q : (own_tile ? 1 : 0)];
     const CUtensorMap* tB = &p.tmB[OP != kOpAG ? ti.q : 0];
-    const int32_t a_row = static_cast<int32_t>(own_tile ? ti.row0 - own0 : ti.row0);
+    int32_t a_row = static_cast<int32_t>(own_tile ? ti.row0 - own0 : ti.row0);
+    if (OP == kOpAG && p.a_from_shards) {
+      // co-located pull: this CTA's 128 rows lie in one shard ((M/W) % 128 == 0); the loads
+      // complete on the stage's mbarrier like any operand load
+      const int32_t s = static_cast<int32_t>(ti.row0 / p.g.Ms);
+      tA = &p.tmA[s];
+      a_row = static_cast<int32_t>(ti.row0 - static_cast<int64_t>(s) * p.g.Ms);
+    }
     // this CTA's columns of B: all 256, or its half of the pair's
     const int32_t b_col = static_cast<int32_t>(ti.col0) + static_cast<int32_t>(rank & 1u) * (NB * 64);
     bool ok = true;
@@ -740,7 +748,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
   const bool fused_rs = RS && !p.plain;
   const bool fused_a2a = A2A && !p.plain;
   int32_t tl = 0;
-  const bool stream_sums = (p.l2_hints & 1) != 0;  // running sums pass through L2 once
+  const bool stream_sums = RS && (p.l2_hints & 1) != 0;  // running sums pass through L2 once
   const uint64_t pol_s = l2_policy_evict_first();
   uint32_t stage_ctr = 0;           // running-sum staging buffer in use (alternates)
   uint32_t ld_par[2] = {0u, 0u};    // phase of each staging buffer's load barrier
@@ -1157,7 +1165,8 @@ __device__ __forceinline__ void for_each_piece(const KParams& p, int32_t wid, in
 // completion barriers bar0, bar0 + 8, ... (one per buffer).  Piece i goes through buffer
 // i % nbuf; the worker keeps nbuf - 1 loads in flight and stores the oldest piece once its load
 // has landed, so loads and stores overlap; a piece is counted towards its chunk once its
-// store's writes are complete, which the worker checks one store later.
+// store's writes are complete, which the worker checks kStoresInFlight stores later (it
+// waits for a store's writes only when that many newer ones are outstanding).
 struct CopyJob {
   uint8_t* dst;
   Piece pc;
@@ -1165,13 +1174,15 @@ struct CopyJob {
 };
 constexpr uint32_t kMaxCopyBufs = 4;
 constexpr uint32_t kDedicatedCopyBufs = 3;  // per worker on a dedicated transfer CTA (48 KiB)
+constexpr int kStoresInFlight = 2;          // stores whose writes a worker does not wait for
 
 static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32_t wid, int32_t nw,
                                     uint8_t* stage, uint32_t bar0, uint32_t nbuf) {
   uint32_t issued = 0;  // loads issued
   uint32_t stored = 0;  // loads waited for and their pieces' stores issued
+  uint32_t counted = 0; // stored pieces counted towards their chunks
   CopyJob jobs[kMaxCopyBufs] = {};  // the piece in each buffer
-  int32_t st_c = -1, st_total = 0;  // the piece stored last, not yet counted
+  int32_t pend_c[kStoresInFlight + 1], pend_total[kStoresInFlight + 1];  // stored, not counted
   auto bar_of = [&](uint32_t i) { return bar0 + 8u * (i % nbuf); };
   auto buf_of = [&](uint32_t i) { return smem_u32(stage + (i % nbuf) * kCopyBuf); };
   auto par_of = [&](uint32_t i) { return (i / nbuf) & 1u; };  // use i / nbuf of its barrier
@@ -1189,11 +1200,15 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32
                  job.pc.nbytes);
     }
     bulk_commit();
+    pend_c[stored % (kStoresInFlight + 1)] = job.c;
+    pend_total[stored % (kStoresInFlight + 1)] = job.total;
     ++stored;
-    bulk_wait<1>();  // the previous piece's writes are complete
-    if (st_c >= 0) signal_piece(p, st_c, st_total);
-    st_c = job.c;
-    st_total = job.total;
+    if (stored - counted > static_cast<uint32_t>(kStoresInFlight)) {
+      bulk_wait<kStoresInFlight>();  // the oldest uncounted piece's writes are complete
+      signal_piece(p, pend_c[counted % (kStoresInFlight + 1)],
+                   pend_total[counted % (kStoresInFlight + 1)]);
+      ++counted;
+    }
     return true;
   };
   auto stop = [&]() { return *L.abort_flag != 0; };
@@ -1225,7 +1240,9 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32
   while (!*L.abort_flag && stored < issued && store_oldest()) {
   }
   bulk_wait<0>();
-  if (!*L.abort_flag && st_c >= 0) signal_piece(p, st_c, st_total);
+  for (; !*L.abort_flag && counted < stored; ++counted)
+    signal_piece(p, pend_c[counted % (kStoresInFlight + 1)],
+                 pend_total[counted % (kStoresInFlight + 1)]);
   // after an abort, the loads still in flight (at most nbuf) land before the CTA can exit
   for (uint32_t i = stored; i < issued; ++i) {
     const uint64_t t0 = globaltimer_ns();
@@ -1235,6 +1252,7 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32
 }
 
 // One vector ld/st copy worker (one warp).
+constexpr int kLdstVecs = 16;
 static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int lane, int32_t wid,
                                      int32_t nw) {
   // the whole warp takes the same decision
@@ -1251,16 +1269,16 @@ static __device__ void run_copy_ldst(const KParams& p, const SmemLayout& L, int 
       uint4* dst = reinterpret_cast<uint4*>(
           p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard + r) * p.ld_gather * 2 +
           pc.boff);
-      // 8 vectors per lane in flight (4 KiB per warp): a copy at HBM rate needs ~32 KiB in
-      // flight per SM
+      // kLdstVecs vectors per lane in flight (8 KiB per warp): a copy at HBM rate needs tens
+      // of KiB in flight per SM
       const int32_t nvec = static_cast<int32_t>(nb >> 4);
-      for (int32_t v = lane; v < nvec; v += 32 * 8) {
-        uint4 x[8];
+      for (int32_t v = lane; v < nvec; v += 32 * kLdstVecs) {
+        uint4 x[kLdstVecs];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < kLdstVecs; ++u)
           if (v + u * 32 < nvec) x[u] = __ldg(src + v + u * 32);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < kLdstVecs; ++u)
           if (v + u * 32 < nvec) dst[v + u * 32] = x[u];
       }
     }
