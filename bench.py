@@ -98,7 +98,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
     ap.add_argument("--workload", default="ffn_pair")
-    ap.add_argument("--backend", default="auto", choices=["auto", "copy_engine", "tma", "ldst"])
+    ap.add_argument("--backend", default="auto", choices=["auto", "copy_engine", "tma", "ldst", "tma_tile"])
     ap.add_argument("--chunk-rows", type=int, default=0, help="0 = the workload's")
     ap.add_argument("--no-swizzle", action="store_true")
     ap.add_argument("--group", type=int, default=0, help="m-tiles per band of the in-chunk "
@@ -917,6 +917,52 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
             got = cl["outs"][0][:128].float()
         errs.append(float((got - ref).abs().max() / ref.abs().max()))
     out["spot_check_vs_cublas_max_rel_err"] = max(errs)
+
+    # How much of the AllGather's transfer the GEMM hid: one call with the debug timeline
+    # attached (the kernel's own global-timer records of each chunk's release and first read,
+    # and of the time its producers spent waiting for flags), at the tuned knobs and with the
+    # in-kernel TMA transfer at the same chunk rows (whose releases are timed on the device)
+    ag_calls = [cl for cl in calls if cl["op"] == "ag"]
+    if ag_calls:
+        cl = ag_calls[0]
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        res = {}
+        variants = {"as_tuned": cl["args"]}
+        if cl["args"].backend != dt.BACKENDS["tma"]:
+            t = dt.DtArgs.from_buffer_copy(cl["args"])
+            t.backend, t.copy_ctas = dt.BACKENDS["tma"], 0
+            if dt.workspace_size(t, dt.OP_AG) <= cl["ws"].numel():
+                variants["tma"] = t
+        for name, a in variants.items():
+            buf = torch.zeros(dt.trace_bytes(a) // 8, dtype=torch.int64, device=dev)
+            dt.ag_gemm(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], a)  # warm
+            dt.trace_attach(buf)
+            try:
+                dt.ag_gemm(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], a)
+                code, info = dt.check(cl["ws"])
+            finally:
+                dt.trace_attach(None)
+            if code != 0:
+                raise RuntimeError(f"traced AllGather device error {info}")
+            tr = dt.trace_decode(buf.cpu().tolist(), a)
+            rel = [c["released_us"] for c in tr["chunks"].values() if c["released_us"] is not None]
+            seen = [c["first_read_us"] for c in tr["chunks"].values()
+                    if c["first_read_us"] is not None]
+            span = max(rel) if rel else (max(seen) if seen else 0.0)
+            exposed = tr["stall_us_total"] / sms  # per SM: the producers' flag waits
+            res[name] = {
+                "backend": [k for k, v in dt.BACKENDS.items() if v == a.backend][0],
+                "chunk_rows": int(a.chunk_rows), "kernel_us": tr["kernel_us"],
+                "transfer_span_us": span,
+                "transfer_span_source": "last in-kernel release" if rel else
+                                        "last first-read of a chunk (copy-engine flags are "
+                                        "written by the copy's stream, not timed)",
+                "stall_us_total": tr["stall_us_total"], "stalled_waits": tr["stalled_waits"],
+                "exposed_us_per_sm": exposed,
+                "hidden_frac": (1.0 - exposed / span) if span > 0 else None}
+        out["ag_overlap"] = dict(res, note="one traced call each; hidden_frac = 1 - (flag-wait "
+                                 "time per SM) / (time from the kernel's start until the last "
+                                 "chunk was released or first read)")
 
     # End to end through the public API with host buffers: every step copies its inputs in
     # from pinned host memory and its outputs out, inside the timed region.  Two device sets
