@@ -40,29 +40,17 @@ METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 tensor peak (1 GPU
 # They hold only for the kernel sources they were taken on (csrc hash) and the knobs
 # "chunk_rows/group/tile_rows"; otherwise the roofline's traffic is null.
 NCU_TRAFFIC = {
-    "rs_w8_m8192_n8192_k3584": {"csrc": "ea0d680da8286dbb",
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch after two
+    # warm-up launches, 256-row tiles; keys "chunk_rows/tile_rows/col_band/l2_hints" (the
+    # group width gives the same order at these chunk sizes: a key holds at most 4 m-tiles)
+    "rs_w8_m8192_n8192_k3584": {"csrc": "42333423845d344c",
                                 "profile": "profiles/fused_gemm_rs_w8_m8192_n8192_k3584.md",
                                 "points": {
-        "1024/8/256": 6.454941e9 + 2.010043e9,     # --set full capture
-        # with 1024-row chunks a destination block is 4 pair m-tiles, so groups 4, 8 and 16
-        # give the same tile order as group 8
-        "1024/4/256": 6.454941e9 + 2.010043e9, "1024/16/256": 6.454941e9 + 2.010043e9,
-        # chunks of 512 / 256 rows: two / one pair m-tiles per chunk, the same order at every
-        # group width (dram metrics only)
-        "512/4/256": 5997152768 + 2004979456, "512/8/256": 5997152768 + 2004979456,
-        "512/16/256": 5997152768 + 2004979456,
-        "256/4/256": 6102649088 + 2006288896, "256/8/256": 6102649088 + 2006288896,
-        "256/16/256": 6102649088 + 2006288896,
-        # chunks of 128 / 64 rows: every pair m-tile has a key of its own (dram metrics only)
-        "128/4/256": 5969986560 + 2005768704, "128/8/256": 5969986560 + 2005768704,
-        "128/16/256": 5969986560 + 2005768704,
-        "64/4/256": 5301320192 + 2003131648, "64/8/256": 5301320192 + 2003131648,
-        "64/16/256": 5301320192 + 2003131648,
-    }},
-    "ag_w8_m8192_n3584_k8192": {"csrc": "ea0d680da8286dbb",
-                                "profile": "profiles/fused_gemm_ag_w8_m8192_n3584_k8192.md",
-                                "points": {
-        "256/8/256": 692.992512e6 + 168.30976e6,   # --set full capture, TMA transfer
+        "1024/256/16/3": 4356852224 + 1993351168, "1024/256/32/3": 5408357376 + 1997502720,
+        "512/256/16/3": 4184011776 + 1992557312, "512/256/32/3": 5883800320 + 1998592256,
+        "256/256/16/3": 4127314176 + 1992650240, "256/256/32/3": 5857759744 + 1998155008,
+        "128/256/16/3": 4150013440 + 1991749888, "128/256/32/3": 5742371072 + 1997810688,
+        "64/256/16/3": 3932042240 + 2000992000, "64/256/32/3": 5304341248 + 2003246592,
     }},
 }
 
@@ -105,6 +93,9 @@ def parse():
                     "raster (0 = the library's 8; fixed, not tuned, when given)")
     ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256],
                     help="tile rows: 128 (one CTA), 256 (a CTA pair), 0 = the library's choice")
+    ap.add_argument("--col-band", type=int, default=0,
+                    help="ReduceScatter / AllReduce column tiles per column band (0 = the "
+                         "library's automatic choice)")
     ap.add_argument("--rank-view", type=int, default=0, help="AllGather rank whose view is computed")
     ap.add_argument("--skip-extras", action="store_true",
                     help="skip the baselines, e2e, CPU oracle and clock sampling")
@@ -531,7 +522,7 @@ def main():
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
 
     # device-resident inputs, outputs, workspaces, argument structs
-    knobs = {"tile_m": args.tile_m}
+    knobs = {"tile_m": args.tile_m, "col_band": args.col_band}
     if args.group:
         knobs["group"] = args.group
     def build_calls():
@@ -651,7 +642,8 @@ def main():
             tuned[cl["op"]] = {"chunk_rows": int(a.chunk_rows),
                                "backend": [k for k, v in dt.BACKENDS.items() if v == a.backend][0],
                                "copy_ctas": int(a.copy_ctas), "group": int(a.group),
-                               "tile_m": int(a.tile_m), "candidates": len(pts)}
+                               "tile_m": int(a.tile_m), "col_band": int(a.col_band),
+                               "candidates": len(pts)}
 
     # warm-up (also writes each workspace's tile order once)
     for _ in range(max(3, args.warmup)):
@@ -735,7 +727,9 @@ def main():
     tr = NCU_TRAFFIC.get(calls[dom]["wl"].name)
     used = calls[dom]["args"]  # the knobs actually timed (after tuning)
     op_id = {"ag": dt.OP_AG, "rs": dt.OP_RS, "ar": dt.OP_AR, "a2a": dt.OP_A2A}[calls[dom]["op"]]
-    knob_key = f"{used.chunk_rows}/{used.group}/{dt.tile_rows(used, op_id)}"
+    hints = int(os.environ.get("DT_L2_HINTS", "3")) & 3  # the library's L2 policies
+    knob_key = (f"{used.chunk_rows}/{dt.tile_rows(used, op_id)}/{dt.col_band(used, op_id)}/"
+                f"{hints}")
     traffic = tr["points"].get(knob_key) if tr and tr["csrc"] == csrc_hash() else None
     line["roofline"] = {
         "bound": "tensor", "kernel": f"fused_gemm_kernel ({calls[dom]['op']})",
@@ -934,6 +928,12 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
             if dt.workspace_size(t, dt.OP_AG) <= cl["ws"].numel():
                 variants["tma"] = t
         for name, a in variants.items():
+            if a.backend == dt.BACKENDS["tma_tile"]:
+                res[name] = {"backend": "tma_tile", "chunk_rows": int(a.chunk_rows),
+                             "note": "no separate transfer: each tile pulls its own rows into "
+                                     "shared memory behind the operand ring's mbarriers, so "
+                                     "no flag is waited for"}
+                continue
             buf = torch.zeros(dt.trace_bytes(a) // 8, dtype=torch.int64, device=dev)
             dt.ag_gemm(cl["shards"], cl["b"], cl["outs"][0], cl["ws"], a)  # warm
             dt.trace_attach(buf)

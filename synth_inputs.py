@@ -223,6 +223,10 @@ WORKLOADS = {
     # 256 / 512 / 1024 sweep)
     "rs_w8_m8192_n8192_k3584": Workload("rs_w8_m8192_n8192_k3584", "rs", 8, 8192, 8192, 3584, 2,
                                         "normal(1.0)", "normal(0.02)", 1024),
+    # the same ReduceScatter with half the tokens (M=4096): a profiling case whose inputs,
+    # running sums and outputs (1.9 GB) still exceed L2
+    "rs_w8_m4096_n8192_k3584": Workload("rs_w8_m4096_n8192_k3584", "rs", 8, 4096, 8192, 3584, 2,
+                                        "normal(1.0)", "normal(0.02)", 512),
     # non-perfect tiling, W=6, U[-1,1], seed 3, chunk 192: every edge ragged
     "ag_w6_m6000_n3000_k5120": Workload("ag_w6_m6000_n3000_k5120", "ag", 6, 6000, 3000, 5120, 3,
                                         "uniform", "uniform", 192),

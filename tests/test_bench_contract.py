@@ -46,8 +46,9 @@ def test_reference_arm_names_the_default_workload():
 def test_traffic_table_covers_every_reduce_tuner_candidate():
     """The roofline's DRAM traffic of the benchmark's dominant launch (the FFN pair's
     ReduceScatter) is looked up by the tuned knobs: every candidate the reduce tuner can pick
-    (chunk rows 64 .. M/W, group widths 4 / 8 / 16, at the library's 256-row tiles) has an
-    entry, and each workload names the profile its figures come from."""
+    (chunk rows 64 .. M/W, the automatic column bands or one band, at the library's 256-row
+    tiles and L2 policies) has an entry, and each workload names the profile its figures come
+    from."""
     import sys
     sys.path.insert(0, ROOT)
     import bench
@@ -57,8 +58,8 @@ def test_traffic_table_covers_every_reduce_tuner_candidate():
     chunks = [c for c in (64, 128, 256, 512, 1024, 2048, 4096) if c < ms] + [ms]
     points = bench.NCU_TRAFFIC[wl.name]["points"]
     for cr in chunks:
-        for g in (4, 8, 16):
-            key = f"{cr}/{g}/256"
+        for nb in (16, 32):
+            key = f"{cr}/256/{nb}/3"
             assert key in points, key
             assert points[key] > 0
     for entry in bench.NCU_TRAFFIC.values():
