@@ -46,11 +46,11 @@ NCU_TRAFFIC = {
     "rs_w8_m8192_n8192_k3584": {"csrc": "42333423845d344c",
                                 "profile": "profiles/fused_gemm_rs_w8_m8192_n8192_k3584.md",
                                 "points": {
-        "1024/256/16/3": 4356852224 + 1993351168, "1024/256/32/3": 5408357376 + 1997502720,
-        "512/256/16/3": 4184011776 + 1992557312, "512/256/32/3": 5883800320 + 1998592256,
-        "256/256/16/3": 4127314176 + 1992650240, "256/256/32/3": 5857759744 + 1998155008,
-        "128/256/16/3": 4150013440 + 1991749888, "128/256/32/3": 5742371072 + 1997810688,
-        "64/256/16/3": 3932042240 + 2000992000, "64/256/32/3": 5304341248 + 2003246592,
+        "1024/256/16/3": 4206936832 + 1993850112, "1024/256/32/3": 5492091648 + 1995920640,
+        "512/256/16/3": 4097069824 + 1992612096, "512/256/32/3": 6038561792 + 1998166272,
+        "256/256/16/3": 4189729280 + 1992555008, "256/256/32/3": 5862915328 + 1998213632,
+        "128/256/16/3": 4137170944 + 1992702208, "128/256/32/3": 5787766784 + 1998498816,
+        "64/256/16/3": 3870661888 + 2000494592, "64/256/32/3": 5136942592 + 2002726144,
     }},
 }
 

@@ -135,6 +135,16 @@ uint64_t default_timeout_ns() {
   return v;
 }
 
+// TMA buffers per worker on a dedicated transfer CTA (2, 3 or 4); DT_COPY_BUFS overrides.
+int32_t ded_bufs_setting() {
+  static int32_t v = [] {
+    const char* e = getenv("DT_COPY_BUFS");
+    const int x = e ? atoi(e) : 3;
+    return static_cast<int32_t>(x < 2 ? 2 : (x > 4 ? 4 : x));
+  }();
+  return v;
+}
+
 // The fused AllGather-GEMM stores C through TMA (1) or per thread (0); DT_C_TMA overrides.
 int32_t c_tma_setting() {
   static int32_t v = [] {
@@ -593,6 +603,7 @@ void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
   p.drop_chunk = -1;
   p.l2_hints = l2_hints_setting();
   p.trace = nullptr;
+  p.ded_bufs = ded_bufs_setting();
 }
 
 // Point the kernel at the attached timeline (if any) and reset it on `stream`: the min words to

@@ -132,6 +132,8 @@ struct KParams {
   int32_t c_tma;           // AG: C leaves through the staging buffers as TMA stores (tmOut[0],
                            // 32-column boxes clipped at M and N); 0: each thread stores its row
   int32_t a_from_shards;   // AG: each tile's A rows are loaded from the owning shard (tmA[s])
+  int32_t ded_bufs;        // TMA buffers per worker on a dedicated transfer CTA: 2, 3 or 4
+                           // (6, 4 or 3 workers)
 };
 
 // AG debug timeline, in 64-bit words: [0] first CTA start (min), [1] last CTA exit (max),
@@ -1173,7 +1175,7 @@ struct CopyJob {
   int32_t c, total;
 };
 constexpr uint32_t kMaxCopyBufs = 4;
-constexpr uint32_t kDedicatedCopyBufs = 3;  // per worker on a dedicated transfer CTA (48 KiB)
+constexpr uint32_t kDedicatedBufsTotal = 12;  // 16 KiB buffers of a dedicated transfer CTA
 constexpr int kStoresInFlight = 2;          // stores whose writes a worker does not wait for
 
 static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32_t wid, int32_t nw,
@@ -1300,7 +1302,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   constexpr bool PAIR = CL > 1;
   constexpr int NS = stages(PAIR, has_staging(OP, COPY));
   static_assert(COPY != kCopyTma ||
-                    4 * kDedicatedCopyBufs * kCopyBuf <= NS * (kAStage + b_stage_bytes(PAIR)),
+                    kDedicatedBufsTotal * kCopyBuf <= NS * (kAStage + b_stage_bytes(PAIR)),
                 "the dedicated TMA workers' buffers fit in the operand ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1361,12 +1363,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 
   if (copier) {
     // dedicated transfer CTA: no GEMM; the operand ring becomes four workers' staging rings
-    // of kDedicatedCopyBufs 16 KiB buffers
+    // of ded_bufs 16 KiB buffers each (12 buffers in all: 6 workers x 2, 4 x 3 or 3 x 4)
     if (OP == kOpAG && !p.plain) {
-      if (COPY == kCopyTma && warp < 4 && lane == 0)
-        run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x) * 4 + warp, p.copy_ctas * 4,
-                     L.a + warp * kDedicatedCopyBufs * kCopyBuf,
-                     smem_u32(L.bars + warp * kDedicatedCopyBufs), kDedicatedCopyBufs);
+      const uint32_t nbuf = static_cast<uint32_t>(p.ded_bufs);
+      const int nwk = static_cast<int>(kDedicatedBufsTotal / nbuf);
+      if (COPY == kCopyTma && warp < nwk && lane == 0)
+        run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x) * nwk + warp, p.copy_ctas * nwk,
+                     L.a + warp * nbuf * kCopyBuf, smem_u32(L.bars + warp * nbuf), nbuf);
       if (COPY == kCopyLdst)
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 8 + warp, p.copy_ctas * 8);
     }
