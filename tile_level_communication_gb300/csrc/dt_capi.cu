@@ -145,6 +145,16 @@ int32_t ded_bufs_setting() {
   return v;
 }
 
+// Bytes of a transfer piece on dedicated transfer CTAs (8 or 16 KiB); DT_COPY_PIECE overrides.
+int32_t ded_piece_setting() {
+  static int32_t v = [] {
+    const char* e = getenv("DT_COPY_PIECE");
+    const int x = e ? atoi(e) : 16384;
+    return static_cast<int32_t>(x <= 8192 ? 8192 : kCopyBuf);
+  }();
+  return v;
+}
+
 // The fused AllGather-GEMM stores C through TMA (1) or per thread (0); DT_C_TMA overrides.
 int32_t c_tma_setting() {
   static int32_t v = [] {
@@ -604,6 +614,7 @@ void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
   p.l2_hints = l2_hints_setting();
   p.trace = nullptr;
   p.ded_bufs = ded_bufs_setting();
+  p.piece_bytes = kCopyBuf;
 }
 
 // Point the kernel at the attached timeline (if any) and reset it on `stream`: the min words to
@@ -624,14 +635,15 @@ dt_status attach_trace(KParams& p, const Derived& d, cudaStream_t stream) {
 // ------------------------------------------------------------------------------ AllGather
 // How the in-kernel transfer cuts a chunk into pieces of at most one 16 KiB staging buffer:
 // whole rows when a row fits (rows_per_piece of them), else 16 KiB segments of one row.
-void set_pieces(KParams& p, const Derived& d) {
+void set_pieces(KParams& p, const Derived& d, bool dedicated) {
   p.row_bytes = d.K * 2;
-  if (p.row_bytes <= kCopyBuf) {
-    p.rows_per_piece = static_cast<int32_t>(kCopyBuf / p.row_bytes);
+  p.piece_bytes = dedicated ? ded_piece_setting() : kCopyBuf;
+  if (p.row_bytes <= p.piece_bytes) {
+    p.rows_per_piece = static_cast<int32_t>(p.piece_bytes / p.row_bytes);
     p.segs_per_row = 1;
   } else {
     p.rows_per_piece = 0;
-    p.segs_per_row = static_cast<int32_t>(cdiv64(p.row_bytes, kCopyBuf));
+    p.segs_per_row = static_cast<int32_t>(cdiv64(p.row_bytes, p.piece_bytes));
   }
   auto pieces = [&](int64_t rows) -> int32_t {
     return p.rows_per_piece > 0 ? static_cast<int32_t>(cdiv64(rows, p.rows_per_piece))
@@ -715,7 +727,7 @@ dt_status ag_gemm_on_scratch(const void* const* a_shards, const void* b, void* c
   p.lda_src = d.lda;
   p.ld_gather = d.ld_gather;
   p.wait_flags = 1;
-  set_pieces(p, d);
+  set_pieces(p, d, false);
   set_drop_chunk(p, d, take_drop_transfer());
   if ((s = make_tmap(&p.tmA[0], p.gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
   if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
@@ -867,7 +879,7 @@ dt_status dt_ag_gemm(const void* const* a_shards, const void* b, void* c, void* 
   p.lda_src = d.lda;
   p.ld_gather = d.ld_gather;
   p.wait_flags = 1;
-  set_pieces(p, d);
+  set_pieces(p, d, d.copy_ctas > 0);
   if ((s = make_tmap(&p.tmA[0], gather, d.K, d.M, d.ld_gather * 2, 64, kBM)) != DT_OK) return s;
   if ((s = make_tmap(&p.tmB[0], b, d.N, d.K, d.ldb * 2, 64, kBK)) != DT_OK) return s;
   p.own_in_place = own_in_place(d) ? 1 : 0;
@@ -1007,7 +1019,7 @@ dt_status dt_allgather(const void* const* a_shards, void* out, void* ws, size_t 
   p.lda_src = d.lda;
   p.ld_gather = ldo;
   p.own_in_place = 0;  // the own shard is copied too
-  set_pieces(p, d);
+  set_pieces(p, d, true);  // every CTA is a transfer CTA
   // descriptors the kernel prefetches at start (unused without tiles)
   if ((s = make_tmap(&p.tmA[0], out, d.K, d.M, ldo * 2, 64, kBM)) != DT_OK) return s;
   p.tmB[0] = p.tmA[0];

@@ -133,7 +133,8 @@ struct KParams {
                            // 32-column boxes clipped at M and N); 0: each thread stores its row
   int32_t a_from_shards;   // AG: each tile's A rows are loaded from the owning shard (tmA[s])
   int32_t ded_bufs;        // TMA buffers per worker on a dedicated transfer CTA: 2, 3 or 4
-                           // (6, 4 or 3 workers)
+  int32_t piece_bytes;     // bytes of one transfer piece and of one TMA worker buffer (a
+                           // multiple of 16, at most kCopyBuf)
 };
 
 // AG debug timeline, in 64-bit words: [0] first CTA start (min), [1] last CTA exit (max),
@@ -1130,8 +1131,8 @@ __device__ __forceinline__ Piece piece_of(const KParams& p, int32_t pc, int32_t 
     pc_.r0 = pc / p.segs_per_row;
     pc_.nr = 1;
     const int32_t seg = pc - pc_.r0 * p.segs_per_row;
-    pc_.boff = static_cast<int64_t>(seg) * kCopyBuf;
-    pc_.nbytes = static_cast<uint32_t>(min64(kCopyBuf, p.row_bytes - pc_.boff));
+    pc_.boff = static_cast<int64_t>(seg) * p.piece_bytes;
+    pc_.nbytes = static_cast<uint32_t>(min64(p.piece_bytes, p.row_bytes - pc_.boff));
   }
   return pc_;
 }
@@ -1163,7 +1164,7 @@ __device__ __forceinline__ void for_each_piece(const KParams& p, int32_t wid, in
   }
 }
 
-// One TMA bulk-copy worker (one thread): `nbuf` staging buffers of kCopyBuf bytes at `stage`,
+// One TMA bulk-copy worker (one thread): `nbuf` staging buffers of p.piece_bytes at `stage`,
 // completion barriers bar0, bar0 + 8, ... (one per buffer).  Piece i goes through buffer
 // i % nbuf; the worker keeps nbuf - 1 loads in flight and stores the oldest piece once its load
 // has landed, so loads and stores overlap; a piece is counted towards its chunk once its
@@ -1175,7 +1176,7 @@ struct CopyJob {
   int32_t c, total;
 };
 constexpr uint32_t kMaxCopyBufs = 4;
-constexpr uint32_t kDedicatedBufsTotal = 12;  // 16 KiB buffers of a dedicated transfer CTA
+constexpr uint32_t kDedicatedRingBytes = 12 * kCopyBuf;  // staging of a dedicated transfer CTA
 constexpr int kStoresInFlight = 2;          // stores whose writes a worker does not wait for
 
 static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32_t wid, int32_t nw,
@@ -1186,7 +1187,9 @@ static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32
   CopyJob jobs[kMaxCopyBufs] = {};  // the piece in each buffer
   int32_t pend_c[kStoresInFlight + 1], pend_total[kStoresInFlight + 1];  // stored, not counted
   auto bar_of = [&](uint32_t i) { return bar0 + 8u * (i % nbuf); };
-  auto buf_of = [&](uint32_t i) { return smem_u32(stage + (i % nbuf) * kCopyBuf); };
+  auto buf_of = [&](uint32_t i) {
+    return smem_u32(stage + (i % nbuf) * static_cast<uint32_t>(p.piece_bytes));
+  };
   auto par_of = [&](uint32_t i) { return (i / nbuf) & 1u; };  // use i / nbuf of its barrier
   auto store_oldest = [&]() -> bool {
     const uint32_t i = stored;
@@ -1302,7 +1305,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   constexpr bool PAIR = CL > 1;
   constexpr int NS = stages(PAIR, has_staging(OP, COPY));
   static_assert(COPY != kCopyTma ||
-                    kDedicatedBufsTotal * kCopyBuf <= NS * (kAStage + b_stage_bytes(PAIR)),
+                    kDedicatedRingBytes <= NS * (kAStage + b_stage_bytes(PAIR)),
                 "the dedicated TMA workers' buffers fit in the operand ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1363,13 +1366,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 
   if (copier) {
     // dedicated transfer CTA: no GEMM; the operand ring becomes four workers' staging rings
-    // of ded_bufs 16 KiB buffers each (12 buffers in all: 6 workers x 2, 4 x 3 or 3 x 4)
+    // of ded_bufs piece-sized buffers each: as many workers (one per warp, at most 8) as the
+    // 192 KiB of the ring hold
     if (OP == kOpAG && !p.plain) {
       const uint32_t nbuf = static_cast<uint32_t>(p.ded_bufs);
-      const int nwk = static_cast<int>(kDedicatedBufsTotal / nbuf);
+      const int nwk = min32(8, static_cast<int32_t>(kDedicatedRingBytes /
+                                                    (static_cast<uint32_t>(p.piece_bytes) * nbuf)));
       if (COPY == kCopyTma && warp < nwk && lane == 0)
         run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x) * nwk + warp, p.copy_ctas * nwk,
-                     L.a + warp * nbuf * kCopyBuf, smem_u32(L.bars + warp * nbuf), nbuf);
+                     L.a + warp * nbuf * p.piece_bytes, smem_u32(L.bars + warp * nbuf), nbuf);
       if (COPY == kCopyLdst)
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 8 + warp, p.copy_ctas * 8);
     }
