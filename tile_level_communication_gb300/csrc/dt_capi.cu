@@ -135,13 +135,12 @@ uint64_t default_timeout_ns() {
   return v;
 }
 
-// TMA buffers per worker on a dedicated transfer CTA (2, 3 or 4); DT_COPY_BUFS overrides.
-// Measured on 256 MiB AllGathers (16 KiB pieces): 6 workers x 2 buffers 5.37-5.54 TB/s, 4 x 3
-// 5.11-5.26, 3 x 4 4.78-4.87: more workers beat deeper rings.
+// TMA buffers per copy ring on a dedicated transfer CTA (2, 3 or 4; four rings at most, each
+// with a loader and a storer thread); DT_COPY_BUFS overrides.
 int32_t ded_bufs_setting() {
   static int32_t v = [] {
     const char* e = getenv("DT_COPY_BUFS");
-    const int x = e ? atoi(e) : 2;
+    const int x = e ? atoi(e) : 3;
     return static_cast<int32_t>(x < 2 ? 2 : (x > 4 ? 4 : x));
   }();
   return v;
