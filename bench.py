@@ -637,13 +637,17 @@ def main():
             else:
                 op_id = {"rs": dt.OP_RS, "ar": dt.OP_AR, "a2a": dt.OP_A2A}[cl["op"]]
                 pts = dt.tune_reduce(op_id, cl["A"], cl["B"], cl["outs"], cl["ws"], cl["args"],
-                                     reps=8)
+                                     reps=16)
             a = cl["args"]
             tuned[cl["op"]] = {"chunk_rows": int(a.chunk_rows),
                                "backend": [k for k, v in dt.BACKENDS.items() if v == a.backend][0],
                                "copy_ctas": int(a.copy_ctas), "group": int(a.group),
                                "tile_m": int(a.tile_m), "col_band": int(a.col_band),
-                               "candidates": len(pts)}
+                               "candidates": len(pts),
+                               "fastest": sorted(({k: p[k] for k in ("chunk_rows", "backend",
+                                                                     "group", "col_band", "ms")}
+                                                  for p in pts if p["status"] == 0 and p["ms"] > 0),
+                                                 key=lambda x: x["ms"])[:4]}
 
     # warm-up (also writes each workspace's tile order once)
     for _ in range(max(3, args.warmup)):

@@ -314,3 +314,12 @@ def test_allgather_pointer_and_workspace_errors(dt):
     # nothing to move: no pointer is touched
     dt.allgather([0, 0], 0, 0, dt.make_args(2, 0, 8, 512), stream=0, ws_bytes=0)
     dt.allgather([0, 0], 0, 0, dt.make_args(2, 512, 8, 0), stream=0, ws_bytes=0)
+
+
+def test_group_widths_that_reorder_nothing(dt):
+    """The tuners time a group width only when it changes the tile order: with 256-row tiles
+    and one chunk per rank, each key holds two m-tiles, so groups 4, 8 and 16 are one order."""
+    w, m, n = 4, 2048, 4096
+    orders = {g: tuple(dt.swizzle_plan(dt.make_args(w, m, n, 2048, chunk_rows=512, group=g),
+                                       dt.OP_RS).tolist()) for g in (1, 4, 8, 16)}
+    assert orders[4] == orders[8] == orders[16] != orders[1]

@@ -132,7 +132,7 @@ struct KParams {
   int32_t c_tma;           // AG: C leaves through the staging buffers as TMA stores (tmOut[0],
                            // 32-column boxes clipped at M and N); 0: each thread stores its row
   int32_t a_from_shards;   // AG: each tile's A rows are loaded from the owning shard (tmA[s])
-  int32_t ded_bufs;        // TMA buffers per copy ring on a dedicated transfer CTA: 2, 3 or 4
+  int32_t ded_bufs;        // TMA buffers per worker on a dedicated transfer CTA: 2, 3 or 4
   int32_t piece_bytes;     // bytes of one transfer piece and of one TMA worker buffer (a
                            // multiple of 16, at most kCopyBuf)
 };
@@ -160,15 +160,14 @@ struct SmemLayout {
   volatile int8_t* chain;        // RS: per piece, first parked partial this tile folds (-1)
   uint32_t* ready_bits;
   int ns;  // pipeline stages
-  // barrier slots: full[ns], empty[ns], tfull[2], tempty[2], copyb[2], fin, copye[2] (at most
-  // 23); on a dedicated transfer CTA all 32 slots belong to its copy rings
+  // barrier slots: full[ns], empty[ns], tfull[2], tempty[2], copyb[2], fin (at most 21); on a
+  // dedicated transfer CTA all 32 slots belong to its copy workers
   __device__ uint32_t full(int s) const { return smem_u32(bars + s); }
   __device__ uint32_t empty(int s) const { return smem_u32(bars + ns + s); }
   __device__ uint32_t tfull(int a) const { return smem_u32(bars + 2 * ns + a); }
   __device__ uint32_t tempty(int a) const { return smem_u32(bars + 2 * ns + 2 + a); }
   __device__ uint32_t copyb(int b) const { return smem_u32(bars + 2 * ns + 4 + b); }
   __device__ uint32_t fin() const { return smem_u32(bars + 2 * ns + 6); }
-  __device__ uint32_t copye(int b) const { return smem_u32(bars + 2 * ns + 7 + b); }
 };
 
 __device__ __forceinline__ void raise_error(const KParams& p, uint32_t code, uint32_t site,
@@ -1180,88 +1179,95 @@ __device__ __forceinline__ void for_each_piece(const KParams& p, int32_t wid, in
   }
 }
 
-// One TMA bulk-copy ring of `nbuf` buffers of p.piece_bytes at `stage`, served by two threads
-// in different warps.  The loader fills buffer i % nbuf with piece i (completion counted on
-// full[b]) once the storer has handed that buffer back (empty[b]); the storer waits for the
-// piece, stores it, waits until the store has read the buffer and hands it back.  A piece is
-// counted towards its chunk once its store's writes are complete, which the storer checks
-// kStoresInFlight stores later.  Both threads walk the same piece sequence (worker `wid` of
-// `nw`).
+// One TMA bulk-copy worker (one thread): `nbuf` staging buffers of p.piece_bytes at `stage`,
+// completion barriers bar0, bar0 + 8, ... (one per buffer).  Piece i goes through buffer
+// i % nbuf; the worker keeps nbuf - 1 loads in flight and stores the oldest piece once its load
+// has landed, so loads and stores overlap; a piece is counted towards its chunk once its
+// store's writes are complete, which the worker checks kStoresInFlight stores later (it
+// waits for a store's writes only when that many newer ones are outstanding).
 struct CopyJob {
   uint8_t* dst;
   Piece pc;
   int32_t c, total;
 };
+constexpr uint32_t kMaxCopyBufs = 4;
 constexpr uint32_t kDedicatedRingBytes = 12 * kCopyBuf;  // staging of a dedicated transfer CTA
-constexpr int kStoresInFlight = 2;          // stores whose writes the storer does not wait for
+constexpr int kStoresInFlight = 2;          // stores whose writes a worker does not wait for
 
 static __device__ void run_copy_tma(const KParams& p, const SmemLayout& L, int32_t wid, int32_t nw,
-                                    uint8_t* stage, uint32_t full0, uint32_t empty0,
-                                    uint32_t nbuf, bool loader) {
-  const uint32_t pb = static_cast<uint32_t>(p.piece_bytes);
-  uint32_t i = 0;        // pieces this thread has handled
-  uint32_t counted = 0;  // storer: stored pieces counted towards their chunks
+                                    uint8_t* stage, uint32_t bar0, uint32_t nbuf) {
+  uint32_t issued = 0;  // loads issued
+  uint32_t stored = 0;  // loads waited for and their pieces' stores issued
+  uint32_t counted = 0; // stored pieces counted towards their chunks
+  CopyJob jobs[kMaxCopyBufs] = {};  // the piece in each buffer
   int32_t pend_c[kStoresInFlight + 1], pend_total[kStoresInFlight + 1];  // stored, not counted
+  auto bar_of = [&](uint32_t i) { return bar0 + 8u * (i % nbuf); };
+  auto buf_of = [&](uint32_t i) {
+    return smem_u32(stage + (i % nbuf) * static_cast<uint32_t>(p.piece_bytes));
+  };
+  auto par_of = [&](uint32_t i) { return (i / nbuf) & 1u; };  // use i / nbuf of its barrier
+  auto store_oldest = [&]() -> bool {
+    const uint32_t i = stored;
+    if (!wait_bar(p, L, bar_of(i), par_of(i), 500 + (i % nbuf))) return false;
+    const CopyJob& job = jobs[i % nbuf];
+    const uint32_t buf = buf_of(i);
+    const uint32_t tot = job.pc.nbytes * static_cast<uint32_t>(job.pc.nr);
+    if (job.pc.nbytes == static_cast<uint32_t>(p.row_bytes) || job.pc.nr == 1) {
+      bulk_s2g(job.dst, buf, tot);  // gather rows are back to back (ld_gather == K)
+    } else {
+      for (int32_t r = 0; r < job.pc.nr; ++r)
+        bulk_s2g(job.dst + static_cast<int64_t>(r) * p.ld_gather * 2, buf + r * job.pc.nbytes,
+                 job.pc.nbytes);
+    }
+    bulk_commit();
+    pend_c[stored % (kStoresInFlight + 1)] = job.c;
+    pend_total[stored % (kStoresInFlight + 1)] = job.total;
+    ++stored;
+    if (stored - counted > static_cast<uint32_t>(kStoresInFlight)) {
+      bulk_wait<kStoresInFlight>();  // the oldest uncounted piece's writes are complete
+      signal_piece(p, pend_c[counted % (kStoresInFlight + 1)],
+                   pend_total[counted % (kStoresInFlight + 1)]);
+      ++counted;
+    }
+    return true;
+  };
   auto stop = [&]() { return *L.abort_flag != 0; };
   for_each_piece(p, wid, nw, stop, [&](int32_t s, int32_t j, int32_t c, int32_t total,
                                        const Piece& pc) -> bool {
-    const uint32_t b = i % nbuf;
-    const uint32_t ph = (i / nbuf) & 1u;  // use i / nbuf of buffer b
     const int64_t row_in_shard = static_cast<int64_t>(j) * p.g.Cr + pc.r0;
-    const uint32_t buf = smem_u32(stage + b * pb);
+    const uint8_t* src = p.shard[s] + row_in_shard * p.lda_src * 2 + pc.boff;
+    // buffer issued % nbuf was last read by the store of piece issued - nbuf, which has been
+    // issued (at most nbuf - 1 pieces are loaded but not stored) and in steady state is the
+    // newest store: wait until every issued store has read its shared memory
+    bulk_wait_read<0>();
+    const uint32_t i = issued;
+    const uint32_t buf = buf_of(i), bar = bar_of(i);
     const uint32_t tot = pc.nbytes * static_cast<uint32_t>(pc.nr);
-    if (loader) {
-      // buffer b was handed back after piece i - nbuf (its (i / nbuf - 1)-th release)
-      if (i >= nbuf && !wait_bar(p, L, empty0 + 8u * b, ph ^ 1u, 510 + b)) return false;
-      const uint8_t* src = p.shard[s] + row_in_shard * p.lda_src * 2 + pc.boff;
-      const uint32_t full = full0 + 8u * b;
-      mbar_expect_tx(full, tot);
-      if (p.src_rows_contig || pc.nr == 1) {
-        bulk_g2s(buf, src, tot, full);
-      } else {
-        for (int32_t r = 0; r < pc.nr; ++r)
-          bulk_g2s(buf + r * pc.nbytes, src + static_cast<int64_t>(r) * p.lda_src * 2, pc.nbytes,
-                   full);
-      }
+    mbar_expect_tx(bar, tot);
+    if (p.src_rows_contig || pc.nr == 1) {
+      bulk_g2s(buf, src, tot, bar);
     } else {
-      if (!wait_bar(p, L, full0 + 8u * b, ph, 520 + b)) return false;
-      uint8_t* dst =
-          p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard) * p.ld_gather * 2 + pc.boff;
-      if (pc.nbytes == static_cast<uint32_t>(p.row_bytes) || pc.nr == 1) {
-        bulk_s2g(dst, buf, tot);  // gather rows are back to back (ld_gather == K)
-      } else {
-        for (int32_t r = 0; r < pc.nr; ++r)
-          bulk_s2g(dst + static_cast<int64_t>(r) * p.ld_gather * 2, buf + r * pc.nbytes, pc.nbytes);
-      }
-      bulk_commit();
-      bulk_wait_read<0>();  // the store has read the buffer: hand it back to the loader
-      mbar_arrive(empty0 + 8u * b);
-      pend_c[i % (kStoresInFlight + 1)] = c;
-      pend_total[i % (kStoresInFlight + 1)] = total;
-      if (i + 1 - counted > static_cast<uint32_t>(kStoresInFlight)) {
-        bulk_wait<kStoresInFlight>();  // the oldest uncounted piece's writes are complete
-        signal_piece(p, pend_c[counted % (kStoresInFlight + 1)],
-                     pend_total[counted % (kStoresInFlight + 1)]);
-        ++counted;
-      }
+      for (int32_t r = 0; r < pc.nr; ++r)
+        bulk_g2s(buf + r * pc.nbytes, src + static_cast<int64_t>(r) * p.lda_src * 2, pc.nbytes, bar);
     }
-    ++i;
-    return true;
+    jobs[i % nbuf] = {
+        p.gather + (static_cast<int64_t>(s) * p.g.Ms + row_in_shard) * p.ld_gather * 2 + pc.boff,
+        pc, c, total};
+    ++issued;
+    // keep nbuf - 1 loads in flight: store the oldest piece once nbuf are outstanding
+    return issued - stored < nbuf || store_oldest();
   });
-  if (loader) {
-    // after an abort, the loads in flight (the last nbuf issued at most) land before the CTA
-    // can exit; no load is issued into a buffer after these
-    for (uint32_t k = i > nbuf ? i - nbuf : 0; k < i; ++k) {
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(full0 + 8u * (k % nbuf), (k / nbuf) & 1u) &&
-             globaltimer_ns() - t0 < p.timeout_ns) {
-      }
+  while (!*L.abort_flag && stored < issued && store_oldest()) {
+  }
+  bulk_wait<0>();
+  for (; !*L.abort_flag && counted < stored; ++counted)
+    signal_piece(p, pend_c[counted % (kStoresInFlight + 1)],
+                 pend_total[counted % (kStoresInFlight + 1)]);
+  // after an abort, the loads still in flight (at most nbuf) land before the CTA can exit
+  for (uint32_t i = stored; i < issued; ++i) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar_of(i), par_of(i)) && globaltimer_ns() - t0 < p.timeout_ns) {
     }
-  } else {
-    bulk_wait<0>();
-    for (; !*L.abort_flag && counted < i; ++counted)
-      signal_piece(p, pend_c[counted % (kStoresInFlight + 1)],
-                   pend_total[counted % (kStoresInFlight + 1)]);
   }
 }
 
@@ -1354,7 +1360,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
         mbar_init(L.copyb(a), 1);
       }
       mbar_init(L.fin(), 1);
-      for (int a = 0; a < 2; ++a) mbar_init(L.copye(a), 1);
     }
     *L.abort_flag = 0;
     *L.unit_flag = 0;
@@ -1376,18 +1381,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 
   if (copier) {
     // dedicated transfer CTA: no GEMM; the operand ring becomes four workers' staging rings
-    // of ded_bufs piece-sized buffers each, each ring served by the lane 0s of a warp pair
-    // (loader, storer): as many rings as the 192 KiB hold, at most four; full barriers in
-    // slots 0-15, empty ones in 16-31
+    // of ded_bufs piece-sized buffers each: as many workers (one per warp, at most 8) as the
+    // 192 KiB of the ring hold
     if (OP == kOpAG && !p.plain) {
       const uint32_t nbuf = static_cast<uint32_t>(p.ded_bufs);
-      const int nring = min32(4, static_cast<int32_t>(kDedicatedRingBytes /
-                                                      (static_cast<uint32_t>(p.piece_bytes) * nbuf)));
-      const int ring = warp >> 1;
-      if (COPY == kCopyTma && ring < nring && lane == 0)
-        run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x) * nring + ring, p.copy_ctas * nring,
-                     L.a + ring * nbuf * p.piece_bytes, smem_u32(L.bars + ring * nbuf),
-                     smem_u32(L.bars + 16 + ring * nbuf), nbuf, (warp & 1) == 0);
+      const int nwk = min32(8, static_cast<int32_t>(kDedicatedRingBytes /
+                                                    (static_cast<uint32_t>(p.piece_bytes) * nbuf)));
+      if (COPY == kCopyTma && warp < nwk && lane == 0)
+        run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x) * nwk + warp, p.copy_ctas * nwk,
+                     L.a + warp * nbuf * p.piece_bytes, smem_u32(L.bars + warp * nbuf), nbuf);
       if (COPY == kCopyLdst)
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 8 + warp, p.copy_ctas * 8);
     }
@@ -1397,9 +1399,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     if ((cl_rank<CL>() & 1u) == 0u) run_mma<OP, CL, NS>(p, L, tmem_base);
   } else if (warp < 4) {
     if (OP == kOpAG && !p.plain && p.copy_ctas == 0) {  // co-located transfer warps
-      if (COPY == kCopyTma && lane == 0)  // warp 2 loads, warp 3 stores
+      if (COPY == kCopyTma && warp == 2 && lane == 0)
         run_copy_tma(p, L, static_cast<int32_t>(blockIdx.x), static_cast<int32_t>(gridDim.x),
-                     L.copy, L.copyb(0), L.copye(0), 2, warp == 2);
+                     L.copy, L.copyb(0), 2);
       if (COPY == kCopyLdst)
         run_copy_ldst(p, L, lane, static_cast<int32_t>(blockIdx.x) * 2 + (warp - 2),
                       static_cast<int32_t>(gridDim.x) * 2);
