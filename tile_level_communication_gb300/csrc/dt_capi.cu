@@ -578,6 +578,28 @@ void set_drop_chunk(KParams& p, const Derived& d, int32_t drop) {
   p.drop_chunk = s * d.nC + j;
 }
 
+// out_h of the AllToAll as a 3-D tensor [W sources][M/W rows][N/W columns]: a box stored at
+// (x, y, source q) is clipped at source q's rows and at the destination's columns.
+dt_status make_a2a_out_tmap(CUtensorMap* tm, void* out, int64_t ms, int64_t nw, int64_t ldc,
+                            int32_t w, bool f32) {
+  PfnEncodeTiled enc = encode_tiled();
+  if (!enc) return fail(DT_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const uint64_t esz = f32 ? 4 : 2;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(nw), static_cast<cuuint64_t>(ms),
+                              static_cast<cuuint64_t>(w)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldc) * esz,
+                                 static_cast<cuuint64_t>(ms) * ldc * esz};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kBM), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(DT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the AllToAll output", (int)r);
+  return DT_OK;
+}
+
 dt_status make_c_tmap(CUtensorMap* tm, void* c, int64_t rows, int64_t cols, int64_t ldc, bool f32) {
   return make_tmap(tm, c, cols, rows, static_cast<uint64_t>(ldc) * (f32 ? 4 : 2), 32, kBM,
                    f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -1319,6 +1341,10 @@ dt_status dt_gemm_a2a(const void* const* a_, const void* const* b_, void* const*
   KParams p;
   if ((s = a2a_params(p, d, a_, b_, ws, epoch)) != DT_OK) return s;
   for (int h = 0; h < d.W; ++h) p.out[h] = out[h];
+  p.c_tma = c_tma_setting();
+  for (int h = 0; h < d.W && p.c_tma; ++h)
+    if ((s = make_a2a_out_tmap(&p.tmOut[h], out[h], d.Ms, d.geom.Nw, d.ldc, d.W, d.f32)) != DT_OK)
+      return s;
   const int sms = a->num_sms > 0 ? std::min(a->num_sms, dev->sms) : dev->sms;
   cudaError_t e = launch_a2a_kernel(p, d.f32, grid_for(d, d.T, sms), stream, d.cl);
   if (e != cudaSuccess) return cuda_fail(e, "fused GEMM-AllToAll launch");

@@ -66,9 +66,9 @@ enum DevCode : uint32_t {
 
 // Dynamic shared memory of a kernel instance: alignment slack, the operand ring, two 16 KiB
 // staging buffers (AllGather: the co-located TMA transfer, else C's boxes on their way to a
-// TMA store; ReduceScatter: running-sum tiles), flags.
-__host__ __device__ constexpr bool has_staging(int op, int copy_mode) {
-  return op != 2 /* kOpA2A */ || copy_mode == kCopyTma;
+// TMA store; ReduceScatter: running-sum tiles; AllToAll: out_h's boxes), flags.
+__host__ __device__ constexpr bool has_staging(int /*op*/, int /*copy_mode*/) {
+  return true;  // every instance has the two staging buffers
 }
 // cl: CTAs per cluster (1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile)
 __host__ __device__ constexpr int kernel_smem_bytes(int op, int copy_mode, int cl) {
@@ -130,7 +130,8 @@ struct KParams {
                            // B_q's k-blocks stay (evict last)
   unsigned long long* trace;  // AG debug timeline (global timer, ns), or null; see trace_*
   int32_t c_tma;           // AG: C leaves through the staging buffers as TMA stores (tmOut[0],
-                           // 32-column boxes clipped at M and N); 0: each thread stores its row
+                           // 32-column boxes clipped at M and N); A2A: out_h does (tmOut[h], 3-D
+                           // [W][M/W][N/W], clipped at each source's rows); 0: per-thread rows
   int32_t a_from_shards;   // AG: each tile's A rows are loaded from the owning shard (tmA[s])
   int32_t ded_bufs;        // TMA buffers per worker on a dedicated transfer CTA: 2, 3 or 4
   int32_t piece_bytes;     // bytes of one transfer piece and of one TMA worker buffer (a
@@ -745,7 +746,8 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
   constexpr bool kStoreF32 = RS || F32;  // ReduceScatter partials are fp32
   // AllGather: C's 32-column boxes go out as TMA stores from the staging buffers (which the
   // co-located TMA transfer, when there is one, needs for itself)
-  const bool c_tma = OP == kOpAG && p.c_tma != 0 && staging_free;
+  const bool c_tma =
+      (OP == kOpAG || (A2A && !p.plain)) && p.c_tma != 0 && staging_free;
   const int qd = warp - 4;  // TMEM lane quadrant this warp may read
   const int et = threadIdx.x - 128;
   const bool fused_rs = RS && !p.plain;
@@ -978,7 +980,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
       // tensor map clips rows at M and columns at N.  A buffer is rewritten once the store
       // issued from it two boxes earlier has read it.
       const int r = qd * 32 + lane;
-      const int ncb = static_cast<int>(min64(kBN, p.g.N - ti.col0) + 31) / 32;
+      const int ncb = static_cast<int>(min64(kBN, ti.col_end - ti.col0) + 31) / 32;
 #pragma unroll 1
       for (int cb = 0; cb < ncb; ++cb) {
         uint8_t* buf = L.copy + (stage_ctr & 1u) * kCopyBuf;
@@ -1008,11 +1010,20 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (et == 0) {
-          tma_store_2d(&p.tmOut[0], smem_u32(buf), static_cast<int32_t>(ti.col0 + cb * 32),
-                       static_cast<int32_t>(ti.row0));
+          if (A2A)  // destination h's block, source q's rows (local), clipped at M/W and N/W
+            tma_store_3d(&p.tmOut[ti.h], smem_u32(buf),
+                         static_cast<int32_t>(ti.col0 - static_cast<int64_t>(ti.h) * p.g.Nw + cb * 32),
+                         static_cast<int32_t>(ti.row0), ti.q);
+          else
+            tma_store_2d(&p.tmOut[0], smem_u32(buf), static_cast<int32_t>(ti.col0 + cb * 32),
+                         static_cast<int32_t>(ti.row0));
           bulk_commit();
         }
         ++stage_ctr;
+      }
+      if (A2A && et == 0) {
+        bulk_wait<0>();  // the tile's rows are in out_h before its chunks are counted
+        fence_proxy_async_global();
       }
     }
 #pragma unroll 1

@@ -92,6 +92,16 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* tm, uint32_
       "r"(src), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
+// 3-D tiled tensor store shared -> global (bulk group), clipped at the tensor's extent in
+// every dimension.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int32_t x,
+                                             int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
