@@ -148,14 +148,14 @@ int32_t ded_bufs_setting() {
   return v;
 }
 
-// Bytes of a transfer piece on dedicated transfer CTAs (8 or 16 KiB); DT_COPY_PIECE overrides.
-// 8 KiB pieces (8 workers) measured 4.4-4.7 TB/s against 5.4-5.5 for 16 KiB: the per-piece
-// work of a worker, not the bytes in flight, sets the rate.
+// Bytes of a transfer piece on dedicated transfer CTAs (8, 16 or 32 KiB); DT_COPY_PIECE
+// overrides.  8 KiB pieces (8 workers) measured 4.4-4.7 TB/s against 5.4-5.5 for 16 KiB: the
+// per-piece work of a worker, not the bytes in flight, sets the rate.
 int32_t ded_piece_setting() {
   static int32_t v = [] {
     const char* e = getenv("DT_COPY_PIECE");
     const int x = e ? atoi(e) : 16384;
-    return static_cast<int32_t>(x <= 8192 ? 8192 : kCopyBuf);
+    return static_cast<int32_t>(x <= 8192 ? 8192 : (x >= 32768 ? 2 * kCopyBuf : kCopyBuf));
   }();
   return v;
 }
