@@ -143,7 +143,7 @@ int32_t ded_bufs_setting() {
   static int32_t v = [] {
     const char* e = getenv("DT_COPY_BUFS");
     const int x = e ? atoi(e) : 2;
-    return static_cast<int32_t>(x < 2 ? 2 : (x > 4 ? 4 : x));
+    return static_cast<int32_t>(x < 1 ? 1 : (x > 4 ? 4 : x));
   }();
   return v;
 }

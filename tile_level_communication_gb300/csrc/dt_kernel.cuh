@@ -133,9 +133,10 @@ struct KParams {
                            // 32-column boxes clipped at M and N); A2A: out_h does (tmOut[h], 3-D
                            // [W][M/W][N/W], clipped at each source's rows); 0: per-thread rows
   int32_t a_from_shards;   // AG: each tile's A rows are loaded from the owning shard (tmA[s])
-  int32_t ded_bufs;        // TMA buffers per worker on a dedicated transfer CTA: 2, 3 or 4
+  int32_t ded_bufs;        // TMA buffers per worker on a dedicated transfer CTA: 1 to 4
   int32_t piece_bytes;     // bytes of one transfer piece and of one TMA worker buffer (a
-                           // multiple of 16, at most kCopyBuf)
+                           // multiple of 16; kCopyBuf, or up to 2 * kCopyBuf on dedicated
+                           // transfer CTAs)
 };
 
 // AG debug timeline, in 64-bit words: [0] first CTA start (min), [1] last CTA exit (max),
