@@ -135,26 +135,27 @@ uint64_t default_timeout_ns() {
   return v;
 }
 
-// TMA buffers per worker on a dedicated transfer CTA (2, 3 or 4); DT_COPY_BUFS overrides.
-// Measured on 256 MiB AllGathers (16 KiB pieces): 6 workers x 2 buffers 5.37-5.54 TB/s, 4 x 3
-// 5.11-5.26, 3 x 4 4.78-4.87: more workers beat deeper rings.  A ring served by a loader and a
-// storer thread in two warps (4 rings of 2-4 buffers) measured 4.67-4.96 TB/s.
+// TMA buffers per worker on a dedicated transfer CTA (1 to 4); DT_COPY_BUFS overrides.
+// Measured on 256 MiB AllGathers at 2048-row chunks (L2 flushed): 32 KiB pieces, 6 workers x 1
+// buffer 5.79-5.91 TB/s, 3 x 2 5.54-5.66; 16 KiB pieces, 8 x 1 5.54, 6 x 2 5.48-5.54, 4 x 3
+// 5.16-5.26, 3 x 4 4.87; 8 KiB pieces 4.35-4.65; a ring per warp pair with separate loader and
+// storer threads 4.67-4.96.  More workers and bigger pieces win: a worker's serial per-piece
+// work, not the bytes in flight, sets the rate.
 int32_t ded_bufs_setting() {
   static int32_t v = [] {
     const char* e = getenv("DT_COPY_BUFS");
-    const int x = e ? atoi(e) : 2;
+    const int x = e ? atoi(e) : 1;
     return static_cast<int32_t>(x < 1 ? 1 : (x > 4 ? 4 : x));
   }();
   return v;
 }
 
 // Bytes of a transfer piece on dedicated transfer CTAs (8, 16 or 32 KiB); DT_COPY_PIECE
-// overrides.  8 KiB pieces (8 workers) measured 4.4-4.7 TB/s against 5.4-5.5 for 16 KiB: the
-// per-piece work of a worker, not the bytes in flight, sets the rate.
+// overrides (see the measurements above).
 int32_t ded_piece_setting() {
   static int32_t v = [] {
     const char* e = getenv("DT_COPY_PIECE");
-    const int x = e ? atoi(e) : 16384;
+    const int x = e ? atoi(e) : 32768;
     return static_cast<int32_t>(x <= 8192 ? 8192 : (x >= 32768 ? 2 * kCopyBuf : kCopyBuf));
   }();
   return v;
