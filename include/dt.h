@@ -257,8 +257,11 @@ dt_status dt_ffn_ag_rs(const void* const* x_shards, const void* w1, const void* 
  * on, then rank+1, ..).  Backends:
  *   DT_XFER_COPY_ENGINE : one (2-D) copy per chunk on `stream`; any ldc.
  *   DT_XFER_TMA / LDST  : one launch of the fused kernel with no GEMM tiles, every CTA (all
- *                         SMs, or a->num_sms) running the transfer workers (4 TMA bulk-copy
- *                         threads or 8 vector ld/st warps per CTA); each chunk's ready flag in
+ *                         SMs, or a->num_sms) running the transfer workers (6 TMA bulk-copy
+ *                         threads moving 32 KiB pieces, or 8 vector ld/st warps, per CTA; the
+ *                         environment variables DT_COPY_PIECE (8192, 16384, 32768) and
+ *                         DT_COPY_BUFS (buffers per TMA worker, 1-4) override the TMA
+ *                         workers' piece size and depth); each chunk's ready flag in
  *                         the workspace is released with the call's epoch.  Needs ldc == K
  *                         (rows land back to back).
  *   DT_XFER_AUTO        : the AllGather-GEMM's rule (copy engine for chunks of >= 8 MiB, else
