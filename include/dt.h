@@ -379,16 +379,19 @@ size_t dt_sizeof_tune_point(void);
  * {4, 8, 16} at the best point.  Scatter-mode candidates
  * (dt_tune_reduce with op DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A): chunk rows x group
  * widths {4, 8, 16}, at the tile rows given, and for DT_OP_GEMM_RS / DT_OP_GEMM_AR x column
- * bands {as given, one band} when the given (or automatic) bands are more than one.  Each
- * candidate runs once as
+ * bands {as given, one band} when the given (or automatic) bands are more than one.  A
+ * candidate whose group width or column band gives the same tile order as an earlier one with
+ * the same chunk rows, tile rows and transfer is not timed.  Each candidate runs once as
  * warm-up and `reps` times timed with CUDA events on `stream` (synchronising).  A forward
  * pass times every candidate and takes the fastest as the reference; a reverse pass times each
  * other candidate between two timings of the reference and scores it by its time over their
  * mean (the GPU's clock drifts as it warms under the power cap; the ratio cancels the drift);
  * a point's reported ms is its score times the reference's median time.  Candidates whose
- * workspace exceeds ws_bytes are skipped.  The
- * fastest knobs are written into *a (chunk_rows, backend, copy_ctas, group, tile_m; swizzle
- * stays on).  `points` (may be NULL) receives
+ * workspace exceeds ws_bytes are skipped.  The knobs kept are those of the largest chunk rows
+ * among the points within 1 % of the fastest (fewer, larger chunks re-stream B from DRAM fewer
+ * times, which a short timing at full clock does not show but a run under the power cap
+ * does), written into *a (chunk_rows, backend, copy_ctas, group, tile_m, col_band;
+ * swizzle stays on).  `points` (may be NULL) receives
  * up to max_points candidates and *n_points their number.  The inputs are read and the
  * outputs written by every candidate; all candidates give bit-identical outputs. */
 dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, void* workspace,
