@@ -387,10 +387,11 @@ size_t dt_sizeof_tune_point(void);
  * other candidate between two timings of the reference and scores it by its time over their
  * mean (the GPU's clock drifts as it warms under the power cap; the ratio cancels the drift);
  * a point's reported ms is its score times the reference's median time.  Candidates whose
- * workspace exceeds ws_bytes are skipped.  The knobs kept are those of the largest chunk rows
- * among the points within 1 % of the fastest (fewer, larger chunks re-stream B from DRAM fewer
- * times, which a short timing at full clock does not show but a run under the power cap
- * does), written into *a (chunk_rows, backend, copy_ctas, group, tile_m, col_band;
+ * workspace exceeds ws_bytes are skipped.  Among the points within 1 % of the fastest, the
+ * knobs kept are those that move the fewest DRAM bytes: the automatic column bands before one
+ * band, then the largest chunk rows (fewer key groups re-stream B fewer times), then the
+ * fastest; a short timing at full clock does not show DRAM bytes, a run under the power cap
+ * does.  They are written into *a (chunk_rows, backend, copy_ctas, group, tile_m, col_band;
  * swizzle stays on).  `points` (may be NULL) receives
  * up to max_points candidates and *n_points their number.  The inputs are read and the
  * outputs written by every candidate; all candidates give bit-identical outputs. */

@@ -1576,13 +1576,16 @@ void drop_same_order(std::vector<dt_args>& cands, int op) {
   cands.swap(keep);
 }
 
-// Pick the point to keep and copy its knobs into *a: the largest chunk rows among the points
-// within kTuneTie of the fastest (then the fastest of those).  The tuner times short bursts at
-// full clock; run for seconds under the power cap, a kernel's clock follows its energy, and
-// fewer, larger chunks mean fewer key groups in the order, each of which re-streams B from DRAM
-// (the largest AllGather with the per-tile pull, 3 s runs: chunk 2048 / 1024 / 256 read 2.52 /
-// 3.06 / 4.28 GB per launch and took 1.282 / 1.315 / 1.343 ms at 1425 / 1387 / 1350-1365 MHz,
-// where their burst times lie within 1 %).
+// Pick the point to keep and copy its knobs into *a: among the points within kTuneTie of the
+// fastest, the one that moves the fewest DRAM bytes: automatic column bands before one band,
+// then the largest chunk rows, then the fastest.  The tuner times short bursts at full clock;
+// run for seconds under the power cap, a kernel's clock follows its energy.  Fewer, larger
+// chunks mean fewer key groups in the order, each of which re-streams B from DRAM (the largest
+// AllGather with the per-tile pull, 3 s runs: chunk 2048 / 1024 / 256 read 2.52 / 3.06 / 4.28
+// GB per launch and took 1.282 / 1.315 / 1.343 ms at 1425 / 1387 / 1350-1365 MHz, where their
+// burst times lie within 1 %); column bands keep B_q's band in L2 (the FFN pair's
+// ReduceScatter reads 4.1-4.2 GB per launch with two bands against 5.5-6.0 GB with one, and
+// runs 3-5 % faster over 200 calls).
 constexpr float kTuneTie = 1.01f;
 dt_status tune_finish(std::vector<dt_tune_point>& pts, dt_args* a, dt_tune_point* out,
                       int32_t max_points, int32_t* n_points) {
@@ -1591,11 +1594,15 @@ dt_status tune_finish(std::vector<dt_tune_point>& pts, dt_args* a, dt_tune_point
     if (pts[i].status == DT_OK && pts[i].ms >= 0 && (fastest < 0 || pts[i].ms < pts[fastest].ms))
       fastest = i;
   int best = fastest;
+  auto fewer_bytes = [&](const dt_tune_point& x, const dt_tune_point& y) {
+    const bool xa = x.col_band == 0, ya = y.col_band == 0;  // automatic bands
+    if (xa != ya) return xa;
+    if (x.chunk_rows != y.chunk_rows) return x.chunk_rows > y.chunk_rows;
+    return x.ms < y.ms;
+  };
   for (int i = 0; fastest >= 0 && i < static_cast<int>(pts.size()); ++i) {
     if (pts[i].status != DT_OK || pts[i].ms < 0 || pts[i].ms > kTuneTie * pts[fastest].ms) continue;
-    if (pts[i].chunk_rows > pts[best].chunk_rows ||
-        (pts[i].chunk_rows == pts[best].chunk_rows && pts[i].ms < pts[best].ms))
-      best = i;
+    if (fewer_bytes(pts[i], pts[best])) best = i;
   }
   if (n_points) *n_points = static_cast<int32_t>(pts.size());
   if (out)
