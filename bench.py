@@ -43,14 +43,14 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch after two
     # warm-up launches, 256-row tiles; keys "chunk_rows/tile_rows/col_band/l2_hints" (the
     # group width gives the same order at these chunk sizes: a key holds at most 4 m-tiles)
-    "rs_w8_m8192_n8192_k3584": {"csrc": "42333423845d344c",
+    "rs_w8_m8192_n8192_k3584": {"csrc": "cbe14ea6121af46e",
                                 "profile": "profiles/fused_gemm_rs_w8_m8192_n8192_k3584.md",
                                 "points": {
-        "1024/256/16/3": 4206936832 + 1993850112, "1024/256/32/3": 5492091648 + 1995920640,
-        "512/256/16/3": 4097069824 + 1992612096, "512/256/32/3": 6038561792 + 1998166272,
-        "256/256/16/3": 4189729280 + 1992555008, "256/256/32/3": 5862915328 + 1998213632,
-        "128/256/16/3": 4137170944 + 1992702208, "128/256/32/3": 5787766784 + 1998498816,
-        "64/256/16/3": 3870661888 + 2000494592, "64/256/32/3": 5136942592 + 2002726144,
+        "1024/256/16/3": 4548564224 + 1997944320, "1024/256/32/3": 5604210432 + 1996624640,
+        "512/256/16/3": 4398675200 + 1993935104, "512/256/32/3": 5485574912 + 1997230848,
+        "256/256/16/3": 4534666240 + 1994084864, "256/256/32/3": 5951836416 + 1997604864,
+        "128/256/16/3": 4497827072 + 1993752320, "128/256/32/3": 5884580096 + 1997792768,
+        "64/256/16/3": 4232500480 + 1991888640, "64/256/32/3": 5848513792 + 1997879552,
     }},
 }
 
@@ -350,8 +350,11 @@ def run_sweep(args):
     peak = peaks()["bf16_tflops_sustained"]
     chunks = [int(x) for x in args.sweep_chunks.split(",")]
     ws = None
+    backends = ["copy_engine", "tma", "ldst"]
+    if (wl.m // wl.world_size) % 128 == 0:
+        backends.append("tma_tile")  # the per-tile pull needs tile-aligned shards
     for cr in chunks:
-        for backend in ["copy_engine", "tma", "ldst"]:
+        for backend in backends:
             for swizzle in [True, False]:
                 a = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, rank=args.rank_view,
                                  chunk_rows=cr, swizzle=swizzle, backend=backend)

@@ -102,7 +102,7 @@ typedef struct dt_args {
   int32_t out_dtype;   /* dt_dtype of C / out_s                                            */
   int32_t tile_m;      /* rows of a tile: 128 (one CTA, tcgen05 cta_group::1), 256 (a cluster
                           of two CTAs on two SMs, cta_group::2: each stages 128 rows of A and
-                          half of the 256 columns of B, 6-7 pipeline stages),
+                          half of the 256 columns of B, 6 pipeline stages),
                           0 = 256 when that leaves at least 76 tiles (one per SM pair) and
                           copy_ctas is even, else 128; copy_ctas must be a multiple of
                           tile_m / 128                                                      */

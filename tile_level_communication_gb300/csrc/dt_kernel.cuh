@@ -4,7 +4,7 @@
 // One CTA per SM, 8 warps; CL CTAs per cluster share a tile of CL x 128 rows (CL = 1: one
 // CTA, tcgen05 cta_group::1; CL = 2: a CTA pair, cta_group::2):
 //   warp 0      TMA producer: per tile, waits (bounded) for the ready flags of the chunks
-//               this CTA's rows live in, then streams A / B k-blocks into a 4- to 7-stage
+//               this CTA's rows live in, then streams A / B k-blocks into a 4- or 6-stage
 //               ring (a pair's stages complete on its even CTA's barriers).
 //   warp 1      MMA issuer (one thread; the even CTA of a pair): tcgen05.mma 128x256x16 or
 //               256x256x16 into one of two TMEM accumulators; allocates / frees TMEM.
