@@ -58,6 +58,10 @@ def test_args_layout_matches(dt):
     (dict(world_size=2, m=8, n=8, k=8, chunk_rows=0), "DT_ERR_INVALID"),
     (dict(world_size=2, m=8, n=8, k=8, lda=4), "DT_ERR_INVALID"),
     (dict(world_size=2, m=8, n=8, k=8, lda=12), "DT_ERR_INVALID"),  # 16-byte rows
+    (dict(world_size=2, m=8, n=8, k=8, tile_m=512), "DT_ERR_UNSUPPORTED"),  # 512-row tiles gone
+    (dict(world_size=2, m=2 * 100, n=8, k=8, backend="tma_tile"), "DT_ERR_UNSUPPORTED"),  # M/W % 128
+    (dict(world_size=2, m=2 * 128, n=8, k=8, backend="tma_tile", copy_ctas=2), "DT_ERR_INVALID"),
+    (dict(world_size=2, m=8, n=8, k=8, col_band=-1), "DT_ERR_INVALID"),
 ])
 def test_argument_errors_are_synchronous(dt, kw, status):
     w = kw.pop("world_size")
@@ -286,6 +290,7 @@ def test_a2a_workspace_holds_only_control(dt):
     (dict(world_size=2, m=512, k=512, ldc=520, backend="tma"), "DT_ERR_UNSUPPORTED"),
     (dict(world_size=2, m=512, k=512, ldc=520, backend="ldst"), "DT_ERR_UNSUPPORTED"),
     (dict(world_size=2, m=512, k=512, lda=500), "DT_ERR_INVALID"),
+    (dict(world_size=2, m=512, k=512, backend="tma_tile"), "DT_ERR_INVALID"),  # not a transfer
 ])
 def test_allgather_argument_errors_are_synchronous(dt, kw, status):
     w = kw.pop("world_size")
@@ -323,3 +328,39 @@ def test_group_widths_that_reorder_nothing(dt):
     orders = {g: tuple(dt.swizzle_plan(dt.make_args(w, m, n, 2048, chunk_rows=512, group=g),
                                        dt.OP_RS).tolist()) for g in (1, 4, 8, 16)}
     assert orders[4] == orders[8] == orders[16] != orders[1]
+
+
+def test_tile_pull_needs_no_gather_buffer(dt):
+    """The per-tile pull reads the shards in place: its workspace is the control block and the
+    tile order only, and only the AllGather-GEMM takes it."""
+    a = dt.make_args(8, 8192, 3584, 8192, chunk_rows=1024, backend="tma_tile")
+    b = dt.make_args(8, 8192, 3584, 8192, chunk_rows=1024, backend="tma")
+    assert dt.workspace_size(a, dt.OP_AG) < 1 << 20
+    assert dt.workspace_size(b, dt.OP_AG) - dt.workspace_size(a, dt.OP_AG) >= 8192 * 8192 * 2
+    with pytest.raises(dt.DtError) as ei:
+        dt.workspace_size(a, dt.OP_RS)
+    assert ei.value.status == dt.capi.DT_ERR_INVALID
+
+
+def test_trace_bytes_and_attach(dt):
+    a = dt.make_args(8, 8192, 3584, 8192, chunk_rows=1000)
+    nc = -(-1024 // 1000)
+    assert dt.trace_bytes(a) == (4 + 3 * 8 * nc) * 8
+    dt.trace_attach(None)
+    with pytest.raises(dt.DtError):
+        dt.trace_attach(12, 64)  # not 8-byte aligned
+    dt.trace_attach(None)
+
+
+def test_trace_decode_marks_missing_events():
+    from tile_level_communication_gb300 import capi
+    a = capi.DtArgs()
+    a.world_size, a.m, a.chunk_rows = 2, 4, 1   # two chunks per rank
+    none = (1 << 64) - 1
+    words = [1000, 9000, 700, 2] + [none] * 12
+    words[4 + 3 * 2] = 3000   # chunk (1, 0): released at +2 us
+    words[6 + 3 * 2] = 3500   # and first read at +2.5 us
+    tr = capi.trace_decode(words, a)
+    assert tr["kernel_us"] == 8.0 and tr["stall_us_total"] == 0.7 and tr["stalled_waits"] == 2
+    assert tr["chunks"][(1, 0)] == {"released_us": 2.0, "first_miss_us": None, "first_read_us": 2.5}
+    assert tr["chunks"][(0, 1)] == {"released_us": None, "first_miss_us": None, "first_read_us": None}
