@@ -42,7 +42,7 @@ struct LaunchState {
 template <int OP, int COPY, bool F32, int CL>
 cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStream_t stream) {
   auto kern = fused_gemm_kernel<OP, COPY, F32, CL>;
-  const int smem = kernel_smem_bytes(OP, COPY, CL);
+  const int smem = kernel_smem_bytes(CL);
   static LaunchState<OP, COPY, F32, CL> state = {};
   int dev = 0;
   cudaError_t de = cudaGetDevice(&dev);

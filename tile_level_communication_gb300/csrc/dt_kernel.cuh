@@ -38,13 +38,10 @@ constexpr int kAStage = kBM * kBK * 2;   // 16 KB: 128 rows x 64 bf16, 128-byte 
 constexpr int kBSlab = kBK * 64 * 2;     // 8 KB: 64 k-rows x 64 bf16 columns
 // Operand ring per CTA: one CTA per tile stages all 256 columns of B (4 slabs, 32 KB) in 4
 // stages; a CTA pair splits them (2 slabs, 16 KB each) and affords 6 stages next to the 32 KB
-// staging buffers, 7 without them.
-__host__ __device__ constexpr int stages(bool pair, bool staging) {
-  return pair ? (staging ? 6 : 7) : 4;
-}
+// staging buffers.
+__host__ __device__ constexpr int stages(bool pair) { return pair ? 6 : 4; }
 __host__ __device__ constexpr int b_slabs(bool pair) { return pair ? 2 : 4; }
 __host__ __device__ constexpr int b_stage_bytes(bool pair) { return b_slabs(pair) * kBSlab; }
-constexpr int kMaxStages = 7;
 constexpr int kCopyBuf = 16384;          // TMA bulk copy staging, two buffers
 constexpr int kTmemCols = 512;           // two 128x256 fp32 accumulators
 constexpr int kMaxW = 16;
@@ -67,13 +64,9 @@ enum DevCode : uint32_t {
 // Dynamic shared memory of a kernel instance: alignment slack, the operand ring, two 16 KiB
 // staging buffers (AllGather: the co-located TMA transfer, else C's boxes on their way to a
 // TMA store; ReduceScatter: running-sum tiles; AllToAll: out_h's boxes), flags.
-__host__ __device__ constexpr bool has_staging(int /*op*/, int /*copy_mode*/) {
-  return true;  // every instance has the two staging buffers
-}
 // cl: CTAs per cluster (1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile)
-__host__ __device__ constexpr int kernel_smem_bytes(int op, int copy_mode, int cl) {
-  return 1024 + stages(cl > 1, has_staging(op, copy_mode)) * (kAStage + b_stage_bytes(cl > 1)) +
-         (has_staging(op, copy_mode) ? 2 * kCopyBuf : 0) + kMiscBytes;
+__host__ __device__ constexpr int kernel_smem_bytes(int cl) {
+  return 1024 + stages(cl > 1) * (kAStage + b_stage_bytes(cl > 1)) + 2 * kCopyBuf + kMiscBytes;
 }
 
 struct KParams {
@@ -1330,7 +1323,7 @@ template <int OP, int COPY, bool F32, int CL>
 __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_constant__ KParams p) {
   static_assert(CL == 1 || CL == 2, "one CTA or a CTA pair per tile");
   constexpr bool PAIR = CL > 1;
-  constexpr int NS = stages(PAIR, has_staging(OP, COPY));
+  constexpr int NS = stages(PAIR);
   static_assert(COPY != kCopyTma ||
                     kDedicatedRingBytes <= NS * (kAStage + b_stage_bytes(PAIR)),
                 "the dedicated TMA workers' buffers fit in the operand ring");
@@ -1342,7 +1335,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   L.a = base;
   L.b = L.a + NS * kAStage;
   L.copy = L.b + NS * b_stage_bytes(PAIR);
-  uint8_t* misc = L.copy + (has_staging(OP, COPY) ? 2 * kCopyBuf : 0);
+  uint8_t* misc = L.copy + 2 * kCopyBuf;
   L.bars = reinterpret_cast<uint64_t*>(misc);  // up to 32 barriers
   L.tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   L.abort_flag = reinterpret_cast<volatile int*>(misc + 260);
