@@ -43,14 +43,14 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch after two
     # warm-up launches, 256-row tiles; keys "chunk_rows/tile_rows/col_band/l2_hints" (the
     # group width gives the same order at these chunk sizes: a key holds at most 4 m-tiles)
-    "rs_w8_m8192_n8192_k3584": {"csrc": "cbe14ea6121af46e",
+    "rs_w8_m8192_n8192_k3584": {"csrc": "f6095990e63b13d1",
                                 "profile": "profiles/fused_gemm_rs_w8_m8192_n8192_k3584.md",
                                 "points": {
-        "1024/256/16/3": 4548564224 + 1997944320, "1024/256/32/3": 5604210432 + 1996624640,
-        "512/256/16/3": 4398675200 + 1993935104, "512/256/32/3": 5485574912 + 1997230848,
-        "256/256/16/3": 4534666240 + 1994084864, "256/256/32/3": 5951836416 + 1997604864,
-        "128/256/16/3": 4497827072 + 1993752320, "128/256/32/3": 5884580096 + 1997792768,
-        "64/256/16/3": 4232500480 + 1991888640, "64/256/32/3": 5848513792 + 1997879552,
+        "1024/256/16/3": 4261060608 + 1992762624, "1024/256/32/3": 5484440064 + 1995351040,
+        "512/256/16/3": 4205401856 + 1994239488, "512/256/32/3": 5621430528 + 1996966400,
+        "256/256/16/3": 4051643136 + 1992036096, "256/256/32/3": 5825911808 + 1997519616,
+        "128/256/16/3": 4200972544 + 1992885760, "128/256/32/3": 5853423104 + 1998317056,
+        "64/256/16/3": 4127108096 + 1992782592, "64/256/32/3": 5865171456 + 1996628480,
     }},
 }
 
