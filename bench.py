@@ -820,33 +820,32 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     # copy rate; L2 flushed before each timed copy (the shards fit in L2 otherwise) by READING a
     # buffer of twice its size: a flush that writes leaves up to 129 MB of dirty lines whose
     # write-back then lands inside the timed copy
-    ag_calls = [cl for cl in calls if cl["op"] == "ag"]
-    if ag_calls:
-        cl = ag_calls[0]
-        wl = cl["wl"]
-        hbm = peaks()["hbm_gbs"]
-        gathered = torch.empty((wl.m, wl.k), dtype=torch.bfloat16, device=dev)
+    hbm = peaks()["hbm_gbs"]
+
+    def copy_path(shards, name, tuned_cr):
+        w = len(shards)
+        m, k = sum(t.shape[0] for t in shards), shards[0].shape[1]
+        gathered = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
         flush = torch.zeros(2 * L2_BYTES // 8, dtype=torch.int64, device=dev)
-        nbytes = wl.m * wl.k * 2
+        nbytes = m * k * 2
         res = {}
-        tuned_cr = int(cl["args"].chunk_rows)
 
         def point(t):
             return {"ms": t, "gbs": 2 * nbytes / (t * 1e-3) / 1e9,
                     "frac": 2 * nbytes / (t * 1e-3) / 1e9 / hbm}
         for be in ("copy_engine", "tma", "ldst"):
             pts = {}
-            for cr in sorted({tuned_cr, 512, 1024, wl.m // wl.world_size}):
-                ga = dt.make_args(wl.world_size, wl.m, 8, wl.k, chunk_rows=cr, backend=be)
+            for cr in sorted({tuned_cr, 512, 1024, m // w}):
+                ga = dt.make_args(w, m, 8, k, chunk_rows=cr, backend=be)
                 gws = torch.zeros(dt.workspace_size(ga, dt.OP_AG), dtype=torch.uint8, device=dev)
-                dt.allgather(cl["shards"], gathered, gws, ga)
+                dt.allgather(shards, gathered, gws, ga)
                 times = []
                 for _ in range(k_side):
                     torch.amax(flush)  # reads 258 MiB: evicts the shards, leaves clean lines
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
-                    dt.allgather(cl["shards"], gathered, gws, ga)
+                    dt.allgather(shards, gathered, gws, ga)
                     e1.record(stream)
                     torch.cuda.synchronize(dev)
                     times.append(e0.elapsed_time(e1))
@@ -857,18 +856,30 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
             best = min(pts, key=pts.get)
             res[be] = dict(point(pts[tuned_cr]), chunk_rows=tuned_cr,
                            best=dict(point(pts[best]), chunk_rows=best))
-        if not torch.equal(gathered.view(torch.int16),
-                           torch.cat(cl["shards"], dim=0).view(torch.int16)):
+        if not torch.equal(gathered.view(torch.int16), torch.cat(shards, dim=0).view(torch.int16)):
             raise RuntimeError("AllGather result differs from the shards")
         del gathered, flush
-        out["copy_path"] = {
-            "what": f"AllGather alone of {wl.name}'s {wl.world_size} shards "
-                    f"({nbytes / 2**20:.0f} MiB) at the fused call's chunk rows and, under "
-                    "`best`, at the fastest of 512, 1024 and one chunk per rank; L2 flushed "
-                    "before each copy by reading a 258 MiB buffer; gbs = 2 x bytes / time "
-                    "(read + write)",
+        return {
+            "what": f"AllGather alone of {name}'s {w} shards ({nbytes / 2**20:.0f} MiB) at the "
+                    "fused call's chunk rows and, under `best`, at the fastest of 512, 1024 and "
+                    "one chunk per rank; L2 flushed before each copy by reading a 258 MiB "
+                    "buffer; gbs = 2 x bytes / time (read + write)",
             "unit": "GB/s", "peak": hbm, "peak_source": "measured HBM copy" if
             peaks()["source"] == "measured" else "fallback", "backends": res}
+
+    ag_calls = [cl for cl in calls if cl["op"] == "ag"]
+    if ag_calls:
+        cl = ag_calls[0]
+        out["copy_path"] = copy_path(cl["shards"], cl["wl"].name, int(cl["args"].chunk_rows))
+        # the same on the largest AllGather's shards (the chunk sweep's workload, 256 MiB):
+        # the copy does not depend on the values, so they are drawn on the device
+        big = WORKLOADS["ag_w8_m16384_n8192_k8192"]
+        if big.name != cl["wl"].name:
+            g = torch.Generator(device=dev).manual_seed(big.seed)
+            shards = [torch.randn((big.m // big.world_size, big.k), generator=g, device=dev)
+                      .to(torch.bfloat16) for _ in range(big.world_size)]
+            out["copy_path_largest_ag"] = copy_path(shards, big.name, 2048)
+            del shards
 
     # context: non-overlapped gather + cuBLAS (AG); cuBLAS partial products + sum (RS)
     def cublas_step():

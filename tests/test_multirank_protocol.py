@@ -20,6 +20,10 @@ tensor cores.  What the test checks is the protocol:
   for that source and increments the destination's counter; a destination reduces a unit
   when its counter reaches the oracle's expected arrivals, always in source order
   q = 0..W-1 whatever order the pushes arrived in.
+* AllToAll: each rank pushes column block h of its tiles to rank h in its scatter order and
+  counts every stored tile on the chunk (h, q, j) it touches; the chunk's last tile releases its
+  flag (the oracle's expected counts), and rank h reads out_h once every flag is up; out_h
+  equals the oracle exactly.
 * A lost chunk (a flag never released) ends the consumer's bounded wait with an error on the
   host, and the ranks leave the test between steps.
 """
@@ -315,3 +319,83 @@ def test_reducescatter_push_protocol_two_ranks():
         assert ((s + 1) % W, 0) in sent[0]
         assert s in {d for d, _ in sent[-1]}
         assert all(any(d == (s + 1) % W for d, _ in units) for units in sent[:1])
+
+
+# ------------------------------------------------------------------------------ AllToAll
+
+A2A_MS, A2A_NW, A2A_K, A2A_CR = 150, 264, 40, 64   # rows per rank, columns per destination
+
+
+def _a2a_inputs():
+    rng = np.random.Generator(np.random.PCG64(33))
+    a = [rng.integers(-3, 4, (A2A_MS, A2A_K)).astype(np.float64) for _ in range(W)]
+    b = [rng.integers(-3, 4, (A2A_K, W * A2A_NW)).astype(np.float64) for _ in range(W)]
+    return a, b
+
+
+def _a2a_worker(rank, port, out):
+    """Rank `rank` pushes column block h of its own tiles to rank h, in its scatter order, and
+    counts each stored tile on the chunk (h, q, j) its rows touch; the chunk's last tile
+    releases the chunk's flag on rank h.  Rank h waits for every chunk's flag, then reads its
+    out_h."""
+    from oracle import plan as oplan
+    store = _store(rank, port)
+    dist.init_process_group("gloo", store=store, rank=rank, world_size=W)
+    dt = _lib()
+    a, b = _a2a_inputs()
+    n = W * A2A_NW
+    args = dt.make_args(W, W * A2A_MS, n, A2A_K, chunk_rows=A2A_CR, tile_m=BM)
+    full = dt.swizzle_plan(args, dt.OP_A2A).tolist()
+    nw, nc, tm, tnw = oplan.a2a_geometry(W, A2A_MS, n, A2A_CR, BM, BN)
+    tn = W * tnw
+    mine = [t for t in full if t // (tm * tn) == rank]
+    expected = oplan.a2a_expected_counts(W, A2A_MS, n, A2A_CR, BM, BN)
+    sent = []
+    for tid in mine:
+        q, rem = divmod(tid, tm * tn)
+        i, c_all = divmod(rem, tn)
+        h, c = divmod(c_all, tnw)
+        r0, r1 = i * BM, min((i + 1) * BM, A2A_MS)
+        c0, c1 = h * nw + c * BN, min(h * nw + (c + 1) * BN, (h + 1) * nw)
+        y = a[q][r0:r1] @ b[q][:, c0:c1]
+        # push: the tile's rows into out_h, rows q * Ms + r, columns c0 - h * Nw ..
+        store.set(f"a2a/out/{h}/{q}/{i}/{c}", y.tobytes())
+        for j in range(r0 // A2A_CR, (r1 - 1) // A2A_CR + 1):
+            done = store.add(f"a2a/cnt/{h}/{q}/{j}", 1)
+            if done == expected[(h, q, j)]:
+                store.set(f"a2a/flag/{h}/{q}/{j}", b"1")   # release: chunk (h, q, j) complete
+        sent.append(h)
+    # the consumer side: rank h's out_h, once every source's chunks are flagged
+    res = np.full((W * A2A_MS, nw), np.nan)
+    for q in range(W):
+        for j in range(nc):
+            store.wait([f"a2a/flag/{rank}/{q}/{j}"], WAIT)
+        for i in range(tm):
+            for c in range(tnw):
+                r0, r1 = i * BM, min((i + 1) * BM, A2A_MS)
+                c0, c1 = c * BN, min((c + 1) * BN, nw)
+                raw = store.get(f"a2a/out/{rank}/{q}/{i}/{c}")
+                res[q * A2A_MS + r0:q * A2A_MS + r1, c0:c1] = \
+                    np.frombuffer(raw).reshape(r1 - r0, c1 - c0)
+    dist.barrier()
+    out[rank] = (res.tobytes(), sent)
+    dist.destroy_process_group()
+
+
+def test_alltoall_push_protocol_two_ranks():
+    from oracle import plan as oplan
+    from oracle import reference
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_a2a_worker, args=(port, out), nprocs=W, join=True)
+        res = dict(out)
+    a, b = _a2a_inputs()
+    ref = reference.gemm_a2a(a, b)
+    for h in range(W):
+        got_bytes, sent = res[h]
+        got = np.frombuffer(got_bytes).reshape(W * A2A_MS, A2A_NW)
+        assert np.array_equal(got, ref[h])                       # exact: integer inputs
+        # rank h sends to h+1 first and keeps its own block for last
+        assert sent[0] == (h + 1) % W and sent[-1] == h
+        assert sent == sorted(sent, key=lambda d: oplan.rs_dpos(h, d, W))
