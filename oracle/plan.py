@@ -29,6 +29,11 @@ Tn = ceil(N/BN); group width G (default 8).
   over the chunks that m-tile i reads.  Tiles (i, n) are sorted by
   (key(i), band(i), n, i), band(i) = (rank of i among the m-tiles that share its
   key, in ascending i) // G.  Chunks are transferred in ascending pos.
+* AllGather column bands (col_band tiles wide; one band = all Tn when B fits the cache): the
+  bands run one after another and each repeats the gather order over every chunk: sort by
+  (n // col_band, key(i), band(i), n, i).  Only one band of B is in use at a time, so a wide B
+  is not re-streamed from DRAM once per key group; the first band still follows the chunks'
+  arrival, the later ones find every chunk landed.
 * AllGather, swizzle off: tile order i-major (i * Tn + n); transfer order
   ascending (s, j); pos(s, j) = s * nC + j.
 * ReduceScatter, swizzle on: source rank q sends to s in the order
@@ -134,17 +139,24 @@ def ag_keys(world_size, rank, m, chunk_rows, bm, swizzle=True):
             for i in range(tm)}
 
 
-def ag_order(world_size, rank, m, n, chunk_rows, bm, bn, swizzle=True, group=8):
-    """Tile ids (i * Tn + n) of the AllGather-GEMM in execution order."""
+def ag_order(world_size, rank, m, n, chunk_rows, bm, bn, swizzle=True, group=8, col_band=None):
+    """Tile ids (i * Tn + n) of the AllGather-GEMM in execution order.
+
+    col_band: column tiles per column band (None: all Tn, one band).  The bands run one after
+    another and each repeats the gather order over every chunk: sort by
+    (n // col_band, key, band, n, i)."""
     _, _, tm, tn = geometry(world_size, m, n, chunk_rows, bm, bn)
     if tm == 0 or tn == 0:
         return []
     if not swizzle:
         return [i * tn + c for i in range(tm) for c in range(tn)]
+    nb = tn if col_band is None else col_band
+    if nb < 1:
+        raise ValueError("col_band must be >= 1")
     keys = ag_keys(world_size, rank, m, chunk_rows, bm, True)
     band = _bands(keys, group)
-    entries = sorted((keys[i], band[i], c, i) for i in range(tm) for c in range(tn))
-    return [i * tn + c for (_, _, c, i) in entries]
+    entries = sorted((c // nb, keys[i], band[i], c, i) for i in range(tm) for c in range(tn))
+    return [i * tn + c for (_, _, _, c, i) in entries]
 
 
 def rs_dpos(q, s, world_size):

@@ -48,6 +48,32 @@ def test_golden_nonperfect_tiling():
             assert plan.rs_order(2, 6, 1, 3, 2, 1) == order
 
 
+def test_golden_ag_column_bands():
+    for head, order in _read_golden("ag_column_bands.txt"):
+        r, ms, cr, tn, g, nb = (int(x) for x in head[1:])
+        assert plan.ag_order(2, r, 2 * ms, tn, cr, 1, 1, group=g, col_band=nb) == order, head[0]
+
+
+@pytest.mark.parametrize("w,r,m,n,cr,bm,bn", [(2, 1, 512, 2048, 128, 128, 256),
+                                              (3, 2, 390, 520, 50, 128, 96),
+                                              (8, 3, 8192, 3584, 1024, 256, 256),
+                                              (5, 0, 35, 17, 3, 4, 1)])
+@pytest.mark.parametrize("nb", [1, 2, 3, 7, 1000])
+def test_ag_column_bands_keep_the_gather_order_inside_each_band(w, r, m, n, cr, bm, bn, nb):
+    """AllGather column bands: a bijection; the bands come one after another; inside a band the
+    order is the band-less order restricted to it (so every band follows the chunks' arrival)."""
+    _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
+    o = plan.ag_order(w, r, m, n, cr, bm, bn, col_band=nb)
+    assert sorted(o) == list(range(tm * tn))
+    bands = [(t % tn) // nb for t in o]
+    assert bands == sorted(bands)
+    base = plan.ag_order(w, r, m, n, cr, bm, bn)
+    for b in set(bands):
+        assert [t for t in o if (t % tn) // nb == b] == [t for t in base if (t % tn) // nb == b]
+    if nb >= tn:
+        assert o == base
+
+
 def test_golden_column_bands():
     for head, order in _read_golden("rs_column_bands.txt"):
         ms, cr, tn, g, nb = (int(x) for x in head[1:])
@@ -265,11 +291,11 @@ def test_chunk_map_covers_rows_once():
 _ORIG_AG_ORDER = plan.ag_order
 
 
-def _mut_ag_order_negative_offset(w, r, m, n, cr, bm, bn, swizzle=True, group=8):
-    return _ORIG_AG_ORDER(w, (-r) % w, m, n, cr, bm, bn, swizzle, group)
+def _mut_ag_order_negative_offset(w, r, m, n, cr, bm, bn, swizzle=True, group=8, col_band=None):
+    return _ORIG_AG_ORDER(w, (-r) % w, m, n, cr, bm, bn, swizzle, group, col_band)
 
 
-def _mut_ag_order_min_key(w, r, m, n, cr, bm, bn, swizzle=True, group=8):
+def _mut_ag_order_min_key(w, r, m, n, cr, bm, bn, swizzle=True, group=8, col_band=None):
     _, _, tm, tn = plan.geometry(w, m, n, cr, bm, bn)
     ms = m // w
     nc = plan.cdiv(ms, cr)
@@ -310,6 +336,11 @@ def _mut_rs_order_own_first(w, m, n, cr, bm, bn, swizzle=True, group=8, col_band
     return [(q * tm + i) * tn + c for (q, _, c, i) in ent]
 
 
+def _mut_ag_order_bands_ignored(w, r, m, n, cr, bm, bn, swizzle=True, group=8, col_band=None):
+    """AllGather column bands ignored."""
+    return _ORIG_AG_ORDER(w, r, m, n, cr, bm, bn, swizzle, group)
+
+
 def _mut_rs_order_bands_ignored(w, m, n, cr, bm, bn, swizzle=True, group=8, col_band=None):
     """Column bands ignored: the band-less order."""
     return _ORIG_RS_ORDER(w, m, n, cr, bm, bn, swizzle, group)
@@ -335,12 +366,13 @@ def _mut_rs_order_band_inside_key(w, m, n, cr, bm, bn, swizzle=True, group=8, co
                                          ("rs_order", _mut_rs_order_ranks_interleaved),
                                          ("rs_order", _mut_rs_order_own_first),
                                          ("rs_order", _mut_rs_order_bands_ignored),
+                                         ("ag_order", _mut_ag_order_bands_ignored),
                                          ("rs_order", _mut_rs_order_band_inside_key)])
 def test_plan_pins_catch_planted_mistakes(name, mutant, monkeypatch):
     monkeypatch.setattr(plan, name, mutant)
     caught = False
     for fn in (test_golden_rank_offset_orders, test_golden_nonperfect_tiling,
-               test_golden_column_bands):
+               test_golden_column_bands, test_golden_ag_column_bands):
         try:
             fn()
         except AssertionError:
