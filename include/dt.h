@@ -117,12 +117,12 @@ typedef struct dt_args {
                           chunks (dedicated SMs); 0 = transfer warps inside every compute CTA
                           (co-located).  AutoOverlap page section 5.3, lowerings 2-5.        */
   int32_t act;         /* AG only: dt_act applied to the fp32 result before it is stored     */
-  int32_t col_band;    /* ReduceScatter / AllReduce tile order: column tiles per column band
-                          (rank q's pass takes the bands one after another, each repeating
-                          the scatter order over every destination); 0 = automatic: one band
-                          when B_q (K x N bf16) fits in 32 MiB, else the fewest equal bands
-                          whose share of B_q does; >= Tn: one band.  AllGather / AllToAll:
-                          unused                                                          */
+  int32_t col_band;    /* AllGather, ReduceScatter / AllReduce tile order: column tiles per
+                          column band (the bands run one after another, each repeating the
+                          gather order over every chunk, or rank q's scatter order over every
+                          destination); 0 = automatic: one band when B (K x N bf16) fits in
+                          32 MiB, else the fewest equal bands whose share of B does; >= Tn:
+                          one band.  AllToAll: unused                                       */
 } dt_args;
 
 typedef enum { DT_ACT_NONE = 0, DT_ACT_GELU_TANH = 1, DT_ACT_SILU = 2 } dt_act;
@@ -298,7 +298,7 @@ dt_status dt_gemm_a2a_kernel_overlap(const void* const* a, const void* const* b,
 
 /* Tiles of the execution order of `op` for `a` (-1 if `a` is invalid), the rows of one
  * tile (128 or 256, tile_m resolved), and the column tiles per column band of the
- * ReduceScatter / AllReduce order (col_band resolved; the tile count Tn for other ops). */
+ * AllGather / ReduceScatter / AllReduce order (col_band resolved; Tn for the AllToAll). */
 int64_t dt_tile_count(const dt_args* a, int op);
 int32_t dt_tile_rows(const dt_args* a, int op);
 int32_t dt_col_band(const dt_args* a, int op);
@@ -375,8 +375,9 @@ size_t dt_sizeof_tune_point(void);
  * communication and the tile order, all by measuring the generated variants).
  * AllGather-GEMM candidates: chunk rows {64 .. 4096, M/W} x {copy engine (when the chunk count
  * stays <= 512), TMA and ld/st with co-located transfer warps, TMA and ld/st on 8 or 16
- * dedicated CTAs, the per-tile pull DT_XFER_TMA_TILE when (M/W) % 128 == 0}; then group widths
- * {4, 8, 16} at the best point.  Scatter-mode candidates
+ * dedicated CTAs, the per-tile pull DT_XFER_TMA_TILE when (M/W) % 128 == 0} x column bands
+ * {as given, one band} when the given (or automatic) bands are more than one; then group
+ * widths {4, 8, 16} at the best point.  Scatter-mode candidates
  * (dt_tune_reduce with op DT_OP_GEMM_RS, DT_OP_GEMM_AR or DT_OP_GEMM_A2A): chunk rows x group
  * widths {4, 8, 16}, at the tile rows given, and for DT_OP_GEMM_RS / DT_OP_GEMM_AR x column
  * bands {as given, one band} when the given (or automatic) bands are more than one.  A

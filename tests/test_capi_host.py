@@ -152,6 +152,10 @@ def test_host_plan_matches_oracle_rs(dt, case, swizzle, bm):
 @pytest.mark.parametrize("bm", TILE_M)
 def test_host_plan_matches_oracle_rs_column_bands(dt, case, nb, bm):
     w, m, n, cr = case
+    for r in sorted({0, w - 1}):
+        a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr, tile_m=bm, col_band=nb)
+        assert dt.swizzle_plan(a, dt.OP_AG).tolist() == oplan.ag_order(w, r, m, n, cr, bm, 256,
+                                                                       col_band=nb), (case, r)
     for op in (dt.OP_RS, dt.OP_AR):
         a = dt.make_args(w, m, n, 8, chunk_rows=cr, tile_m=bm, col_band=nb)
         tn = -(-n // 256)
@@ -171,9 +175,12 @@ def test_automatic_column_bands(dt, w, m, n, k, want):
     a = dt.make_args(w, m, n, k, chunk_rows=128)
     assert dt.col_band(a, dt.OP_RS) == want
     assert dt.col_band(a, dt.OP_AR) == want
-    assert dt.col_band(a, dt.OP_AG) == -(-n // 256)   # other ops: one band
+    assert dt.col_band(a, dt.OP_AG) == want   # the AllGather's B is K x N as well
     bm = dt.tile_rows(a, dt.OP_RS)
     assert dt.swizzle_plan(a, dt.OP_RS).tolist() == oplan.rs_order(w, m, n, 128, bm, 256,
+                                                                   col_band=want)
+    bm = dt.tile_rows(a, dt.OP_AG)
+    assert dt.swizzle_plan(a, dt.OP_AG).tolist() == oplan.ag_order(w, 0, m, n, 128, bm, 256,
                                                                    col_band=want)
 
 

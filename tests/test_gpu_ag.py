@@ -71,6 +71,10 @@ def test_small_bit_identical_across_variants(dt, small):
                     c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=cr, backend=backend,
                              swizzle=swizzle, rank=1, tile_m=tile_m)
                     assert bits_equal(c, base), (tile_m, backend, swizzle, cr)
+            for nb in (1, 2):  # column bands
+                c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=64, backend=backend, rank=1,
+                         tile_m=tile_m, col_band=nb)
+                assert bits_equal(c, base), (tile_m, backend, nb)
         c = _run(dt, inp, wl.m, wl.n, wl.k, chunk_rows=128, fn=dt.ag_gemm_kernel_overlap,
                  tile_m=tile_m)
         assert bits_equal(c, base), tile_m

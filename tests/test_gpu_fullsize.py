@@ -102,7 +102,9 @@ AG_VARIANTS = ([dict(chunk_rows=c, backend=be, tile_m=256, swizzle=True)
                 for c in (256, 1024) for t in (128, 256) for s in (True, False)
                 if (t, s) != (256, True)] +
                [dict(chunk_rows=c, backend="tma_tile", tile_m=t, swizzle=True)
-                for c in (256, 2048) for t in (128, 256)])
+                for c in (256, 2048) for t in (128, 256)] +
+               [dict(chunk_rows=1024, backend=be, tile_m=256, swizzle=True, col_band=nb)
+                for be in ("tma_tile", "copy_engine") for nb in (3, 32)])
 
 
 @pytest.fixture(scope="module")
@@ -129,7 +131,8 @@ def ag_full(dt):
 
 @pytest.mark.parametrize("variant", AG_VARIANTS,
                          ids=[f"c{v['chunk_rows']}-{v['backend']}-t{v['tile_m']}-"
-                              f"{'sw' if v['swizzle'] else 'nosw'}" for v in AG_VARIANTS])
+                              f"{'sw' if v['swizzle'] else 'nosw'}-b{v.get('col_band', 0)}"
+                              for v in AG_VARIANTS])
 def test_ag_full_size_bit_identical_across_variants(ag_full, variant):
     wl, inp, run, base = ag_full
     assert bits_equal(run(**variant), base), variant

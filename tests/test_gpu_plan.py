@@ -38,6 +38,13 @@ def test_device_plan_matches_oracle(dt, case, swizzle, bm):
         buf.fill_(-1)
         dt.swizzle_plan_device(a, dt.OP_RS, buf)
         assert buf.cpu().tolist() == oplan.rs_order(w, m, n, cr, bm, 256, swizzle, col_band=nb)
+        r = w - 1
+        a = dt.make_args(w, m, n, 8, rank=r, chunk_rows=cr, swizzle=swizzle, tile_m=bm,
+                         col_band=nb)
+        t = dt.tile_count(a, dt.OP_AG)
+        abuf = torch.full((t,), -1, dtype=torch.int32, device="cuda")
+        dt.swizzle_plan_device(a, dt.OP_AG, abuf)
+        assert abuf.cpu().tolist() == oplan.ag_order(w, r, m, n, cr, bm, 256, swizzle, col_band=nb)
     if n % (8 * w) == 0:  # the AllToAll over the same rows, each rank's M/W of them
         a = dt.make_args(w, m, n, 8, chunk_rows=cr, swizzle=swizzle, tile_m=bm)
         t = dt.tile_count(a, dt.OP_A2A)

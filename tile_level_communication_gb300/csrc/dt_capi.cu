@@ -253,9 +253,9 @@ dt_status derive(const dt_args* a, int op, Derived* d) {
   d->geom = a2a ? make_geom_a2a(d->W, d->M, d->N, d->Cr, d->bm, kBN, d->G, d->swizzle ? 1 : 0)
               : make_geom(d->W, d->rank, d->M, d->N, d->Cr, d->bm, kBN, d->G, d->swizzle ? 1 : 0);
   if (a->col_band < 0) return fail(DT_ERR_INVALID, "col_band must be >= 0");
-  if (op == DT_OP_GEMM_RS || op == DT_OP_GEMM_AR) {
-    // column bands: one band of B_q (K x band columns, bf16) within kBandBytes, so that it
-    // stays in L2 while the pass visits every destination
+  if (op != DT_OP_GEMM_A2A) {
+    // column bands: one band of B (K x band columns, bf16) within kBandBytes, so that it stays
+    // in L2 while the order visits every destination (ReduceScatter) or chunk (AllGather)
     const int32_t tn = d->geom.Tn;
     int32_t nb = a->col_band;
     if (nb == 0) {
@@ -1633,6 +1633,9 @@ dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, v
   DevCtx* dev = nullptr;
   if ((s = dev_ctx(&dev)) != DT_OK) return s;
   auto call = [&](dt_args& cand) { return dt_ag_gemm(a_shards, b, c, ws, ws_bytes, &cand, stream); };
+  // column bands: as given, and one band when that differs
+  std::vector<int32_t> bands = {a->col_band};
+  if (d.geom.Nb < d.Tn) bands.push_back(d.Tn);
   std::vector<dt_args> cands;
   for (int64_t cr : chunk_candidates(d.Ms)) {
     const int64_t nchunks = d.W * cdiv64(d.Ms, cr);
@@ -1646,13 +1649,16 @@ dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, v
       }
     if (d.Ms % kBM == 0) vs.push_back({DT_XFER_TMA_TILE, 0});  // per-tile pull, co-located
     for (const V& v : vs) {
-      dt_args cand = *a;
-      cand.chunk_rows = cr;
-      cand.backend = v.be;
-      cand.copy_ctas = v.copy;
-      cand.swizzle = 1;
-      cand.group = a->group > 0 ? a->group : 8;
-      cands.push_back(cand);
+      for (int32_t nb : bands) {
+        dt_args cand = *a;
+        cand.chunk_rows = cr;
+        cand.backend = v.be;
+        cand.copy_ctas = v.copy;
+        cand.swizzle = 1;
+        cand.group = a->group > 0 ? a->group : 8;
+        cand.col_band = nb;
+        cands.push_back(cand);
+      }
     }
   }
   std::vector<dt_tune_point> pts = tune_all(t, cands, DT_OP_AG_GEMM, call);
@@ -1668,6 +1674,7 @@ dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, v
       cand.chunk_rows = base.chunk_rows;
       cand.backend = base.backend;
       cand.copy_ctas = base.copy_ctas;
+      cand.col_band = base.col_band;
       cand.swizzle = 1;
       cand.group = g;
       gc.push_back(cand);

@@ -14,7 +14,8 @@
 // Definition (the same one the oracle sorts by):
 //   chunk (s, j) = rows [s*Ms + j*Cr, s*Ms + min((j+1)*Cr, Ms)),  nC = ceil(Ms / Cr)
 //   AG: pos(s, j) = ((s - r) mod W) * nC + j;  key(i) = max pos of the chunks m-tile i reads;
-//       order = sort (i, n) by (key(i), band(i), n, i)
+//       order = sort (i, n) by (n / Nb, key(i), band(i), n, i): column bands of Nb tiles one
+//       after another, each repeating the gather order (Nb = Tn: one band)
 //   RS: dpos_q(s) = (s - q - 1) mod W;  key(q, i) = min over written chunks of dpos*nC + j;
 //       order = sort (q, i, n) by (q, n / Nb, key, band, n, i): the virtual source ranks one
 //       after another, each in its own scatter order, so every destination receives its
@@ -47,7 +48,7 @@ struct Geom {
   int32_t W, rank, BM, BN, nC, Tm, Tn, G, swizzle;
   int64_t Nw;   // AllToAll: columns per destination (N / W); 0 otherwise
   int32_t Tnw;  // AllToAll: column tiles per destination; 0 otherwise
-  int32_t Nb;   // ReduceScatter: column tiles per column band (Tn: one band)
+  int32_t Nb;   // AllGather / ReduceScatter: column tiles per column band (Tn: one band)
 };
 
 DT_HD int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -132,7 +133,8 @@ DT_HD int32_t ag_count_below(const Geom& g, int32_t rot0, int32_t k) {
   }
   return lo;
 }
-// execution position of AllGather tile (i, n)
+// execution position of AllGather tile (i, n): the full column bands before n's (Tm*Nb each),
+// then n's band (nbw columns wide) laid out like a band-less order over those columns
 DT_HD int64_t ag_position(const Geom& g, int32_t i, int32_t n) {
   if (!g.swizzle) return static_cast<int64_t>(i) * g.Tn + n;
   const int32_t rot0 = ag_rot0(g);
@@ -140,7 +142,10 @@ DT_HD int64_t ag_position(const Geom& g, int32_t i, int32_t n) {
   const int32_t k = ag_key(g, rot0, u);
   const int32_t ug = ag_count_below(g, rot0, k);
   const int32_t ue = ag_count_below(g, rot0, k + 1);
-  return static_cast<int64_t>(ug) * g.Tn + band_offset(ug, ue, u, n, g.Tn, g.G);
+  const int32_t b = n / g.Nb;
+  const int32_t nbw = min32(g.Nb, g.Tn - b * g.Nb);
+  return static_cast<int64_t>(b) * g.Tm * g.Nb + static_cast<int64_t>(ug) * nbw +
+         band_offset(ug, ue, u, n - b * g.Nb, nbw, g.G);
 }
 // chunk moved at transfer step tc (own rank first, then r+1, r+2, ...)
 DT_HD void ag_transfer_chunk(const Geom& g, int32_t tc, int32_t& s, int32_t& j) {
