@@ -1577,8 +1577,10 @@ void drop_same_order(std::vector<dt_args>& cands, int op) {
 }
 
 // Pick the point to keep and copy its knobs into *a: among the points within kTuneTie of the
-// fastest, the one that moves the fewest DRAM bytes: automatic column bands before one band,
-// then the largest chunk rows, then the fastest.  The tuner times short bursts at full clock;
+// fastest, the one that moves the fewest DRAM bytes: for the reduce ops automatic column bands
+// before one band, then the largest chunk rows, then the fastest; for the AllGather the
+// largest chunk rows, then the fastest (its column bands move more bytes at some chunk sizes
+// and fewer at others: measured, not ranked).  The tuner times short bursts at full clock;
 // run for seconds under the power cap, a kernel's clock follows its energy.  Fewer, larger
 // chunks mean fewer key groups in the order, each of which re-streams B from DRAM (the largest
 // AllGather with the per-tile pull, 3 s runs: chunk 2048 / 1024 / 256 read 2.52 / 3.06 / 4.28
@@ -1588,7 +1590,7 @@ void drop_same_order(std::vector<dt_args>& cands, int op) {
 // runs 3-5 % faster over 200 calls).
 constexpr float kTuneTie = 1.01f;
 dt_status tune_finish(std::vector<dt_tune_point>& pts, dt_args* a, dt_tune_point* out,
-                      int32_t max_points, int32_t* n_points) {
+                      int32_t max_points, int32_t* n_points, bool bands_first) {
   int fastest = -1;
   for (int i = 0; i < static_cast<int>(pts.size()); ++i)
     if (pts[i].status == DT_OK && pts[i].ms >= 0 && (fastest < 0 || pts[i].ms < pts[fastest].ms))
@@ -1596,7 +1598,7 @@ dt_status tune_finish(std::vector<dt_tune_point>& pts, dt_args* a, dt_tune_point
   int best = fastest;
   auto fewer_bytes = [&](const dt_tune_point& x, const dt_tune_point& y) {
     const bool xa = x.col_band == 0, ya = y.col_band == 0;  // automatic bands
-    if (xa != ya) return xa;
+    if (bands_first && xa != ya) return xa;
     if (x.chunk_rows != y.chunk_rows) return x.chunk_rows > y.chunk_rows;
     return x.ms < y.ms;
   };
@@ -1684,7 +1686,7 @@ dt_status dt_tune_ag_gemm(const void* const* a_shards, const void* b, void* c, v
     if (gc.size() > 1)
       for (const dt_tune_point& pt : tune_all(t, gc, DT_OP_AG_GEMM, call)) pts.push_back(pt);
   }
-  return tune_finish(pts, a, points, max_points, n_points);
+  return tune_finish(pts, a, points, max_points, n_points, false);
 }
 
 dt_status dt_tune_reduce(int op, const void* const* a_, const void* const* b_, void* const* out,
@@ -1720,7 +1722,7 @@ dt_status dt_tune_reduce(int op, const void* const* a_, const void* const* b_, v
   }
   drop_same_order(cands, op);
   std::vector<dt_tune_point> pts = tune_all(t, cands, op, call);
-  return tune_finish(pts, a, points, max_points, n_points);
+  return tune_finish(pts, a, points, max_points, n_points, true);
 }
 
 dt_status dt_ffn_ag_rs(const void* const* x_shards, const void* w1, const void* const* w2,
