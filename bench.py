@@ -43,14 +43,14 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch after two
     # warm-up launches, 256-row tiles; keys "chunk_rows/tile_rows/col_band/l2_hints" (the
     # group width gives the same order at these chunk sizes: a key holds at most 4 m-tiles)
-    "rs_w8_m8192_n8192_k3584": {"csrc": "f6095990e63b13d1",
+    "rs_w8_m8192_n8192_k3584": {"csrc": "5bcd8666a2ae1e81",
                                 "profile": "profiles/fused_gemm_rs_w8_m8192_n8192_k3584.md",
                                 "points": {
-        "1024/256/16/3": 4261060608 + 1992762624, "1024/256/32/3": 5484440064 + 1995351040,
-        "512/256/16/3": 4205401856 + 1994239488, "512/256/32/3": 5621430528 + 1996966400,
-        "256/256/16/3": 4051643136 + 1992036096, "256/256/32/3": 5825911808 + 1997519616,
-        "128/256/16/3": 4200972544 + 1992885760, "128/256/32/3": 5853423104 + 1998317056,
-        "64/256/16/3": 4127108096 + 1992782592, "64/256/32/3": 5865171456 + 1996628480,
+        "1024/256/16/3": 4250193920 + 1993266944, "1024/256/32/3": 5610113280 + 1996678144,
+        "512/256/16/3": 4052715776 + 1990631168, "512/256/32/3": 5622775552 + 1997062144,
+        "256/256/16/3": 4088491264 + 1992518144, "256/256/32/3": 5878787840 + 1997745664,
+        "128/256/16/3": 4011194112 + 1990395904, "128/256/32/3": 5841342464 + 1997944576,
+        "64/256/16/3": 3986237696 + 1989184256, "64/256/32/3": 5928660224 + 1997003008,
     }},
 }
 
