@@ -28,6 +28,10 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+# one hardware work queue per stream (the default of 8 is shared out round robin, and a copy
+# stream that shares a queue with the compute stream waits behind its kernels); read when the
+# CUDA context is created, so set before any CUDA call
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
 
 import numpy as np  # noqa: E402
 
@@ -501,6 +505,61 @@ def run_allgather_only(args):
 
 
 # ----------------------------------------------------------------------------- fused arm
+class Arena:
+    """One flat device buffer handing out consecutive 256-byte-aligned bf16 tensors: the
+    step's inputs (or outputs) then cross the host link as one copy."""
+    ALIGN = 256
+
+    def __init__(self, capacity, dev):
+        import torch
+        self.buf = torch.empty(capacity, dtype=torch.uint8, device=dev)
+        self.used = 0
+
+    def take(self, shape):
+        import torch
+        n = int(np.prod(shape)) * 2
+        if self.used + n > self.buf.numel():
+            raise RuntimeError("arena too small")
+        t = self.buf[self.used:self.used + n].view(torch.bfloat16).view(*shape)
+        self.used += -(-n // self.ALIGN) * self.ALIGN
+        return t
+
+    def put(self, bits):
+        import torch
+        t = self.take(bits.shape)
+        t.copy_(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16))
+        return t
+
+    def span(self, t):
+        """Byte range of tensor `t` (one of this arena's) inside the buffer."""
+        lo = t.data_ptr() - self.buf.data_ptr()
+        return lo, lo + t.numel() * t.element_size()
+
+    @staticmethod
+    def capacity(arrays):
+        return sum(-(-a.nbytes // Arena.ALIGN) * Arena.ALIGN for a in arrays)
+
+
+def _input_arrays(inp):
+    """Every array a workload's inputs hold (an upper bound on what the step uploads)."""
+    out = []
+    for v in vars(inp).values():
+        if isinstance(v, np.ndarray):
+            out.append(v)
+        elif isinstance(v, (list, tuple)):
+            out.extend(x for x in v if isinstance(x, np.ndarray))
+    return out
+
+
+def _output_bytes(wl):
+    """Bytes of a step's outputs for one workload, padded per output tensor."""
+    w = wl.world_size
+    pad = Arena.ALIGN * (w + 1)
+    if wl.op == "ar":
+        return w * wl.m * wl.n * 2 + pad
+    return wl.m * wl.n * 2 + pad  # ag: C; rs: the W row blocks; a2a: the W column blocks; ffn: out_s
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -521,15 +580,19 @@ def main():
     ops = workload_ops(args.workload)
     inputs = [wl.make() for wl in ops]
 
-    def up(bits):
-        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-
     # device-resident inputs, outputs, workspaces, argument structs
     knobs = {"tile_m": args.tile_m, "col_band": args.col_band}
     if args.group:
         knobs["group"] = args.group
+    in_capacity = sum(Arena.capacity(_input_arrays(inp)) for inp in inputs)
+    out_capacity = sum(_output_bytes(wl) for wl in ops)
+
     def build_calls():
-        """One set of device-resident inputs, outputs, workspaces and argument structs."""
+        """One set of device-resident inputs, outputs, workspaces and argument structs; the
+        inputs sit back to back in one arena and the outputs in another (`arenas`)."""
+        in_arena, out_arena = Arena(in_capacity, dev), Arena(out_capacity, dev)
+        up = in_arena.put
+        out = out_arena.take
         calls = []
         in_bytes = out_bytes = 0
         for wl, inp in zip(ops, inputs):
@@ -556,8 +619,7 @@ def main():
                 probe = dt.make_args(w, wl.m, wl.n, fr, chunk_rows=64, lda=w * fr)
                 ws_rs = torch.zeros(max(dt.workspace_size(a_rs, dt.OP_RS),
                                         dt.workspace_size(probe, dt.OP_RS)), dtype=torch.uint8, device=dev)
-                outs = [torch.empty((wl.m // w, wl.n), dtype=torch.bfloat16, device=dev)
-                        for _ in range(w)]
+                outs = [out((wl.m // w, wl.n)) for _ in range(w)]
                 calls.append(dict(op="rs", wl=rs_wl, args=a_rs, ins=w2, acts=[],
                                   A=[h[:, q * fr:(q + 1) * fr] for q in range(w)], B=w2, outs=outs,
                                   ws=ws_rs))
@@ -569,7 +631,7 @@ def main():
                                  swizzle=not args.no_swizzle, backend=args.backend, **knobs)
                 shards = [up(s) for s in inp.shards]
                 b = up(inp.b)
-                c = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device=dev)
+                c = out((wl.m, wl.n))
                 probe = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=64)
                 need = max(dt.workspace_size(a, dt.OP_AG), dt.workspace_size(probe, dt.OP_AG))
                 ws = torch.zeros(need, dtype=torch.uint8, device=dev)
@@ -581,8 +643,7 @@ def main():
                                  **knobs)
                 A = [up(x) for x in inp.a]
                 b = up(inp.b[0])  # the replicated weight, held once
-                outs = [torch.empty((wl.m, wl.n // w), dtype=torch.bfloat16, device=dev)
-                        for _ in range(w)]
+                outs = [out((wl.m, wl.n // w)) for _ in range(w)]
                 y = [torch.empty((wl.m // w, wl.n), dtype=torch.bfloat16, device=dev)
                      for _ in range(w)]  # the baseline's per-rank GEMM outputs
                 probe = dt.make_args(w, wl.m, wl.n, wl.k, chunk_rows=64)
@@ -596,8 +657,7 @@ def main():
                 A = [up(x) for x in inp.a]
                 B = [up(x) for x in inp.b]
                 rows = wl.m // wl.world_size if wl.op == "rs" else wl.m  # AllReduce: every rank all rows
-                outs = [torch.empty((rows, wl.n), dtype=torch.bfloat16, device=dev)
-                        for _ in range(wl.world_size)]
+                outs = [out((rows, wl.n)) for _ in range(wl.world_size)]
                 op_id = dt.OP_RS if wl.op == "rs" else dt.OP_AR
                 probe = dt.make_args(wl.world_size, wl.m, wl.n, wl.k, chunk_rows=64)
                 need = max(dt.workspace_size(a, op_id), dt.workspace_size(probe, op_id))
@@ -605,9 +665,9 @@ def main():
                 calls.append(dict(op=wl.op, wl=wl, args=a, ins=A + B, acts=A, A=A, B=B, outs=outs, ws=ws))
             in_bytes += sum(t.numel() * 2 for t in calls[-1]["ins"])
             out_bytes += sum(t.numel() * 2 for t in calls[-1]["outs"])
-        return calls, in_bytes, out_bytes
+        return calls, in_bytes, out_bytes, (in_arena, out_arena)
 
-    calls, in_bytes, out_bytes = build_calls()
+    calls, in_bytes, out_bytes, arenas = build_calls()
 
     def run_call(cl, fused=True):
         if cl["op"] == "ag":
@@ -758,7 +818,7 @@ def main():
     if not args.skip_extras and rank == 0:
         line["clocks"] = sampler.summary(w0, w1)
         line.update(extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_bytes,
-                           ops, inputs, value, world, pk, build_calls))
+                           ops, inputs, value, world, pk, build_calls, arenas))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
@@ -767,7 +827,7 @@ def main():
 
 
 def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_bytes, ops, inputs,
-           value, world, pk, build_calls):
+           value, world, pk, build_calls, arenas):
     out = {}
     stream = torch.cuda.current_stream(dev)
     k_side = max(3, min(args.steps, 20))
@@ -1028,61 +1088,67 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     # End to end through the public API with host buffers: every step copies its inputs in
     # from pinned host memory and its outputs out, inside the timed region.  Two device sets
     # of inputs / outputs / workspaces let step i+1's host-to-device copy and step i-1's
-    # device-to-host copy run on their own streams while step i computes.
-    sets = [calls, build_calls()[0]]
+    # device-to-host copy run on their own streams while step i computes.  Each set's inputs
+    # sit back to back in one arena and its outputs in another, so a step's inputs cross the
+    # link as one copy and its outputs as one copy (many small copies spread over several
+    # streams reached the link rate in some processes and two thirds of it in others).
+    second, _, _, arenas2 = build_calls()
+    sets = [calls, second]
+    set_arenas = [arenas, arenas2]
     for c1, c2 in zip(sets[0], sets[1]):
         c2["args"] = c1["args"]  # the tuned knobs
-    host_in = [[t.cpu().pin_memory() for t in cl["ins"]] for cl in calls]
-    host_out = [[[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in cl["outs"]]
-                 for cl in calls] for _ in range(2)]
+    in_used, out_used = arenas[0].used, arenas[1].used
+    host_in = torch.empty(in_used, dtype=torch.uint8, pin_memory=True)
+    host_in.copy_(arenas[0].buf[:in_used])
+    host_out = [torch.empty(out_used, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
     s_main = torch.cuda.current_stream(dev)
-    n_cs = 4  # copy streams per direction: the copies spread over several copy engines
-    s_h2d = [torch.cuda.Stream(dev) for _ in range(n_cs)]
-    s_d2h = [torch.cuda.Stream(dev) for _ in range(n_cs)]
-    ev_in = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(2)]
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(2)]
-    pairs_in = [[(d_, h_) for cl, hs in zip(sets[k], host_in) for d_, h_ in zip(cl["ins"], hs)]
-                for k in range(2)]
-    pairs_out = [[(d_, h_) for cl, hs in zip(sets[k], host_out[k])
-                  for d_, h_ in zip(cl["outs"], hs)] for k in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
+    def merged(spans):
+        spans = sorted(spans)
+        out_ = [list(spans[0])]
+        for lo, hi in spans[1:]:
+            if lo <= -(-out_[-1][1] // Arena.ALIGN) * Arena.ALIGN:
+                out_[-1][1] = max(out_[-1][1], hi)
+            else:
+                out_.append([lo, hi])
+        return [tuple(x) for x in out_]
+
+    ranges_all = [(0, in_used)]
     # the same with the weights resident in HBM: only the activations cross the link each step
-    pairs_act = [[(d_, h_) for cl, hs in zip(sets[k], host_in) for d_, h_ in zip(cl["ins"], hs)
-                  if any(d_ is x for x in cl["acts"])] for k in range(2)]
-    act_bytes = sum(d_.numel() * d_.element_size() for d_, _ in pairs_act[0])
+    ranges_act = merged([arenas[0].span(t) for cl in calls for t in cl["acts"]])
+    act_bytes = sum(t.numel() * t.element_size() for cl in calls for t in cl["acts"])
 
-    def e2e_steps(n, pairs_in=pairs_in):
+    def e2e_steps(n, ranges=ranges_all):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         gc.disable()  # the host enqueues only a few steps ahead: a collector pause idles the GPU
         e0.record(s_main)
-        for st in s_h2d:
-            st.wait_event(e0)
+        s_h2d.wait_event(e0)
         for i in range(n):
             k = i % 2
-            for j, st in enumerate(s_h2d):
-                if i >= 2:
-                    st.wait_event(ev_done[k])     # step i-2 has finished reading set k's inputs
-                with torch.cuda.stream(st):
-                    for d_, h_ in pairs_in[k][j::n_cs]:
-                        d_.copy_(h_, non_blocking=True)
-                    ev_in[k][j].record(st)
-                s_main.wait_event(ev_in[k][j])
-                if i >= 2:
-                    s_main.wait_event(ev_out[k][j])  # step i-2's outputs have been copied out
+            dst_in, dst_out = set_arenas[k][0].buf, set_arenas[k][1].buf
+            if i >= 2:
+                s_h2d.wait_event(ev_done[k])  # step i-2 has finished reading set k's inputs
+            with torch.cuda.stream(s_h2d):
+                for lo, hi in ranges:
+                    dst_in[lo:hi].copy_(host_in[lo:hi], non_blocking=True)
+                ev_in[k].record(s_h2d)
+            s_main.wait_event(ev_in[k])
+            if i >= 2:
+                s_main.wait_event(ev_out[k])  # step i-2's outputs have been copied out
             for cl in sets[k]:
                 run_call(cl)
             ev_done[k].record(s_main)
-            for j, st in enumerate(s_d2h):
-                st.wait_event(ev_done[k])
-                with torch.cuda.stream(st):
-                    for d_, h_ in pairs_out[k][j::n_cs]:
-                        h_.copy_(d_, non_blocking=True)
-                    ev_out[k][j].record(st)
+            s_d2h.wait_event(ev_done[k])
+            with torch.cuda.stream(s_d2h):
+                host_out[k].copy_(dst_out[:out_used], non_blocking=True)
+                ev_out[k].record(s_d2h)
         for k in range(min(n, 2)):
-            for ev in ev_out[k]:
-                s_main.wait_event(ev)
+            s_main.wait_event(ev_out[k])
         e1.record(s_main)
         torch.cuda.synchronize(dev)
         gc.enable()
@@ -1092,7 +1158,7 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     # steady state: the first step's copy-in and the last step's copy-out overlap nothing
     n_e = max(4, min(args.steps, 50))
     ms_e = e2e_steps(n_e) / n_e
-    ms_act = e2e_steps(n_e, pairs_act) / n_e
+    ms_act = e2e_steps(n_e, ranges_act) / n_e
     # The host-to-device copies of step i+1 run on the copy engines while step i computes, so an
     # AllGather whose chunks also move on the copy engines queues behind them.  Time the same
     # steps with the AllGather's chunks moved by the in-kernel TMA transfer and keep the faster.
@@ -1105,7 +1171,7 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
             cl["args"].backend = dt.BACKENDS["tma"]
         e2e_steps(2)
         ms_e_tma = e2e_steps(n_e) / n_e
-        ms_act_tma = e2e_steps(n_e, pairs_act) / n_e
+        ms_act_tma = e2e_steps(n_e, ranges_act) / n_e
         ag_be = {"as_tuned": {"ms_per_step": ms_e, "weights_resident_ms_per_step": ms_act},
                  "tma": {"ms_per_step": ms_e_tma, "weights_resident_ms_per_step": ms_act_tma}}
         if ms_e_tma < ms_e:
@@ -1125,12 +1191,10 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
             code, info = dt.check(cl["ws"])
             if code != 0:
                 raise RuntimeError(f"device error in the end-to-end run {info}")
-    # the outputs that came back are the GEMM's: spot check the last step's against the device
+    # the outputs that came back are the GEMM's: check the last step's against the device
     last = (n_e - 1) % 2
-    for cl, hs in zip(sets[last], host_out[last]):
-        for d_, h_ in zip(cl["outs"], hs):
-            if not torch.equal(d_.cpu().view(torch.int16), h_.view(torch.int16)):
-                raise RuntimeError("end-to-end outputs differ from the device's")
+    if not torch.equal(set_arenas[last][1].buf[:out_used].cpu(), host_out[last]):
+        raise RuntimeError("end-to-end outputs differ from the device's")
     # the host link's own rate, measured here: one 512 MiB pinned copy each way, best of 3; the
     # step's inputs cannot arrive faster than in_bytes at the host-to-device rate
     link_bytes = 1 << 29
@@ -1160,7 +1224,7 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     out["e2e"] = {"value": world * flops_step / (ms_e * 1e-3) / 1e12, "unit": "TFLOP/s",
                   "ms_per_step": ms_e, "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                   "pipelined": "step i+1's inputs in and step i-1's outputs out overlap step i, "
-                               f"each spread over {n_cs} copy streams",
+                               "each as one copy (inputs and outputs packed in one buffer each)",
                   "link": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
                            "floor_ms_per_step": floor_ms, "frac_of_floor": floor_ms / ms_e,
                            "note": "floor = the larger of the step's input bytes at the measured "

@@ -417,8 +417,9 @@ dt_status dt_debug_drop_transfer(int32_t step);
 /* Debug timeline of the fused AllGather-GEMM: how much of the chunk transfer the GEMM hid.
  * (DITRON page, paper section 4.1: most of the communication of a large AllGather-GEMM is
  * hidden behind the GEMM; AutoOverlap page, section 2: what kernel-level overlap leaves
- * exposed.)  While a buffer is attached, every dt_ag_gemm call resets it on its stream and its
- * kernel records, in 64-bit global-timer nanoseconds:
+ * exposed.)  While a buffer is attached, every dt_ag_gemm call (and every dt_allgather call on
+ * an in-kernel backend, whose kernel has no GEMM: words [2], [3] and [6 + 3c] stay as reset)
+ * resets it on its stream and its kernel records, in 64-bit global-timer nanoseconds:
  *   [0] first CTA start, [1] last CTA exit, [2] total time the GEMM's producers spent waiting
  *   for ready flags (summed over waits), [3] how many waits found their chunk missing;
  *   then per chunk c = s * nC + j (rank s, chunk j):

@@ -467,6 +467,9 @@ __global__ void plan_kernel(Geom g, int op, int32_t* order, int32_t T) {
 __global__ void prepare_kernel(Geom g, int op, int32_t* order, int32_t T, uint32_t* ctl,
                                int64_t ctl_words, const uint32_t* err,
                                const unsigned long long* tag, unsigned long long expected) {
+  // the fused kernel behind this grid may start launching now: it waits for this grid's
+  // completion before it reads or writes global memory
+  griddep_launch_dependents();
   if (*tag == expected && err[0] == 0u) return;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
@@ -1039,6 +1042,7 @@ dt_status dt_allgather(const void* const* a_shards, void* out, void* ws, size_t 
   uint8_t* w = reinterpret_cast<uint8_t*>(ws);
   KParams p;
   fill_common(p, d, ws, epoch);
+  if ((s = attach_trace(p, d, stream)) != DT_OK) return s;
   p.T = 0;  // no GEMM tiles: every CTA is a transfer CTA
   for (int i = 0; i < d.W; ++i) p.shard[i] = reinterpret_cast<const uint8_t*>(a_shards[i]);
   p.gather = dst;

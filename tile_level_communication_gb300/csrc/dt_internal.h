@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include "dt.h"
 #include "dt_kernel.cuh"
 
@@ -39,6 +41,17 @@ struct LaunchState {
   int max_clusters[kMaxDevices];
 };
 
+// Whether the fused kernel is launched with programmatic stream serialization, so that its
+// launch and set-up overlap the prepare kernel before it in the stream (the kernel waits for
+// that grid before it touches global memory): on unless DT_PDL=0.
+inline bool pdl_setting() {
+  static const bool v = [] {
+    const char* e = getenv("DT_PDL");
+    return e ? atoi(e) != 0 : true;
+  }();
+  return v;
+}
+
 template <int OP, int COPY, bool F32, int CL>
 cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStream_t stream) {
   auto kern = fused_gemm_kernel<OP, COPY, F32, CL>;
@@ -58,7 +71,7 @@ cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStrea
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   if (CL > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
@@ -86,6 +99,14 @@ cudaError_t launch_fused(const KParams& p, int grid, bool cooperative, cudaStrea
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+  }
+  // not with the cooperative attribute, and not while a debug timeline is attached (its reset
+  // is a memset between the prepare kernel and this one)
+  if (pdl_setting() && !(CL == 1 && cooperative) && p.trace == nullptr) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs += 1;
   }
   return cudaLaunchKernelEx(&cfg, kern, p);
 }

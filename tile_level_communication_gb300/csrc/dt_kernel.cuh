@@ -1347,7 +1347,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) trace_min(p.trace, 0);
   if (threadIdx.x < kReadyBitsWords) L.ready_bits[threadIdx.x] = 0u;
   const bool copier = static_cast<int32_t>(blockIdx.x) < p.copy_ctas;
   if (threadIdx.x == 0) {
@@ -1383,6 +1382,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   if constexpr (PAIR) cluster_sync();  // the cluster's barriers exist before any CTA signals them
   tc_fence_after();
   const uint32_t tmem_base = copier ? 0u : *L.tmem_slot;
+  // everything above touches only shared memory, TMEM and the parameter space, so it may
+  // overlap the grid before this one (launched with programmatic stream serialization after
+  // the prepare kernel); no global memory is read or written before that grid has completed
+  griddep_wait();
+  if (threadIdx.x == 0) trace_min(p.trace, 0);
 
   if (copier) {
     // dedicated transfer CTA: no GEMM; the operand ring becomes four workers' staging rings

@@ -19,6 +19,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------------------ programmatic dependent launch
+// A grid launched with programmatic stream serialization may start while the grid before it in
+// the stream still runs; griddep_wait() returns once that grid has completed and its memory
+// operations are visible (at once for a grid launched without the attribute).
+// griddep_launch_dependents() lets the next grid in the stream start launching.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
