@@ -109,6 +109,8 @@ def parse():
                     help="AllGather chunk x backend x swizzle sweep of --workload (default: the "
                          "largest AllGather); one JSON line per point")
     ap.add_argument("--sweep-chunks", default="64,128,256,512,2048")
+    ap.add_argument("--sweep-rounds", type=int, default=5,
+                    help="rounds over all sweep points (each point's median is reported)")
     ap.add_argument("--allgather-only", action="store_true",
                     help="time the AllGather's chunk transfer alone (dt_allgather) on the shards "
                          "of --workload's AllGather, per backend (or --backend), L2 flushed by "
@@ -338,7 +340,8 @@ def peaks():
 # ----------------------------------------------------------------------------- sweep
 def run_sweep(args):
     """Chunk rows x transfer backend x swizzle on one AllGather workload (config 5 of the
-    benchmark plan): inputs generated and uploaded once, each point warmed up then timed."""
+    benchmark plan): inputs generated and uploaded once, every point warmed up, then timed
+    (--steps calls back to back) once in each of --sweep-rounds interleaved rounds."""
     import torch
 
     import tile_level_communication_gb300 as dt
@@ -351,12 +354,16 @@ def run_sweep(args):
     shards = [up(x) for x in inp.shards]
     b = up(inp.b)
     c = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device="cuda")
-    peak = peaks()["bf16_tflops_sustained"]
+    peak = peaks()["bf16_tflops"]
     chunks = [int(x) for x in args.sweep_chunks.split(",")]
     ws = None
     backends = ["copy_engine", "tma", "ldst"]
     if (wl.m // wl.world_size) % 128 == 0:
         backends.append("tma_tile")  # the per-tile pull needs tile-aligned shards
+    # every point is timed once per round and the rounds interleave the points, so that the
+    # GPU's drift in clock and power over the sweep falls on every point alike; each point
+    # reports the median of its rounds
+    points = []
     for cr in chunks:
         for backend in backends:
             for swizzle in [True, False]:
@@ -365,21 +372,30 @@ def run_sweep(args):
                 need = dt.workspace_size(a, dt.OP_AG)
                 if ws is None or ws.numel() < need:
                     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
-                for _ in range(max(3, args.warmup)):
-                    dt.ag_gemm(shards, b, c, ws, a)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                torch.cuda.synchronize()
-                e0.record()
-                for _ in range(args.steps):
-                    dt.ag_gemm(shards, b, c, ws, a)
-                e1.record()
-                torch.cuda.synchronize()
-                st, info = dt.check(ws)
-                ms = e0.elapsed_time(e1) / args.steps
-                tf = wl.flops / (ms * 1e-3) / 1e12
-                print(json.dumps({"sweep": name, "chunk_rows": cr, "backend": backend,
-                                  "swizzle": swizzle, "ms": ms, "tflops": tf,
-                                  "frac_of_sustained_peak": tf / peak, "status": st}), flush=True)
+                points.append(dict(chunk_rows=cr, backend=backend, swizzle=swizzle, args=a, ms=[]))
+    for p in points:
+        for _ in range(max(3, args.warmup)):
+            dt.ag_gemm(shards, b, c, ws, p["args"])
+    for _ in range(args.sweep_rounds):
+        for p in points:
+            dt.ag_gemm(shards, b, c, ws, p["args"])  # its order and flags in the workspace
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(args.steps):
+                dt.ag_gemm(shards, b, c, ws, p["args"])
+            e1.record()
+            torch.cuda.synchronize()
+            p["ms"].append(e0.elapsed_time(e1) / args.steps)
+    st, info = dt.check(ws)
+    if st != 0:
+        raise RuntimeError(f"device error in the sweep {info}")
+    for p in points:
+        ms = statistics.median(p["ms"])
+        tf = wl.flops / (ms * 1e-3) / 1e12
+        print(json.dumps({"sweep": name, "chunk_rows": p["chunk_rows"], "backend": p["backend"],
+                          "swizzle": p["swizzle"], "ms": ms, "ms_rounds": p["ms"], "tflops": tf,
+                          "frac_of_burst_peak": tf / peak}), flush=True)
     return 0
 
 
