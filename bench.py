@@ -47,14 +47,14 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch after two
     # warm-up launches, 256-row tiles; keys "chunk_rows/tile_rows/col_band/l2_hints" (the
     # group width gives the same order at these chunk sizes: a key holds at most 4 m-tiles)
-    "rs_w8_m8192_n8192_k3584": {"csrc": "5bcd8666a2ae1e81",
+    "rs_w8_m8192_n8192_k3584": {"csrc": "c68d5a2fc6b7c530",
                                 "profile": "profiles/fused_gemm_rs_w8_m8192_n8192_k3584.md",
                                 "points": {
-        "1024/256/16/3": 4250193920 + 1993266944, "1024/256/32/3": 5610113280 + 1996678144,
-        "512/256/16/3": 4052715776 + 1990631168, "512/256/32/3": 5622775552 + 1997062144,
-        "256/256/16/3": 4088491264 + 1992518144, "256/256/32/3": 5878787840 + 1997745664,
-        "128/256/16/3": 4011194112 + 1990395904, "128/256/32/3": 5841342464 + 1997944576,
-        "64/256/16/3": 3986237696 + 1989184256, "64/256/32/3": 5928660224 + 1997003008,
+        "1024/256/16/3": 4265689600 + 1994286080, "1024/256/32/3": 5632776960 + 1996518144,
+        "512/256/16/3": 4782523136 + 1998116352, "512/256/32/3": 5657114880 + 1999714048,
+        "256/256/16/3": 4591319296 + 1996596992, "256/256/32/3": 5934045696 + 1998628352,
+        "128/256/16/3": 4883532288 + 1999624448, "128/256/32/3": 5952347136 + 1999419392,
+        "64/256/16/3": 4559926784 + 1999392512, "64/256/32/3": 5786437632 + 1998811136,
     }},
 }
 
