@@ -177,6 +177,16 @@ dt_status make_c_tmap(CUtensorMap* tm, void* c, int64_t rows, int64_t cols, int6
 // Bytes of B_q that one column band of the ReduceScatter order may use (automatic col_band).
 constexpr int64_t kBandBytes = 32ll << 20;
 
+// ReduceScatter / AllReduce middle sources fold with a TMA reduce-add (1) or a load, add and
+// store (0); DT_RS_REDUCE overrides.
+int32_t rs_reduce_setting() {
+  static int32_t v = [] {
+    const char* e = getenv("DT_RS_REDUCE");
+    return e ? (atoi(e) != 0 ? 1 : 0) : 1;
+  }();
+  return v;
+}
+
 // L2 cache policies of the fused kernels (KParams::l2_hints); DT_L2_HINTS overrides.
 int32_t l2_hints_setting() {
   static int32_t v = [] {
@@ -643,6 +653,7 @@ void fill_common(KParams& p, const Derived& d, void* ws, uint32_t epoch) {
   p.act = d.act;
   p.drop_chunk = -1;
   p.l2_hints = l2_hints_setting();
+  p.rs_reduce = rs_reduce_setting();
   p.trace = nullptr;
   p.ded_bufs = ded_bufs_setting();
   p.piece_bytes = kCopyBuf;

@@ -130,6 +130,9 @@ struct KParams {
   int32_t piece_bytes;     // bytes of one transfer piece and of one TMA worker buffer (a
                            // multiple of 16; kCopyBuf, or up to 2 * kCopyBuf on dedicated
                            // transfer CTAs)
+  int32_t rs_reduce;       // ReduceScatter / AllReduce: a source between the first and the last
+                           // folds its partial into the running sum with a TMA reduce-add (1)
+                           // rather than a load, an add and a store (0)
 };
 
 // AG debug timeline, in 64-bit words: [0] first CTA start (min), [1] last CTA exit (max),
@@ -856,7 +859,11 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
       }
     }
     if (tma_tile) {
-      const bool load = t_in_order && t_d > 0;
+      // a middle source adds its partial into the running sum in place (TMA reduce-add: the
+      // fp32 add of the loading path, done by the memory system, so nothing waits for a load);
+      // the first one stores it, the last one loads the running sum to round the final sum
+      const bool red = t_in_order && t_d > 0 && t_d < p.g.W - 1 && p.rs_reduce != 0;
+      const bool load = t_in_order && t_d > 0 && !red;
       const bool last = t_in_order && t_d == p.g.W - 1;
       const CUtensorMap* store_map = t_in_order ? &p.tmAcc : &p.tmPark;
       const int32_t store_y =
@@ -867,6 +874,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
       const int ncb = static_cast<int>(min64(kBN, p.g.N - ti.col0) + 31) / 32;  // 32-column boxes
       // Box cb+1's running sum is loaded into the other buffer while box cb is processed.  The
       // buffers are free at the start of a tile (its predecessor waited for all its stores).
+      if (et == 0 && red) fence_proxy_async_global();  // as below, for the reductions
       if (et == 0 && load) {
         // the unit's word was acquired through the generic proxy; the loads below are TMA
         fence_proxy_async_global();
@@ -884,7 +892,9 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
         const int64_t c0 = ti.col0 + cb * 32;
         const int b = static_cast<int>(stage_ctr & 1u);
         uint8_t* buf = L.copy + b * kCopyBuf;
-        if (et == 0) {
+        if (et == 0 && red) {
+          bulk_wait_read<1>();  // box cb-2's reduction has read this buffer
+        } else if (et == 0) {
           bulk_wait_read<0>();  // box cb-1's store has read the other buffer
           if (load && cb + 1 < ncb) {
             mbar_expect_tx(L.copyb(b ^ 1), kCopyBuf);
@@ -942,7 +952,13 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (et == 0) {
-          if (!last) {
+          if (red) {
+            if (stream_sums)
+              tma_reduce_add_2d_hint(&p.tmAcc, smem_u32(buf), static_cast<int32_t>(c0), store_y,
+                                     pol_s);
+            else
+              tma_reduce_add_2d(&p.tmAcc, smem_u32(buf), static_cast<int32_t>(c0), store_y);
+          } else if (!last) {
             if (stream_sums)
               tma_store_2d_hint(store_map, smem_u32(buf), static_cast<int32_t>(c0), store_y, pol_s);
             else

@@ -104,6 +104,25 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* tm, uint32_
       "r"(src), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
+// 2-D tiled tensor reduction shared -> global (bulk group): the box in global memory at (x, y)
+// becomes itself plus the shared-memory box, element by element, the add done by the memory
+// system in the tensor map's element type; clipped like a store.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* tm, uint32_t src, int32_t x,
+                                                  int32_t y) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], "
+      "[%1];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap* tm, uint32_t src,
+                                                       int32_t x, int32_t y, uint64_t pol) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(tm)),
+      "r"(src), "r"(x), "r"(y), "l"(pol)
+      : "memory");
+}
 // 3-D tiled tensor store shared -> global (bulk group), clipped at the tensor's extent in
 // every dimension.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int32_t x,
