@@ -388,12 +388,13 @@ size_t dt_sizeof_tune_point(void);
  * other candidate between two timings of the reference and scores it by its time over their
  * mean (the GPU's clock drifts as it warms under the power cap; the ratio cancels the drift);
  * a point's reported ms is its score times the reference's median time.  Candidates whose
- * workspace exceeds ws_bytes are skipped.  Among the points within 1 % of the fastest, the
- * knobs kept are those that move the fewest DRAM bytes: for the reduce ops the automatic
- * column bands before one band, then the largest chunk rows, then the fastest; for the
- * AllGather the largest chunk rows (fewer key groups re-stream B fewer times), then the
- * fastest.  A short timing at full clock does not show DRAM bytes, a run under the power cap
- * does.  They are written into *a (chunk_rows, backend, copy_ctas, group, tile_m, col_band;
+ * workspace exceeds ws_bytes are skipped.  The knobs kept are those that move the fewest DRAM
+ * bytes among near-equal points (a short timing at full clock does not show DRAM bytes, a run
+ * under the power cap does): for the reduce ops the automatic column bands unless one band is
+ * more than 4 % faster, then, among the points of the kept band setting within 1 % of its
+ * fastest, the largest chunk rows, then the fastest; for the AllGather, among the points within
+ * 1 % of the fastest, the largest chunk rows (fewer key groups re-stream B fewer times), then
+ * the fastest.  They are written into *a (chunk_rows, backend, copy_ctas, group, tile_m, col_band;
  * swizzle stays on).  `points` (may be NULL) receives
  * up to max_points candidates and *n_points their number.  The inputs are read and the
  * outputs written by every candidate; all candidates give bit-identical outputs. */

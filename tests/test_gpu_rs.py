@@ -184,6 +184,44 @@ def test_full_size_sampled(dt):
     assert all(torch.isfinite(o.float()).all() for o in outs)
 
 
+def test_tuner_reduce_keeps_automatic_bands_unless_one_band_is_clearly_faster(dt):
+    """A B_q above the 32 MiB band budget (here 4096 x 8192 bf16) makes the reduce tuner time
+    every candidate with the automatic column bands and with one band.  The kept point: the
+    automatic bands unless one band is more than 4 % faster in the tuner's bursts (they read less
+    DRAM, which longer runs under the power cap reward), then among the points within 1 % of the
+    fastest of the kept band setting, the largest chunk rows, then the fastest."""
+    w, m, n, k = 2, 1024, 8192, 4096
+    inp = make_rs_inputs(w, m, n, k, seed=57)
+    args = dt.make_args(w, m, n, k, chunk_rows=256)
+    assert dt.col_band(args, dt.OP_RS) < n // 256  # more than one automatic band
+    a = [dev_bf16(x) for x in inp.a]
+    b = [dev_bf16(x) for x in inp.b]
+    outs = [out_tensor(m // w, n, "bf16") for _ in range(w)]
+    probe = dt.make_args(w, m, n, k, chunk_rows=64)
+    ws = workspace(max(dt.workspace_size(probe, dt.OP_RS), dt.workspace_size(args, dt.OP_RS)))
+    pts = dt.tune_reduce(dt.OP_RS, a, b, outs, ws, args, reps=2)
+    ran = [p for p in pts if p["status"] == 0 and p["ms"] > 0]
+    assert {p["col_band"] for p in ran} == {0, n // 256}
+    fastest = min(ran, key=lambda p: p["ms"])
+    pool = ran
+    auto = [p for p in ran if p["col_band"] == 0]
+    best_auto = min(auto, key=lambda p: p["ms"])
+    if fastest["col_band"] != 0 and best_auto["ms"] <= 1.04 * fastest["ms"]:
+        fastest, pool = best_auto, auto
+    near = [p for p in pool if p["ms"] <= 1.01 * fastest["ms"]]
+    if any(p["col_band"] == 0 for p in near):
+        near = [p for p in near if p["col_band"] == 0]
+    top = max(p["chunk_rows"] for p in near)
+    best = min((p for p in near if p["chunk_rows"] == top), key=lambda p: p["ms"])
+    assert (args.chunk_rows, args.col_band, args.group) == (best["chunk_rows"], best["col_band"],
+                                                            best["group"])
+    tuned = [out_tensor(m // w, n, "bf16") for _ in range(w)]
+    dt.gemm_rs(a, b, tuned, ws, args)
+    assert dt.check(ws)[0] == 0
+    base = _run(dt, inp, m, n, k, chunk_rows=256)
+    assert all(bits_equal(t, x) for t, x in zip(tuned, base))
+
+
 def test_tuner_reduce_identical_output(dt, w4):
     wl, inp, ref = w4
     args = dt.make_args(4, wl.m, wl.n, wl.k, chunk_rows=256)

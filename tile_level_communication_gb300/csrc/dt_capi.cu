@@ -1591,35 +1591,54 @@ void drop_same_order(std::vector<dt_args>& cands, int op) {
   cands.swap(keep);
 }
 
-// Pick the point to keep and copy its knobs into *a: among the points within kTuneTie of the
-// fastest, the one that moves the fewest DRAM bytes: for the reduce ops automatic column bands
-// before one band, then the largest chunk rows, then the fastest; for the AllGather the
-// largest chunk rows, then the fastest (its column bands move more bytes at some chunk sizes
-// and fewer at others: measured, not ranked).  The tuner times short bursts at full clock;
-// run for seconds under the power cap, a kernel's clock follows its energy.  Fewer, larger
-// chunks mean fewer key groups in the order, each of which re-streams B from DRAM (the largest
-// AllGather with the per-tile pull, 3 s runs: chunk 2048 / 1024 / 256 read 2.52 / 3.06 / 4.28
-// GB per launch and took 1.282 / 1.315 / 1.343 ms at 1425 / 1387 / 1350-1365 MHz, where their
-// burst times lie within 1 %); column bands keep B_q's band in L2 (the FFN pair's
-// ReduceScatter reads 4.1-4.2 GB per launch with two bands against 5.5-6.0 GB with one, and
-// runs 3-5 % faster over 200 calls).
+// Pick the point to keep and copy its knobs into *a.  The tuner times short bursts at full
+// clock; run for longer under the power cap, a kernel's clock follows its energy, so among
+// near-equal points the one that moves the fewest DRAM bytes is kept.
+// * Reduce ops: automatic column bands (they keep B_q's band in L2: the FFN pair's
+//   ReduceScatter reads 3.9-4.9 GB per launch with two bands against 5.3-5.9 GB with one) are
+//   kept unless one band is more than kBandTie faster in the burst: in the timed steps of the
+//   benchmark, after the tuner, two bands took 2.06-2.11 ms and one band 2.17-2.21 ms on the
+//   same boxes, while the tuner's bursts had put one band up to ~1 % ahead.
+// * Then, among the points within kTuneTie of the fastest (of the kept bands), the largest
+//   chunk rows, then the fastest.  Fewer, larger chunks mean fewer key groups in the order, each
+//   of which re-streams B from DRAM (the largest AllGather with the per-tile pull, 3 s runs:
+//   chunk 2048 / 1024 / 256 read 2.52 / 3.06 / 4.28 GB per launch and took 1.282 / 1.315 /
+//   1.343 ms at 1425 / 1387 / 1350-1365 MHz, where their burst times lie within 1 %).  The
+//   AllGather's column bands move more bytes at some chunk sizes and fewer at others, so they
+//   are measured, not ranked.
 constexpr float kTuneTie = 1.01f;
+constexpr float kBandTie = 1.04f;
 dt_status tune_finish(std::vector<dt_tune_point>& pts, dt_args* a, dt_tune_point* out,
                       int32_t max_points, int32_t* n_points, bool bands_first) {
+  auto ran = [&](const dt_tune_point& x) { return x.status == DT_OK && x.ms >= 0; };
   int fastest = -1;
   for (int i = 0; i < static_cast<int>(pts.size()); ++i)
-    if (pts[i].status == DT_OK && pts[i].ms >= 0 && (fastest < 0 || pts[i].ms < pts[fastest].ms))
-      fastest = i;
+    if (ran(pts[i]) && (fastest < 0 || pts[i].ms < pts[fastest].ms)) fastest = i;
+  // reduce ops: stay with the automatic bands when their best point is within kBandTie
+  bool auto_only = false;
+  if (bands_first && fastest >= 0 && pts[fastest].col_band != 0) {
+    int best_auto = -1;
+    for (int i = 0; i < static_cast<int>(pts.size()); ++i)
+      if (ran(pts[i]) && pts[i].col_band == 0 && (best_auto < 0 || pts[i].ms < pts[best_auto].ms))
+        best_auto = i;
+    if (best_auto >= 0 && pts[best_auto].ms <= kBandTie * pts[fastest].ms) {
+      fastest = best_auto;
+      auto_only = true;
+    }
+  }
   int best = fastest;
-  auto fewer_bytes = [&](const dt_tune_point& x, const dt_tune_point& y) {
-    const bool xa = x.col_band == 0, ya = y.col_band == 0;  // automatic bands
-    if (bands_first && xa != ya) return xa;
+  auto larger_chunk = [&](const dt_tune_point& x, const dt_tune_point& y) {
     if (x.chunk_rows != y.chunk_rows) return x.chunk_rows > y.chunk_rows;
     return x.ms < y.ms;
   };
   for (int i = 0; fastest >= 0 && i < static_cast<int>(pts.size()); ++i) {
-    if (pts[i].status != DT_OK || pts[i].ms < 0 || pts[i].ms > kTuneTie * pts[fastest].ms) continue;
-    if (fewer_bytes(pts[i], pts[best])) best = i;
+    if (!ran(pts[i]) || pts[i].ms > kTuneTie * pts[fastest].ms) continue;
+    if (auto_only && pts[i].col_band != 0) continue;
+    if (bands_first && !auto_only && (pts[i].col_band == 0) != (pts[best].col_band == 0)) {
+      if (pts[i].col_band == 0) best = i;  // automatic bands before one band
+      continue;
+    }
+    if (larger_chunk(pts[i], pts[best])) best = i;
   }
   if (n_points) *n_points = static_cast<int32_t>(pts.size());
   if (out)
