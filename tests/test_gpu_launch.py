@@ -1,13 +1,15 @@
 """Launch mode of the fused kernel, and the AllGather's debug timeline, through the C ABI.
 
 * Programmatic dependent launch (the fused kernel's launch and set-up overlap the prepare
-  kernel before it; the kernel waits for that grid before it touches global memory) changes no
-  bit: every op gives the same outputs with it (the default) and with DT_PDL=0 (plain stream
-  order): the AllGather-GEMM on each transfer backend and on one CTA or a CTA pair per tile,
-  the GEMM-ReduceScatter, the GEMM-AllReduce, the GEMM-AllToAll, the fixed-scratch
-  AllGather-GEMM and dt_allgather.  The setting is read once per process, so each mode runs
-  in a child process.  The DITRON page, section 6, asks for bit-identical results from the
-  adapted kernels whatever their schedule.
+  kernel before it; the kernel waits for that grid before it touches global memory) and the
+  ReduceScatter's fold path (a middle source's TMA reduce-add into the running sum, or a load,
+  an add and a store) change no bit: every op gives the same outputs by default, with
+  DT_PDL=0 (plain stream order) and with DT_RS_REDUCE=0: the AllGather-GEMM on each transfer
+  backend and on one CTA or a CTA pair per tile, the GEMM-ReduceScatter and GEMM-AllReduce
+  (bf16 and fp32 outputs; six ranks whose tiles are cut by destination and chunk boundaries),
+  the GEMM-AllToAll, the fixed-scratch AllGather-GEMM and dt_allgather.  The settings are read
+  once per process, so each mode runs in a child process.  The DITRON page, section 6, asks for
+  bit-identical results from the adapted kernels whatever their schedule.
 * dt_allgather on an in-kernel backend records the timeline: every chunk is released inside
   the kernel's span, and no GEMM word is written.
 """
@@ -70,14 +72,28 @@ for be in ("tma", "ldst"):
 rs = make_rs_inputs(w, 2048, 1024, 512, seed=72)
 A, B = [up(x) for x in rs.a], [up(x) for x in rs.b]
 for op, fn, rows in (("rs", dt.gemm_rs, 512), ("ar", dt.gemm_ar, 2048)):
-    a = dt.make_args(w, 2048, 1024, 512, chunk_rows=256)
-    opid = dt.OP_RS if op == "rs" else dt.OP_AR
-    ws = torch.zeros(dt.workspace_size(a, opid), dtype=torch.uint8, device="cuda")
-    outs = [torch.full((rows, 1024), float("nan"), dtype=torch.bfloat16, device="cuda")
-            for _ in range(w)]
+    for odt in ("bf16", "f32"):
+        a = dt.make_args(w, 2048, 1024, 512, chunk_rows=256, out_dtype=odt)
+        opid = dt.OP_RS if op == "rs" else dt.OP_AR
+        ws = torch.zeros(dt.workspace_size(a, opid), dtype=torch.uint8, device="cuda")
+        tdt = torch.bfloat16 if odt == "bf16" else torch.float32
+        outs = [torch.full((rows, 1024), float("nan"), dtype=tdt, device="cuda") for _ in range(w)]
+        for _ in range(2):
+            fn(A, B, outs, ws, a)
+        res[f"{op}/{odt}"] = [digest([o.view(torch.int16) for o in outs]), dt.check(ws)[0]]
+# six ranks, 200 rows each: 128-row tiles cut by destination and chunk boundaries, a ragged
+# last tile, ragged columns
+w6, m6, n6, k6 = 6, 1200, 600, 384
+rs6 = make_rs_inputs(w6, m6, n6, k6, seed=75)
+A6, B6 = [up(x) for x in rs6.a], [up(x) for x in rs6.b]
+for tm in (128, 256):
+    a = dt.make_args(w6, m6, n6, k6, chunk_rows=96, tile_m=tm)
+    ws = torch.zeros(dt.workspace_size(a, dt.OP_RS), dtype=torch.uint8, device="cuda")
+    outs = [torch.full((m6 // w6, n6), float("nan"), dtype=torch.bfloat16, device="cuda")
+            for _ in range(w6)]
     for _ in range(2):
-        fn(A, B, outs, ws, a)
-    res[op] = [digest(outs), dt.check(ws)[0]]
+        dt.gemm_rs(A6, B6, outs, ws, a)
+    res[f"rs6/{tm}"] = [digest(outs), dt.check(ws)[0]]
 
 a2 = make_a2a_inputs(w, 4 * 256, 4 * 256, 512, seed=73)
 A, B = [up(x) for x in a2.a], [up(x) for x in a2.b]
@@ -92,8 +108,8 @@ print(json.dumps(res))
 """
 
 
-def _child(pdl):
-    env = dict(os.environ, DT_PDL=str(pdl))
+def _child(pdl, reduce=1):
+    env = dict(os.environ, DT_PDL=str(pdl), DT_RS_REDUCE=str(reduce))
     r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, capture_output=True,
                        text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-3000:]
@@ -106,12 +122,16 @@ def dt():
     return load_dt()
 
 
-def test_programmatic_dependent_launch_changes_no_bit(dt):
-    on, off = _child(1), _child(0)
-    assert on.keys() == off.keys() and len(on) == 14
-    for name in on:
-        assert on[name][1] == 0 and off[name][1] == 0, (name, on[name], off[name])
-        assert on[name][0] == off[name][0], name
+def test_launch_mode_and_fold_path_change_no_bit(dt):
+    base = _child(1)
+    assert len(base) == 18
+    for name, (_, st) in base.items():
+        assert st == 0, (name, st)
+    for other in (_child(0), _child(1, reduce=0)):
+        assert other.keys() == base.keys()
+        for name in base:
+            assert other[name][1] == 0, (name, other[name])
+            assert other[name][0] == base[name][0], name
 
 
 @pytest.mark.parametrize("backend", ["tma", "ldst"])
