@@ -122,16 +122,22 @@ def test_edge_shapes(dt, case, out_dtype, tile_m):
         _check_all(outs, ref, out_dtype, what=f"{case}")
 
 
-def test_padded_leading_dims_and_canaries(dt):
-    w, m, n, k = 3, 3 * 50, 72, 96
+@pytest.mark.parametrize("ms", [50, 100])
+def test_padded_leading_dims_and_canaries(dt, ms):
+    """Padded A, B and out rows; the columns past N stay untouched.  50 rows per rank: a 128-row
+    tile spans three destinations (row by row); 100 rows: tiles across two destinations, whose
+    final sums go to the first by TMA and to the second from the threads' registers."""
+    w, m, n, k = 3, 3 * ms, 72, 96
     inp = make_rs_inputs(w, m, n, k, seed=78)
     ref = _oracle(inp)
     lda, ldb, ldc = 104, 80, 88
     for out_dtype in ["bf16", "f32"]:
-        outs = _run(dt, inp, m, n, k, out_dtype, lda=lda, ldb=ldb, ldc=ldc, chunk_rows=16)
-        _check_all(outs, ref, out_dtype, n)
-        for o in outs:
-            assert torch.isnan(o[:, n:].float()).all()
+        for tile_m in (128, 256):
+            outs = _run(dt, inp, m, n, k, out_dtype, lda=lda, ldb=ldb, ldc=ldc, chunk_rows=16,
+                        tile_m=tile_m)
+            _check_all(outs, ref, out_dtype, n)
+            for o in outs:
+                assert torch.isnan(o[:, n:].float()).all()
 
 
 def test_k_zero(dt):

@@ -187,6 +187,19 @@ int32_t rs_reduce_setting() {
   return v;
 }
 
+// Per-wave rotation of the CTAs' slots in the tile order (KParams::rot) of the ReduceScatter and
+// AllReduce, whose tiles cut by destination boundaries fold at a higher cost and recur at fixed
+// slots of a wave: one slot per wave; DT_ROT overrides (0: every CTA takes the same slot of
+// every wave, as the AllGather and AllToAll do, whose tiles cost alike).
+int32_t rot_setting() {
+  static int32_t v = [] {
+    const char* e = getenv("DT_ROT");
+    const int x = e ? atoi(e) : 1;
+    return static_cast<int32_t>(x < 0 ? 0 : x);
+  }();
+  return v;
+}
+
 // L2 cache policies of the fused kernels (KParams::l2_hints); DT_L2_HINTS overrides.
 int32_t l2_hints_setting() {
   static int32_t v = [] {
@@ -1156,6 +1169,7 @@ static dt_status rs_params(KParams& p, const Derived& d, const void* const* a_,
   p.unit_cnt = reinterpret_cast<uint32_t*>(w + d.off_cnt);
   p.pieces_max = d.pieces_max;
   p.ar_copies = d.op == DT_OP_GEMM_AR ? ar_copies_of(d, out) : 0;
+  p.rot = rot_setting();
   // running sums [M][N] fp32 and park slots [W (W-1) Ms][N] fp32, moved in 32 x 128 boxes
   dt_status st = make_tmap(&p.tmAcc, p.recv, d.N, d.M, d.N * 4, 32, kBM, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
   if (st != DT_OK) return st;

@@ -127,6 +127,7 @@ struct KParams {
                            // [W][M/W][N/W], clipped at each source's rows); 0: per-thread rows
   int32_t a_from_shards;   // AG: each tile's A rows are loaded from the owning shard (tmA[s])
   int32_t ded_bufs;        // TMA buffers per worker on a dedicated transfer CTA: 1 to 4
+  int32_t rot;             // per-wave rotation of the CTAs' slots in the tile order (pos_at)
   int32_t piece_bytes;     // bytes of one transfer piece and of one TMA worker buffer (a
                            // multiple of 16; kCopyBuf, or up to 2 * kCopyBuf on dedicated
                            // transfer CTAs)
@@ -304,6 +305,23 @@ template <int CL>
 __device__ __forceinline__ int32_t pos_stride(const KParams& p) {
   return (static_cast<int32_t>(gridDim.x) - p.copy_ctas) / CL;
 }
+// The position a CTA (or pair) takes in wave k, the k-th run of pos_stride consecutive
+// positions: slot (first_pos + k * rot) of the wave.  Every wave runs the same positions
+// whatever rot is; with rot != 0 a CTA does not take the same slot in every wave, so tiles that
+// cost more and recur at fixed slots (those cut by destination boundaries) spread over the CTAs.
+// A position past the end (last wave) is skipped, not the end of the loop.
+template <int CL>
+__device__ __forceinline__ int32_t pos_at(const KParams& p, int32_t k) {
+  const uint32_t S = static_cast<uint32_t>(pos_stride<CL>(p));
+  const uint32_t r = static_cast<uint32_t>(p.rot) % S;
+  const uint32_t slot = (static_cast<uint32_t>(first_pos<CL>(p)) + static_cast<uint32_t>(k) * r) % S;
+  return k * static_cast<int32_t>(S) + static_cast<int32_t>(slot);
+}
+template <int CL>
+__device__ __forceinline__ int32_t wave_count(const KParams& p) {
+  const int32_t S = pos_stride<CL>(p);
+  return (p.T + S - 1) / S;
+}
 
 // Warp-wide bounded wait: every lane polls, a vote makes the outcome the warp's, so all lanes
 // leave a loop together (the producer and MMA roles run as whole warps that stay converged;
@@ -329,10 +347,13 @@ __device__ void run_producer(const KParams& p, const SmemLayout& L) {
   uint32_t full0_lead = full0;  // stage 0's full barrier in the pair leader (cluster address)
   if constexpr (PAIR) full0_lead = mapa_shared(full0, rank & ~1u);
   uint32_t kit = 0;  // k-blocks issued so far (the last one, if any, is kit - 1)
-  int32_t t_next = tile_id(p, first_pos<CL>(p));
-  for (int32_t pos = first_pos<CL>(p); pos < p.T; pos += pos_stride<CL>(p)) {
+  const int32_t nwaves = wave_count<CL>(p);
+  int32_t t_next = tile_id(p, pos_at<CL>(p, 0));
+  for (int32_t k = 0; k < nwaves; ++k) {
+    const int32_t pos = pos_at<CL>(p, k);
     const int32_t t_cur = t_next;
-    t_next = tile_id(p, pos + pos_stride<CL>(p));
+    t_next = tile_id(p, pos_at<CL>(p, k + 1));
+    if (pos >= p.T) continue;
     const TileInfo ti = decode_tile<OP, CL>(p, t_cur);
     if (!ti.valid) {
       if (elect_one()) raise_error(p, kDevBadTile, static_cast<uint32_t>(pos), blockIdx.x, 0);
@@ -458,10 +479,13 @@ __device__ void run_mma(const KParams& p, const SmemLayout& L, uint32_t tmem_bas
   const uint32_t full0 = L.full(0), empty0 = L.empty(0);
   const uint64_t adesc0 = smem_desc_sw128(smem_u32(L.a), 16, 1024);
   const uint64_t bdesc0 = smem_desc_sw128(smem_u32(L.b), kBSlab, 1024);
-  int32_t t_next = tile_id(p, first_pos<CL>(p));
-  for (int32_t pos = first_pos<CL>(p); pos < p.T; pos += pos_stride<CL>(p)) {
+  const int32_t nwaves = wave_count<CL>(p);
+  int32_t t_next = tile_id(p, pos_at<CL>(p, 0));
+  for (int32_t k = 0; k < nwaves; ++k) {
+    const int32_t pos = pos_at<CL>(p, k);
     const int32_t t_cur = t_next;
-    t_next = tile_id(p, pos + pos_stride<CL>(p));
+    t_next = tile_id(p, pos_at<CL>(p, k + 1));
+    if (pos >= p.T) continue;
     const TileInfo ti = decode_tile<OP, CL>(p, t_cur);
     if (!ti.valid) continue;
     const int acc = tl & 1;
@@ -761,10 +785,13 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
     tempty_bar0 = mapa_shared(tempty_bar0, lead);
     tempty_bar1 = mapa_shared(tempty_bar1, lead);
   }
-  int32_t t_next = tile_id(p, first_pos<CL>(p));
-  for (int32_t pos = first_pos<CL>(p); pos < p.T; pos += pos_stride<CL>(p)) {
+  const int32_t nwaves = wave_count<CL>(p);
+  int32_t t_next = tile_id(p, pos_at<CL>(p, 0));
+  for (int32_t k = 0; k < nwaves; ++k) {
+    const int32_t pos = pos_at<CL>(p, k);
     const int32_t t_cur = t_next;
-    t_next = tile_id(p, pos + pos_stride<CL>(p));
+    t_next = tile_id(p, pos_at<CL>(p, k + 1));
+    if (pos >= p.T) continue;
     const TileInfo ti = decode_tile<OP, CL>(p, t_cur);
     if (!ti.valid) continue;
     const int acc = tl & 1;
@@ -832,7 +859,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
     // partial, land in one output (the AllReduce's outputs are [M][N]; a ReduceScatter tile
     // across two destinations needs two).  The rest go row by row.
     bool tma_tile = false;
-    int32_t t_s = 0, t_d = 0;
+    int32_t t_s = 0, t_s1 = 0, t_d = 0;
     int64_t t_lr0 = 0;
     bool t_in_order = false;
     if (fused_rs && ti.row_end > ti.row0) {
@@ -847,13 +874,14 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
         const int32_t np = (s1 * p.g.nC + j1) - (s0 * p.g.nC + j0) + 1;  // pieces of the tile
         bool all = true;
         for (int32_t k = 0; k < np && all; ++k) all = (L.last_mask[k >> 5] >> (k & 31)) & 1u;
-        if (all && (d < p.g.W - 1 || p.ar_copies > 0 || s0 == s1)) {
+        if (all && (d < p.g.W - 1 || p.ar_copies > 0 || s1 <= s0 + 1)) {
           tma_tile = true;
           t_in_order = true;
         }
       }
       if (tma_tile) {
         t_s = s0;
+        t_s1 = s1;
         t_d = d;
         t_lr0 = ti.row0 - static_cast<int64_t>(s0) * p.g.Ms;
       }
@@ -872,6 +900,13 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
                                                 p.g.Ms + t_lr0);
       const int r = qd * 32 + lane;  // this thread's row of the tile
       const int ncb = static_cast<int>(min64(kBN, p.g.N - ti.col0) + 31) / 32;  // 32-column boxes
+      // the final sums of a ReduceScatter tile across two destinations: the box goes to the
+      // first one as a TMA store (its tensor map ends at that destination's last row), and the
+      // threads whose rows belong to the second store them from registers
+      const int64_t split_row = static_cast<int64_t>(t_s + 1) * p.g.Ms;
+      const bool row_to_s1 = last && p.ar_copies == 0 && t_s1 != t_s && ti.row0 + r >= split_row &&
+                             ti.row0 + r < ti.row_end;
+      const int64_t lr1 = row_to_s1 ? ti.row0 + r - split_row : 0;
       // Box cb+1's running sum is loaded into the other buffer while box cb is processed.  The
       // buffers are free at the start of a tile (its predecessor waited for all its stores).
       if (et == 0 && red) fence_proxy_async_global();  // as below, for the reductions
@@ -934,6 +969,7 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
           // has read its running-sum row out of the same buffer
           named_bar_sync(1, 128);
           uint4* orow = reinterpret_cast<uint4*>(buf + r * 64);
+          __nv_bfloat16* orow1 = reinterpret_cast<__nv_bfloat16*>(p.out[t_s1]) + lr1 * p.ldc + c0;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 w;
@@ -942,12 +978,21 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
             w.z = pack_bf16x2(__float_as_uint(a[8 * u + 4]), __float_as_uint(a[8 * u + 5]));
             w.w = pack_bf16x2(__float_as_uint(a[8 * u + 6]), __float_as_uint(a[8 * u + 7]));
             orow[u] = w;
+            if (row_to_s1 && c0 + u * 8 < p.g.N) reinterpret_cast<uint4*>(orow1)[u] = w;
           }
         } else {
           // the running sum (or the fp32 final sum) in the box's swizzled layout
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             rowp[c ^ (r & 7)] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+          if (row_to_s1) {  // fp32 final sums of the second destination's rows
+            float* orow1 = reinterpret_cast<float*>(p.out[t_s1]) + lr1 * p.ldc + c0;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              if (c0 + c * 4 < p.g.N)
+                reinterpret_cast<float4*>(orow1)[c] =
+                    make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+          }
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
