@@ -47,14 +47,14 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch after two
     # warm-up launches, 256-row tiles; keys "chunk_rows/tile_rows/col_band/l2_hints" (the
     # group width gives the same order at these chunk sizes: a key holds at most 4 m-tiles)
-    "rs_w8_m8192_n8192_k3584": {"csrc": "b6d4a7b0abbf92c7",
+    "rs_w8_m8192_n8192_k3584": {"csrc": "4d49cbf858bdd59b",
                                 "profile": "profiles/fused_gemm_rs_w8_m8192_n8192_k3584.md",
                                 "points": {
-        "1024/256/16/3": 4450141184 + 1993742080, "1024/256/32/3": 5289470976 + 1996200960,
-        "512/256/16/3": 4037755392 + 1992145664, "512/256/32/3": 5361176064 + 1996941056,
-        "256/256/16/3": 4088296192 + 1994069760, "256/256/32/3": 5460451328 + 1997676288,
-        "128/256/16/3": 3991516928 + 1993197312, "128/256/32/3": 5419882240 + 1997408000,
-        "64/256/16/3": 3863543808 + 1990645504, "64/256/32/3": 5501735680 + 1996324608,
+        "1024/256/16/3": 4780279040 + 1994510592, "1024/256/32/3": 5637179904 + 1999952896,
+        "512/256/16/3": 4512529152 + 1994844416, "512/256/32/3": 5606185472 + 1999094272,
+        "256/256/16/3": 4324142592 + 1993550592, "256/256/32/3": 5665274624 + 1999829248,
+        "128/256/16/3": 4341614848 + 1993489408, "128/256/32/3": 5656622592 + 2000904448,
+        "64/256/16/3": 3950166272 + 1992458240, "64/256/32/3": 5581372416 + 1999354624,
     }},
 }
 
