@@ -1138,36 +1138,62 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     ranges_act = merged([arenas[0].span(t) for cl in calls for t in cl["acts"]])
     act_bytes = sum(t.numel() * t.element_size() for cl in calls for t in cl["acts"])
 
+    timing = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    e2e_parts = []  # per run: median copy-in, compute and copy-out time of a step, and the lag
+                    # from step i's compute start to step i+1's copy-in start
+
     def e2e_steps(n, ranges=ranges_all):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0, e1 = timing(), timing()
+        marks = [[timing() for _ in range(6)] for _ in range(n)]  # h2d, compute, d2h: start, end
         torch.cuda.synchronize(dev)
         gc.disable()  # the host enqueues only a few steps ahead: a collector pause idles the GPU
         e0.record(s_main)
         s_h2d.wait_event(e0)
         for i in range(n):
             k = i % 2
+            mk = marks[i]
             dst_in, dst_out = set_arenas[k][0].buf, set_arenas[k][1].buf
             if i >= 2:
                 s_h2d.wait_event(ev_done[k])  # step i-2 has finished reading set k's inputs
             with torch.cuda.stream(s_h2d):
+                mk[0].record(s_h2d)
                 for lo, hi in ranges:
                     dst_in[lo:hi].copy_(host_in[lo:hi], non_blocking=True)
+                mk[1].record(s_h2d)
                 ev_in[k].record(s_h2d)
             s_main.wait_event(ev_in[k])
             if i >= 2:
                 s_main.wait_event(ev_out[k])  # step i-2's outputs have been copied out
+            mk[2].record(s_main)
             for cl in sets[k]:
                 run_call(cl)
+            mk[3].record(s_main)
             ev_done[k].record(s_main)
             s_d2h.wait_event(ev_done[k])
             with torch.cuda.stream(s_d2h):
+                mk[4].record(s_d2h)
                 host_out[k].copy_(dst_out[:out_used], non_blocking=True)
+                mk[5].record(s_d2h)
                 ev_out[k].record(s_d2h)
         for k in range(min(n, 2)):
             s_main.wait_event(ev_out[k])
         e1.record(s_main)
         torch.cuda.synchronize(dev)
         gc.enable()
+        if n >= 4:
+            mid = marks[1:n - 1]
+            parts = {"h2d": [m[0].elapsed_time(m[1]) for m in mid],
+                     "compute": [m[2].elapsed_time(m[3]) for m in mid],
+                     "d2h": [m[4].elapsed_time(m[5]) for m in mid],
+                     # step i's compute start to step i+1's copy-in start (the overlap), and
+                     # step i's compute end to step i+1's compute start (the gap between steps)
+                     "next_h2d_after_compute_start": [
+                         marks[i][2].elapsed_time(marks[i + 1][0]) for i in range(1, n - 2)],
+                     "compute_gap": [
+                         marks[i][3].elapsed_time(marks[i + 1][2]) for i in range(1, n - 2)]}
+            e2e_parts.append(dict(
+                {f"{k_}_ms": statistics.median(v_) for k_, v_ in parts.items()},
+                **{f"{k_}_max_ms": max(v_) for k_, v_ in parts.items()}))
         return e0.elapsed_time(e1)
 
     e2e_steps(2)  # warm-up (second set's tile orders, pinned pages)
@@ -1178,8 +1204,11 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
     e2e_reps = 5
 
     def e2e_median(ranges=ranges_all):
+        del e2e_parts[:]
         runs = [e2e_steps(n_e, ranges) / n_e for _ in range(e2e_reps)]
-        return statistics.median(runs), runs
+        parts = [dict({k_: round(v_, 4) for k_, v_ in p_.items()}, ms_per_step=round(r_, 4))
+                 for p_, r_ in zip(e2e_parts, runs)]
+        return statistics.median(runs), parts
 
     ms_e, runs_e = e2e_median()
     ms_act, runs_act = e2e_median(ranges_act)
@@ -1249,15 +1278,19 @@ def extras(args, dt, torch, dev, calls, run_call, flops_step, in_bytes, out_byte
                   "ms_per_step": ms_e, "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                   "pipelined": "step i+1's inputs in and step i-1's outputs out overlap step i, "
                                "each as one copy (inputs and outputs packed in one buffer each)",
-                  "runs_ms_per_step": runs_e,
-                  "timing": f"median of {e2e_reps} runs of {n_e} pipelined steps",
+                  "runs": runs_e,
+                  "timing": f"median of {e2e_reps} runs of {n_e} pipelined steps; per run the "
+                            "median and the largest step time of each part (events on the copy "
+                            "and compute streams), how long after step i's compute starts step "
+                            "i+1's copy-in starts, and the gap from one step's compute to the "
+                            "next",
                   "link": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
                            "floor_ms_per_step": floor_ms, "frac_of_floor": floor_ms / ms_e,
                            "note": "floor = the larger of the step's input bytes at the measured "
                                    "pinned host-to-device rate and the device step time"},
                   "weights_resident": {
                       "value": world * flops_step / (ms_act * 1e-3) / 1e12, "ms_per_step": ms_act,
-                      "runs_ms_per_step": runs_act,
+                      "runs": runs_act,
                       "h2d_bytes_per_step": act_bytes, "d2h_bytes_per_step": out_bytes,
                       "floor_ms_per_step": max(act_bytes / (h2d_gbs * 1e9) * 1e3, ms_dev),
                       "note": "the weights (B, B_q, W1, W2) stay in HBM; the activations are "
