@@ -406,6 +406,22 @@ dt_status dt_tune_reduce(int op, const void* const* a, const void* const* b, voi
                          dt_tune_point* points, int32_t max_points, int32_t* n_points,
                          void* stream);
 
+/* Environment settings, read once per process at the first call that needs them (for
+ * measurement and comparison; the defaults are the library's choices):
+ *   DT_PDL=0        launch the fused kernel without programmatic stream serialization (default 1:
+ *                   its launch and set-up overlap the prepare kernel before it; it waits for that
+ *                   grid before it touches global memory).
+ *   DT_RS_REDUCE=0  ReduceScatter / AllReduce middle sources fold with a load, an add and a store
+ *                   (default 1: a TMA reduce-add into the running sum; same bits).
+ *   DT_ROT=r        ReduceScatter / AllReduce: the CTA pairs' slot in each wave of the tile order
+ *                   rotates by r per wave (default 1; 0: the same slot every wave; same bits).
+ *   DT_L2_HINTS=h   ReduceScatter / AllReduce L2 policies: bit 0 running sums, park slots and
+ *                   final sums evict first, bit 1 B_q evict last (default 3).
+ *   DT_C_TMA=0      AllGather-GEMM / AllToAll outputs stored per thread (default 1: TMA stores).
+ *   DT_COPY_PIECE=b, DT_COPY_BUFS=n   dedicated in-kernel transfer workers' piece size (8192,
+ *                   16384 or 32768 bytes; default 32768) and buffers per worker (1-4; default 1).
+ * Every setting gives the same output bits. */
+
 /* Failure-detection testing, host side only: the next AllGather-GEMM call on this process
  * (dt_ag_gemm on any backend, or dt_ag_gemm_static_scratch) leaves out the copy and the
  * ready-flag write of transfer step `step` (the position in the gather order; -1 clears): the

@@ -295,8 +295,8 @@ __device__ __forceinline__ TileInfo decode_tile(const KParams& p, int32_t t) {
   return ti;
 }
 
-// Compute CTAs are blockIdx.x >= copy_ctas; they (or their pairs) take the tile order round
-// robin.
+// Compute CTAs are blockIdx.x >= copy_ctas; they (or their pairs) take the tile order one wave
+// of pos_stride positions at a time (pos_at).
 template <int CL>
 __device__ __forceinline__ int32_t first_pos(const KParams& p) {
   return (static_cast<int32_t>(blockIdx.x) - p.copy_ctas) / CL;
@@ -850,14 +850,15 @@ __device__ void run_epilogue(const KParams& p, const SmemLayout& L, uint32_t tme
         in_order = (L.last_mask[k >> 5] >> (k & 31)) & 1u;
       }
     }
-    // Tiles move their running sums with TMA: a 128 x 32 fp32 box of the running sum is loaded
-    // into a 128-byte-swizzled staging buffer, each thread adds its row of the accumulator,
-    // and the box goes back (or to a park slot) as one bulk store.  A whole 128-row tile inside
-    // one unit always can (in order or parked); a tile cut by chunk or destination boundaries,
-    // or the ragged last tile, can when every piece folds in order (the running sums are one
-    // [M][N] array, so the box spans the pieces) and its final sums, if this is the last
-    // partial, land in one output (the AllReduce's outputs are [M][N]; a ReduceScatter tile
-    // across two destinations needs two).  The rest go row by row.
+    // Tiles move their running sums with TMA in 128 x 32 fp32 boxes through a 128-byte-swizzled
+    // staging buffer: the first source stores its partial, a middle one reduce-adds it into the
+    // running sum, the last one loads the running sum, adds and stores the final sums (a park
+    // slot takes a partial that is early).  A whole 128-row tile inside one unit always can (in
+    // order or parked); a tile cut by chunk or destination boundaries, or the ragged last tile,
+    // can when every piece folds in order (the running sums are one [M][N] array, so the box
+    // spans the pieces) and, for the last partial of a ReduceScatter tile, its rows lie in at
+    // most two destinations (the second's rows are stored from registers).  The rest go row by
+    // row.
     bool tma_tile = false;
     int32_t t_s = 0, t_s1 = 0, t_d = 0;
     int64_t t_lr0 = 0;
