@@ -3,8 +3,9 @@
 * Programmatic dependent launch (the fused kernel's launch and set-up overlap the prepare
   kernel before it; the kernel waits for that grid before it touches global memory) and the
   ReduceScatter's fold path (a middle source's TMA reduce-add into the running sum, or a load,
-  an add and a store) change no bit: every op gives the same outputs by default, with
-  DT_PDL=0 (plain stream order) and with DT_RS_REDUCE=0: the AllGather-GEMM on each transfer
+  an add and a store) and schedule (the rotation of the CTA pairs' slots per wave) change no
+  bit: every op gives the same outputs by default, with DT_PDL=0 (plain stream order), with
+  DT_RS_REDUCE=0 and with DT_ROT=0 or 7: the AllGather-GEMM on each transfer
   backend and on one CTA or a CTA pair per tile, the GEMM-ReduceScatter and GEMM-AllReduce
   (bf16 and fp32 outputs; six ranks whose tiles are cut by destination and chunk boundaries),
   the GEMM-AllToAll, the fixed-scratch AllGather-GEMM and dt_allgather.  The settings are read
@@ -108,8 +109,8 @@ print(json.dumps(res))
 """
 
 
-def _child(pdl, reduce=1):
-    env = dict(os.environ, DT_PDL=str(pdl), DT_RS_REDUCE=str(reduce))
+def _child(pdl, reduce=1, rot=1):
+    env = dict(os.environ, DT_PDL=str(pdl), DT_RS_REDUCE=str(reduce), DT_ROT=str(rot))
     r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, capture_output=True,
                        text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-3000:]
@@ -122,12 +123,12 @@ def dt():
     return load_dt()
 
 
-def test_launch_mode_and_fold_path_change_no_bit(dt):
+def test_launch_mode_fold_path_and_schedule_change_no_bit(dt):
     base = _child(1)
     assert len(base) == 18
     for name, (_, st) in base.items():
         assert st == 0, (name, st)
-    for other in (_child(0), _child(1, reduce=0)):
+    for other in (_child(0), _child(1, reduce=0), _child(1, rot=0), _child(1, rot=7)):
         assert other.keys() == base.keys()
         for name in base:
             assert other[name][1] == 0, (name, other[name])
