@@ -707,25 +707,46 @@ __device__ __forceinline__ void fold_row32(const KParams& p, int32_t s, int64_t 
 }
 
 // The 128 epilogue threads fold parked partial e of rows [lo, hi) (destination s), column tile n.
+// Each thread has kParkVecs vectors of the running sum and of the parked partial in flight at
+// once (a unit is up to 128 x 256 fp32: 64 vectors per thread, which one at a time would be
+// 64 dependent round trips to memory).
+constexpr int kParkVecs = 8;
 template <bool F32>
 __device__ void fold_parked(const KParams& p, int32_t s, int64_t lo, int64_t hi, int32_t n,
                             int32_t e, int et) {
   const int64_t c0 = static_cast<int64_t>(n) * kBN;
   const int32_t nv = static_cast<int32_t>(min64(kBN, p.g.N - c0)) >> 2;
   const int32_t nrows = static_cast<int32_t>(hi - lo);
-  for (int32_t idx = et; idx < nrows * nv; idx += 128) {
-    const int32_t r = idx / nv;
-    const int32_t v = idx - r * nv;
-    const int64_t row = lo + r;
-    const int64_t lr = row - static_cast<int64_t>(s) * p.g.Ms;
-    const int64_t col = c0 + v * 4;
-    const float4 a = ldcg_f4(acc_ptr(p, row, col));
-    const float4 b = ldcg_f4(park_ptr(p, s, e, lr, col));
-    const float4 r4 = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-    if (e == p.g.W - 1) {
-      store_out4<F32>(p, s, lr, col, r4);
-    } else {
-      *reinterpret_cast<float4*>(acc_ptr(p, row, col)) = r4;
+  const int32_t total = nrows * nv;
+  for (int32_t base = et; base < total; base += 128 * kParkVecs) {
+    float4 a[kParkVecs], b[kParkVecs];
+#pragma unroll
+    for (int u = 0; u < kParkVecs; ++u) {
+      const int32_t idx = base + u * 128;
+      if (idx < total) {
+        const int32_t r = idx / nv;
+        const int64_t row = lo + r;
+        const int64_t col = c0 + (idx - r * nv) * 4;
+        a[u] = ldcg_f4(acc_ptr(p, row, col));
+        b[u] = ldcg_f4(park_ptr(p, s, e, row - static_cast<int64_t>(s) * p.g.Ms, col));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kParkVecs; ++u) {
+      const int32_t idx = base + u * 128;
+      if (idx < total) {
+        const int32_t r = idx / nv;
+        const int64_t row = lo + r;
+        const int64_t lr = row - static_cast<int64_t>(s) * p.g.Ms;
+        const int64_t col = c0 + (idx - r * nv) * 4;
+        const float4 r4 = make_float4(a[u].x + b[u].x, a[u].y + b[u].y, a[u].z + b[u].z,
+                                      a[u].w + b[u].w);
+        if (e == p.g.W - 1) {
+          store_out4<F32>(p, s, lr, col, r4);
+        } else {
+          *reinterpret_cast<float4*>(acc_ptr(p, row, col)) = r4;
+        }
+      }
     }
   }
 }
