@@ -47,14 +47,14 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch after two
     # warm-up launches, 256-row tiles; keys "chunk_rows/tile_rows/col_band/l2_hints" (the
     # group width gives the same order at these chunk sizes: a key holds at most 4 m-tiles)
-    "rs_w8_m8192_n8192_k3584": {"csrc": "4d49cbf858bdd59b",
+    "rs_w8_m8192_n8192_k3584": {"csrc": "719259b6f03ac510",
                                 "profile": "profiles/fused_gemm_rs_w8_m8192_n8192_k3584.md",
                                 "points": {
-        "1024/256/16/3": 4780279040 + 1994510592, "1024/256/32/3": 5637179904 + 1999952896,
-        "512/256/16/3": 4512529152 + 1994844416, "512/256/32/3": 5606185472 + 1999094272,
-        "256/256/16/3": 4324142592 + 1993550592, "256/256/32/3": 5665274624 + 1999829248,
-        "128/256/16/3": 4341614848 + 1993489408, "128/256/32/3": 5656622592 + 2000904448,
-        "64/256/16/3": 3950166272 + 1992458240, "64/256/32/3": 5581372416 + 1999354624,
+        "1024/256/16/3": 3936388352 + 1991550720, "1024/256/32/3": 5236883968 + 1993030400,
+        "512/256/16/3": 3808375552 + 1991179008, "512/256/32/3": 5351156736 + 1995966976,
+        "256/256/16/3": 4036418816 + 1993510144, "256/256/32/3": 5534166784 + 1998488832,
+        "128/256/16/3": 4168581376 + 1993465600, "128/256/32/3": 5486107904 + 1998518016,
+        "64/256/16/3": 3797574400 + 1990460160, "64/256/32/3": 5485989632 + 1996728320,
     }},
 }
 
