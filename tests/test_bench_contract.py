@@ -64,3 +64,32 @@ def test_traffic_table_covers_every_reduce_tuner_candidate():
             assert points[key] > 0
     for entry in bench.NCU_TRAFFIC.values():
         assert os.path.exists(os.path.join(ROOT, entry["profile"])), entry["profile"]
+
+
+def test_arena_packs_inputs_back_to_back():
+    """The end-to-end step's inputs (and outputs) sit in one buffer each, so that a step's bytes
+    cross the host link as one copy: consecutive 256-byte-aligned tensors, their byte spans, and
+    the capacity bound that the input arrays give."""
+    import numpy as np
+    import pytest
+    torch = pytest.importorskip("torch")
+    sys.path.insert(0, ROOT)
+    import bench
+    from synth_inputs import make_rs_inputs
+    inp = make_rs_inputs(2, 64, 40, 24, seed=3)
+    arrays = bench._input_arrays(inp)
+    assert len(arrays) == 4 and all(a.dtype == np.uint16 for a in arrays)
+    arena = bench.Arena(bench.Arena.capacity(arrays), "cpu")
+    ts = [arena.put(a) for a in inp.a + inp.b]
+    spans = [arena.span(t) for t in ts]
+    for (lo, hi), t, a in zip(spans, ts, inp.a + inp.b):
+        assert lo % bench.Arena.ALIGN == 0 and hi - lo == a.nbytes
+        assert t.shape == a.shape and t.dtype == torch.bfloat16
+        assert np.array_equal(t.view(torch.int16).numpy().view(np.uint16), a)
+    assert all(spans[i][1] <= spans[i + 1][0] for i in range(len(spans) - 1))  # back to back
+    assert arena.used <= arena.buf.numel()
+    with pytest.raises(RuntimeError, match="arena too small"):
+        arena.take((1024, 1024))
+    # outputs: the step's bytes, padded per tensor
+    wl = bench.WORKLOADS["rs_w8_m8192_n8192_k3584"]
+    assert bench._output_bytes(wl) >= wl.m * wl.n * 2
